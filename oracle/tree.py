@@ -1,0 +1,82 @@
+"""Draft-tree bookkeeping: depth, RoPE positions, ancestor mask and bitmask.
+
+Source: "Advanced speculative decoding: tree drafts and EAGLE", section "Why
+trees" and its ``tree_mask`` / ``depths`` helpers: node i sees the committed
+prefix, its ancestors and itself; its position is prefix length + depth, so
+siblings share a position.  The root (node 0, parent -1) is the token the
+target gave in the previous step.
+
+Representation used on both sides: ``parents`` int32 [N] with parents[0] = -1
+and 0 <= parents[i] < i (topological order), N <= 64, so the visibility row
+of node i fits a 64-bit word: bit j set <=> node j is i or an ancestor of i.
+
+Pinned by: the 6x6 mask the page prints for parents [-1, 0, 0, 1, 1, 2]
+(tests/golden/tree_mask_6.txt) and by agreement between the brute-force
+ancestor walk and the bitmask recurrence on random trees.
+"""
+import numpy as np
+
+MAX_NODES = 64
+
+
+def validate(parents):
+    """Raise ValueError unless ``parents`` is a topologically ordered tree."""
+    p = [int(v) for v in parents]
+    if not p or len(p) > MAX_NODES:
+        raise ValueError("tree must have 1..64 nodes")
+    if p[0] != -1:
+        raise ValueError("node 0 must be the root (parent -1)")
+    for i in range(1, len(p)):
+        if not 0 <= p[i] < i:
+            raise ValueError(f"parent of node {i} must be in [0, {i})")
+
+
+def depths(parents):
+    d = []
+    for i, p in enumerate(parents):
+        d.append(0 if p == -1 else d[int(p)] + 1)
+    return np.asarray(d, dtype=np.int64)
+
+
+def positions(parents, prefix_len):
+    """RoPE position of each node: prefix_len + depth."""
+    return int(prefix_len) + depths(parents)
+
+
+def mask_matrix(parents):
+    """Boolean [N, N] visibility matrix by walking up from each node."""
+    n = len(parents)
+    m = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        j = i
+        while j != -1:
+            m[i, j] = True
+            j = int(parents[j])
+    return m
+
+
+def anc_bits(parents):
+    """uint64 [N]: bit j of entry i set <=> node j is node i or one of its ancestors."""
+    validate(parents)
+    out = []
+    for i, p in enumerate(parents):
+        bits = 1 << i
+        if p != -1:
+            bits |= out[int(p)]
+        out.append(bits)
+    return np.asarray(out, dtype=np.uint64)
+
+
+def children(parents, node):
+    """Children of ``node`` in ascending node index."""
+    return [c for c in range(len(parents)) if int(parents[c]) == node]
+
+
+def path_to(parents, node):
+    """Nodes from the root down to ``node`` inclusive."""
+    out = []
+    j = int(node)
+    while j != -1:
+        out.append(j)
+        j = int(parents[j])
+    return out[::-1]

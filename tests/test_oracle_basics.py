@@ -1,0 +1,175 @@
+"""Pins of the oracle's Philox, DSM, tree and compaction functions (CPU only)."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import compact, dsm, philox, tree
+
+
+def _read_rows(path):
+    rows = []
+    for line in open(path):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line)
+    return rows
+
+
+# ----------------------------------------------------------------------------- Philox
+def test_philox_known_answers(golden_dir):
+    rows = _read_rows(os.path.join(golden_dir, "philox4x32_10_kat.txt"))
+    assert len(rows) == 3
+    for row in rows:
+        v = [int(x, 16) for x in row.split()]
+        assert philox.philox4x32_10(v[0:4], v[4:6]) == tuple(v[6:10])
+
+
+def test_philox_vectorised_matches_scalar():
+    r = np.random.default_rng(5)
+    c = r.integers(0, 2**32, size=(4, 257), dtype=np.uint64)
+    k = r.integers(0, 2**32, size=(2, 257), dtype=np.uint64)
+    out = philox.philox4x32_10_np(c[0], c[1], c[2], c[3], k[0], k[1])
+    for i in range(257):
+        ref = philox.philox4x32_10([int(x) for x in c[:, i]], [int(x) for x in k[:, i]])
+        assert tuple(int(o[i]) for o in out) == ref
+
+
+def test_philox_uniformity():
+    # 2**16 words of the stream: mean and bit balance of a uniform 32-bit source
+    n = 1 << 16
+    out = philox.philox4x32_10_np(np.arange(n), 0, 0, 0, 123, 456)
+    u = out[0].astype(np.float64) / 2**32
+    assert abs(u.mean() - 0.5) < 4 * math.sqrt(1 / 12 / n)
+    bits = np.unpackbits(out[1].astype(">u4").view(np.uint8))
+    assert abs(bits.mean() - 0.5) < 4 * 0.5 / math.sqrt(bits.size)
+
+
+# ----------------------------------------------------------------------------- DSM
+def test_exp_matches_exp_within_ulps():
+    t = np.concatenate([-np.random.default_rng(0).random(100000) * 64,
+                        [0.0, -1e-30, -0.5, -1.0, -math.log(2.0), -63.999]]).astype(np.float32)
+    e = dsm.exp_f32(t).astype(np.float64)
+    ref = np.exp(t.astype(np.float64))
+    rel = np.abs(e - ref) / ref
+    assert rel.max() < 4 * 2.0 ** -24
+    assert dsm.exp_f32(np.float32([0.0]))[0] == 1.0
+
+
+def test_exp_underflow_and_monotone():
+    assert dsm.exp_f32(np.float32([-64.5, -100.0, -np.inf])).tolist() == [0.0, 0.0, 0.0]
+    t = np.sort(-np.random.default_rng(1).random(20000).astype(np.float32) * 30)
+    e = dsm.exp_f32(t)
+    assert np.all(np.diff(e.astype(np.float64)) >= 0)
+
+
+@pytest.mark.parametrize("S", [2**31, 2**31 + 1, 3 * 2**31, 7 * 2**31 + 12345, 128256 * 2**31 - 1,
+                               2**52 + 2**40 + 17, 2**31 * 1000003])
+def test_log31_matches_log(S):
+    got = float(dsm.log31(S))
+    ref = math.log(S / 2**31)
+    assert abs(got - ref) <= 4e-7 * max(1.0, abs(ref))
+
+
+def test_weights_match_softmax():
+    r = np.random.default_rng(2)
+    for V, T in ((8, 1.0), (1000, 1.0), (128256, 1.0), (5000, 0.7), (5000, 2.5)):
+        z = (3 * r.standard_normal(V)).astype(np.float32)
+        W, S = dsm.weights(z, dsm.inv_temperature(T))
+        assert W.max() == 2**31 and S == int(W.sum())
+        p = W / S
+        x = z.astype(np.float64) / T
+        sm = np.exp(x - x.max())
+        sm /= sm.sum()
+        # truncation to 2**-31 per entry plus fp32 rounding of t_i
+        assert np.abs(p - sm).max() <= V * 2.0**-31 + 2e-6 * sm.max()
+        lq = dsm.logq(z) if T == 1.0 else None
+        if lq is not None:
+            big = sm > 1e-6
+            assert np.abs(lq[big] - np.log(sm[big])).max() < 1e-5
+
+
+def test_logq_of_certain_token_is_zero():
+    z = np.full(16, -1000.0, np.float32)
+    z[3] = 0.0
+    lq = dsm.logq(z)
+    assert lq[3] == 0.0
+
+
+# ----------------------------------------------------------------------------- tree
+def test_tree_mask_golden(golden_dir):
+    rows = _read_rows(os.path.join(golden_dir, "tree_mask_6.txt"))
+    parents = [int(x) for x in rows[0].split(":")[1].split()]
+    want = np.array([[int(x) for x in r.split()] for r in rows[1:]], dtype=bool)
+    assert (tree.mask_matrix(parents) == want).all()
+    bits = tree.anc_bits(parents)
+    for i in range(6):
+        assert [(int(bits[i]) >> j) & 1 for j in range(6)] == want[i].astype(int).tolist()
+    assert tree.depths(parents).tolist() == [0, 1, 1, 2, 2, 2]
+    assert tree.positions(parents, 10).tolist() == [10, 11, 11, 12, 12, 12]
+
+
+def test_bitmask_matches_brute_force_on_random_trees():
+    r = np.random.default_rng(3)
+    for n in (1, 2, 7, 60, 64):
+        for _ in range(5):
+            parents = synth.random_tree(r, n, max_depth=min(63, n), max_children=10)
+            m = tree.mask_matrix(parents)
+            bits = tree.anc_bits(parents)
+            for i in range(n):
+                row = np.array([(int(bits[i]) >> j) & 1 for j in range(n)], dtype=bool)
+                assert (row == m[i]).all()
+            # depth = number of strict ancestors
+            assert (tree.depths(parents) == m.sum(1) - 1).all()
+
+
+def test_random_tree_shape():
+    r = np.random.default_rng(4)
+    for _ in range(20):
+        p = synth.random_tree(r, 60)
+        tree.validate(p)
+        d = tree.depths(p)
+        assert d.max() <= 6
+        counts = np.bincount(p[1:], minlength=60)
+        assert counts.max() <= 10
+
+
+@pytest.mark.parametrize("bad", [[0], [-1, 1], [-1, 0, 3, 1], [-1, -1], list(range(-1, 64))])
+def test_tree_validate_rejects(bad):
+    with pytest.raises(ValueError):
+        tree.validate(bad)
+
+
+# ----------------------------------------------------------------------------- compaction
+def test_compaction_equals_sequential_append():
+    r = np.random.default_rng(6)
+    layers, B, Hkv, S_max, D, N, width = 3, 4, 2, 40, 8, 12, 7
+    kc = r.standard_normal((layers, B, Hkv, S_max, D)).astype(np.float32)
+    vc = r.standard_normal((layers, B, Hkv, S_max, D)).astype(np.float32)
+    tk = r.standard_normal((layers, B, N, Hkv, D)).astype(np.float32)
+    tv = r.standard_normal((layers, B, N, Hkv, D)).astype(np.float32)
+    aux = r.standard_normal((B, N, 6)).astype(np.float32)
+    L = np.array([0, 5, 20, 33])
+    paths, alen = np.full((B, width), -1), np.zeros(B, int)
+    for b in range(B):
+        parents = synth.random_tree(r, N, max_depth=6, max_children=3)
+        leaf = int(r.integers(0, N))
+        p = tree.path_to(parents, leaf)[: S_max - L[b]]
+        paths[b, : len(p)] = p
+        alen[b] = len(p) - 1
+    k2, v2, slot, newL, aux_out = compact.compact_kv(kc, vc, tk, tv, paths, alen, L, width, aux)
+    for b in range(B):
+        # sequential append: one position at a time, like a cache.update per accepted token
+        ks = [kc[:, b, :, j] for j in range(L[b])]
+        for j in range(alen[b] + 1):
+            ks.append(tk[:, b, paths[b, j]])
+        seq = np.stack(ks, 2) if ks else None
+        assert (k2[:, b, :, : L[b] + alen[b] + 1] == seq).all()
+        assert (k2[:, b, :, L[b] + alen[b] + 1:] == kc[:, b, :, L[b] + alen[b] + 1:]).all()
+        assert newL[b] == L[b] + alen[b] + 1
+        assert slot[b, : alen[b] + 1].tolist() == list(range(L[b], L[b] + alen[b] + 1))
+        assert (slot[b, alen[b] + 1:] == -1).all()
+        assert (aux_out[b, : alen[b] + 1] == aux[b, paths[b, : alen[b] + 1]]).all()
+        assert (v2[:, b, :, L[b]: L[b] + alen[b] + 1] == np.moveaxis(tv[:, b, paths[b, : alen[b] + 1]], 1, 2)).all()

@@ -1,0 +1,206 @@
+"""Pins of the oracle's attention, tiny Llama / EAGLE-3 head and draft-tree builder (CPU only)."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import attention as att
+from oracle import draft_tree, llama, tree
+from oracle.accept import order_key
+
+
+# ----------------------------------------------------------------------------- RoPE / attention
+def test_rope_preserves_norm_and_is_relative():
+    r = np.random.default_rng(0)
+    D = 128
+    q = r.standard_normal((1, 1, D))
+    k = r.standard_normal((1, 1, D))
+    for m, n in ((3, 1), (300, 298), (700, 698)):
+        qm, kn = att.rope_apply(q, [m]), att.rope_apply(k, [n])
+        assert abs(np.linalg.norm(qm) - np.linalg.norm(q)) < 1e-9
+        if m < 400:
+            # relative-position property: <R_m q, R_n k> depends only on m - n
+            ref = float((att.rope_apply(q, [2]) * att.rope_apply(k, [0])).sum())
+            assert abs(float((qm * kn).sum()) - ref) < 2e-3
+    assert np.allclose(att.rope_apply(q, [0]), q)
+
+
+def _inputs(seed, N, L, Hq=4, Hkv=2, D=16, parents=None):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((1, N, Hq, D))
+    tk = r.standard_normal((1, N, Hkv, D))
+    tv = r.standard_normal((1, N, Hkv, D))
+    kc = r.standard_normal((1, Hkv, L + 5, D))
+    vc = r.standard_normal((1, Hkv, L + 5, D))
+    if parents is None:
+        parents = synth.random_tree(r, N, max_depth=4, max_children=3)
+    return q, tk, tv, kc, vc, np.asarray(parents)[None]
+
+
+def test_chain_tree_is_causal_attention():
+    N, L, Hq, Hkv, D = 6, 9, 4, 2, 16
+    q, tk, tv, kc, vc, parents = _inputs(1, N, L, parents=synth.chain_tree(N))
+    o, lse, kr = att.verify_attention(q, tk, tv, kc, vc, parents, [L])
+    pos = L + np.arange(N)
+    qr = att.rope_apply(q[0], pos)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        keys = np.concatenate([kc[0, g, :L], kr[0, :, g]], 0)
+        vals = np.concatenate([vc[0, g, :L], tv[0, :, g]], 0)
+        qs = np.concatenate([np.zeros((L, D)), qr[:, h]], 0)          # prefix rows unused
+        ref = att.causal_attention(qs, keys, vals, 1 / math.sqrt(D))[L:]
+        assert np.abs(o[0, :, h] - ref).max() < 1e-12
+
+
+def test_each_node_equals_its_path_as_a_sequence():
+    N, L, Hq, Hkv, D = 12, 7, 4, 2, 16
+    q, tk, tv, kc, vc, parents = _inputs(2, N, L)
+    o, lse, kr = att.verify_attention(q, tk, tv, kc, vc, parents, [L])
+    par = parents[0].tolist()
+    for i in range(N):
+        path = tree.path_to(par, i)
+        pos = L + np.arange(len(path))
+        qr = att.rope_apply(q[0, path], pos)
+        krp = att.rope_apply(tk[0, path], pos)
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            keys = np.concatenate([kc[0, g, :L], krp[:, g]], 0)
+            vals = np.concatenate([vc[0, g, :L], tv[0, path, g]], 0)
+            qs = np.concatenate([np.zeros((L, D)), qr[:, h]], 0)
+            ref = att.causal_attention(qs, keys, vals, 1 / math.sqrt(D))[-1]
+            assert np.abs(o[0, i, h] - ref).max() < 1e-12
+            s = keys @ qr[-1, h] / math.sqrt(D)
+            assert abs(lse[0, i, h] - math.log(np.exp(s).sum())) < 1e-9
+
+
+def test_empty_prefix():
+    q, tk, tv, kc, vc, parents = _inputs(3, 5, 0)
+    o, lse, kr = att.verify_attention(q, tk, tv, kc, vc, parents, [0])
+    # the root sees only itself: output = its own value row
+    for h in range(4):
+        assert np.abs(o[0, 0, h] - tv[0, 0, h // 2]).max() < 1e-12
+
+
+# ----------------------------------------------------------------------------- tiny Llama / EAGLE-3
+def _tiny():
+    cfg = synth.TINY
+    tw = synth.llama_weights(0, **cfg)
+    target = llama.Llama(tw, cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                         aux_layers=synth.TINY_AUX_LAYERS)
+    dw = synth.eagle3_weights(0, cfg["d"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                              cfg["ffn"], cfg["vocab"], embed=tw["embed"], lm_head=tw["lm_head"])
+    draft = llama.Eagle3Draft(dw, cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"])
+    return target, draft
+
+
+def _builder(depth, top_k, n_nodes):
+    def build(draft, d_cache, a_last, pending, L):
+        res = draft_tree.draft_tree_for_sequence(draft, d_cache, a_last, pending, L, depth, top_k, n_nodes)
+        return res["tokens"].tolist(), res["parents"].tolist()
+    return build
+
+
+def test_greedy_speculative_equals_vanilla_chain():
+    """Tiny lossless check: K = 4 chain, 64 new tokens, output == vanilla greedy."""
+    target, draft = _tiny()
+    prompt = synth.tiny_prompt(0)
+    ref = llama.vanilla_greedy(target, prompt, 64)
+    out, accepted = llama.speculative_greedy(target, draft, prompt, 64, _builder(4, 1, 5))
+    assert out == ref
+    assert len(out) == 64
+    assert all(0 <= a <= 4 for a in accepted)
+
+
+def test_greedy_speculative_equals_vanilla_tree():
+    target, draft = _tiny()
+    prompt = synth.tiny_prompt(1)
+    ref = llama.vanilla_greedy(target, prompt, 24)
+    out, _ = llama.speculative_greedy(target, draft, prompt, 24, _builder(3, 3, 10))
+    assert out == ref
+
+
+def _tree_vs_paths(target, prompt, parents, tokens, visible):
+    cache = target.new_cache()
+    P = len(prompt)
+    _, _, nk, nv = target.forward(prompt, np.arange(P), cache, llama.chain_visible(P))
+    target.commit(cache, nk, nv, list(range(P)))
+    logits, _, _, _ = target.forward(tokens, P + tree.depths(parents), cache, visible)
+    worst = 0.0
+    for i in range(len(parents)):
+        path = tree.path_to(parents, i)
+        c2 = target.new_cache()
+        seq = prompt + [tokens[j] for j in path]
+        ref, _, _, _ = target.forward(seq, np.arange(len(seq)), c2, llama.chain_visible(len(seq)))
+        worst = max(worst, float(np.abs(logits[i] - ref[-1]).max()))
+    return worst
+
+
+def test_tree_verify_logits_equal_path_logits():
+    """Each node's logits equal prefix + its path run as an ordinary sequence; the
+    comparison is sharp: a mask that lets every node see every node is caught."""
+    target, _ = _tiny()
+    prompt = synth.tiny_prompt(2)[:10]
+    parents = [-1, 0, 0, 1, 1, 2, 3, 5]
+    tokens = [7, 100, 200, 30, 31, 45, 12, 9]
+    assert _tree_vs_paths(target, prompt, parents, tokens, llama.tree_visible(parents)) < 1e-12
+    everything = [list(range(len(parents)))] * len(parents)
+    assert _tree_vs_paths(target, prompt, parents, tokens, everything) > 1e-6
+
+
+def test_aux_taps_enter_layers():
+    target, _ = _tiny()
+    prompt = synth.tiny_prompt(0)[:5]
+    cache = target.new_cache()
+    _, aux, _, _ = target.forward(prompt, np.arange(5), cache, llama.chain_visible(5))
+    assert aux.shape == (5, 3 * 64)
+    # layer-1 tap is the output of layer 0: embedding + attention + MLP residuals
+    emb = target.w["embed"][prompt].astype(np.float64)
+    assert not np.allclose(aux[:, :64], emb)
+
+
+# ----------------------------------------------------------------------------- dynamic tree
+def _random_expand(seed, V):
+    r = np.random.default_rng(seed)
+
+    def expand(t, front):
+        return (2.0 * r.standard_normal((len(front), V))).astype(np.float32)
+    return expand
+
+
+@pytest.mark.parametrize("depth,top_k,n_nodes", [(6, 10, 60), (4, 3, 16), (3, 5, 9), (5, 1, 6)])
+def test_dynamic_tree_invariants(depth, top_k, n_nodes):
+    logs = []
+    base = _random_expand(depth * 100 + top_k, 300)
+
+    def expand(t, front):
+        out = base(t, front)
+        logs.append(out)
+        return out
+
+    res = draft_tree.select_tree(expand, depth, top_k, n_nodes)
+    parents, dep, cands = res["parents"], res["depth"], res["cands"]
+    tree.validate(parents)
+    assert len(parents) == n_nodes
+    assert dep.max() <= depth and (dep == tree.depths(parents)).all()
+    # final set = the top N-1 by (score desc, depth asc, creation asc), brute force
+    keys = sorted(((-float(c["score"]), c["depth"], c["creation"]) for c in cands))
+    chosen = sorted((-float(cands[i]["score"]), cands[i]["depth"], cands[i]["creation"]) for i in res["chosen"])
+    assert chosen == keys[: n_nodes - 1]
+    # ancestor-closed; siblings in descending score, parents precede children
+    for i in range(1, n_nodes):
+        assert res["score"][i] <= res["score"][parents[i]] or parents[i] == 0
+    # frontier at each depth = the top_k candidates of the previous depth
+    for t in range(2, depth + 1):
+        prev = [i for i, c in enumerate(cands) if c["depth"] == t - 1]
+        prev.sort(key=lambda i: (-float(cands[i]["score"]), cands[i]["creation"]))
+        assert res["frontiers"][t - 1] == prev[:top_k]
+    # each expansion contributes the row's top-k tokens (ties to the lower id)
+    first = [c for c in cands if c["depth"] == 1]
+    row = logs[0][0]
+    assert [c["token"] for c in first] == list(np.lexsort((np.arange(300), -order_key(row)))[:top_k])
+
+
+def test_top1_tree_is_a_chain():
+    res = draft_tree.select_tree(_random_expand(5, 100), 4, 1, 5)
+    assert res["parents"].tolist() == [-1, 0, 1, 2, 3]
