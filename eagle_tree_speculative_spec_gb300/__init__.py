@@ -1,0 +1,11 @@
+"""GB300-native EAGLE-3 draft-and-verify step: CUDA kernels behind the libeagle3 C ABI.
+
+The compute path is libeagle3.so (hand-written CUDA for sm_103a); this
+package only builds it and marshals torch tensors into its C argument
+structs.  See include/eagle3.h for the contract of every entry point.
+"""
+from ._lib import (GREEDY, SAMPLED, TOPK, Eagle3Error, eagle3_accept, eagle3_compact_kv,
+                   eagle3_verify_attn, lib)
+
+__all__ = ["GREEDY", "TOPK", "SAMPLED", "Eagle3Error", "eagle3_accept", "eagle3_compact_kv",
+           "eagle3_verify_attn", "lib"]

@@ -1,0 +1,147 @@
+// Shared device helpers: Philox4x32-10, the deterministic fixed-point softmax
+// (EXP, LOG31), fp32 total order, status words, bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/eagle3.h"
+
+#define E3_DEV __device__ __forceinline__
+
+namespace e3 {
+
+// ------------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11, section 3): ten rounds of two 32x32->64 multiplies with the key bumped by the Weyl
+// constants between rounds.
+// ------------------------------------------------------------------------------------------------
+struct U4 {
+    uint32_t x0, x1, x2, x3;
+};
+
+E3_DEV U4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0, uint32_t k1) {
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint32_t hi0 = __umulhi(M0, c0), lo0 = M0 * c0;
+        const uint32_t hi1 = __umulhi(M1, c2), lo1 = M1 * c2;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return U4{c0, c1, c2, c3};
+}
+
+// Counter layout of the acceptance stage: (slot + 256 * node, b, step lo, step hi), key = seed.
+constexpr int SLOT_RESIDUAL = 64;
+constexpr int SLOT_DRAW = 128;
+
+E3_DEV U4 accept_draw(uint64_t seed, uint64_t step, int b, int node, int slot) {
+    return philox4x32_10((uint32_t)slot + 256u * (uint32_t)node, (uint32_t)b, (uint32_t)step,
+                         (uint32_t)(step >> 32), (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Deterministic fixed-point softmax.  Every step is an explicit IEEE fp32 round-to-nearest op
+// (no contraction into FMA), so the result is bit-identical to a CPU that follows the same steps.
+//   EXP(t), t <= 0: Cody-Waite reduction t = k ln2 + r with ln2 = LN2_HI + LN2_LO (LN2_HI has 16
+//   significant bits so k * LN2_HI is exact), Taylor polynomial of e^r of degree 7 (coefficients
+//   1/j! rounded to fp32) in Horner form, exact scaling by 2^k; t < -64 gives 0.
+//   W = floor(EXP(t) * 2^31) as an integer (exact: a power-of-two scaling then truncation).
+//   LOG31(S) ~ ln(S * 2^-31): S = 2^e * m with m the top 24 bits of S, folded into
+//   [sqrt(1/2), sqrt(2)); ln m = 2 s (1 + s^2/3 + ... + s^10/11), s = (m - 1) / (m + 1).
+// ------------------------------------------------------------------------------------------------
+constexpr int FIX_BITS = 31;
+constexpr float LN2_HI = 0x1.62e4p-1f;        // ln 2 rounded to 16 significant bits
+constexpr float LN2_LO = 0x1.7f7d1cp-20f;     // fp32(ln 2 - LN2_HI)
+constexpr float LOG2E = 0x1.715476p+0f;       // fp32(1 / ln 2)
+constexpr float LN2_F = 0x1.62e43p-1f;        // fp32(ln 2)
+constexpr float SQRT2_F = 0x1.6a09e6p+0f;     // fp32(sqrt 2)
+
+E3_DEV float dsm_exp(float t) {
+    if (!(t >= -64.0f)) return 0.0f;   // also catches NaN and -inf
+    const float k = rintf(__fmul_rn(t, LOG2E));
+    float r = __fsub_rn(t, __fmul_rn(k, LN2_HI));
+    r = __fsub_rn(r, __fmul_rn(k, LN2_LO));
+    float p = 0x1.a01a02p-13f;                 // 1/7!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);   // 1/6!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);    // 1/5!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);     // 1/4!
+    p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);      // 1/3!
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    const int ki = (int)k;                                    // in [-93, 0]
+    return __fmul_rn(p, __int_as_float((ki + 127) << 23));    // exact: normal power of two
+}
+
+// t_i = fp32(fp32(z_i - m) * invT)
+E3_DEV float dsm_scaled(float z, float m, float inv_t) { return __fmul_rn(__fsub_rn(z, m), inv_t); }
+
+E3_DEV uint32_t dsm_weight(float t) {
+    // EXP(t) * 2^31 <= 2^31 is exact in fp32; truncation to an integer is the floor (t <= 0 -> >= 0)
+    return (uint32_t)__fmul_rn(dsm_exp(t), 2147483648.0f);
+}
+
+E3_DEV int bitlen64(uint64_t v) { return v ? 64 - __clzll((long long)v) : 0; }
+
+E3_DEV float dsm_log31(uint64_t S) {
+    int e = bitlen64(S) - 1;
+    const uint64_t mant = e >= 23 ? (S >> (e - 23)) : (S << (23 - e));   // in [2^23, 2^24)
+    float m = __fmul_rn((float)(uint32_t)mant, 0x1p-23f);                 // exact
+    if (m > SQRT2_F) {
+        m = __fmul_rn(m, 0.5f);
+        e += 1;
+    }
+    const float s = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+    const float s2 = __fmul_rn(s, s);
+    float q = 0x1.745d18p-4f;                   // 1/11
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.c71c72p-4f);      // 1/9
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.24924ap-3f);      // 1/7
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.99999ap-3f);      // 1/5
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.555556p-2f);      // 1/3
+    q = __fadd_rn(__fmul_rn(q, s2), 1.0f);
+    const float lnm = __fmul_rn(__fmul_rn(2.0f, s), q);
+    return __fadd_rn(__fmul_rn((float)(e - FIX_BITS), LN2_F), lnm);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Total order on fp32 bit patterns: a > b as floats <=> key(a) > key(b) (and +0 > -0, NaN on top).
+// Packed with the index so that the maximum of the packed value is the maximum key with the
+// lowest index.
+// ------------------------------------------------------------------------------------------------
+E3_DEV uint32_t order_key(float z) {
+    const int32_t i = __float_as_int(z);
+    const int32_t k = i < 0 ? (i ^ 0x7FFFFFFF) : i;
+    return (uint32_t)k ^ 0x80000000u;   // signed order -> unsigned order
+}
+E3_DEV float key_to_float(uint32_t u) {
+    const int32_t k = (int32_t)(u ^ 0x80000000u);
+    return __int_as_float(k < 0 ? (k ^ 0x7FFFFFFF) : k);
+}
+E3_DEV uint64_t pack_argmax(float z, uint32_t idx) {
+    return ((uint64_t)order_key(z) << 32) | (uint64_t)(0xFFFFFFFFu - idx);
+}
+E3_DEV uint32_t unpack_idx(uint64_t p) { return 0xFFFFFFFFu - (uint32_t)p; }
+
+// ------------------------------------------------------------------------------------------------
+// Status words and bounded waits.
+// ------------------------------------------------------------------------------------------------
+E3_DEV void flag(int32_t *dev_status, int bits) {
+    if (dev_status) atomicOr(dev_status, bits);
+}
+
+// ~2 s at 2 GHz: a wait that outlives this has lost its producer
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
+
+E3_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+}  // namespace e3

@@ -1,0 +1,212 @@
+/*
+ * eagle3.h - C ABI of libeagle3, one EAGLE-3 draft-and-verify step on one GPU.
+ *
+ * Every entry point is asynchronous on the given CUDA stream and returns an
+ * eagle3_status_t.  Argument, shape and capacity errors are detected on the
+ * host, before anything is launched, and returned synchronously.  Errors that
+ * only the device can see (a malformed parent array, a token id out of range,
+ * a wait that ran out of time) are OR-ed into the caller's optional device
+ * word `dev_status` (EAGLE3_DEV_* bits); the call itself still returns
+ * EAGLE3_OK.  A failed launch returns EAGLE3_ERR_CUDA.
+ *
+ * Memory: every pointer in an argument struct is caller-owned DEVICE memory
+ * unless its comment says otherwise.  The library allocates nothing; calls
+ * that need scratch space take a caller-owned device workspace whose size the
+ * matching *_workspace_size() function returns (0 means none is needed).
+ * Tensors are dense, row-major, with the innermost dimension last, and must
+ * start on a 16-byte boundary.  bf16 values are passed as uint16_t bit
+ * patterns.  The library keeps no state between calls except cached device
+ * attributes; calls on different streams do not share memory.
+ *
+ * Tree conventions (all entry points): a draft tree of N <= 64 nodes is a
+ * parent array `parents[N]` with parents[0] = -1 (node 0 is the root, the
+ * token the target produced last step) and 0 <= parents[i] < i.  Node i sees
+ * the cached prefix, its ancestors and itself; its position is
+ * prefix_len + depth(i).
+ */
+#ifndef EAGLE3_H
+#define EAGLE3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *eagle3_stream_t; /* identical to cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    EAGLE3_OK = 0,
+    EAGLE3_ERR_INVALID_ARGUMENT = 1, /* null pointer, misaligned pointer, negative or inconsistent size */
+    EAGLE3_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. head_dim != 128, N > 64)      */
+    EAGLE3_ERR_CAPACITY = 3,         /* prefix + tree would not fit the cache (S_max)                 */
+    EAGLE3_ERR_BAD_TREE = 4,         /* host-visible tree parameters are inconsistent                */
+    EAGLE3_ERR_CUDA = 5,             /* a CUDA runtime call or kernel launch failed                   */
+    EAGLE3_ERR_WORKSPACE = 6         /* workspace missing or smaller than *_workspace_size()          */
+} eagle3_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels (device-detected conditions). */
+#define EAGLE3_DEV_BAD_TREE   0x1 /* parents[0] != -1 or parents[i] not in [0, i): that sequence is skipped  */
+#define EAGLE3_DEV_BAD_TOKEN  0x2 /* a token id outside [0, vocab): that sequence is skipped                 */
+#define EAGLE3_DEV_CAPACITY   0x4 /* a per-sequence length exceeded the bound given on the host              */
+#define EAGLE3_DEV_TIMEOUT    0x8 /* a bounded wait inside a kernel gave up; outputs of that block are void */
+#define EAGLE3_DEV_PATH_TRUNC 0x10 /* an accepted path was longer than max_path: it was cut                 */
+
+const char *eagle3_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int eagle3_version(void);
+
+/* ------------------------------------------------------------------------------------------------
+ * eagle3_accept - lossless acceptance of a verified draft tree.
+ *
+ * Defines: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", sections III.5
+ * and X.3-X.6 (accept a drafted token x with probability min(1, p(x)/q(x)); on rejection resample
+ * from norm(max(0, p - q)); if every draft is accepted draw a bonus token from the last target
+ * distribution), "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation"
+ * (greedy walk: follow the child whose token equals the target argmax) and exercise 2 (multiple
+ * candidates per node: try the children in turn, replacing p by the residual after each
+ * rejection), and "Speculative Decoding (EAGLE3) in the vLLM Neuron Framework", section
+ * "Rejection Sampling" (output rows of accepted drafts then the correction or bonus token,
+ * padded with -1).
+ *
+ * Modes:
+ *   EAGLE3_ACCEPT_GREEDY   temperature 0: pred = argmax of the node's target logits (fp32 total
+ *                          order of bit patterns, lowest id on ties); move to the lowest-index child
+ *                          whose token == pred; stop when there is none.  next_root = last pred.
+ *   EAGLE3_ACCEPT_TOPK     temperature T > 0 with children chosen deterministically (top-k of the
+ *                          draft): q is the point mass on each child, so child x is accepted with
+ *                          probability p_cur(x) and rejected children are removed from p.
+ *   EAGLE3_ACCEPT_SAMPLED  temperature T > 0 with children drawn without replacement from the
+ *                          draft's distribution q = softmax(draft_logits / T): recursive rejection
+ *                          sampling with the residual max(0, p - q) and q renormalised after each
+ *                          removed child.
+ * Probabilities are the deterministic fixed-point softmax: W_i = floor(EXP((z_i - max z) / T) *
+ * 2^31) with a specified fp32 EXP, p_i = W_i / sum W; every comparison is exact integer
+ * arithmetic.  Random words come from Philox4x32-10 (Salmon et al., SC'11) with key = seed and
+ * counter = (slot + 256 * node, b, step low, step high): U32 = word 0 for the accept test of the
+ * s-th child (slot s), R64 = word1:word2 for the residual / bonus draw (slot 64).
+ * ---------------------------------------------------------------------------------------------- */
+typedef enum {
+    EAGLE3_ACCEPT_GREEDY = 0,
+    EAGLE3_ACCEPT_TOPK = 1,
+    EAGLE3_ACCEPT_SAMPLED = 2
+} eagle3_accept_mode_t;
+
+typedef struct {
+    int32_t mode;               /* eagle3_accept_mode_t                                               */
+    int32_t batch;              /* B >= 0                                                              */
+    int32_t n_nodes;            /* N in [1, 64]                                                        */
+    int32_t vocab;              /* V in [1, 2^22]                                                      */
+    int32_t max_path;           /* width W of path / emitted rows, >= 1 (a path of depth d needs d+1)  */
+    float temperature;          /* T > 0 for TOPK / SAMPLED; ignored for GREEDY                        */
+    uint64_t seed;              /* Philox key                                                          */
+    uint64_t step;              /* draft-and-verify cycle counter (Philox counter words 2, 3)          */
+    const float *target_logits; /* [B, N, V] fp32: target logits at every tree node                   */
+    const float *draft_logits;  /* [B, N, V] fp32: draft logits at every node (SAMPLED only, else NULL)*/
+    const int32_t *tokens;      /* [B, N] token of each node (node 0's entry is not read)              */
+    const int32_t *parents;     /* [B, N] parent arrays                                                */
+    int32_t *accept_len;        /* [B] out: number of accepted draft nodes n (path has n+1 nodes)      */
+    int32_t *path;              /* [B, W] out: node ids root..last accepted, then -1                   */
+    int32_t *emitted;           /* [B, W] out: tokens of path[1..n], then next_root, then -1           */
+    int32_t *next_root;         /* [B] out: correction / bonus token (the next step's root)           */
+    int32_t *dev_status;        /* [1] optional device word for EAGLE3_DEV_* bits (may be NULL)       */
+} eagle3_accept_args_t;
+
+size_t eagle3_accept_workspace_size(const eagle3_accept_args_t *args);
+eagle3_status_t eagle3_accept(const eagle3_accept_args_t *args, void *workspace, size_t workspace_bytes,
+                              eagle3_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * eagle3_compact_kv - copy the accepted path's K/V into contiguous cache slots.
+ *
+ * Defines: "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation" (the
+ * path's K/V were computed during verification at the right positions; append them to the cache
+ * without recomputation, drop the rejected nodes) and "EAGLE-3: Engineering Implementation of LLM
+ * Inference Acceleration", section XI.4 (the target cache keeps exactly the committed positions).
+ *
+ * For each sequence b with L = prefix_len[b] and n = accept_len[b]: for j = 0..n, every layer and
+ * KV head, cache slot L + j <- tree row path[b, j]; slot_map[b, j] = L + j (then -1); optional aux
+ * rows are gathered in path order; finally prefix_len[b] = L + n + 1.  Copies are bit-exact.
+ * Source and destination must not overlap (the tree K/V live in their own buffers).
+ * Sequences with L + n + 1 > s_max or a path entry outside [0, N) are skipped and flagged.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t n_layers;            /* >= 1                                                              */
+    int32_t batch;               /* B >= 0                                                            */
+    int32_t n_nodes;             /* N in [1, 64]                                                      */
+    int32_t n_kv_heads;          /* Hkv >= 1                                                          */
+    int32_t head_dim;            /* D >= 1                                                            */
+    int32_t elem_bytes;          /* 2 (bf16) or 4 (fp32)                                              */
+    int32_t s_max;               /* cache capacity in positions                                       */
+    int32_t max_path;            /* width W of path / slot_map rows                                   */
+    int64_t cache_layer_stride;  /* elements between consecutive layers of k_cache / v_cache          */
+    int64_t tree_layer_stride;   /* elements between consecutive layers of tree_k / tree_v            */
+    void *k_cache;               /* [layers][B, Hkv, s_max, D]                                        */
+    void *v_cache;               /* [layers][B, Hkv, s_max, D]                                        */
+    const void *tree_k;          /* [layers][B, N, Hkv, D] (already rotated by eagle3_verify_attn)    */
+    const void *tree_v;          /* [layers][B, N, Hkv, D]                                            */
+    const int32_t *path;         /* [B, W] from eagle3_accept                                         */
+    const int32_t *accept_len;   /* [B]                                                               */
+    int32_t *prefix_len;         /* [B] in: L; out: L + n + 1                                         */
+    int32_t *slot_map;           /* [B, W] out                                                        */
+    int32_t aux_dim;             /* A: elements per aux row; 0 = no aux gather                        */
+    const void *aux_tree;        /* [B, N, A] (elem_bytes each) or NULL                               */
+    void *aux_out;               /* [B, W, A] or NULL                                                 */
+    int32_t *dev_status;         /* optional                                                          */
+} eagle3_compact_args_t;
+
+eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *args, eagle3_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * eagle3_verify_attn - tree-masked verify attention for one layer (bf16, GQA, head_dim 128).
+ *
+ * Defines: "Advanced speculative decoding: tree drafts and EAGLE", sections "Why trees" and
+ * "Implementation" (forward_with_mask: every node attends to the whole cached prefix and to the
+ * tree nodes its mask row allows - itself and its ancestors - at position prefix_len + depth) and
+ * "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", appendix C (rotate-half
+ * RoPE with inv_j = theta^(-2j/D); grouped-query attention; scores scaled by sm_scale).
+ *
+ * For each sequence b (L = prefix_len[b]), node i and query head h (KV head g = h / (Hq/Hkv)):
+ *   out[b,i,h] = sum_j softmax_j(q_i . k_j * sm_scale) v_j over keys j in
+ *                {cache positions 0..L-1} U {tree nodes that are i or an ancestor of i}.
+ * q and tree_k arrive un-rotated; the kernel applies RoPE at position L + depth(i) to both, and
+ * writes the rotated tree keys back into tree_k (so eagle3_compact_kv copies rotated keys).  The
+ * cache holds rotated keys.  fp32 softmax and accumulation; out in bf16.  lse (optional) gets the
+ * natural-log sum of exp of the scaled scores.
+ * The prefix is split across CTAs (split-KV) by a plan made from max_prefix_len (a host bound on
+ * every prefix_len[b]); partial results are merged by a second kernel in a fixed order.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t batch;              /* B >= 0                                                             */
+    int32_t n_nodes;            /* N in [1, 64]                                                       */
+    int32_t n_heads;            /* Hq, a multiple of n_kv_heads                                       */
+    int32_t n_kv_heads;         /* Hkv                                                                */
+    int32_t head_dim;           /* D; 128 is supported                                                */
+    int32_t s_max;              /* cache capacity; max_prefix_len + N <= s_max is required            */
+    int32_t max_prefix_len;     /* host bound on prefix_len[b]                                        */
+    int32_t num_splits;         /* 0 = choose automatically                                           */
+    float rope_theta;           /* e.g. 500000                                                        */
+    float sm_scale;             /* 0 = 1/sqrt(D)                                                      */
+    const uint16_t *q;          /* [B, N, Hq, D] bf16, un-rotated                                     */
+    uint16_t *tree_k;           /* [B, N, Hkv, D] bf16, in: un-rotated, out: rotated                  */
+    const uint16_t *tree_v;     /* [B, N, Hkv, D] bf16                                                */
+    const uint16_t *k_cache;    /* [B, Hkv, s_max, D] bf16, rotated keys                              */
+    const uint16_t *v_cache;    /* [B, Hkv, s_max, D] bf16                                            */
+    const int32_t *parents;     /* [B, N]                                                             */
+    const int32_t *prefix_len;  /* [B]                                                                */
+    uint16_t *out;              /* [B, N, Hq, D] bf16                                                 */
+    float *lse;                 /* [B, N, Hq] fp32 or NULL                                            */
+    int32_t *dev_status;        /* optional                                                           */
+} eagle3_verify_attn_args_t;
+
+size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *args);
+eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *args, void *workspace,
+                                   size_t workspace_bytes, eagle3_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE3_H */

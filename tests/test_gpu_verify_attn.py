@@ -1,0 +1,75 @@
+"""GPU parity: eagle3_verify_attn against the fp64 oracle (bf16 tolerance 2e-2 abs / 1e-2 rel)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import attention as oatt
+from tests._util import close, require_gpu
+
+pytestmark = pytest.mark.gpu
+ATOL, RTOL = 2e-2, 1e-2
+
+
+def _run(inp, max_prefix, num_splits=0, lse=True):
+    from eagle_tree_speculative_spec_gb300 import eagle3_verify_attn
+    dev = require_gpu()
+    q, tk, tv = inp["q"].to(dev), inp["tree_k"].to(dev).clone(), inp["tree_v"].to(dev)
+    kc, vc = inp["k_cache"].to(dev), inp["v_cache"].to(dev)
+    parents = torch.as_tensor(inp["parents"], device=dev)
+    plen = torch.as_tensor(inp["prefix_len"], device=dev)
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse_t = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev) if lse else None
+    eagle3_verify_attn(q, tk, tv, kc, vc, parents, plen, out, max_prefix_len=max_prefix, lse=lse_t,
+                       num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), (lse_t.cpu().numpy() if lse else None), tk.float().cpu().numpy()
+
+
+def _check(inp, got, rows):
+    o, lse, krot = got
+    ref_o, ref_lse, ref_k = oatt.verify_attention(inp["q_f32"], inp["tree_k_f32"], inp["tree_v_f32"],
+                                                  inp["k_cache_f32"], inp["v_cache_f32"], inp["parents"],
+                                                  inp["prefix_len"], batch_rows=rows)
+    for b in rows:
+        ok, err = close(o[b], ref_o[b], ATOL, RTOL)
+        assert ok, f"out b={b} max err {err}"
+        ok, err = close(krot[b], ref_k[b], 1e-2, 1e-2)
+        assert ok, f"rotated tree_k b={b} max err {err}"
+        if lse is not None:
+            ok, err = close(lse[b], ref_lse[b], ATOL, RTOL)
+            assert ok, f"lse b={b} max err {err}"
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 3])
+def test_verify_small_ragged(splits):
+    Hq, Hkv, D, N = 32, 8, 128, 60
+    lens = [0, 1, 63, 64, 65, 200]
+    inp = synth.verify_attn_batch(31, len(lens), N, Hq, Hkv, D, lens, S_max=300)
+    got = _run(inp, max(lens), num_splits=splits)
+    _check(inp, got, range(len(lens)))
+
+
+@pytest.mark.parametrize("N", [1, 2, 17, 64])
+def test_verify_node_counts(N):
+    inp = synth.verify_attn_batch(32, 2, N, 32, 8, 128, [100, 37], S_max=200)
+    got = _run(inp, 100)
+    _check(inp, got, range(2))
+
+
+def test_verify_other_gqa_ratio():
+    inp = synth.verify_attn_batch(33, 2, 40, 16, 2, 128, [130, 77], S_max=200)   # rep 8: 320 rows > 256
+    with pytest.raises(Exception):
+        _run(inp, 130)
+    inp = synth.verify_attn_batch(33, 2, 30, 16, 2, 128, [130, 77], S_max=200)   # rep 8 x 30 nodes = 240 rows
+    _check(inp, _run(inp, 130), range(2))
+
+
+@pytest.mark.parametrize("B,L", [(1, 512), (8, 4096), (64, 4096), (1, 16384)])
+def test_verify_full_size(B, L):
+    """Llama-3.1-8B shapes (32/8 heads, head_dim 128, N = 60) at the sizes of the verify workload;
+    the oracle checks sampled sequences."""
+    inp = synth.verify_attn_batch(3, B, 60, 32, 8, 128, [L] * B, S_max=L + 64)
+    got = _run(inp, L)
+    rows = sorted({0, B // 2, B - 1})
+    _check(inp, got, rows)
