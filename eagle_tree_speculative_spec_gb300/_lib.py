@@ -66,6 +66,15 @@ class VerifyAttnArgs(ctypes.Structure):
                 ("parents", _p), ("prefix_len", _p), ("out", _p), ("lse", _p), ("dev_status", _p)]
 
 
+class LinearArgs(ctypes.Structure):
+    _fields_ = [("m", _i32), ("n", _i32), ("k", _i32), ("epilogue", _i32), ("splits", _i32),
+                ("ld_x", _i64), ("ld_w", _i64), ("ld_out", _i64), ("ld_res", _i64),
+                ("x", _p), ("w", _p), ("w2", _p), ("out", _p), ("residual", _p), ("dev_status", _p)]
+
+
+EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU = 0, 1, 2, 3
+
+
 def _declare(L):
     P = ctypes.POINTER
     L.eagle3_status_string.restype = ctypes.c_char_p
@@ -81,6 +90,10 @@ def _declare(L):
     L.eagle3_verify_attn_workspace_size.argtypes = [P(VerifyAttnArgs)]
     L.eagle3_verify_attn.restype = ctypes.c_int
     L.eagle3_verify_attn.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_linear_workspace_size.restype = ctypes.c_size_t
+    L.eagle3_linear_workspace_size.argtypes = [P(LinearArgs)]
+    L.eagle3_linear.restype = ctypes.c_int
+    L.eagle3_linear.argtypes = [P(LinearArgs), _p, ctypes.c_size_t, _p]
 
 
 def status_string(status):
@@ -214,3 +227,27 @@ def eagle3_verify_attn(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len,
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.eagle3_verify_attn(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_verify_attn")
+
+
+def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, splits=0, dev_status=None,
+                  workspace=None, stream=None):
+    """out = epilogue(x W^T) on the tensor cores.  x [m, k] bf16, w (and w2) [n, k] bf16,
+    out [m, n] bf16 (fp32 for EPI_F32), residual [m, n] bf16 for EPI_BF16_RESIDUAL."""
+    m, k = x.shape
+    n = w.shape[0]
+    if w.shape[1] != k or (w2 is not None and tuple(w2.shape) != (n, k)):
+        raise ValueError("weight shapes do not match x")
+    if tuple(out.shape) != (m, n):
+        raise ValueError(f"out must be [{m}, {n}]")
+    want = torch.float32 if epilogue == EPI_F32 else torch.bfloat16
+    bf = torch.bfloat16
+    a = LinearArgs(m=m, n=n, k=k, epilogue=int(epilogue), splits=int(splits), ld_x=0, ld_w=0, ld_out=0, ld_res=0,
+                   x=_ptr(x, bf, "x"), w=_ptr(w, bf, "w"), w2=_ptr(w2, bf, "w2"), out=_ptr(out, want, "out"),
+                   residual=_ptr(residual, bf, "residual"), dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+    L = lib()
+    need = L.eagle3_linear_workspace_size(ctypes.byref(a))
+    if workspace is None:
+        workspace = _workspace(need, x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.eagle3_linear(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_linear")

@@ -1,0 +1,57 @@
+/*
+ * eagle3_linear.h - the tensor-core linear layer of libeagle3 (building block).
+ *
+ * Defines: the bias-free nn.Linear projections of "EAGLE-3: Engineering Implementation of LLM
+ * Inference Acceleration", section VIII and appendix C (fc 3k -> k, q/k/v from 2k, o, SwiGLU
+ * gate/up/down, lm_head), out = x W^T, used by the draft head and by the target layers that
+ * verify a tree.  bf16 inputs, fp32 accumulation on the tcgen05 tensor cores, fused epilogues:
+ *   EAGLE3_EPI_BF16           out (bf16) = x W^T
+ *   EAGLE3_EPI_F32            out (fp32) = x W^T                    (logits)
+ *   EAGLE3_EPI_BF16_RESIDUAL  out (bf16) = residual + x W^T         (residual stream; out may be
+ *                                                                    the residual buffer itself)
+ *   EAGLE3_EPI_SWIGLU         out (bf16) = silu(x W^T) * (x W2^T)   (W = gate, W2 = up, both [n, k])
+ * Shapes: x [m, k] (row pitch ld_x), W and W2 [n, k] (row pitch ld_w), out [m, n] (pitch ld_out),
+ * residual [m, n] (pitch ld_res); a pitch of 0 means dense.  k and every pitch must be multiples of
+ * 8 elements and x, W, W2 must start on 16-byte boundaries.  All pointers are caller-owned device
+ * memory.  When the k dimension is split across CTAs (small m), fp32 partials go to the caller's
+ * workspace (eagle3_linear_workspace_size bytes) and are added in split order: results do not
+ * depend on the launch configuration beyond that fixed order.  Errors: as in eagle3.h.
+ */
+#ifndef EAGLE3_LINEAR_H
+#define EAGLE3_LINEAR_H
+
+#include "eagle3.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EAGLE3_EPI_BF16 = 0,
+    EAGLE3_EPI_F32 = 1,
+    EAGLE3_EPI_BF16_RESIDUAL = 2,
+    EAGLE3_EPI_SWIGLU = 3
+} eagle3_epilogue_t;
+
+typedef struct {
+    int32_t m, n, k;            /* rows of x, rows of W (= output columns), contraction length   */
+    int32_t epilogue;           /* eagle3_epilogue_t                                              */
+    int32_t splits;             /* k splits; 0 = choose from the shape                            */
+    int64_t ld_x, ld_w, ld_out, ld_res;   /* row pitches in elements, 0 = dense                   */
+    const uint16_t *x;          /* [m, k] bf16                                                    */
+    const uint16_t *w;          /* [n, k] bf16                                                    */
+    const uint16_t *w2;         /* [n, k] bf16 (SWIGLU only)                                      */
+    void *out;                  /* [m, n] bf16 or fp32                                            */
+    const uint16_t *residual;   /* [m, n] bf16 (BF16_RESIDUAL only)                               */
+    int32_t *dev_status;        /* optional EAGLE3_DEV_* word                                     */
+} eagle3_linear_args_t;
+
+size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *args);
+eagle3_status_t eagle3_linear(const eagle3_linear_args_t *args, void *workspace, size_t workspace_bytes,
+                              eagle3_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE3_LINEAR_H */

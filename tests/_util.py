@@ -6,12 +6,12 @@ import pytest
 import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "eagle3.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("eagle3.h", "eagle3_linear.h")]
 
 
 def header_functions():
     """Names of the functions include/eagle3.h declares."""
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|eagle3_status_t|size_t|int)\s*(eagle3_\w+)\s*\(",
                                  text, flags=re.M)))
 

@@ -1,0 +1,100 @@
+"""GPU numerics of the tcgen05 linear layer against an fp64 matmul of the same bf16 inputs
+(bf16 outputs: 2e-2 abs + 1e-2 rel; fp32 outputs: 1e-3 abs + 1e-3 rel)."""
+import numpy as np
+import pytest
+import torch
+
+from tests._util import close, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(m, n, k, seed, swiglu=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(m, k, generator=g).to(torch.bfloat16)
+    w = (0.02 * torch.randn(n, k, generator=g)).to(torch.bfloat16)
+    w2 = (0.02 * torch.randn(n, k, generator=g)).to(torch.bfloat16) if swiglu else None
+    return x, w, w2
+
+
+def _ref(x, w):
+    return x.double().numpy() @ w.double().numpy().T
+
+
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def _run(m, n, k, epi, seed=0, splits=0):
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16_RESIDUAL, EPI_F32, EPI_SWIGLU, eagle3_linear
+    dev = require_gpu()
+    x, w, w2 = _inputs(m, n, k, seed, swiglu=epi == EPI_SWIGLU)
+    res = torch.randn(m, n).to(torch.bfloat16) if epi == EPI_BF16_RESIDUAL else None
+    out = torch.full((m, n), float("nan"), dtype=torch.float32 if epi == EPI_F32 else torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    eagle3_linear(x.to(dev), w.to(dev), out, epilogue=epi, w2=None if w2 is None else w2.to(dev),
+                  residual=None if res is None else res.to(dev), splits=splits, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.float().cpu().numpy()
+    if epi == EPI_SWIGLU:
+        want = _silu(_ref(x, w)) * _ref(x, w2)
+    else:
+        want = _ref(x, w)
+        if res is not None:
+            want = want + res.double().numpy()
+    return got, want
+
+
+def test_linear_single_tile():
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16
+    got, want = _run(128, 256, 64, EPI_BF16)
+    ok, err = close(got, want, 2e-2, 1e-2)
+    assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,splits", [
+    (128, 256, 128, 1), (5, 1000, 64, 0), (130, 300, 200, 0), (10, 4096, 12288, 0), (10, 4096, 12288, 3),
+    (640, 6144, 8192, 0), (257, 512, 4096, 2), (1, 256, 64, 0)])
+def test_linear_bf16(m, n, k, splits):
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16
+    got, want = _run(m, n, k, EPI_BF16, seed=m + n + k, splits=splits)
+    ok, err = close(got, want, 2e-2, 1e-2)
+    assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k", [(10, 128256, 4096), (130, 1000, 4096), (64, 4096, 64)])
+def test_linear_f32_logits(m, n, k):
+    from eagle_tree_speculative_spec_gb300 import EPI_F32
+    got, want = _run(m, n, k, EPI_F32, seed=1)
+    ok, err = close(got, want, 1e-3, 1e-3)
+    assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,splits", [(10, 4096, 4096, 0), (640, 4096, 14336, 0), (70, 256, 256, 1)])
+def test_linear_residual(m, n, k, splits):
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16_RESIDUAL
+    got, want = _run(m, n, k, EPI_BF16_RESIDUAL, seed=2, splits=splits)
+    ok, err = close(got, want, 2e-2, 1e-2)
+    assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,splits", [(10, 14336, 4096, 0), (640, 14336, 4096, 0), (33, 300, 512, 3)])
+def test_linear_swiglu(m, n, k, splits):
+    from eagle_tree_speculative_spec_gb300 import EPI_SWIGLU
+    got, want = _run(m, n, k, EPI_SWIGLU, seed=3, splits=splits)
+    ok, err = close(got, want, 2e-2, 1e-2)
+    assert ok, err
+
+
+def test_linear_in_place_residual():
+    """out may be the residual buffer itself (x = x + o_proj(attn))."""
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16_RESIDUAL, eagle3_linear
+    dev = require_gpu()
+    x, w, _ = _inputs(64, 512, 512, 9)
+    r = torch.randn(64, 512).to(torch.bfloat16)
+    buf = r.to(dev).clone()
+    eagle3_linear(x.to(dev), w.to(dev), buf, epilogue=EPI_BF16_RESIDUAL, residual=buf)
+    torch.cuda.synchronize()
+    ok, err = close(buf.float().cpu().numpy(), _ref(x, w) + r.double().numpy(), 2e-2, 1e-2)
+    assert ok, err
