@@ -1,0 +1,532 @@
+"""Benchmark: one EAGLE-3 draft-and-verify step per iteration on GB300.
+
+Workload (default): Llama-3.1-8B-shaped random-init target (32 layers, d 4096, GQA 32/8, FFN
+14336, vocab 128256, bf16) and EAGLE-3 draft head (fc 12288->4096, one decoder layer, own LM
+head), batch 64, 2048-token prefixes, 60-node dynamic trees (depth 6, top-k 10), temperature 1
+(TOPK rejection sampling, Philox seed 2), compaction of the accepted path into the caches.  A
+step is: eagle3_draft_tree -> 32 target layers over the tree (RMSNorm with fused aux taps,
+tcgen05 QKV / O / SwiGLU / down GEMMs, eagle3_verify_attn) -> final norm -> LM head (fp32
+logits) -> eagle3_accept -> eagle3_compact_kv; its outputs feed the next step (a real decoding
+loop).  Metric: verified tree tokens per second (B * N per step).
+
+Every number comes from CUDA events on the launching stream; the dominant kernel (the tcgen05
+GEMM) and the verify attention are also timed per launch inside the timed region.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "verified tree tokens/s per GB300 (draft+verify+accept); verify-attn HBM GB/s"
+UNIT = "tokens/s"
+
+CFG = dict(layers=32, d=4096, Hq=32, Hkv=8, D=128, F=14336, V=128256, taps=(2, 15, 29),
+           B=64, N=60, L0=2048, depth=6, top_k=10, W=7, temperature=1.0, seed=2)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons), timestamped on arrival.
+
+    The sampler is started before the warm-up so that its own start-up is not inside the timed
+    region; summary() keeps only the samples that arrived inside [t0, t1]."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1]
+        if not rows:      # timed region shorter than one period: take the nearest samples
+            rows = [r for (t, r) in self.rows][-2:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        num = lambda v: v.replace(".", "", 1).isdigit()
+        sm = sorted(float(r[1]) for r in rows if num(r[1]))
+        mx = max([float(r[2]) for r in rows if num(r[2])] or [0.0])
+        reasons = sorted({self.NAMES[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------------------- GPU arm
+class Engine:
+    """Device state of the speculative-decoding loop and one step over the C ABI."""
+
+    def __init__(self, cfg, steps_total, dev, timing=True):
+        import eagle_tree_speculative_spec_gb300 as e3
+        self.e3, self.cfg, self.dev, self.timing = e3, cfg, dev, timing
+        c = cfg
+        B, N, d, V, D = c["B"], c["N"], c["d"], c["V"], c["D"]
+        Hq, Hkv, F, Lyr = c["Hq"], c["Hkv"], c["F"], c["layers"]
+        self.qkv_w = (Hq + 2 * Hkv) * D
+        self.S = c["L0"] + c["W"] * (steps_total + 2) + 64
+        g = torch.Generator(device=dev)
+        g.manual_seed(1234)
+        bf = torch.bfloat16
+
+        def w(*shape, std=0.02):
+            return (torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * std).to(bf)
+
+        ones = lambda n: torch.ones(n, device=dev, dtype=bf)
+        # target (random init N(0, 0.02), norms 1)
+        self.embed = w(V, d)
+        self.wqkv = [w(self.qkv_w, d) for _ in range(Lyr)]
+        self.wo = [w(d, Hq * D) for _ in range(Lyr)]
+        self.wg = [w(F, d) for _ in range(Lyr)]
+        self.wu = [w(F, d) for _ in range(Lyr)]
+        self.wd = [w(d, F) for _ in range(Lyr)]
+        self.norm1 = [ones(d) for _ in range(Lyr)]
+        self.norm2 = [ones(d) for _ in range(Lyr)]
+        self.final_norm = ones(d)
+        self.lm_head = w(V, d)
+        # draft head (shares the target embedding; own LM head)
+        self.draft_w = {"w_fc": w(d, 3 * d), "embed": self.embed, "input_norm": ones(d), "hidden_norm": ones(d),
+                        "w_qkv": w(self.qkv_w, 2 * d), "w_o": w(d, Hq * D), "post_norm": ones(d),
+                        "w_gate": w(F, d), "w_up": w(F, d), "w_down": w(d, F), "final_norm": ones(d),
+                        "lm_head": w(V, d)}
+        # caches: prefixes of L0 positions of N(0, 1) keys / values (as if prefilled)
+        S = self.S
+        self.k_cache = torch.zeros(Lyr, B, Hkv, S, D, device=dev, dtype=bf)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.k_cache[..., : c["L0"], :].normal_(generator=g)
+        self.v_cache[..., : c["L0"], :].normal_(generator=g)
+        self.dk_cache = torch.zeros(B, Hkv, S, D, device=dev, dtype=bf)
+        self.dv_cache = torch.zeros_like(self.dk_cache)
+        self.dk_cache[..., : c["L0"] - 1, :].normal_(generator=g)
+        self.dv_cache[..., : c["L0"] - 1, :].normal_(generator=g)
+        i32 = torch.int32
+        self.prefix_len = torch.full((B,), c["L0"], dtype=i32, device=dev)
+        self.draft_len = torch.full((B,), c["L0"] - 1, dtype=i32, device=dev)
+        # catch-up input of the first step: the last prompt position's aux states and the root token
+        W = c["W"]
+        self.aux_in = torch.zeros(B, W, 3 * d, device=dev, dtype=bf)
+        self.aux_in[:, 0].normal_(generator=g)
+        self.next_tok = torch.randint(0, V, (B, W), generator=g, device=dev, dtype=i32)
+        self.tc = torch.ones(B, dtype=i32, device=dev)
+        # per-step buffers
+        self.tokens = torch.empty(B, N, dtype=i32, device=dev)
+        self.parents = torch.empty(B, N, dtype=i32, device=dev)
+        self.depth = torch.empty(B, N, dtype=i32, device=dev)
+        self.anc = torch.empty(B, N, dtype=torch.int64, device=dev)
+        self.score = torch.empty(B, N, dtype=torch.float32, device=dev)
+        R = B * N
+        self.x = torch.empty(R, d, device=dev, dtype=bf)
+        self.h = torch.empty(R, d, device=dev, dtype=bf)
+        self.qkv = torch.empty(Lyr, R, self.qkv_w, device=dev, dtype=bf)
+        self.attn = torch.empty(R, Hq * D, device=dev, dtype=bf)
+        self.act = torch.empty(R, F, device=dev, dtype=bf)
+        self.aux_tree = torch.empty(R, 3 * d, device=dev, dtype=bf)
+        self.logits = torch.empty(R, V, device=dev, dtype=torch.float32)
+        self.accept_len = torch.empty(B, dtype=i32, device=dev)
+        self.path = torch.empty(B, W, dtype=i32, device=dev)
+        self.next_root = torch.empty(B, dtype=i32, device=dev)
+        self.slot_map = torch.empty(B, W, dtype=i32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        # workspaces (sized once for the largest shapes)
+        self.ws_lin = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.ws_attn = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.ws_acc = torch.empty(16, dtype=torch.uint8, device=dev)
+        self.ws_draft = None
+        self.steps_done = 0
+        self.kernel_ms = {"gemm": 0.0, "verify_attn": 0.0}
+        self.kernel_calls = {"gemm": 0, "verify_attn": 0}
+        self._ev = []
+
+    # -- per-launch timing of the dominant kernels (CUDA events on the launching stream)
+    def _timed(self, kind, fn):
+        if not self.timing:
+            fn()
+            return
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        self._ev.append((kind, a, b))
+
+    def collect(self):
+        torch.cuda.synchronize()
+        for kind, a, b in self._ev:
+            self.kernel_ms[kind] += a.elapsed_time(b)
+            self.kernel_calls[kind] += 1
+        self._ev = []
+
+    def reset_counters(self):
+        self.collect()
+        self.kernel_ms = {k: 0.0 for k in self.kernel_ms}
+        self.kernel_calls = {k: 0 for k in self.kernel_calls}
+
+    def lin(self, x, w, out, **kw):
+        self._timed("gemm", lambda: self.e3.eagle3_linear(x, w, out, workspace=self.ws_lin, **kw))
+
+    def step(self):
+        e3, c = self.e3, self.cfg
+        B, N, d, D, Hq, Hkv = c["B"], c["N"], c["d"], c["D"], c["Hq"], c["Hkv"]
+        R = B * N
+        max_prefix = c["L0"] + c["W"] * self.steps_done
+        # ---- draft: catch-up of the committed positions + dynamic tree
+        if self.ws_draft is None:
+            a = e3._lib.draft_tree_args(self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
+                                        self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
+                                        n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
+                                        max_draft_len=self.S - c["W"] - 1)
+            self.ws_draft = torch.empty(e3._lib.eagle3_draft_tree_workspace_size(a), dtype=torch.uint8,
+                                        device=self.dev)
+        e3.eagle3_draft_tree(self.draft_w, self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
+                             self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
+                             n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
+                             max_draft_len=max_prefix - 1, workspace=self.ws_draft, dev_status=self.dev_status)
+        # ---- verify: the target over the tree (positions prefix_len + depth)
+        taps = {t: i for i, t in enumerate(c["taps"])}
+        e3.eagle3_rmsnorm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap_out=self.x)
+        for l in range(c["layers"]):
+            if l > 0:
+                tap = self.aux_tree[:, taps[l] * d:(taps[l] + 1) * d] if l in taps else None
+                e3.eagle3_rmsnorm(self.x, self.norm1[l], self.h, tap_out=tap)
+            qkv = self.qkv[l]
+            self.lin(self.h, self.wqkv[l], qkv)
+            q = qkv.view(B, N, self.qkv_w)[:, :, : Hq * D].unflatten(2, (Hq, D))
+            kt = qkv.view(B, N, self.qkv_w)[:, :, Hq * D:(Hq + Hkv) * D].unflatten(2, (Hkv, D))
+            vt = qkv.view(B, N, self.qkv_w)[:, :, (Hq + Hkv) * D:].unflatten(2, (Hkv, D))
+            self._timed("verify_attn", lambda: e3.eagle3_verify_attn(
+                q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
+                self.attn.view(B, N, Hq, D), max_prefix_len=max_prefix, workspace=self.ws_attn,
+                dev_status=self.dev_status))
+            self.lin(self.attn, self.wo[l], self.x, epilogue=e3.EPI_BF16_RESIDUAL, residual=self.x)
+            e3.eagle3_rmsnorm(self.x, self.norm2[l], self.h)
+            self.lin(self.h, self.wg[l], self.act, epilogue=e3.EPI_SWIGLU, w2=self.wu[l])
+            self.lin(self.act, self.wd[l], self.x, epilogue=e3.EPI_BF16_RESIDUAL, residual=self.x)
+        e3.eagle3_rmsnorm(self.x, self.final_norm, self.h)
+        self.lin(self.h, self.lm_head, self.logits, epilogue=e3.EPI_F32)
+        # ---- accept (TOPK rejection sampling at T = 1) and compaction
+        e3.eagle3_accept(e3.TOPK, self.logits.view(B, N, c["V"]), self.tokens, self.parents, self.accept_len,
+                         self.path, self.next_tok, self.next_root, temperature=c["temperature"], seed=c["seed"],
+                         step=self.steps_done, workspace=self.ws_acc, dev_status=self.dev_status)
+        self._compact()
+        self.steps_done += 1
+
+    def _compact(self):
+        c = self.cfg
+        B, N, d = c["B"], c["N"], c["d"]
+        R = B * N
+        # flat views that start at the first key / value element of layer 0
+        kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=c["Hq"] * c["D"])
+        vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(c["Hq"] + c["Hkv"]) * c["D"])
+        self.e3.eagle3_compact_kv(self.k_cache, self.v_cache, kflat, vflat, self.path, self.accept_len,
+                                  self.prefix_len, self.slot_map, aux_tree=self.aux_tree.view(B, N, 3 * d),
+                                  aux_out=self.aux_in, committed=self.tc, tree_node_stride=self.qkv_w,
+                                  tree_layer_stride=R * self.qkv_w, dev_status=self.dev_status)
+
+    def flops_per_step(self):
+        """Algorithmic GEMM flops of one step (target verify + draft head)."""
+        c = self.cfg
+        d, F, V, Hq, D, qw = c["d"], c["F"], c["V"], c["Hq"], c["D"], self.qkv_w
+        R = c["B"] * c["N"]
+        per_layer = 2 * R * (d * qw + Hq * D * d + 2 * d * F + F * d)
+        target = c["layers"] * per_layer + 2 * R * d * V
+        rows_d = c["B"] * c["top_k"]
+        draft_layer = lambda m: 2 * m * (2 * d * qw + Hq * D * d + 2 * d * F + F * d)
+        tc_rows = c["B"] * c["W"]          # catch-up rows are padded to W per sequence
+        draft = (2 * tc_rows * 3 * d * d + draft_layer(tc_rows) + 2 * c["B"] * d * V
+                 + (c["depth"] - 1) * (draft_layer(rows_d) + 2 * rows_d * d * V))
+        return target, draft
+
+    def attn_bytes_per_launch(self, L):
+        """Algorithmic HBM bytes of one verify-attention launch (one layer, whole batch)."""
+        c = self.cfg
+        B, N, Hq, Hkv, D = c["B"], c["N"], c["Hq"], c["Hkv"], c["D"]
+        kv_prefix = 2 * B * Hkv * L * D * 2
+        tree_kv = 2 * B * N * Hkv * D * 2
+        rot_write = B * N * Hkv * D * 2
+        q_o = 2 * B * N * Hq * D * 2
+        return kv_prefix + tree_kv + rot_write + q_o
+
+
+def run_gpu(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    cfg = dict(CFG)
+    cfg["B"] = args.batch
+    eng = Engine(cfg, args.steps * 2 + args.warmup + 2, dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        eng.step()
+    eng.reset_counters()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall0 = time.time()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    acc_before = int(eng.steps_done)
+    t0.record()
+    accepted = torch.zeros((), dtype=torch.int64, device=dev)
+    for _ in range(args.steps):
+        eng.step()
+        accepted += (eng.accept_len.to(torch.int64) + 1).sum()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    wall1 = time.time()
+    clocks.stop()
+    clk = clocks.summary(wall0, wall1)
+    eng.collect()
+    if world > 1:
+        dist.barrier()
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    status = int(eng.dev_status.item())
+
+    # ---- e2e through host buffers: per step H2D of the step's inputs, D2H of its result
+    c = cfg
+    host_aux = eng.aux_in.cpu().pin_memory()
+    host_tok = eng.next_tok.cpu().pin_memory()
+    host_tc = eng.tc.cpu().pin_memory()
+    out_tok = torch.empty_like(eng.next_tok, device="cpu").pin_memory()
+    out_len = torch.empty_like(eng.accept_len, device="cpu").pin_memory()
+    eng.timing = False
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        eng.aux_in.copy_(host_aux, non_blocking=True)
+        eng.next_tok.copy_(host_tok, non_blocking=True)
+        eng.tc.copy_(host_tc, non_blocking=True)
+        eng.step()
+        out_tok.copy_(eng.next_tok, non_blocking=True)
+        out_len.copy_(eng.accept_len, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = host_aux.numel() * 2 + host_tok.numel() * 4 + host_tc.numel() * 4
+    d2h = out_tok.numel() * 4 + out_len.numel() * 4
+
+    units = cfg["B"] * cfg["N"] * args.steps * world
+    value = units / (ms / 1e3)
+    hbm, tf_burst, tf_sust, src = peaks()
+    tgt_f, drf_f = eng.flops_per_step()
+    gemm_ms = eng.kernel_ms["gemm"] / max(1, args.steps)
+    gemm_calls = eng.kernel_calls["gemm"] / max(1, args.steps)
+    gemm_tflops = (tgt_f + drf_f) / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    attn_ms = eng.kernel_ms["verify_attn"] / max(1, eng.kernel_calls["verify_attn"])
+    L_mid = cfg["L0"] + cfg["W"] * (args.warmup + args.steps // 2)
+    attn_gbs = eng.attn_bytes_per_launch(L_mid) / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
+    tau = float(accepted.item()) / (cfg["B"] * args.steps) - 1.0
+    launches_per_step = gemm_calls + cfg["layers"] * 2 + 3 * cfg["layers"] + 4 + _draft_launches(cfg)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (random-init weights N(0,0.02), N(0,1) caches, uniform tokens)",
+        "config": {"workload": "EAGLE-3 draft-and-verify step, Llama-3.1-8B-shaped target + EAGLE-3 head, "
+                               "B=64, N=60 (depth 6, top-k 10), prefix 2048, T=1, compaction on",
+                   "global_batch": cfg["B"] * world, "seq_len": cfg["L0"], "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (16 GB of weights streamed per step)"},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1) if gemm_tflops else None,
+                     "peak": tf_sust, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / tf_sust, 4) if gemm_tflops else None, "traffic": None,
+                     "kernel": "gemm_tc_kernel (all tcgen05 projections of the step)",
+                     "peak_source": f"{src} bf16_tflops_sustained"},
+        "verify_attn": {"achieved_gbs": round(attn_gbs, 1) if attn_gbs else None, "peak_gbs": hbm,
+                        "frac": round(attn_gbs / hbm, 4) if attn_gbs else None,
+                        "frac_of_8tbs": round(attn_gbs / 8000.0, 4) if attn_gbs else None,
+                        "ms_per_launch": round(attn_ms, 4), "prefix_len": L_mid},
+        "accepted_tokens_per_s": round(float(accepted.item()) * world / (ms / 1e3), 2),
+        "tau": round(tau, 4),
+        "e2e": {"value": round(units / (e2e_ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clk,
+        "dev_status": status,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _draft_launches(cfg):
+    # catch-up: meta, fc, prologue, qkv, attn, O, norm, swiglu, down, append, norm, lm, topk, select
+    # per depth 2..D: prologue, qkv, attn, O, norm, swiglu, down, norm, lm, topk, select; final select;
+    # split-K GEMMs add a reduce launch (counted in the GEMM events above as part of the call)
+    return 14 + (cfg["depth"] - 1) * 11 + 1
+
+
+# ----------------------------------------------------------------------------------------- oracle arm
+def oracle_sample_seconds(cfg, rng_seed=0):
+    """Time the oracle (as it stands) on a bounded sample of the step for ONE sequence and
+    extrapolate to the full step of that sequence:
+      t_attn  one layer of verify attention (60 nodes, 32 heads, 2048 prefix)
+      t_proj  one target layer's projections for the 60 rows (row by row, fp64)
+      t_lm    the LM head for 6 of the 60 rows over 1/8 of the vocabulary (scaled x80)
+      t_acc   TOPK acceptance over the 60-node tree (V = 128256)
+    step(seq) ~= 32 (t_attn + t_proj) + t_lm + t_acc + draft, with the draft estimated as
+    51/60 of one layer's projections plus its own attention and 51/60 of the LM head."""
+    import numpy as np
+
+    import synth
+    from oracle import accept as oacc
+    from oracle import attention as oatt
+    from oracle.llama import _rows, rmsnorm, silu
+    c = cfg
+    d, F, V, Hq, Hkv, D, N = c["d"], c["F"], c["V"], c["Hq"], c["Hkv"], c["D"], c["N"]
+    r = synth.rng(rng_seed, 5)
+    t = {}
+    inp = synth.verify_attn_batch(rng_seed, 1, N, Hq, Hkv, D, [c["L0"]], S_max=c["L0"] + N)
+    t0 = time.perf_counter()
+    oatt.verify_attention(inp["q_f32"], inp["tree_k_f32"], inp["tree_v_f32"], inp["k_cache_f32"],
+                          inp["v_cache_f32"], inp["parents"], inp["prefix_len"])
+    t["attn"] = time.perf_counter() - t0
+    x = r.standard_normal((N, d)).astype(np.float32)
+    wq = (0.02 * r.standard_normal(((Hq + 2 * Hkv) * D, d))).astype(np.float32)
+    wo = (0.02 * r.standard_normal((d, Hq * D))).astype(np.float32)
+    wg = (0.02 * r.standard_normal((F, d))).astype(np.float32)
+    wu = (0.02 * r.standard_normal((F, d))).astype(np.float32)
+    wd = (0.02 * r.standard_normal((d, F))).astype(np.float32)
+    t0 = time.perf_counter()
+    h = rmsnorm(x, np.ones(d), 1e-5)
+    _rows(wq, h)
+    y = x + _rows(wo, h[:, : Hq * D])
+    h2 = rmsnorm(y, np.ones(d), 1e-5)
+    _rows(wd, silu(_rows(wg, h2)) * _rows(wu, h2))
+    t["proj"] = time.perf_counter() - t0
+    del wq, wo, wg, wu, wd
+    lm = (0.02 * r.standard_normal((V // 8, d))).astype(np.float32)     # 1/8 of the vocabulary
+    t0 = time.perf_counter()
+    _rows(lm, h[:6])
+    t["lm"] = (time.perf_counter() - t0) * (N / 6) * 8
+    del lm
+    zt, zd, parents = synth.accept_row(1, 0, N, V)
+    tokens = synth.tokens_top_draft(zd, parents)
+    t0 = time.perf_counter()
+    oacc.accept_topk(tokens, parents, zt, 1.0, 2, 0, 0)
+    t["acc"] = time.perf_counter() - t0
+    rows_d = 1 + (c["depth"] - 1) * c["top_k"]
+    draft = (rows_d / N) * (t["proj"] + t["lm"] + t["attn"])
+    step = c["layers"] * (t["attn"] + t["proj"]) + t["lm"] + t["acc"] + draft
+    return step, t
+
+
+def cpu_baseline(cfg):
+    step, parts = oracle_sample_seconds(cfg)
+    threads = torch.get_num_threads()
+    try:
+        import numpy as np  # noqa: F401
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        pass
+    value = cfg["N"] / step          # verified tree tokens per second for one sequence on the host
+    return {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": ("one sequence: one layer of verify attention (60 nodes, 2048 prefix), one target "
+                       "layer's projections and 6 LM-head rows (1/8 of the vocabulary) in fp64, TOPK acceptance at V=128256; "
+                       "extrapolated to 32 layers + LM head + draft head; seconds per part: "
+                       + ", ".join(f"{k}={v:.2f}" for k, v in parts.items()))}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = dict(CFG)
+    for _ in range(args.warmup):
+        pass   # the oracle has no warm state; warm-up steps are not run
+    total = 0.0
+    per = []
+    for i in range(args.steps):
+        step, _ = oracle_sample_seconds(cfg, rng_seed=i)
+        per.append(step)
+        total += step * cfg["B"]        # the batch runs one sequence after another on the host
+    ms = total / args.steps * 1e3
+    value = cfg["B"] * cfg["N"] * args.steps / total
+    cb = cpu_baseline(cfg)
+    cb["value"] = round(value, 6)
+    line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "EAGLE-3 draft-and-verify step, Llama-3.1-8B-shaped target + EAGLE-3 head, "
+                                   "B=64, N=60 (depth 6, top-k 10), prefix 2048, T=1, compaction on",
+                       "global_batch": cfg["B"], "seq_len": cfg["L0"], "parallelism": "host cores"},
+            "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -52,16 +52,16 @@ class AcceptArgs(ctypes.Structure):
 class CompactArgs(ctypes.Structure):
     _fields_ = [("n_layers", _i32), ("batch", _i32), ("n_nodes", _i32), ("n_kv_heads", _i32),
                 ("head_dim", _i32), ("elem_bytes", _i32), ("s_max", _i32), ("max_path", _i32),
-                ("cache_layer_stride", _i64), ("tree_layer_stride", _i64),
+                ("cache_layer_stride", _i64), ("tree_layer_stride", _i64), ("tree_node_stride", _i64),
                 ("k_cache", _p), ("v_cache", _p), ("tree_k", _p), ("tree_v", _p),
-                ("path", _p), ("accept_len", _p), ("prefix_len", _p), ("slot_map", _p),
+                ("path", _p), ("accept_len", _p), ("prefix_len", _p), ("slot_map", _p), ("committed", _p),
                 ("aux_dim", _i32), ("aux_tree", _p), ("aux_out", _p), ("dev_status", _p)]
 
 
 class VerifyAttnArgs(ctypes.Structure):
     _fields_ = [("batch", _i32), ("n_nodes", _i32), ("n_heads", _i32), ("n_kv_heads", _i32),
                 ("head_dim", _i32), ("s_max", _i32), ("max_prefix_len", _i32), ("num_splits", _i32),
-                ("rope_theta", _f32), ("sm_scale", _f32),
+                ("q_node_stride", _i64), ("kv_node_stride", _i64), ("rope_theta", _f32), ("sm_scale", _f32),
                 ("q", _p), ("tree_k", _p), ("tree_v", _p), ("k_cache", _p), ("v_cache", _p),
                 ("parents", _p), ("prefix_len", _p), ("out", _p), ("lse", _p), ("dev_status", _p)]
 
@@ -73,6 +73,28 @@ class LinearArgs(ctypes.Structure):
 
 
 EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU = 0, 1, 2, 3
+
+DRAFT_WEIGHT_NAMES = ("w_fc", "embed", "input_norm", "hidden_norm", "w_qkv", "w_o", "post_norm", "w_gate",
+                      "w_up", "w_down", "final_norm", "lm_head")
+
+
+class DraftWeights(ctypes.Structure):
+    _fields_ = [(n, _p) for n in DRAFT_WEIGHT_NAMES]
+
+
+class DraftTreeArgs(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("hidden", _i32), ("n_heads", _i32), ("n_kv_heads", _i32), ("head_dim", _i32),
+                ("ffn", _i32), ("vocab", _i32), ("depth", _i32), ("top_k", _i32), ("n_nodes", _i32),
+                ("tc_max", _i32), ("s_max", _i32), ("max_draft_len", _i32), ("rope_theta", _f32), ("rms_eps", _f32),
+                ("aux", _p), ("next_tokens", _p), ("tc", _p), ("draft_k_cache", _p), ("draft_v_cache", _p),
+                ("draft_len", _p), ("tokens", _p), ("parents", _p), ("depth_out", _p), ("anc_mask", _p),
+                ("score", _p), ("dbg_logits", _p), ("dev_status", _p)]
+
+
+class RmsnormArgs(ctypes.Structure):
+    _fields_ = [("rows", _i32), ("dim", _i32), ("n_src", _i32), ("eps", _f32), ("ld_in", _i64), ("ld_out", _i64),
+                ("ld_tap", _i64), ("input", _p), ("w", _p), ("gather", _p), ("out", _p), ("tap_out", _p),
+                ("dev_status", _p)]
 
 
 def _declare(L):
@@ -94,6 +116,12 @@ def _declare(L):
     L.eagle3_linear_workspace_size.argtypes = [P(LinearArgs)]
     L.eagle3_linear.restype = ctypes.c_int
     L.eagle3_linear.argtypes = [P(LinearArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_draft_tree_workspace_size.restype = ctypes.c_size_t
+    L.eagle3_draft_tree_workspace_size.argtypes = [P(DraftTreeArgs)]
+    L.eagle3_draft_tree.restype = ctypes.c_int
+    L.eagle3_draft_tree.argtypes = [P(DraftWeights), P(DraftTreeArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_rmsnorm.restype = ctypes.c_int
+    L.eagle3_rmsnorm.argtypes = [P(RmsnormArgs), _p]
 
 
 def status_string(status):
@@ -164,31 +192,56 @@ def eagle3_accept(mode, target_logits, tokens, parents, accept_len, path, emitte
 
 
 def eagle3_compact_kv(k_cache, v_cache, tree_k, tree_v, path, accept_len, prefix_len, slot_map, *,
-                      aux_tree=None, aux_out=None, dev_status=None, stream=None):
-    """k_cache / v_cache [layers, B, Hkv, S_max, D]; tree_k / tree_v [layers, B, N, Hkv, D]
-    (bf16 or fp32, same dtype); path / slot_map [B, W]; accept_len, prefix_len [B] int32."""
+                      aux_tree=None, aux_out=None, committed=None, tree_node_stride=0, tree_layer_stride=0,
+                      dev_status=None, stream=None):
+    """k_cache / v_cache [layers, B, Hkv, S_max, D] (bf16 or fp32); tree_k / tree_v: [layers, B, N, Hkv, D]
+    tensors, or flat views into fused QKV buffers described by tree_node_stride / tree_layer_stride
+    (elements; then pass tree_k / tree_v as 1-D tensors starting at the first key / value element);
+    path / slot_map [B, W]; accept_len, prefix_len [B] int32; aux_tree [B, N, A], aux_out [B, W, A]."""
     layers, B, Hkv, S, D = k_cache.shape
-    N = tree_k.shape[2]
+    if tree_k.dim() == 5:
+        N = tree_k.shape[2]
+        if tuple(tree_k.shape) != (layers, B, N, Hkv, D) or tree_v.shape != tree_k.shape:
+            raise ValueError("cache / tree shapes do not match")
+        tls, tns = B * N * Hkv * D, Hkv * D
+    else:
+        if not (tree_node_stride and tree_layer_stride):
+            raise ValueError("flat tree_k / tree_v need tree_node_stride and tree_layer_stride")
+        tls, tns = int(tree_layer_stride), int(tree_node_stride)
+        N = (tls // tns) // B
     if tree_k.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype or tree_v.dtype != k_cache.dtype:
         raise TypeError("caches and tree K/V must share one dtype")
-    if tuple(tree_k.shape) != (layers, B, N, Hkv, D) or tree_v.shape != tree_k.shape or v_cache.shape != k_cache.shape:
-        raise ValueError("cache / tree shapes do not match")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
     A = 0 if aux_tree is None else aux_tree.shape[-1]
     a = CompactArgs(n_layers=layers, batch=B, n_nodes=N, n_kv_heads=Hkv, head_dim=D,
                     elem_bytes=k_cache.element_size(), s_max=S, max_path=path.shape[1],
-                    cache_layer_stride=B * Hkv * S * D, tree_layer_stride=B * N * Hkv * D,
+                    cache_layer_stride=B * Hkv * S * D, tree_layer_stride=tls, tree_node_stride=tns,
                     k_cache=_ptr(k_cache, None, "k_cache"), v_cache=_ptr(v_cache, None, "v_cache"),
-                    tree_k=_ptr(tree_k, None, "tree_k"), tree_v=_ptr(tree_v, None, "tree_v"),
+                    tree_k=tree_k.data_ptr(), tree_v=tree_v.data_ptr(),
                     path=_ptr(path, torch.int32, "path"), accept_len=_ptr(accept_len, torch.int32, "accept_len"),
                     prefix_len=_ptr(prefix_len, torch.int32, "prefix_len"),
-                    slot_map=_ptr(slot_map, torch.int32, "slot_map"), aux_dim=A,
+                    slot_map=_ptr(slot_map, torch.int32, "slot_map"),
+                    committed=_ptr(committed, torch.int32, "committed"), aux_dim=A,
                     aux_tree=_ptr(aux_tree, None, "aux_tree"), aux_out=_ptr(aux_out, None, "aux_out"),
                     dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+    for t in (tree_k, tree_v):
+        if not t.is_cuda:
+            raise ValueError("tree_k / tree_v must be CUDA tensors")
     _check(lib().eagle3_compact_kv(ctypes.byref(a), _stream(stream)), "eagle3_compact_kv")
+
+
+def _view_ptr(t, dtype, name):
+    """Data pointer of a (possibly strided) view whose innermost dimension is contiguous."""
+    if not t.is_cuda or t.dtype != dtype or t.stride(-1) != 1:
+        raise ValueError(f"{name} must be a {dtype} CUDA tensor with a contiguous last dimension")
+    return t.data_ptr()
 
 
 def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
                      lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None):
+    """q [B, N, Hq, D] and tree_k / tree_v [B, N, Hkv, D] may be node-strided views (e.g. slices of a
+    fused [B, N, (Hq + 2 Hkv) * D] projection output); everything else is dense."""
     B, N, Hq, D = q.shape
     Hkv = tree_k.shape[2]
     S = k_cache.shape[2]
@@ -198,10 +251,18 @@ def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, o
         if tuple(t.shape) != shape:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
     bf = torch.bfloat16
+    qs = q.stride()
+    ks = tree_k.stride()
+    if qs[3] != 1 or qs[2] != D or qs[0] != N * qs[1]:
+        raise ValueError("q must be node-strided with dense heads")
+    if ks[3] != 1 or ks[2] != D or ks[0] != N * ks[1] or tree_v.stride() != tree_k.stride():
+        raise ValueError("tree_k / tree_v must share one node stride with dense heads")
     return VerifyAttnArgs(batch=B, n_nodes=N, n_heads=Hq, n_kv_heads=Hkv, head_dim=D, s_max=S,
                           max_prefix_len=int(max_prefix_len), num_splits=int(num_splits),
+                          q_node_stride=qs[1], kv_node_stride=ks[1],
                           rope_theta=float(rope_theta), sm_scale=float(sm_scale),
-                          q=_ptr(q, bf, "q"), tree_k=_ptr(tree_k, bf, "tree_k"), tree_v=_ptr(tree_v, bf, "tree_v"),
+                          q=_view_ptr(q, bf, "q"), tree_k=_view_ptr(tree_k, bf, "tree_k"),
+                          tree_v=_view_ptr(tree_v, bf, "tree_v"),
                           k_cache=_ptr(k_cache, bf, "k_cache"), v_cache=_ptr(v_cache, bf, "v_cache"),
                           parents=_ptr(parents, torch.int32, "parents"),
                           prefix_len=_ptr(prefix_len, torch.int32, "prefix_len"),
@@ -251,3 +312,68 @@ def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, split
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.eagle3_linear(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_linear")
+
+
+def draft_tree_args(aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out, anc_mask, score, *,
+                    n_heads, ffn, vocab, depth, top_k, max_draft_len, rope_theta=500000.0, rms_eps=1e-5,
+                    dbg_logits=None, dev_status=None):
+    B, tc_max, d3 = aux.shape
+    Hkv, S, D = k_cache.shape[1:]
+    N = tokens.shape[1]
+    bf, i32 = torch.bfloat16, torch.int32
+    return DraftTreeArgs(batch=B, hidden=d3 // 3, n_heads=n_heads, n_kv_heads=Hkv, head_dim=D, ffn=ffn, vocab=vocab,
+                         depth=depth, top_k=top_k, n_nodes=N, tc_max=tc_max, s_max=S, max_draft_len=int(max_draft_len),
+                         rope_theta=float(rope_theta), rms_eps=float(rms_eps),
+                         aux=_ptr(aux, bf, "aux"), next_tokens=_ptr(next_tokens, i32, "next_tokens"),
+                         tc=_ptr(tc, i32, "tc"), draft_k_cache=_ptr(k_cache, bf, "k_cache"),
+                         draft_v_cache=_ptr(v_cache, bf, "v_cache"), draft_len=_ptr(draft_len, i32, "draft_len"),
+                         tokens=_ptr(tokens, i32, "tokens"), parents=_ptr(parents, i32, "parents"),
+                         depth_out=_ptr(depth_out, i32, "depth_out"), anc_mask=_ptr(anc_mask, torch.int64, "anc_mask"),
+                         score=_ptr(score, torch.float32, "score"),
+                         dbg_logits=_ptr(dbg_logits, torch.float32, "dbg_logits"),
+                         dev_status=_ptr(dev_status, i32, "dev_status"))
+
+
+def draft_weights(w):
+    """DraftWeights from a dict of contiguous bf16 CUDA tensors named as in DRAFT_WEIGHT_NAMES."""
+    return DraftWeights(**{n: _ptr(w[n], torch.bfloat16, n) for n in DRAFT_WEIGHT_NAMES})
+
+
+def eagle3_draft_tree_workspace_size(args):
+    return lib().eagle3_draft_tree_workspace_size(ctypes.byref(args))
+
+
+def eagle3_draft_tree(weights, aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out,
+                      anc_mask, score, *, n_heads, ffn, vocab, depth, top_k, max_draft_len, rope_theta=500000.0,
+                      rms_eps=1e-5, dbg_logits=None, dev_status=None, workspace=None, stream=None):
+    """Draft head + dynamic tree.  weights: dict of bf16 tensors (see DRAFT_WEIGHT_NAMES);
+    aux [B, tc_max, 3d] bf16; next_tokens [B, tc_max] / tc [B] / draft_len [B] int32; caches
+    [B, Hkv, S, D] bf16; outputs [B, N] (anc_mask int64 bit patterns of the uint64 masks)."""
+    a = draft_tree_args(aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out, anc_mask, score,
+                        n_heads=n_heads, ffn=ffn, vocab=vocab, depth=depth, top_k=top_k, max_draft_len=max_draft_len,
+                        rope_theta=rope_theta, rms_eps=rms_eps, dbg_logits=dbg_logits, dev_status=dev_status)
+    wts = draft_weights(weights)
+    L = lib()
+    need = L.eagle3_draft_tree_workspace_size(ctypes.byref(a))
+    if workspace is None:
+        workspace = _workspace(need, aux.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.eagle3_draft_tree(ctypes.byref(wts), ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)),
+           "eagle3_draft_tree")
+
+
+def eagle3_rmsnorm(x, w, out, *, eps=1e-5, gather=None, tap_out=None, dev_status=None, stream=None):
+    """out[r] = w * rmsnorm(x[gather[r] if gather else r]); tap_out[r] = that input row (optional)."""
+    rows = out.shape[0]
+    dim = w.shape[0]
+    bf = torch.bfloat16
+    a = RmsnormArgs(rows=rows, dim=dim, n_src=x.shape[0], eps=float(eps), ld_in=x.stride(0), ld_out=out.stride(0),
+                    ld_tap=0 if tap_out is None else tap_out.stride(0), input=x.data_ptr(), w=_ptr(w, bf, "w"),
+                    gather=_ptr(gather, torch.int32, "gather"), out=out.data_ptr(),
+                    tap_out=None if tap_out is None else tap_out.data_ptr(),
+                    dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+    for name, t in (("x", x), ("out", out), ("tap_out", tap_out)):
+        if t is not None and (not t.is_cuda or t.dtype != bf or t.stride(-1) != 1):
+            raise ValueError(f"{name} must be a bf16 CUDA tensor with unit inner stride")
+    _check(lib().eagle3_rmsnorm(ctypes.byref(a), _stream(stream)), "eagle3_rmsnorm")

@@ -18,11 +18,11 @@ constexpr int NT = 128;
 
 struct Params {
     int L_layers, B, N, Hkv, D, E, S, W, A;
-    int64_t cache_ls, tree_ls;
+    int64_t cache_ls, tree_ls, tree_ns;
     uint8_t *k_cache, *v_cache;
     const uint8_t *tree_k, *tree_v;
     const int32_t *path, *accept_len;
-    int32_t *prefix_len, *slot_map, *dev_status;
+    int32_t *prefix_len, *slot_map, *committed, *dev_status;
     const uint8_t *aux_tree;
     uint8_t *aux_out;
 };
@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(NT) compact_copy_kernel(const Params p) {
         return;
     }
     const size_t drow = (size_t)p.D * p.E;   // one head's row in bytes
-    const uint8_t *tsrc = (kv ? p.tree_v : p.tree_k) + (size_t)layer * p.tree_ls * p.E +
-                          ((size_t)b * p.N + src) * p.Hkv * drow;
+    const uint8_t *tsrc = (kv ? p.tree_v : p.tree_k) + ((size_t)layer * p.tree_ls +
+                          ((size_t)b * p.N + src) * (size_t)p.tree_ns) * p.E;
     uint8_t *cdst = (kv ? p.v_cache : p.k_cache) + (size_t)layer * p.cache_ls * p.E;
     for (int h = 0; h < p.Hkv; ++h) {
         uint8_t *d = cdst + (((size_t)b * p.Hkv + h) * p.S + (size_t)(L + j)) * drow;
@@ -93,6 +93,7 @@ __global__ void compact_finish_kernel(const Params p) {
     }
     for (int j = 0; j < p.W; ++j) p.slot_map[(size_t)b * p.W + j] = (ok && j <= n) ? L + j : -1;
     if (ok) p.prefix_len[b] = L + n + 1;
+    if (p.committed) p.committed[b] = ok ? n + 1 : 0;
 }
 
 }  // namespace
@@ -113,7 +114,10 @@ extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eag
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->aux_dim > 0 && (!a->aux_tree || !a->aux_out)) return EAGLE3_ERR_INVALID_ARGUMENT;
     const int64_t dense_cache = (int64_t)a->batch * a->n_kv_heads * a->s_max * a->head_dim;
-    const int64_t dense_tree = (int64_t)a->batch * a->n_nodes * a->n_kv_heads * a->head_dim;
+    if (a->tree_node_stride < 0 || (a->tree_node_stride && a->tree_node_stride < (int64_t)a->n_kv_heads * a->head_dim))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    const int64_t tree_ns = a->tree_node_stride ? a->tree_node_stride : (int64_t)a->n_kv_heads * a->head_dim;
+    const int64_t dense_tree = (int64_t)a->batch * a->n_nodes * tree_ns;
     if (a->n_layers > 1 && (a->cache_layer_stride < dense_cache || a->tree_layer_stride < dense_tree))
         return EAGLE3_ERR_INVALID_ARGUMENT;
 
@@ -129,6 +133,7 @@ extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eag
     p.A = a->aux_dim;
     p.cache_ls = a->n_layers > 1 ? a->cache_layer_stride : dense_cache;
     p.tree_ls = a->n_layers > 1 ? a->tree_layer_stride : dense_tree;
+    p.tree_ns = tree_ns;
     p.k_cache = (uint8_t *)a->k_cache;
     p.v_cache = (uint8_t *)a->v_cache;
     p.tree_k = (const uint8_t *)a->tree_k;
@@ -137,6 +142,7 @@ extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eag
     p.accept_len = a->accept_len;
     p.prefix_len = a->prefix_len;
     p.slot_map = a->slot_map;
+    p.committed = a->committed;
     p.dev_status = a->dev_status;
     p.aux_tree = (const uint8_t *)a->aux_tree;
     p.aux_out = (uint8_t *)a->aux_out;

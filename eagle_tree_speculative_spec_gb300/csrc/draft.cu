@@ -1,0 +1,865 @@
+// eagle3_draft_tree: the EAGLE-3 draft head and its dynamic top-k tree; eagle3_rmsnorm.
+//
+// Sources: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", sections VIII
+// (two-stream draft decoder layer, frozen embedding, final norm + LM head, pre-norm recurrent
+// state), IX (fc over the concatenated aux states), XI (catch-up, drafting positions, cache
+// rollback), IV.3 / XI.6 (EAGLE-2 dynamic tree: expand by draft confidence, prune at the end) and
+// appendix C (RMSNorm, RoPE); "EAGLE-3: Training-Time Test for Speculative Decoding", "Dynamic
+// Draft Trees Spend Verification Where It Can Pay Off"; "Advanced speculative decoding: tree
+// drafts and EAGLE" (top-k children per node, node 0 is the root).
+//
+// Data flow of one call (rows of a draft step are ordered rank-major, row = r * B + b, so the rows
+// of one depth are one contiguous block and each projection is a single tensor-core GEMM):
+//   catch-up   fc GEMM -> prologue (two RMSNorms, concat) -> QKV GEMM -> tree attention (chain
+//              over the draft cache) -> O GEMM (+x) -> RMSNorm -> SwiGLU GEMM -> down GEMM (+x1)
+//              -> append rotated K/V to the draft cache -> final RMSNorm of the root row -> LM
+//              head (fp32 logits) -> row top-k + fixed-point log-normaliser -> candidates
+//   depth 2..D the same layer for the top_k frontier rows of the previous depth, attending to the
+//              draft cache plus their ancestors' rows in a K/V pool; selection of the next frontier
+//   final      rerank of all candidates, emission of tokens / parents / depth / masks / scores
+// Every selection decision compares fp32 scores built with the same RN operations as the CPU
+// oracle, so for the same logits the tree is bit-identical.
+#include <algorithm>
+
+#include "../../include/eagle3_linear.h"
+#include "attn.cuh"
+
+namespace e3 {
+namespace {
+
+constexpr int KMAX = 16;
+constexpr int HD = 128;
+constexpr int MAX_SLOTS = 64;
+
+// ------------------------------------------------------------------------------------------------
+// RMSNorm helpers: one CTA of 128 threads per row.
+// ------------------------------------------------------------------------------------------------
+constexpr int NT_NORM = 128;
+
+E3_DEV float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
+    return t;
+}
+
+// out = w * x * rsqrt(mean(x^2) + eps), fp32 statistics, bf16 out
+E3_DEV void norm_row(const __nv_bfloat16 *x, const __nv_bfloat16 *w, __nv_bfloat16 *out, int dim, float eps,
+                     __nv_bfloat16 *tap, float *red) {
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+        const float v = __bfloat162float(x[i]);
+        ss += v * v;
+    }
+    const float r = rsqrtf(block_sum(ss, red) / (float)dim + eps);
+    for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+        const __nv_bfloat16 xv = x[i];
+        out[i] = __float2bfloat16_rn(__bfloat162float(w[i]) * (__bfloat162float(xv) * r));
+        if (tap) tap[i] = xv;
+    }
+}
+
+struct NormParams {
+    int rows, dim, n_src;
+    float eps;
+    int64_t ld_in, ld_out, ld_tap;
+    const __nv_bfloat16 *in, *w;
+    const int32_t *gather;
+    __nv_bfloat16 *out, *tap;
+    int32_t *dev_status;
+};
+
+__global__ void __launch_bounds__(NT_NORM) rmsnorm_kernel(const NormParams p) {
+    __shared__ float red[NT_NORM / 32];
+    const int r = blockIdx.x;
+    int src = p.gather ? p.gather[r] : r;
+    if (src < 0 || src >= p.n_src) {
+        if (threadIdx.x == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TOKEN);
+        src = 0;
+    }
+    norm_row(p.in + (size_t)src * p.ld_in, p.w, p.out + (size_t)r * p.ld_out, p.dim, p.eps,
+             p.tap ? p.tap + (size_t)r * p.ld_tap : nullptr, red);
+}
+
+// Draft prologue: a2k[r] = [input_norm(embed[tok[r]]) ; hidden_norm(x[r])], optionally x copied
+// to xres[r].  Catch-up rows past tc[b] use token 0 (their outputs are never read).
+struct PrologueParams {
+    int rows, d, vocab, tc_max;
+    float eps;
+    const __nv_bfloat16 *embed, *w_in, *w_hid;
+    const int32_t *tokens;         // [rows]
+    const int32_t *tc;             // catch-up validity (rows = b * tc_max + i) or null
+    const __nv_bfloat16 *x;        // x rows base
+    const int32_t *x_row;          // [rows] absolute row of x, or null (row r)
+    __nv_bfloat16 *a2k, *xres;
+    int32_t *dev_status;
+};
+
+__global__ void __launch_bounds__(NT_NORM) draft_prologue_kernel(const PrologueParams p) {
+    __shared__ float red[NT_NORM / 32];
+    const int r = blockIdx.x;
+    int tok = p.tokens[r];
+    bool valid = true;
+    if (p.tc) valid = (r % p.tc_max) < p.tc[r / p.tc_max];
+    if (!valid) tok = 0;
+    if (tok < 0 || tok >= p.vocab) {
+        if (threadIdx.x == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TOKEN);
+        tok = 0;
+    }
+    const __nv_bfloat16 *x = p.x + (size_t)(p.x_row ? p.x_row[r] : r) * p.d;
+    __nv_bfloat16 *o = p.a2k + (size_t)r * 2 * p.d;
+    norm_row(p.embed + (size_t)tok * p.d, p.w_in, o, p.d, p.eps, nullptr, red);
+    norm_row(x, p.w_hid, o + p.d, p.d, p.eps, p.xres ? p.xres + (size_t)r * p.d : nullptr, red);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Row top-k (k <= 16) by (logit desc, token asc) and the fixed-point log-normaliser at T = 1.
+// ------------------------------------------------------------------------------------------------
+constexpr int NT_TOPK = 256;
+
+E3_DEV uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const uint64_t t = __shfl_xor_sync(0xffffffffu, v, o);
+        v = t > v ? t : v;
+    }
+    return v;
+}
+
+// merge the 32 sorted lists held by the lanes into the top-k of their union (all lanes get it)
+E3_DEV void warp_merge(uint64_t (&best)[KMAX], uint64_t (&res)[KMAX], int k) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        const uint64_t m = warp_max_u64(best[0]);
+        res[j] = j < k ? m : 0ull;
+        if (best[0] == m && m != 0ull) {   // packed values are unique: exactly one lane pops
+#pragma unroll
+            for (int q = 0; q < KMAX - 1; ++q) best[q] = best[q + 1];
+            best[KMAX - 1] = 0ull;
+        }
+    }
+}
+
+E3_DEV void insert_best(uint64_t (&best)[KMAX], uint64_t v) {
+    if (v <= best[KMAX - 1]) return;
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) {
+        if (v > best[q]) {
+            const uint64_t t = best[q];
+            best[q] = v;
+            v = t;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int64_t ld, int V, int k,
+                                                       int32_t *out_tok, float *out_lq) {
+    __shared__ uint64_t wres[NT_TOPK / 32][KMAX];
+    __shared__ uint64_t fin[KMAX];
+    __shared__ uint64_t sred[NT_TOPK / 32];
+    const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *z = logits + (size_t)row * ld;
+    uint64_t best[KMAX];
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) best[q] = 0ull;
+    const bool vec = ((((uintptr_t)z) & 15) == 0);
+    const int n4 = vec ? V / 4 : 0;
+    for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
+        insert_best(best, pack_argmax(v.x, 4 * j));
+        insert_best(best, pack_argmax(v.y, 4 * j + 1));
+        insert_best(best, pack_argmax(v.z, 4 * j + 2));
+        insert_best(best, pack_argmax(v.w, 4 * j + 3));
+    }
+    for (int i = 4 * n4 + threadIdx.x; i < V; i += NT_TOPK) insert_best(best, pack_argmax(__ldg(z + i), i));
+    uint64_t res[KMAX];
+    warp_merge(best, res, k);
+    if (lane == 0)
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) wres[warp][q] = res[q];
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT_TOPK / 32 ? wres[lane][q] : 0ull;
+        warp_merge(best, res, k);
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) fin[q] = res[q];
+    }
+    __syncthreads();
+    // fixed-point normaliser over the whole row with m = the row maximum
+    const float m = key_to_float((uint32_t)(fin[0] >> 32));
+    uint64_t s = 0;
+    for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
+        // each weight is up to 2^31: widen before adding
+        s += (uint64_t)dsm_weight(dsm_scaled(v.x, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.y, m, 1.0f)) +
+             (uint64_t)dsm_weight(dsm_scaled(v.z, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.w, m, 1.0f));
+    }
+    for (int i = 4 * n4 + threadIdx.x; i < V; i += NT_TOPK) s += dsm_weight(dsm_scaled(__ldg(z + i), m, 1.0f));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) sred[warp] = s;
+    __syncthreads();
+    if (threadIdx.x < k) {
+        uint64_t S = 0;
+        for (int w = 0; w < NT_TOPK / 32; ++w) S += sred[w];
+        const float ln_s = dsm_log31(S);
+        const uint64_t e = fin[threadIdx.x];
+        const float zx = key_to_float((uint32_t)(e >> 32));
+        out_tok[(size_t)row * k + threadIdx.x] = (int32_t)unpack_idx(e);
+        out_lq[(size_t)row * k + threadIdx.x] = __fsub_rn(dsm_scaled(zx, m, 1.0f), ln_s);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Candidate table and selection (one CTA per sequence).
+// ------------------------------------------------------------------------------------------------
+struct Tree {
+    int B, K, depth, n_nodes, maxc, tc_max, rows_c;   // rows_c = B * tc_max (a-buffer rows of catch-up)
+    float *c_score;          // [B, maxc]
+    int32_t *c_tok, *c_par, *c_dc;   // c_dc = depth << 16 | creation
+    int32_t *n_cand;         // [B]
+    int32_t *frontier;       // [B, KMAX] candidate ids in rank order
+    int32_t *row_tok, *row_x;        // [K * B] next depth rows (rank-major)
+    uint64_t *pool_anc;      // [B, MAX_SLOTS]
+    int32_t *pool_pos;       // [B, MAX_SLOTS]
+    const int32_t *root_row; // [B] a-buffer row of the root (last catch-up row)
+    const int32_t *draft_len;
+    const int32_t *topk_tok;
+    const float *topk_lq;
+    const int32_t *next_tokens, *tc;
+    int32_t *out_tok, *out_par, *out_depth;
+    uint64_t *out_anc;
+    float *out_score;
+    int32_t *dev_status;
+};
+
+E3_DEV uint32_t score_key(float s) { return order_key(__fadd_rn(s, 0.0f)); }   // -0 -> +0
+
+// rank of entry i among n by `key` (unique keys, descending): count of larger keys
+template <class KF>
+E3_DEV int rank_desc(int i, int n, KF key) {
+    const uint64_t ki = key(i);
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += key(j) > ki;
+    return r;
+}
+
+// Choose the next frontier among the candidates [c0, c0 + n) (all of depth t) and describe the
+// rows of depth t + 1 (frontier of depth t) for the next iteration.
+E3_DEV void make_frontier(const Tree &T, int b, int t, int c0, int n, int32_t *sfront) {
+    const float *sc = T.c_score + (size_t)b * T.maxc;
+    const int32_t *dc = T.c_dc + (size_t)b * T.maxc;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int r = rank_desc(i, n, [&](int j) {
+            return ((uint64_t)score_key(sc[c0 + j]) << 32) | (uint64_t)(0xFFFFu - (uint32_t)(dc[c0 + j] & 0xFFFF));
+        });
+        if (r < T.K) sfront[r] = c0 + i;
+    }
+    __syncthreads();
+    const int L = T.draft_len[b];
+    for (int r = threadIdx.x; r < T.K && r < n; r += blockDim.x) {
+        const int f = sfront[r];
+        const int slot = (t - 1) * T.K + r;                       // pool slot of this frontier row
+        int pslot = -1;                                          // pool slot of its parent's row
+        int xrow = T.root_row[b];
+        if (t >= 2) {
+            const int prank = (dc[f] & 0xFFFF) / T.K;            // the row that produced it
+            pslot = (t - 2) * T.K + prank;
+            xrow = T.rows_c + pslot * T.B + b;
+        }
+        T.frontier[(size_t)b * KMAX + r] = f;
+        T.row_tok[(size_t)r * T.B + b] = T.c_tok[(size_t)b * T.maxc + f];
+        T.row_x[(size_t)r * T.B + b] = xrow;
+        T.pool_anc[(size_t)b * MAX_SLOTS + slot] =
+            (pslot >= 0 ? T.pool_anc[(size_t)b * MAX_SLOTS + pslot] : 0ull) | (1ull << slot);
+        T.pool_pos[(size_t)b * MAX_SLOTS + slot] = L - 1 + t;
+    }
+}
+
+// Depth-t candidates from the top-k of the rows of depth t (t = 1: the root row of sequence b;
+// t >= 2: frontier rank r of depth t - 1 at row r * B + b), then the next frontier.
+__global__ void select_step_kernel(const Tree T, int t) {
+    __shared__ int32_t sfront[KMAX];
+    const int b = blockIdx.x;
+    const int K = T.K;
+    const int base = t == 1 ? 0 : T.n_cand[b];
+    const int nrows = t == 1 ? 1 : K;
+    const int n = nrows * K;
+    float *sc = T.c_score + (size_t)b * T.maxc;
+    for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
+        const int r = idx / K, c = idx % K;
+        const size_t trow = t == 1 ? (size_t)b : (size_t)r * T.B + b;
+        const float lq = T.topk_lq[trow * K + c];
+        const int id = base + idx;
+        int par = -1;
+        float s = lq;
+        if (t >= 2) {
+            par = T.frontier[(size_t)b * KMAX + r];
+            s = __fadd_rn(sc[par], lq);
+        }
+        sc[id] = s;
+        T.c_tok[(size_t)b * T.maxc + id] = T.topk_tok[trow * K + c];
+        T.c_par[(size_t)b * T.maxc + id] = par;
+        T.c_dc[(size_t)b * T.maxc + id] = (t << 16) | (r * K + c);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) T.n_cand[b] = base + n;
+    if (t < T.depth) make_frontier(T, b, t, base, n, sfront);
+}
+
+// Final rerank: top n_nodes - 1 of all candidates, emitted after the root.
+__global__ void select_final_kernel(const Tree T) {
+    extern __shared__ uint8_t sm_raw[];
+    int32_t *chosen = (int32_t *)sm_raw;                       // [n_nodes - 1] by final rank
+    int32_t *order = chosen + MAX_SLOTS;                       // [n_nodes - 1] node order
+    int16_t *node_of = (int16_t *)(order + MAX_SLOTS);        // [maxc]
+    const int b = blockIdx.x;
+    const int n = T.n_cand[b], keep = min(T.n_nodes - 1, n);
+    const float *sc = T.c_score + (size_t)b * T.maxc;
+    const int32_t *dc = T.c_dc + (size_t)b * T.maxc;
+    auto key1 = [&](int j) {
+        return ((uint64_t)score_key(sc[j]) << 32) | ((uint64_t)(15 - (dc[j] >> 16)) << 16) |
+               (uint64_t)(0xFFFFu - (uint32_t)(dc[j] & 0xFFFF));
+    };
+    for (int j = threadIdx.x; j < T.maxc; j += blockDim.x) node_of[j] = -1;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int r = rank_desc(i, n, key1);
+        if (r < keep) chosen[r] = i;
+    }
+    __syncthreads();
+    auto key2 = [&](int q) {
+        const int j = chosen[q];
+        return ((uint64_t)(15 - (dc[j] >> 16)) << 48) | ((uint64_t)score_key(sc[j]) << 16) |
+               (uint64_t)(0xFFFFu - (uint32_t)(dc[j] & 0xFFFF));
+    };
+    for (int q = threadIdx.x; q < keep; q += blockDim.x) {
+        const int r = rank_desc(q, keep, key2);
+        order[r] = chosen[q];
+        node_of[chosen[q]] = (int16_t)(r + 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const size_t o = (size_t)b * T.n_nodes;
+        const int root = T.next_tokens[(size_t)b * T.tc_max + max(0, T.tc[b] - 1)];
+        T.out_tok[o] = root;
+        T.out_par[o] = -1;
+        T.out_depth[o] = 0;
+        T.out_score[o] = 0.0f;
+        T.out_anc[o] = 1ull;
+        bool bad = false;
+        for (int m = 1; m <= keep; ++m) {
+            const int j = order[m - 1];
+            const int pc = T.c_par[(size_t)b * T.maxc + j];
+            int pn = pc < 0 ? 0 : node_of[pc];
+            if (pn < 0 || pn >= m) {
+                bad = true;
+                pn = 0;
+            }
+            T.out_tok[o + m] = T.c_tok[(size_t)b * T.maxc + j];
+            T.out_par[o + m] = pn;
+            T.out_depth[o + m] = dc[j] >> 16;
+            T.out_score[o + m] = sc[j];
+            T.out_anc[o + m] = T.out_anc[o + pn] | (1ull << m);
+        }
+        for (int m = keep + 1; m < T.n_nodes; ++m) {   // fewer candidates than nodes: pad with the root
+            T.out_tok[o + m] = root;
+            T.out_par[o + m] = 0;
+            T.out_depth[o + m] = 1;
+            T.out_score[o + m] = -INFINITY;
+            T.out_anc[o + m] = 1ull | (1ull << m);
+        }
+        if (bad) flag(T.dev_status, EAGLE3_DEV_BAD_TREE);
+    }
+}
+
+// Catch-up bookkeeping: chain masks / positions of the catch-up rows and the root row index.
+__global__ void catchup_meta_kernel(int B, int tc_max, const int32_t *draft_len, const int32_t *tc,
+                                    uint64_t *cu_anc, int32_t *cu_pos, int32_t *root_row, int32_t *dev_status) {
+    const int b = blockIdx.x;
+    for (int i = threadIdx.x; i < tc_max; i += blockDim.x) {
+        cu_anc[(size_t)b * tc_max + i] = i >= 63 ? ~0ull : ((1ull << (i + 1)) - 1ull);
+        cu_pos[(size_t)b * tc_max + i] = draft_len[b] + i;
+    }
+    if (threadIdx.x == 0) {
+        int t = tc[b];
+        if (t < 1 || t > tc_max) {
+            flag(dev_status, EAGLE3_DEV_CAPACITY);
+            t = max(1, min(t, tc_max));
+        }
+        root_row[b] = b * tc_max + t - 1;
+    }
+}
+
+// Append the catch-up rows' rotated K and V to the draft cache, then advance draft_len.
+__global__ void append_kv_kernel(int B, int tc_max, int Hkv, int S, int qkv_w, int k_off, int v_off,
+                                 const __nv_bfloat16 *qkv, __nv_bfloat16 *kc, __nv_bfloat16 *vc, int32_t *draft_len,
+                                 const int32_t *tc, int max_len, int32_t *dev_status) {
+    const int b = blockIdx.x;
+    const int L = draft_len[b];
+    const int t = max(1, min(tc[b], tc_max));
+    const bool ok = L >= 0 && L + t <= S && L <= max_len;
+    if (ok) {
+        const int chunks = t * Hkv * (HD / 8);
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+            const int i = c / (Hkv * (HD / 8)), g = (c / (HD / 8)) % Hkv, d8 = (c % (HD / 8)) * 8;
+            const __nv_bfloat16 *src = qkv + (size_t)(b * tc_max + i) * qkv_w;
+            const size_t dst = (((size_t)b * Hkv + g) * S + (size_t)(L + i)) * HD + d8;
+            *reinterpret_cast<uint4 *>(kc + dst) = *reinterpret_cast<const uint4 *>(src + k_off + g * HD + d8);
+            *reinterpret_cast<uint4 *>(vc + dst) = *reinterpret_cast<const uint4 *>(src + v_off + g * HD + d8);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (ok) draft_len[b] = L + t;
+        else flag(dev_status, EAGLE3_DEV_CAPACITY);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host orchestration.
+// ------------------------------------------------------------------------------------------------
+struct Layout {
+    size_t off[32];
+    size_t total;
+    int n = 0;
+    size_t add(size_t bytes) {
+        const size_t o = total;
+        total += (bytes + 255) & ~(size_t)255;
+        off[n++] = o;
+        return o;
+    }
+};
+
+struct Dims {
+    int B, d, Hq, Hkv, F, V, K, depth, N, tc_max, S, max_len;
+    int qkv_w, Rc, Rd, R, P, maxc, lm_rows;
+};
+
+Dims dims_of(const eagle3_draft_tree_args_t *a) {
+    Dims m;
+    m.B = a->batch;
+    m.d = a->hidden;
+    m.Hq = a->n_heads;
+    m.Hkv = a->n_kv_heads;
+    m.F = a->ffn;
+    m.V = a->vocab;
+    m.K = a->top_k;
+    m.depth = a->depth;
+    m.N = a->n_nodes;
+    m.tc_max = a->tc_max;
+    m.S = a->s_max;
+    m.max_len = a->max_draft_len;
+    m.qkv_w = (m.Hq + 2 * m.Hkv) * HD;
+    m.Rc = m.B * m.tc_max;
+    m.Rd = m.K * m.B;
+    m.R = std::max(m.Rc, m.Rd);
+    m.P = (m.depth - 1) * m.K;
+    m.maxc = m.K + (m.depth - 1) * m.K * m.K;
+    m.lm_rows = std::max(m.B, m.Rd);
+    return m;
+}
+
+eagle3_status_t draft_validate(const eagle3_draft_tree_args_t *a) {
+    if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->batch < 0 || a->hidden < 8 || a->n_heads < 1 || a->n_kv_heads < 1 || a->ffn < 8 || a->vocab < 1 ||
+        a->depth < 1 || a->top_k < 1 || a->n_nodes < 2 || a->tc_max < 1 || a->s_max < 1 || a->max_draft_len < 0)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->n_heads % a->n_kv_heads || a->hidden % 8 || a->ffn % 8) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->head_dim != HD || a->top_k > KMAX || a->depth > 8 || a->n_nodes > 64 || a->tc_max > 64)
+        return EAGLE3_ERR_UNSUPPORTED;
+    if ((a->depth - 1) * a->top_k > MAX_SLOTS) return EAGLE3_ERR_UNSUPPORTED;
+    if (a->top_k * (a->n_heads / a->n_kv_heads) > 256 || a->tc_max * (a->n_heads / a->n_kv_heads) > 256)
+        return EAGLE3_ERR_UNSUPPORTED;
+    if (a->top_k > a->vocab) return EAGLE3_ERR_UNSUPPORTED;
+    if ((int64_t)a->max_draft_len + a->tc_max > a->s_max) return EAGLE3_ERR_CAPACITY;
+    if (a->batch == 0) return EAGLE3_OK;
+    if (!a->aux || !a->next_tokens || !a->tc || !a->draft_k_cache || !a->draft_v_cache || !a->draft_len ||
+        !a->tokens || !a->parents || !a->depth_out || !a->anc_mask || !a->score)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    return EAGLE3_OK;
+}
+
+eagle3_linear_args_t lin(int m, int n, int k, int epi, const void *x, const void *w, void *out, const void *res = nullptr,
+                         const void *w2 = nullptr, int32_t *st = nullptr) {
+    eagle3_linear_args_t l;
+    l.m = m;
+    l.n = n;
+    l.k = k;
+    l.epilogue = epi;
+    l.splits = 0;
+    l.ld_x = l.ld_w = l.ld_out = l.ld_res = 0;
+    l.x = (const uint16_t *)x;
+    l.w = (const uint16_t *)w;
+    l.w2 = (const uint16_t *)w2;
+    l.out = out;
+    l.residual = (const uint16_t *)res;
+    l.dev_status = st;
+    return l;
+}
+
+struct Plan {
+    Layout lay;
+    size_t o_g, o_a2k, o_xres, o_qkvc, o_pool, o_attn, o_x1, o_h, o_act, o_abuf, o_nrm, o_logits, o_ttok, o_tlq;
+    size_t o_cs, o_ct, o_cp, o_cd, o_ncand, o_front, o_rtok, o_rx, o_panc, o_ppos, o_canc, o_cpos, o_root, o_gws,
+        o_aws;
+    size_t gws, aws;
+};
+
+AttnLaunch catchup_attn(const Dims &m, const eagle3_draft_tree_args_t *a, uint8_t *ws, const Plan &pl) {
+    AttnLaunch l;
+    l.B = m.B;
+    l.n_slots = m.tc_max;
+    l.q_lo = 0;
+    l.q_hi = m.tc_max;
+    l.Hq = m.Hq;
+    l.Hkv = m.Hkv;
+    l.S = m.S;
+    l.max_prefix = m.max_len;
+    l.num_splits = 0;
+    l.rope_theta = a->rope_theta;
+    l.sm_scale = 1.0f / sqrtf((float)HD);
+    __nv_bfloat16 *qkv = (__nv_bfloat16 *)(ws + pl.o_qkvc);
+    l.q = qkv;
+    l.q_si = m.qkv_w;
+    l.q_sb = (int64_t)m.tc_max * m.qkv_w;
+    l.k = qkv + (size_t)m.Hq * HD;
+    l.k_si = l.q_si;
+    l.k_sb = l.q_sb;
+    l.v = qkv + (size_t)(m.Hq + m.Hkv) * HD;
+    l.v_si = l.q_si;
+    l.v_sb = l.q_sb;
+    l.out = (__nv_bfloat16 *)(ws + pl.o_attn);
+    l.o_si = (int64_t)m.Hq * HD;
+    l.o_sb = (int64_t)m.tc_max * m.Hq * HD;
+    l.k_cache = (const __nv_bfloat16 *)a->draft_k_cache;
+    l.v_cache = (const __nv_bfloat16 *)a->draft_v_cache;
+    l.parents = nullptr;
+    l.anc = (const uint64_t *)(ws + pl.o_canc);
+    l.pos = (const int32_t *)(ws + pl.o_cpos);
+    l.anc_sb = l.pos_sb = m.tc_max;
+    l.prefix_len = a->draft_len;
+    l.lse = nullptr;
+    l.dev_status = a->dev_status;
+    return l;
+}
+
+AttnLaunch depth_attn(const Dims &m, const eagle3_draft_tree_args_t *a, uint8_t *ws, const Plan &pl, int t) {
+    AttnLaunch l;
+    l.B = m.B;
+    l.n_slots = m.P;
+    l.q_lo = (t - 2) * m.K;
+    l.q_hi = (t - 1) * m.K;
+    l.Hq = m.Hq;
+    l.Hkv = m.Hkv;
+    l.S = m.S;
+    l.max_prefix = m.max_len + m.tc_max;
+    l.num_splits = 0;
+    l.rope_theta = a->rope_theta;
+    l.sm_scale = 1.0f / sqrtf((float)HD);
+    __nv_bfloat16 *pool = (__nv_bfloat16 *)(ws + pl.o_pool);
+    l.q = pool;
+    l.q_sb = m.qkv_w;
+    l.q_si = (int64_t)m.B * m.qkv_w;
+    l.k = pool + (size_t)m.Hq * HD;
+    l.k_sb = l.q_sb;
+    l.k_si = l.q_si;
+    l.v = pool + (size_t)(m.Hq + m.Hkv) * HD;
+    l.v_sb = l.q_sb;
+    l.v_si = l.q_si;
+    l.out = (__nv_bfloat16 *)(ws + pl.o_attn);
+    l.o_sb = (int64_t)m.Hq * HD;
+    l.o_si = (int64_t)m.B * m.Hq * HD;
+    l.k_cache = (const __nv_bfloat16 *)a->draft_k_cache;
+    l.v_cache = (const __nv_bfloat16 *)a->draft_v_cache;
+    l.parents = nullptr;
+    l.anc = (const uint64_t *)(ws + pl.o_panc);
+    l.pos = (const int32_t *)(ws + pl.o_ppos);
+    l.anc_sb = l.pos_sb = MAX_SLOTS;
+    l.prefix_len = a->draft_len;
+    l.lse = nullptr;
+    l.dev_status = a->dev_status;
+    return l;
+}
+
+Plan make_plan(const Dims &m, const eagle3_draft_tree_args_t *a) {
+    Plan pl;
+    Layout &L = pl.lay;
+    L.total = 0;
+    const size_t bf = 2;
+    pl.o_g = L.add((size_t)m.Rc * m.d * bf);
+    pl.o_a2k = L.add((size_t)m.R * 2 * m.d * bf);
+    pl.o_xres = L.add((size_t)m.Rd * m.d * bf);
+    pl.o_qkvc = L.add((size_t)m.Rc * m.qkv_w * bf);
+    pl.o_pool = L.add((size_t)std::max(1, m.P) * m.B * m.qkv_w * bf);
+    pl.o_attn = L.add((size_t)m.R * m.Hq * HD * bf);
+    pl.o_x1 = L.add((size_t)m.R * m.d * bf);
+    pl.o_h = L.add((size_t)m.R * m.d * bf);
+    pl.o_act = L.add((size_t)m.R * m.F * bf);
+    pl.o_abuf = L.add((size_t)(m.Rc + std::max(1, m.P) * m.B) * m.d * bf);
+    pl.o_nrm = L.add((size_t)m.lm_rows * m.d * bf);
+    pl.o_logits = L.add(a->dbg_logits ? 16 : (size_t)m.lm_rows * m.V * 4);
+    pl.o_ttok = L.add((size_t)m.lm_rows * m.K * 4);
+    pl.o_tlq = L.add((size_t)m.lm_rows * m.K * 4);
+    pl.o_cs = L.add((size_t)m.B * m.maxc * 4);
+    pl.o_ct = L.add((size_t)m.B * m.maxc * 4);
+    pl.o_cp = L.add((size_t)m.B * m.maxc * 4);
+    pl.o_cd = L.add((size_t)m.B * m.maxc * 4);
+    pl.o_ncand = L.add((size_t)m.B * 4);
+    pl.o_front = L.add((size_t)m.B * KMAX * 4);
+    pl.o_rtok = L.add((size_t)m.Rd * 4);
+    pl.o_rx = L.add((size_t)m.Rd * 4);
+    pl.o_panc = L.add((size_t)m.B * MAX_SLOTS * 8);
+    pl.o_ppos = L.add((size_t)m.B * MAX_SLOTS * 4);
+    pl.o_canc = L.add((size_t)m.B * m.tc_max * 8);
+    pl.o_cpos = L.add((size_t)m.B * m.tc_max * 4);
+    pl.o_root = L.add((size_t)m.B * 4);
+    // GEMM split-K workspace: the largest any projection of this call asks for
+    size_t g = 0;
+    const int shapes[][4] = {{m.Rc, m.d, 3 * m.d, EAGLE3_EPI_BF16},       {m.R, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
+                             {m.R, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.R, m.F, m.d, EAGLE3_EPI_SWIGLU},
+                             {m.R, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL},   {m.B, m.V, m.d, EAGLE3_EPI_F32},
+                             {m.Rd, m.V, m.d, EAGLE3_EPI_F32},            {m.Rd, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
+                             {m.Rd, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.Rd, m.F, m.d, EAGLE3_EPI_SWIGLU},
+                             {m.Rd, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL},  {m.Rc, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
+                             {m.Rc, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.Rc, m.F, m.d, EAGLE3_EPI_SWIGLU},
+                             {m.Rc, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL}};
+    // sizing only: any non-null 16-byte aligned address passes the checks (nothing is dereferenced)
+    const uint16_t *dummy = reinterpret_cast<const uint16_t *>((uintptr_t)256);
+    for (auto &s : shapes) {
+        eagle3_linear_args_t l = lin(s[0], s[1], s[2], s[3], dummy, dummy, (void *)dummy, dummy, dummy);
+        g = std::max(g, eagle3_linear_workspace_size(&l));
+    }
+    pl.gws = g;
+    pl.o_gws = L.add(g + 16);
+    size_t at = 0;
+    uint8_t *fake = nullptr;
+    at = std::max(at, tree_attn_workspace(catchup_attn(m, a, fake, pl)));
+    for (int t = 2; t <= m.depth; ++t) at = std::max(at, tree_attn_workspace(depth_attn(m, a, fake, pl, t)));
+    pl.aws = at;
+    pl.o_aws = L.add(at + 16);
+    return pl;
+}
+
+}  // namespace
+}  // namespace e3
+
+using namespace e3;
+
+extern "C" size_t eagle3_draft_tree_workspace_size(const eagle3_draft_tree_args_t *a) {
+    if (draft_validate(a) != EAGLE3_OK || a->batch == 0) return 0;
+    const Dims m = dims_of(a);
+    return make_plan(m, a).lay.total + 256;
+}
+
+#define E3_TRY(x)                                     \
+    do {                                              \
+        const eagle3_status_t _s = (x);               \
+        if (_s != EAGLE3_OK) return _s;               \
+    } while (0)
+#define E3_LAUNCHED()                                                   \
+    do {                                                                \
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA; \
+    } while (0)
+
+extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, const eagle3_draft_tree_args_t *a,
+                                             void *workspace, size_t ws_bytes, eagle3_stream_t stream_) {
+    E3_TRY(draft_validate(a));
+    if (a->batch == 0) return EAGLE3_OK;
+    if (!W || !W->w_fc || !W->embed || !W->input_norm || !W->hidden_norm || !W->w_qkv || !W->w_o || !W->post_norm ||
+        !W->w_gate || !W->w_up || !W->w_down || !W->final_norm || !W->lm_head)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    const Dims m = dims_of(a);
+    const Plan pl = make_plan(m, a);
+    if (!workspace || ws_bytes < pl.lay.total + 256) return EAGLE3_ERR_WORKSPACE;
+    uint8_t *ws = (uint8_t *)(((uintptr_t)workspace + 255) & ~(uintptr_t)255);
+    cudaStream_t st = (cudaStream_t)stream_;
+    auto P = [&](size_t o) { return (void *)(ws + o); };
+    void *gws = P(pl.o_gws);
+    void *aws = P(pl.o_aws);
+    const int d = m.d, B = m.B, K = m.K;
+    __nv_bfloat16 *abuf = (__nv_bfloat16 *)P(pl.o_abuf);
+    float *logits_base = a->dbg_logits ? a->dbg_logits : (float *)P(pl.o_logits);
+
+    NormParams np;
+    np.dim = d;
+    np.eps = a->rms_eps;
+    np.gather = nullptr;
+    np.tap = nullptr;
+    np.ld_tap = 0;
+    np.dev_status = a->dev_status;
+
+    // ---------------------------------------------------------------- catch-up rows
+    catchup_meta_kernel<<<B, 64, 0, st>>>(B, m.tc_max, a->draft_len, a->tc, (uint64_t *)P(pl.o_canc),
+                                          (int32_t *)P(pl.o_cpos), (int32_t *)P(pl.o_root), a->dev_status);
+    E3_LAUNCHED();
+    {
+        eagle3_linear_args_t l = lin(m.Rc, d, 3 * d, EAGLE3_EPI_BF16, a->aux, W->w_fc, P(pl.o_g), nullptr, nullptr,
+                                     a->dev_status);
+        E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
+    }
+    PrologueParams pp;
+    pp.d = d;
+    pp.vocab = m.V;
+    pp.tc_max = m.tc_max;
+    pp.eps = a->rms_eps;
+    pp.embed = (const __nv_bfloat16 *)W->embed;
+    pp.w_in = (const __nv_bfloat16 *)W->input_norm;
+    pp.w_hid = (const __nv_bfloat16 *)W->hidden_norm;
+    pp.dev_status = a->dev_status;
+    pp.rows = m.Rc;
+    pp.tokens = a->next_tokens;
+    pp.tc = a->tc;
+    pp.x = (const __nv_bfloat16 *)P(pl.o_g);
+    pp.x_row = nullptr;
+    pp.a2k = (__nv_bfloat16 *)P(pl.o_a2k);
+    pp.xres = nullptr;
+    draft_prologue_kernel<<<m.Rc, NT_NORM, 0, st>>>(pp);
+    E3_LAUNCHED();
+
+    auto layer_tail = [&](int rows, const void *x_res, void *a_out) -> eagle3_status_t {
+        // attention output -> O (+x) -> post norm -> SwiGLU -> down (+x1) = a
+        eagle3_linear_args_t l1 = lin(rows, d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL, P(pl.o_attn), W->w_o, P(pl.o_x1),
+                                      x_res, nullptr, a->dev_status);
+        E3_TRY(eagle3_linear(&l1, gws, pl.gws, stream_));
+        NormParams n2 = np;
+        n2.rows = rows;
+        n2.n_src = rows;
+        n2.ld_in = n2.ld_out = d;
+        n2.in = (const __nv_bfloat16 *)P(pl.o_x1);
+        n2.w = (const __nv_bfloat16 *)W->post_norm;
+        n2.out = (__nv_bfloat16 *)P(pl.o_h);
+        rmsnorm_kernel<<<rows, NT_NORM, 0, st>>>(n2);
+        E3_LAUNCHED();
+        eagle3_linear_args_t l2 = lin(rows, m.F, d, EAGLE3_EPI_SWIGLU, P(pl.o_h), W->w_gate, P(pl.o_act), nullptr,
+                                      W->w_up, a->dev_status);
+        E3_TRY(eagle3_linear(&l2, gws, pl.gws, stream_));
+        eagle3_linear_args_t l3 = lin(rows, d, m.F, EAGLE3_EPI_BF16_RESIDUAL, P(pl.o_act), W->w_down, a_out, P(pl.o_x1),
+                                      nullptr, a->dev_status);
+        return eagle3_linear(&l3, gws, pl.gws, stream_);
+    };
+    auto lm_head = [&](int rows, const __nv_bfloat16 *a_rows, const int32_t *gather, float *logits) -> eagle3_status_t {
+        NormParams n3 = np;
+        n3.rows = rows;
+        n3.n_src = gather ? m.Rc : rows;
+        n3.ld_in = n3.ld_out = d;
+        n3.in = a_rows;
+        n3.gather = gather;
+        n3.w = (const __nv_bfloat16 *)W->final_norm;
+        n3.out = (__nv_bfloat16 *)P(pl.o_nrm);
+        rmsnorm_kernel<<<rows, NT_NORM, 0, st>>>(n3);
+        E3_LAUNCHED();
+        eagle3_linear_args_t l = lin(rows, m.V, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
+                                     a->dev_status);
+        E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
+        topk_kernel<<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq));
+        E3_LAUNCHED();
+        return EAGLE3_OK;
+    };
+
+    {
+        eagle3_linear_args_t l = lin(m.Rc, m.qkv_w, 2 * d, EAGLE3_EPI_BF16, P(pl.o_a2k), W->w_qkv, P(pl.o_qkvc), nullptr,
+                                     nullptr, a->dev_status);
+        E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
+        E3_TRY(tree_attn_launch(catchup_attn(m, a, ws, pl), aws, pl.aws, st));
+        E3_TRY(layer_tail(m.Rc, P(pl.o_g), abuf));
+        append_kv_kernel<<<B, 256, 0, st>>>(B, m.tc_max, m.Hkv, m.S, m.qkv_w, m.Hq * HD, (m.Hq + m.Hkv) * HD,
+                                            (const __nv_bfloat16 *)P(pl.o_qkvc), (__nv_bfloat16 *)a->draft_k_cache,
+                                            (__nv_bfloat16 *)a->draft_v_cache, a->draft_len, a->tc, m.max_len,
+                                            a->dev_status);
+        E3_LAUNCHED();
+        E3_TRY(lm_head(B, abuf, (const int32_t *)P(pl.o_root), logits_base));
+    }
+
+    Tree T;
+    T.B = B;
+    T.K = K;
+    T.depth = m.depth;
+    T.n_nodes = m.N;
+    T.maxc = m.maxc;
+    T.tc_max = m.tc_max;
+    T.rows_c = m.Rc;
+    T.c_score = (float *)P(pl.o_cs);
+    T.c_tok = (int32_t *)P(pl.o_ct);
+    T.c_par = (int32_t *)P(pl.o_cp);
+    T.c_dc = (int32_t *)P(pl.o_cd);
+    T.n_cand = (int32_t *)P(pl.o_ncand);
+    T.frontier = (int32_t *)P(pl.o_front);
+    T.row_tok = (int32_t *)P(pl.o_rtok);
+    T.row_x = (int32_t *)P(pl.o_rx);
+    T.pool_anc = (uint64_t *)P(pl.o_panc);
+    T.pool_pos = (int32_t *)P(pl.o_ppos);
+    T.root_row = (const int32_t *)P(pl.o_root);
+    T.draft_len = a->draft_len;
+    T.topk_tok = (const int32_t *)P(pl.o_ttok);
+    T.topk_lq = (const float *)P(pl.o_tlq);
+    T.next_tokens = a->next_tokens;
+    T.tc = a->tc;
+    T.out_tok = a->tokens;
+    T.out_par = a->parents;
+    T.out_depth = a->depth_out;
+    T.out_anc = a->anc_mask;
+    T.out_score = a->score;
+    T.dev_status = a->dev_status;
+    select_step_kernel<<<B, 256, 0, st>>>(T, 1);
+    E3_LAUNCHED();
+
+    // ---------------------------------------------------------------- depth rows
+    for (int t = 2; t <= m.depth; ++t) {
+        const int rows = m.Rd;
+        PrologueParams q = pp;
+        q.rows = rows;
+        q.tokens = T.row_tok;
+        q.tc = nullptr;
+        q.x = abuf;
+        q.x_row = T.row_x;
+        q.xres = (__nv_bfloat16 *)P(pl.o_xres);
+        draft_prologue_kernel<<<rows, NT_NORM, 0, st>>>(q);
+        E3_LAUNCHED();
+        __nv_bfloat16 *pool_rows = (__nv_bfloat16 *)P(pl.o_pool) + (size_t)(t - 2) * rows * m.qkv_w;
+        eagle3_linear_args_t l = lin(rows, m.qkv_w, 2 * d, EAGLE3_EPI_BF16, P(pl.o_a2k), W->w_qkv, pool_rows, nullptr,
+                                     nullptr, a->dev_status);
+        E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
+        E3_TRY(tree_attn_launch(depth_attn(m, a, ws, pl, t), aws, pl.aws, st));
+        __nv_bfloat16 *a_rows = abuf + (size_t)(m.Rc + (t - 2) * rows) * d;
+        E3_TRY(layer_tail(rows, P(pl.o_xres), a_rows));
+        float *logits = logits_base + (a->dbg_logits ? (size_t)(t - 1) * rows * m.V : 0);
+        E3_TRY(lm_head(rows, a_rows, nullptr, logits));
+        select_step_kernel<<<B, 256, 0, st>>>(T, t);
+        E3_LAUNCHED();
+    }
+    const size_t fsm = 2 * MAX_SLOTS * 4 + (size_t)m.maxc * 2 + 16;
+    select_final_kernel<<<B, 256, fsm, st>>>(T);
+    E3_LAUNCHED();
+    return EAGLE3_OK;
+}
+
+extern "C" eagle3_status_t eagle3_rmsnorm(const eagle3_rmsnorm_args_t *a, eagle3_stream_t stream) {
+    if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->rows < 0 || a->dim < 1 || a->n_src < 0 || a->ld_in < 0 || a->ld_out < 0 || a->ld_tap < 0 || !(a->eps >= 0.0f))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->rows == 0) return EAGLE3_OK;
+    if (!a->in || !a->w || !a->out) return EAGLE3_ERR_INVALID_ARGUMENT;
+    NormParams p;
+    p.rows = a->rows;
+    p.dim = a->dim;
+    p.n_src = a->n_src ? a->n_src : a->rows;
+    p.eps = a->eps;
+    p.ld_in = a->ld_in ? a->ld_in : a->dim;
+    p.ld_out = a->ld_out ? a->ld_out : a->dim;
+    p.ld_tap = a->ld_tap ? a->ld_tap : a->dim;
+    p.in = (const __nv_bfloat16 *)a->in;
+    p.w = (const __nv_bfloat16 *)a->w;
+    p.gather = a->gather;
+    p.out = (__nv_bfloat16 *)a->out;
+    p.tap = (__nv_bfloat16 *)a->tap_out;
+    p.dev_status = a->dev_status;
+    rmsnorm_kernel<<<a->rows, NT_NORM, 0, (cudaStream_t)stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? EAGLE3_OK : EAGLE3_ERR_CUDA;
+}

@@ -13,7 +13,7 @@
 // also processes the tree tile: tree keys are rotated in-kernel at L + depth, written back, and
 // masked with the ancestor bitmask built from the parent array.  With more than one split the
 // partial (O, m, l) go to the workspace and a second kernel merges them in split order.
-#include "common.cuh"
+#include "attn.cuh"
 
 namespace e3 {
 namespace {
@@ -27,18 +27,27 @@ constexpr int LDS = D + 8;          // padded smem row (bf16 elements): conflict
 constexpr float LOG2E_F = 1.4426950408889634f;
 
 struct Params {
-    int B, N, Hq, Hkv, S, splits, tiles_per_split, rep;
+    int B, n_slots, q_lo, q_hi, Hq, Hkv, S, splits, tiles_per_split, rep, max_prefix;
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
+    // element (b, slot i, head h) lives at base + b * sb + i * si + h * D
     const __nv_bfloat16 *q;
-    __nv_bfloat16 *tree_k;
-    const __nv_bfloat16 *tree_v, *k_cache, *v_cache;
-    const int32_t *parents, *prefix_len;
-    __nv_bfloat16 *out;
-    float *lse;
-    float *part_o, *part_ml;        // [splits][B][N][Hq][D], [splits][B][N][Hq][2]
+    int64_t q_sb, q_si;
+    __nv_bfloat16 *k;               // tree keys; slots [q_lo, q_hi) are rotated in place
+    int64_t k_sb, k_si;
+    const __nv_bfloat16 *v;
+    int64_t v_sb, v_si;
+    __nv_bfloat16 *out;             // query slot i -> row (i - q_lo)
+    int64_t o_sb, o_si;
+    const __nv_bfloat16 *k_cache, *v_cache;   // [B, Hkv, S, D]
+    const int32_t *parents;         // [B, n_slots] or null: then anc / pos are given
+    const uint64_t *anc;            // [B, anc_sb] ancestor-or-self bits over slots
+    const int32_t *pos;             // [B, pos_sb] RoPE positions of the slots
+    int anc_sb, pos_sb;
+    const int32_t *prefix_len;
+    float *lse;                     // [B, nq, Hq] or null
+    float *part_o, *part_ml;        // [splits][B][nq][Hq][D], [splits][B][nq][Hq][2]
     int32_t *dev_status;
-    int max_prefix;
 };
 
 struct __align__(16) Smem {
@@ -46,7 +55,7 @@ struct __align__(16) Smem {
     __nv_bfloat16 k[2][BK * LDS];
     __nv_bfloat16 v[2][BK * LDS];
     uint64_t anc[64];
-    int32_t depth[64];
+    int32_t pos[64];
     int32_t bad;
 };
 
@@ -107,30 +116,39 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
     Smem &s = *reinterpret_cast<Smem *>(smem_raw);
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int N = p.N, rep = p.rep, nrows = N * rep;
+    const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo, nrows = nq * rep;
     const bool last = split == p.splits - 1;
 
-    // ---- tree: depth and ancestor bits (validated); prefix length
-    if (tid == 0) {
-        int bad = 0;
-        for (int i = 0; i < N; ++i) {
-            const int par = p.parents[(size_t)b * N + i];
-            if ((i == 0 && par != -1) || (i > 0 && (par < 0 || par >= i))) {
-                bad = 1;
-                s.depth[i] = 0;
-                s.anc[i] = 1ull << i;
-                continue;
-            }
-            s.depth[i] = i ? s.depth[par] + 1 : 0;
-            s.anc[i] = (i ? s.anc[par] : 0ull) | (1ull << i);
-        }
-        s.bad = bad;
-        if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
-    }
     int L = p.prefix_len[b];
     if (L < 0 || L > p.max_prefix) {
         if (tid == 0 && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
         L = max(0, min(L, p.max_prefix));
+    }
+    // ---- tree slots: ancestor-or-self bits and RoPE positions
+    if (tid == 0) {
+        if (p.parents) {
+            int bad = 0, depth[64];
+            for (int i = 0; i < nk; ++i) {
+                const int par = p.parents[(size_t)b * p.n_slots + i];
+                if ((i == 0 && par != -1) || (i > 0 && (par < 0 || par >= i))) {
+                    bad = 1;
+                    depth[i] = 0;
+                    s.anc[i] = 1ull << i;
+                } else {
+                    depth[i] = i ? depth[par] + 1 : 0;
+                    s.anc[i] = (i ? s.anc[par] : 0ull) | (1ull << i);
+                }
+                s.pos[i] = L + depth[i];
+            }
+            s.bad = bad;
+            if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+        } else {
+            for (int i = 0; i < nk; ++i) {
+                s.anc[i] = p.anc[(size_t)b * p.anc_sb + i] & (nk >= 64 ? ~0ull : ((1ull << nk) - 1));
+                s.pos[i] = p.pos[(size_t)b * p.pos_sb + i];
+            }
+            s.bad = 0;
+        }
     }
     __syncthreads();
 
@@ -144,9 +162,9 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
     for (int r = warp; r < ROWS; r += NWARP) {
         __nv_bfloat16 *dst = s.q + r * LDS;
         if (r < nrows) {
-            const int i = r / rep, hh = r % rep;
-            const __nv_bfloat16 *src = p.q + (((size_t)b * N + i) * p.Hq + (size_t)g * rep + hh) * D;
-            rope_row(src, dst, nullptr, L + s.depth[i], p.inv_freq, lane);
+            const int i = p.q_lo + r / rep, hh = r % rep;
+            const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
+            rope_row(src, dst, nullptr, s.pos[i], p.inv_freq, lane);
         } else {
             for (int j = lane; j < D; j += 32) dst[j] = __float2bfloat16_rn(0.0f);
         }
@@ -168,31 +186,38 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
     };
     const int n_prefix_tiles = n_tiles - (last ? 1 : 0);
     auto stage_tree_tile = [&](int buf) {
-        // rotated tree keys (written back once) and tree values; rows >= N zeroed
+        // tree slots [0, q_hi): keys of the query slots are rotated here and written back once
+        // (by the last split only), earlier slots were rotated when they were queries; rows past
+        // q_hi are zero
         for (int i = warp; i < BK; i += NWARP) {
             __nv_bfloat16 *kd = s.k[buf] + i * LDS, *vd = s.v[buf] + i * LDS;
-            if (i < N) {
-                const size_t off = (((size_t)b * N + i) * p.Hkv + g) * D;
-                // each lane reads elements lane + 32u (u < 4) and writes back the same four, so
-                // the in-place rotation has no cross-lane hazard
-                __nv_bfloat16 tmp[4];
+            if (i < nk) {
+                __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
+                const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
+                if (i >= p.q_lo) {
+                    // each lane reads elements lane + 32u (u < 4) and writes back the same four,
+                    // so the in-place rotation has no cross-lane hazard
+                    __nv_bfloat16 tmp[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) tmp[u] = p.tree_k[off + lane + 32 * u];
-                const float pos = (float)(L + s.depth[i]);
+                    for (int u = 0; u < 4; ++u) tmp[u] = kg[lane + 32 * u];
+                    const float pos = (float)s.pos[i];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {   // pairs (j, j + 64), j = lane + 32u
-                    const int j = lane + 32 * u;
-                    const float x1 = __bfloat162float(tmp[u]), x2 = __bfloat162float(tmp[u + 2]);
-                    float sn, cs;
-                    sincosf(__fmul_rn(pos, p.inv_freq[j]), &sn, &cs);
-                    const __nv_bfloat16 o1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
-                    const __nv_bfloat16 o2 = __float2bfloat16_rn(x2 * cs + x1 * sn);
-                    kd[j] = o1;
-                    kd[j + 64] = o2;
-                    p.tree_k[off + j] = o1;
-                    p.tree_k[off + j + 64] = o2;
+                    for (int u = 0; u < 2; ++u) {   // pairs (j, j + 64), j = lane + 32u
+                        const int j = lane + 32 * u;
+                        const float x1 = __bfloat162float(tmp[u]), x2 = __bfloat162float(tmp[u + 2]);
+                        float sn, cs;
+                        sincosf(__fmul_rn(pos, p.inv_freq[j]), &sn, &cs);
+                        const __nv_bfloat16 o1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
+                        const __nv_bfloat16 o2 = __float2bfloat16_rn(x2 * cs + x1 * sn);
+                        kd[j] = o1;
+                        kd[j + 64] = o2;
+                        kg[j] = o1;
+                        kg[j + 64] = o2;
+                    }
+                } else {
+                    for (int j = lane; j < D; j += 32) kd[j] = kg[j];
                 }
-                for (int j = lane; j < D; j += 32) vd[j] = p.tree_v[off + j];
+                for (int j = lane; j < D; j += 32) vd[j] = vg[j];
             } else {
                 for (int j = lane; j < D; j += 32) {
                     kd[j] = __float2bfloat16_rn(0.0f);
@@ -234,7 +259,7 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
         __syncthreads();
 
         const int key0 = tree_tile ? 0 : k_lo + t * BK;
-        const int key_end = tree_tile ? N : k_hi;
+        const int key_end = tree_tile ? nk : k_hi;
         // ---- S = Q K^T for 32 rows x 64 keys
         float sc[2][8][4];
 #pragma unroll
@@ -271,7 +296,7 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int row = row_base + mt * 16 + (lane >> 2) + hr * 8;
-                const uint64_t bits = (tree_tile && row < nrows) ? s.anc[row / rep] : 0ull;
+                const uint64_t bits = (tree_tile && row < nrows) ? s.anc[p.q_lo + row / rep] : 0ull;
                 float mx = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt)
@@ -344,27 +369,29 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
         for (int hr = 0; hr < 2; ++hr) {
             const int row = row_base + mt * 16 + (lane >> 2) + hr * 8;
             if (row >= nrows) continue;
-            const int i = row / rep, h = g * rep + row % rep;
-            const size_t orow = ((size_t)b * N + i) * p.Hq + h;
+            const int qi = row / rep, h = g * rep + row % rep;
+            const size_t prow = ((size_t)b * nq + qi) * p.Hq + h;      // partial / lse row
             if (p.splits == 1) {
+                __nv_bfloat16 *orow = p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D;
                 const float inv_l = l_run[mt][hr] > 0.0f ? 1.0f / l_run[mt][hr] : 0.0f;
 #pragma unroll
                 for (int nt = 0; nt < 16; ++nt) {
                     const int d = nt * 8 + (lane & 3) * 2;
-                    *reinterpret_cast<__nv_bfloat162 *>(p.out + orow * D + d) =
+                    *reinterpret_cast<__nv_bfloat162 *>(orow + d) =
                         __floats2bfloat162_rn(o[mt][nt][hr * 2] * inv_l, o[mt][nt][hr * 2 + 1] * inv_l);
                 }
                 if (p.lse && (lane & 3) == 0)
-                    p.lse[orow] = (m_run[mt][hr] + log2f(l_run[mt][hr])) * 0.6931471805599453f;
+                    p.lse[prow] = (m_run[mt][hr] + log2f(l_run[mt][hr])) * 0.6931471805599453f;
             } else {
-                float *po = p.part_o + ((size_t)split * p.B * N * p.Hq + orow) * D;
+                const size_t rows = (size_t)p.B * nq * p.Hq;
+                float *po = p.part_o + ((size_t)split * rows + prow) * D;
 #pragma unroll
                 for (int nt = 0; nt < 16; ++nt) {
                     const int d = nt * 8 + (lane & 3) * 2;
                     *reinterpret_cast<float2 *>(po + d) = make_float2(o[mt][nt][hr * 2], o[mt][nt][hr * 2 + 1]);
                 }
                 if ((lane & 3) == 0) {
-                    float *pm = p.part_ml + ((size_t)split * p.B * N * p.Hq + orow) * 2;
+                    float *pm = p.part_ml + ((size_t)split * rows + prow) * 2;
                     pm[0] = m_run[mt][hr];
                     pm[1] = l_run[mt][hr];
                 }
@@ -372,11 +399,12 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
         }
 }
 
-// Merge split partials in split order: one warp per (b, node, head) row.
+// Merge split partials in split order: one warp per (b, query slot, head) row.
 __global__ void verify_combine_kernel(const Params p) {
+    const int nq = p.q_hi - p.q_lo;
+    const int rows = p.B * nq * p.Hq;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    const int rows = p.B * p.N * p.Hq;
     if (row >= rows) return;
     const size_t stride = (size_t)rows;
     float M = -INFINITY;
@@ -394,16 +422,16 @@ __global__ void verify_combine_kernel(const Params p) {
         acc[3] += w * v.w;
     }
     const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-    __nv_bfloat16 *dst = p.out + (size_t)row * D + lane * 4;
+    const int h = row % p.Hq, qi = (row / p.Hq) % nq, b = row / (p.Hq * nq);
+    __nv_bfloat16 *dst = p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D + lane * 4;
     *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(acc[0] * inv_l, acc[1] * inv_l);
     *reinterpret_cast<__nv_bfloat162 *>(dst + 2) = __floats2bfloat162_rn(acc[2] * inv_l, acc[3] * inv_l);
     if (p.lse && lane == 0) p.lse[row] = (M + log2f(l)) * 0.6931471805599453f;
 }
 
-int plan_splits(int B, int Hkv, int max_prefix, int requested, int sm_count) {
+int plan_splits(int ctas, int max_prefix, int requested, int sm_count) {
     const int tiles = (max_prefix + BK - 1) / BK;
     if (requested > 0) return max(1, min(requested, max(1, tiles)));
-    const int ctas = B * Hkv;
     if (ctas >= sm_count || tiles <= 2) return 1;
     int s = (sm_count + ctas - 1) / ctas;       // fill the GPU once
     s = min(s, max(1, tiles / 2));              // at least two tiles per split
@@ -422,69 +450,57 @@ int sm_count_cached() {
 }
 
 }  // namespace
-}  // namespace e3
 
-using namespace e3;
-
-static eagle3_status_t verify_validate(const eagle3_verify_attn_args_t *a) {
-    if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (a->batch < 0 || a->n_nodes < 1 || a->n_heads < 1 || a->n_kv_heads < 1 || a->head_dim < 1 ||
-        a->s_max < 1 || a->max_prefix_len < 0 || a->num_splits < 0)
-        return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (a->n_heads % a->n_kv_heads) return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (a->head_dim != D || a->n_nodes > 64) return EAGLE3_ERR_UNSUPPORTED;
-    if (a->n_nodes * (a->n_heads / a->n_kv_heads) > ROWS) return EAGLE3_ERR_UNSUPPORTED;
-    if ((int64_t)a->max_prefix_len + a->n_nodes > a->s_max) return EAGLE3_ERR_CAPACITY;
-    if (!(a->rope_theta > 0.0f) || a->sm_scale < 0.0f) return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (a->batch == 0) return EAGLE3_OK;
-    const void *ptrs[] = {a->q, a->tree_k, a->tree_v, a->k_cache, a->v_cache, a->out};
-    for (const void *ptr : ptrs)
-        if (!ptr || ((uintptr_t)ptr & 15)) return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (!a->parents || !a->prefix_len) return EAGLE3_ERR_INVALID_ARGUMENT;
-    return EAGLE3_OK;
-}
-
-extern "C" size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *a) {
-    if (verify_validate(a) != EAGLE3_OK || a->batch == 0) return 0;
-    const int splits = plan_splits(a->batch, a->n_kv_heads, a->max_prefix_len, a->num_splits, sm_count_cached());
-    if (splits == 1) return 0;
-    const size_t rows = (size_t)a->batch * a->n_nodes * a->n_heads;
+size_t tree_attn_workspace(const AttnLaunch &a) {
+    const int splits = plan_splits(a.B * a.Hkv, a.max_prefix, a.num_splits, sm_count_cached());
+    if (splits == 1 || a.B == 0) return 0;
+    const size_t rows = (size_t)a.B * (a.q_hi - a.q_lo) * a.Hq;
     return (size_t)splits * rows * (D + 2) * sizeof(float);
 }
 
-extern "C" eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *a, void *workspace,
-                                              size_t ws_bytes, eagle3_stream_t stream) {
-    const eagle3_status_t st = verify_validate(a);
-    if (st != EAGLE3_OK || a->batch == 0) return st;
-    const int splits = plan_splits(a->batch, a->n_kv_heads, a->max_prefix_len, a->num_splits, sm_count_cached());
-    const size_t need = eagle3_verify_attn_workspace_size(a);
+eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (a.B == 0 || a.q_hi <= a.q_lo) return EAGLE3_OK;
+    const int splits = plan_splits(a.B * a.Hkv, a.max_prefix, a.num_splits, sm_count_cached());
+    const size_t need = tree_attn_workspace(a);
     if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
-
     Params p;
-    p.B = a->batch;
-    p.N = a->n_nodes;
-    p.Hq = a->n_heads;
-    p.Hkv = a->n_kv_heads;
-    p.S = a->s_max;
-    p.rep = a->n_heads / a->n_kv_heads;
+    p.B = a.B;
+    p.n_slots = a.n_slots;
+    p.q_lo = a.q_lo;
+    p.q_hi = a.q_hi;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.S = a.S;
+    p.rep = a.Hq / a.Hkv;
     p.splits = splits;
-    const int tiles = (a->max_prefix_len + BK - 1) / BK;
-    p.tiles_per_split = (tiles + splits - 1) / splits;
-    p.max_prefix = a->max_prefix_len;
-    const float sm_scale = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)D);
-    p.scale_log2 = sm_scale * LOG2E_F;
-    for (int j = 0; j < D / 2; ++j) p.inv_freq[j] = (float)pow((double)a->rope_theta, -2.0 * j / D);
-    p.q = (const __nv_bfloat16 *)a->q;
-    p.tree_k = (__nv_bfloat16 *)a->tree_k;
-    p.tree_v = (const __nv_bfloat16 *)a->tree_v;
-    p.k_cache = (const __nv_bfloat16 *)a->k_cache;
-    p.v_cache = (const __nv_bfloat16 *)a->v_cache;
-    p.parents = a->parents;
-    p.prefix_len = a->prefix_len;
-    p.out = (__nv_bfloat16 *)a->out;
-    p.lse = a->lse;
-    p.dev_status = a->dev_status;
-    const size_t rows = (size_t)a->batch * a->n_nodes * a->n_heads;
+    const int tiles = (a.max_prefix + BK - 1) / BK;
+    p.tiles_per_split = max(1, (tiles + splits - 1) / splits);
+    p.max_prefix = a.max_prefix;
+    p.scale_log2 = a.sm_scale * LOG2E_F;
+    for (int j = 0; j < D / 2; ++j) p.inv_freq[j] = (float)pow((double)a.rope_theta, -2.0 * j / D);
+    p.q = a.q;
+    p.q_sb = a.q_sb;
+    p.q_si = a.q_si;
+    p.k = a.k;
+    p.k_sb = a.k_sb;
+    p.k_si = a.k_si;
+    p.v = a.v;
+    p.v_sb = a.v_sb;
+    p.v_si = a.v_si;
+    p.out = a.out;
+    p.o_sb = a.o_sb;
+    p.o_si = a.o_si;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.parents = a.parents;
+    p.anc = a.anc;
+    p.pos = a.pos;
+    p.anc_sb = a.anc_sb;
+    p.pos_sb = a.pos_sb;
+    p.prefix_len = a.prefix_len;
+    p.lse = a.lse;
+    p.dev_status = a.dev_status;
+    const size_t rows = (size_t)a.B * (a.q_hi - a.q_lo) * a.Hq;
     p.part_o = splits > 1 ? (float *)workspace : nullptr;
     p.part_ml = splits > 1 ? (float *)workspace + (size_t)splits * rows * D : nullptr;
 
@@ -496,11 +512,87 @@ extern "C" eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *a
             return EAGLE3_ERR_CUDA;
         attr_done = true;
     }
-    verify_attn_kernel<<<dim3(splits, a->n_kv_heads, a->batch), NT, smem, (cudaStream_t)stream>>>(p);
+    verify_attn_kernel<<<dim3(splits, a.Hkv, a.B), NT, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
-        verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, (cudaStream_t)stream>>>(p);
+        verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
     return EAGLE3_OK;
+}
+
+}  // namespace e3
+
+using namespace e3;
+
+static eagle3_status_t verify_validate(const eagle3_verify_attn_args_t *a) {
+    if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->batch < 0 || a->n_nodes < 1 || a->n_heads < 1 || a->n_kv_heads < 1 || a->head_dim < 1 ||
+        a->s_max < 1 || a->max_prefix_len < 0 || a->num_splits < 0 || a->q_node_stride < 0 || a->kv_node_stride < 0)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->n_heads % a->n_kv_heads) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->head_dim != D || a->n_nodes > 64) return EAGLE3_ERR_UNSUPPORTED;
+    if (a->n_nodes * (a->n_heads / a->n_kv_heads) > ROWS) return EAGLE3_ERR_UNSUPPORTED;
+    if ((int64_t)a->max_prefix_len + a->n_nodes > a->s_max) return EAGLE3_ERR_CAPACITY;
+    if (!(a->rope_theta > 0.0f) || a->sm_scale < 0.0f) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if ((a->q_node_stride && (a->q_node_stride < (int64_t)a->n_heads * D || a->q_node_stride % 8)) ||
+        (a->kv_node_stride && (a->kv_node_stride < (int64_t)a->n_kv_heads * D || a->kv_node_stride % 8)))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->batch == 0) return EAGLE3_OK;
+    const void *ptrs[] = {a->q, a->tree_k, a->tree_v, a->k_cache, a->v_cache, a->out};
+    for (const void *ptr : ptrs)
+        if (!ptr || ((uintptr_t)ptr & 15)) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (!a->parents || !a->prefix_len) return EAGLE3_ERR_INVALID_ARGUMENT;
+    return EAGLE3_OK;
+}
+
+static AttnLaunch verify_launch(const eagle3_verify_attn_args_t *a) {
+    AttnLaunch l;
+    l.B = a->batch;
+    l.n_slots = a->n_nodes;
+    l.q_lo = 0;
+    l.q_hi = a->n_nodes;
+    l.Hq = a->n_heads;
+    l.Hkv = a->n_kv_heads;
+    l.S = a->s_max;
+    l.max_prefix = a->max_prefix_len;
+    l.num_splits = a->num_splits;
+    l.rope_theta = a->rope_theta;
+    l.sm_scale = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)D);
+    const int64_t qs = a->q_node_stride ? a->q_node_stride : (int64_t)a->n_heads * D;
+    const int64_t kvs = a->kv_node_stride ? a->kv_node_stride : (int64_t)a->n_kv_heads * D;
+    l.q = (const __nv_bfloat16 *)a->q;
+    l.q_si = qs;
+    l.q_sb = qs * a->n_nodes;
+    l.k = (__nv_bfloat16 *)a->tree_k;
+    l.k_si = kvs;
+    l.k_sb = kvs * a->n_nodes;
+    l.v = (const __nv_bfloat16 *)a->tree_v;
+    l.v_si = kvs;
+    l.v_sb = kvs * a->n_nodes;
+    l.out = (__nv_bfloat16 *)a->out;
+    l.o_si = (int64_t)a->n_heads * D;
+    l.o_sb = l.o_si * a->n_nodes;
+    l.k_cache = (const __nv_bfloat16 *)a->k_cache;
+    l.v_cache = (const __nv_bfloat16 *)a->v_cache;
+    l.parents = a->parents;
+    l.anc = nullptr;
+    l.pos = nullptr;
+    l.anc_sb = l.pos_sb = 0;
+    l.prefix_len = a->prefix_len;
+    l.lse = a->lse;
+    l.dev_status = a->dev_status;
+    return l;
+}
+
+extern "C" size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *a) {
+    if (verify_validate(a) != EAGLE3_OK || a->batch == 0) return 0;
+    return tree_attn_workspace(verify_launch(a));
+}
+
+extern "C" eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *a, void *workspace,
+                                              size_t ws_bytes, eagle3_stream_t stream) {
+    const eagle3_status_t st = verify_validate(a);
+    if (st != EAGLE3_OK || a->batch == 0) return st;
+    return tree_attn_launch(verify_launch(a), workspace, ws_bytes, (cudaStream_t)stream);
 }

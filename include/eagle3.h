@@ -143,14 +143,17 @@ typedef struct {
     int32_t max_path;            /* width W of path / slot_map rows                                   */
     int64_t cache_layer_stride;  /* elements between consecutive layers of k_cache / v_cache          */
     int64_t tree_layer_stride;   /* elements between consecutive layers of tree_k / tree_v            */
+    int64_t tree_node_stride;    /* elements between consecutive nodes of tree_k / tree_v; 0 = Hkv*D */
     void *k_cache;               /* [layers][B, Hkv, s_max, D]                                        */
     void *v_cache;               /* [layers][B, Hkv, s_max, D]                                        */
-    const void *tree_k;          /* [layers][B, N, Hkv, D] (already rotated by eagle3_verify_attn)    */
-    const void *tree_v;          /* [layers][B, N, Hkv, D]                                            */
+    const void *tree_k;          /* [layers][B, N, Hkv, D] node pitch tree_node_stride (rotated keys) */
+    const void *tree_v;          /* [layers][B, N, Hkv, D] node pitch tree_node_stride                */
     const int32_t *path;         /* [B, W] from eagle3_accept                                         */
     const int32_t *accept_len;   /* [B]                                                               */
     int32_t *prefix_len;         /* [B] in: L; out: L + n + 1                                         */
     int32_t *slot_map;           /* [B, W] out                                                        */
+    int32_t *committed;          /* [B] optional out: n + 1 positions committed (0 if skipped); this is
+                                    the next draft catch-up row count                                */
     int32_t aux_dim;             /* A: elements per aux row; 0 = no aux gather                        */
     const void *aux_tree;        /* [B, N, A] (elem_bytes each) or NULL                               */
     void *aux_out;               /* [B, W, A] or NULL                                                 */
@@ -177,6 +180,9 @@ eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *args, eagle3_stre
  * natural-log sum of exp of the scaled scores.
  * The prefix is split across CTAs (split-KV) by a plan made from max_prefix_len (a host bound on
  * every prefix_len[b]); partial results are merged by a second kernel in a fixed order.
+ * Node pitches let q / tree_k / tree_v be views into one fused QKV projection output
+ * [B * N, (Hq + 2 Hkv) * D]; rotating tree_k twice (calling twice on the same buffers) rotates the
+ * keys twice, so each verify pass must start from freshly projected keys.
  * ---------------------------------------------------------------------------------------------- */
 typedef struct {
     int32_t batch;              /* B >= 0                                                             */
@@ -187,11 +193,13 @@ typedef struct {
     int32_t s_max;              /* cache capacity; max_prefix_len + N <= s_max is required            */
     int32_t max_prefix_len;     /* host bound on prefix_len[b]                                        */
     int32_t num_splits;         /* 0 = choose automatically                                           */
+    int64_t q_node_stride;      /* elements between consecutive nodes of q; 0 = Hq * D (dense)        */
+    int64_t kv_node_stride;     /* elements between consecutive nodes of tree_k / tree_v; 0 = Hkv * D */
     float rope_theta;           /* e.g. 500000                                                        */
     float sm_scale;             /* 0 = 1/sqrt(D)                                                      */
-    const uint16_t *q;          /* [B, N, Hq, D] bf16, un-rotated                                     */
-    uint16_t *tree_k;           /* [B, N, Hkv, D] bf16, in: un-rotated, out: rotated                  */
-    const uint16_t *tree_v;     /* [B, N, Hkv, D] bf16                                                */
+    const uint16_t *q;          /* [B, N, Hq, D] bf16 (node pitch q_node_stride), un-rotated           */
+    uint16_t *tree_k;           /* [B, N, Hkv, D] bf16 (node pitch kv_node_stride), rotated in place   */
+    const uint16_t *tree_v;     /* [B, N, Hkv, D] bf16 (node pitch kv_node_stride)                    */
     const uint16_t *k_cache;    /* [B, Hkv, s_max, D] bf16, rotated keys                              */
     const uint16_t *v_cache;    /* [B, Hkv, s_max, D] bf16                                            */
     const int32_t *parents;     /* [B, N]                                                             */
@@ -204,6 +212,109 @@ typedef struct {
 size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *args);
 eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *args, void *workspace,
                                    size_t workspace_bytes, eagle3_stream_t stream);
+
+
+/* ------------------------------------------------------------------------------------------------
+ * eagle3_draft_tree - EAGLE-3 draft head and its dynamic top-k draft tree.
+ *
+ * Defines: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", sections VIII-IX
+ * (fc: bias-free Linear(3d -> d) fusing the three aux target states of a committed position;
+ * one decoder layer over two streams - input_norm(e) and hidden_norm(x) concatenated to 2d feed
+ * q/k/v, the residual stream is x, SwiGLU MLP - then final norm and LM head; the embedding is the
+ * target's), section XI (catch-up of committed positions (g_i, e_{t_{i+1}}) into the draft cache,
+ * then drafting rows (a, e_token) one position further per depth), sections IV.3 / XI.6 and
+ * "EAGLE-3: Training-Time Test for Speculative Decoding", "Dynamic Draft Trees" (expand, then
+ * rerank by cumulative log-probability).
+ *
+ * One call: (1) catch-up: rows i < tc[b] of sequence b are (g = fc(aux[b,i]), e = embed[next_tokens
+ * [b,i]]) at positions draft_len[b] + i, causal over the draft cache; their rotated K/V are
+ * appended to the draft cache and draft_len[b] += tc[b] (= L, the target prefix length).  The last
+ * catch-up row (whose token is the root) gives the depth-1 logits.  (2) depth t = 2..depth: the
+ * top_k best depth-(t-1) candidates (score desc, creation asc) each run one draft row (x = a of its
+ * parent's row, e = its token) at position L - 1 + (t - 1), attending to the draft cache, to its
+ * ancestors' rows and to itself; each row's top_k tokens become candidates with score = parent
+ * score + logq (ties in top-k go to the lower token id).  logq is the deterministic fixed-point
+ * log-softmax at T = 1 (see eagle3_accept).  (3) the n_nodes - 1 best candidates by (score desc,
+ * depth asc, creation asc) - ancestor-closed - are emitted after the root in (depth asc, score
+ * desc, creation asc) order, with creation = frontier rank * top_k + child rank.
+ * Weights are bf16 [out, in]; q/k/v rows are stacked in w_qkv ((Hq + 2 Hkv) * D rows).  head_dim
+ * 128; top_k <= 16; (depth - 1) * top_k <= 64; n_nodes - 1 <= top_k + (depth - 1) * top_k^2.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+    const uint16_t *w_fc;        /* [d, 3d]                                                          */
+    const uint16_t *embed;       /* [V, d] token embedding (the target's table)                      */
+    const uint16_t *input_norm;  /* [d] RMSNorm weight of the embedding stream                       */
+    const uint16_t *hidden_norm; /* [d] RMSNorm weight of the feature stream                         */
+    const uint16_t *w_qkv;       /* [(Hq + 2 Hkv) * D, 2d]                                           */
+    const uint16_t *w_o;         /* [d, Hq * D]                                                      */
+    const uint16_t *post_norm;   /* [d]                                                              */
+    const uint16_t *w_gate;      /* [F, d]                                                           */
+    const uint16_t *w_up;        /* [F, d]                                                           */
+    const uint16_t *w_down;      /* [d, F]                                                           */
+    const uint16_t *final_norm;  /* [d]                                                              */
+    const uint16_t *lm_head;     /* [V, d]                                                           */
+} eagle3_draft_weights_t;
+
+typedef struct {
+    int32_t batch;               /* B                                                                */
+    int32_t hidden;              /* d                                                                */
+    int32_t n_heads, n_kv_heads, head_dim;   /* Hq, Hkv, D (= 128)                                    */
+    int32_t ffn;                 /* F                                                                */
+    int32_t vocab;               /* V                                                                */
+    int32_t depth;               /* tree depth (>= 1)                                                */
+    int32_t top_k;               /* children per expanded node (1..16)                               */
+    int32_t n_nodes;             /* nodes emitted including the root (2..64)                         */
+    int32_t tc_max;              /* catch-up rows per sequence in aux / next_tokens (1..64)          */
+    int32_t s_max;               /* draft cache capacity                                             */
+    int32_t max_draft_len;       /* host bound on draft_len[b]; max_draft_len + tc_max <= s_max      */
+    float rope_theta;            /* e.g. 500000                                                      */
+    float rms_eps;               /* e.g. 1e-5                                                        */
+    const uint16_t *aux;         /* [B, tc_max, 3d] bf16 aux target states of the committed positions */
+    const int32_t *next_tokens;  /* [B, tc_max]: token after each committed position; row tc[b]-1 holds the root */
+    const int32_t *tc;           /* [B] catch-up rows per sequence, 1..tc_max                        */
+    uint16_t *draft_k_cache;     /* [B, Hkv, s_max, D] bf16, rotated keys                            */
+    uint16_t *draft_v_cache;     /* [B, Hkv, s_max, D] bf16                                          */
+    int32_t *draft_len;          /* [B] in: cached positions; out: + tc[b]                           */
+    int32_t *tokens;             /* [B, n_nodes] out: node tokens (node 0 = root)                    */
+    int32_t *parents;            /* [B, n_nodes] out                                                 */
+    int32_t *depth_out;          /* [B, n_nodes] out                                                 */
+    uint64_t *anc_mask;          /* [B, n_nodes] out: bit j set <=> node j is the node or an ancestor */
+    float *score;                /* [B, n_nodes] out: cumulative logq (root 0)                       */
+    float *dbg_logits;           /* optional [depth, top_k * B, V] fp32: every draft row's logits;
+                                    depth 1 uses rows 0..B-1 (row b), depth t rows r * B + b for
+                                    frontier rank r; may be NULL                                    */
+    int32_t *dev_status;         /* optional                                                         */
+} eagle3_draft_tree_args_t;
+
+size_t eagle3_draft_tree_workspace_size(const eagle3_draft_tree_args_t *args);
+eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *weights, const eagle3_draft_tree_args_t *args,
+                                  void *workspace, size_t workspace_bytes, eagle3_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * eagle3_rmsnorm - RMSNorm rows (building block of the target layers that verify a tree).
+ *
+ * Defines: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", appendix C (RMSNorm:
+ * w * x * rsqrt(mean(x^2) + eps), statistics in fp32) and section IX.6 / "Speculative Decoding
+ * (EAGLE3) in the vLLM Neuron Framework", "Auxiliary Hidden State Extraction" (the aux taps are the
+ * hidden states entering a decoder layer, i.e. the input of its first norm).
+ * out[r] = w * norm(in[src(r)]), src(r) = gather[r] when gather is given (an embedding lookup:
+ * `in` is then the [V, d] table and gather holds token ids) else r.  When tap_out is given, the
+ * un-normalised input row is also copied to tap_out[r] (pitch ld_tap).  bf16 in / out.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t rows, dim;
+    int32_t n_src;               /* rows of `in` (for gather bounds); 0 = rows                       */
+    float eps;
+    int64_t ld_in, ld_out, ld_tap;   /* pitches in elements, 0 = dim                                 */
+    const uint16_t *in;
+    const uint16_t *w;           /* [dim]                                                            */
+    const int32_t *gather;       /* [rows] or NULL                                                   */
+    uint16_t *out;
+    uint16_t *tap_out;           /* or NULL                                                          */
+    int32_t *dev_status;
+} eagle3_rmsnorm_args_t;
+
+eagle3_status_t eagle3_rmsnorm(const eagle3_rmsnorm_args_t *args, eagle3_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -94,11 +94,14 @@ def select_tree(expand, depth, top_k, n_nodes, cands=None):
 
 
 def draft_tree_for_sequence(draft, d_cache, a_root, root_token, L, depth, top_k, n_nodes,
-                            logits_log=None):
+                            logits_log=None, select_logits=None):
     """Build the tree for one sequence with the oracle draft model.
 
     d_cache holds draft K/V for positions 0..L-1; a_root is the last catch-up
-    row's output.  ``logits_log`` (a list) receives each depth's fp32 logits."""
+    row's output.  ``logits_log`` (a list) receives each depth's fp32 logits.
+    ``select_logits(t, frontier)``, when given, supplies the logits the selection
+    uses (replay of another implementation's logits); the oracle still runs and
+    logs its own rows for that tree, so the two can be compared row by row."""
     cands, rows_a, rows_k, rows_v, row_of = [], [], [], [], {}
 
     def expand(t, front):
@@ -129,7 +132,7 @@ def draft_tree_for_sequence(draft, d_cache, a_root, root_token, L, depth, top_k,
         out = out.astype(np.float32)
         if logits_log is not None:
             logits_log.append(out)
-        return out
+        return out if select_logits is None else np.asarray(select_logits(t, front), dtype=np.float32)
 
     res = select_tree(expand, depth, top_k, n_nodes, cands)
     res["tokens"][0] = root_token
