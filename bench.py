@@ -180,13 +180,18 @@ class Engine:
         self.kernel_ms = {"gemm": 0.0, "verify_attn": 0.0}
         self.kernel_calls = {"gemm": 0, "verify_attn": 0}
         self._ev = []
+        # events are created once and reused: creating timing events inside the loop is not free
+        self._pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(512)]
 
     # -- per-launch timing of the dominant kernels (CUDA events on the launching stream)
     def _timed(self, kind, fn):
         if not self.timing:
             fn()
             return
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if len(self._ev) >= len(self._pool):
+            self.collect()
+        a, b = self._pool[len(self._ev)]
         a.record()
         fn()
         b.record()
