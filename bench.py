@@ -516,6 +516,114 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------------------- kernels
+def _time_loop(fn, steps, warmup, flush=None):
+    """Average device time per call with CUDA events; optional L2 flush between calls."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+    return total / steps
+
+
+def run_kernel(args):
+    """Single-kernel measurements of the rows of the path (not the headline line)."""
+    import eagle_tree_speculative_spec_gb300 as e3
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    hbm, tf_burst, tf_sust, src = peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    out = {"kernel": args.kernel}
+    if args.kernel == "verify_attn":
+        B, L, N, Hq, Hkv, D = args.batch, args.prefix, 60, 32, 8, 128
+        S = L + 64
+        bf = torch.bfloat16
+        q = torch.randn(B, N, Hq, D, generator=g, device=dev).to(bf)
+        tk = torch.randn(B, N, Hkv, D, generator=g, device=dev).to(bf)
+        tv = torch.randn(B, N, Hkv, D, generator=g, device=dev).to(bf)
+        kc = torch.zeros(B, Hkv, S, D, device=dev, dtype=bf)
+        vc = torch.zeros_like(kc)
+        kc[:, :, :L].normal_(generator=g)
+        vc[:, :, :L].normal_(generator=g)
+        import synth
+        r = synth.rng(3)
+        parents = torch.as_tensor(synth.random_tree(r, N)).to(torch.int32).repeat(B, 1).to(dev)
+        plen = torch.full((B,), L, dtype=torch.int32, device=dev)
+        o = torch.empty(B, N, Hq, D, device=dev, dtype=bf)
+        a = e3._lib.verify_attn_args(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L)
+        ws = torch.empty(max(16, e3._lib.eagle3_verify_attn_workspace_size(a)), dtype=torch.uint8, device=dev)
+        fn = lambda: e3.eagle3_verify_attn(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L, workspace=ws)
+        ms = _time_loop(fn, args.steps, args.warmup, flush if B * L * 4096 < 512e6 else None)
+        nbytes = B * (4096 * L + 245760 + 122880 + 983040)
+        out.update(batch=B, prefix=L, ms=round(ms, 4), gbs=round(nbytes / ms / 1e6, 1),
+                   frac_measured=round(nbytes / ms / 1e6 / hbm, 4), frac_8tbs=round(nbytes / ms / 1e6 / 8000, 4),
+                   tflops=round(983040 * L * B / ms / 1e9, 1), bytes=nbytes)
+    elif args.kernel == "accept":
+        import synth
+        B, N, V, W = args.batch, 60, 128256, 7
+        mode = {"greedy": e3.GREEDY, "topk": e3.TOPK, "sampled": e3.SAMPLED}[args.mode]
+        zt, zd, parents, tokens = synth.accept_batch(1, B, N, V, sampled=mode == e3.SAMPLED)
+        zt_d = torch.as_tensor(zt, device=dev)
+        zd_d = torch.as_tensor(zd, device=dev) if mode == e3.SAMPLED else None
+        tok_d = torch.as_tensor(tokens, device=dev)
+        par_d = torch.as_tensor(parents, device=dev)
+        alen = torch.empty(B, dtype=torch.int32, device=dev)
+        path = torch.empty(B, W, dtype=torch.int32, device=dev)
+        emitted = torch.empty(B, W, dtype=torch.int32, device=dev)
+        nroot = torch.empty(B, dtype=torch.int32, device=dev)
+        ws = torch.empty(2 * B * V * 4 + 16, dtype=torch.uint8, device=dev)
+        fn = lambda: e3.eagle3_accept(mode, zt_d, tok_d, par_d, alen, path, emitted, nroot, draft_logits=zd_d,
+                                      temperature=1.0, seed=1, workspace=ws)
+        ms = _time_loop(fn, args.steps, args.warmup, flush)
+        visited = int((alen.to(torch.int64) + 1).sum().item())
+        rows = visited * (2 if mode == e3.SAMPLED else 1)
+        nbytes = rows * V * 4
+        out.update(batch=B, mode=args.mode, ms=round(ms, 4), visited_rows=visited,
+                   gbs_visited=round(nbytes / ms / 1e6, 1), us=round(ms * 1e3, 1))
+    elif args.kernel == "draft":
+        c = dict(CFG)
+        c["B"] = args.batch
+        eng = Engine(c, 4, dev, timing=False)
+        B = c["B"]
+        tc1 = torch.ones(B, dtype=torch.int32, device=dev)
+        dl0 = eng.draft_len.clone()
+        a = e3._lib.draft_tree_args(eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache, eng.draft_len,
+                                    eng.tokens, eng.parents, eng.depth, eng.anc, eng.score, n_heads=c["Hq"],
+                                    ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
+                                    max_draft_len=c["L0"])
+        ws = torch.empty(e3._lib.eagle3_draft_tree_workspace_size(a), dtype=torch.uint8, device=dev)
+
+        def fn():
+            eng.draft_len.copy_(dl0)
+            e3.eagle3_draft_tree(eng.draft_w, eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache,
+                                 eng.draft_len, eng.tokens, eng.parents, eng.depth, eng.anc, eng.score,
+                                 n_heads=c["Hq"], ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
+                                 max_draft_len=c["L0"], workspace=ws)
+        ms = _time_loop(fn, args.steps, args.warmup)
+        d, F, V, qw = c["d"], c["F"], c["V"], eng.qkv_w
+        layer = lambda m: 2 * m * (2 * d * qw + c["Hq"] * 128 * d + 2 * d * F + F * d)
+        rows_c = B * c["W"]
+        flops = 2 * rows_c * 3 * d * d + layer(rows_c) + 2 * B * d * V + 5 * (layer(10 * B) + 2 * 10 * B * d * V)
+        wbytes = 2 * (3 * d * d + 2 * d * qw + c["Hq"] * 128 * d + 3 * d * F + d * V)
+        out.update(batch=B, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
+                   frac_tensor=round(flops / ms / 1e9 / tf_sust, 4),
+                   weight_gbs_6_passes=round(6 * wbytes / ms / 1e6, 1))
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -524,10 +632,16 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft"],
+                    help="time one kernel of the path instead of the whole step")
+    ap.add_argument("--prefix", type=int, default=4096)
+    ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.kernel:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel:
+        run_kernel(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -1,30 +1,53 @@
-// eagle3_verify_attn: tree-masked verify attention (bf16, GQA, head_dim 128), split-KV.
+// eagle3_verify_attn: tree-masked verify attention (bf16, GQA, head_dim 128), split-KV, on the
+// tcgen05 tensor cores with TMEM accumulators.
 //
 // Sources: "Advanced speculative decoding: tree drafts and EAGLE", sections "Why trees" and
 // "Implementation" (forward_with_mask: each node sees the whole prefix plus itself and its
 // ancestors; position = prefix length + depth); "EAGLE-3: Engineering Implementation of LLM
 // Inference Acceleration", appendix C (rotate-half RoPE, GQA, 1/sqrt(D) scaling).
 //
-// One CTA per (sequence b, KV head g, split s).  The N tree nodes times the Hq/Hkv query heads
-// that share KV head g form up to 256 query rows (row = node * rep + head), so the whole GQA
-// group streams each K/V tile once.  Each of the 8 warps owns 32 rows.  K/V tiles of 64 keys are
-// double-buffered in shared memory with cp.async; S = Q K^T and O += P V run on the bf16 tensor
-// cores (mma.m16n8k16, fp32 accumulate) with an online softmax in the log2 domain.  The last split
-// also processes the tree tile: tree keys are rotated in-kernel at L + depth, written back, and
-// masked with the ancestor bitmask built from the parent array.  With more than one split the
-// partial (O, m, l) go to the workspace and a second kernel merges them in split order.
+// One CTA per (sequence b, KV head g, split s).  The query slots times the Hq/Hkv heads that share
+// KV head g form up to 256 query rows (row = slot * rep + head), i.e. up to two 128-row M tiles,
+// so the whole GQA group streams each K/V tile from HBM once.  Warp roles:
+//   warp 0        TMA: 64-key K and V tiles of the prefix (128B-swizzled) into a 3-stage ring
+//   warp 1        tcgen05.mma issuer: S = Q K^T (M 128, N 64) into a double-buffered TMEM tile per
+//                 M tile, then O += P V (M 128, N 128, V as an MN-major operand) into TMEM
+//   warps 2..9    softmax, four warps per M tile, one thread per query row: the row's 64 scores
+//                 come out of TMEM into registers (no shuffles), masked, exponentiated in the log2
+//                 domain and written as bf16 P to shared memory; O is rescaled in TMEM only when
+//                 the running maximum grows by more than 8 (the result is the same, the
+//                 intermediate weights stay below 2^8)
+// The last split also processes the tree tile: the query slots' keys are rotated in-kernel at
+// their positions and written back, then masked with the ancestor bitmask.  With more than one
+// split the partial (O, m, l) go to the workspace and a second kernel merges them in split order.
+// All waits are bounded; a timeout sets EAGLE3_DEV_TIMEOUT and the CTA drains and exits.
+#include <cudaTypedefs.h>
+
 #include "attn.cuh"
+#include "tc.cuh"
 
 namespace e3 {
 namespace {
 
 constexpr int D = 128;
-constexpr int ROWS = 256;           // query rows per CTA (N * rep <= 256)
+constexpr int ROWS = 256;           // query rows per CTA (two M tiles)
+constexpr int MT = 128;             // rows per M tile
 constexpr int BK = 64;              // keys per tile
-constexpr int NWARP = 8;
+constexpr int ST = 3;               // K/V stages
+constexpr int NWARP = 10;
 constexpr int NT = NWARP * 32;
-constexpr int LDS = D + 8;          // padded smem row (bf16 elements): conflict-free ldmatrix
 constexpr float LOG2E_F = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+constexpr uint32_t Q_TILE = MT * D * 2;          // 32 KB: two 64-column blocks of 16 KB
+constexpr uint32_t KV_TILE = BK * D * 2;         // 16 KB: two 64-column blocks of 8 KB
+constexpr uint32_t P_TILE = MT * BK * 2;         // 16 KB
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE;
+constexpr uint32_t OFF_TREE = OFF_KV + ST * 2 * KV_TILE;
+constexpr uint32_t OFF_P = OFF_TREE + 2 * KV_TILE;
+constexpr uint32_t SMEM_DYN = OFF_P + 2 * P_TILE + 1024;   // + alignment slack
+static_assert(SMEM_DYN + 1024 <= 232448, "shared memory budget");
 
 struct Params {
     int B, n_slots, q_lo, q_hi, Hq, Hkv, S, splits, tiles_per_split, rep, max_prefix;
@@ -39,7 +62,6 @@ struct Params {
     int64_t v_sb, v_si;
     __nv_bfloat16 *out;             // query slot i -> row (i - q_lo)
     int64_t o_sb, o_si;
-    const __nv_bfloat16 *k_cache, *v_cache;   // [B, Hkv, S, D]
     const int32_t *parents;         // [B, n_slots] or null: then anc / pos are given
     const uint64_t *anc;            // [B, anc_sb] ancestor-or-self bits over slots
     const int32_t *pos;             // [B, pos_sb] RoPE positions of the slots
@@ -50,73 +72,72 @@ struct Params {
     int32_t *dev_status;
 };
 
-struct __align__(16) Smem {
-    __nv_bfloat16 q[ROWS * LDS];
-    __nv_bfloat16 k[2][BK * LDS];
-    __nv_bfloat16 v[2][BK * LDS];
+struct SmemStatic {
+    uint64_t kv_full[ST], kv_empty[ST];
+    uint64_t s_full[2][2], s_free[2][2], p_full[2], pv_done[2], mma_done;
     uint64_t anc[64];
     int32_t pos[64];
-    int32_t bad;
+    uint32_t tmem_base;
+    int abort_flag;
 };
 
-E3_DEV void cp_async16(void *smem, const void *gmem, bool pred) {
-    const uint32_t s = smem_u32(smem);
-    const int n = pred ? 16 : 0;   // zero-fill when out of range
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n));
-}
-E3_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-E3_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-E3_DEV void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(smem_u32(p)));
-}
-E3_DEV void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(smem_u32(p)));
-}
-E3_DEV void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-E3_DEV uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
+// warp-uniform bounded wait (lane 0 polls, the outcome is broadcast)
+E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Rotate one 128-wide row (rotate-half RoPE) at position pos, fp32 math, bf16 out.
-E3_DEV void rope_row(const __nv_bfloat16 *src, __nv_bfloat16 *dst_smem, __nv_bfloat16 *dst_global,
-                     int pos, const float *inv_freq, int lane) {
-    // lane handles pairs j = lane, lane + 32 (j < 64) and their partners j + 64
+// rotate-half RoPE of one 128-wide row into a 128B-swizzled tile row (and optionally back to
+// global memory); lane j handles the pairs (j, j + 64) and (j + 32, j + 96)
+E3_DEV void rope_row_sw(const __nv_bfloat16 *src, uint8_t *tile, int row, uint32_t block_bytes,
+                        __nv_bfloat16 *writeback, float pos, const float *inv_freq, int lane) {
+    __nv_bfloat16 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = src[lane + 32 * u];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int j = lane + 32 * u;
-        const float x1 = __bfloat162float(src[j]), x2 = __bfloat162float(src[j + 64]);
+        const float x1 = __bfloat162float(x[u]), x2 = __bfloat162float(x[u + 2]);
         float sn, cs;
-        sincosf(__fmul_rn((float)pos, inv_freq[j]), &sn, &cs);
+        sincosf(__fmul_rn(pos, inv_freq[j]), &sn, &cs);
         const __nv_bfloat16 o1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
         const __nv_bfloat16 o2 = __float2bfloat16_rn(x2 * cs + x1 * sn);
-        dst_smem[j] = o1;
-        dst_smem[j + 64] = o2;
-        if (dst_global) {
-            dst_global[j] = o1;
-            dst_global[j + 64] = o2;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, j, block_bytes)) = o1;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, j + 64, block_bytes)) = o2;
+        if (writeback) {
+            writeback[j] = o1;
+            writeback[j + 64] = o2;
         }
     }
 }
 
-__global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+E3_DEV void copy_row_sw(const __nv_bfloat16 *src, uint8_t *tile, int row, uint32_t block_bytes, int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int c = lane + 32 * u;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, c, block_bytes)) = src[c];
+    }
+}
+
+E3_DEV void zero_row_sw(uint8_t *tile, int row, uint32_t block_bytes, int lane) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, lane + 32 * u, block_bytes)) =
+            __float2bfloat16_rn(0.0f);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ SmemStatic ss;
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    volatile int *abort = &ss.abort_flag;
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo, nrows = nq * rep;
+    const int n_mt = (nrows + MT - 1) / MT;
     const bool last = split == p.splits - 1;
 
     int L = p.prefix_len[b];
@@ -124,8 +145,29 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
         if (tid == 0 && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
         L = max(0, min(L, p.max_prefix));
     }
-    // ---- tree slots: ancestor-or-self bits and RoPE positions
+    const int t_lo = split * p.tiles_per_split;
+    const int k_lo = min(L, t_lo * BK);
+    const int k_hi = last ? L : min(L, (t_lo + p.tiles_per_split) * BK);
+    const int n_prefix = (k_hi - k_lo + BK - 1) / BK;
+    const int n_tiles = n_prefix + (last ? 1 : 0);
+
     if (tid == 0) {
+        for (int s = 0; s < ST; ++s) {
+            tc::mbar_init(&ss.kv_full[s], 1);
+            tc::mbar_init(&ss.kv_empty[s], 1);
+        }
+        for (int m = 0; m < 2; ++m) {
+            for (int u = 0; u < 2; ++u) {
+                tc::mbar_init(&ss.s_full[m][u], 1);
+                tc::mbar_init(&ss.s_free[m][u], 4);
+            }
+            tc::mbar_init(&ss.p_full[m], 4);
+            tc::mbar_init(&ss.pv_done[m], 1);
+        }
+        tc::mbar_init(&ss.mma_done, 1);
+        ss.abort_flag = 0;
+        tc::fence_barrier_init();
+        // tree slots: ancestor-or-self bits and RoPE positions
         if (p.parents) {
             int bad = 0, depth[64];
             for (int i = 0; i < nk; ++i) {
@@ -133,270 +175,304 @@ __global__ void __launch_bounds__(NT, 1) verify_attn_kernel(const Params p) {
                 if ((i == 0 && par != -1) || (i > 0 && (par < 0 || par >= i))) {
                     bad = 1;
                     depth[i] = 0;
-                    s.anc[i] = 1ull << i;
+                    ss.anc[i] = 1ull << i;
                 } else {
                     depth[i] = i ? depth[par] + 1 : 0;
-                    s.anc[i] = (i ? s.anc[par] : 0ull) | (1ull << i);
+                    ss.anc[i] = (i ? ss.anc[par] : 0ull) | (1ull << i);
                 }
-                s.pos[i] = L + depth[i];
+                ss.pos[i] = L + depth[i];
             }
-            s.bad = bad;
             if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
         } else {
             for (int i = 0; i < nk; ++i) {
-                s.anc[i] = p.anc[(size_t)b * p.anc_sb + i] & (nk >= 64 ? ~0ull : ((1ull << nk) - 1));
-                s.pos[i] = p.pos[(size_t)b * p.pos_sb + i];
+                ss.anc[i] = p.anc[(size_t)b * p.anc_sb + i] & (nk >= 64 ? ~0ull : ((1ull << nk) - 1));
+                ss.pos[i] = p.pos[(size_t)b * p.pos_sb + i];
             }
-            s.bad = 0;
         }
     }
+    if (warp == 1) tc::tmem_alloc(&ss.tmem_base, 512);
     __syncthreads();
 
-    // ---- prefix key range of this split
-    const int t_lo = split * p.tiles_per_split;
-    const int k_lo = min(L, t_lo * BK);
-    const int k_hi = last ? L : min(L, (t_lo + p.tiles_per_split) * BK);
-    const int n_tiles = (k_hi - k_lo + BK - 1) / BK + (last ? 1 : 0);   // + the tree tile
-
-    // ---- Q rows (rotated) into smem; zero padding rows
-    for (int r = warp; r < ROWS; r += NWARP) {
-        __nv_bfloat16 *dst = s.q + r * LDS;
-        if (r < nrows) {
-            const int i = p.q_lo + r / rep, hh = r % rep;
-            const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
-            rope_row(src, dst, nullptr, s.pos[i], p.inv_freq, lane);
-        } else {
-            for (int j = lane; j < D; j += 32) dst[j] = __float2bfloat16_rn(0.0f);
-        }
-    }
-
-    const __nv_bfloat16 *kc = p.k_cache + ((size_t)b * p.Hkv + g) * (size_t)p.S * D;
-    const __nv_bfloat16 *vc = p.v_cache + ((size_t)b * p.Hkv + g) * (size_t)p.S * D;
-
-    auto load_tile = [&](int t, int buf) {
-        // prefix tiles: cp.async from the cache; the tree tile is written by the warps below
-        const int key0 = k_lo + t * BK;
-        for (int c = tid; c < BK * (D / 8); c += NT) {
-            const int kr = c / (D / 8), kc8 = (c % (D / 8)) * 8;
-            const bool ok = key0 + kr < k_hi;
-            const size_t off = (size_t)(ok ? key0 + kr : 0) * D + kc8;
-            cp_async16(s.k[buf] + kr * LDS + kc8, kc + off, ok);
-            cp_async16(s.v[buf] + kr * LDS + kc8, vc + off, ok);
-        }
-    };
-    const int n_prefix_tiles = n_tiles - (last ? 1 : 0);
-    auto stage_tree_tile = [&](int buf) {
-        // tree slots [0, q_hi): keys of the query slots are rotated here and written back once
-        // (by the last split only), earlier slots were rotated when they were queries; rows past
-        // q_hi are zero
-        for (int i = warp; i < BK; i += NWARP) {
-            __nv_bfloat16 *kd = s.k[buf] + i * LDS, *vd = s.v[buf] + i * LDS;
-            if (i < nk) {
-                __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
-                const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
-                if (i >= p.q_lo) {
-                    // each lane reads elements lane + 32u (u < 4) and writes back the same four,
-                    // so the in-place rotation has no cross-lane hazard
-                    __nv_bfloat16 tmp[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) tmp[u] = kg[lane + 32 * u];
-                    const float pos = (float)s.pos[i];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {   // pairs (j, j + 64), j = lane + 32u
-                        const int j = lane + 32 * u;
-                        const float x1 = __bfloat162float(tmp[u]), x2 = __bfloat162float(tmp[u + 2]);
-                        float sn, cs;
-                        sincosf(__fmul_rn(pos, p.inv_freq[j]), &sn, &cs);
-                        const __nv_bfloat16 o1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
-                        const __nv_bfloat16 o2 = __float2bfloat16_rn(x2 * cs + x1 * sn);
-                        kd[j] = o1;
-                        kd[j + 64] = o2;
-                        kg[j] = o1;
-                        kg[j + 64] = o2;
-                    }
-                } else {
-                    for (int j = lane; j < D; j += 32) kd[j] = kg[j];
-                }
-                for (int j = lane; j < D; j += 32) vd[j] = vg[j];
+    // ---- softmax warps stage Q (rotated) and, in the last split, the tree tile
+    if (warp >= 2) {
+        const int w8 = warp - 2;
+        for (int r = w8; r < n_mt * MT; r += 8) {
+            uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
+            if (r < nrows) {
+                const int i = p.q_lo + r / rep, hh = r % rep;
+                const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
+                rope_row_sw(src, tile, r % MT, Q_TILE / 2, nullptr, (float)ss.pos[i], p.inv_freq, lane);
             } else {
-                for (int j = lane; j < D; j += 32) {
-                    kd[j] = __float2bfloat16_rn(0.0f);
-                    vd[j] = __float2bfloat16_rn(0.0f);
+                zero_row_sw(tile, r % MT, Q_TILE / 2, lane);
+            }
+        }
+        if (last) {
+            uint8_t *tk = sm + OFF_TREE, *tv = sm + OFF_TREE + KV_TILE;
+            for (int i = w8; i < BK; i += 8) {
+                if (i < nk) {
+                    __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
+                    const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
+                    if (i >= p.q_lo) rope_row_sw(kg, tk, i, KV_TILE / 2, kg, (float)ss.pos[i], p.inv_freq, lane);
+                    else copy_row_sw(kg, tk, i, KV_TILE / 2, lane);
+                    copy_row_sw(vg, tv, i, KV_TILE / 2, lane);
+                } else {
+                    zero_row_sw(tk, i, KV_TILE / 2, lane);
+                    zero_row_sw(tv, i, KV_TILE / 2, lane);
                 }
             }
         }
-    };
-
-    // ---- accumulators: 2 m16 tiles per warp; O over 16 n8 tiles of D; running max / sum
-    float o[2][16][4];
-    float m_run[2][2], l_run[2][2];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.0f;
-        m_run[mt][0] = m_run[mt][1] = -INFINITY;
-        l_run[mt][0] = l_run[mt][1] = 0.0f;
+        tc::fence_proxy_async_smem();
     }
-    const int row_base = warp * 32;
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = ss.tmem_base;
 
-    if (n_tiles > 0) {
-        if (n_prefix_tiles > 0) load_tile(0, 0);
-        cp_async_commit();
-    }
-    for (int t = 0; t < n_tiles; ++t) {
-        const int buf = t & 1;
-        const bool tree_tile = last && t == n_tiles - 1;
-        if (t + 1 < n_tiles) {
-            if (t + 1 < n_prefix_tiles) load_tile(t + 1, buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        if (tree_tile) stage_tree_tile(buf);
-        __syncthreads();
-
-        const int key0 = tree_tile ? 0 : k_lo + t * BK;
-        const int key_end = tree_tile ? nk : k_hi;
-        // ---- S = Q K^T for 32 rows x 64 keys
-        float sc[2][8][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.0f;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            uint32_t a[2][4];
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const __nv_bfloat16 *qa = s.q + (row_base + mt * 16 + (lane & 15)) * LDS + kk * 16 + (lane >> 4) * 8;
-                ldsm_x4(a[mt][0], a[mt][1], a[mt][2], a[mt][3], qa);
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_prefix > 0) {
+            tc::prefetch_tmap(&tm_k);
+            tc::prefetch_tmap(&tm_v);
+            const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
+            uint32_t issued = 0, last_par = 0;
+            for (int j = 0; j < n_prefix; ++j) {
+                const int s = j % ST;
+                const uint32_t ph = (uint32_t)(j / ST) & 1u;
+                if (!tc::mbar_wait(&ss.kv_empty[s], ph ^ 1u, abort)) {
+                    flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+                    break;
+                }
+                uint8_t *kd = sm + OFF_KV + s * 2 * KV_TILE, *vd = kd + KV_TILE;
+                tc::mbar_expect_tx(&ss.kv_full[s], 2 * KV_TILE);
+                const int y = row0 + j * BK;
+                tc::tma_load_2d(kd, &tm_k, 0, y, &ss.kv_full[s]);
+                tc::tma_load_2d(kd + KV_TILE / 2, &tm_k, 64, y, &ss.kv_full[s]);
+                tc::tma_load_2d(vd, &tm_v, 0, y, &ss.kv_full[s]);
+                tc::tma_load_2d(vd + KV_TILE / 2, &tm_v, 64, y, &ss.kv_full[s]);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
             }
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {   // pairs of n8 tiles (16 keys)
-                uint32_t b0, b1, b2, b3;
-                const int krow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                const __nv_bfloat16 *kb = s.k[buf] + krow * LDS + kk * 16 + ((lane >> 3) & 1) * 8;
-                ldsm_x4(b0, b1, b2, b3, kb);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    mma_bf16(sc[mt][2 * np], a[mt][0], a[mt][1], a[mt][2], a[mt][3], b0, b1);
-                    mma_bf16(sc[mt][2 * np + 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], b2, b3);
+            // no TMA write may be in flight when the CTA exits (bounded)
+            for (int s = 0; s < ST; ++s) {
+                if (!((issued >> s) & 1u)) continue;
+                const long long t0 = clock64();
+                while (!tc::mbar_try(&ss.kv_full[s], (last_par >> s) & 1u) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
                 }
             }
         }
-        // ---- mask, online softmax (log2 domain), P in bf16
-        uint32_t pa[2][4][4];
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t IDESC_S = tc::idesc_bf16(MT, BK);
+            constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
+            bool ok = true;
+            auto k_tile = [&](int j) -> uint8_t * {
+                return j < n_prefix ? sm + OFF_KV + (j % ST) * 2 * KV_TILE : sm + OFF_TREE;
+            };
+            auto issue_s = [&](int j) {
+                if (j < n_prefix) {
+                    if (!tc::mbar_wait(&ss.kv_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
+                        ok = false;
+                        return;
+                    }
+                }
+                tc::fence_after();
+                const uint32_t kaddr = smem_u32(k_tile(j));
+                for (int m = 0; m < n_mt && ok; ++m) {
+                    if (!tc::mbar_wait(&ss.s_free[m][j & 1], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        return;
+                    }
+                    tc::fence_after();
+                    const uint32_t qaddr = smem_u32(sm + OFF_Q + m * Q_TILE);
+                    const uint32_t d_s = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+                        tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
+                                        tc::desc_sw128(kaddr + blk * (KV_TILE / 2) + kk * 32), IDESC_S,
+                                        k > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&ss.s_full[m][j & 1]);
+                }
+            };
+            issue_s(0);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (j + 1 < n_tiles) issue_s(j + 1);
+                if (!ok) break;
+                const uint32_t vaddr = smem_u32(k_tile(j) + KV_TILE);
+                for (int m = 0; m < n_mt; ++m) {
+                    if (!tc::mbar_wait(&ss.p_full[m], (uint32_t)j & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t paddr = smem_u32(sm + OFF_P + m * P_TILE);
+                    const uint32_t d_o = tmem + (uint32_t)(m * 128);
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = row_base + mt * 16 + (lane >> 2) + hr * 8;
-                const uint64_t bits = (tree_tile && row < nrows) ? s.anc[p.q_lo + row / rep] : 0ull;
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        tc::mma_bf16_ss(d_o, tc::desc_sw128(paddr + kk * 32),
+                                        tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(&ss.pv_done[m]);
+                }
+                if (!ok) break;
+                if (j < n_prefix) tc::mma_commit(&ss.kv_empty[j % ST]);
+            }
+            if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            tc::mma_commit(&ss.mma_done);
+            const long long t0 = clock64();
+            while (!tc::mbar_try(&ss.mma_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax warps
+        const int m = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int rl = quarter * 32 + lane;              // row within the M tile
+        const int row = m * MT + rl;
+        if (m < n_mt) {
+            const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+            const uint64_t bits = row < nrows ? ss.anc[p.q_lo + row / rep] : 0ull;
+            float m_run = -INFINITY, l_run = 0.0f;
+            bool ok = true;
+            uint8_t *prow = sm + OFF_P + m * P_TILE;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int u = j & 1;
+                if (!warp_wait(&ss.s_full[m][u], (uint32_t)(j >> 1) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
+                float sc[64];
+                {
+                    float a[32], c[32];
+                    tc::tmem_ld32(t_lane + 256u + (uint32_t)(m * 128 + u * 64), a);
+                    tc::tmem_ld32(t_lane + 256u + (uint32_t)(m * 128 + u * 64 + 32), c);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        sc[i] = a[i];
+                        sc[32 + i] = c[i];
+                    }
+                }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ss.s_free[m][u]);
+                const bool tree = j == n_prefix;         // the last split's final tile
+                const int key0 = k_lo + j * BK;
                 float mx = -INFINITY;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int key = key0 + nt * 8 + (lane & 3) * 2 + e;
-                        const int local = nt * 8 + (lane & 3) * 2 + e;
-                        bool ok = key < key_end;
-                        if (tree_tile) ok = ok && ((bits >> local) & 1ull);
-                        float v = sc[mt][nt][hr * 2 + e] * p.scale_log2;
-                        v = ok ? v : -INFINITY;
-                        sc[mt][nt][hr * 2 + e] = v;
-                        mx = fmaxf(mx, v);
+                for (int i = 0; i < 64; ++i) {
+                    const bool valid = tree ? (i < nk && ((bits >> i) & 1ull)) : (key0 + i < k_hi);
+                    const float v = valid ? sc[i] * p.scale_log2 : -INFINITY;
+                    sc[i] = v;
+                    mx = fmaxf(mx, v);
+                }
+                if (j > 0) {
+                    // the previous P V must be done before P is overwritten or O rescaled
+                    if (!warp_wait(&ss.pv_done[m], (uint32_t)(j - 1) & 1u, abort)) {
+                        ok = false;
+                        break;
                     }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[mt][hr], mx);
-                const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-                const float corr = exp2f(m_run[mt][hr] - m_use);
-                m_run[mt][hr] = m_new;
+                    tc::fence_after();
+                }
+                const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                    const float corr = need ? (m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
+                    if (j > 0) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            tc::tmem_ld32(t_lane + (uint32_t)(m * 128 + c * 32), o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= corr;
+                            tc::tmem_st32(t_lane + (uint32_t)(m * 128 + c * 32), o);
+                        }
+                    }
+                    l_run *= corr;
+                    m_run = m_new;
+                }
+                const float mu = m_run == -INFINITY ? 0.0f : m_run;
                 float sum = 0.0f;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(sc[mt][nt][hr * 2 + e] - m_use);
-                        sc[mt][nt][hr * 2 + e] = pv;
-                        sum += pv;
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = exp2f(sc[c * 8 + 2 * e] - mu), p1 = exp2f(sc[c * 8 + 2 * e + 1] - mu);
+                        sum += p0 + p1;
+                        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                        w[e] = *reinterpret_cast<uint32_t *>(&h);
                     }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                l_run[mt][hr] = l_run[mt][hr] * corr + sum;
+                    *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(rl, c * 8, P_TILE)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                l_run += sum;
+                tc::fence_proxy_async_smem();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ss.p_full[m]);
+            }
+            if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            // ---- epilogue: O / l
+            float o[D];
+            bool have = false;
+            if (ok && n_tiles > 0 && warp_wait(&ss.pv_done[m], (uint32_t)(n_tiles - 1) & 1u, abort)) {
+                tc::fence_after();
 #pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    o[mt][nt][hr * 2] *= corr;
-                    o[mt][nt][hr * 2 + 1] *= corr;
+                for (int c = 0; c < D / 32; ++c) {
+                    float t[32];
+                    tc::tmem_ld32(t_lane + (uint32_t)(m * 128 + c * 32), t);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[c * 32 + i] = t[i];
+                }
+                have = true;
+            }
+            if (!have) {
+                m_run = -INFINITY;
+                l_run = 0.0f;
+#pragma unroll
+                for (int i = 0; i < D; ++i) o[i] = 0.0f;
+            }
+            if (row < nrows) {
+                const int qi = row / rep, h = g * rep + row % rep;
+                const size_t prow_i = ((size_t)b * nq + qi) * p.Hq + h;
+                if (p.splits == 1) {
+                    __nv_bfloat16 *dst = p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D;
+                    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+#pragma unroll
+                    for (int c = 0; c < D; c += 8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 hv = __floats2bfloat162_rn(o[c + 2 * e] * inv_l, o[c + 2 * e + 1] * inv_l);
+                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    if (p.lse) p.lse[prow_i] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+                } else {
+                    const size_t rows_all = (size_t)p.B * nq * p.Hq;
+                    float *po = p.part_o + ((size_t)split * rows_all + prow_i) * D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                    float *pm = p.part_ml + ((size_t)split * rows_all + prow_i) * 2;
+                    pm[0] = m_run;
+                    pm[1] = l_run;
                 }
             }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                pa[mt][kk][0] = pack_bf16(sc[mt][2 * kk][0], sc[mt][2 * kk][1]);
-                pa[mt][kk][1] = pack_bf16(sc[mt][2 * kk][2], sc[mt][2 * kk][3]);
-                pa[mt][kk][2] = pack_bf16(sc[mt][2 * kk + 1][0], sc[mt][2 * kk + 1][1]);
-                pa[mt][kk][3] = pack_bf16(sc[mt][2 * kk + 1][2], sc[mt][2 * kk + 1][3]);
-            }
         }
-        // ---- O += P V
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // 16 keys per step
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {   // pairs of n8 tiles of D
-                uint32_t b0, b1, b2, b3;
-                const int vrow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const __nv_bfloat16 *vb = s.v[buf] + vrow * LDS + np * 16 + (lane >> 4) * 8;
-                ldsm_x4_t(b0, b1, b2, b3, vb);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    mma_bf16(o[mt][2 * np], pa[mt][kk][0], pa[mt][kk][1], pa[mt][kk][2], pa[mt][kk][3], b0, b1);
-                    mma_bf16(o[mt][2 * np + 1], pa[mt][kk][0], pa[mt][kk][1], pa[mt][kk][2], pa[mt][kk][3], b2, b3);
-                }
-            }
-        }
-        __syncthreads();   // buffer `buf` is reloaded two iterations later
     }
 
-    // ---- epilogue: final output (one split) or partials
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int row = row_base + mt * 16 + (lane >> 2) + hr * 8;
-            if (row >= nrows) continue;
-            const int qi = row / rep, h = g * rep + row % rep;
-            const size_t prow = ((size_t)b * nq + qi) * p.Hq + h;      // partial / lse row
-            if (p.splits == 1) {
-                __nv_bfloat16 *orow = p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D;
-                const float inv_l = l_run[mt][hr] > 0.0f ? 1.0f / l_run[mt][hr] : 0.0f;
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    const int d = nt * 8 + (lane & 3) * 2;
-                    *reinterpret_cast<__nv_bfloat162 *>(orow + d) =
-                        __floats2bfloat162_rn(o[mt][nt][hr * 2] * inv_l, o[mt][nt][hr * 2 + 1] * inv_l);
-                }
-                if (p.lse && (lane & 3) == 0)
-                    p.lse[prow] = (m_run[mt][hr] + log2f(l_run[mt][hr])) * 0.6931471805599453f;
-            } else {
-                const size_t rows = (size_t)p.B * nq * p.Hq;
-                float *po = p.part_o + ((size_t)split * rows + prow) * D;
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    const int d = nt * 8 + (lane & 3) * 2;
-                    *reinterpret_cast<float2 *>(po + d) = make_float2(o[mt][nt][hr * 2], o[mt][nt][hr * 2 + 1]);
-                }
-                if ((lane & 3) == 0) {
-                    float *pm = p.part_ml + ((size_t)split * rows + prow) * 2;
-                    pm[0] = m_run[mt][hr];
-                    pm[1] = l_run[mt][hr];
-                }
-            }
-        }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
 }
 
 // Merge split partials in split order: one warp per (b, query slot, head) row.
@@ -427,6 +503,32 @@ __global__ void verify_combine_kernel(const Params p) {
     *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(acc[0] * inv_l, acc[1] * inv_l);
     *reinterpret_cast<__nv_bfloat162 *>(dst + 2) = __floats2bfloat162_rn(acc[2] * inv_l, acc[3] * inv_l);
     if (p.lse && lane == 0) p.lse[row] = (M + log2f(l)) * 0.6931471805599453f;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+// [rows, 128] bf16 cache viewed as a 2-D tensor; 64 x 64 boxes, 128-byte swizzle
+bool make_cache_map(CUtensorMap *m, const void *base, int64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)BK};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int plan_splits(int ctas, int max_prefix, int requested, int sm_count) {
@@ -490,8 +592,6 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
     p.out = a.out;
     p.o_sb = a.o_sb;
     p.o_si = a.o_si;
-    p.k_cache = a.k_cache;
-    p.v_cache = a.v_cache;
     p.parents = a.parents;
     p.anc = a.anc;
     p.pos = a.pos;
@@ -504,15 +604,18 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
     p.part_o = splits > 1 ? (float *)workspace : nullptr;
     p.part_ml = splits > 1 ? (float *)workspace + (size_t)splits * rows * D : nullptr;
 
-    const size_t smem = sizeof(Smem);
+    CUtensorMap mk, mv;
+    const int64_t cache_rows = (int64_t)a.B * a.Hkv * a.S;
+    if (!make_cache_map(&mk, a.k_cache, cache_rows) || !make_cache_map(&mv, a.v_cache, cache_rows))
+        return EAGLE3_ERR_CUDA;
     static bool attr_done = false;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        if (cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_DYN) !=
             cudaSuccess)
             return EAGLE3_ERR_CUDA;
         attr_done = true;
     }
-    verify_attn_kernel<<<dim3(splits, a.Hkv, a.B), NT, smem, stream>>>(p);
+    verify_attn_kernel<<<dim3(splits, a.Hkv, a.B), NT, SMEM_DYN, stream>>>(mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
         verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
