@@ -33,8 +33,8 @@ constexpr int D = 128;
 constexpr int ROWS = 256;           // query rows per CTA (two M tiles)
 constexpr int MT = 128;             // rows per M tile
 constexpr int BK = 64;              // keys per tile
-constexpr int ST = 3;               // K/V stages
-constexpr int NWARP = 10;
+constexpr int ST = 2;               // K and V stages (each its own ring)
+constexpr int NWARP = 11;             // 0: K loads, 1: MMA, 2..9: softmax, 10: V loads
 constexpr int NT = NWARP * 32;
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -46,7 +46,7 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE;
 constexpr uint32_t OFF_TREE = OFF_KV + ST * 2 * KV_TILE;
 constexpr uint32_t OFF_P = OFF_TREE + 2 * KV_TILE;
-constexpr uint32_t SMEM_DYN = OFF_P + 2 * P_TILE + 1024;   // + alignment slack
+constexpr uint32_t SMEM_DYN = OFF_P + 4 * P_TILE + 1024;   // P double-buffered per M tile; + alignment
 static_assert(SMEM_DYN + 1024 <= 232448, "shared memory budget");
 
 struct Params {
@@ -73,13 +73,22 @@ struct Params {
 };
 
 struct SmemStatic {
-    uint64_t kv_full[ST], kv_empty[ST];
-    uint64_t s_full[2][2], s_free[2][2], p_full[2], pv_done[2], mma_done;
+    uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
+    // every per-tile barrier is double-buffered by tile parity: a producer may run one tile ahead
+    // of its consumer, and a phase that completes twice before it is awaited would be lost
+    uint64_t s_full[2][2], s_free[2][2], p_full[2][2], pv_done[2][2], mma_done;
     uint64_t anc[64];
     int32_t pos[64];
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// 2^x on the special-function unit (flushes subnormal results to zero)
+E3_DEV float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // warp-uniform bounded wait (lane 0 polls, the outcome is broadcast)
 E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -153,16 +162,20 @@ __global__ void __launch_bounds__(NT, 1)
 
     if (tid == 0) {
         for (int s = 0; s < ST; ++s) {
-            tc::mbar_init(&ss.kv_full[s], 1);
-            tc::mbar_init(&ss.kv_empty[s], 1);
+            tc::mbar_init(&ss.k_full[s], 1);
+            tc::mbar_init(&ss.k_empty[s], 1);
+            tc::mbar_init(&ss.v_full[s], 1);
+            tc::mbar_init(&ss.v_empty[s], 1);
         }
         for (int m = 0; m < 2; ++m) {
             for (int u = 0; u < 2; ++u) {
                 tc::mbar_init(&ss.s_full[m][u], 1);
                 tc::mbar_init(&ss.s_free[m][u], 4);
             }
-            tc::mbar_init(&ss.p_full[m], 4);
-            tc::mbar_init(&ss.pv_done[m], 1);
+            tc::mbar_init(&ss.p_full[m][0], 4);
+            tc::mbar_init(&ss.p_full[m][1], 4);
+            tc::mbar_init(&ss.pv_done[m][0], 1);
+            tc::mbar_init(&ss.pv_done[m][1], 1);
         }
         tc::mbar_init(&ss.mma_done, 1);
         ss.abort_flag = 0;
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
 
     // ---- softmax warps stage Q (rotated) and, in the last split, the tree tile
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 10) {
         const int w8 = warp - 2;
         for (int r = w8; r < n_mt * MT; r += 8) {
             uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
@@ -228,27 +241,31 @@ __global__ void __launch_bounds__(NT, 1)
     tc::fence_after();
     const uint32_t tmem = ss.tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 10) {
+        // ------------------------------------------------------------------ TMA producers
+        // warp 0 streams K tiles, warp 10 V tiles; each has its own ring so that a K stage is
+        // refilled as soon as its S MMA is done, long before the V of the same tile is used
         if (lane == 0 && n_prefix > 0) {
-            tc::prefetch_tmap(&tm_k);
-            tc::prefetch_tmap(&tm_v);
+            const bool is_k = warp == 0;
+            const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+            uint64_t *full = is_k ? ss.k_full : ss.v_full;
+            uint64_t *empty = is_k ? ss.k_empty : ss.v_empty;
+            uint8_t *ring = sm + OFF_KV + (is_k ? 0 : ST * KV_TILE);
+            tc::prefetch_tmap(map);
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             uint32_t issued = 0, last_par = 0;
             for (int j = 0; j < n_prefix; ++j) {
                 const int s = j % ST;
                 const uint32_t ph = (uint32_t)(j / ST) & 1u;
-                if (!tc::mbar_wait(&ss.kv_empty[s], ph ^ 1u, abort)) {
+                if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) {
                     flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
                     break;
                 }
-                uint8_t *kd = sm + OFF_KV + s * 2 * KV_TILE, *vd = kd + KV_TILE;
-                tc::mbar_expect_tx(&ss.kv_full[s], 2 * KV_TILE);
+                uint8_t *dst = ring + s * KV_TILE;
+                tc::mbar_expect_tx(&full[s], KV_TILE);
                 const int y = row0 + j * BK;
-                tc::tma_load_2d(kd, &tm_k, 0, y, &ss.kv_full[s]);
-                tc::tma_load_2d(kd + KV_TILE / 2, &tm_k, 64, y, &ss.kv_full[s]);
-                tc::tma_load_2d(vd, &tm_v, 0, y, &ss.kv_full[s]);
-                tc::tma_load_2d(vd + KV_TILE / 2, &tm_v, 64, y, &ss.kv_full[s]);
+                tc::tma_load_2d(dst, map, 0, y, &full[s]);
+                tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
             }
@@ -256,7 +273,7 @@ __global__ void __launch_bounds__(NT, 1)
             for (int s = 0; s < ST; ++s) {
                 if (!((issued >> s) & 1u)) continue;
                 const long long t0 = clock64();
-                while (!tc::mbar_try(&ss.kv_full[s], (last_par >> s) & 1u) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+                while (!tc::mbar_try(&full[s], (last_par >> s) & 1u) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
                 }
             }
         }
@@ -267,11 +284,14 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
             bool ok = true;
             auto k_tile = [&](int j) -> uint8_t * {
-                return j < n_prefix ? sm + OFF_KV + (j % ST) * 2 * KV_TILE : sm + OFF_TREE;
+                return j < n_prefix ? sm + OFF_KV + (j % ST) * KV_TILE : sm + OFF_TREE;
+            };
+            auto v_tile = [&](int j) -> uint8_t * {
+                return j < n_prefix ? sm + OFF_KV + (ST + j % ST) * KV_TILE : sm + OFF_TREE + KV_TILE;
             };
             auto issue_s = [&](int j) {
                 if (j < n_prefix) {
-                    if (!tc::mbar_wait(&ss.kv_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
+                    if (!tc::mbar_wait(&ss.k_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
                         ok = false;
                         return;
                     }
@@ -295,19 +315,24 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                     tc::mma_commit(&ss.s_full[m][j & 1]);
                 }
+                if (ok && j < n_prefix) tc::mma_commit(&ss.k_empty[j % ST]);   // K stage free once S is done
             };
+            // two S tiles in flight; each iteration: P V of tile j as soon as its P is ready, then S(j + 2)
             issue_s(0);
+            if (n_tiles > 1 && ok) issue_s(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j + 1 < n_tiles) issue_s(j + 1);
-                if (!ok) break;
-                const uint32_t vaddr = smem_u32(k_tile(j) + KV_TILE);
+                if (j < n_prefix && !tc::mbar_wait(&ss.v_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t vaddr = smem_u32(v_tile(j));
                 for (int m = 0; m < n_mt; ++m) {
-                    if (!tc::mbar_wait(&ss.p_full[m], (uint32_t)j & 1u, abort)) {
+                    if (!tc::mbar_wait(&ss.p_full[m][j & 1], (uint32_t)(j >> 1) & 1u, abort)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t paddr = smem_u32(sm + OFF_P + m * P_TILE);
+                    const uint32_t paddr = smem_u32(sm + OFF_P + (m * 2 + (j & 1)) * P_TILE);
                     const uint32_t d_o = tmem + (uint32_t)(m * 128);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -315,10 +340,11 @@ __global__ void __launch_bounds__(NT, 1)
                                         tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
                                         (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc::mma_commit(&ss.pv_done[m]);
+                    tc::mma_commit(&ss.pv_done[m][j & 1]);
                 }
                 if (!ok) break;
-                if (j < n_prefix) tc::mma_commit(&ss.kv_empty[j % ST]);
+                if (j < n_prefix) tc::mma_commit(&ss.v_empty[j % ST]);
+                if (j + 2 < n_tiles) issue_s(j + 2);
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             tc::mma_commit(&ss.mma_done);
@@ -337,7 +363,7 @@ __global__ void __launch_bounds__(NT, 1)
             const uint64_t bits = row < nrows ? ss.anc[p.q_lo + row / rep] : 0ull;
             float m_run = -INFINITY, l_run = 0.0f;
             bool ok = true;
-            uint8_t *prow = sm + OFF_P + m * P_TILE;
+            uint8_t *pbase = sm + OFF_P + m * 2 * P_TILE;
             for (int j = 0; j < n_tiles; ++j) {
                 const int u = j & 1;
                 if (!warp_wait(&ss.s_full[m][u], (uint32_t)(j >> 1) & 1u, abort)) {
@@ -361,26 +387,37 @@ __global__ void __launch_bounds__(NT, 1)
                 if (lane == 0) tc::mbar_arrive(&ss.s_free[m][u]);
                 const bool tree = j == n_prefix;         // the last split's final tile
                 const int key0 = k_lo + j * BK;
-                float mx = -INFINITY;
+                const bool full = !tree && key0 + BK <= k_hi;  // every key of the tile is visible
+                // scale (and mask) with four independent max chains
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const bool valid = tree ? (i < nk && ((bits >> i) & 1ull)) : (key0 + i < k_hi);
-                    const float v = valid ? sc[i] * p.scale_log2 : -INFINITY;
-                    sc[i] = v;
-                    mx = fmaxf(mx, v);
+                    for (int i = 0; i < 64; ++i) {
+                        sc[i] *= p.scale_log2;
+                        mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const bool valid = tree ? (i < nk && ((bits >> i) & 1ull)) : (key0 + i < k_hi);
+                        sc[i] = valid ? sc[i] * p.scale_log2 : -INFINITY;
+                        mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
+                    }
                 }
-                if (j > 0) {
-                    // the previous P V must be done before P is overwritten or O rescaled
-                    if (!warp_wait(&ss.pv_done[m], (uint32_t)(j - 1) & 1u, abort)) {
+                const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
+                const bool any_need = __any_sync(0xffffffffu, need);
+                if (any_need && j > 0) {
+                    // O is about to be rescaled: the previous P V must be finished first
+                    if (!warp_wait(&ss.pv_done[m][(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                 }
-                const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
-                if (__any_sync(0xffffffffu, need)) {
+                if (any_need) {
                     const float m_new = need ? fmaxf(m_run, mx) : m_run;
-                    const float corr = need ? (m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new)) : 1.0f;
+                    const float corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
                     if (j > 0) {
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
@@ -395,31 +432,41 @@ __global__ void __launch_bounds__(NT, 1)
                     m_run = m_new;
                 }
                 const float mu = m_run == -INFINITY ? 0.0f : m_run;
-                float sum = 0.0f;
+                // exponentials and the row sum (four chains), packed to bf16 pairs
+                uint32_t pk[32];
+                float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float p0 = exp2f(sc[c * 8 + 2 * e] - mu), p1 = exp2f(sc[c * 8 + 2 * e + 1] - mu);
-                        sum += p0 + p1;
-                        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                        w[e] = *reinterpret_cast<uint32_t *>(&h);
-                    }
-                    *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(rl, c * 8, P_TILE)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = fast_exp2(sc[2 * e] - mu), p1 = fast_exp2(sc[2 * e + 1] - mu);
+                    sq[e & 3] += p0 + p1;
+                    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                    pk[e] = *reinterpret_cast<uint32_t *>(&h);
                 }
+                const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+                if (j > 1) {
+                    // P buffer j & 1 was last read by the P V of tile j - 2
+                    if (!warp_wait(&ss.pv_done[m][j & 1], (uint32_t)((j - 2) >> 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(pbase + (j & 1) * P_TILE + tc::sw128_offset(rl, c * 8, P_TILE)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 l_run += sum;
                 tc::fence_proxy_async_smem();
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.p_full[m]);
+                if (lane == 0) tc::mbar_arrive(&ss.p_full[m][j & 1]);
             }
             if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             // ---- epilogue: O / l
             float o[D];
             bool have = false;
-            if (ok && n_tiles > 0 && warp_wait(&ss.pv_done[m], (uint32_t)(n_tiles - 1) & 1u, abort)) {
+            if (ok && n_tiles > 0 &&
+                warp_wait(&ss.pv_done[m][(n_tiles - 1) & 1], (uint32_t)((n_tiles - 1) >> 1) & 1u, abort)) {
                 tc::fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
