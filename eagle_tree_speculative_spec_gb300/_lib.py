@@ -112,6 +112,8 @@ def _declare(L):
     L.eagle3_verify_attn_workspace_size.argtypes = [P(VerifyAttnArgs)]
     L.eagle3_verify_attn.restype = ctypes.c_int
     L.eagle3_verify_attn.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_verify_attn_noalloc.restype = ctypes.c_int
+    L.eagle3_verify_attn_noalloc.argtypes = [P(VerifyAttnArgs), _p]
     L.eagle3_linear_workspace_size.restype = ctypes.c_size_t
     L.eagle3_linear_workspace_size.argtypes = [P(LinearArgs)]
     L.eagle3_linear.restype = ctypes.c_int
@@ -377,3 +379,13 @@ def eagle3_rmsnorm(x, w, out, *, eps=1e-5, gather=None, tap_out=None, dev_status
         if t is not None and (not t.is_cuda or t.dtype != bf or t.stride(-1) != 1):
             raise ValueError(f"{name} must be a bf16 CUDA tensor with unit inner stride")
     _check(lib().eagle3_rmsnorm(ctypes.byref(a), _stream(stream)), "eagle3_rmsnorm")
+
+
+def eagle3_verify_attn_noalloc(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
+                               lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None,
+                               stream=None):
+    """eagle3_verify_attn without a workspace: the library's static scratch holds the split partials."""
+    a = verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out,
+                         max_prefix_len=max_prefix_len, lse=lse, rope_theta=rope_theta, sm_scale=sm_scale,
+                         num_splits=num_splits, dev_status=dev_status)
+    _check(lib().eagle3_verify_attn_noalloc(ctypes.byref(a), _stream(stream)), "eagle3_verify_attn_noalloc")

@@ -746,3 +746,44 @@ extern "C" eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *a
     if (st != EAGLE3_OK || a->batch == 0) return st;
     return tree_attn_launch(verify_launch(a), workspace, ws_bytes, (cudaStream_t)stream);
 }
+
+// ------------------------------------------------------------------------------------------------
+// eagle3_verify_attn_noalloc: the same attention for callers that cannot allocate device memory
+// (for example a runtime that hands all device memory to its own pool before the first step, or
+// code that must not allocate while it is being captured into a CUDA graph).  The split-KV
+// partials live in a file-scope device array of fixed size instead of a caller workspace.
+// ------------------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)32 << 20;   // 32 MiB, held by every device that loads the library
+__device__ __align__(256) uint8_t g_verify_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Host code cannot use the array's name as a device address: look the address up once per device
+// (with that device current) and keep it.
+void *noalloc_scratch_address() {
+    static std::mutex mu;
+    static void *addr[128] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_verify_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" eagle3_status_t eagle3_verify_attn_noalloc(const eagle3_verify_attn_args_t *a, eagle3_stream_t stream) {
+    const eagle3_status_t st = verify_validate(a);
+    if (st != EAGLE3_OK || a->batch == 0) return st;
+    void *scratch = noalloc_scratch_address();     // first call on a device: address lookup
+    if (!scratch) return EAGLE3_ERR_CUDA;
+    const AttnLaunch l = verify_launch(a);
+    if (tree_attn_workspace(l) > NOALLOC_SCRATCH_BYTES) return EAGLE3_ERR_WORKSPACE;
+    return tree_attn_launch(l, scratch, NOALLOC_SCRATCH_BYTES, (cudaStream_t)stream);
+}

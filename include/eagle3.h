@@ -216,6 +216,22 @@ size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *args);
 eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *args, void *workspace,
                                    size_t workspace_bytes, eagle3_stream_t stream);
 
+/* eagle3_verify_attn_noalloc - eagle3_verify_attn for callers that cannot allocate device memory.
+ * The pages have no counterpart: this exists for callers whose device memory is all handed to
+ * another owner (a serving runtime's preallocated pool, a process that must not call cudaMalloc
+ * while a step is being captured into a CUDA graph), so they cannot provide a workspace.
+ * Same arguments, semantics and results as eagle3_verify_attn; the split-KV partials go to a
+ * 32 MiB scratch array that the library places in device memory (every GPU that loads the library
+ * holds it until the process exits).  The call allocates nothing: no cudaMalloc / cudaFree.
+ *  - The first call on each device looks up the scratch address (cudaGetSymbolAddress) with that
+ *    device current; make that first call before any stream capture.
+ *  - A split plan that needs more than 32 MiB (batch * n_nodes * n_heads * splits * 520 bytes)
+ *    returns EAGLE3_ERR_WORKSPACE before launching; pass a smaller num_splits to fit.
+ *  - All calls share the one scratch array: calls that can overlap on the GPU (different streams,
+ *    no ordering between them) race on it.  Nothing in it needs to start at zero: every partial
+ *    is written before it is read, and a call never reads an earlier call's contents. */
+eagle3_status_t eagle3_verify_attn_noalloc(const eagle3_verify_attn_args_t *args, eagle3_stream_t stream);
+
 
 /* ------------------------------------------------------------------------------------------------
  * eagle3_draft_tree - EAGLE-3 draft head and its dynamic top-k draft tree.
