@@ -10,13 +10,16 @@
 // KV head g form up to 256 query rows (row = slot * rep + head), i.e. up to two 128-row M tiles,
 // so the whole GQA group streams each K/V tile from HBM once.  Warp roles:
 //   warp 0        TMA: 64-key K and V tiles of the prefix (128B-swizzled) into a 3-stage ring
-//   warp 1        tcgen05.mma issuer: S = Q K^T (M 128, N 64) into a double-buffered TMEM tile per
-//                 M tile, then O += P V (M 128, N 128, V as an MN-major operand) into TMEM
+//   warps 1, 11   tcgen05.mma issuers, one per M tile so that the two tiles' chains do not wait on
+//                 each other: S = Q K^T (M 128, N 64) into a double-buffered TMEM tile, then
+//                 O += P V (M 128, N 128; P read from TMEM, V an MN-major smem operand); a K or V
+//                 stage is released when both issuers have committed
 //   warps 2..9    softmax, four warps per M tile, one thread per query row: the row's 64 scores
 //                 come out of TMEM into registers (no shuffles), masked, exponentiated in the log2
-//                 domain and written as bf16 P to shared memory; O is rescaled in TMEM only when
-//                 the running maximum grows by more than 8 (the result is the same, the
-//                 intermediate weights stay below 2^8)
+//                 domain and written back over the same TMEM columns as packed bf16 P; O is
+//                 rescaled in TMEM only when the running maximum grows by more than 8 (the result
+//                 is the same, the intermediate weights stay below 2^8)
+//   warp 10       TMA: V tiles (K and V have separate rings)
 // The last split also processes the tree tile: the query slots' keys are rotated in-kernel at
 // their positions and written back, then masked with the ancestor bitmask.  With more than one
 // split the partial (O, m, l) go to the workspace and a second kernel merges them in split order.
@@ -33,20 +36,18 @@ constexpr int D = 128;
 constexpr int ROWS = 256;           // query rows per CTA (two M tiles)
 constexpr int MT = 128;             // rows per M tile
 constexpr int BK = 64;              // keys per tile
-constexpr int ST = 2;               // K and V stages (each its own ring)
-constexpr int NWARP = 11;             // 0: K loads, 1: MMA, 2..9: softmax, 10: V loads
+constexpr int ST = 4;               // K and V stages (each its own ring)
+constexpr int NWARP = 12;             // 0: K loads, 1 and 11: MMA (one per M tile), 2..9: softmax, 10: V loads
 constexpr int NT = NWARP * 32;
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 constexpr uint32_t Q_TILE = MT * D * 2;          // 32 KB: two 64-column blocks of 16 KB
 constexpr uint32_t KV_TILE = BK * D * 2;         // 16 KB: two 64-column blocks of 8 KB
-constexpr uint32_t P_TILE = MT * BK * 2;         // 16 KB
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE;
 constexpr uint32_t OFF_TREE = OFF_KV + ST * 2 * KV_TILE;
-constexpr uint32_t OFF_P = OFF_TREE + 2 * KV_TILE;
-constexpr uint32_t SMEM_DYN = OFF_P + 4 * P_TILE + 1024;   // P double-buffered per M tile; + alignment
+constexpr uint32_t SMEM_DYN = OFF_TREE + 2 * KV_TILE + 1024;   // + alignment slack
 static_assert(SMEM_DYN + 1024 <= 232448, "shared memory budget");
 
 struct Params {
@@ -76,7 +77,7 @@ struct SmemStatic {
     uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
     // every per-tile barrier is double-buffered by tile parity: a producer may run one tile ahead
     // of its consumer, and a phase that completes twice before it is awaited would be lost
-    uint64_t s_full[2][2], s_free[2][2], p_full[2][2], pv_done[2][2], mma_done;
+    uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], mma_done[2];
     uint64_t anc[64];
     int32_t pos[64];
     uint32_t tmem_base;
@@ -163,21 +164,19 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) {
         for (int s = 0; s < ST; ++s) {
             tc::mbar_init(&ss.k_full[s], 1);
-            tc::mbar_init(&ss.k_empty[s], 1);
+            tc::mbar_init(&ss.k_empty[s], n_mt);
             tc::mbar_init(&ss.v_full[s], 1);
-            tc::mbar_init(&ss.v_empty[s], 1);
+            tc::mbar_init(&ss.v_empty[s], n_mt);
         }
         for (int m = 0; m < 2; ++m) {
-            for (int u = 0; u < 2; ++u) {
-                tc::mbar_init(&ss.s_full[m][u], 1);
-                tc::mbar_init(&ss.s_free[m][u], 4);
-            }
+            for (int u = 0; u < 2; ++u) tc::mbar_init(&ss.s_full[m][u], 1);
             tc::mbar_init(&ss.p_full[m][0], 4);
             tc::mbar_init(&ss.p_full[m][1], 4);
             tc::mbar_init(&ss.pv_done[m][0], 1);
             tc::mbar_init(&ss.pv_done[m][1], 1);
         }
-        tc::mbar_init(&ss.mma_done, 1);
+        tc::mbar_init(&ss.mma_done[0], 1);
+        tc::mbar_init(&ss.mma_done[1], 1);
         ss.abort_flag = 0;
         tc::fence_barrier_init();
         // tree slots: ancestor-or-self bits and RoPE positions
@@ -277,9 +276,10 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+    } else if (warp == 1 || warp == 11) {
+        // ------------------------------------------------------------------ MMA issuers
+        const int m = warp == 1 ? 0 : 1;
+        if (lane == 0 && n_tiles > 0 && m < n_mt) {
             constexpr uint32_t IDESC_S = tc::idesc_bf16(MT, BK);
             constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
             bool ok = true;
@@ -296,26 +296,23 @@ __global__ void __launch_bounds__(NT, 1)
                         return;
                     }
                 }
+                // the S/P buffer j & 1 last held P(j - 2): its P V must be finished
+                if (j >= 2 && !tc::mbar_wait(&ss.pv_done[m][j & 1], (uint32_t)((j - 2) >> 1) & 1u, abort)) {
+                    ok = false;
+                    return;
+                }
                 tc::fence_after();
                 const uint32_t kaddr = smem_u32(k_tile(j));
-                for (int m = 0; m < n_mt && ok; ++m) {
-                    if (!tc::mbar_wait(&ss.s_free[m][j & 1], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort)) {
-                        ok = false;
-                        return;
-                    }
-                    tc::fence_after();
-                    const uint32_t qaddr = smem_u32(sm + OFF_Q + m * Q_TILE);
-                    const uint32_t d_s = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);
+                const uint32_t qaddr = smem_u32(sm + OFF_Q + m * Q_TILE);
+                const uint32_t d_s = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-                        tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
-                                        tc::desc_sw128(kaddr + blk * (KV_TILE / 2) + kk * 32), IDESC_S,
-                                        k > 0 ? 1u : 0u);
-                    }
-                    tc::mma_commit(&ss.s_full[m][j & 1]);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+                    tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
+                                    tc::desc_sw128(kaddr + blk * (KV_TILE / 2) + kk * 32), IDESC_S, k > 0 ? 1u : 0u);
                 }
-                if (ok && j < n_prefix) tc::mma_commit(&ss.k_empty[j % ST]);   // K stage free once S is done
+                tc::mma_commit(&ss.s_full[m][j & 1]);
+                if (j < n_prefix) tc::mma_commit(&ss.k_empty[j % ST]);   // K stage free once S is done
             };
             // two S tiles in flight; each iteration: P V of tile j as soon as its P is ready, then S(j + 2)
             issue_s(0);
@@ -326,30 +323,27 @@ __global__ void __launch_bounds__(NT, 1)
                     break;
                 }
                 const uint32_t vaddr = smem_u32(v_tile(j));
-                for (int m = 0; m < n_mt; ++m) {
-                    if (!tc::mbar_wait(&ss.p_full[m][j & 1], (uint32_t)(j >> 1) & 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    const uint32_t paddr = smem_u32(sm + OFF_P + (m * 2 + (j & 1)) * P_TILE);
-                    const uint32_t d_o = tmem + (uint32_t)(m * 128);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc::mma_bf16_ss(d_o, tc::desc_sw128(paddr + kk * 32),
-                                        tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
-                                        (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::mma_commit(&ss.pv_done[m][j & 1]);
+                if (!tc::mbar_wait(&ss.p_full[m][j & 1], (uint32_t)(j >> 1) & 1u, abort)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                tc::fence_after();
+                const uint32_t t_p = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);   // P over S
+                const uint32_t d_o = tmem + (uint32_t)(m * 128);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    tc::mma_bf16_ts(d_o, t_p + (uint32_t)(kk * 8),
+                                    tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&ss.pv_done[m][j & 1]);
                 if (j < n_prefix) tc::mma_commit(&ss.v_empty[j % ST]);
                 if (j + 2 < n_tiles) issue_s(j + 2);
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
-            tc::mma_commit(&ss.mma_done);
+            tc::mma_commit(&ss.mma_done[m]);
             const long long t0 = clock64();
-            while (!tc::mbar_try(&ss.mma_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            while (!tc::mbar_try(&ss.mma_done[m], 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
             }
         }
     } else {
@@ -363,7 +357,6 @@ __global__ void __launch_bounds__(NT, 1)
             const uint64_t bits = row < nrows ? ss.anc[p.q_lo + row / rep] : 0ull;
             float m_run = -INFINITY, l_run = 0.0f;
             bool ok = true;
-            uint8_t *pbase = sm + OFF_P + m * 2 * P_TILE;
             for (int j = 0; j < n_tiles; ++j) {
                 const int u = j & 1;
                 if (!warp_wait(&ss.s_full[m][u], (uint32_t)(j >> 1) & 1u, abort)) {
@@ -382,9 +375,6 @@ __global__ void __launch_bounds__(NT, 1)
                         sc[32 + i] = c[i];
                     }
                 }
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.s_free[m][u]);
                 const bool tree = j == n_prefix;         // the last split's final tile
                 const int key0 = k_lo + j * BK;
                 const bool full = !tree && key0 + BK <= k_hi;  // every key of the tile is visible
@@ -443,20 +433,9 @@ __global__ void __launch_bounds__(NT, 1)
                     pk[e] = *reinterpret_cast<uint32_t *>(&h);
                 }
                 const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-                if (j > 1) {
-                    // P buffer j & 1 was last read by the P V of tile j - 2
-                    if (!warp_wait(&ss.pv_done[m][j & 1], (uint32_t)((j - 2) >> 1) & 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(pbase + (j & 1) * P_TILE + tc::sw128_offset(rl, c * 8, P_TILE)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                // P over the S columns it came from (the next S into this buffer waits for P V)
+                tc::tmem_st32u(t_lane + 256u + (uint32_t)(m * 128 + u * 64), pk);
                 l_run += sum;
-                tc::fence_proxy_async_smem();
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ss.p_full[m][j & 1]);
