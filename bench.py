@@ -182,19 +182,19 @@ class Engine:
         self._ev = []
         # events are created once and reused: creating timing events inside the loop is not free
         self._pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                      for _ in range(512)]
+                      for _ in range(4096)]
 
     # -- per-launch timing of the dominant kernels (CUDA events on the launching stream)
     def _timed(self, kind, fn):
-        if not self.timing:
-            fn()
-            return
         if len(self._ev) >= len(self._pool):
-            self.collect()
+            self._pool += [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                           for _ in range(len(self._pool))]
         a, b = self._pool[len(self._ev)]
         a.record()
-        fn()
+        status = fn()
         b.record()
+        if status:
+            raise RuntimeError(f"libeagle3 call failed with status {status}")
         self._ev.append((kind, a, b))
 
     def collect(self):
@@ -209,66 +209,124 @@ class Engine:
         self.kernel_ms = {k: 0.0 for k in self.kernel_ms}
         self.kernel_calls = {k: 0 for k in self.kernel_calls}
 
-    def lin(self, x, w, out, **kw):
-        self._timed("gemm", lambda: self.e3.eagle3_linear(x, w, out, workspace=self.ws_lin, **kw))
-
-    def step(self):
+    # -- the step as a list of prepared C calls: every argument struct is built once, only the fields
+    #    that change between steps (host bounds, the Philox step counter) are patched before a call
+    def _prepare(self):
+        import ctypes
         e3, c = self.e3, self.cfg
+        L = e3._lib.lib()
         B, N, d, D, Hq, Hkv = c["B"], c["N"], c["d"], c["D"], c["Hq"], c["Hkv"]
         R = B * N
-        max_prefix = c["L0"] + c["W"] * self.steps_done
-        # ---- draft: catch-up of the committed positions + dynamic tree
-        if self.ws_draft is None:
-            a = e3._lib.draft_tree_args(self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
-                                        self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
-                                        n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                                        max_draft_len=self.S - c["W"] - 1)
-            self.ws_draft = torch.empty(e3._lib.eagle3_draft_tree_workspace_size(a), dtype=torch.uint8,
-                                        device=self.dev)
-        e3.eagle3_draft_tree(self.draft_w, self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
-                             self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
-                             n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                             max_draft_len=max_prefix - 1, workspace=self.ws_draft, dev_status=self.dev_status)
-        # ---- verify: the target over the tree (positions prefix_len + depth)
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        ops = []
+        keep = []                                       # keep structs alive
+
+        def ws(t):
+            return (ctypes.c_void_p(t.data_ptr()), ctypes.c_size_t(t.numel())) if t is not None else (None, 0)
+
+        # draft
+        da = e3._lib.draft_tree_args(self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
+                                     self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
+                                     n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
+                                     max_draft_len=self.S - c["W"] - 1, dev_status=self.dev_status)
+        self.ws_draft = torch.empty(L.eagle3_draft_tree_workspace_size(ctypes.byref(da)), dtype=torch.uint8,
+                                    device=self.dev)
+        dw = e3._lib.draft_weights(self.draft_w)
+        keep += [da, dw]
+        wp, wb = ws(self.ws_draft)
+        ops.append((None, lambda a=da, w=dw: L.eagle3_draft_tree(ctypes.byref(w), ctypes.byref(a), wp, wb, st),
+                    ("draft", da)))
+
+        def norm(x, w, out, gather=None, tap=None):
+            a = e3._lib.RmsnormArgs(rows=out.shape[0], dim=w.shape[0], n_src=x.shape[0], eps=1e-5, ld_in=x.stride(0),
+                                    ld_out=out.stride(0), ld_tap=0 if tap is None else tap.stride(0),
+                                    input=x.data_ptr(), w=w.data_ptr(),
+                                    gather=None if gather is None else gather.data_ptr(), out=out.data_ptr(),
+                                    tap_out=None if tap is None else tap.data_ptr(),
+                                    dev_status=self.dev_status.data_ptr())
+            keep.append(a)
+            ops.append((None, lambda a=a: L.eagle3_rmsnorm(ctypes.byref(a), st), None))
+
+        lp, lb = ws(self.ws_lin)
+
+        def lin(x, w, out, epi=0, w2=None, res=None):
+            a = e3._lib.LinearArgs(m=x.shape[0], n=w.shape[0], k=x.shape[1], epilogue=epi, splits=0, ld_x=0, ld_w=0,
+                                   ld_out=0, ld_res=0, x=x.data_ptr(), w=w.data_ptr(),
+                                   w2=None if w2 is None else w2.data_ptr(), out=out.data_ptr(),
+                                   residual=None if res is None else res.data_ptr(),
+                                   dev_status=self.dev_status.data_ptr())
+            keep.append(a)
+            ops.append(("gemm", lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st), None))
+
         taps = {t: i for i, t in enumerate(c["taps"])}
-        e3.eagle3_rmsnorm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap_out=self.x)
+        norm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap=self.x)
+        ap, ab = ws(self.ws_attn)
         for l in range(c["layers"]):
             if l > 0:
                 tap = self.aux_tree[:, taps[l] * d:(taps[l] + 1) * d] if l in taps else None
-                e3.eagle3_rmsnorm(self.x, self.norm1[l], self.h, tap_out=tap)
+                norm(self.x, self.norm1[l], self.h, tap=tap)
             qkv = self.qkv[l]
-            self.lin(self.h, self.wqkv[l], qkv)
+            lin(self.h, self.wqkv[l], qkv)
             q = qkv.view(B, N, self.qkv_w)[:, :, : Hq * D].unflatten(2, (Hq, D))
             kt = qkv.view(B, N, self.qkv_w)[:, :, Hq * D:(Hq + Hkv) * D].unflatten(2, (Hkv, D))
             vt = qkv.view(B, N, self.qkv_w)[:, :, (Hq + Hkv) * D:].unflatten(2, (Hkv, D))
-            self._timed("verify_attn", lambda: e3.eagle3_verify_attn(
-                q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
-                self.attn.view(B, N, Hq, D), max_prefix_len=max_prefix, workspace=self.ws_attn,
-                dev_status=self.dev_status))
-            self.lin(self.attn, self.wo[l], self.x, epilogue=e3.EPI_BF16_RESIDUAL, residual=self.x)
-            e3.eagle3_rmsnorm(self.x, self.norm2[l], self.h)
-            self.lin(self.h, self.wg[l], self.act, epilogue=e3.EPI_SWIGLU, w2=self.wu[l])
-            self.lin(self.act, self.wd[l], self.x, epilogue=e3.EPI_BF16_RESIDUAL, residual=self.x)
-        e3.eagle3_rmsnorm(self.x, self.final_norm, self.h)
-        self.lin(self.h, self.lm_head, self.logits, epilogue=e3.EPI_F32)
-        # ---- accept (TOPK rejection sampling at T = 1) and compaction
-        e3.eagle3_accept(e3.TOPK, self.logits.view(B, N, c["V"]), self.tokens, self.parents, self.accept_len,
-                         self.path, self.next_tok, self.next_root, temperature=c["temperature"], seed=c["seed"],
-                         step=self.steps_done, workspace=self.ws_acc, dev_status=self.dev_status)
-        self._compact()
-        self.steps_done += 1
+            va = e3._lib.verify_attn_args(q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
+                                          self.attn.view(B, N, Hq, D), max_prefix_len=c["L0"],
+                                          dev_status=self.dev_status)
+            keep.append(va)
+            ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st), ("verify", va)))
+            lin(self.attn, self.wo[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
+            norm(self.x, self.norm2[l], self.h)
+            lin(self.h, self.wg[l], self.act, epi=e3.EPI_SWIGLU, w2=self.wu[l])
+            lin(self.act, self.wd[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
+        norm(self.x, self.final_norm, self.h)
+        lin(self.h, self.lm_head, self.logits, epi=e3.EPI_F32)
+        aa = e3._lib.AcceptArgs(mode=e3.TOPK, batch=B, n_nodes=N, vocab=c["V"], max_path=c["W"],
+                                temperature=c["temperature"], seed=c["seed"], step=0,
+                                target_logits=self.logits.data_ptr(), draft_logits=None,
+                                tokens=self.tokens.data_ptr(), parents=self.parents.data_ptr(),
+                                accept_len=self.accept_len.data_ptr(), path=self.path.data_ptr(),
+                                emitted=self.next_tok.data_ptr(), next_root=self.next_root.data_ptr(),
+                                dev_status=self.dev_status.data_ptr())
+        keep.append(aa)
+        cp, cb = ws(self.ws_acc)
+        ops.append((None, lambda a=aa: L.eagle3_accept(ctypes.byref(a), cp, cb, st), ("accept", aa)))
+        kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=Hq * D)
+        vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(Hq + Hkv) * D)
+        ca = e3._lib.CompactArgs(n_layers=c["layers"], batch=B, n_nodes=N, n_kv_heads=Hkv, head_dim=D, elem_bytes=2,
+                                 s_max=self.S, max_path=c["W"], cache_layer_stride=B * Hkv * self.S * D,
+                                 tree_layer_stride=R * self.qkv_w, tree_node_stride=self.qkv_w,
+                                 k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
+                                 tree_k=kflat.data_ptr(), tree_v=vflat.data_ptr(), path=self.path.data_ptr(),
+                                 accept_len=self.accept_len.data_ptr(), prefix_len=self.prefix_len.data_ptr(),
+                                 slot_map=self.slot_map.data_ptr(), committed=self.tc.data_ptr(), aux_dim=3 * d,
+                                 aux_tree=self.aux_tree.data_ptr(), aux_out=self.aux_in.data_ptr(),
+                                 dev_status=self.dev_status.data_ptr())
+        keep.append(ca)
+        ops.append((None, lambda a=ca: L.eagle3_compact_kv(ctypes.byref(a), st), None))
+        self._ops, self._keep = ops, keep
 
-    def _compact(self):
+    def step(self):
         c = self.cfg
-        B, N, d = c["B"], c["N"], c["d"]
-        R = B * N
-        # flat views that start at the first key / value element of layer 0
-        kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=c["Hq"] * c["D"])
-        vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(c["Hq"] + c["Hkv"]) * c["D"])
-        self.e3.eagle3_compact_kv(self.k_cache, self.v_cache, kflat, vflat, self.path, self.accept_len,
-                                  self.prefix_len, self.slot_map, aux_tree=self.aux_tree.view(B, N, 3 * d),
-                                  aux_out=self.aux_in, committed=self.tc, tree_node_stride=self.qkv_w,
-                                  tree_layer_stride=R * self.qkv_w, dev_status=self.dev_status)
+        if not hasattr(self, "_ops"):
+            self._prepare()
+        max_prefix = c["L0"] + c["W"] * self.steps_done
+        for kind, call, patch in self._ops:
+            if patch is not None:
+                what, a = patch
+                if what == "verify":
+                    a.max_prefix_len = max_prefix
+                elif what == "draft":
+                    a.max_draft_len = max_prefix - 1
+                elif what == "accept":
+                    a.step = self.steps_done
+            if kind is not None and self.timing:
+                self._timed(kind, call)
+            else:
+                status = call()
+                if status:
+                    raise RuntimeError(f"libeagle3 call failed with status {status}")
+        self.steps_done += 1
 
     def flops_per_step(self):
         """Algorithmic GEMM flops of one step (target verify + draft head)."""

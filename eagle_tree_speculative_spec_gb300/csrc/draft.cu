@@ -64,6 +64,58 @@ E3_DEV void norm_row(const __nv_bfloat16 *x, const __nv_bfloat16 *w, __nv_bfloat
     }
 }
 
+// Vectorised variant: the row is read once with 16-byte loads (CH chunks of 8 values per thread),
+// kept in registers for the scale pass.  Needs dim % 8 == 0 and 16-byte aligned rows.
+template <int CH>
+E3_DEV void norm_row_vec(const __nv_bfloat16 *x, const __nv_bfloat16 *w, __nv_bfloat16 *out, int dim, float eps,
+                         __nv_bfloat16 *tap, float *red) {
+    const int nchunk = dim >> 3;
+    uint4 xv[CH];
+    float ss = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int ch = threadIdx.x + c * (int)blockDim.x;
+        if (ch < nchunk) {
+            xv[c] = *reinterpret_cast<const uint4 *>(x + ch * 8);
+            const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(&xv[c]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float v = __bfloat162float(h[e]);
+                ss += v * v;
+            }
+        }
+    }
+    const float r = rsqrtf(block_sum(ss, red) / (float)dim + eps);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int ch = threadIdx.x + c * (int)blockDim.x;
+        if (ch < nchunk) {
+            const uint4 wv = *reinterpret_cast<const uint4 *>(w + ch * 8);
+            const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(&xv[c]);
+            const __nv_bfloat16 *wh = reinterpret_cast<const __nv_bfloat16 *>(&wv);
+            uint4 o;
+            __nv_bfloat16 *oh = reinterpret_cast<__nv_bfloat16 *>(&o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) oh[e] = __float2bfloat16_rn(__bfloat162float(wh[e]) * (__bfloat162float(h[e]) * r));
+            *reinterpret_cast<uint4 *>(out + ch * 8) = o;
+            if (tap) *reinterpret_cast<uint4 *>(tap + ch * 8) = xv[c];
+        }
+    }
+}
+
+// chooses the vector path when the row and its pointers allow it
+E3_DEV void norm_row_any(const __nv_bfloat16 *x, const __nv_bfloat16 *w, __nv_bfloat16 *out, int dim, float eps,
+                         __nv_bfloat16 *tap, float *red) {
+    const bool vec = (dim % 8 == 0) &&
+                     (((uintptr_t)x | (uintptr_t)w | (uintptr_t)out | (uintptr_t)(tap ? tap : out)) & 15) == 0;
+    const int per = (dim / 8 + (int)blockDim.x - 1) / (int)blockDim.x;
+    if (vec && per <= 1) norm_row_vec<1>(x, w, out, dim, eps, tap, red);
+    else if (vec && per <= 2) norm_row_vec<2>(x, w, out, dim, eps, tap, red);
+    else if (vec && per <= 4) norm_row_vec<4>(x, w, out, dim, eps, tap, red);
+    else if (vec && per <= 8) norm_row_vec<8>(x, w, out, dim, eps, tap, red);
+    else norm_row(x, w, out, dim, eps, tap, red);
+}
+
 struct NormParams {
     int rows, dim, n_src;
     float eps;
@@ -82,8 +134,8 @@ __global__ void __launch_bounds__(NT_NORM) rmsnorm_kernel(const NormParams p) {
         if (threadIdx.x == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TOKEN);
         src = 0;
     }
-    norm_row(p.in + (size_t)src * p.ld_in, p.w, p.out + (size_t)r * p.ld_out, p.dim, p.eps,
-             p.tap ? p.tap + (size_t)r * p.ld_tap : nullptr, red);
+    norm_row_any(p.in + (size_t)src * p.ld_in, p.w, p.out + (size_t)r * p.ld_out, p.dim, p.eps,
+                 p.tap ? p.tap + (size_t)r * p.ld_tap : nullptr, red);
 }
 
 // Draft prologue: a2k[r] = [input_norm(embed[tok[r]]) ; hidden_norm(x[r])], optionally x copied
@@ -113,8 +165,8 @@ __global__ void __launch_bounds__(NT_NORM) draft_prologue_kernel(const PrologueP
     }
     const __nv_bfloat16 *x = p.x + (size_t)(p.x_row ? p.x_row[r] : r) * p.d;
     __nv_bfloat16 *o = p.a2k + (size_t)r * 2 * p.d;
-    norm_row(p.embed + (size_t)tok * p.d, p.w_in, o, p.d, p.eps, nullptr, red);
-    norm_row(x, p.w_hid, o + p.d, p.d, p.eps, p.xres ? p.xres + (size_t)r * p.d : nullptr, red);
+    norm_row_any(p.embed + (size_t)tok * p.d, p.w_in, o, p.d, p.eps, nullptr, red);
+    norm_row_any(x, p.w_hid, o + p.d, p.d, p.eps, p.xres ? p.xres + (size_t)r * p.d : nullptr, red);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -169,7 +221,22 @@ __global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int6
     for (int q = 0; q < KMAX; ++q) best[q] = 0ull;
     const bool vec = ((((uintptr_t)z) & 15) == 0);
     const int n4 = vec ? V / 4 : 0;
-    for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
+    constexpr int U = 4;   // float4 loads in flight per thread
+    int j0 = threadIdx.x;
+    for (; j0 + (U - 1) * NT_TOPK < n4; j0 += U * NT_TOPK) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(z) + j0 + u * NT_TOPK);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * NT_TOPK;
+            insert_best(best, pack_argmax(v[u].x, 4 * j));
+            insert_best(best, pack_argmax(v[u].y, 4 * j + 1));
+            insert_best(best, pack_argmax(v[u].z, 4 * j + 2));
+            insert_best(best, pack_argmax(v[u].w, 4 * j + 3));
+        }
+    }
+    for (int j = j0; j < n4; j += NT_TOPK) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
         insert_best(best, pack_argmax(v.x, 4 * j));
         insert_best(best, pack_argmax(v.y, 4 * j + 1));
@@ -195,6 +262,7 @@ __global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int6
     // fixed-point normaliser over the whole row with m = the row maximum
     const float m = key_to_float((uint32_t)(fin[0] >> 32));
     uint64_t s = 0;
+#pragma unroll 4
     for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
         // each weight is up to 2^31: widen before adding
