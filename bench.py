@@ -109,6 +109,9 @@ class Engine:
         Hq, Hkv, F, Lyr = c["Hq"], c["Hkv"], c["F"], c["layers"]
         self.qkv_w = (Hq + 2 * Hkv) * D
         self.S = c["L0"] + c["W"] * (steps_total + 2) + 64
+        # host-side length bound of every launch, fixed for the run so one captured graph serves every step
+        # (the kernels read the exact per-sequence lengths from device memory)
+        self.max_prefix = c["L0"] + c["W"] * (steps_total + 1)
         g = torch.Generator(device=dev)
         g.manual_seed(1234)
         bf = torch.bfloat16
@@ -171,6 +174,7 @@ class Engine:
         self.next_root = torch.empty(B, dtype=i32, device=dev)
         self.slot_map = torch.empty(B, W, dtype=i32, device=dev)
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        self.step_counter = torch.zeros(1, dtype=torch.int64, device=dev)   # Philox step, advanced on device
         # workspaces (sized once for the largest shapes)
         self.ws_lin = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
         self.ws_attn = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -185,24 +189,29 @@ class Engine:
                       for _ in range(4096)]
 
     # -- per-launch timing of the dominant kernels (CUDA events on the launching stream)
-    def _timed(self, kind, fn):
-        if len(self._ev) >= len(self._pool):
-            self._pool += [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                           for _ in range(len(self._pool))]
-        a, b = self._pool[len(self._ev)]
+    def _timed(self, kind, fn, evs, external=False):
+        if external:
+            a, b = (torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True))
+        else:
+            if len(self._ev) >= len(self._pool):
+                self._pool += [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                               for _ in range(len(self._pool))]
+            a, b = self._pool[len(self._ev)]
         a.record()
         status = fn()
         b.record()
         if status:
             raise RuntimeError(f"libeagle3 call failed with status {status}")
-        self._ev.append((kind, a, b))
+        evs.append((kind, a, b))
 
-    def collect(self):
+    def collect(self, evs=None):
         torch.cuda.synchronize()
-        for kind, a, b in self._ev:
+        for kind, a, b in (self._ev if evs is None else evs):
             self.kernel_ms[kind] += a.elapsed_time(b)
             self.kernel_calls[kind] += 1
-        self._ev = []
+        if evs is None:
+            self._ev = []
 
     def reset_counters(self):
         self.collect()
@@ -228,14 +237,13 @@ class Engine:
         da = e3._lib.draft_tree_args(self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
                                      self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
                                      n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                                     max_draft_len=self.S - c["W"] - 1, dev_status=self.dev_status)
+                                     max_draft_len=self.max_prefix - 1, dev_status=self.dev_status)
         self.ws_draft = torch.empty(L.eagle3_draft_tree_workspace_size(ctypes.byref(da)), dtype=torch.uint8,
                                     device=self.dev)
         dw = e3._lib.draft_weights(self.draft_w)
         keep += [da, dw]
         wp, wb = ws(self.ws_draft)
-        ops.append((None, lambda a=da, w=dw: L.eagle3_draft_tree(ctypes.byref(w), ctypes.byref(a), wp, wb, st),
-                    ("draft", da)))
+        ops.append((None, lambda a=da, w=dw: L.eagle3_draft_tree(ctypes.byref(w), ctypes.byref(a), wp, wb, st)))
 
         def norm(x, w, out, gather=None, tap=None):
             a = e3._lib.RmsnormArgs(rows=out.shape[0], dim=w.shape[0], n_src=x.shape[0], eps=1e-5, ld_in=x.stride(0),
@@ -245,7 +253,7 @@ class Engine:
                                     tap_out=None if tap is None else tap.data_ptr(),
                                     dev_status=self.dev_status.data_ptr())
             keep.append(a)
-            ops.append((None, lambda a=a: L.eagle3_rmsnorm(ctypes.byref(a), st), None))
+            ops.append((None, lambda a=a: L.eagle3_rmsnorm(ctypes.byref(a), st)))
 
         lp, lb = ws(self.ws_lin)
 
@@ -256,7 +264,7 @@ class Engine:
                                    residual=None if res is None else res.data_ptr(),
                                    dev_status=self.dev_status.data_ptr())
             keep.append(a)
-            ops.append(("gemm", lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st), None))
+            ops.append(("gemm", lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st)))
 
         taps = {t: i for i, t in enumerate(c["taps"])}
         norm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap=self.x)
@@ -271,10 +279,10 @@ class Engine:
             kt = qkv.view(B, N, self.qkv_w)[:, :, Hq * D:(Hq + Hkv) * D].unflatten(2, (Hkv, D))
             vt = qkv.view(B, N, self.qkv_w)[:, :, (Hq + Hkv) * D:].unflatten(2, (Hkv, D))
             va = e3._lib.verify_attn_args(q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
-                                          self.attn.view(B, N, Hq, D), max_prefix_len=c["L0"],
+                                          self.attn.view(B, N, Hq, D), max_prefix_len=self.max_prefix,
                                           dev_status=self.dev_status)
             keep.append(va)
-            ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st), ("verify", va)))
+            ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st)))
             lin(self.attn, self.wo[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
             norm(self.x, self.norm2[l], self.h)
             lin(self.h, self.wg[l], self.act, epi=e3.EPI_SWIGLU, w2=self.wu[l])
@@ -287,10 +295,10 @@ class Engine:
                                 tokens=self.tokens.data_ptr(), parents=self.parents.data_ptr(),
                                 accept_len=self.accept_len.data_ptr(), path=self.path.data_ptr(),
                                 emitted=self.next_tok.data_ptr(), next_root=self.next_root.data_ptr(),
-                                dev_status=self.dev_status.data_ptr())
+                                dev_status=self.dev_status.data_ptr(), step_counter=self.step_counter.data_ptr())
         keep.append(aa)
         cp, cb = ws(self.ws_acc)
-        ops.append((None, lambda a=aa: L.eagle3_accept(ctypes.byref(a), cp, cb, st), ("accept", aa)))
+        ops.append((None, lambda a=aa: L.eagle3_accept(ctypes.byref(a), cp, cb, st)))
         kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=Hq * D)
         vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(Hq + Hkv) * D)
         ca = e3._lib.CompactArgs(n_layers=c["layers"], batch=B, n_nodes=N, n_kv_heads=Hkv, head_dim=D, elem_bytes=2,
@@ -303,30 +311,50 @@ class Engine:
                                  aux_tree=self.aux_tree.data_ptr(), aux_out=self.aux_in.data_ptr(),
                                  dev_status=self.dev_status.data_ptr())
         keep.append(ca)
-        ops.append((None, lambda a=ca: L.eagle3_compact_kv(ctypes.byref(a), st), None))
+        ops.append((None, lambda a=ca: L.eagle3_compact_kv(ctypes.byref(a), st)))
         self._ops, self._keep = ops, keep
 
-    def step(self):
-        c = self.cfg
-        if not hasattr(self, "_ops"):
-            self._prepare()
-        max_prefix = c["L0"] + c["W"] * self.steps_done
-        for kind, call, patch in self._ops:
-            if patch is not None:
-                what, a = patch
-                if what == "verify":
-                    a.max_prefix_len = max_prefix
-                elif what == "draft":
-                    a.max_draft_len = max_prefix - 1
-                elif what == "accept":
-                    a.step = self.steps_done
-            if kind is not None and self.timing:
-                self._timed(kind, call)
+    def _issue(self, evs, external=False):
+        for kind, call in self._ops:
+            if kind is not None and evs is not None:
+                self._timed(kind, call, evs, external)
             else:
                 status = call()
                 if status:
                     raise RuntimeError(f"libeagle3 call failed with status {status}")
+
+    def step(self):
+        """One eager step: every C call issued from the host."""
+        if not hasattr(self, "_ops"):
+            self._prepare()
+        self._issue(self._ev if self.timing else None)
         self.steps_done += 1
+
+    def capture(self, n):
+        """Capture n CUDA graphs of one step each (same kernels; each graph owns its timing events, so
+        every replay of a timed loop over the n graphs can be read back afterwards)."""
+        if not hasattr(self, "_ops"):
+            self._prepare()
+        self.graphs = []
+        pool = None
+        for _ in range(n):
+            try:
+                g = torch.cuda.CUDAGraph(keep_graph=True)
+            except TypeError:
+                g = torch.cuda.CUDAGraph()
+            evs = []
+            with torch.cuda.graph(g, pool=pool, stream=torch.cuda.current_stream()):
+                self._issue(evs if self.timing else None, external=True)
+            pool = g.pool()
+            self.graphs.append((g, evs))
+
+    def replay(self, i):
+        self.graphs[i % len(self.graphs)][0].replay()
+        self.steps_done += 1
+
+    def graph_kernels(self):
+        """Kernel nodes of the first captured graph, by function name (driver graph API)."""
+        return graph_kernel_names(self.graphs[0][0])
 
     def flops_per_step(self):
         """Algorithmic GEMM flops of one step (target verify + draft head)."""
@@ -353,6 +381,56 @@ class Engine:
         return kv_prefix + tree_kv + rot_write + q_o
 
 
+class _KernelNodeParams(__import__("ctypes").Structure):
+    import ctypes as _c
+    _fields_ = [("func", _c.c_void_p), ("grid", _c.c_uint * 3), ("block", _c.c_uint * 3), ("smem", _c.c_uint),
+                ("kernel_params", _c.c_void_p), ("extra", _c.c_void_p), ("kern", _c.c_void_p), ("ctx", _c.c_void_p)]
+
+
+def graph_kernel_names(g):
+    """{kernel name: launches} over the kernel nodes of a captured graph (driver graph API), or None."""
+    import ctypes
+    import re
+    try:
+        raw = g.raw_cuda_graph()
+        cu = ctypes.CDLL("libcuda.so.1")
+    except Exception:
+        return None
+    n = ctypes.c_size_t(0)
+    if cu.cuGraphGetNodes(ctypes.c_void_p(raw), None, ctypes.byref(n)) != 0:
+        return None
+    nodes = (ctypes.c_void_p * max(1, n.value))()
+    if cu.cuGraphGetNodes(ctypes.c_void_p(raw), nodes, ctypes.byref(n)) != 0:
+        return None
+    out = {}
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0 or t.value != 0:
+            continue                                        # 0: CU_GRAPH_NODE_TYPE_KERNEL
+        prm = _KernelNodeParams()
+        name = ctypes.c_char_p()
+        if cu.cuGraphKernelNodeGetParams_v2(ctypes.c_void_p(nodes[i]), ctypes.byref(prm)) != 0:
+            key = "?"
+        elif prm.func and cu.cuFuncGetName(ctypes.byref(name), ctypes.c_void_p(prm.func)) == 0 and name.value:
+            key = name.value.decode()
+        elif prm.kern and cu.cuKernelGetName(ctypes.byref(name), ctypes.c_void_p(prm.kern)) == 0 and name.value:
+            key = name.value.decode()
+        else:
+            key = "?"
+        m = re.search(r"([A-Za-z_][A-Za-z0-9_]*_kernel)", key)
+        key = m.group(1) if m else key
+        out[key] = out.get(key, 0) + 1
+    return out
+
+
+def external_events_ok():
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
 def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -366,22 +444,37 @@ def run_gpu(args):
     __graft_entry__.build()
     cfg = dict(CFG)
     cfg["B"] = args.batch
-    eng = Engine(cfg, args.steps * 2 + args.warmup + 2, dev)
+    # all work on one side stream: graph capture needs a stream other than the legacy default one
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    eng = Engine(cfg, args.steps * 2 + max(args.warmup, args.steps) + 3, dev)
+    use_graph = not args.eager
+    if use_graph and not external_events_ok():
+        eng.timing = False                      # timing events cannot live inside a graph: time kernels eagerly
     clocks = ClockSampler(local)
     clocks.start()
-    for _ in range(args.warmup):
-        eng.step()
+    eng.step()                                  # eager warm-up: kernel attributes, tensor maps, first touch
+    if use_graph:
+        eng.capture(args.steps)
+        for i in range(max(args.warmup, args.steps)):   # the first launch of a graph uploads it: do all
+            eng.replay(i)
+    else:
+        for _ in range(args.warmup):
+            eng.step()
     eng.reset_counters()
     torch.cuda.synchronize()
+    prefix_before = int(eng.prefix_len.sum())
     if world > 1:
         dist.barrier()
     wall0 = time.time()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    acc_before = int(eng.steps_done)
     t0.record()
     accepted = torch.zeros((), dtype=torch.int64, device=dev)
-    for _ in range(args.steps):
-        eng.step()
+    for i in range(args.steps):
+        if use_graph:
+            eng.replay(i)
+        else:
+            eng.step()
         accepted += (eng.accept_len.to(torch.int64) + 1).sum()
     t1.record()
     torch.cuda.synchronize()
@@ -389,7 +482,19 @@ def run_gpu(args):
     wall1 = time.time()
     clocks.stop()
     clk = clocks.summary(wall0, wall1)
-    eng.collect()
+    # mean verified prefix over the timed steps (the prefix grows by the accepted length + 1 per step)
+    L_mean = (prefix_before + int(eng.prefix_len.sum())) / (2.0 * cfg["B"])
+    if use_graph and eng.timing:
+        for _, evs in eng.graphs:
+            eng.collect(evs)
+    elif use_graph:                             # per-kernel times from eager steps after the timed region
+        eng.timing = True
+        for _ in range(min(args.steps, 5)):
+            eng.step()
+        eng.collect()
+    else:
+        eng.collect()
+    kernels = eng.graph_kernels() if use_graph else None
     if world > 1:
         dist.barrier()
         tt = torch.tensor([ms], device=dev)
@@ -408,11 +513,14 @@ def run_gpu(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record()
-    for _ in range(args.steps):
+    for i in range(args.steps):
         eng.aux_in.copy_(host_aux, non_blocking=True)
         eng.next_tok.copy_(host_tok, non_blocking=True)
         eng.tc.copy_(host_tc, non_blocking=True)
-        eng.step()
+        if use_graph:
+            eng.replay(i)
+        else:
+            eng.step()
         out_tok.copy_(eng.next_tok, non_blocking=True)
         out_len.copy_(eng.accept_len, non_blocking=True)
     e1.record()
@@ -429,10 +537,12 @@ def run_gpu(args):
     gemm_calls = eng.kernel_calls["gemm"] / max(1, args.steps)
     gemm_tflops = (tgt_f + drf_f) / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
     attn_ms = eng.kernel_ms["verify_attn"] / max(1, eng.kernel_calls["verify_attn"])
-    L_mid = cfg["L0"] + cfg["W"] * (args.warmup + args.steps // 2)
-    attn_gbs = eng.attn_bytes_per_launch(L_mid) / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
+    attn_gbs = eng.attn_bytes_per_launch(L_mean) / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
     tau = float(accepted.item()) / (cfg["B"] * args.steps) - 1.0
-    launches_per_step = gemm_calls + cfg["layers"] * 2 + 3 * cfg["layers"] + 4 + _draft_launches(cfg)
+    if kernels:
+        launches_per_step = sum(kernels.values())
+    else:
+        launches_per_step = gemm_calls + cfg["layers"] * 2 + 3 * cfg["layers"] + 4 + _draft_launches(cfg)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -450,12 +560,14 @@ def run_gpu(args):
         "verify_attn": {"achieved_gbs": round(attn_gbs, 1) if attn_gbs else None, "peak_gbs": hbm,
                         "frac": round(attn_gbs / hbm, 4) if attn_gbs else None,
                         "frac_of_8tbs": round(attn_gbs / 8000.0, 4) if attn_gbs else None,
-                        "ms_per_launch": round(attn_ms, 4), "prefix_len": L_mid},
+                        "ms_per_launch": round(attn_ms, 4), "prefix_len": round(L_mean, 1)},
         "accepted_tokens_per_s": round(float(accepted.item()) * world / (ms / 1e3), 2),
         "tau": round(tau, 4),
         "e2e": {"value": round(units / (e2e_ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(launches_per_step * args.steps)),
+        "launches_per_step": kernels if kernels else {"estimate": launches_per_step},
+        "issue": "cuda-graph replay, one graph per step" if use_graph else "eager C-ABI calls",
         "clocks": clk,
         "dev_status": status,
     }
@@ -690,6 +802,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="issue every C call from the host instead of "
+                                                          "replaying captured CUDA graphs")
     ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)

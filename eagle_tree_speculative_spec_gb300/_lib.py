@@ -46,7 +46,8 @@ class AcceptArgs(ctypes.Structure):
     _fields_ = [("mode", _i32), ("batch", _i32), ("n_nodes", _i32), ("vocab", _i32), ("max_path", _i32),
                 ("temperature", _f32), ("seed", _u64), ("step", _u64),
                 ("target_logits", _p), ("draft_logits", _p), ("tokens", _p), ("parents", _p),
-                ("accept_len", _p), ("path", _p), ("emitted", _p), ("next_root", _p), ("dev_status", _p)]
+                ("accept_len", _p), ("path", _p), ("emitted", _p), ("next_root", _p), ("dev_status", _p),
+                ("step_counter", _p)]
 
 
 class CompactArgs(ctypes.Structure):
@@ -166,7 +167,7 @@ def _workspace(nbytes, device):
 
 # ----------------------------------------------------------------------------- entry points
 def eagle3_accept(mode, target_logits, tokens, parents, accept_len, path, emitted, next_root, *,
-                  draft_logits=None, temperature=1.0, seed=0, step=0, dev_status=None,
+                  draft_logits=None, temperature=1.0, seed=0, step=0, dev_status=None, step_counter=None,
                   workspace=None, stream=None):
     """Acceptance of a verified tree.  target_logits [B, N, V] fp32; tokens / parents [B, N]
     int32; outputs accept_len [B], path / emitted [B, W], next_root [B] int32."""
@@ -179,7 +180,8 @@ def eagle3_accept(mode, target_logits, tokens, parents, accept_len, path, emitte
                    accept_len=_ptr(accept_len, torch.int32, "accept_len"), path=_ptr(path, torch.int32, "path"),
                    emitted=_ptr(emitted, torch.int32, "emitted"),
                    next_root=_ptr(next_root, torch.int32, "next_root"),
-                   dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+                   dev_status=_ptr(dev_status, torch.int32, "dev_status"),
+                   step_counter=_ptr(step_counter, torch.int64, "step_counter"))
     if tuple(tokens.shape) != (B, N) or tuple(parents.shape) != (B, N):
         raise ValueError("tokens and parents must be [B, N]")
     if emitted.shape != path.shape or accept_len.numel() != B or next_root.numel() != B:

@@ -37,6 +37,7 @@ struct Params {
     const int32_t *tokens, *parents;
     int32_t *accept_len, *path, *emitted, *next_root, *dev_status;
     uint32_t *ws_p, *ws_q;   // [B, V] each, SAMPLED only
+    const uint64_t *step_counter;   // when set, the step is read from device memory
 };
 
 struct Smem {
@@ -186,6 +187,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
     const int rank = (int)cluster.block_rank();
     const int b = blockIdx.x / CL;
     const int N = p.N, V = p.V;
+    const uint64_t step = p.step_counter ? *p.step_counter : p.step;
     int phase = 0;
 
     // ---- tree into shared memory, validated identically by every CTA
@@ -289,7 +291,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
         for (int c = node + 1; c < N && next < 0; ++c) {
             if (s.parents[c] != node) continue;
             const int x = s.tokens[c];
-            const U4 rnd = accept_draw(p.seed, p.step, b, node, sib);
+            const U4 rnd = accept_draw(p.seed, step, b, node, sib);
             ++sib;
             if (!sampled) {
                 bool gone = false;
@@ -352,7 +354,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
         if (next >= 0 && threadIdx.x == 0 && rank == 0) flag(p.dev_status, EAGLE3_DEV_PATH_TRUNC);
 
         // ---------------- all children rejected (or a leaf): residual / bonus draw
-        const U4 rnd = accept_draw(p.seed, p.step, b, node, SLOT_RESIDUAL);
+        const U4 rnd = accept_draw(p.seed, step, b, node, SLOT_RESIDUAL);
         const uint64_t r64 = ((uint64_t)rnd.x1 << 32) | rnd.x2;
         const uint64_t target = (uint64_t)(((unsigned __int128)r64 * Sp) >> 64);
         // slice sums of the current weights (TOPK: minus the rejected children in each slice)
@@ -392,6 +394,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
         return;
     }
 }
+
+__global__ void step_increment_kernel(uint64_t *counter) { *counter += 1; }
 
 }  // namespace
 }  // namespace e3
@@ -444,6 +448,13 @@ extern "C" eagle3_status_t eagle3_accept(const eagle3_accept_args_t *a, void *wo
     p.dev_status = a->dev_status;
     p.ws_p = sampled ? (uint32_t *)workspace : nullptr;
     p.ws_q = sampled ? (uint32_t *)workspace + (size_t)a->batch * a->vocab : nullptr;
+    p.step_counter = a->step_counter;
     accept_kernel<<<dim3(a->batch * CL), dim3(NT), 0, (cudaStream_t)stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? EAGLE3_OK : EAGLE3_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    if (a->step_counter) {
+        // stream-ordered after every CTA of the acceptance kernel has read the counter
+        step_increment_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(a->step_counter);
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
+    return EAGLE3_OK;
 }

@@ -78,8 +78,10 @@ struct SmemStatic {
     // every per-tile barrier is double-buffered by tile parity: a producer may run one tile ahead
     // of its consumer, and a phase that completes twice before it is awaited would be lost
     uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], mma_done[2];
+    uint64_t q_ready;               // the softmax warps have staged Q (and the tree tile)
     uint64_t anc[64];
     int32_t pos[64];
+    int32_t par[64];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -98,43 +100,37 @@ E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// rotate-half RoPE of one 128-wide row into a 128B-swizzled tile row (and optionally back to
-// global memory); lane j handles the pairs (j, j + 64) and (j + 32, j + 96)
-E3_DEV void rope_row_sw(const __nv_bfloat16 *src, uint8_t *tile, int row, uint32_t block_bytes,
-                        __nv_bfloat16 *writeback, float pos, const float *inv_freq, int lane) {
-    __nv_bfloat16 x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = src[lane + 32 * u];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int j = lane + 32 * u;
-        const float x1 = __bfloat162float(x[u]), x2 = __bfloat162float(x[u + 2]);
-        float sn, cs;
-        sincosf(__fmul_rn(pos, inv_freq[j]), &sn, &cs);
-        const __nv_bfloat16 o1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
-        const __nv_bfloat16 o2 = __float2bfloat16_rn(x2 * cs + x1 * sn);
-        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, j, block_bytes)) = o1;
-        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, j + 64, block_bytes)) = o2;
-        if (writeback) {
-            writeback[j] = o1;
-            writeback[j + 64] = o2;
-        }
-    }
+// Rows are staged 16 bytes at a time: a 128-wide bf16 row is two 64-column blocks of eight 16-byte
+// chunks, and a 128-byte swizzle keeps each chunk contiguous.  Lane group c (0..7) of a row owns
+// chunk c of both blocks, i.e. the rotate-half pairs (8c + e, 64 + 8c + e), e = 0..7.
+E3_DEV uint4 ld16(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+E3_DEV void st_chunk(uint8_t *tile, int row, int chunk, uint32_t block_bytes, uint4 v) {
+    *reinterpret_cast<uint4 *>(tile + tc::sw128_offset(row, chunk * 8, block_bytes)) = v;
 }
 
-E3_DEV void copy_row_sw(const __nv_bfloat16 *src, uint8_t *tile, int row, uint32_t block_bytes, int lane) {
+// cos / sin of pos * inv_freq[8c + e], e = 0..7
+E3_DEV void rope_angles(float pos, const float *inv_freq, int c, float cs[8], float sn[8]) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int c = lane + 32 * u;
-        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, c, block_bytes)) = src[c];
-    }
+    for (int e = 0; e < 8; ++e) sincosf(__fmul_rn(pos, inv_freq[8 * c + e]), &sn[e], &cs[e]);
 }
 
-E3_DEV void zero_row_sw(uint8_t *tile, int row, uint32_t block_bytes, int lane) {
+// rotate-half RoPE of chunk pair c of one row: (x1, x2) -> (x1 cos - x2 sin, x2 cos + x1 sin)
+E3_DEV void rope_chunks(uint4 &lo, uint4 &hi, const float cs[8], const float sn[8]) {
+    const __nv_bfloat162 *a = reinterpret_cast<const __nv_bfloat162 *>(&lo);
+    const __nv_bfloat162 *bb = reinterpret_cast<const __nv_bfloat162 *>(&hi);
+    uint4 o1, o2;
+    __nv_bfloat162 *r1 = reinterpret_cast<__nv_bfloat162 *>(&o1);
+    __nv_bfloat162 *r2 = reinterpret_cast<__nv_bfloat162 *>(&o2);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<__nv_bfloat16 *>(tile + tc::sw128_offset(row, lane + 32 * u, block_bytes)) =
-            __float2bfloat16_rn(0.0f);
+    for (int e = 0; e < 4; ++e) {
+        const float2 x1 = __bfloat1622float2(a[e]), x2 = __bfloat1622float2(bb[e]);
+        const float c0 = cs[2 * e], c1 = cs[2 * e + 1], s0 = sn[2 * e], s1 = sn[2 * e + 1];
+        r1[e] = __floats2bfloat162_rn(x1.x * c0 - x2.x * s0, x1.y * c1 - x2.y * s1);
+        r2[e] = __floats2bfloat162_rn(x2.x * c0 + x1.x * s0, x2.y * c1 + x1.y * s1);
+    }
+    lo = o1;
+    hi = o2;
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -161,6 +157,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int n_prefix = (k_hi - k_lo + BK - 1) / BK;
     const int n_tiles = n_prefix + (last ? 1 : 0);
 
+    // ---- phase A: barriers, TMEM, raw tree description into shared memory
     if (tid == 0) {
         for (int s = 0; s < ST; ++s) {
             tc::mbar_init(&ss.k_full[s], 1);
@@ -177,63 +174,21 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mbar_init(&ss.mma_done[0], 1);
         tc::mbar_init(&ss.mma_done[1], 1);
+        tc::mbar_init(&ss.q_ready, 8);
         ss.abort_flag = 0;
         tc::fence_barrier_init();
-        // tree slots: ancestor-or-self bits and RoPE positions
-        if (p.parents) {
-            int bad = 0, depth[64];
-            for (int i = 0; i < nk; ++i) {
-                const int par = p.parents[(size_t)b * p.n_slots + i];
-                if ((i == 0 && par != -1) || (i > 0 && (par < 0 || par >= i))) {
-                    bad = 1;
-                    depth[i] = 0;
-                    ss.anc[i] = 1ull << i;
-                } else {
-                    depth[i] = i ? depth[par] + 1 : 0;
-                    ss.anc[i] = (i ? ss.anc[par] : 0ull) | (1ull << i);
-                }
-                ss.pos[i] = L + depth[i];
-            }
-            if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
-        } else {
-            for (int i = 0; i < nk; ++i) {
+    }
+    if (warp == 1) tc::tmem_alloc(&ss.tmem_base, 512);
+    if (warp == 2 || warp == 3) {
+        const int i = tid - 64;
+        if (i < nk) {
+            if (p.parents) {
+                ss.par[i] = p.parents[(size_t)b * p.n_slots + i];
+            } else {
                 ss.anc[i] = p.anc[(size_t)b * p.anc_sb + i] & (nk >= 64 ? ~0ull : ((1ull << nk) - 1));
                 ss.pos[i] = p.pos[(size_t)b * p.pos_sb + i];
             }
         }
-    }
-    if (warp == 1) tc::tmem_alloc(&ss.tmem_base, 512);
-    __syncthreads();
-
-    // ---- softmax warps stage Q (rotated) and, in the last split, the tree tile
-    if (warp >= 2 && warp < 10) {
-        const int w8 = warp - 2;
-        for (int r = w8; r < n_mt * MT; r += 8) {
-            uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
-            if (r < nrows) {
-                const int i = p.q_lo + r / rep, hh = r % rep;
-                const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
-                rope_row_sw(src, tile, r % MT, Q_TILE / 2, nullptr, (float)ss.pos[i], p.inv_freq, lane);
-            } else {
-                zero_row_sw(tile, r % MT, Q_TILE / 2, lane);
-            }
-        }
-        if (last) {
-            uint8_t *tk = sm + OFF_TREE, *tv = sm + OFF_TREE + KV_TILE;
-            for (int i = w8; i < BK; i += 8) {
-                if (i < nk) {
-                    __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
-                    const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
-                    if (i >= p.q_lo) rope_row_sw(kg, tk, i, KV_TILE / 2, kg, (float)ss.pos[i], p.inv_freq, lane);
-                    else copy_row_sw(kg, tk, i, KV_TILE / 2, lane);
-                    copy_row_sw(vg, tv, i, KV_TILE / 2, lane);
-                } else {
-                    zero_row_sw(tk, i, KV_TILE / 2, lane);
-                    zero_row_sw(tv, i, KV_TILE / 2, lane);
-                }
-            }
-        }
-        tc::fence_proxy_async_smem();
     }
     tc::fence_before();
     __syncthreads();
@@ -289,6 +244,8 @@ __global__ void __launch_bounds__(NT, 1)
             auto v_tile = [&](int j) -> uint8_t * {
                 return j < n_prefix ? sm + OFF_KV + (ST + j % ST) * KV_TILE : sm + OFF_TREE + KV_TILE;
             };
+            // Q and the tree tile are written by the softmax warps (generic proxy, fenced)
+            if (!tc::mbar_wait(&ss.q_ready, 0, abort)) ok = false;
             auto issue_s = [&](int j) {
                 if (j < n_prefix) {
                     if (!tc::mbar_wait(&ss.k_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
@@ -315,7 +272,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (j < n_prefix) tc::mma_commit(&ss.k_empty[j % ST]);   // K stage free once S is done
             };
             // two S tiles in flight; each iteration: P V of tile j as soon as its P is ready, then S(j + 2)
-            issue_s(0);
+            if (ok) issue_s(0);
             if (n_tiles > 1 && ok) issue_s(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 if (j < n_prefix && !tc::mbar_wait(&ss.v_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
@@ -348,6 +305,86 @@ __global__ void __launch_bounds__(NT, 1)
         }
     } else {
         // ------------------------------------------------------------------ softmax warps
+        const int w8 = warp - 2;
+        // ancestor-or-self bits and positions: slot i walks its own parent chain (parents < i)
+        if (p.parents && w8 < 2) {
+            const int i = tid - 64;
+            if (i < nk) {
+                auto invalid = [&](int j) {
+                    const int pj = ss.par[j];
+                    return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
+                };
+                uint64_t bits = 1ull << i;
+                int d = 0, j = i;
+                const bool bad = invalid(i);
+                while (j > 0 && !invalid(j)) {
+                    j = ss.par[j];
+                    bits |= 1ull << j;
+                    ++d;
+                }
+                ss.anc[i] = bits;
+                ss.pos[i] = L + d;
+                if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+            }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight softmax warps only
+        {
+            const int c = lane & 7, sub = lane >> 3;
+            // Q rows (row = slot * rep + head), rotated at the slot's position
+            for (int sl = w8; sl < nq; sl += 8) {
+                const int i = p.q_lo + sl;
+                float cs[8], sn[8];
+                rope_angles((float)ss.pos[i], p.inv_freq, c, cs, sn);
+                for (int hh = sub; hh < rep; hh += 4) {
+                    const int r = sl * rep + hh;
+                    const __nv_bfloat16 *src =
+                        p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
+                    uint4 lo = ld16(src + 8 * c), hi = ld16(src + 64 + 8 * c);
+                    rope_chunks(lo, hi, cs, sn);
+                    uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
+                    st_chunk(tile, r % MT, c, Q_TILE / 2, lo);
+                    st_chunk(tile, r % MT, c + 8, Q_TILE / 2, hi);
+                }
+            }
+            // zero rows of the last M tile
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int k = (tid - 64); k < (n_mt * MT - nrows) * 16; k += 256) {
+                const int r = nrows + k / 16, ch = k % 16;
+                st_chunk(sm + OFF_Q + (r / MT) * Q_TILE, r % MT, ch, Q_TILE / 2, z);
+            }
+            if (last) {
+                // the tree tile: keys of the query slots rotated (and written back), others copied
+                uint8_t *tk = sm + OFF_TREE, *tv = sm + OFF_TREE + KV_TILE;
+                for (int i = w8 * 4 + sub; i < BK; i += 32) {
+                    if (i < nk) {
+                        __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
+                        const __nv_bfloat16 *vg =
+                            p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
+                        uint4 klo = ld16(kg + 8 * c), khi = ld16(kg + 64 + 8 * c);
+                        const uint4 vlo = ld16(vg + 8 * c), vhi = ld16(vg + 64 + 8 * c);
+                        if (i >= p.q_lo) {
+                            float cs[8], sn[8];
+                            rope_angles((float)ss.pos[i], p.inv_freq, c, cs, sn);
+                            rope_chunks(klo, khi, cs, sn);
+                            *reinterpret_cast<uint4 *>(kg + 8 * c) = klo;
+                            *reinterpret_cast<uint4 *>(kg + 64 + 8 * c) = khi;
+                        }
+                        st_chunk(tk, i, c, KV_TILE / 2, klo);
+                        st_chunk(tk, i, c + 8, KV_TILE / 2, khi);
+                        st_chunk(tv, i, c, KV_TILE / 2, vlo);
+                        st_chunk(tv, i, c + 8, KV_TILE / 2, vhi);
+                    } else {
+                        st_chunk(tk, i, c, KV_TILE / 2, z);
+                        st_chunk(tk, i, c + 8, KV_TILE / 2, z);
+                        st_chunk(tv, i, c, KV_TILE / 2, z);
+                        st_chunk(tv, i, c + 8, KV_TILE / 2, z);
+                    }
+                }
+            }
+            tc::fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ss.q_ready);
+        }
         const int m = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int rl = quarter * 32 + lane;              // row within the M tile
@@ -591,6 +628,13 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
     const int splits = plan_splits(a.B * a.Hkv, a.max_prefix, a.num_splits, sm_count_cached());
     const size_t need = tree_attn_workspace(a);
     if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
+    // rows of q / tree k / tree v / out are moved 16 bytes at a time
+    const int64_t strides[] = {a.q_sb, a.q_si, a.k_sb, a.k_si, a.v_sb, a.v_si, a.o_sb, a.o_si};
+    for (int64_t st : strides)
+        if (st % 8) return EAGLE3_ERR_INVALID_ARGUMENT;
+    const void *row_bases[] = {a.q, a.k, a.v, a.out};
+    for (const void *r : row_bases)
+        if ((uintptr_t)r & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
     Params p;
     p.B = a.B;
     p.n_slots = a.n_slots;

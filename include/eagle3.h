@@ -112,6 +112,9 @@ typedef struct {
     int32_t *emitted;           /* [B, W] out: tokens of path[1..n], then next_root, then -1           */
     int32_t *next_root;         /* [B] out: correction / bonus token (the next step's root)           */
     int32_t *dev_status;        /* [1] optional device word for EAGLE3_DEV_* bits (may be NULL)       */
+    uint64_t *step_counter;     /* [1] optional device word: when not NULL the Philox step is read from
+                                   it (the `step` field is ignored) and it is incremented after the
+                                   call, so a captured CUDA graph draws fresh numbers on every replay */
 } eagle3_accept_args_t;
 
 size_t eagle3_accept_workspace_size(const eagle3_accept_args_t *args);

@@ -118,3 +118,34 @@ def test_accept_full_size(mode):
     rows = [0, 1, 17, 31, 42, 63] if mode == oacc.SAMPLED else list(range(0, 64, 4)) + [63]
     _compare(got, mode, zt, zd, tokens, parents, W, rows, seed=1)
     assert (got["accept_len"] >= 0).all() and (got["accept_len"] <= 6).all()
+
+
+@pytest.mark.parametrize("mode", [oacc.TOPK, oacc.SAMPLED])
+def test_accept_device_step_counter(mode):
+    """A device step counter replaces the host `step` and advances by one per call, so a captured graph
+    draws fresh numbers on every replay: three replays give the oracle's results for steps s, s+1, s+2."""
+    from eagle_tree_speculative_spec_gb300 import eagle3_accept
+    dev = require_gpu()
+    B, N, V, W = 4, 30, 2000, 8
+    zt, zd, parents, tokens = synth.accept_batch(13, B, N, V, sampled=(mode == oacc.SAMPLED))
+    t = lambda a, dt: torch.as_tensor(np.ascontiguousarray(a), dtype=dt, device=dev)
+    zt_d, tok_d, par_d = t(zt, torch.float32), t(tokens, torch.int32), t(parents, torch.int32)
+    zd_d = t(zd, torch.float32) if mode == oacc.SAMPLED else None
+    s0 = 2**32 - 2                                  # the carry into the counter's high word is exercised
+    counter = torch.tensor([s0], dtype=torch.int64, device=dev)
+    out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+               path=torch.empty(B, W, dtype=torch.int32, device=dev),
+               emitted=torch.empty(B, W, dtype=torch.int32, device=dev),
+               next_root=torch.empty(B, dtype=torch.int32, device=dev))
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        eagle3_accept(mode, zt_d, tok_d, par_d, out["accept_len"], out["path"], out["emitted"], out["next_root"],
+                      draft_logits=zd_d, seed=3, step=12345, step_counter=counter,
+                      stream=torch.cuda.current_stream())
+    for r in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        got = {k: v.cpu().numpy() for k, v in out.items()}
+        _compare(got, mode, zt, zd, tokens, parents, W, range(B), seed=3, step=s0 + r)
+    assert int(counter.item()) == s0 + 3
