@@ -468,6 +468,7 @@ def run_gpu(args):
         dist.barrier()
     wall0 = time.time()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t0.record()
     accepted = torch.zeros((), dtype=torch.int64, device=dev)
     for i in range(args.steps):
@@ -476,9 +477,11 @@ def run_gpu(args):
         else:
             eng.step()
         accepted += (eng.accept_len.to(torch.int64) + 1).sum()
+        step_ev[i].record()
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    step_ms = [round((t0 if i == 0 else step_ev[i - 1]).elapsed_time(step_ev[i]), 3) for i in range(args.steps)]
     wall1 = time.time()
     clocks.stop()
     clk = clocks.summary(wall0, wall1)
@@ -569,6 +572,7 @@ def run_gpu(args):
         "launches_per_step": kernels if kernels else {"estimate": launches_per_step},
         "issue": "cuda-graph replay, one graph per step" if use_graph else "eager C-ABI calls",
         "clocks": clk,
+        "step_ms": step_ms,
         "dev_status": status,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -209,48 +209,100 @@ E3_DEV void insert_best(uint64_t (&best)[KMAX], uint64_t v) {
     }
 }
 
+// Row top-k by (value desc, index asc) and the row's fixed-point normaliser.  One CTA per row.
+// Each warp keeps its current top-k in shared memory and the packed key of its k-th best as a
+// threshold: an element below the threshold cannot enter the top-k, so it costs one compare;
+// the rest are appended (ballot-compacted) to a per-warp buffer that is merged into the list
+// only when it fills up.  For a row in random order about k ln(n / k) elements pass.
+constexpr int TK_CAP = 256;   // candidate buffer per warp (two float4 groups of a warp)
+
+// merge a warp's candidate buffer into its list (KMAX entries, the first k meaningful); returns
+// the new k-th best (0 while fewer than k candidates have been seen)
+E3_DEV uint64_t warp_flush(uint64_t *list, const uint64_t *cand, int cnt, int k, int lane) {
+    uint64_t best[KMAX];
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) best[q] = 0ull;
+#pragma unroll
+    for (int t = 0; t < (KMAX + TK_CAP + 31) / 32; ++t) {
+        const int i = lane + 32 * t;
+        if (i < KMAX + cnt) insert_best(best, i < KMAX ? list[i] : cand[i - KMAX]);
+    }
+    __syncwarp();
+    uint64_t res[KMAX];
+    warp_merge(best, res, k);
+    if (lane == 0)
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) list[q] = res[q];
+    __syncwarp();
+    return list[k - 1];   // (selecting res[k - 1] in registers would demote res to local memory)
+}
+
 __global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int64_t ld, int V, int k,
                                                        int32_t *out_tok, float *out_lq) {
+    __shared__ uint64_t buf[NT_TOPK / 32][TK_CAP];
     __shared__ uint64_t wres[NT_TOPK / 32][KMAX];
     __shared__ uint64_t fin[KMAX];
     __shared__ uint64_t sred[NT_TOPK / 32];
     const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float *z = logits + (size_t)row * ld;
-    uint64_t best[KMAX];
-#pragma unroll
-    for (int q = 0; q < KMAX; ++q) best[q] = 0ull;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    if (lane < KMAX) wres[warp][lane] = 0ull;
+    __syncwarp();
+    uint64_t tau = 0ull;           // packed key of the warp's k-th best so far (0: fewer than k)
+    float tau_f = key_to_float(0u);  // a NaN: every value passes `!(v < tau_f)`
+    int cnt = 0;                   // warp-uniform fill of buf[warp]
+
+    // merge the buffer into the warp's list and raise the threshold
+    auto flush = [&]() {
+        tau = warp_flush(wres[warp], buf[warp], cnt, k, lane);
+        tau_f = key_to_float((uint32_t)(tau >> 32));
+        cnt = 0;
+    };
+    // one element per lane: append it when it can still enter the top-k (all lanes call this)
+    auto offer = [&](float v, uint32_t idx, bool valid) {
+        bool pass = valid && !(v < tau_f);
+        uint64_t key = 0ull;
+        if (pass) {
+            key = pack_argmax(v, idx);
+            pass = key > tau;
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, pass);
+        if (pass) buf[warp][cnt + __popc(m & lt_mask)] = key;
+        cnt += __popc(m);
+    };
+
     const bool vec = ((((uintptr_t)z) & 15) == 0);
     const int n4 = vec ? V / 4 : 0;
     constexpr int U = 4;   // float4 loads in flight per thread
-    int j0 = threadIdx.x;
-    for (; j0 + (U - 1) * NT_TOPK < n4; j0 += U * NT_TOPK) {
+    const int n4u = n4 / (U * NT_TOPK) * (U * NT_TOPK);   // float4 groups every lane has
+    for (int j0 = threadIdx.x; j0 < n4u; j0 += U * NT_TOPK) {
         float4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(z) + j0 + u * NT_TOPK);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * NT_TOPK;
-            insert_best(best, pack_argmax(v[u].x, 4 * j));
-            insert_best(best, pack_argmax(v[u].y, 4 * j + 1));
-            insert_best(best, pack_argmax(v[u].z, 4 * j + 2));
-            insert_best(best, pack_argmax(v[u].w, 4 * j + 3));
+            const bool any = !(v[u].x < tau_f) || !(v[u].y < tau_f) || !(v[u].z < tau_f) || !(v[u].w < tau_f);
+            if (!__any_sync(0xffffffffu, any)) continue;
+            if (cnt + 4 * 32 > TK_CAP) flush();
+            const uint32_t j = 4u * (uint32_t)(j0 + u * NT_TOPK);
+            offer(v[u].x, j, true);
+            offer(v[u].y, j + 1, true);
+            offer(v[u].z, j + 2, true);
+            offer(v[u].w, j + 3, true);
         }
     }
-    for (int j = j0; j < n4; j += NT_TOPK) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
-        insert_best(best, pack_argmax(v.x, 4 * j));
-        insert_best(best, pack_argmax(v.y, 4 * j + 1));
-        insert_best(best, pack_argmax(v.z, 4 * j + 2));
-        insert_best(best, pack_argmax(v.w, 4 * j + 3));
+    // the rest, one element per lane per round, with warp-uniform trip counts
+    for (int base = 4 * n4u; base < V; base += NT_TOPK) {
+        const int i = base + threadIdx.x;
+        const bool valid = i < V;
+        const float v = valid ? __ldg(z + i) : 0.0f;
+        if (cnt + 32 > TK_CAP) flush();
+        offer(v, (uint32_t)i, valid);
     }
-    for (int i = 4 * n4 + threadIdx.x; i < V; i += NT_TOPK) insert_best(best, pack_argmax(__ldg(z + i), i));
-    uint64_t res[KMAX];
-    warp_merge(best, res, k);
-    if (lane == 0)
-#pragma unroll
-        for (int q = 0; q < KMAX; ++q) wres[warp][q] = res[q];
+    if (cnt > 0) flush();
     __syncthreads();
     if (warp == 0) {
+        uint64_t best[KMAX], res[KMAX];
 #pragma unroll
         for (int q = 0; q < KMAX; ++q) best[q] = lane < NT_TOPK / 32 ? wres[lane][q] : 0ull;
         warp_merge(best, res, k);
