@@ -41,6 +41,7 @@ constexpr int NWARP = 12;             // 0: K loads, 1 and 11: MMA (one per M ti
 constexpr int NT = NWARP * 32;
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
+constexpr int ROPE_TABLE_POS = 32;    // positions in the per-CTA angle table (16 KB of float2)
 
 constexpr uint32_t Q_TILE = MT * D * 2;          // 32 KB: two 64-column blocks of 16 KB
 constexpr uint32_t KV_TILE = BK * D * 2;         // 16 KB: two 64-column blocks of 8 KB
@@ -49,6 +50,7 @@ constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE;
 constexpr uint32_t OFF_TREE = OFF_KV + ST * 2 * KV_TILE;
 constexpr uint32_t SMEM_DYN = OFF_TREE + 2 * KV_TILE + 1024;   // + alignment slack
 static_assert(SMEM_DYN + 1024 <= 232448, "shared memory budget");
+static_assert(ROPE_TABLE_POS * (D / 2) * sizeof(float2) <= KV_TILE, "angle table fits the tree-V tile");
 
 struct Params {
     int B, n_slots, q_lo, q_hi, Hq, Hkv, S, splits, tiles_per_split, rep, max_prefix;
@@ -330,20 +332,82 @@ __global__ void __launch_bounds__(NT, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight softmax warps only
         {
             const int c = lane & 7, sub = lane >> 3;
-            // Q rows (row = slot * rep + head), rotated at the slot's position
-            for (int sl = w8; sl < nq; sl += 8) {
-                const int i = p.q_lo + sl;
-                float cs[8], sn[8];
-                rope_angles((float)ss.pos[i], p.inv_freq, c, cs, sn);
-                for (int hh = sub; hh < rep; hh += 4) {
-                    const int r = sl * rep + hh;
-                    const __nv_bfloat16 *src =
-                        p.q + (size_t)b * p.q_sb + (size_t)i * p.q_si + ((size_t)g * rep + hh) * D;
-                    uint4 lo = ld16(src + 8 * c), hi = ld16(src + 64 + 8 * c);
-                    rope_chunks(lo, hi, cs, sn);
-                    uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
-                    st_chunk(tile, r % MT, c, Q_TILE / 2, lo);
-                    st_chunk(tile, r % MT, c + 8, Q_TILE / 2, hi);
+            // RoPE angles: the slots of a tree share few positions (prefix length + depth), so
+            // cos / sin of every position in [pos_lo, pos_lo + span) are computed once per CTA into
+            // the tree-V tile area (free until the tree V rows are staged below); a position
+            // outside the table is computed directly.  Same arguments, so the same values.
+            int pos_lo = 0x7fffffff, pos_hi = -1;
+            for (int i = 0; i < nk; ++i) {
+                pos_lo = min(pos_lo, ss.pos[i]);
+                pos_hi = max(pos_hi, ss.pos[i]);
+            }
+            const int span = min(pos_hi - pos_lo + 1, ROPE_TABLE_POS);
+            float2 *table = reinterpret_cast<float2 *>(sm + OFF_TREE + KV_TILE);
+            for (int e = tid - 64; e < span * (D / 2); e += 256) {
+                float sn, cs;
+                sincosf(__fmul_rn((float)(pos_lo + e / (D / 2)), p.inv_freq[e % (D / 2)]), &sn, &cs);
+                table[e] = make_float2(cs, sn);
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            auto angles = [&](int pos, float cs[8], float sn[8]) {
+                const int d = pos - pos_lo;
+                if (d >= 0 && d < span) {
+                    const float4 *t4 = reinterpret_cast<const float4 *>(table + d * (D / 2) + 8 * c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float4 v = t4[u];
+                        cs[2 * u] = v.x;
+                        sn[2 * u] = v.y;
+                        cs[2 * u + 1] = v.z;
+                        sn[2 * u + 1] = v.w;
+                    }
+                } else {
+                    rope_angles((float)pos, p.inv_freq, c, cs, sn);
+                }
+            };
+            // tree rows of the last split: issued first, used after the Q rows
+            uint4 kl[2], kh[2], vl[2], vh[2];
+            if (last) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int i = w8 * 4 + sub + 32 * t;
+                    if (i < nk) {
+                        const __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
+                        const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
+                        kl[t] = ld16(kg + 8 * c);
+                        kh[t] = ld16(kg + 64 + 8 * c);
+                        vl[t] = ld16(vg + 8 * c);
+                        vh[t] = ld16(vg + 64 + 8 * c);
+                    }
+                }
+            }
+            // Q rows (row = slot * rep + head), rotated at the slot's position.  Warp w8 takes the
+            // slots w8 + 8 t (t < 8, i.e. all of them, nq <= 64), lane group `sub` the heads
+            // sub + 4 h; all of a warp's loads are issued before the first is used.
+            for (int hh = sub, h4 = 0; h4 * 4 < rep; hh += 4, ++h4) {
+                uint4 lo[8], hi[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int sl = w8 + 8 * t;
+                    if (sl < nq && hh < rep) {
+                        const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)(p.q_lo + sl) * p.q_si +
+                                                   ((size_t)g * rep + hh) * D;
+                        lo[t] = ld16(src + 8 * c);
+                        hi[t] = ld16(src + 64 + 8 * c);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const int sl = w8 + 8 * t;
+                    if (sl < nq && hh < rep) {
+                        float cs[8], sn[8];
+                        angles(ss.pos[p.q_lo + sl], cs, sn);
+                        rope_chunks(lo[t], hi[t], cs, sn);
+                        const int r = sl * rep + hh;
+                        uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
+                        st_chunk(tile, r % MT, c, Q_TILE / 2, lo[t]);
+                        st_chunk(tile, r % MT, c + 8, Q_TILE / 2, hi[t]);
+                    }
                 }
             }
             // zero rows of the last M tile
@@ -353,29 +417,37 @@ __global__ void __launch_bounds__(NT, 1)
                 st_chunk(sm + OFF_Q + (r / MT) * Q_TILE, r % MT, ch, Q_TILE / 2, z);
             }
             if (last) {
-                // the tree tile: keys of the query slots rotated (and written back), others copied
+                // the tree tile: keys of the query slots rotated (and written back), others copied;
+                // then the values, over the angle table
                 uint8_t *tk = sm + OFF_TREE, *tv = sm + OFF_TREE + KV_TILE;
-                for (int i = w8 * 4 + sub; i < BK; i += 32) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int i = w8 * 4 + sub + 32 * t;
                     if (i < nk) {
                         __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
-                        const __nv_bfloat16 *vg =
-                            p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
-                        uint4 klo = ld16(kg + 8 * c), khi = ld16(kg + 64 + 8 * c);
-                        const uint4 vlo = ld16(vg + 8 * c), vhi = ld16(vg + 64 + 8 * c);
+                        uint4 klo = kl[t], khi = kh[t];
                         if (i >= p.q_lo) {
                             float cs[8], sn[8];
-                            rope_angles((float)ss.pos[i], p.inv_freq, c, cs, sn);
+                            angles(ss.pos[i], cs, sn);
                             rope_chunks(klo, khi, cs, sn);
                             *reinterpret_cast<uint4 *>(kg + 8 * c) = klo;
                             *reinterpret_cast<uint4 *>(kg + 64 + 8 * c) = khi;
                         }
                         st_chunk(tk, i, c, KV_TILE / 2, klo);
                         st_chunk(tk, i, c + 8, KV_TILE / 2, khi);
-                        st_chunk(tv, i, c, KV_TILE / 2, vlo);
-                        st_chunk(tv, i, c + 8, KV_TILE / 2, vhi);
                     } else {
                         st_chunk(tk, i, c, KV_TILE / 2, z);
                         st_chunk(tk, i, c + 8, KV_TILE / 2, z);
+                    }
+                }
+                asm volatile("bar.sync 1, 256;" ::: "memory");   // every table read is done
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int i = w8 * 4 + sub + 32 * t;
+                    if (i < nk) {
+                        st_chunk(tv, i, c, KV_TILE / 2, vl[t]);
+                        st_chunk(tv, i, c + 8, KV_TILE / 2, vh[t]);
+                    } else {
                         st_chunk(tv, i, c, KV_TILE / 2, z);
                         st_chunk(tv, i, c + 8, KV_TILE / 2, z);
                     }

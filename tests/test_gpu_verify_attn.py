@@ -57,6 +57,15 @@ def test_verify_node_counts(N):
     _check(inp, got, range(2))
 
 
+@pytest.mark.parametrize("N", [33, 64])
+def test_verify_deep_chain(N):
+    """A chain of N nodes has N distinct RoPE positions: the kernel's per-block angle table holds 32,
+    the deeper positions take the direct path."""
+    inp = synth.verify_attn_batch(34, 2, N, 32, 8, 128, [90, 5], S_max=200)
+    inp["parents"] = np.stack([synth.chain_tree(N)] * 2)
+    _check(inp, _run(inp, 90), range(2))
+
+
 def test_verify_other_gqa_ratio():
     inp = synth.verify_attn_batch(33, 2, 40, 16, 2, 128, [130, 77], S_max=200)   # rep 8: 320 rows > 256
     with pytest.raises(Exception):
