@@ -255,11 +255,9 @@ __global__ void __launch_bounds__(NT, 1)
                         return;
                     }
                 }
-                // the S/P buffer j & 1 last held P(j - 2): its P V must be finished
-                if (j >= 2 && !tc::mbar_wait(&ss.pv_done[m][j & 1], (uint32_t)((j - 2) >> 1) & 1u, abort)) {
-                    ok = false;
-                    return;
-                }
+                // the S/P buffer j & 1 last held P(j - 2), read by P V(j - 2): that MMA was issued earlier
+                // by this thread, and tcgen05.mma operations from one thread execute in issue order,
+                // so S(j) cannot overwrite P(j - 2) before it has been read; no wait is needed
                 tc::fence_after();
                 const uint32_t kaddr = smem_u32(k_tile(j));
                 const uint32_t qaddr = smem_u32(sm + OFF_Q + m * Q_TILE);
@@ -670,7 +668,7 @@ int plan_splits(int ctas, int max_prefix, int requested, int sm_count) {
     const int tiles = (max_prefix + BK - 1) / BK;
     if (requested > 0) return max(1, min(requested, max(1, tiles)));
     if (ctas >= sm_count || tiles <= 2) return 1;
-    int s = (sm_count + ctas - 1) / ctas;       // fill the GPU once
+    int s = sm_count / ctas;                    // at most one wave
     s = min(s, max(1, tiles / 2));              // at least two tiles per split
     return max(1, s);
 }
@@ -686,29 +684,41 @@ int sm_count_cached() {
     return n;
 }
 
-}  // namespace
+// A launch covers sequences [b0, b0 + nb) with `splits` KV splits.  When the (sequence, KV head)
+// blocks fill some waves of the GPU and leave a tail smaller than half a wave, the full waves run
+// unsplit and the tail sequences are split over the SMs the tail would leave idle.
+struct Part {
+    int b0, nb, splits;
+};
 
-size_t tree_attn_workspace(const AttnLaunch &a) {
-    const int splits = plan_splits(a.B * a.Hkv, a.max_prefix, a.num_splits, sm_count_cached());
-    if (splits == 1 || a.B == 0) return 0;
-    const size_t rows = (size_t)a.B * (a.q_hi - a.q_lo) * a.Hq;
-    return (size_t)splits * rows * (D + 2) * sizeof(float);
+int plan_parts(const AttnLaunch &a, Part parts[2]) {
+    const int sms = sm_count_cached();
+    const int items = a.B * a.Hkv;
+    if (a.num_splits == 0 && items > sms && items % sms) {
+        const int b0 = (items / sms) * sms / a.Hkv;
+        const int tail = (a.B - b0) * a.Hkv;
+        if (b0 > 0 && b0 < a.B && 2 * tail <= sms) {
+            parts[0] = {0, b0, 1};
+            parts[1] = {b0, a.B - b0, plan_splits(tail, a.max_prefix, 0, sms)};
+            return 2;
+        }
+    }
+    parts[0] = {0, a.B, plan_splits(items, a.max_prefix, a.num_splits, sms)};
+    return 1;
 }
 
-eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
-    if (a.B == 0 || a.q_hi <= a.q_lo) return EAGLE3_OK;
-    const int splits = plan_splits(a.B * a.Hkv, a.max_prefix, a.num_splits, sm_count_cached());
-    const size_t need = tree_attn_workspace(a);
-    if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
-    // rows of q / tree k / tree v / out are moved 16 bytes at a time
-    const int64_t strides[] = {a.q_sb, a.q_si, a.k_sb, a.k_si, a.v_sb, a.v_si, a.o_sb, a.o_si};
-    for (int64_t st : strides)
-        if (st % 8) return EAGLE3_ERR_INVALID_ARGUMENT;
-    const void *row_bases[] = {a.q, a.k, a.v, a.out};
-    for (const void *r : row_bases)
-        if ((uintptr_t)r & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
+size_t part_workspace(const AttnLaunch &a, const Part &pt) {
+    if (pt.splits == 1 || pt.nb == 0) return 0;
+    const size_t rows = (size_t)pt.nb * (a.q_hi - a.q_lo) * a.Hq;
+    return (size_t)pt.splits * rows * (D + 2) * sizeof(float);
+}
+
+eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace, cudaStream_t stream) {
+    const int splits = pt.splits;
+    const size_t b0 = (size_t)pt.b0;
+    const int nq = a.q_hi - a.q_lo;
     Params p;
-    p.B = a.B;
+    p.B = pt.nb;
     p.n_slots = a.n_slots;
     p.q_lo = a.q_lo;
     p.q_hi = a.q_hi;
@@ -722,34 +732,67 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
     p.max_prefix = a.max_prefix;
     p.scale_log2 = a.sm_scale * LOG2E_F;
     for (int j = 0; j < D / 2; ++j) p.inv_freq[j] = (float)pow((double)a.rope_theta, -2.0 * j / D);
-    p.q = a.q;
+    p.q = a.q + b0 * a.q_sb;
     p.q_sb = a.q_sb;
     p.q_si = a.q_si;
-    p.k = a.k;
+    p.k = a.k + b0 * a.k_sb;
     p.k_sb = a.k_sb;
     p.k_si = a.k_si;
-    p.v = a.v;
+    p.v = a.v + b0 * a.v_sb;
     p.v_sb = a.v_sb;
     p.v_si = a.v_si;
-    p.out = a.out;
+    p.out = a.out + b0 * a.o_sb;
     p.o_sb = a.o_sb;
     p.o_si = a.o_si;
-    p.parents = a.parents;
-    p.anc = a.anc;
-    p.pos = a.pos;
+    p.parents = a.parents ? a.parents + b0 * a.n_slots : nullptr;
+    p.anc = a.anc ? a.anc + b0 * a.anc_sb : nullptr;
+    p.pos = a.pos ? a.pos + b0 * a.pos_sb : nullptr;
     p.anc_sb = a.anc_sb;
     p.pos_sb = a.pos_sb;
-    p.prefix_len = a.prefix_len;
-    p.lse = a.lse;
+    p.prefix_len = a.prefix_len + b0;
+    p.lse = a.lse ? a.lse + b0 * nq * a.Hq : nullptr;
     p.dev_status = a.dev_status;
-    const size_t rows = (size_t)a.B * (a.q_hi - a.q_lo) * a.Hq;
+    const size_t rows = (size_t)pt.nb * nq * a.Hq;
     p.part_o = splits > 1 ? (float *)workspace : nullptr;
     p.part_ml = splits > 1 ? (float *)workspace + (size_t)splits * rows * D : nullptr;
 
     CUtensorMap mk, mv;
-    const int64_t cache_rows = (int64_t)a.B * a.Hkv * a.S;
-    if (!make_cache_map(&mk, a.k_cache, cache_rows) || !make_cache_map(&mv, a.v_cache, cache_rows))
+    const size_t cache_off = b0 * a.Hkv * a.S * D;
+    const int64_t cache_rows = (int64_t)pt.nb * a.Hkv * a.S;
+    if (!make_cache_map(&mk, a.k_cache + cache_off, cache_rows) ||
+        !make_cache_map(&mv, a.v_cache + cache_off, cache_rows))
         return EAGLE3_ERR_CUDA;
+    verify_attn_kernel<<<dim3(splits, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    if (splits > 1) {
+        verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
+    return EAGLE3_OK;
+}
+
+}  // namespace
+
+size_t tree_attn_workspace(const AttnLaunch &a) {
+    if (a.B == 0) return 0;
+    Part parts[2];
+    const int n = plan_parts(a, parts);
+    size_t need = 0;
+    for (int i = 0; i < n; ++i) need = std::max(need, part_workspace(a, parts[i]));   // parts run in order
+    return need;
+}
+
+eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (a.B == 0 || a.q_hi <= a.q_lo) return EAGLE3_OK;
+    const size_t need = tree_attn_workspace(a);
+    if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
+    // rows of q / tree k / tree v / out are moved 16 bytes at a time
+    const int64_t strides[] = {a.q_sb, a.q_si, a.k_sb, a.k_si, a.v_sb, a.v_si, a.o_sb, a.o_si};
+    for (int64_t st : strides)
+        if (st % 8) return EAGLE3_ERR_INVALID_ARGUMENT;
+    const void *row_bases[] = {a.q, a.k, a.v, a.out};
+    for (const void *r : row_bases)
+        if ((uintptr_t)r & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
     static bool attr_done = false;
     if (!attr_done) {
         if (cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_DYN) !=
@@ -757,11 +800,11 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
             return EAGLE3_ERR_CUDA;
         attr_done = true;
     }
-    verify_attn_kernel<<<dim3(splits, a.Hkv, a.B), NT, SMEM_DYN, stream>>>(mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
-    if (splits > 1) {
-        verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    Part parts[2];
+    const int n = plan_parts(a, parts);
+    for (int i = 0; i < n; ++i) {
+        const eagle3_status_t st = launch_part(a, parts[i], workspace, stream);
+        if (st != EAGLE3_OK) return st;
     }
     return EAGLE3_OK;
 }
