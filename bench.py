@@ -181,8 +181,8 @@ class Engine:
         self.ws_acc = torch.empty(16, dtype=torch.uint8, device=dev)
         self.ws_draft = None
         self.steps_done = 0
-        self.kernel_ms = {"gemm": 0.0, "verify_attn": 0.0}
-        self.kernel_calls = {"gemm": 0, "verify_attn": 0}
+        self.kernel_ms = {"gemm": 0.0, "gemm_gateup": 0.0, "verify_attn": 0.0}
+        self.kernel_calls = {"gemm": 0, "gemm_gateup": 0, "verify_attn": 0}
         self._ev = []
         # events are created once and reused: creating timing events inside the loop is not free
         self._pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -257,14 +257,14 @@ class Engine:
 
         lp, lb = ws(self.ws_lin)
 
-        def lin(x, w, out, epi=0, w2=None, res=None):
+        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm"):
             a = e3._lib.LinearArgs(m=x.shape[0], n=w.shape[0], k=x.shape[1], epilogue=epi, splits=0, ld_x=0, ld_w=0,
                                    ld_out=0, ld_res=0, x=x.data_ptr(), w=w.data_ptr(),
                                    w2=None if w2 is None else w2.data_ptr(), out=out.data_ptr(),
                                    residual=None if res is None else res.data_ptr(),
                                    dev_status=self.dev_status.data_ptr())
             keep.append(a)
-            ops.append(("gemm", lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st)))
+            ops.append((kind, lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st)))
 
         taps = {t: i for i, t in enumerate(c["taps"])}
         norm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap=self.x)
@@ -285,7 +285,7 @@ class Engine:
             ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st)))
             lin(self.attn, self.wo[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
             norm(self.x, self.norm2[l], self.h)
-            lin(self.h, self.wg[l], self.act, epi=e3.EPI_SWIGLU, w2=self.wu[l])
+            lin(self.h, self.wg[l], self.act, epi=e3.EPI_SWIGLU, w2=self.wu[l], kind="gemm_gateup")
             lin(self.act, self.wd[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
         norm(self.x, self.final_norm, self.h)
         lin(self.h, self.lm_head, self.logits, epi=e3.EPI_F32)
@@ -541,9 +541,15 @@ def run_gpu(args):
     value = units / (ms / 1e3)
     hbm, tf_burst, tf_sust, src = peaks()
     tgt_f, drf_f = eng.flops_per_step()
-    gemm_ms = eng.kernel_ms["gemm"] / max(1, args.steps)
-    gemm_calls = eng.kernel_calls["gemm"] / max(1, args.steps)
-    gemm_tflops = (tgt_f + drf_f) / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    # the target's projections are timed one by one; the draft head's run inside eagle3_draft_tree
+    gemm_ms = (eng.kernel_ms["gemm"] + eng.kernel_ms["gemm_gateup"]) / max(1, args.steps)
+    gemm_calls = (eng.kernel_calls["gemm"] + eng.kernel_calls["gemm_gateup"]) / max(1, args.steps)
+    gemm_tflops = tgt_f / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    # the dominant launch: the SwiGLU gate + up projection of a target layer
+    R = cfg["B"] * cfg["N"]
+    gu_flops = 2.0 * R * (2 * cfg["F"]) * cfg["d"]
+    gu_ms = eng.kernel_ms["gemm_gateup"] / max(1, eng.kernel_calls["gemm_gateup"])
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12 if gu_ms > 0 else None
     attn_ms = eng.kernel_ms["verify_attn"] / max(1, eng.kernel_calls["verify_attn"])
     attn_gbs = eng.attn_bytes_per_launch(L_mean) / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
     tau = float(accepted.item()) / (cfg["B"] * args.steps) - 1.0
@@ -560,11 +566,17 @@ def run_gpu(args):
                                "B=64, N=60 (depth 6, top-k 10), prefix 2048, T=1, compaction on",
                    "global_batch": cfg["B"] * world, "seq_len": cfg["L0"], "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (16 GB of weights streamed per step)"},
-        "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1) if gemm_tflops else None,
+        "roofline": {"bound": "tensor", "achieved": round(gu_tflops, 1) if gu_tflops else None,
                      "peak": tf_sust, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / tf_sust, 4) if gemm_tflops else None, "traffic": None,
-                     "kernel": "gemm_tc_kernel (all tcgen05 projections of the step)",
-                     "peak_source": f"{src} bf16_tflops_sustained"},
+                     "frac": round(gu_tflops / tf_sust, 4) if gu_tflops else None,
+                     "traffic": GATEUP_TRAFFIC_BYTES,
+                     "kernel": f"gemm_tc_kernel, SwiGLU gate+up projection M={R} N=2x{cfg['F']} K={cfg['d']} "
+                               f"({gu_flops / 1e12:.3f} TFLOP per launch, {cfg['layers']} launches per step)",
+                     "ms_per_launch": round(gu_ms, 4),
+                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside the step)",
+                     "all_target_gemms": {"achieved": round(gemm_tflops, 1) if gemm_tflops else None,
+                                          "frac": round(gemm_tflops / tf_sust, 4) if gemm_tflops else None,
+                                          "launches_per_step": gemm_calls}},
         "verify_attn": {"achieved_gbs": round(attn_gbs, 1) if attn_gbs else None, "peak_gbs": hbm,
                         "frac": round(attn_gbs / hbm, 4) if attn_gbs else None,
                         "frac_of_8tbs": round(attn_gbs / 8000.0, 4) if attn_gbs else None,
@@ -586,6 +598,11 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# DRAM bytes (read + write) of one SwiGLU gate+up launch at the bench shape, from the ncu capture
+# summarised in profiles/gemm_gateup_m3840.md (set it to None when the kernel changes)
+GATEUP_TRAFFIC_BYTES = 267010560 + 96883712
 
 
 def _draft_launches(cfg):
@@ -800,6 +817,23 @@ def run_kernel(args):
         out.update(batch=B, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
                    frac_tensor=round(flops / ms / 1e9 / tf_sust, 4),
                    weight_gbs_6_passes=round(6 * wbytes / ms / 1e6, 1))
+    elif args.kernel == "gemm":
+        # one projection of the target layer at the step's shape (default: the SwiGLU gate + up
+        # projection, M = B * N rows); x, w, w2 random bf16, output bf16
+        M = args.batch * CFG["N"]
+        N, K = args.n, args.k
+        bf = torch.bfloat16
+        x = (torch.randn(M, K, generator=g, device=dev) * 0.5).to(bf)
+        w = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(bf)
+        epi = {"swiglu": e3.EPI_SWIGLU, "bf16": e3.EPI_BF16, "f32": e3.EPI_F32}[args.epilogue]
+        w2 = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(bf) if epi == e3.EPI_SWIGLU else None
+        o = torch.empty(M, N, device=dev, dtype=torch.float32 if epi == e3.EPI_F32 else bf)
+        ws = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        fn = lambda: e3.eagle3_linear(x, w, o, epilogue=epi, w2=w2, workspace=ws)
+        ms = _time_loop(fn, args.steps, args.warmup)
+        flops = 2.0 * M * N * K * (2 if w2 is not None else 1)
+        out.update(m=M, n=N, k=K, epilogue=args.epilogue, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
+                   frac_sustained=round(flops / ms / 1e9 / tf_sust, 4), frac_burst=round(flops / ms / 1e9 / tf_burst, 4))
     print(json.dumps(out), flush=True)
 
 
@@ -813,7 +847,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="issue every C call from the host instead of "
                                                           "replaying captured CUDA graphs")
-    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft"],
+    ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
+    ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
+    ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32"])
+    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)
     ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
