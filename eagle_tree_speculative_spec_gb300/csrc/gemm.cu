@@ -11,8 +11,19 @@
 // overlaps the main loop of the next.  Work units are (m tile, n tile, k split), m fastest, so
 // concurrently running CTAs share the same weight tile in L2.  With more than one k split the
 // fp32 partials go to a workspace and a second kernel adds them in split order and applies the
-// epilogue (deterministic).  Every mbarrier wait is bounded; on a timeout the kernel records
-// EAGLE3_DEV_TIMEOUT, stops issuing work, drains its own TMA loads and frees its TMEM.
+// epilogue (deterministic).
+//
+// Stream-K: when the output tiles do not fill whole waves of the GPU, all but the last full wave
+// run as above (m fastest, so the CTAs of a wave share weight tiles in L2), and the remaining
+// tiles' (tile, k-block) iterations are cut into equal contiguous shares, one per CTA.  A tile cut by a share boundary is
+// finished by the CTA that covers its first k-block (it reaches that tile last, at the end of its
+// share): the CTAs covering the rest of the tile wrote their fp32 accumulators to a workspace slot
+// at the start of their own shares and raised a flag; the owner adds the slots in CTA order
+// (deterministic) and applies the epilogue.  Blocks wait on one another here, so this mode is a
+// cooperative launch (all CTAs resident), and the waits are bounded like every other wait.
+//
+// Every mbarrier wait is bounded; on a timeout the kernel records EAGLE3_DEV_TIMEOUT, stops
+// issuing work, drains its own TMA loads and frees its TMEM.
 #include <algorithm>
 #include <cudaTypedefs.h>
 
@@ -34,7 +45,71 @@ struct GemmParams {
     const __nv_bfloat16 *residual;
     int64_t ld_res;
     float *ws;                       // [splits][M][n_acc] fp32 partials (splits > 1)
+    int streamk;                     // stream-K schedule (cooperative launch)
+    int dp_tiles;                    // stream-K: tiles [0, dp_tiles) run whole, data-parallel
+    long long T;                     // stream-K: (tiles - dp_tiles) * kb_total iterations, shared out
+    float4 *sk_part;                 // stream-K: [grid][BN / 4][BM] fp32 accumulator slots (float4 of
+                                     // 4 columns, rows fastest: a warp's 32 rows are 512 contiguous bytes)
+    int *sk_flag;                    // stream-K: [grid] warps of the slot's CTA that have written it
     int32_t *dev_status;
+};
+
+// One piece of work of a CTA: k-blocks [kb0, kb1) of output tile (mb, nb).
+enum { IT_FULL = 0, IT_SPLITK = 1, IT_CONTRIB = 2, IT_OWNER = 3 };
+struct Item {
+    int mb, nb, sp, kb0, kb1, kind, u;
+};
+
+// The same sequence of items for the producer, the MMA issuer and the epilogue of a CTA.
+// first k-block iteration (counted from the first stream-K tile) of CTA c's share
+E3_DEV long long sk_start(const GemmParams &p, long long c) { return p.T * c / gridDim.x; }
+
+struct WorkIter {
+    int unit;
+    long long it, it1;
+    E3_DEV void init(const GemmParams &p) {
+        unit = blockIdx.x;
+        if (p.streamk) {
+            it = (long long)p.dp_tiles * p.kb_total + sk_start(p, blockIdx.x);
+            it1 = (long long)p.dp_tiles * p.kb_total + sk_start(p, blockIdx.x + 1);
+        }
+    }
+    E3_DEV bool next(const GemmParams &p, Item &w) {
+        if (p.streamk && unit < p.dp_tiles) {
+            w.u = unit;
+            w.mb = unit % p.tiles_m;
+            w.nb = unit / p.tiles_m;
+            w.sp = 0;
+            w.kb0 = 0;
+            w.kb1 = p.kb_total;
+            w.kind = IT_FULL;
+            unit += gridDim.x;
+            return true;
+        }
+        if (p.streamk) {
+            if (it >= it1) return false;
+            w.u = (int)(it / p.kb_total);
+            w.kb0 = (int)(it % p.kb_total);
+            w.kb1 = (int)min((long long)p.kb_total, (long long)w.kb0 + (it1 - it));
+            w.mb = w.u % p.tiles_m;
+            w.nb = w.u / p.tiles_m;
+            w.sp = 0;
+            w.kind = (w.kb0 == 0 && w.kb1 == p.kb_total) ? IT_FULL : (w.kb0 > 0 ? IT_CONTRIB : IT_OWNER);
+            it += w.kb1 - w.kb0;
+            return true;
+        }
+        if (unit >= p.units) return false;
+        w.u = unit;
+        w.mb = unit % p.tiles_m;
+        const int r = unit / p.tiles_m;
+        w.nb = r % p.tiles_n;
+        w.sp = r / p.tiles_n;
+        w.kb0 = w.sp * p.kb_per_split;
+        w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
+        w.kind = p.splits > 1 ? IT_SPLITK : IT_FULL;
+        unit += gridDim.x;
+        return true;
+    }
 };
 
 template <int BN>
@@ -130,13 +205,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::fence_after();
     const uint32_t tmem = *tmem_base_slot;
 
-    auto decode = [&](int unit, int &mb, int &nb, int &sp) {
-        mb = unit % p.tiles_m;
-        const int r = unit / p.tiles_m;
-        nb = r % p.tiles_n;
-        sp = r / p.tiles_n;
-    };
-
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -144,11 +212,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             uint32_t phase = 0;
             uint32_t last_parity = 0, issued_mask = 0;   // parity of the last load issued per stage
             bool ok = true;
-            for (int unit = blockIdx.x; unit < p.units && ok; unit += gridDim.x) {
-                int mb, nb, sp;
-                decode(unit, mb, nb, sp);
-                const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-                for (int kb = kb0; kb < kb1; ++kb) {
+            WorkIter wi;
+            wi.init(p);
+            Item w;
+            while (ok && wi.next(p, w)) {
+                const int mb = w.mb, nb = w.nb;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort)) {
                         ok = false;
                         break;
@@ -190,10 +259,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int unit = blockIdx.x; unit < p.units && ok; unit += gridDim.x) {
-                int mb, nb, sp;
-                decode(unit, mb, nb, sp);
-                const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+            WorkIter wi;
+            wi.init(p);
+            Item w;
+            while (ok && wi.next(p, w)) {
+                const int kb0 = w.kb0, kb1 = w.kb1;
                 if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort)) {
                     ok = false;
                     break;
@@ -239,9 +309,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
-            int mb, nb, sp;
-            decode(unit, mb, nb, sp);
+        WorkIter wi;
+        wi.init(p);
+        Item w;
+        while (wi.next(p, w)) {
+            const int mb = w.mb, nb = w.nb, sp = w.sp;
             // warp-uniform wait: lane 0 polls, the outcome is broadcast, so a timeout can never
             // split the warp in front of the warp-collective TMEM loads below
             int ok = 0;
@@ -252,25 +324,81 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 break;
             }
             tc::fence_after();
-            const int row = mb * BM + quarter * 32 + lane;
+            const int rl = quarter * 32 + lane;       // row within the tile
+            const int row = mb * BM + rl;
             const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            if (p.splits > 1) {
+            // stream-K owner: the CTAs after this one whose shares start inside this tile hold the
+            // rest of its k-blocks; wait (bounded, warp-uniform) until all their warps wrote
+            int c_lo = 0, c_hi = 0;
+            if (w.kind == IT_OWNER) {
+                c_lo = blockIdx.x + 1;
+                c_hi = c_lo;
+                const long long tile_end = (long long)(w.u + 1 - p.dp_tiles) * p.kb_total;
+                while (c_hi < (int)gridDim.x && sk_start(p, c_hi) < tile_end) ++c_hi;
+                int fine = 1;
+                if (lane == 0) {
+                    for (int c = c_lo; c < c_hi && fine; ++c) {
+                        const long long t0 = clock64();
+                        while (atomicAdd(&p.sk_flag[c], 0) < 4) {
+                            if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+                                fine = 0;
+                                flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+                                break;
+                            }
+                        }
+                    }
+                }
+                fine = __shfl_sync(0xffffffffu, fine, 0);
+                if (!fine) c_hi = c_lo;
+                __threadfence();
+            }
+            // add the stream-K contributions to a chunk of 32 accumulator columns
+            auto add_contrib = [&](float (&v)[32], int col) {
+                for (int c = c_lo; c < c_hi; ++c) {
+                    const float4 *src = p.sk_part + (size_t)c * (BN / 4) * BM + (size_t)(col / 4) * BM + rl;
+                    float4 q[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) q[i] = __ldcg(src + (size_t)i * BM);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        v[4 * i] += q[i].x;
+                        v[4 * i + 1] += q[i].y;
+                        v[4 * i + 2] += q[i].z;
+                        v[4 * i + 3] += q[i].w;
+                    }
+                }
+            };
+            if (w.kind == IT_CONTRIB) {
+                // this CTA's slot; then count this warp in
+                float4 *dst = p.sk_part + (size_t)blockIdx.x * (BN / 4) * BM + rl;
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tc::tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        __stcg(dst + (size_t)(c * 8 + i) * BM, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(&p.sk_flag[blockIdx.x], 1);
+            } else if (p.splits > 1) {
                 // fp32 partials in accumulator layout.  tcgen05.ld is warp-collective: every lane
                 // loads, only lanes that own a row < M store.
-                float *w = p.ws + ((size_t)sp * p.M + (row < p.M ? row : 0)) * p.n_acc + (size_t)nb * BN;
+                float *wsr = p.ws + ((size_t)sp * p.M + (row < p.M ? row : 0)) * p.n_acc + (size_t)nb * BN;
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tc::tmem_ld32(t_row + c * 32, v);
                     if (row < p.M) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(w + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                            *reinterpret_cast<float4 *>(wsr + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                     }
                 }
             } else if (!swiglu) {
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tc::tmem_ld32(t_row + c * 32, v);
+                    add_contrib(v, c * 32);
                     store_chunk(p, row, nb * BN + c * 32, v);
                 }
             } else {
@@ -278,6 +406,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     float g[32], u[32];
                     tc::tmem_ld32(t_row + c * 32, g);
                     tc::tmem_ld32(t_row + BN / 2 + c * 32, u);
+                    add_contrib(g, c * 32);
+                    add_contrib(u, BN / 2 + c * 32);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) g[i] = silu(g[i]) * u[i];
                     store_chunk(p, row, nb * (BN / 2) + c * 32, g);
@@ -372,7 +502,8 @@ int sm_count() {
 }
 
 struct Plan {
-    int bn, tiles_m, tiles_n, splits, kb_total, kb_per_split, units, n_acc, grid;
+    int bn, tiles_m, tiles_n, splits, kb_total, kb_per_split, units, n_acc, grid, streamk, dp_tiles;
+    size_t ws_bytes;
 };
 
 Plan plan(const eagle3_linear_args_t *a) {
@@ -385,14 +516,31 @@ Plan plan(const eagle3_linear_args_t *a) {
     pl.kb_total = (a->k + BK - 1) / BK;
     const int tiles = pl.tiles_m * pl.tiles_n;
     const int sms = sm_count();
+    pl.n_acc = pl.tiles_n * pl.bn;
+    // stream-K when whole tiles would leave the last wave less than 97% full and a tile's main loop
+    // is long (K >= 12288): the fix-up (a flag reset before the launch, fp32 slots through L2) and
+    // the cooperative launch, which cannot start under the previous kernel's last wave, cost about
+    // as much as the quantisation they remove when K is 4096
+    const int waves = (tiles + sms - 1) / sms;
+    pl.dp_tiles = tiles / sms >= 2 ? (tiles / sms - 1) * sms : 0;   // whole waves kept data-parallel
+    const long long T = (long long)(tiles - pl.dp_tiles) * pl.kb_total;
+    pl.streamk = a->splits <= 0 && pl.kb_total >= 192 && (double)tiles / ((double)waves * sms) < 0.97 &&
+                 T >= 8LL * sms;
+    if (pl.streamk) {
+        pl.splits = 1;
+        pl.kb_per_split = pl.kb_total;
+        pl.units = tiles;
+        pl.grid = sms;
+        pl.ws_bytes = (size_t)sms * BM * pl.bn * sizeof(float) + (size_t)sms * sizeof(int);
+        return pl;
+    }
     int splits = a->splits > 0 ? a->splits : 1;
-    if (a->splits <= 0 && tiles < sms) splits = std::max(1, std::min(pl.kb_total / 4, sms / tiles));
     splits = std::max(1, std::min(splits, pl.kb_total));
     pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
     pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
     pl.units = tiles * pl.splits;
-    pl.n_acc = pl.tiles_n * pl.bn;
     pl.grid = std::min(pl.units, sms);
+    pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * a->m * pl.n_acc * sizeof(float) : 0;
     return pl;
 }
 
@@ -418,8 +566,7 @@ using namespace e3;
 
 extern "C" size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *a) {
     if (validate(a) != EAGLE3_OK || a->m == 0) return 0;
-    const Plan pl = plan(a);
-    return pl.splits > 1 ? (size_t)pl.splits * a->m * pl.n_acc * sizeof(float) : 0;
+    return plan(a).ws_bytes;
 }
 
 extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *workspace, size_t ws_bytes,
@@ -427,7 +574,7 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     const eagle3_status_t st = validate(a);
     if (st != EAGLE3_OK || a->m == 0) return st;
     const Plan pl = plan(a);
-    const size_t need = pl.splits > 1 ? (size_t)pl.splits * a->m * pl.n_acc * sizeof(float) : 0;
+    const size_t need = pl.ws_bytes;
     if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
     const bool swiglu = a->epilogue == EAGLE3_EPI_SWIGLU;
     const int64_t ld_x = a->ld_x ? a->ld_x : a->k, ld_w = a->ld_w ? a->ld_w : a->k;
@@ -458,6 +605,11 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.residual = (const __nv_bfloat16 *)a->residual;
     p.ld_res = a->ld_res ? a->ld_res : a->n;
     p.ws = (float *)workspace;
+    p.streamk = pl.streamk;
+    p.dp_tiles = pl.streamk ? pl.dp_tiles : 0;
+    p.T = (long long)(pl.tiles_m * pl.tiles_n - p.dp_tiles) * pl.kb_total;
+    p.sk_part = pl.streamk ? (float4 *)workspace : nullptr;
+    p.sk_flag = pl.streamk ? (int *)((uint8_t *)workspace + (size_t)pl.grid * BM * pl.bn * sizeof(float)) : nullptr;
     p.dev_status = a->dev_status;
 
     using C = Cfg<256>;
@@ -468,7 +620,24 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
             return EAGLE3_ERR_CUDA;
         attr = true;
     }
-    gemm_tc_kernel<256><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, p);
+    if (pl.streamk) {
+        // flags start at zero; blocks wait on one another, so all of them must be resident
+        if (cudaMemsetAsync(p.sk_flag, 0, (size_t)pl.grid * sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(pl.grid);
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr_coop[1];
+        attr_coop[0].id = cudaLaunchAttributeCooperative;
+        attr_coop[0].val.cooperative = 1;
+        cfg.attrs = attr_coop;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, ma, mb, mb2, p) != cudaSuccess) return EAGLE3_ERR_CUDA;
+    } else {
+        gemm_tc_kernel<256><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, p);
+    }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (pl.splits > 1) {
         const size_t total = (size_t)a->m * a->n;

@@ -98,3 +98,19 @@ def test_linear_in_place_residual():
     torch.cuda.synchronize()
     ok, err = close(buf.float().cpu().numpy(), _ref(x, w) + r.double().numpy(), 2e-2, 1e-2)
     assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,epi", [
+    (768, 4096, 12288, "bf16"), (300, 1000, 12296, "bf16"), (130, 4096, 14336, "residual"),
+    (200, 4096, 12288, "f32"), (640, 2048, 12288, "swiglu"), (1, 4096, 14336, "bf16"),
+    (3840, 4096, 14336, "bf16")])
+def test_linear_stream_k(m, n, k, epi):
+    """Long-K shapes whose output tiles leave the last wave partly empty run the stream-K schedule:
+    tiles cut between CTAs are finished by the CTA holding their first k-block, which adds the
+    others' fp32 slots in CTA order (M = 3840 also has data-parallel waves in front)."""
+    import eagle_tree_speculative_spec_gb300 as e3
+    code = {"bf16": e3.EPI_BF16, "residual": e3.EPI_BF16_RESIDUAL, "f32": e3.EPI_F32, "swiglu": e3.EPI_SWIGLU}[epi]
+    got, want = _run(m, n, k, code, seed=5)
+    atol, rtol = (1e-3, 1e-3) if epi == "f32" else (2e-2, 1e-2)
+    ok, err = close(got, want, atol, rtol)
+    assert ok, err
