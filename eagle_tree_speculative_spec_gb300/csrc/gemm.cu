@@ -51,6 +51,7 @@ struct GemmParams {
     float4 *sk_part;                 // stream-K: [grid][BN / 4][BM] fp32 accumulator slots (float4 of
                                      // 4 columns, rows fastest: a warp's 32 rows are 512 contiguous bytes)
     int *sk_flag;                    // stream-K: [grid] warps of the slot's CTA that have written it
+    int tma_out;                     // outputs leave through shared memory and TMA stores
     int32_t *dev_status;
 };
 
@@ -119,7 +120,11 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /* align */ + 256 /* barriers */;
+    // epilogue staging: per epilogue warp two boxes of 32 rows x 128 bytes (128B-swizzled)
+    static constexpr int EPI_BOX = 32 * 128;
+    static constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024 /* align */ + 256 /* barriers */;
+    static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 E3_DEV float silu(float x) { return x / (1.0f + __expf(-x)); }
@@ -168,13 +173,15 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
 template <int BN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_b2, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_out,
+                   const GemmParams p) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sa = smem;                                   // STAGES x A tile
     uint8_t *sb = smem + C::STAGES * C::A_BYTES;          // STAGES x B tile
-    uint64_t *bars = (uint64_t *)(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t *epi = smem + C::STAGES * C::STAGE_BYTES;     // 4 warps x 2 output boxes (1024-aligned)
+    uint64_t *bars = (uint64_t *)(epi + C::EPI_BYTES);
     uint64_t *full = bars, *empty = bars + C::STAGES, *tfull = bars + 2 * C::STAGES, *tempty = tfull + 2;
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_base_slot = (uint32_t *)(mma_done + 1);
@@ -309,6 +316,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         int acc = 0;
         uint32_t acc_phase = 0;
+        int sbuf = 0;                                 // output staging buffer of this warp
         WorkIter wi;
         wi.init(p);
         Item w;
@@ -394,6 +402,74 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             *reinterpret_cast<float4 *>(wsr + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                     }
                 }
+            } else if (p.tma_out) {
+                // 128-byte-wide chunks of this warp's 32 rows: 32 fp32 or 64 bf16 columns
+                const int y = mb * BM + quarter * 32;
+                const bool f32 = p.epi == EAGLE3_EPI_F32;
+                const int chunks = (swiglu ? BN / 2 : BN) / (f32 ? 32 : 64);
+                for (int sc = 0; sc < chunks; ++sc) {
+                    uint4 u[8];
+                    if (f32) {
+                        float v[32];
+                        tc::tmem_ld32(t_row + sc * 32, v);
+                        add_contrib(v, sc * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            u[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                              __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+                    } else {
+                        float v[64];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float t[32];
+                            if (!swiglu) {
+                                tc::tmem_ld32(t_row + sc * 64 + h * 32, t);
+                                add_contrib(t, sc * 64 + h * 32);
+                            } else {
+                                float g[32];
+                                const int c = sc * 2 + h;
+                                tc::tmem_ld32(t_row + c * 32, g);
+                                tc::tmem_ld32(t_row + BN / 2 + c * 32, t);
+                                add_contrib(g, c * 32);
+                                add_contrib(t, BN / 2 + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) t[i] = silu(g[i]) * t[i];
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[h * 32 + i] = t[i];
+                        }
+                        const int col0 = (swiglu ? nb * (BN / 2) : nb * BN) + sc * 64;
+                        if (p.epi == EAGLE3_EPI_BF16_RESIDUAL && row < p.M) {
+                            const __nv_bfloat16 *r = p.residual + (size_t)row * p.ld_res + col0;
+                            for (int i = 0; i < 64; ++i)
+                                if (col0 + i < p.N) v[i] += __bfloat162float(r[i]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * j], v[8 * j + 1]);
+                            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+                            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+                            u[j] = make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                                              *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                        }
+                    }
+                    // the buffer was last stored from two chunks ago: that store must have read it
+                    uint8_t *box = epi + (quarter * 2 + sbuf) * C::EPI_BOX;
+                    if (lane == 0) tc::bulk_wait_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) = u[j];
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    const int x = (swiglu ? nb * (BN / 2) : nb * BN) + sc * (f32 ? 32 : 64);
+                    if (lane == 0 && x < p.N && y < p.M) {   // boxes wholly outside the output are skipped
+                        tc::tma_store_2d(&tm_out, x, y, box);
+                        tc::bulk_commit();
+                    }
+                    sbuf ^= 1;
+                }
             } else if (!swiglu) {
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
@@ -421,6 +497,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) tc::bulk_wait<0>();            // every output store has completed
+        __syncwarp();
     }
 
     tc::fence_before();
@@ -487,6 +565,21 @@ bool make_map(CUtensorMap *m, const void *base, int rows, int cols, int64_t ld_e
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// output [rows, cols] (fp32 or bf16) for TMA stores: 32-row boxes 128 bytes wide, 128B swizzle
+bool make_out_map(CUtensorMap *m, void *base, int rows, int cols, int64_t ld_elems, bool f32) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = f32 ? 4 : 2;
+    if (((uintptr_t)base & 15) || (ld_elems * es) % 16) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_elems * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -611,6 +704,9 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.sk_part = pl.streamk ? (float4 *)workspace : nullptr;
     p.sk_flag = pl.streamk ? (int *)((uint8_t *)workspace + (size_t)pl.grid * BM * pl.bn * sizeof(float)) : nullptr;
     p.dev_status = a->dev_status;
+    CUtensorMap mo;
+    p.tma_out = make_out_map(&mo, a->out, a->m, a->n, p.ld_out, a->epilogue == EAGLE3_EPI_F32) ? 1 : 0;
+    if (!p.tma_out) mo = ma;   // unused
 
     using C = Cfg<256>;
     static bool attr = false;
@@ -634,9 +730,9 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
         attr_coop[0].val.cooperative = 1;
         cfg.attrs = attr_coop;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, ma, mb, mb2, p) != cudaSuccess) return EAGLE3_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, ma, mb, mb2, mo, p) != cudaSuccess) return EAGLE3_ERR_CUDA;
     } else {
-        gemm_tc_kernel<256><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, p);
+        gemm_tc_kernel<256><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
     }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (pl.splits > 1) {
