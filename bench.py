@@ -820,7 +820,7 @@ def run_kernel(args):
     elif args.kernel == "gemm":
         # one projection of the target layer at the step's shape (default: the SwiGLU gate + up
         # projection, M = B * N rows); x, w, w2 random bf16, output bf16
-        M = args.batch * CFG["N"]
+        M = args.m if args.m > 0 else args.batch * CFG["N"]
         N, K = args.n, args.k
         bf = torch.bfloat16
         x = (torch.randn(M, K, generator=g, device=dev) * 0.5).to(bf)
@@ -847,6 +847,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="issue every C call from the host instead of "
                                                           "replaying captured CUDA graphs")
+    ap.add_argument("--m", type=int, default=0, help="--kernel gemm: rows (default batch x tree nodes)")
     ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
     ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
     ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32"])
