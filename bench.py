@@ -731,6 +731,61 @@ def _time_loop(fn, steps, warmup, flush=None):
     return total / steps
 
 
+def run_generate(args):
+    """The end-to-end run of the workload: every sequence generates `--generate` new tokens (each
+    step emits accept_len + 1 >= 1 tokens per sequence, so that many steps always suffice); reports
+    throughput and the measured acceptance length."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    cfg = dict(CFG)
+    cfg["B"] = args.batch
+    n_new = args.generate
+    eng = Engine(cfg, n_new + 2, dev, timing=False)
+    eng.step()                                    # warm-up step (its tokens are not counted)
+    eng.capture(1)
+    gen = torch.zeros(cfg["B"], dtype=torch.int64, device=dev)
+    steps_needed = torch.zeros((), dtype=torch.int64, device=dev)
+    eng.replay(0)
+    gen += eng.accept_len.to(torch.int64) + 1      # warm the bookkeeping ops too
+    gen.zero_()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    wall0 = time.time()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n_new):
+        eng.replay(0)
+        steps_needed += (gen < n_new).to(torch.int64).max()
+        gen += eng.accept_len.to(torch.int64) + 1
+    t1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clocks.stop()
+    ms = t0.elapsed_time(t1)
+    g = gen.cpu()
+    emitted = int(g.sum())
+    line = {
+        "mode": "generate", "new_tokens_per_sequence": n_new, "batch": cfg["B"], "steps": n_new,
+        "steps_until_every_sequence_had_n_new": int(steps_needed.item()),
+        "ms_total": round(ms, 2), "ms_per_step": round(ms / n_new, 4),
+        "verified_tree_tokens_per_s": round(cfg["B"] * cfg["N"] * n_new / (ms / 1e3), 1),
+        "emitted_tokens_per_s": round(emitted / (ms / 1e3), 1),
+        "acceptance_length_mean": round(emitted / (cfg["B"] * n_new), 4),
+        "emitted_per_sequence_min_max": [int(g.min()), int(g.max())],
+        "final_prefix_len_mean": round(float(eng.prefix_len.float().mean()), 1),
+        "dev_status": int(eng.dev_status.item()),
+        "clocks": clocks.summary(wall0, wall1),
+        "config": "B=64, N=60 (depth 6, top-k 10), prefix 2048, T=1, Philox seed 2, compaction on; "
+                  "random-init weights, N(0,1) prefilled caches",
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_kernel(args):
     """Single-kernel measurements of the rows of the path (not the headline line)."""
     import eagle_tree_speculative_spec_gb300 as e3
@@ -847,6 +902,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="issue every C call from the host instead of "
                                                           "replaying captured CUDA graphs")
+    ap.add_argument("--generate", type=int, default=0,
+                    help="run until every sequence has this many new tokens and report the acceptance length")
     ap.add_argument("--m", type=int, default=0, help="--kernel gemm: rows (default batch x tree nodes)")
     ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
     ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
@@ -858,7 +915,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and not args.kernel:
         args.warmup = 3
-    if args.kernel:
+    if args.generate:
+        run_generate(args)
+    elif args.kernel:
         run_kernel(args)
     elif args.impl == "reference":
         run_reference(args)
