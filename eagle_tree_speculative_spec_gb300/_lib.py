@@ -92,6 +92,20 @@ class DraftTreeArgs(ctypes.Structure):
                 ("score", _p), ("dbg_logits", _p), ("dev_status", _p)]
 
 
+F32_EPI_NONE, F32_EPI_RESIDUAL, F32_EPI_SWIGLU = 0, 1, 2
+
+
+class F32LinearArgs(ctypes.Structure):
+    _fields_ = [("m", _i64), ("n", _i64), ("k", _i64), ("epilogue", _i32), ("ld_x", _i64), ("ld_out", _i64),
+                ("ld_res", _i64), ("x", _p), ("w", _p), ("w2", _p), ("residual", _p), ("out", _p)]
+
+
+class F32AttnArgs(ctypes.Structure):
+    _fields_ = [("n_rows", _i32), ("n_heads", _i32), ("n_kv_heads", _i32), ("head_dim", _i32), ("cache_len", _i32),
+                ("s_max", _i32), ("scale", _f32), ("ld_q", _i64), ("ld_kv", _i64), ("q", _p), ("k_new", _p),
+                ("v_new", _p), ("k_cache", _p), ("v_cache", _p), ("visible", _p), ("out", _p)]
+
+
 class RmsnormArgs(ctypes.Structure):
     _fields_ = [("rows", _i32), ("dim", _i32), ("n_src", _i32), ("eps", _f32), ("ld_in", _i64), ("ld_out", _i64),
                 ("ld_tap", _i64), ("input", _p), ("w", _p), ("gather", _p), ("out", _p), ("tap_out", _p),
@@ -125,6 +139,18 @@ def _declare(L):
     L.eagle3_draft_tree.argtypes = [P(DraftWeights), P(DraftTreeArgs), _p, ctypes.c_size_t, _p]
     L.eagle3_rmsnorm.restype = ctypes.c_int
     L.eagle3_rmsnorm.argtypes = [P(RmsnormArgs), _p]
+    L.eagle3_f32_linear.restype = ctypes.c_int
+    L.eagle3_f32_linear.argtypes = [P(F32LinearArgs), _p]
+    L.eagle3_f32_rmsnorm.restype = ctypes.c_int
+    L.eagle3_f32_rmsnorm.argtypes = [_i64, _i64, _p, _i64, _p, _p, _f32, _p, _i64, _p]
+    L.eagle3_f32_rope.restype = ctypes.c_int
+    L.eagle3_f32_rope.argtypes = [_i64, _i32, _i32, _p, _i64, _p, _f32, _p]
+    L.eagle3_f32_gather.restype = ctypes.c_int
+    L.eagle3_f32_gather.argtypes = [_i64, _i64, _p, _p, _p, _i64, _p]
+    L.eagle3_f32_argmax.restype = ctypes.c_int
+    L.eagle3_f32_argmax.argtypes = [_i64, _i64, _p, _p, _p]
+    L.eagle3_f32_attn.restype = ctypes.c_int
+    L.eagle3_f32_attn.argtypes = [P(F32AttnArgs), _p]
 
 
 def status_string(status):
@@ -391,3 +417,76 @@ def eagle3_verify_attn_noalloc(q, tree_k, tree_v, k_cache, v_cache, parents, pre
                          max_prefix_len=max_prefix_len, lse=lse, rope_theta=rope_theta, sm_scale=sm_scale,
                          num_splits=num_splits, dev_status=dev_status)
     _check(lib().eagle3_verify_attn_noalloc(ctypes.byref(a), _stream(stream)), "eagle3_verify_attn_noalloc")
+
+
+# ----------------------------------------------------------------------------- fp32 small-model blocks
+def _rows_pitch(t, what):
+    """Row pitch (elements) of a 2-D view whose rows are contiguous."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{what} must be a 2-D view with contiguous rows")
+    return t.stride(0)
+
+
+def _vptr(t, dtype, name):
+    """Pointer of a 2-D row view (rows contiguous, any row pitch), or None."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    _rows_pitch(t, name)
+    return t.data_ptr()
+
+
+def eagle3_f32_linear(x, w, out, *, epilogue=F32_EPI_NONE, w2=None, residual=None, stream=None):
+    """out = epilogue(x W^T) in fp32; x [m, k], w (and w2) [n, k], out / residual [m, n] row views."""
+    m, k = x.shape
+    n = w.shape[0]
+    a = F32LinearArgs(m=m, n=n, k=k, epilogue=int(epilogue), ld_x=_rows_pitch(x, "x"), ld_out=_rows_pitch(out, "out"),
+                      ld_res=0 if residual is None else _rows_pitch(residual, "residual"),
+                      x=_vptr(x, torch.float32, "x"), w=_ptr(w, torch.float32, "w"), w2=_ptr(w2, torch.float32, "w2"),
+                      residual=_vptr(residual, torch.float32, "residual"), out=_vptr(out, torch.float32, "out"))
+    _check(lib().eagle3_f32_linear(ctypes.byref(a), _stream(stream)), "eagle3_f32_linear")
+
+
+def eagle3_f32_rmsnorm(x, w, out, *, eps=1e-5, gather=None, stream=None):
+    rows = out.shape[0] if gather is None else gather.numel()
+    dim = w.numel()
+    _check(lib().eagle3_f32_rmsnorm(rows, dim, _vptr(x, torch.float32, "x"), _rows_pitch(x, "x"),
+                                    _ptr(gather, torch.int32, "gather"), _ptr(w, torch.float32, "w"), eps,
+                                    _vptr(out, torch.float32, "out"), _rows_pitch(out, "out"), _stream(stream)),
+           "eagle3_f32_rmsnorm")
+
+
+def eagle3_f32_rope(x, heads, head_dim, pos, *, theta=500000.0, stream=None):
+    """x [rows, >= heads * head_dim] row view, rotated in place at positions pos [rows] int32."""
+    _check(lib().eagle3_f32_rope(x.shape[0], heads, head_dim, _vptr(x, torch.float32, "x"), _rows_pitch(x, "x"),
+                                 _ptr(pos, torch.int32, "pos"), theta, _stream(stream)), "eagle3_f32_rope")
+
+
+def eagle3_f32_gather(table, idx, out, *, stream=None):
+    _check(lib().eagle3_f32_gather(idx.numel(), table.shape[1], _ptr(table, torch.float32, "table"),
+                                   _ptr(idx, torch.int32, "idx"), _vptr(out, torch.float32, "out"),
+                                   _rows_pitch(out, "out"), _stream(stream)), "eagle3_f32_gather")
+
+
+def eagle3_f32_argmax(logits, out, *, stream=None):
+    _check(lib().eagle3_f32_argmax(logits.shape[0], logits.shape[1], _vptr(logits, torch.float32, "logits"),
+                                   _ptr(out, torch.int32, "out"), _stream(stream)), "eagle3_f32_argmax")
+
+
+def eagle3_f32_attn(q, k_new, v_new, k_cache, v_cache, visible, out, *, n_heads, n_kv_heads, head_dim, cache_len,
+                    scale=0.0, stream=None):
+    """q [T, >= Hq*D] and k_new / v_new [T, >= Hkv*D] row views (rotated); k_cache / v_cache
+    [Hkv, s_max, D]; visible [T] int64 bitmasks over the new rows; out [T, Hq, D]."""
+    a = F32AttnArgs(n_rows=q.shape[0], n_heads=n_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
+                    cache_len=int(cache_len), s_max=k_cache.shape[1], scale=float(scale),
+                    ld_q=_rows_pitch(q, "q"), ld_kv=_rows_pitch(k_new, "k_new"),
+                    q=_vptr(q, torch.float32, "q"), k_new=_vptr(k_new, torch.float32, "k_new"),
+                    v_new=_vptr(v_new, torch.float32, "v_new"), k_cache=_ptr(k_cache, torch.float32, "k_cache"),
+                    v_cache=_ptr(v_cache, torch.float32, "v_cache"), visible=_ptr(visible, torch.int64, "visible"),
+                    out=_ptr(out, torch.float32, "out"))
+    if _rows_pitch(v_new, "v_new") != a.ld_kv:
+        raise ValueError("k_new and v_new must share a row pitch")
+    _check(lib().eagle3_f32_attn(ctypes.byref(a), _stream(stream)), "eagle3_f32_attn")
