@@ -6,23 +6,25 @@
 // ancestors; position = prefix length + depth); "EAGLE-3: Engineering Implementation of LLM
 // Inference Acceleration", appendix C (rotate-half RoPE, GQA, 1/sqrt(D) scaling).
 //
-// One CTA per (sequence b, KV head g, split s).  The query slots times the Hq/Hkv heads that share
-// KV head g form up to 256 query rows (row = slot * rep + head), i.e. up to two 128-row M tiles,
-// so the whole GQA group streams each K/V tile from HBM once.  Warp roles:
-//   warp 0        TMA: 64-key K and V tiles of the prefix (128B-swizzled) into a 3-stage ring
-//   warps 1, 11   tcgen05.mma issuers, one per M tile so that the two tiles' chains do not wait on
-//                 each other: S = Q K^T (M 128, N 64) into a double-buffered TMEM tile, then
-//                 O += P V (M 128, N 128; P read from TMEM, V an MN-major smem operand); a K or V
-//                 stage is released when both issuers have committed
-//   warps 2..9    softmax, four warps per M tile, one thread per query row: the row's 64 scores
-//                 come out of TMEM into registers (no shuffles), masked, exponentiated in the log2
-//                 domain and written back over the same TMEM columns as packed bf16 P; O is
-//                 rescaled in TMEM only when the running maximum grows by more than 8 (the result
-//                 is the same, the intermediate weights stay below 2^8)
-//   warp 10       TMA: V tiles (K and V have separate rings)
-// The last split also processes the tree tile: the query slots' keys are rotated in-kernel at
-// their positions and written back, then masked with the ancestor bitmask.  With more than one
-// split the partial (O, m, l) go to the workspace and a second kernel merges them in split order.
+// One CTA per (sequence b, KV head g, split s, half h).  The query slots times the Hq/Hkv heads
+// that share KV head g form the query rows (row = slot * rep + head); when they are more than one
+// 128-row M tile, the slots are cut into two halves and each half is its own CTA (adjacent blocks,
+// so the second read of every K/V tile comes from L2).  Warp roles:
+//   warp 0        TMA: 128-key K tiles of the prefix (128B-swizzled) into a 3-stage ring
+//   warp 10       TMA: V tiles into a 2-stage ring
+//   warp 1        S = Q K^T (M 128, N 128) into one of three TMEM buffers; S(j) waits only for its
+//                 K tile and for P V(j - 3), which read the buffer last
+//   warp 11       O += P V (M 128, N 128; P read from TMEM, V an MN-major smem operand)
+//   warps 2..9    Q staging (rotated, 16-byte chunks), then the softmax: two
+//                 warps per TMEM lane quarter, each taking half of a row's 128 scores; the two halves
+//                 exchange their row maxima through shared memory once per tile.  Scores are
+//                 exponentiated in the log2 domain and written back over the same TMEM columns as
+//                 packed bf16 P; O is rescaled in TMEM only when the running maximum grows by more
+//                 than 8 (the result is the same, the intermediate weights stay below 2^8)
+// A kernel before this one rotates the query slots' keys in tree_k at their positions (prefix
+// length + depth); the last split then also streams the tree tile (64 rows of tree_k / tree_v, by
+// TMA like the prefix) and masks it with the ancestor bitmask.  With more than one split the
+// partial (O, m, l) go to the workspace and another kernel merges them in split order.
 // All waits are bounded; a timeout sets EAGLE3_DEV_TIMEOUT and the CTA drains and exits.
 #include <cudaTypedefs.h>
 
@@ -33,33 +35,42 @@ namespace e3 {
 namespace {
 
 constexpr int D = 128;
-constexpr int ROWS = 256;           // query rows per CTA (two M tiles)
-constexpr int MT = 128;             // rows per M tile
-constexpr int BK = 64;              // keys per tile
-constexpr int ST = 4;               // K and V stages (each its own ring)
-constexpr int NWARP = 12;             // 0: K loads, 1 and 11: MMA (one per M tile), 2..9: softmax, 10: V loads
+constexpr int MT = 128;             // query rows per CTA (one M tile)
+constexpr int BK = 128;             // keys per prefix tile
+constexpr int BKT = 64;             // keys of the tree tile
+constexpr int ST_K = 3;             // K stages
+constexpr int ST_V = 2;             // V stages
+constexpr int NS = 3;               // S / P buffers in TMEM
+constexpr int NWARP = 12;           // 0: K loads, 1: S MMAs, 2..9: softmax, 10: V loads, 11: P V MMAs
 constexpr int NT = NWARP * 32;
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr int ROPE_TABLE_POS = 32;    // positions in the per-CTA angle table (16 KB of float2)
 
 constexpr uint32_t Q_TILE = MT * D * 2;          // 32 KB: two 64-column blocks of 16 KB
-constexpr uint32_t KV_TILE = BK * D * 2;         // 16 KB: two 64-column blocks of 8 KB
+constexpr uint32_t KV_TILE = BK * D * 2;         // 32 KB: two 64-column blocks of 16 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE;
-constexpr uint32_t OFF_TREE = OFF_KV + ST * 2 * KV_TILE;
-constexpr uint32_t SMEM_DYN = OFF_TREE + 2 * KV_TILE + 1024;   // + alignment slack
+constexpr uint32_t OFF_K = OFF_Q + Q_TILE;                 // K ring; the tree tile (64 keys) uses the first
+constexpr uint32_t OFF_V = OFF_K + ST_K * KV_TILE;         // V ring    half of each 64-column block of a stage
+constexpr uint32_t OFF_TABLE = OFF_V + KV_TILE;            // RoPE angles while Q is staged (V stage 1)
+constexpr uint32_t SMEM_DYN = OFF_V + ST_V * KV_TILE + 1024;   // + alignment slack
+// TMEM columns: O at [0, 128); S / P buffer u at TM_S + 128 u
+constexpr uint32_t TM_S = 128;
 static_assert(SMEM_DYN + 1024 <= 232448, "shared memory budget");
-static_assert(ROPE_TABLE_POS * (D / 2) * sizeof(float2) <= KV_TILE, "angle table fits the tree-V tile");
+static_assert(ROPE_TABLE_POS * (D / 2) * sizeof(float2) <= KV_TILE, "angle table fits a V stage");
+static_assert(TM_S + NS * BK <= 512, "TMEM budget");
 
 struct Params {
     int B, n_slots, q_lo, q_hi, Hq, Hkv, S, splits, tiles_per_split, rep, max_prefix;
+    int halves;                     // CTAs per (sequence, KV head, split): 1 or 2
+    int tree_slot_inner;            // tree maps: slots are the middle dimension (else the outer)
+    int s_mid;                      // with two halves, the first half's query slots are [q_lo, q_lo + s_mid)
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
     // element (b, slot i, head h) lives at base + b * sb + i * si + h * D
     const __nv_bfloat16 *q;
     int64_t q_sb, q_si;
-    __nv_bfloat16 *k;               // tree keys; slots [q_lo, q_hi) are rotated in place
+    __nv_bfloat16 *k;               // tree keys; slots [q_lo, q_hi) are rotated in place (second kernel)
     int64_t k_sb, k_si;
     const __nv_bfloat16 *v;
     int64_t v_sb, v_si;
@@ -76,14 +87,17 @@ struct Params {
 };
 
 struct SmemStatic {
-    uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
-    // every per-tile barrier is double-buffered by tile parity: a producer may run one tile ahead
-    // of its consumer, and a phase that completes twice before it is awaited would be lost
-    uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], mma_done[2];
+    uint64_t k_full[ST_K], k_empty[ST_K], v_full[ST_V], v_empty[ST_V];
+    // per S / P buffer u (tiles u, u + 3, ...): a phase can never complete twice before it is
+    // awaited, because S(j + 3) waits for P V(j), which waits for P(j)
+    uint64_t s_full[NS], p_full[NS], pv_done[NS];
+    uint64_t s_done, pv_mma_done;
     uint64_t q_ready;               // the softmax warps have staged Q (and the tree tile)
     uint64_t anc[64];
     int32_t pos[64];
     int32_t par[64];
+    float mx_x[2][2][MT];           // [tile parity][column half][row]: each half's row maximum
+    float l_x[2][MT];               // [column half][row]: each half's row sum, at the end
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -137,20 +151,24 @@ E3_DEV void rope_chunks(uint4 &lo, uint4 &hi, const float cs[8], const float sn[
 
 __global__ void __launch_bounds__(NT, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_tk, const __grid_constant__ CUtensorMap tm_tv,
                        const Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ SmemStatic ss;
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     volatile int *abort = &ss.abort_flag;
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int half = blockIdx.x % p.halves, split = blockIdx.x / p.halves, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo, nrows = nq * rep;
-    const int n_mt = (nrows + MT - 1) / MT;
+    const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo;
+    // this CTA's query slots [s_lo, s_hi) and rows (row = (slot - s_lo) * rep + head)
+    const int s_lo = p.q_lo + (half ? p.s_mid : 0);
+    const int s_hi = p.halves == 1 ? p.q_hi : (half ? p.q_hi : p.q_lo + p.s_mid);
+    const int nrows = (s_hi - s_lo) * rep;
     const bool last = split == p.splits - 1;
 
     int L = p.prefix_len[b];
     if (L < 0 || L > p.max_prefix) {
-        if (tid == 0 && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
+        if (tid == 0 && split == 0 && g == 0 && half == 0) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
         L = max(0, min(L, p.max_prefix));
     }
     const int t_lo = split * p.tiles_per_split;
@@ -161,21 +179,21 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- phase A: barriers, TMEM, raw tree description into shared memory
     if (tid == 0) {
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < ST_K; ++s) {
             tc::mbar_init(&ss.k_full[s], 1);
-            tc::mbar_init(&ss.k_empty[s], n_mt);
+            tc::mbar_init(&ss.k_empty[s], 1);
+        }
+        for (int s = 0; s < ST_V; ++s) {
             tc::mbar_init(&ss.v_full[s], 1);
-            tc::mbar_init(&ss.v_empty[s], n_mt);
+            tc::mbar_init(&ss.v_empty[s], 1);
         }
-        for (int m = 0; m < 2; ++m) {
-            for (int u = 0; u < 2; ++u) tc::mbar_init(&ss.s_full[m][u], 1);
-            tc::mbar_init(&ss.p_full[m][0], 4);
-            tc::mbar_init(&ss.p_full[m][1], 4);
-            tc::mbar_init(&ss.pv_done[m][0], 1);
-            tc::mbar_init(&ss.pv_done[m][1], 1);
+        for (int u = 0; u < NS; ++u) {
+            tc::mbar_init(&ss.s_full[u], 1);
+            tc::mbar_init(&ss.p_full[u], 8);
+            tc::mbar_init(&ss.pv_done[u], 1);
         }
-        tc::mbar_init(&ss.mma_done[0], 1);
-        tc::mbar_init(&ss.mma_done[1], 1);
+        tc::mbar_init(&ss.s_done, 1);
+        tc::mbar_init(&ss.pv_mma_done, 1);
         tc::mbar_init(&ss.q_ready, 8);
         ss.abort_flag = 0;
         tc::fence_barrier_init();
@@ -197,110 +215,127 @@ __global__ void __launch_bounds__(NT, 1)
     tc::fence_after();
     const uint32_t tmem = ss.tmem_base;
 
+    auto k_tile = [&](int j) -> uint8_t * { return sm + OFF_K + (j % ST_K) * KV_TILE; };
+    auto v_tile = [&](int j) -> uint8_t * { return sm + OFF_V + (j % ST_V) * KV_TILE; };
+
     if (warp == 0 || warp == 10) {
         // ------------------------------------------------------------------ TMA producers
-        // warp 0 streams K tiles, warp 10 V tiles; each has its own ring so that a K stage is
-        // refilled as soon as its S MMA is done, long before the V of the same tile is used
-        if (lane == 0 && n_prefix > 0) {
+        // warp 0 streams K tiles, warp 10 V tiles: the prefix from the cache, then (last split)
+        // the tree tile, 64 rows of this KV head's tree keys / values (rotated beforehand)
+        if (lane == 0 && n_tiles > 0) {
             const bool is_k = warp == 0;
+            const int stages = is_k ? ST_K : ST_V;
             const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+            const CUtensorMap *tmap = is_k ? &tm_tk : &tm_tv;
             uint64_t *full = is_k ? ss.k_full : ss.v_full;
             uint64_t *empty = is_k ? ss.k_empty : ss.v_empty;
-            uint8_t *ring = sm + OFF_KV + (is_k ? 0 : ST * KV_TILE);
+            uint8_t *ring = sm + (is_k ? OFF_K : OFF_V);
             tc::prefetch_tmap(map);
+            if (last) tc::prefetch_tmap(tmap);
+            // V stage 1 holds the RoPE angle table until Q is staged
+            bool go = is_k || tc::mbar_wait(&ss.q_ready, 0, abort);
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             uint32_t issued = 0, last_par = 0;
-            for (int j = 0; j < n_prefix; ++j) {
-                const int s = j % ST;
-                const uint32_t ph = (uint32_t)(j / ST) & 1u;
+            for (int j = 0; j < n_tiles && go; ++j) {
+                const int s = j % stages;
+                const uint32_t ph = (uint32_t)(j / stages) & 1u;
                 if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) {
                     flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
                     break;
                 }
                 uint8_t *dst = ring + s * KV_TILE;
-                tc::mbar_expect_tx(&full[s], KV_TILE);
-                const int y = row0 + j * BK;
-                tc::tma_load_2d(dst, map, 0, y, &full[s]);
-                tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
+                if (j < n_prefix) {
+                    tc::mbar_expect_tx(&full[s], KV_TILE);
+                    const int y = row0 + j * BK;
+                    tc::tma_load_2d(dst, map, 0, y, &full[s]);
+                    tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
+                } else {
+                    tc::mbar_expect_tx(&full[s], 2 * BKT * 128);
+                    const int y = p.tree_slot_inner ? 0 : b, z = p.tree_slot_inner ? b : 0;
+                    tc::tma_load_3d(dst, tmap, g * D, y, z, &full[s]);
+                    tc::tma_load_3d(dst + KV_TILE / 2, tmap, g * D + 64, y, z, &full[s]);
+                }
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
             }
+            if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             // no TMA write may be in flight when the CTA exits (bounded)
-            for (int s = 0; s < ST; ++s) {
+            for (int s = 0; s < stages; ++s) {
                 if (!((issued >> s) & 1u)) continue;
                 const long long t0 = clock64();
                 while (!tc::mbar_try(&full[s], (last_par >> s) & 1u) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
                 }
             }
         }
-    } else if (warp == 1 || warp == 11) {
-        // ------------------------------------------------------------------ MMA issuers
-        const int m = warp == 1 ? 0 : 1;
-        if (lane == 0 && n_tiles > 0 && m < n_mt) {
-            constexpr uint32_t IDESC_S = tc::idesc_bf16(MT, BK);
-            constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
-            bool ok = true;
-            auto k_tile = [&](int j) -> uint8_t * {
-                return j < n_prefix ? sm + OFF_KV + (j % ST) * KV_TILE : sm + OFF_TREE;
-            };
-            auto v_tile = [&](int j) -> uint8_t * {
-                return j < n_prefix ? sm + OFF_KV + (ST + j % ST) * KV_TILE : sm + OFF_TREE + KV_TILE;
-            };
-            // Q and the tree tile are written by the softmax warps (generic proxy, fenced)
-            if (!tc::mbar_wait(&ss.q_ready, 0, abort)) ok = false;
-            auto issue_s = [&](int j) {
-                if (j < n_prefix) {
-                    if (!tc::mbar_wait(&ss.k_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
-                        ok = false;
-                        return;
-                    }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ S = Q K^T issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t IDESC_P = tc::idesc_bf16(MT, BK);
+            constexpr uint32_t IDESC_T = tc::idesc_bf16(MT, BKT);
+            bool ok = tc::mbar_wait(&ss.q_ready, 0, abort);   // Q and the tree tile are staged
+            const uint32_t qaddr = smem_u32(sm + OFF_Q);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const bool tree = j == n_prefix;
+                if (!tc::mbar_wait(&ss.k_full[j % ST_K], (uint32_t)(j / ST_K) & 1u, abort)) {
+                    ok = false;
+                    break;
                 }
-                // the S/P buffer j & 1 last held P(j - 2), read by P V(j - 2): that MMA was issued earlier
-                // by this thread, and tcgen05.mma operations from one thread execute in issue order,
-                // so S(j) cannot overwrite P(j - 2) before it has been read; no wait is needed
+                // buffer j % 3 last held P(j - 3): P V(j - 3) must have read it (another thread issues it)
+                if (j >= NS && !tc::mbar_wait(&ss.pv_done[j % NS], (uint32_t)((j - NS) / NS) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
                 tc::fence_after();
                 const uint32_t kaddr = smem_u32(k_tile(j));
-                const uint32_t qaddr = smem_u32(sm + OFF_Q + m * Q_TILE);
-                const uint32_t d_s = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);
+                const uint32_t kblk = KV_TILE / 2;
+                const uint32_t d_s = tmem + TM_S + (uint32_t)((j % NS) * BK);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
                     tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
-                                    tc::desc_sw128(kaddr + blk * (KV_TILE / 2) + kk * 32), IDESC_S, k > 0 ? 1u : 0u);
+                                    tc::desc_sw128(kaddr + blk * kblk + kk * 32), tree ? IDESC_T : IDESC_P,
+                                    k > 0 ? 1u : 0u);
                 }
-                tc::mma_commit(&ss.s_full[m][j & 1]);
-                if (j < n_prefix) tc::mma_commit(&ss.k_empty[j % ST]);   // K stage free once S is done
-            };
-            // two S tiles in flight; each iteration: P V of tile j as soon as its P is ready, then S(j + 2)
-            if (ok) issue_s(0);
-            if (n_tiles > 1 && ok) issue_s(1);
+                tc::mma_commit(&ss.s_full[j % NS]);
+                tc::mma_commit(&ss.k_empty[j % ST_K]);   // K stage free once S is done
+            }
+            if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            tc::mma_commit(&ss.s_done);
+            const long long t0 = clock64();
+            while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            }
+        }
+    } else if (warp == 11) {
+        // ------------------------------------------------------------------ O += P V issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
+            bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j < n_prefix && !tc::mbar_wait(&ss.v_full[j % ST], (uint32_t)(j / ST) & 1u, abort)) {
+                const bool tree = j == n_prefix;
+                if (!tc::mbar_wait(&ss.v_full[j % ST_V], (uint32_t)(j / ST_V) & 1u, abort)) {
                     ok = false;
                     break;
                 }
-                const uint32_t vaddr = smem_u32(v_tile(j));
-                if (!tc::mbar_wait(&ss.p_full[m][j & 1], (uint32_t)(j >> 1) & 1u, abort)) {
+                if (!tc::mbar_wait(&ss.p_full[j % NS], (uint32_t)(j / NS) & 1u, abort)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
-                const uint32_t t_p = tmem + 256u + (uint32_t)(m * 128 + (j & 1) * 64);   // P over S
-                const uint32_t d_o = tmem + (uint32_t)(m * 128);
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    tc::mma_bf16_ts(d_o, t_p + (uint32_t)(kk * 8),
-                                    tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                const uint32_t vaddr = smem_u32(v_tile(j));
+                const uint32_t vblk = KV_TILE / 2;
+                const uint32_t t_p = tmem + TM_S + (uint32_t)((j % NS) * BK);   // P over S
+                const int ksteps = (tree ? BKT : BK) / 16;
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    tc::mma_bf16_ts(tmem, t_p + (uint32_t)(kk * 8), tc::desc_mn_sw128(vaddr + kk * 2048, vblk, 1024),
+                                    IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc::mma_commit(&ss.pv_done[m][j & 1]);
-                if (j < n_prefix) tc::mma_commit(&ss.v_empty[j % ST]);
-                if (j + 2 < n_tiles) issue_s(j + 2);
+                tc::mma_commit(&ss.pv_done[j % NS]);
+                tc::mma_commit(&ss.v_empty[j % ST_V]);
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
-            tc::mma_commit(&ss.mma_done[m]);
+            tc::mma_commit(&ss.pv_mma_done);
             const long long t0 = clock64();
-            while (!tc::mbar_try(&ss.mma_done[m], 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            while (!tc::mbar_try(&ss.pv_mma_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
             }
         }
     } else {
@@ -324,23 +359,21 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 ss.anc[i] = bits;
                 ss.pos[i] = L + d;
-                if (bad && split == 0 && g == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+                if (bad && split == 0 && g == 0 && half == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
             }
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight softmax warps only
         {
             const int c = lane & 7, sub = lane >> 3;
-            // RoPE angles: the slots of a tree share few positions (prefix length + depth), so
-            // cos / sin of every position in [pos_lo, pos_lo + span) are computed once per CTA into
-            // the tree-V tile area (free until the tree V rows are staged below); a position
-            // outside the table is computed directly.  Same arguments, so the same values.
+            // RoPE angles of every position in [pos_lo, pos_lo + span), once per CTA, in V stage 1
+            // (its first load waits for Q to be staged); others are computed directly
             int pos_lo = 0x7fffffff, pos_hi = -1;
             for (int i = 0; i < nk; ++i) {
                 pos_lo = min(pos_lo, ss.pos[i]);
                 pos_hi = max(pos_hi, ss.pos[i]);
             }
             const int span = min(pos_hi - pos_lo + 1, ROPE_TABLE_POS);
-            float2 *table = reinterpret_cast<float2 *>(sm + OFF_TREE + KV_TILE);
+            float2 *table = reinterpret_cast<float2 *>(sm + OFF_TABLE);
             for (int e = tid - 64; e < span * (D / 2); e += 256) {
                 float sn, cs;
                 sincosf(__fmul_rn((float)(pos_lo + e / (D / 2)), p.inv_freq[e % (D / 2)]), &sn, &cs);
@@ -363,32 +396,15 @@ __global__ void __launch_bounds__(NT, 1)
                     rope_angles((float)pos, p.inv_freq, c, cs, sn);
                 }
             };
-            // tree rows of the last split: issued first, used after the Q rows
-            uint4 kl[2], kh[2], vl[2], vh[2];
-            if (last) {
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int i = w8 * 4 + sub + 32 * t;
-                    if (i < nk) {
-                        const __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
-                        const __nv_bfloat16 *vg = p.v + (size_t)b * p.v_sb + (size_t)i * p.v_si + (size_t)g * D;
-                        kl[t] = ld16(kg + 8 * c);
-                        kh[t] = ld16(kg + 64 + 8 * c);
-                        vl[t] = ld16(vg + 8 * c);
-                        vh[t] = ld16(vg + 64 + 8 * c);
-                    }
-                }
-            }
-            // Q rows (row = slot * rep + head), rotated at the slot's position.  Warp w8 takes the
-            // slots w8 + 8 t (t < 8, i.e. all of them, nq <= 64), lane group `sub` the heads
-            // sub + 4 h; all of a warp's loads are issued before the first is used.
+            // Q rows of this CTA's slots: warp w8 takes slots s_lo + w8 + 8 t, lane group `sub` the
+            // heads sub + 4 h; all of a warp's loads are issued before the first is used
             for (int hh = sub, h4 = 0; h4 * 4 < rep; hh += 4, ++h4) {
                 uint4 lo[8], hi[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int sl = w8 + 8 * t;
-                    if (sl < nq && hh < rep) {
-                        const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)(p.q_lo + sl) * p.q_si +
+                    if (s_lo + sl < s_hi && hh < rep) {
+                        const __nv_bfloat16 *src = p.q + (size_t)b * p.q_sb + (size_t)(s_lo + sl) * p.q_si +
                                                    ((size_t)g * rep + hh) * D;
                         lo[t] = ld16(src + 8 * c);
                         hi[t] = ld16(src + 64 + 8 * c);
@@ -397,203 +413,183 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     const int sl = w8 + 8 * t;
-                    if (sl < nq && hh < rep) {
+                    if (s_lo + sl < s_hi && hh < rep) {
                         float cs[8], sn[8];
-                        angles(ss.pos[p.q_lo + sl], cs, sn);
+                        angles(ss.pos[s_lo + sl], cs, sn);
                         rope_chunks(lo[t], hi[t], cs, sn);
                         const int r = sl * rep + hh;
-                        uint8_t *tile = sm + OFF_Q + (r / MT) * Q_TILE;
-                        st_chunk(tile, r % MT, c, Q_TILE / 2, lo[t]);
-                        st_chunk(tile, r % MT, c + 8, Q_TILE / 2, hi[t]);
+                        st_chunk(sm + OFF_Q, r, c, Q_TILE / 2, lo[t]);
+                        st_chunk(sm + OFF_Q, r, c + 8, Q_TILE / 2, hi[t]);
                     }
                 }
             }
-            // zero rows of the last M tile
+            // zero rows of the M tile
             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            for (int k = (tid - 64); k < (n_mt * MT - nrows) * 16; k += 256) {
+            for (int k = (tid - 64); k < (MT - nrows) * 16; k += 256) {
                 const int r = nrows + k / 16, ch = k % 16;
-                st_chunk(sm + OFF_Q + (r / MT) * Q_TILE, r % MT, ch, Q_TILE / 2, z);
-            }
-            if (last) {
-                // the tree tile: keys of the query slots rotated (and written back), others copied;
-                // then the values, over the angle table
-                uint8_t *tk = sm + OFF_TREE, *tv = sm + OFF_TREE + KV_TILE;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int i = w8 * 4 + sub + 32 * t;
-                    if (i < nk) {
-                        __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
-                        uint4 klo = kl[t], khi = kh[t];
-                        if (i >= p.q_lo) {
-                            float cs[8], sn[8];
-                            angles(ss.pos[i], cs, sn);
-                            rope_chunks(klo, khi, cs, sn);
-                            *reinterpret_cast<uint4 *>(kg + 8 * c) = klo;
-                            *reinterpret_cast<uint4 *>(kg + 64 + 8 * c) = khi;
-                        }
-                        st_chunk(tk, i, c, KV_TILE / 2, klo);
-                        st_chunk(tk, i, c + 8, KV_TILE / 2, khi);
-                    } else {
-                        st_chunk(tk, i, c, KV_TILE / 2, z);
-                        st_chunk(tk, i, c + 8, KV_TILE / 2, z);
-                    }
-                }
-                asm volatile("bar.sync 1, 256;" ::: "memory");   // every table read is done
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const int i = w8 * 4 + sub + 32 * t;
-                    if (i < nk) {
-                        st_chunk(tv, i, c, KV_TILE / 2, vl[t]);
-                        st_chunk(tv, i, c + 8, KV_TILE / 2, vh[t]);
-                    } else {
-                        st_chunk(tv, i, c, KV_TILE / 2, z);
-                        st_chunk(tv, i, c + 8, KV_TILE / 2, z);
-                    }
-                }
+                st_chunk(sm + OFF_Q, r, ch, Q_TILE / 2, z);
             }
             tc::fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor cores
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ss.q_ready);
         }
-        const int m = (warp - 2) >> 2;
+        // two warps per TMEM lane quarter: quarter = warp % 4 (the lanes this warp may access),
+        // hc = which half of the tile's columns (and of O's columns) this warp takes
         const int quarter = warp & 3;
+        const int hc = w8 >> 2;
         const int rl = quarter * 32 + lane;              // row within the M tile
-        const int row = m * MT + rl;
-        if (m < n_mt) {
-            const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-            const uint64_t bits = row < nrows ? ss.anc[p.q_lo + row / rep] : 0ull;
-            float m_run = -INFINITY, l_run = 0.0f;
-            bool ok = true;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int u = j & 1;
-                if (!warp_wait(&ss.s_full[m][u], (uint32_t)(j >> 1) & 1u, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after();
-                float sc[64];
-                {
-                    float a[32], c[32];
-                    tc::tmem_ld32(t_lane + 256u + (uint32_t)(m * 128 + u * 64), a);
-                    tc::tmem_ld32(t_lane + 256u + (uint32_t)(m * 128 + u * 64 + 32), c);
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint64_t bits = rl < nrows ? ss.anc[s_lo + rl / rep] : 0ull;
+        float m_run = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        // every softmax warp runs every iteration (the row-maximum exchange is a barrier of all
+        // eight): after a timeout a warp skips its waits and finishes the loop on garbage
+        for (int j = 0; j < n_tiles; ++j) {
+            const int u = j % NS;
+            if (ok && !warp_wait(&ss.s_full[u], (uint32_t)(j / NS) & 1u, abort)) ok = false;
+            tc::fence_after();
+            const bool tree = j == n_prefix;             // the last split's final tile
+            const int hw = (tree ? BKT : BK) / 2;        // columns of this warp: 64 (prefix) or 32 (tree)
+            const int col0 = hc * hw;                    // first of them within the tile
+            float sc[64];
+            {
+                float a[32];
+                tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0), a);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        sc[i] = a[i];
-                        sc[32 + i] = c[i];
-                    }
-                }
-                const bool tree = j == n_prefix;         // the last split's final tile
-                const int key0 = k_lo + j * BK;
-                const bool full = !tree && key0 + BK <= k_hi;  // every key of the tile is visible
-                // scale (and mask) with four independent max chains
-                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (full) {
+                for (int i = 0; i < 32; ++i) sc[i] = a[i];
+                if (hw == 64) {
+                    tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0 + 32), a);
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        sc[i] *= p.scale_log2;
-                        mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
-                    }
+                    for (int i = 0; i < 32; ++i) sc[32 + i] = a[i];
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const bool valid = tree ? (i < nk && ((bits >> i) & 1ull)) : (key0 + i < k_hi);
-                        sc[i] = valid ? sc[i] * p.scale_log2 : -INFINITY;
-                        mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
-                    }
+                    for (int i = 0; i < 32; ++i) sc[32 + i] = -INFINITY;
                 }
-                const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-                const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
-                const bool any_need = __any_sync(0xffffffffu, need);
-                if (any_need && j > 0) {
-                    // O is about to be rescaled: the previous P V must be finished first
-                    if (!warp_wait(&ss.pv_done[m][(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                }
-                if (any_need) {
-                    const float m_new = need ? fmaxf(m_run, mx) : m_run;
-                    const float corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
-                    if (j > 0) {
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            tc::tmem_ld32(t_lane + (uint32_t)(m * 128 + c * 32), o);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= corr;
-                            tc::tmem_st32(t_lane + (uint32_t)(m * 128 + c * 32), o);
-                        }
-                    }
-                    l_run *= corr;
-                    m_run = m_new;
-                }
-                const float mu = m_run == -INFINITY ? 0.0f : m_run;
-                // exponentials and the row sum (four chains), packed to bf16 pairs
-                uint32_t pk[32];
-                float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = fast_exp2(sc[2 * e] - mu), p1 = fast_exp2(sc[2 * e + 1] - mu);
-                    sq[e & 3] += p0 + p1;
-                    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                    pk[e] = *reinterpret_cast<uint32_t *>(&h);
-                }
-                const float sum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
-                // P over the S columns it came from (the next S into this buffer waits for P V)
-                tc::tmem_st32u(t_lane + 256u + (uint32_t)(m * 128 + u * 64), pk);
-                l_run += sum;
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.p_full[m][j & 1]);
             }
-            if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
-            // ---- epilogue: O / l
-            float o[D];
-            bool have = false;
-            if (ok && n_tiles > 0 &&
-                warp_wait(&ss.pv_done[m][(n_tiles - 1) & 1], (uint32_t)((n_tiles - 1) >> 1) & 1u, abort)) {
+            const int key0 = k_lo + j * BK + col0;
+            const bool full = !tree && key0 + hw <= k_hi;   // every key of this half is visible
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    sc[i] *= p.scale_log2;
+                    mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const int key = col0 + i;            // tree: node index
+                    const bool valid =
+                        i < hw && (tree ? (key < nk && ((bits >> key) & 1ull)) : (key0 + i < k_hi));
+                    sc[i] = valid ? sc[i] * p.scale_log2 : -INFINITY;
+                    mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
+                }
+            }
+            // row maximum of the whole tile: exchange with the warp holding the other half
+            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            ss.mx_x[j & 1][hc][rl] = mx;
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            mx = fmaxf(mx, ss.mx_x[j & 1][hc ^ 1][rl]);
+            const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
+            const bool any_need = __any_sync(0xffffffffu, need);
+            if (any_need && j > 0) {
+                // O is about to be rescaled: the previous P V must be finished first
+                if (ok && !warp_wait(&ss.pv_done[(j - 1) % NS], (uint32_t)((j - 1) / NS) & 1u, abort)) ok = false;
                 tc::fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float t[32];
-                    tc::tmem_ld32(t_lane + (uint32_t)(m * 128 + c * 32), t);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[c * 32 + i] = t[i];
-                }
-                have = true;
             }
-            if (!have) {
-                m_run = -INFINITY;
-                l_run = 0.0f;
+            if (any_need) {
+                const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                const float corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
+                if (j > 0) {
 #pragma unroll
-                for (int i = 0; i < D; ++i) o[i] = 0.0f;
-            }
-            if (row < nrows) {
-                const int qi = row / rep, h = g * rep + row % rep;
-                const size_t prow_i = ((size_t)b * nq + qi) * p.Hq + h;
-                if (p.splits == 1) {
-                    __nv_bfloat16 *dst = p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D;
-                    const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+                    for (int cc = 0; cc < 2; ++cc) {   // this warp's 64 columns of O
+                        float o[32];
+                        const uint32_t ta = t_lane + (uint32_t)(hc * 64 + cc * 32);
+                        tc::tmem_ld32(ta, o);
 #pragma unroll
-                    for (int c = 0; c < D; c += 8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 hv = __floats2bfloat162_rn(o[c + 2 * e] * inv_l, o[c + 2 * e + 1] * inv_l);
-                            w[e] = *reinterpret_cast<uint32_t *>(&hv);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int i = 0; i < 32; ++i) o[i] *= corr;
+                        tc::tmem_st32(ta, o);
                     }
-                    if (p.lse) p.lse[prow_i] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-                } else {
-                    const size_t rows_all = (size_t)p.B * nq * p.Hq;
-                    float *po = p.part_o + ((size_t)split * rows_all + prow_i) * D;
+                }
+                l_run *= corr;
+                m_run = m_new;
+            }
+            const float mu = m_run == -INFINITY ? 0.0f : m_run;
+            // exponentials and this half's row sum (four chains), packed to bf16 pairs
+            uint32_t pk[32];
+            float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(po + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = fast_exp2(sc[2 * e] - mu), p1 = fast_exp2(sc[2 * e + 1] - mu);
+                sq[e & 3] += p0 + p1;
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+            // P of this half over the buffer's first columns: both halves have read their scores
+            // (they exchanged maxima after their loads), so the writes cannot overtake a read
+            if (hw == 64)
+                tc::tmem_st32u(t_lane + TM_S + (uint32_t)(u * BK + hc * 32), pk);
+            else
+                tc::tmem_st16u(t_lane + TM_S + (uint32_t)(u * BK + hc * 16), pk);   // tree tile: 16 columns
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ss.p_full[u]);
+        }
+        if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+        // ---- epilogue: this warp's 64 columns of O / l
+        ss.l_x[hc][rl] = l_run;
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        const float l_all = ss.l_x[0][rl] + ss.l_x[1][rl];
+        float o[64];
+        bool have = false;
+        if (ok && n_tiles > 0 &&
+            warp_wait(&ss.pv_done[(n_tiles - 1) % NS], (uint32_t)((n_tiles - 1) / NS) & 1u, abort)) {
+            tc::fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                float t[32];
+                tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[cc * 32 + i] = t[i];
+            }
+            have = true;
+        }
+        float m_fin = m_run, l_fin = l_all;
+        if (!have) {
+            m_fin = -INFINITY;
+            l_fin = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) o[i] = 0.0f;
+        }
+        if (rl < nrows) {
+            const int qi = s_lo - p.q_lo + rl / rep, h = g * rep + rl % rep;
+            const size_t prow_i = ((size_t)b * nq + qi) * p.Hq + h;
+            if (p.splits == 1) {
+                __nv_bfloat16 *dst =
+                    p.out + (size_t)b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D + (size_t)hc * 64;
+                const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        __nv_bfloat162 hv = __floats2bfloat162_rn(o[cc + 2 * e] * inv_l, o[cc + 2 * e + 1] * inv_l);
+                        w[e] = *reinterpret_cast<uint32_t *>(&hv);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                if (p.lse && hc == 0) p.lse[prow_i] = (m_fin + log2f(l_fin)) * 0.6931471805599453f;
+            } else {
+                const size_t rows_all = (size_t)p.B * nq * p.Hq;
+                float *po = p.part_o + ((size_t)split * rows_all + prow_i) * D + (size_t)hc * 64;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 4)
+                    *reinterpret_cast<float4 *>(po + cc) = make_float4(o[cc], o[cc + 1], o[cc + 2], o[cc + 3]);
+                if (hc == 0) {
                     float *pm = p.part_ml + ((size_t)split * rows_all + prow_i) * 2;
-                    pm[0] = m_run;
-                    pm[1] = l_run;
+                    pm[0] = m_fin;
+                    pm[1] = l_fin;
                 }
             }
         }
@@ -606,6 +602,46 @@ __global__ void __launch_bounds__(NT, 1)
         tc::fence_after();
         tc::tmem_dealloc(tmem, 512);
     }
+}
+
+// Rotated tree keys back into tree_k: one warp per (sequence, query slot, KV head), at the slot's
+// position (prefix length + depth from the parent array, or the given position), with the same
+// angle arguments and arithmetic the attention kernel used in shared memory.
+__global__ void tree_rotate_kernel(const Params p) {
+    const int nq = p.q_hi - p.q_lo;
+    const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= (int64_t)p.B * nq * p.Hkv) return;
+    const int g = (int)(w % p.Hkv);
+    const int i = p.q_lo + (int)((w / p.Hkv) % nq);
+    const int b = (int)(w / ((int64_t)p.Hkv * nq));
+    int pos;
+    if (p.parents) {
+        int L = p.prefix_len[b];
+        L = max(0, min(L, p.max_prefix));
+        const int32_t *par = p.parents + (size_t)b * p.n_slots;
+        auto invalid = [&](int j) {
+            const int pj = par[j];
+            return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
+        };
+        int d = 0, j = i;
+        while (j > 0 && !invalid(j)) {
+            j = par[j];
+            ++d;
+        }
+        pos = L + d;
+    } else {
+        pos = p.pos[(size_t)b * p.pos_sb + i];
+    }
+    const int c = lane & 7, part = lane >> 3;   // lanes 0..7 take the row, the others idle
+    if (part != 0) return;
+    __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
+    uint4 lo = ld16(kg + 8 * c), hi = ld16(kg + 64 + 8 * c);
+    float cs[8], sn[8];
+    rope_angles((float)pos, p.inv_freq, c, cs, sn);
+    rope_chunks(lo, hi, cs, sn);
+    *reinterpret_cast<uint4 *>(kg + 8 * c) = lo;
+    *reinterpret_cast<uint4 *>(kg + 64 + 8 * c) = hi;
 }
 
 // Merge split partials in split order: one warp per (b, query slot, head) row.
@@ -652,6 +688,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [rows, 128] bf16 cache viewed as a 2-D tensor; 64 x 64 boxes, 128-byte swizzle
+// tree K or V of one launch part as a 3-D tensor of the Hkv * D elements of a node, the slots < nk
+// and the sequences, the outer two ordered by pitch (slot-major when the slot pitch is the smaller);
+// boxes of 64 elements x 64 slots x 1 sequence, 128-byte swizzle: in shared memory a box is 64 slot
+// rows of 128 B, laid out like the first 64 keys of a cache tile; slots >= nk read as zeros
+bool make_tree_map(CUtensorMap *m, const void *base, int nb, int nk, int64_t kv_width, int64_t sb, int64_t si) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const bool slot_inner = si <= sb;
+    const cuuint64_t dims[3] = {(cuuint64_t)kv_width, (cuuint64_t)(slot_inner ? nk : nb), (cuuint64_t)(slot_inner ? nb : nk)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(slot_inner ? si : sb) * 2, (cuuint64_t)(slot_inner ? sb : si) * 2};
+    const cuuint32_t box[3] = {64, slot_inner ? (cuuint32_t)BKT : 1u, slot_inner ? 1u : (cuuint32_t)BKT};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_cache_map(CUtensorMap *m, const void *base, int64_t rows) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -684,6 +737,20 @@ int sm_count_cached() {
     return n;
 }
 
+// Query rows of a (sequence, KV head): one 128-row M tile per CTA; more rows are cut into two
+// halves of whole slots.  Returns the CTAs per (sequence, KV head, split) and the first half's
+// slot count, or 0 when the rows do not fit (a half would exceed 128 rows).
+int plan_halves(int nq, int rep, int *s_mid) {
+    if (nq * rep <= MT) {
+        *s_mid = nq;
+        return 1;
+    }
+    const int mid = (nq + 1) / 2;
+    if (mid * rep > MT || (nq - mid) * rep > MT) return 0;
+    *s_mid = mid;
+    return 2;
+}
+
 // A launch covers sequences [b0, b0 + nb) with `splits` KV splits.  When the (sequence, KV head)
 // blocks fill some waves of the GPU and leave a tail smaller than half a wave, the full waves run
 // unsplit and the tail sequences are split over the SMs the tail would leave idle.
@@ -693,10 +760,12 @@ struct Part {
 
 int plan_parts(const AttnLaunch &a, Part parts[2]) {
     const int sms = sm_count_cached();
-    const int items = a.B * a.Hkv;
+    int s_mid = 0;
+    const int per_b = a.Hkv * max(1, plan_halves(a.q_hi - a.q_lo, a.Hq / a.Hkv, &s_mid));   // CTAs per sequence
+    const int items = a.B * per_b;
     if (a.num_splits == 0 && items > sms && items % sms) {
-        const int b0 = (items / sms) * sms / a.Hkv;
-        const int tail = (a.B - b0) * a.Hkv;
+        const int b0 = (items / sms) * sms / per_b;
+        const int tail = (a.B - b0) * per_b;
         if (b0 > 0 && b0 < a.B && 2 * tail <= sms) {
             parts[0] = {0, b0, 1};
             parts[1] = {b0, a.B - b0, plan_splits(tail, a.max_prefix, 0, sms)};
@@ -726,6 +795,8 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     p.Hkv = a.Hkv;
     p.S = a.S;
     p.rep = a.Hq / a.Hkv;
+    p.halves = plan_halves(nq, p.rep, &p.s_mid);
+    if (p.halves == 0) return EAGLE3_ERR_UNSUPPORTED;
     p.splits = splits;
     const int tiles = (a.max_prefix + BK - 1) / BK;
     p.tiles_per_split = max(1, (tiles + splits - 1) / splits);
@@ -757,12 +828,25 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     p.part_ml = splits > 1 ? (float *)workspace + (size_t)splits * rows * D : nullptr;
 
     CUtensorMap mk, mv;
+    const int nk_all = a.q_hi;                       // tree slots visible as keys
+    p.tree_slot_inner = a.k_si <= a.k_sb ? 1 : 0;
+    if ((a.v_si <= a.v_sb ? 1 : 0) != p.tree_slot_inner) return EAGLE3_ERR_UNSUPPORTED;
     const size_t cache_off = b0 * a.Hkv * a.S * D;
     const int64_t cache_rows = (int64_t)pt.nb * a.Hkv * a.S;
     if (!make_cache_map(&mk, a.k_cache + cache_off, cache_rows) ||
         !make_cache_map(&mv, a.v_cache + cache_off, cache_rows))
         return EAGLE3_ERR_CUDA;
-    verify_attn_kernel<<<dim3(splits, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, p);
+    CUtensorMap mtk, mtv;
+    if (!make_tree_map(&mtk, p.k, pt.nb, nk_all, (int64_t)a.Hkv * D, a.k_sb, a.k_si) ||
+        !make_tree_map(&mtv, p.v, pt.nb, nk_all, (int64_t)a.Hkv * D, a.v_sb, a.v_si))
+        return EAGLE3_ERR_CUDA;
+    {
+        // the query slots' keys rotated in tree_k first; the attention streams them like the prefix
+        const int64_t warps = (int64_t)pt.nb * nq * a.Hkv;
+        tree_rotate_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
+    verify_attn_kernel<<<dim3(splits * p.halves, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, mtk, mtv, p);
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
         verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
@@ -820,7 +904,8 @@ static eagle3_status_t verify_validate(const eagle3_verify_attn_args_t *a) {
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->n_heads % a->n_kv_heads) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->head_dim != D || a->n_nodes > 64) return EAGLE3_ERR_UNSUPPORTED;
-    if (a->n_nodes * (a->n_heads / a->n_kv_heads) > ROWS) return EAGLE3_ERR_UNSUPPORTED;
+    int s_mid = 0;
+    if (!plan_halves(a->n_nodes, a->n_heads / a->n_kv_heads, &s_mid)) return EAGLE3_ERR_UNSUPPORTED;
     if ((int64_t)a->max_prefix_len + a->n_nodes > a->s_max) return EAGLE3_ERR_CAPACITY;
     if (!(a->rope_theta > 0.0f) || a->sm_scale < 0.0f) return EAGLE3_ERR_INVALID_ARGUMENT;
     if ((a->q_node_stride && (a->q_node_stride < (int64_t)a->n_heads * D || a->q_node_stride % 8)) ||
