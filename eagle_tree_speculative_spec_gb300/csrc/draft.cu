@@ -20,6 +20,7 @@
 // Every selection decision compares fp32 scores built with the same RN operations as the CPU
 // oracle, so for the same logits the tree is bit-identical.
 #include <algorithm>
+#include <cooperative_groups.h>
 
 #include "../../include/eagle3_linear.h"
 #include "attn.cuh"
@@ -237,24 +238,26 @@ E3_DEV uint64_t warp_flush(uint64_t *list, const uint64_t *cand, int cnt, int k,
     return list[k - 1];   // (selecting res[k - 1] in registers would demote res to local memory)
 }
 
-__global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int64_t ld, int V, int k,
-                                                       int32_t *out_tok, float *out_lq) {
-    __shared__ uint64_t buf[NT_TOPK / 32][TK_CAP];
-    __shared__ uint64_t wres[NT_TOPK / 32][KMAX];
-    __shared__ uint64_t fin[KMAX];
-    __shared__ uint64_t sred[NT_TOPK / 32];
-    const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float *z = logits + (size_t)row * ld;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    if (lane < KMAX) wres[warp][lane] = 0ull;
-    __syncwarp();
-    uint64_t tau = 0ull;           // packed key of the warp's k-th best so far (0: fewer than k)
-    float tau_f = key_to_float(0u);  // a NaN: every value passes `!(v < tau_f)`
-    int cnt = 0;                   // warp-uniform fill of buf[warp]
+struct TopkSmem {
+    uint64_t buf[NT_TOPK / 32][TK_CAP];
+    uint64_t wres[NT_TOPK / 32][KMAX];
+    uint64_t fin[KMAX];
+    uint64_t sred[NT_TOPK / 32];
+    uint64_t s_cta;                 // this CTA's share of the normaliser (cluster version)
+};
 
-    // merge the buffer into the warp's list and raise the threshold
+// Top-k candidates of the slice [lo, hi) of row z into sm.fin (sorted, KMAX entries, the first k
+// meaningful; 0 = none).
+E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    if (lane < KMAX) sm.wres[warp][lane] = 0ull;
+    __syncwarp();
+    uint64_t tau = 0ull;             // packed key of the warp's k-th best so far (0: fewer than k)
+    float tau_f = key_to_float(0u);  // a NaN: every value passes `!(v < tau_f)`
+    int cnt = 0;                     // warp-uniform fill of buf[warp]
     auto flush = [&]() {
-        tau = warp_flush(wres[warp], buf[warp], cnt, k, lane);
+        tau = warp_flush(sm.wres[warp], sm.buf[warp], cnt, k, lane);
         tau_f = key_to_float((uint32_t)(tau >> 32));
         cnt = 0;
     };
@@ -267,24 +270,25 @@ __global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int6
             pass = key > tau;
         }
         const uint32_t m = __ballot_sync(0xffffffffu, pass);
-        if (pass) buf[warp][cnt + __popc(m & lt_mask)] = key;
+        if (pass) sm.buf[warp][cnt + __popc(m & lt_mask)] = key;
         cnt += __popc(m);
     };
-
-    const bool vec = ((((uintptr_t)z) & 15) == 0);
-    const int n4 = vec ? V / 4 : 0;
+    const float *zs = z + lo;
+    const int n = hi - lo;
+    const bool vec = ((((uintptr_t)zs) & 15) == 0);
+    const int n4 = vec ? n / 4 : 0;
     constexpr int U = 4;   // float4 loads in flight per thread
     const int n4u = n4 / (U * NT_TOPK) * (U * NT_TOPK);   // float4 groups every lane has
     for (int j0 = threadIdx.x; j0 < n4u; j0 += U * NT_TOPK) {
         float4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(z) + j0 + u * NT_TOPK);
+        for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(zs) + j0 + u * NT_TOPK);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool any = !(v[u].x < tau_f) || !(v[u].y < tau_f) || !(v[u].z < tau_f) || !(v[u].w < tau_f);
             if (!__any_sync(0xffffffffu, any)) continue;
             if (cnt + 4 * 32 > TK_CAP) flush();
-            const uint32_t j = 4u * (uint32_t)(j0 + u * NT_TOPK);
+            const uint32_t j = (uint32_t)lo + 4u * (uint32_t)(j0 + u * NT_TOPK);
             offer(v[u].x, j, true);
             offer(v[u].y, j + 1, true);
             offer(v[u].z, j + 2, true);
@@ -292,49 +296,121 @@ __global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int6
         }
     }
     // the rest, one element per lane per round, with warp-uniform trip counts
-    for (int base = 4 * n4u; base < V; base += NT_TOPK) {
+    for (int base = 4 * n4u; base < n; base += NT_TOPK) {
         const int i = base + threadIdx.x;
-        const bool valid = i < V;
-        const float v = valid ? __ldg(z + i) : 0.0f;
+        const bool valid = i < n;
+        const float v = valid ? __ldg(zs + i) : 0.0f;
         if (cnt + 32 > TK_CAP) flush();
-        offer(v, (uint32_t)i, valid);
+        offer(v, (uint32_t)(lo + i), valid);
     }
     if (cnt > 0) flush();
     __syncthreads();
     if (warp == 0) {
         uint64_t best[KMAX], res[KMAX];
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT_TOPK / 32 ? wres[lane][q] : 0ull;
+        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT_TOPK / 32 ? sm.wres[lane][q] : 0ull;
         warp_merge(best, res, k);
         if (lane == 0)
 #pragma unroll
-            for (int q = 0; q < KMAX; ++q) fin[q] = res[q];
+            for (int q = 0; q < KMAX; ++q) sm.fin[q] = res[q];
     }
     __syncthreads();
-    // fixed-point normaliser over the whole row with m = the row maximum
-    const float m = key_to_float((uint32_t)(fin[0] >> 32));
+}
+
+// Fixed-point normaliser terms of the slice [lo, hi) of row z with m = the row maximum: the CTA's
+// sum (valid in thread 0)
+E3_DEV uint64_t normaliser_slice(TopkSmem &sm, const float *z, int lo, int hi, float m) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *zs = z + lo;
+    const int n = hi - lo;
+    const bool vec = ((((uintptr_t)zs) & 15) == 0);
+    const int n4 = vec ? n / 4 : 0;
     uint64_t s = 0;
 #pragma unroll 4
     for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(z) + j);
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(zs) + j);
         // each weight is up to 2^31: widen before adding
         s += (uint64_t)dsm_weight(dsm_scaled(v.x, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.y, m, 1.0f)) +
              (uint64_t)dsm_weight(dsm_scaled(v.z, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.w, m, 1.0f));
     }
-    for (int i = 4 * n4 + threadIdx.x; i < V; i += NT_TOPK) s += dsm_weight(dsm_scaled(__ldg(z + i), m, 1.0f));
+    for (int i = 4 * n4 + threadIdx.x; i < n; i += NT_TOPK) s += dsm_weight(dsm_scaled(__ldg(zs + i), m, 1.0f));
 #pragma unroll
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sred[warp] = s;
+    if (lane == 0) sm.sred[warp] = s;
     __syncthreads();
+    uint64_t S = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < NT_TOPK / 32; ++w) S += sm.sred[w];
+    return S;
+}
+
+E3_DEV void topk_write(const uint64_t *fin, uint64_t S, float m, int row, int k, int32_t *out_tok, float *out_lq) {
     if (threadIdx.x < k) {
-        uint64_t S = 0;
-        for (int w = 0; w < NT_TOPK / 32; ++w) S += sred[w];
         const float ln_s = dsm_log31(S);
         const uint64_t e = fin[threadIdx.x];
         const float zx = key_to_float((uint32_t)(e >> 32));
         out_tok[(size_t)row * k + threadIdx.x] = (int32_t)unpack_idx(e);
         out_lq[(size_t)row * k + threadIdx.x] = __fsub_rn(dsm_scaled(zx, m, 1.0f), ln_s);
     }
+}
+
+// One CTA per row (many rows).
+__global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int64_t ld, int V, int k,
+                                                       int32_t *out_tok, float *out_lq) {
+    __shared__ TopkSmem sm;
+    const int row = blockIdx.x;
+    const float *z = logits + (size_t)row * ld;
+    topk_slice(sm, z, 0, V, k);
+    const float m = key_to_float((uint32_t)(sm.fin[0] >> 32));
+    __shared__ uint64_t S;
+    const uint64_t s = normaliser_slice(sm, z, 0, V, m);
+    if (threadIdx.x == 0) S = s;
+    __syncthreads();
+    topk_write(sm.fin, S, m, row, k, out_tok, out_lq);
+}
+
+// A cluster of TOPK_CL CTAs per row (few rows): CTA r scans slice r, the slices' top-k lists and
+// normaliser sums are combined through distributed shared memory in rank order.
+constexpr int TOPK_CL = 8;
+__global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
+    topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, int32_t *out_tok, float *out_lq) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ TopkSmem sm;
+    __shared__ uint64_t fin_all[KMAX];
+    const int rank = (int)cluster.block_rank(), row = blockIdx.x / TOPK_CL;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *z = logits + (size_t)row * ld;
+    const int slice = ((V + TOPK_CL - 1) / TOPK_CL + 3) / 4 * 4;   // a multiple of 4 elements
+    const int lo = min(V, rank * slice), hi = min(V, lo + slice);
+    topk_slice(sm, z, lo, hi, k);
+    cluster.sync();
+    if (warp == 0) {
+        uint64_t best[KMAX], res[KMAX];
+        const uint64_t *src = cluster.map_shared_rank(sm.fin, lane < TOPK_CL ? lane : 0);
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) best[q] = lane < TOPK_CL ? src[q] : 0ull;
+        warp_merge(best, res, k);
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) fin_all[q] = res[q];
+    }
+    __syncthreads();
+    const float m = key_to_float((uint32_t)(fin_all[0] >> 32));
+    const uint64_t s = normaliser_slice(sm, z, lo, hi, m);
+    if (threadIdx.x == 0) sm.s_cta = s;
+    cluster.sync();
+    if (rank == 0) {
+        __shared__ uint64_t S;
+        if (threadIdx.x == 0) {
+            uint64_t t = 0;
+            for (int r = 0; r < TOPK_CL; ++r) t += *cluster.map_shared_rank(&sm.s_cta, r);
+            S = t;
+        }
+        __syncthreads();
+        topk_write(fin_all, S, m, row, k, out_tok, out_lq);
+    }
+    cluster.sync();   // no CTA leaves while its shared memory may still be read
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -878,7 +954,18 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         eagle3_linear_args_t l = lin(rows, m.V, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
                                      a->dev_status);
         E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
-        topk_kernel<<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq));
+        // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs
+        static int sms = 0;
+        if (!sms) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        }
+        if ((int64_t)rows * TOPK_CL <= 2LL * sms)
+            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok),
+                                                                    (float *)P(pl.o_tlq));
+        else
+            topk_kernel<<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq));
         E3_LAUNCHED();
         return EAGLE3_OK;
     };

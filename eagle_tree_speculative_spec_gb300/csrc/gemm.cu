@@ -362,6 +362,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             // add the stream-K contributions to a chunk of 32 accumulator columns
             auto add_contrib = [&](float (&v)[32], int col) {
+                if (row >= p.M) return;   // rows past M are never stored, so never exchanged
                 for (int c = c_lo; c < c_hi; ++c) {
                     const float4 *src = p.sk_part + (size_t)c * (BN / 4) * BM + (size_t)(col / 4) * BM + rl;
                     float4 q[8];
@@ -381,10 +382,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float4 *dst = p.sk_part + (size_t)blockIdx.x * (BN / 4) * BM + rl;
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
-                    tc::tmem_ld32(t_row + c * 32, v);
+                    tc::tmem_ld32(t_row + c * 32, v);   // warp-collective: every lane loads
+                    if (row < p.M) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        __stcg(dst + (size_t)(c * 8 + i) * BM, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                        for (int i = 0; i < 8; ++i)
+                            __stcg(dst + (size_t)(c * 8 + i) * BM,
+                                   make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    }
                 }
                 __threadfence();
                 __syncwarp();
@@ -617,8 +621,9 @@ Plan plan(const eagle3_linear_args_t *a) {
     const int waves = (tiles + sms - 1) / sms;
     pl.dp_tiles = tiles / sms >= 2 ? (tiles / sms - 1) * sms : 0;   // whole waves kept data-parallel
     const long long T = (long long)(tiles - pl.dp_tiles) * pl.kb_total;
-    pl.streamk = a->splits <= 0 && pl.kb_total >= 192 && (double)tiles / ((double)waves * sms) < 0.97 &&
-                 T >= 8LL * sms;
+    // (or when there is a single M tile: the launch streams weights and every SM should share it)
+    pl.streamk = a->splits <= 0 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
+                 (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms;
     if (pl.streamk) {
         pl.splits = 1;
         pl.kb_per_split = pl.kb_total;
