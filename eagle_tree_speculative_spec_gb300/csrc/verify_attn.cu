@@ -109,6 +109,13 @@ E3_DEV float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction
+E3_DEV float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // warp-uniform bounded wait (lane 0 polls, the outcome is broadcast)
 E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     int ok = 0;
@@ -468,25 +475,24 @@ __global__ void __launch_bounds__(NT, 1)
             }
             const int key0 = k_lo + j * BK + col0;
             const bool full = !tree && key0 + hw <= k_hi;   // every key of this half is visible
+            // the maximum is taken over the raw scores (the scale is positive, so it commutes) and
+            // the scale is applied inside the exponent's argument
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (full) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    sc[i] *= p.scale_log2;
-                    mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
-                }
+                for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], sc[i], sc[i + 1]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
                     const int key = col0 + i;            // tree: node index
                     const bool valid =
                         i < hw && (tree ? (key < nk && ((bits >> key) & 1ull)) : (key0 + i < k_hi));
-                    sc[i] = valid ? sc[i] * p.scale_log2 : -INFINITY;
+                    sc[i] = valid ? sc[i] : -INFINITY;
                     mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
                 }
             }
             // row maximum of the whole tile: exchange with the warp holding the other half
-            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
             ss.mx_x[j & 1][hc][rl] = mx;
             asm volatile("bar.sync 2, 256;" ::: "memory");
             mx = fmaxf(mx, ss.mx_x[j & 1][hc ^ 1][rl]);
@@ -514,18 +520,22 @@ __global__ void __launch_bounds__(NT, 1)
                 l_run *= corr;
                 m_run = m_new;
             }
-            const float mu = m_run == -INFINITY ? 0.0f : m_run;
+            const float nmu = m_run == -INFINITY ? 0.0f : -m_run;
             // exponentials and this half's row sum (four chains), packed to bf16 pairs
+            // (paired fp32 FMA and add: one instruction per two scores)
             uint32_t pk[32];
-            float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float2 sq[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(nmu, nmu);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float p0 = fast_exp2(sc[2 * e] - mu), p1 = fast_exp2(sc[2 * e + 1] - mu);
-                sq[e & 3] += p0 + p1;
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                const float2 x = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sc2, nmu2);
+                const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                sq[e & 3] = __fadd2_rn(sq[e & 3], pe);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(pe.x, pe.y);
                 pk[e] = *reinterpret_cast<uint32_t *>(&h2);
             }
-            l_run += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+            const float2 s01 = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
+            l_run += s01.x + s01.y;
             // P of this half over the buffer's first columns: both halves have read their scores
             // (they exchanged maxima after their loads), so the writes cannot overtake a read
             if (hw == 64)
