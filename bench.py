@@ -880,11 +880,13 @@ def run_kernel(args):
         bf = torch.bfloat16
         x = (torch.randn(M, K, generator=g, device=dev) * 0.5).to(bf)
         w = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(bf)
-        epi = {"swiglu": e3.EPI_SWIGLU, "bf16": e3.EPI_BF16, "f32": e3.EPI_F32}[args.epilogue]
+        epi = {"swiglu": e3.EPI_SWIGLU, "bf16": e3.EPI_BF16, "f32": e3.EPI_F32,
+               "residual": e3.EPI_BF16_RESIDUAL}[args.epilogue]
         w2 = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(bf) if epi == e3.EPI_SWIGLU else None
+        res = torch.randn(M, N, generator=g, device=dev).to(bf) if epi == e3.EPI_BF16_RESIDUAL else None
         o = torch.empty(M, N, device=dev, dtype=torch.float32 if epi == e3.EPI_F32 else bf)
         ws = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        fn = lambda: e3.eagle3_linear(x, w, o, epilogue=epi, w2=w2, workspace=ws)
+        fn = lambda: e3.eagle3_linear(x, w, o, epilogue=epi, w2=w2, residual=res, workspace=ws)
         ms = _time_loop(fn, args.steps, args.warmup)
         flops = 2.0 * M * N * K * (2 if w2 is not None else 1)
         out.update(m=M, n=N, k=K, epilogue=args.epilogue, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
@@ -907,7 +909,7 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="--kernel gemm: rows (default batch x tree nodes)")
     ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
     ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
-    ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32"])
+    ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32", "residual"])
     ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)

@@ -129,6 +129,44 @@ struct Cfg {
 
 E3_DEV float silu(float x) { return x / (1.0f + __expf(-x)); }
 
+// Residual columns [col0, col0 + 8 n) of one row as n 16-byte vectors (bounds-checked element by
+// element at the right edge or for an unaligned row), read through L2 only: each value is read once.
+template <int NV>
+E3_DEV void load_residual(const GemmParams &p, int row, int col0, uint4 (&r)[NV]) {
+    const __nv_bfloat16 *src = p.residual + (size_t)row * p.ld_res + col0;
+    if (col0 + 8 * NV <= p.N && ((((uintptr_t)src) & 15) == 0)) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) r[j] = __ldcg(reinterpret_cast<const uint4 *>(src) + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            uint16_t h[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = 8 * j + e;
+                h[e] = col0 + c < p.N ? reinterpret_cast<const uint16_t *>(src)[c] : (uint16_t)0;
+            }
+            r[j] = make_uint4(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16),
+                              h[4] | ((uint32_t)h[5] << 16), h[6] | ((uint32_t)h[7] << 16));
+        }
+    }
+}
+
+template <int NV>
+E3_DEV void add_residual(float *v, const uint4 (&r)[NV]) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const uint32_t w4[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[e]);
+            const float2 f = __bfloat1622float2(h);
+            v[8 * j + 2 * e] += f.x;
+            v[8 * j + 2 * e + 1] += f.y;
+        }
+    }
+}
+
 // Epilogue of one 32-column chunk of one row, from fp32 accumulators.
 E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)[32]) {
     if (row >= p.M) return;
@@ -148,9 +186,9 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
 #pragma unroll
     for (int i = 0; i < 32; ++i) w[i] = v[i];
     if (p.epi == EAGLE3_EPI_BF16_RESIDUAL) {
-        const __nv_bfloat16 *r = p.residual + (size_t)row * p.ld_res + col0;
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) w[i] += __bfloat162float(r[i]);
+        uint4 r[4];
+        load_residual(p, row, col0, r);
+        add_residual(w, r);
     }
     if (col0 + 32 <= p.N && ((((uintptr_t)o) & 15) == 0)) {
 #pragma unroll
@@ -322,6 +360,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Item w;
         while (wi.next(p, w)) {
             const int mb = w.mb, nb = w.nb, sp = w.sp;
+            if (p.epi == EAGLE3_EPI_BF16_RESIDUAL && w.kind != IT_CONTRIB && p.splits == 1) {
+                // pull this tile's residual row into L2 while the main loop runs (one bulk prefetch
+                // of the row's whole-16-byte part; the epilogue reads it from there)
+                const int prow = mb * BM + quarter * 32 + lane, col0 = nb * BN;
+                if (prow < p.M && col0 < p.N) {
+                    const __nv_bfloat16 *src = p.residual + (size_t)prow * p.ld_res + col0;
+                    const uint32_t bytes = (uint32_t)(min(BN, p.N - col0) * 2) & ~15u;
+                    if (bytes && ((((uintptr_t)src) & 15) == 0)) tc::prefetch_l2(src, bytes);
+                }
+            }
             // warp-uniform wait: lane 0 polls, the outcome is broadcast, so a timeout can never
             // split the warp in front of the warp-collective TMEM loads below
             int ok = 0;
@@ -411,7 +459,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int y = mb * BM + quarter * 32;
                 const bool f32 = p.epi == EAGLE3_EPI_F32;
                 const int chunks = (swiglu ? BN / 2 : BN) / (f32 ? 32 : 64);
+                // residual rows one chunk ahead, so that their latency hides behind a chunk's work
+                const bool res = p.epi == EAGLE3_EPI_BF16_RESIDUAL && row < p.M;
+                uint4 r_cur[8], r_next[8];
+                if (res) load_residual(p, row, nb * BN, r_cur);
                 for (int sc = 0; sc < chunks; ++sc) {
+                    if (res && sc + 1 < chunks) load_residual(p, row, nb * BN + (sc + 1) * 64, r_next);
                     uint4 u[8];
                     if (f32) {
                         float v[32];
@@ -442,12 +495,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[h * 32 + i] = t[i];
                         }
-                        const int col0 = (swiglu ? nb * (BN / 2) : nb * BN) + sc * 64;
-                        if (p.epi == EAGLE3_EPI_BF16_RESIDUAL && row < p.M) {
-                            const __nv_bfloat16 *r = p.residual + (size_t)row * p.ld_res + col0;
-                            for (int i = 0; i < 64; ++i)
-                                if (col0 + i < p.N) v[i] += __bfloat162float(r[i]);
-                        }
+                        if (res) add_residual(v, r_cur);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * j], v[8 * j + 1]);
@@ -473,6 +521,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         tc::bulk_commit();
                     }
                     sbuf ^= 1;
+                    if (res) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) r_cur[j] = r_next[j];
+                    }
                 }
             } else if (!swiglu) {
                 for (int c = 0; c < BN / 32; ++c) {

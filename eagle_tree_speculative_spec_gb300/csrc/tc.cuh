@@ -208,6 +208,11 @@ E3_DEV void tmem_st16u(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned address, size a multiple of 16).
+E3_DEV void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (tensor cores).
 E3_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
