@@ -614,13 +614,13 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
-// Rotated tree keys back into tree_k: one warp per (sequence, query slot, KV head), at the slot's
-// position (prefix length + depth from the parent array, or the given position), with the same
-// angle arguments and arithmetic the attention kernel used in shared memory.
+// Rotated tree keys back into tree_k: eight threads per (sequence, query slot, KV head) row, four
+// rows per warp, at the slot's position (prefix length + depth from the parent array, or the given
+// position), with the same angle arguments and arithmetic the attention kernel uses for Q.
 __global__ void tree_rotate_kernel(const Params p) {
     const int nq = p.q_hi - p.q_lo;
-    const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t w = t >> 3;                    // row
     if (w >= (int64_t)p.B * nq * p.Hkv) return;
     const int g = (int)(w % p.Hkv);
     const int i = p.q_lo + (int)((w / p.Hkv) % nq);
@@ -643,8 +643,7 @@ __global__ void tree_rotate_kernel(const Params p) {
     } else {
         pos = p.pos[(size_t)b * p.pos_sb + i];
     }
-    const int c = lane & 7, part = lane >> 3;   // lanes 0..7 take the row, the others idle
-    if (part != 0) return;
+    const int c = (int)(t & 7);                  // 16-byte chunks c and c + 8 (dims 8c.. and 64 + 8c..)
     __nv_bfloat16 *kg = p.k + (size_t)b * p.k_sb + (size_t)i * p.k_si + (size_t)g * D;
     uint4 lo = ld16(kg + 8 * c), hi = ld16(kg + 64 + 8 * c);
     float cs[8], sn[8];
@@ -853,7 +852,7 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     {
         // the query slots' keys rotated in tree_k first; the attention streams them like the prefix
         const int64_t warps = (int64_t)pt.nb * nq * a.Hkv;
-        tree_rotate_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
+        tree_rotate_kernel<<<(unsigned)((warps + 31) / 32), 256, 0, stream>>>(p);   // 32 rows per block
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
     verify_attn_kernel<<<dim3(splits * p.halves, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, mtk, mtv, p);
