@@ -674,7 +674,13 @@ Plan plan(const eagle3_linear_args_t *a) {
     pl.dp_tiles = tiles / sms >= 2 ? (tiles / sms - 1) * sms : 0;   // whole waves kept data-parallel
     const long long T = (long long)(tiles - pl.dp_tiles) * pl.kb_total;
     // (or when there is a single M tile: the launch streams weights and every SM should share it)
-    pl.streamk = a->splits <= 0 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
+    // A single M tile whose N tiles fill at most half the SMs streams its weights through split-K
+    // instead: up to 8 k-splits of at least 4 k-blocks, reduced in split order (measured faster
+    // than stream-K for these rows-few, weight-bound launches).
+    int auto_splits = 1;
+    if (a->splits <= 0 && pl.tiles_m == 1 && 2 * tiles <= sms)
+        auto_splits = std::max(1, std::min({8, sms / tiles, pl.kb_total / 4}));
+    pl.streamk = a->splits <= 0 && auto_splits == 1 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
                  (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms;
     if (pl.streamk) {
         pl.splits = 1;
@@ -684,7 +690,7 @@ Plan plan(const eagle3_linear_args_t *a) {
         pl.ws_bytes = (size_t)sms * BM * pl.bn * sizeof(float) + (size_t)sms * sizeof(int);
         return pl;
     }
-    int splits = a->splits > 0 ? a->splits : 1;
+    int splits = a->splits > 0 ? a->splits : auto_splits;
     splits = std::max(1, std::min(splits, pl.kb_total));
     pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
     pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
