@@ -674,12 +674,22 @@ Plan plan(const eagle3_linear_args_t *a) {
     pl.dp_tiles = tiles / sms >= 2 ? (tiles / sms - 1) * sms : 0;   // whole waves kept data-parallel
     const long long T = (long long)(tiles - pl.dp_tiles) * pl.kb_total;
     // (or when there is a single M tile: the launch streams weights and every SM should share it)
-    // A single M tile whose N tiles fill at most half the SMs streams its weights through split-K
-    // instead: up to 8 k-splits of at least 4 k-blocks, reduced in split order (measured faster
-    // than stream-K for these rows-few, weight-bound launches).
+    // A single M tile with at most two waves of N tiles streams its weights through split-K
+    // instead (measured faster than stream-K for these rows-few, weight-bound launches): the split
+    // count in 1..8 (at least 4 k-blocks each) whose units fill their last wave best, a larger
+    // count only when it fills it by 2% more; the partials are reduced in split order.
     int auto_splits = 1;
-    if (a->splits <= 0 && pl.tiles_m == 1 && 2 * tiles <= sms)
-        auto_splits = std::max(1, std::min({8, sms / tiles, pl.kb_total / 4}));
+    if (a->splits <= 0 && pl.tiles_m == 1 && tiles <= 2 * sms) {
+        double best = 0.0;
+        for (int sp = 1; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
+            const int units = tiles * sp, w = (units + sms - 1) / sms;
+            const double fill = (double)units / ((double)w * sms);
+            if (fill > best + 0.02) {
+                best = fill;
+                auto_splits = sp;
+            }
+        }
+    }
     pl.streamk = a->splits <= 0 && auto_splits == 1 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
                  (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms;
     if (pl.streamk) {
