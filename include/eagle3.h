@@ -183,7 +183,7 @@ eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *args, eagle3_stre
  * natural-log sum of exp of the scaled scores.
  * The prefix is split across CTAs (split-KV) by a plan made from max_prefix_len (a host bound on
  * every prefix_len[b]); partial results are merged by a second kernel in a fixed order.
- * Cache slots at positions >= prefix_len are read in whole 64-key tiles and multiplied by a zero
+ * Cache slots at positions >= prefix_len are read in whole 128-key tiles and multiplied by a zero
  * weight, so they must hold finite values (zero-initialise a cache once; compaction only ever
  * writes finite rows).
  * Node pitches let q / tree_k / tree_v be views into one fused QKV projection output

@@ -13,9 +13,11 @@
  * Shapes: x [m, k] (row pitch ld_x), W and W2 [n, k] (row pitch ld_w), out [m, n] (pitch ld_out),
  * residual [m, n] (pitch ld_res); a pitch of 0 means dense.  k and every pitch must be multiples of
  * 8 elements and x, W, W2 must start on 16-byte boundaries.  All pointers are caller-owned device
- * memory.  When the k dimension is split across CTAs (small m), fp32 partials go to the caller's
- * workspace (eagle3_linear_workspace_size bytes) and are added in split order: results do not
- * depend on the launch configuration beyond that fixed order.  Errors: as in eagle3.h.
+ * memory.  When the k dimension is split across CTAs (few rows, or long k with a partial last
+ * wave), fp32 partials go to the caller's workspace (eagle3_linear_workspace_size bytes) and are
+ * added in a fixed order (split order, or CTA order for a stream-K plan).  The split points come
+ * from the shape and the device's SM count, so results are reproducible on a given GPU model and
+ * agree with any other order within fp32 rounding.  Errors: as in eagle3.h.
  */
 #ifndef EAGLE3_LINEAR_H
 #define EAGLE3_LINEAR_H
