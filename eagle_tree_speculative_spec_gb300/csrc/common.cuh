@@ -91,6 +91,33 @@ E3_DEV uint32_t dsm_weight(float t) {
     return (uint32_t)__fmul_rn(dsm_exp(t), 2147483648.0f);
 }
 
+// dsm_weight(dsm_scaled(z, m, inv_t)) for two values at once.  The same RN operations run lane by
+// lane on paired fp32 multiplies and adds (no fusion; a - b is computed as a + (-b), which IEEE
+// rounding makes identical), so each weight is bit-identical to the scalar path.
+E3_DEV uint2 dsm_weight_pair(float z0, float z1, float m, float inv_t) {
+    auto dup = [](float x) { return make_float2(x, x); };
+    auto neg = [](float2 x) { return make_float2(-x.x, -x.y); };
+    const float2 t = __fmul2_rn(__fadd2_rn(make_float2(z0, z1), dup(-m)), dup(inv_t));
+    // below -64 (or NaN) the weight is 0; clamp so that the exponent arithmetic stays in range
+    const float2 tc = make_float2(fmaxf(t.x, -64.0f), fmaxf(t.y, -64.0f));
+    const float2 kl = __fmul2_rn(tc, dup(LOG2E));
+    const float2 k = make_float2(rintf(kl.x), rintf(kl.y));
+    float2 r = __fadd2_rn(tc, neg(__fmul2_rn(k, dup(LN2_HI))));
+    r = __fadd2_rn(r, neg(__fmul2_rn(k, dup(LN2_LO))));
+    float2 q = dup(0x1.a01a02p-13f);                       // 1/7!
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(0x1.6c16c2p-10f));   // 1/6!
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(0x1.111112p-7f));    // 1/5!
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(0x1.555556p-5f));    // 1/4!
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(0x1.555556p-3f));    // 1/3!
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(0.5f));
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(1.0f));
+    q = __fadd2_rn(__fmul2_rn(q, r), dup(1.0f));
+    const float2 e = __fmul2_rn(q, make_float2(__int_as_float(((int)k.x + 127) << 23),
+                                               __int_as_float(((int)k.y + 127) << 23)));
+    const float2 w = __fmul2_rn(e, dup(2147483648.0f));
+    return make_uint2(t.x >= -64.0f ? (uint32_t)w.x : 0u, t.y >= -64.0f ? (uint32_t)w.y : 0u);
+}
+
 E3_DEV int bitlen64(uint64_t v) { return v ? 64 - __clzll((long long)v) : 0; }
 
 E3_DEV float dsm_log31(uint64_t S) {

@@ -330,8 +330,8 @@ E3_DEV uint64_t normaliser_slice(TopkSmem &sm, const float *z, int lo, int hi, f
     for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(zs) + j);
         // each weight is up to 2^31: widen before adding
-        s += (uint64_t)dsm_weight(dsm_scaled(v.x, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.y, m, 1.0f)) +
-             (uint64_t)dsm_weight(dsm_scaled(v.z, m, 1.0f)) + (uint64_t)dsm_weight(dsm_scaled(v.w, m, 1.0f));
+        const uint2 w01 = dsm_weight_pair(v.x, v.y, m, 1.0f), w23 = dsm_weight_pair(v.z, v.w, m, 1.0f);
+        s += ((uint64_t)w01.x + w01.y) + ((uint64_t)w23.x + w23.y);
     }
     for (int i = 4 * n4 + threadIdx.x; i < n; i += NT_TOPK) s += dsm_weight(dsm_scaled(__ldg(zs + i), m, 1.0f));
 #pragma unroll
