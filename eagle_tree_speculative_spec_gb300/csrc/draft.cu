@@ -238,6 +238,14 @@ E3_DEV uint64_t warp_flush(uint64_t *list, const uint64_t *cand, int cnt, int k,
     return list[k - 1];   // (selecting res[k - 1] in registers would demote res to local memory)
 }
 
+// max of four floats in two instructions, NaN if any is NaN
+E3_DEV float max4_nan(float4 v) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(v.x), "f"(v.y), "f"(v.z));
+    asm("max.NaN.f32 %0, %0, %1;" : "+f"(r) : "f"(v.w));
+    return r;
+}
+
 struct TopkSmem {
     uint64_t buf[NT_TOPK / 32][TK_CAP];
     uint64_t wres[NT_TOPK / 32][KMAX];
@@ -285,7 +293,9 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
         for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(zs) + j0 + u * NT_TOPK);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const bool any = !(v[u].x < tau_f) || !(v[u].y < tau_f) || !(v[u].z < tau_f) || !(v[u].w < tau_f);
+            // some element is not below the threshold <=> their maximum is not (a NaN propagates, and
+            // passes, as it does element by element)
+            const bool any = !(max4_nan(v[u]) < tau_f);
             if (!__any_sync(0xffffffffu, any)) continue;
             if (cnt + 4 * 32 > TK_CAP) flush();
             const uint32_t j = (uint32_t)lo + 4u * (uint32_t)(j0 + u * NT_TOPK);
