@@ -667,8 +667,8 @@ def oracle_sample_seconds(cfg, rng_seed=0):
     return step, t
 
 
-def cpu_baseline(cfg):
-    step, parts = oracle_sample_seconds(cfg)
+def host_threads():
+    """Threads the host's NumPy BLAS may use (the oracle's matrix products)."""
     threads = torch.get_num_threads()
     try:
         import numpy as np  # noqa: F401
@@ -676,6 +676,12 @@ def cpu_baseline(cfg):
         threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:
         pass
+    return threads
+
+
+def cpu_baseline(cfg):
+    step, parts = oracle_sample_seconds(cfg)
+    threads = host_threads()
     value = cfg["N"] / step          # verified tree tokens per second for one sequence on the host
     return {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": ("one sequence: one layer of verify attention (60 nodes, 2048 prefix), one target "
@@ -891,6 +897,64 @@ def run_kernel(args):
         flops = 2.0 * M * N * K * (2 if w2 is not None else 1)
         out.update(m=M, n=N, k=K, epilogue=args.epilogue, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
                    frac_sustained=round(flops / ms / 1e9 / tf_sust, 4), frac_burst=round(flops / ms / 1e9 / tf_burst, 4))
+    elif args.kernel == "tiny":
+        # the tiny lossless configuration (fp32, 4-layer d = 64 target and its EAGLE-3 head, 32-token
+        # prompt): greedy speculative decoding with a K = 4 chain and vanilla greedy decoding, 64 new
+        # tokens each, timed on the wall clock (the loop is host-driven: the accepted length is read
+        # back every cycle); both must produce the same tokens
+        import synth
+        from eagle_tree_speculative_spec_gb300 import tiny
+        cfg = synth.TINY
+        tw = synth.llama_weights(0, **cfg)
+        dw = synth.eagle3_weights(0, cfg["d"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["ffn"],
+                                  cfg["vocab"], embed=tw["embed"], lm_head=tw["lm_head"])
+        prompt, new = synth.tiny_prompt(0), 64
+        make_t = lambda: tiny.TinyTarget(tw, cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                                         synth.TINY_AUX_LAYERS, 160, dev)
+        make_d = lambda: tiny.TinyDraft(dw, cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], 160, dev)
+
+        def timed(fn, reps):
+            ts, res = [], None
+            for _ in range(reps):
+                objs = fn[1]()                       # weights uploaded outside the timed region
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                res = fn[0](*objs)
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            return sorted(ts)[len(ts) // 2], res
+        spec = (lambda t, d: tiny.speculative_greedy(t, d, prompt, new, k_draft=4), lambda: (make_t(), make_d()))
+        van = (lambda t: tiny.vanilla_greedy(t, prompt, new), lambda: (make_t(),))
+        timed(spec, 1)
+        timed(van, 1)
+        reps = max(3, args.steps)
+        t_spec, (tok_spec, accepted) = timed(spec, reps)
+        t_van, tok_van = timed(van, reps)
+        out.update(new_tokens=new, speculative_ms_per_token=round(1e3 * t_spec / new, 4),
+                   vanilla_ms_per_token=round(1e3 * t_van / new, 4), cycles=len(accepted),
+                   accepted_per_cycle=round(sum(accepted) / len(accepted), 3),
+                   speculative_equals_vanilla=tok_spec == tok_van, dtype="f32")
+        if not args.no_cpu_baseline:
+            # the oracle on the host: the same two decodes in fp64 NumPy, one run each
+            from oracle import draft_tree as odt
+            from oracle import llama as oll
+            ot = oll.Llama(tw, cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                           aux_layers=synth.TINY_AUX_LAYERS)
+            od = oll.Eagle3Draft(dw, cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"])
+
+            def chain(draft, d_cache, a_last, pending, L):
+                r = odt.draft_tree_for_sequence(draft, d_cache, a_last, pending, L, 4, 1, 5)
+                return r["tokens"].tolist(), r["parents"].tolist()
+            t0 = time.perf_counter()
+            ref_spec, _ = oll.speculative_greedy(ot, od, prompt, new, chain)
+            t1 = time.perf_counter()
+            ref_van = oll.vanilla_greedy(ot, prompt, new)
+            t2 = time.perf_counter()
+            out["cpu_baseline"] = {"kind": "oracle", "cores": host_threads(), "unit": "ms/token",
+                                   "speculative_ms_per_token": round(1e3 * (t1 - t0) / new, 3),
+                                   "vanilla_ms_per_token": round(1e3 * (t2 - t1) / new, 3),
+                                   "sample": "the full 64-token runs, single process",
+                                   "matches_gpu": ref_spec == tok_spec and ref_van == tok_van}
     print(json.dumps(out), flush=True)
 
 
@@ -910,7 +974,7 @@ def main():
     ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
     ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
     ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32", "residual"])
-    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm"],
+    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm", "tiny"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)
     ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
