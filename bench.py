@@ -423,6 +423,22 @@ def graph_kernel_names(g):
     return out
 
 
+def max_over_ranks(x, dev):
+    """The largest value over the ranks of the process group (the job's time is the slowest
+    rank's); x itself with no group or a single rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def external_events_ok():
     try:
         torch.cuda.Event(enable_timing=True, external=True)
@@ -505,9 +521,7 @@ def run_gpu(args):
     kernels = eng.graph_kernels() if use_graph else None
     if world > 1:
         dist.barrier()
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dev)
     status = int(eng.dev_status.item())
 
     # ---- e2e through host buffers: per step H2D of the step's inputs, D2H of its result
@@ -533,12 +547,12 @@ def run_gpu(args):
         out_len.copy_(eng.accept_len, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     h2d = host_aux.numel() * 2 + host_tok.numel() * 4 + host_tc.numel() * 4
     d2h = out_tok.numel() * 4 + out_len.numel() * 4
 
     units = cfg["B"] * cfg["N"] * args.steps * world
-    value = units / (ms / 1e3)
+    value = job_rate(cfg["B"] * cfg["N"] * args.steps, world, ms)
     hbm, tf_burst, tf_sust, src = peaks()
     tgt_f, drf_f = eng.flops_per_step()
     # the target's projections are timed one by one; the draft head's run inside eagle3_draft_tree
