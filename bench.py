@@ -101,9 +101,12 @@ class ClockSampler:
 class Engine:
     """Device state of the speculative-decoding loop and one step over the C ABI."""
 
-    def __init__(self, cfg, steps_total, dev, timing=True):
+    def __init__(self, cfg, steps_total, dev, timing=True, fused_rope=True):
         import eagle_tree_speculative_spec_gb300 as e3
         self.e3, self.cfg, self.dev, self.timing = e3, cfg, dev, timing
+        # the target's QKV projection rotates q and the tree keys (EPI_BF16_ROPE) and the verify
+        # attention takes them as they are; False: the attention rotates them itself
+        self.fused_rope = fused_rope
         c = cfg
         B, N, d, V, D = c["B"], c["N"], c["d"], c["V"], c["D"]
         Hq, Hkv, F, Lyr = c["Hq"], c["Hkv"], c["F"], c["layers"]
@@ -257,12 +260,15 @@ class Engine:
 
         lp, lb = ws(self.ws_lin)
 
-        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm"):
+        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm", rope_cols=0):
             a = e3._lib.LinearArgs(m=x.shape[0], n=w.shape[0], k=x.shape[1], epilogue=epi, splits=0, ld_x=0, ld_w=0,
                                    ld_out=0, ld_res=0, x=x.data_ptr(), w=w.data_ptr(),
                                    w2=None if w2 is None else w2.data_ptr(), out=out.data_ptr(),
                                    residual=None if res is None else res.data_ptr(),
-                                   dev_status=self.dev_status.data_ptr())
+                                   dev_status=self.dev_status.data_ptr(), rope_cols=rope_cols,
+                                   rope_rows_per_seq=N, rope_theta=500000.0,
+                                   rope_base=self.prefix_len.data_ptr() if rope_cols else None,
+                                   rope_depth=self.depth.data_ptr() if rope_cols else None)
             keep.append(a)
             ops.append((kind, lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st)))
 
@@ -274,13 +280,17 @@ class Engine:
                 tap = self.aux_tree[:, taps[l] * d:(taps[l] + 1) * d] if l in taps else None
                 norm(self.x, self.norm1[l], self.h, tap=tap)
             qkv = self.qkv[l]
-            lin(self.h, self.wqkv[l], qkv)
+            if self.fused_rope:
+                # q and the tree keys leave the projection rotated at prefix_len + depth
+                lin(self.h, self.wqkv[l], qkv, epi=e3.EPI_BF16_ROPE, rope_cols=(Hq + Hkv) * D)
+            else:
+                lin(self.h, self.wqkv[l], qkv)
             q = qkv.view(B, N, self.qkv_w)[:, :, : Hq * D].unflatten(2, (Hq, D))
             kt = qkv.view(B, N, self.qkv_w)[:, :, Hq * D:(Hq + Hkv) * D].unflatten(2, (Hkv, D))
             vt = qkv.view(B, N, self.qkv_w)[:, :, (Hq + Hkv) * D:].unflatten(2, (Hkv, D))
             va = e3._lib.verify_attn_args(q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
                                           self.attn.view(B, N, Hq, D), max_prefix_len=self.max_prefix,
-                                          dev_status=self.dev_status)
+                                          dev_status=self.dev_status, qk_rotated=self.fused_rope)
             keep.append(va)
             ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st)))
             lin(self.attn, self.wo[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
@@ -463,7 +473,7 @@ def run_gpu(args):
     # all work on one side stream: graph capture needs a stream other than the legacy default one
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    eng = Engine(cfg, args.steps * 2 + max(args.warmup, args.steps) + 3, dev)
+    eng = Engine(cfg, args.steps * 2 + max(args.warmup, args.steps) + 3, dev, fused_rope=not args.rope_in_attention)
     use_graph = not args.eager
     if use_graph and not external_events_ok():
         eng.timing = False                      # timing events cannot live inside a graph: time kernels eagerly
@@ -764,7 +774,7 @@ def run_generate(args):
     cfg = dict(CFG)
     cfg["B"] = args.batch
     n_new = args.generate
-    eng = Engine(cfg, n_new + 2, dev, timing=False)
+    eng = Engine(cfg, n_new + 2, dev, timing=False, fused_rope=not args.rope_in_attention)
     eng.step()                                    # warm-up step (its tokens are not counted)
     eng.capture(1)
     gen = torch.zeros(cfg["B"], dtype=torch.int64, device=dev)
@@ -992,6 +1002,8 @@ def main():
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)
     ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
+    ap.add_argument("--rope-in-attention", action="store_true",
+                    help="plain QKV projection, RoPE applied inside the verify attention (the unfused path)")
     args = ap.parse_args()
     if args.warmup < 3 and not args.kernel:
         args.warmup = 3

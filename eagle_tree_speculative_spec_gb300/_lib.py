@@ -64,16 +64,19 @@ class VerifyAttnArgs(ctypes.Structure):
                 ("head_dim", _i32), ("s_max", _i32), ("max_prefix_len", _i32), ("num_splits", _i32),
                 ("q_node_stride", _i64), ("kv_node_stride", _i64), ("rope_theta", _f32), ("sm_scale", _f32),
                 ("q", _p), ("tree_k", _p), ("tree_v", _p), ("k_cache", _p), ("v_cache", _p),
-                ("parents", _p), ("prefix_len", _p), ("out", _p), ("lse", _p), ("dev_status", _p)]
+                ("parents", _p), ("prefix_len", _p), ("out", _p), ("lse", _p), ("dev_status", _p),
+                ("qk_rotated", _i32)]
 
 
 class LinearArgs(ctypes.Structure):
     _fields_ = [("m", _i32), ("n", _i32), ("k", _i32), ("epilogue", _i32), ("splits", _i32),
                 ("ld_x", _i64), ("ld_w", _i64), ("ld_out", _i64), ("ld_res", _i64),
-                ("x", _p), ("w", _p), ("w2", _p), ("out", _p), ("residual", _p), ("dev_status", _p)]
+                ("x", _p), ("w", _p), ("w2", _p), ("out", _p), ("residual", _p), ("dev_status", _p),
+                ("rope_cols", _i32), ("rope_rows_per_seq", _i32), ("rope_theta", ctypes.c_float),
+                ("rope_base", _p), ("rope_depth", _p)]
 
 
-EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU = 0, 1, 2, 3
+EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU, EPI_BF16_ROPE = 0, 1, 2, 3, 4
 
 DRAFT_WEIGHT_NAMES = ("w_fc", "embed", "input_norm", "hidden_norm", "w_qkv", "w_o", "post_norm", "w_gate",
                       "w_up", "w_down", "final_norm", "lm_head")
@@ -269,9 +272,10 @@ def _view_ptr(t, dtype, name):
 
 
 def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
-                     lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None):
+                     lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None, qk_rotated=False):
     """q [B, N, Hq, D] and tree_k / tree_v [B, N, Hkv, D] may be node-strided views (e.g. slices of a
-    fused [B, N, (Hq + 2 Hkv) * D] projection output); everything else is dense."""
+    fused [B, N, (Hq + 2 Hkv) * D] projection output); everything else is dense.  qk_rotated: q and
+    tree_k already carry RoPE at prefix_len + depth (EPI_BF16_ROPE projection)."""
     B, N, Hq, D = q.shape
     Hkv = tree_k.shape[2]
     S = k_cache.shape[2]
@@ -297,7 +301,7 @@ def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, o
                           parents=_ptr(parents, torch.int32, "parents"),
                           prefix_len=_ptr(prefix_len, torch.int32, "prefix_len"),
                           out=_ptr(out, bf, "out"), lse=_ptr(lse, torch.float32, "lse"),
-                          dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+                          dev_status=_ptr(dev_status, torch.int32, "dev_status"), qk_rotated=1 if qk_rotated else 0)
 
 
 def eagle3_verify_attn_workspace_size(args):
@@ -306,11 +310,12 @@ def eagle3_verify_attn_workspace_size(args):
 
 def eagle3_verify_attn(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
                        lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None,
-                       workspace=None, stream=None):
-    """Tree-masked verify attention for one layer (bf16, head_dim 128); rotates tree_k in place."""
+                       workspace=None, stream=None, qk_rotated=False):
+    """Tree-masked verify attention for one layer (bf16, head_dim 128); rotates tree_k in place
+    unless qk_rotated (q and tree_k already rotated)."""
     a = verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out,
                          max_prefix_len=max_prefix_len, lse=lse, rope_theta=rope_theta, sm_scale=sm_scale,
-                         num_splits=num_splits, dev_status=dev_status)
+                         num_splits=num_splits, dev_status=dev_status, qk_rotated=qk_rotated)
     L = lib()
     need = L.eagle3_verify_attn_workspace_size(ctypes.byref(a))
     if workspace is None:
@@ -321,9 +326,12 @@ def eagle3_verify_attn(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len,
 
 
 def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, splits=0, dev_status=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, rope_cols=0, rope_rows_per_seq=1, rope_theta=500000.0,
+                  rope_base=None, rope_depth=None):
     """out = epilogue(x W^T) on the tensor cores.  x [m, k] bf16, w (and w2) [n, k] bf16,
-    out [m, n] bf16 (fp32 for EPI_F32), residual [m, n] bf16 for EPI_BF16_RESIDUAL."""
+    out [m, n] bf16 (fp32 for EPI_F32), residual [m, n] bf16 for EPI_BF16_RESIDUAL.
+    EPI_BF16_ROPE rotates columns [0, rope_cols) per 128-wide head at row position
+    rope_base[row // rope_rows_per_seq] + rope_depth[row] (int32 device tensors)."""
     m, k = x.shape
     n = w.shape[0]
     if w.shape[1] != k or (w2 is not None and tuple(w2.shape) != (n, k)):
@@ -334,7 +342,10 @@ def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, split
     bf = torch.bfloat16
     a = LinearArgs(m=m, n=n, k=k, epilogue=int(epilogue), splits=int(splits), ld_x=0, ld_w=0, ld_out=0, ld_res=0,
                    x=_ptr(x, bf, "x"), w=_ptr(w, bf, "w"), w2=_ptr(w2, bf, "w2"), out=_ptr(out, want, "out"),
-                   residual=_ptr(residual, bf, "residual"), dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+                   residual=_ptr(residual, bf, "residual"), dev_status=_ptr(dev_status, torch.int32, "dev_status"),
+                   rope_cols=int(rope_cols), rope_rows_per_seq=int(rope_rows_per_seq), rope_theta=float(rope_theta),
+                   rope_base=_ptr(rope_base, torch.int32, "rope_base"),
+                   rope_depth=_ptr(rope_depth, torch.int32, "rope_depth"))
     L = lib()
     need = L.eagle3_linear_workspace_size(ctypes.byref(a))
     if workspace is None:
@@ -411,11 +422,11 @@ def eagle3_rmsnorm(x, w, out, *, eps=1e-5, gather=None, tap_out=None, dev_status
 
 def eagle3_verify_attn_noalloc(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
                                lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None,
-                               stream=None):
+                               stream=None, qk_rotated=False):
     """eagle3_verify_attn without a workspace: the library's static scratch holds the split partials."""
     a = verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out,
                          max_prefix_len=max_prefix_len, lse=lse, rope_theta=rope_theta, sm_scale=sm_scale,
-                         num_splits=num_splits, dev_status=dev_status)
+                         num_splits=num_splits, dev_status=dev_status, qk_rotated=qk_rotated)
     _check(lib().eagle3_verify_attn_noalloc(ctypes.byref(a), _stream(stream)), "eagle3_verify_attn_noalloc")
 
 

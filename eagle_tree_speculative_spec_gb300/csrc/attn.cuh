@@ -30,6 +30,7 @@ struct AttnLaunch {
     const int32_t *prefix_len;
     float *lse;
     int32_t *dev_status;
+    int qk_rotated = 0;              // q and the tree keys arrive rotated (no RoPE, no tree_k write)
 };
 
 size_t tree_attn_workspace(const AttnLaunch &a);

@@ -694,7 +694,7 @@ eagle3_status_t draft_validate(const eagle3_draft_tree_args_t *a) {
 
 eagle3_linear_args_t lin(int m, int n, int k, int epi, const void *x, const void *w, void *out, const void *res = nullptr,
                          const void *w2 = nullptr, int32_t *st = nullptr) {
-    eagle3_linear_args_t l;
+    eagle3_linear_args_t l = {};
     l.m = m;
     l.n = n;
     l.k = k;

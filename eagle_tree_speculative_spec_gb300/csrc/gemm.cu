@@ -53,6 +53,11 @@ struct GemmParams {
     int *sk_flag;                    // stream-K: [grid] warps of the slot's CTA that have written it
     int tma_out;                     // outputs leave through shared memory and TMA stores
     int32_t *dev_status;
+    // BF16_ROPE: columns [0, rope_cols) rotated per 128-wide head at row position
+    // rope_base[row / rope_rows] + rope_depth[row]
+    int rope_cols, rope_rows;
+    const int32_t *rope_base, *rope_depth;
+    float rope_inv[64];              // theta^(-2j/128), computed in double, rounded to float
 };
 
 // One piece of work of a CTA: k-blocks [kb0, kb1) of output tile (mb, nb).
@@ -128,6 +133,20 @@ struct Cfg {
 };
 
 E3_DEV float silu(float x) { return x / (1.0f + __expf(-x)); }
+
+// sin and cos of an fp32 RoPE angle (|a| < 2^17): Cody-Waite reduction by 2 pi with a three-part
+// float split of 2 pi (each product exact inside its fused multiply-add), then the special-function
+// unit's sin / cos on the reduced argument in [-pi, pi] (absolute error ~1e-6, below the rounding
+// of the fp32 angle itself and of the bf16 output)
+constexpr float TWO_PI_A = 0x1.921fb6p+2f, TWO_PI_B = -0x1.777a5cp-23f, TWO_PI_C = -0x1.ee59dap-48f;
+constexpr float INV_TWO_PI = 0x1.45f306p-3f;
+E3_DEV void rope_sincos(float a, float &s, float &c) {
+    const float k = rintf(a * INV_TWO_PI);
+    float r = fmaf(-k, TWO_PI_A, a);
+    r = fmaf(-k, TWO_PI_B, r);
+    r = fmaf(-k, TWO_PI_C, r);
+    __sincosf(r, &s, &c);
+}
 
 // Residual columns [col0, col0 + 8 n) of one row as n 16-byte vectors (bounds-checked element by
 // element at the right edge or for an unaligned row), read through L2 only: each value is read once.
@@ -208,7 +227,9 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
     }
 }
 
-template <int BN>
+// ROPE: the instantiation with the rotary epilogue (kept apart so that the others do not carry its
+// registers)
+template <int BN, bool ROPE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_out,
@@ -463,10 +484,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool res = p.epi == EAGLE3_EPI_BF16_RESIDUAL && row < p.M;
                 uint4 r_cur[8], r_next[8];
                 if (res) load_residual(p, row, nb * BN, r_cur);
+                // RoPE: this row's position (the chunk pairs of a head are rotated together)
+                const bool rope_epi = ROPE && p.epi == EAGLE3_EPI_BF16_ROPE;
+                float rope_pos = 0.0f;
+                if (rope_epi && row < p.M) rope_pos = (float)(p.rope_base[row / p.rope_rows] + p.rope_depth[row]);
+                uint4 u_hi[8];                // the second half of a rotated head, for the next chunk
                 for (int sc = 0; sc < chunks; ++sc) {
                     if (res && sc + 1 < chunks) load_residual(p, row, nb * BN + (sc + 1) * 64, r_next);
                     uint4 u[8];
-                    if (f32) {
+                    const bool rot = rope_epi && nb * BN + sc * 64 < p.rope_cols;   // chunks pair up: BN % 128 == 0
+                    if (ROPE && rot && (sc & 1)) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) u[j] = u_hi[j];
+                    } else if (ROPE && rot) {
+                        // dims 0..63 of the head (this chunk) with dims 64..127 (the next chunk)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float a[32], c[32];
+                            tc::tmem_ld32(t_row + sc * 64 + h * 32, a);
+                            tc::tmem_ld32(t_row + (sc + 1) * 64 + h * 32, c);
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                float lo[2], hi[2];
+#pragma unroll
+                                for (int q = 0; q < 2; ++q) {
+                                    float sn, cs;
+                                    rope_sincos(__fmul_rn(rope_pos, p.rope_inv[h * 32 + e + q]), sn, cs);
+                                    lo[q] = a[e + q] * cs - c[e + q] * sn;
+                                    hi[q] = c[e + q] * cs + a[e + q] * sn;
+                                }
+                                __nv_bfloat162 l2 = __floats2bfloat162_rn(lo[0], lo[1]);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(hi[0], hi[1]);
+                                const int wi = h * 16 + e / 2;   // packed word of the 64-column chunk
+                                reinterpret_cast<uint32_t *>(u)[wi] = *reinterpret_cast<uint32_t *>(&l2);
+                                reinterpret_cast<uint32_t *>(u_hi)[wi] = *reinterpret_cast<uint32_t *>(&h2);
+                            }
+                        }
+                    } else if (f32) {
                         float v[32];
                         tc::tmem_ld32(t_row + sc * 32, v);
                         add_contrib(v, sc * 32);
@@ -679,7 +733,8 @@ Plan plan(const eagle3_linear_args_t *a) {
     // count in 1..8 (at least 4 k-blocks each) whose units fill their last wave best, a larger
     // count only when it fills it by 2% more; the partials are reduced in split order.
     int auto_splits = 1;
-    if (a->splits <= 0 && pl.tiles_m == 1 && tiles <= 2 * sms) {
+    const bool rope = a->epilogue == EAGLE3_EPI_BF16_ROPE;   // rotated in the epilogue: one k pass per tile
+    if (!rope && a->splits <= 0 && pl.tiles_m == 1 && tiles <= 2 * sms) {
         double best = 0.0;
         for (int sp = 1; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
             const int units = tiles * sp, w = (units + sms - 1) / sms;
@@ -690,7 +745,7 @@ Plan plan(const eagle3_linear_args_t *a) {
             }
         }
     }
-    pl.streamk = a->splits <= 0 && auto_splits == 1 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
+    pl.streamk = !rope && a->splits <= 0 && auto_splits == 1 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
                  (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms;
     if (pl.streamk) {
         pl.splits = 1;
@@ -700,7 +755,7 @@ Plan plan(const eagle3_linear_args_t *a) {
         pl.ws_bytes = (size_t)sms * BM * pl.bn * sizeof(float) + (size_t)sms * sizeof(int);
         return pl;
     }
-    int splits = a->splits > 0 ? a->splits : auto_splits;
+    int splits = rope ? 1 : (a->splits > 0 ? a->splits : auto_splits);
     splits = std::max(1, std::min(splits, pl.kb_total));
     pl.kb_per_split = (pl.kb_total + splits - 1) / splits;
     pl.splits = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
@@ -713,10 +768,19 @@ Plan plan(const eagle3_linear_args_t *a) {
 eagle3_status_t validate(const eagle3_linear_args_t *a) {
     if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->m < 0 || a->n < 1 || a->k < 1 || a->splits < 0) return EAGLE3_ERR_INVALID_ARGUMENT;
-    if (a->epilogue < EAGLE3_EPI_BF16 || a->epilogue > EAGLE3_EPI_SWIGLU) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->epilogue < EAGLE3_EPI_BF16 || a->epilogue > EAGLE3_EPI_BF16_ROPE) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->epilogue == EAGLE3_EPI_BF16_ROPE) {
+        if (a->rope_cols < 0 || a->rope_cols > a->n || a->rope_cols % 128 || a->rope_rows_per_seq < 1 ||
+            !(a->rope_theta > 0.0f) || a->splits > 1)
+            return EAGLE3_ERR_INVALID_ARGUMENT;
+        const int64_t ld_o = a->ld_out ? a->ld_out : a->n;
+        if (((uintptr_t)a->out & 15) || (ld_o % 8)) return EAGLE3_ERR_UNSUPPORTED;   // TMA-stored output
+    }
     if (a->k % 8) return EAGLE3_ERR_UNSUPPORTED;   // 16-byte row pitch for TMA
     if (a->m == 0) return EAGLE3_OK;
     if (!a->x || !a->w || !a->out) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->epilogue == EAGLE3_EPI_BF16_ROPE && a->rope_cols > 0 && (!a->rope_base || !a->rope_depth))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->epilogue == EAGLE3_EPI_SWIGLU && !a->w2) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->epilogue == EAGLE3_EPI_BF16_RESIDUAL && !a->residual) return EAGLE3_ERR_INVALID_ARGUMENT;
     const int64_t ld_x = a->ld_x ? a->ld_x : a->k, ld_w = a->ld_w ? a->ld_w : a->k;
@@ -777,15 +841,24 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.sk_part = pl.streamk ? (float4 *)workspace : nullptr;
     p.sk_flag = pl.streamk ? (int *)((uint8_t *)workspace + (size_t)pl.grid * BM * pl.bn * sizeof(float)) : nullptr;
     p.dev_status = a->dev_status;
+    p.rope_cols = a->epilogue == EAGLE3_EPI_BF16_ROPE ? a->rope_cols : 0;
+    p.rope_rows = a->rope_rows_per_seq > 0 ? a->rope_rows_per_seq : 1;
+    p.rope_base = a->rope_base;
+    p.rope_depth = a->rope_depth;
+    for (int j = 0; j < 64; ++j)
+        p.rope_inv[j] = p.rope_cols ? (float)std::pow((double)a->rope_theta, -2.0 * j / 128.0) : 0.0f;
     CUtensorMap mo;
     p.tma_out = make_out_map(&mo, a->out, a->m, a->n, p.ld_out, a->epilogue == EAGLE3_EPI_F32) ? 1 : 0;
     if (!p.tma_out) mo = ma;   // unused
+    if (p.rope_cols && !p.tma_out) return EAGLE3_ERR_UNSUPPORTED;
 
     using C = Cfg<256>;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_tc_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(gemm_tc_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+                cudaSuccess)
             return EAGLE3_ERR_CUDA;
         attr = true;
     }
@@ -803,9 +876,12 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
         attr_coop[0].val.cooperative = 1;
         cfg.attrs = attr_coop;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, ma, mb, mb2, mo, p) != cudaSuccess) return EAGLE3_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, false>, ma, mb, mb2, mo, p) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
+    } else if (p.rope_cols) {
+        gemm_tc_kernel<256, true><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
     } else {
-        gemm_tc_kernel<256><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
+        gemm_tc_kernel<256, false><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
     }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (pl.splits > 1) {

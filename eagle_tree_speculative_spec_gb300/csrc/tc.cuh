@@ -53,6 +53,14 @@ E3_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, int x, int y, in
         : "memory");
 }
 
+E3_DEV void tma_load_4d(void *smem_dst, const CUtensorMap *map, int x, int y, int z, int w, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];\n" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // TMA store of a 2-D box from shared memory (bulk-group completion), and the waits on it
 E3_DEV void tma_store_2d(const CUtensorMap *map, int x, int y, const void *smem_src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(

@@ -65,6 +65,7 @@ struct Params {
     int halves;                     // CTAs per (sequence, KV head, split): 1 or 2
     int tree_slot_inner;            // tree maps: slots are the middle dimension (else the outer)
     int s_mid;                      // with two halves, the first half's query slots are [q_lo, q_lo + s_mid)
+    int qk_rotated;                 // q and the tree keys arrive rotated: Q is loaded by TMA as is
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
     // element (b, slot i, head h) lives at base + b * sb + i * si + h * D
@@ -159,7 +160,7 @@ E3_DEV void rope_chunks(uint4 &lo, uint4 &hi, const float cs[8], const float sn[
 __global__ void __launch_bounds__(NT, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_tk, const __grid_constant__ CUtensorMap tm_tv,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap tm_q, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ SmemStatic ss;
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mbar_init(&ss.s_done, 1);
         tc::mbar_init(&ss.pv_mma_done, 1);
-        tc::mbar_init(&ss.q_ready, 8);
+        tc::mbar_init(&ss.q_ready, p.qk_rotated ? 1 : 8);   // the Q load, or the eight staging warps
         ss.abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -239,8 +240,21 @@ __global__ void __launch_bounds__(NT, 1)
             uint8_t *ring = sm + (is_k ? OFF_K : OFF_V);
             tc::prefetch_tmap(map);
             if (last) tc::prefetch_tmap(tmap);
-            // V stage 1 holds the RoPE angle table until Q is staged
-            bool go = is_k || tc::mbar_wait(&ss.q_ready, 0, abort);
+            // V stage 1 holds the RoPE angle table until Q is staged (not used when Q arrives rotated)
+            bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort);
+            if (is_k && p.qk_rotated) {
+                // Q as is: two 64-column blocks of (slot, head) rows, rows = slot * rep + head
+                tc::prefetch_tmap(&tm_q);
+                tc::mbar_expect_tx(&ss.q_ready, Q_TILE);
+                const int hs = g * rep;
+                if (p.tree_slot_inner) {
+                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, s_lo, b, &ss.q_ready);
+                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, s_lo, b, &ss.q_ready);
+                } else {
+                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, b, s_lo, &ss.q_ready);
+                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, b, s_lo, &ss.q_ready);
+                }
+            }
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             uint32_t issued = 0, last_par = 0;
             for (int j = 0; j < n_tiles && go; ++j) {
@@ -266,6 +280,11 @@ __global__ void __launch_bounds__(NT, 1)
                 last_par = (last_par & ~(1u << s)) | (ph << s);
             }
             if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            if (is_k && p.qk_rotated) {   // the Q load too (bounded)
+                const long long t0 = clock64();
+                while (!tc::mbar_try(&ss.q_ready, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+                }
+            }
             // no TMA write may be in flight when the CTA exits (bounded)
             for (int s = 0; s < stages; ++s) {
                 if (!((issued >> s) & 1u)) continue;
@@ -370,7 +389,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight softmax warps only
-        {
+        if (!p.qk_rotated) {
             const int c = lane & 7, sub = lane >> 3;
             // RoPE angles of every position in [pos_lo, pos_lo + span), once per CTA, in V stage 1
             // (its first load waits for Q to be staged); others are computed directly
@@ -714,6 +733,25 @@ bool make_tree_map(CUtensorMap *m, const void *base, int nb, int nk, int64_t kv_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [B, slots, Hq, 128] (slot or batch pitch outermost) as a 4-D tensor whose box is one KV head's
+// rep query heads x MT / rep slots x 64 columns: the box lands as rows slot * rep + head, 128-byte
+// swizzled like the other tiles
+bool make_q_map(CUtensorMap *m, const void *base, int nb, int n_slots, int Hq, int rep, int64_t sb, int64_t si) {
+    auto fn = encode_fn();
+    if (!fn || rep < 1 || MT % rep || MT / rep > 256 || ((uintptr_t)base & 15) || (sb % 8) || (si % 8)) return false;
+    const bool slot_inner = si <= sb;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)(slot_inner ? n_slots : nb),
+                                (cuuint64_t)(slot_inner ? nb : n_slots)};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)(slot_inner ? si : sb) * 2,
+                                   (cuuint64_t)(slot_inner ? sb : si) * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)rep, slot_inner ? (cuuint32_t)(MT / rep) : 1u,
+                               slot_inner ? 1u : (cuuint32_t)(MT / rep)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_cache_map(CUtensorMap *m, const void *base, int64_t rows) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -849,13 +887,18 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     if (!make_tree_map(&mtk, p.k, pt.nb, nk_all, (int64_t)a.Hkv * D, a.k_sb, a.k_si) ||
         !make_tree_map(&mtv, p.v, pt.nb, nk_all, (int64_t)a.Hkv * D, a.v_sb, a.v_si))
         return EAGLE3_ERR_CUDA;
-    {
+    p.qk_rotated = a.qk_rotated ? 1 : 0;
+    CUtensorMap mq = mk;   // unused unless Q arrives rotated
+    if (p.qk_rotated) {
+        if ((a.q_si <= a.q_sb ? 1 : 0) != p.tree_slot_inner) return EAGLE3_ERR_UNSUPPORTED;
+        if (!make_q_map(&mq, p.q, pt.nb, a.n_slots, a.Hq, p.rep, a.q_sb, a.q_si)) return EAGLE3_ERR_UNSUPPORTED;
+    } else {
         // the query slots' keys rotated in tree_k first; the attention streams them like the prefix
         const int64_t warps = (int64_t)pt.nb * nq * a.Hkv;
         tree_rotate_kernel<<<(unsigned)((warps + 31) / 32), 256, 0, stream>>>(p);   // 32 rows per block
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
-    verify_attn_kernel<<<dim3(splits * p.halves, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, mtk, mtv, p);
+    verify_attn_kernel<<<dim3(splits * p.halves, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, mtk, mtv, mq, p);
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
         verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
@@ -964,6 +1007,7 @@ static AttnLaunch verify_launch(const eagle3_verify_attn_args_t *a) {
     l.prefix_len = a->prefix_len;
     l.lse = a->lse;
     l.dev_status = a->dev_status;
+    l.qk_rotated = a->qk_rotated ? 1 : 0;
     return l;
 }
 

@@ -213,6 +213,10 @@ typedef struct {
     uint16_t *out;              /* [B, N, Hq, D] bf16                                                 */
     float *lse;                 /* [B, N, Hq] fp32 or NULL                                            */
     int32_t *dev_status;        /* optional                                                           */
+    int32_t qk_rotated;         /* 1: q and tree_k arrive already rotated at prefix_len + depth (e.g.
+                                   from eagle3_linear's EAGLE3_EPI_BF16_ROPE); neither is rotated
+                                   again and tree_k is not written.  Needs (Hq / Hkv) to divide 128
+                                   and a q node pitch of whole 16 bytes (else EAGLE3_ERR_UNSUPPORTED) */
 } eagle3_verify_attn_args_t;
 
 size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *args);

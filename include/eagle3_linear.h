@@ -10,6 +10,18 @@
  *   EAGLE3_EPI_BF16_RESIDUAL  out (bf16) = residual + x W^T         (residual stream; out may be
  *                                                                    the residual buffer itself)
  *   EAGLE3_EPI_SWIGLU         out (bf16) = silu(x W^T) * (x W2^T)   (W = gate, W2 = up, both [n, k])
+ *   EAGLE3_EPI_BF16_ROPE      out (bf16) = x W^T with rotate-half RoPE applied (in fp32, before the
+ *                             rounding) to the columns [0, rope_cols) taken as 128-wide heads: row r
+ *                             sits at position pos = rope_base[r / rope_rows_per_seq] + rope_depth[r]
+ *                             and, per head, column pair (j, j + 64), j < 64, becomes
+ *                             (x_j cos a_j - x_{j+64} sin a_j, x_{j+64} cos a_j + x_j sin a_j) with
+ *                             a_j = fp32(pos * inv_j), inv_j = theta^(-2j/128) computed in double and
+ *                             rounded to float ("EAGLE-3: Engineering Implementation of LLM Inference
+ *                             Acceleration", appendix C: rotate-half RoPE; "Advanced speculative
+ *                             decoding: tree drafts and EAGLE", section "Implementation": a tree
+ *                             node sits at prefix length + depth).  This is the q / k part of a fused
+ *                             QKV projection leaving already rotated; the k-split plans are not used
+ *                             and the output must be 16-byte aligned with a pitch of whole 16 bytes.
  * Shapes: x [m, k] (row pitch ld_x), W and W2 [n, k] (row pitch ld_w), out [m, n] (pitch ld_out),
  * residual [m, n] (pitch ld_res); a pitch of 0 means dense.  k and every pitch must be multiples of
  * 8 elements and x, W, W2 must start on 16-byte boundaries.  All pointers are caller-owned device
@@ -32,7 +44,8 @@ typedef enum {
     EAGLE3_EPI_BF16 = 0,
     EAGLE3_EPI_F32 = 1,
     EAGLE3_EPI_BF16_RESIDUAL = 2,
-    EAGLE3_EPI_SWIGLU = 3
+    EAGLE3_EPI_SWIGLU = 3,
+    EAGLE3_EPI_BF16_ROPE = 4
 } eagle3_epilogue_t;
 
 typedef struct {
@@ -46,6 +59,12 @@ typedef struct {
     void *out;                  /* [m, n] bf16 or fp32                                            */
     const uint16_t *residual;   /* [m, n] bf16 (BF16_RESIDUAL only)                               */
     int32_t *dev_status;        /* optional EAGLE3_DEV_* word                                     */
+    /* BF16_ROPE only (ignored otherwise) */
+    int32_t rope_cols;          /* rotated columns, a multiple of 128, <= n                        */
+    int32_t rope_rows_per_seq;  /* rows of one sequence (row r belongs to sequence r / this)       */
+    float rope_theta;           /* > 0                                                            */
+    const int32_t *rope_base;   /* [ceil(m / rope_rows_per_seq)] base position per sequence        */
+    const int32_t *rope_depth;  /* [m] offset per row                                             */
 } eagle3_linear_args_t;
 
 size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *args);

@@ -114,3 +114,30 @@ def test_linear_stream_k(m, n, k, epi):
     atol, rtol = (1e-3, 1e-3) if epi == "f32" else (2e-2, 1e-2)
     ok, err = close(got, want, atol, rtol)
     assert ok, err
+
+
+@pytest.mark.parametrize("m,rows_per_seq,n_heads,rope_heads", [(120, 60, 6, 5), (3840, 60, 48, 40), (7, 7, 3, 2)])
+def test_linear_rope_epilogue(m, rows_per_seq, n_heads, rope_heads):
+    """EPI_BF16_ROPE: the fused projection leaves its first rope_heads 128-wide heads rotated at
+    position base[row // rows_per_seq] + depth[row] (rotate-half RoPE, angles fp32(pos * inv_j)),
+    the rest plain; against the fp64 product rotated by the oracle's RoPE."""
+    from oracle import attention as oatt
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16_ROPE, eagle3_linear
+    dev = require_gpu()
+    n, k = n_heads * 128, 256
+    x, w, _ = _inputs(m, n, k, 5)
+    g = np.random.default_rng(6)
+    n_seq = (m + rows_per_seq - 1) // rows_per_seq
+    base = g.integers(0, 20000, n_seq).astype(np.int32)
+    depth = g.integers(0, 7, m).astype(np.int32)
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=dev)
+    eagle3_linear(x.to(dev), w.to(dev), out, epilogue=EPI_BF16_ROPE, rope_cols=rope_heads * 128,
+                  rope_rows_per_seq=rows_per_seq, rope_theta=500000.0,
+                  rope_base=torch.as_tensor(base, device=dev), rope_depth=torch.as_tensor(depth, device=dev))
+    torch.cuda.synchronize()
+    want = _ref(x, w)
+    pos = base[np.arange(m) // rows_per_seq] + depth
+    rot = want[:, : rope_heads * 128].reshape(m, rope_heads, 128)
+    want[:, : rope_heads * 128] = oatt.rope_apply(rot, pos, 500000.0).reshape(m, rope_heads * 128)
+    ok, err = close(out.float().cpu().numpy(), want, 2e-2, 1e-2)
+    assert ok, f"max err {err}"

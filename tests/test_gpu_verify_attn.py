@@ -82,3 +82,35 @@ def test_verify_full_size(B, L):
     got = _run(inp, L)
     rows = sorted({0, B // 2, B - 1})
     _check(inp, got, rows)
+
+
+@pytest.mark.parametrize("B,L", [(3, 200), (64, 2048)])
+def test_verify_qk_rotated(B, L):
+    """qk_rotated: q and tree_k arrive rotated at prefix_len + depth (as the RoPE projection leaves
+    them); the output equals the oracle's on the un-rotated inputs and tree_k is left as given."""
+    from eagle_tree_speculative_spec_gb300 import eagle3_verify_attn
+    dev = require_gpu()
+    lens = [L] * B if B > 8 else [L, 0, L // 3]
+    inp = synth.verify_attn_batch(35, B, 60, 32, 8, 128, lens, S_max=max(lens) + 64)
+    par = np.asarray(inp["parents"])
+    depth = np.zeros(par.shape, np.int64)
+    for i in range(1, par.shape[1]):
+        depth[:, i] = depth[np.arange(B), par[:, i]] + 1
+    pos = np.asarray(inp["prefix_len"])[:, None] + depth                   # [B, N]
+    rot = lambda t: np.stack([oatt.rope_apply(t[b], pos[b]) for b in range(B)], 0)
+    q_r = torch.as_tensor(rot(inp["q_f32"]), dtype=torch.float32).to(torch.bfloat16)
+    k_r = torch.as_tensor(rot(inp["tree_k_f32"]), dtype=torch.float32).to(torch.bfloat16)
+    tk = k_r.to(dev).clone()
+    out = torch.full(inp["q"].shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    eagle3_verify_attn(q_r.to(dev), tk, inp["tree_v"].to(dev), inp["k_cache"].to(dev), inp["v_cache"].to(dev),
+                       torch.as_tensor(par, device=dev), torch.as_tensor(inp["prefix_len"], device=dev), out,
+                       max_prefix_len=max(lens), qk_rotated=True)
+    torch.cuda.synchronize()
+    assert torch.equal(tk.cpu(), k_r)
+    rows = sorted({0, B // 2, B - 1})
+    ref_o, _, _ = oatt.verify_attention(inp["q_f32"], inp["tree_k_f32"], inp["tree_v_f32"], inp["k_cache_f32"],
+                                        inp["v_cache_f32"], inp["parents"], inp["prefix_len"], batch_rows=rows)
+    o = out.float().cpu().numpy()
+    for b in rows:
+        ok, err = close(o[b], ref_o[b], ATOL, RTOL)
+        assert ok, f"out b={b} max err {err}"
