@@ -386,7 +386,7 @@ class Engine:
         B, N, Hq, Hkv, D = c["B"], c["N"], c["Hq"], c["Hkv"], c["D"]
         kv_prefix = 2 * B * Hkv * L * D * 2
         tree_kv = 2 * B * N * Hkv * D * 2
-        rot_write = B * N * Hkv * D * 2
+        rot_write = 0 if self.fused_rope else B * N * Hkv * D * 2   # the in-call rotation writes tree_k back
         q_o = 2 * B * N * Hq * D * 2
         return kv_prefix + tree_kv + rot_write + q_o
 
@@ -846,10 +846,14 @@ def run_kernel(args):
         o = torch.empty(B, N, Hq, D, device=dev, dtype=bf)
         a = e3._lib.verify_attn_args(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L)
         ws = torch.empty(max(16, e3._lib.eagle3_verify_attn_workspace_size(a)), dtype=torch.uint8, device=dev)
-        fn = lambda: e3.eagle3_verify_attn(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L, workspace=ws)
+        # default: q and tree_k taken as already rotated (the fused RoPE projection's output, as in the
+        # step); --rope-in-attention: the call rotates them (and writes the rotated tree keys back)
+        qkr = not args.rope_in_attention
+        fn = lambda: e3.eagle3_verify_attn(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L, workspace=ws,
+                                           qk_rotated=qkr)
         ms = _time_loop(fn, args.steps, args.warmup, flush if B * L * 4096 < 512e6 else None)
-        nbytes = B * (4096 * L + 245760 + 122880 + 983040)
-        out.update(batch=B, prefix=L, ms=round(ms, 4), gbs=round(nbytes / ms / 1e6, 1),
+        nbytes = B * (4096 * L + 245760 + 983040 + (0 if qkr else 122880))
+        out.update(batch=B, prefix=L, qk_rotated=qkr, ms=round(ms, 4), gbs=round(nbytes / ms / 1e6, 1),
                    frac_measured=round(nbytes / ms / 1e6 / hbm, 4), frac_8tbs=round(nbytes / ms / 1e6 / 8000, 4),
                    tflops=round(983040 * L * B / ms / 1e9, 1), bytes=nbytes)
     elif args.kernel == "accept":
