@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(NT, 1)
     const int n_prefix = (k_hi - k_lo + BK - 1) / BK;
     const int n_tiles = n_prefix + (last ? 1 : 0);
 
-    // ---- phase A: barriers, TMEM, raw tree description into shared memory
+    // ---- phase A: barriers, TMEM, raw tree description into shared memory.  Thread 0, which is also
+    // the K producer, issues the first K tiles (and Q when it arrives rotated) as soon as their
+    // barriers exist, so that the loads are in flight during the rest of phase A.
+    int npre = 0;                   // K tiles issued in phase A
     if (tid == 0) {
         for (int s = 0; s < ST_K; ++s) {
             tc::mbar_init(&ss.k_full[s], 1);
@@ -205,6 +208,28 @@ __global__ void __launch_bounds__(NT, 1)
         tc::mbar_init(&ss.q_ready, p.qk_rotated ? 1 : 8);   // the Q load, or the eight staging warps
         ss.abort_flag = 0;
         tc::fence_barrier_init();
+        if (n_tiles > 0) {
+            if (p.qk_rotated) {
+                // Q as is: two 64-column blocks of (slot, head) rows, rows = slot * rep + head
+                tc::mbar_expect_tx(&ss.q_ready, Q_TILE);
+                const int hs = g * rep;
+                if (p.tree_slot_inner) {
+                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, s_lo, b, &ss.q_ready);
+                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, s_lo, b, &ss.q_ready);
+                } else {
+                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, b, s_lo, &ss.q_ready);
+                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, b, s_lo, &ss.q_ready);
+                }
+            }
+            const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
+            npre = min(ST_K, n_prefix);   // fresh stages: nothing to wait for
+            for (int j = 0; j < npre; ++j) {
+                uint8_t *dst = sm + OFF_K + j * KV_TILE;
+                tc::mbar_expect_tx(&ss.k_full[j], KV_TILE);
+                tc::tma_load_2d(dst, &tm_k, 0, row0 + j * BK, &ss.k_full[j]);
+                tc::tma_load_2d(dst + KV_TILE / 2, &tm_k, 64, row0 + j * BK, &ss.k_full[j]);
+            }
+        }
     }
     if (warp == 1) tc::tmem_alloc(&ss.tmem_base, 512);
     if (warp == 2 || warp == 3) {
@@ -242,22 +267,10 @@ __global__ void __launch_bounds__(NT, 1)
             if (last) tc::prefetch_tmap(tmap);
             // V stage 1 holds the RoPE angle table until Q is staged (not used when Q arrives rotated)
             bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort);
-            if (is_k && p.qk_rotated) {
-                // Q as is: two 64-column blocks of (slot, head) rows, rows = slot * rep + head
-                tc::prefetch_tmap(&tm_q);
-                tc::mbar_expect_tx(&ss.q_ready, Q_TILE);
-                const int hs = g * rep;
-                if (p.tree_slot_inner) {
-                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, s_lo, b, &ss.q_ready);
-                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, s_lo, b, &ss.q_ready);
-                } else {
-                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, b, s_lo, &ss.q_ready);
-                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, b, s_lo, &ss.q_ready);
-                }
-            }
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
-            uint32_t issued = 0, last_par = 0;
-            for (int j = 0; j < n_tiles && go; ++j) {
+            const int j0 = is_k ? npre : 0;                  // thread 0 issued K tiles [0, npre) in phase A
+            uint32_t issued = is_k ? (1u << npre) - 1u : 0u, last_par = 0;
+            for (int j = j0; j < n_tiles && go; ++j) {
                 const int s = j % stages;
                 const uint32_t ph = (uint32_t)(j / stages) & 1u;
                 if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) {
