@@ -11,7 +11,11 @@
 // overlaps the main loop of the next.  Work units are (m tile, n tile, k split), m fastest, so
 // concurrently running CTAs share the same weight tile in L2.  With more than one k split the
 // fp32 partials go to a workspace and a second kernel adds them in split order and applies the
-// epilogue (deterministic).
+// epilogue (deterministic).  A single M tile with at most two waves of N tiles takes the split
+// count (up to 8) whose units fill their last wave best: those launches stream weights with few
+// rows.  Outputs leave through 128B-swizzled shared memory and TMA stores where the output allows
+// it.  The RoPE epilogue (q/k heads of a fused QKV projection, rotated before rounding) is a
+// separate instantiation of the kernel.
 //
 // Stream-K: when the output tiles do not fill whole waves of the GPU, all but the last full wave
 // run as above (m fastest, so the CTAs of a wave share weight tiles in L2), and the remaining

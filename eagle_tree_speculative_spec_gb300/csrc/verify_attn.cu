@@ -23,7 +23,10 @@
 //                 than 8 (the result is the same, the intermediate weights stay below 2^8)
 // A kernel before this one rotates the query slots' keys in tree_k at their positions (prefix
 // length + depth); the last split then also streams the tree tile (64 rows of tree_k / tree_v, by
-// TMA like the prefix) and masks it with the ancestor bitmask.  With more than one split the
+// TMA like the prefix) and masks it with the ancestor bitmask.  When q and the tree keys arrive
+// already rotated (qk_rotated: the QKV projection applied RoPE), that kernel does not run and Q
+// comes in by one 4-D TMA load instead of the softmax warps' staging.  Thread 0 issues Q and the
+// first K tiles as soon as it has initialised their barriers.  With more than one split the
 // partial (O, m, l) go to the workspace and another kernel merges them in split order.
 // All waits are bounded; a timeout sets EAGLE3_DEV_TIMEOUT and the CTA drains and exits.
 #include <cudaTypedefs.h>
