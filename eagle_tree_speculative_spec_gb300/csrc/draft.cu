@@ -210,11 +210,13 @@ E3_DEV void insert_best(uint64_t (&best)[KMAX], uint64_t v) {
     }
 }
 
-// Row top-k by (value desc, index asc) and the row's fixed-point normaliser.  One CTA per row.
-// Each warp keeps its current top-k in shared memory and the packed key of its k-th best as a
-// threshold: an element below the threshold cannot enter the top-k, so it costs one compare;
-// the rest are appended (ballot-compacted) to a per-warp buffer that is merged into the list
-// only when it fills up.  For a row in random order about k ln(n / k) elements pass.
+// Row top-k by (value desc, index asc) and the row's fixed-point normaliser.  One CTA per row, or
+// a cluster of CTAs per row when rows are few.  Each warp keeps its current top-k in shared
+// memory and the packed key of its k-th best as a threshold: an element below the threshold
+// cannot enter the top-k, so it costs one compare (one per four elements: their NaN-propagating
+// maximum); the rest are appended (ballot-compacted) to a per-warp buffer that is merged into the
+// list only when it fills up.  For a row in random order about k ln(n / k) elements pass.  The
+// normaliser pass weighs two elements per paired-fp32 instruction, bit-identical to one at a time.
 constexpr int TK_CAP = 256;   // candidate buffer per warp (two float4 groups of a warp)
 
 // merge a warp's candidate buffer into its list (KMAX entries, the first k meaningful); returns
