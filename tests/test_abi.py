@@ -89,3 +89,30 @@ def test_compact_host_validation():
     assert L.eagle3_compact_kv(ctypes.byref(a), None) == 1        # null pointers
     a.batch = 0
     assert L.eagle3_compact_kv(ctypes.byref(a), None) == 0
+
+
+def _linear(**kw):
+    base = dict(m=128, n=768, k=256, epilogue=4, splits=0, ld_x=0, ld_w=0, ld_out=0, ld_res=0, x=16, w=16, w2=None,
+                out=16, residual=None, dev_status=None, rope_cols=640, rope_rows_per_seq=60, rope_theta=500000.0,
+                rope_base=16, rope_depth=16)
+    base.update(kw)
+    return B.LinearArgs(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(m=0), 0),
+    (dict(rope_cols=100), 1),          # not whole 128-wide heads
+    (dict(rope_cols=896), 1),          # beyond the output columns
+    (dict(rope_rows_per_seq=0), 1),
+    (dict(rope_theta=0.0), 1),
+    (dict(splits=2), 1),               # the RoPE epilogue runs unsplit
+    (dict(rope_base=None), 1),
+    (dict(rope_depth=None), 1),
+    (dict(out=24), 2),                 # outputs leave by TMA: 16-byte aligned only
+    (dict(ld_out=772), 2),             # ... with a whole-16-byte row pitch
+    (dict(epilogue=5), 1),
+])
+def test_linear_rope_host_validation(kw, want):
+    L = built_lib()
+    a = _linear(**kw)
+    assert L.eagle3_linear(ctypes.byref(a), None, 0, None) == want

@@ -141,3 +141,34 @@ def test_linear_rope_epilogue(m, rows_per_seq, n_heads, rope_heads):
     want[:, : rope_heads * 128] = oatt.rope_apply(rot, pos, 500000.0).reshape(m, rope_heads * 128)
     ok, err = close(out.float().cpu().numpy(), want, 2e-2, 1e-2)
     assert ok, f"max err {err}"
+
+
+def test_linear_rope_epilogue_padded_pitch():
+    """The RoPE epilogue through the C ABI with a padded output pitch (ld_out = n + 64): the padding
+    columns are left alone."""
+    import ctypes
+    from oracle import attention as oatt
+    from eagle_tree_speculative_spec_gb300 import EPI_BF16_ROPE
+    from eagle_tree_speculative_spec_gb300 import _lib as E
+    dev = require_gpu()
+    m, n, k, rows_per_seq = 100, 512, 256, 50
+    x, w, _ = _inputs(m, n, k, 7)
+    base = torch.tensor([40, 900], dtype=torch.int32, device=dev)
+    depth = torch.arange(m, dtype=torch.int32, device=dev) % 7
+    out = torch.full((m, n + 64), 3.0, dtype=torch.bfloat16, device=dev)
+    xd, wd = x.to(dev), w.to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = E.LinearArgs(m=m, n=n, k=k, epilogue=EPI_BF16_ROPE, splits=0, ld_x=0, ld_w=0, ld_out=n + 64, ld_res=0,
+                     x=xd.data_ptr(), w=wd.data_ptr(), w2=None, out=out.data_ptr(), residual=None,
+                     dev_status=st.data_ptr(), rope_cols=256, rope_rows_per_seq=rows_per_seq, rope_theta=10000.0,
+                     rope_base=base.data_ptr(), rope_depth=depth.data_ptr())
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    assert E.lib().eagle3_linear(ctypes.byref(a), ws.data_ptr(), ws.numel(), None) == 0
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    assert (got[:, n:] == 3.0).all()
+    want = _ref(x, w)
+    pos = base.cpu().numpy()[np.arange(m) // rows_per_seq] + depth.cpu().numpy()
+    want[:, :256] = oatt.rope_apply(want[:, :256].reshape(m, 2, 128), pos, 10000.0).reshape(m, 256)
+    ok, err = close(got[:, :n], want, 2e-2, 1e-2)
+    assert ok, f"max err {err}"

@@ -84,15 +84,12 @@ def test_verify_full_size(B, L):
     _check(inp, got, rows)
 
 
-@pytest.mark.parametrize("B,L", [(3, 200), (64, 2048)])
-def test_verify_qk_rotated(B, L):
-    """qk_rotated: q and tree_k arrive rotated at prefix_len + depth (as the RoPE projection leaves
-    them); the output equals the oracle's on the un-rotated inputs and tree_k is left as given."""
+def _run_rotated(inp, lens, num_splits=0):
+    """q and tree_k rotated at prefix_len + depth by the oracle's RoPE, then the qk_rotated call."""
     from eagle_tree_speculative_spec_gb300 import eagle3_verify_attn
     dev = require_gpu()
-    lens = [L] * B if B > 8 else [L, 0, L // 3]
-    inp = synth.verify_attn_batch(35, B, 60, 32, 8, 128, lens, S_max=max(lens) + 64)
     par = np.asarray(inp["parents"])
+    B = par.shape[0]
     depth = np.zeros(par.shape, np.int64)
     for i in range(1, par.shape[1]):
         depth[:, i] = depth[np.arange(B), par[:, i]] + 1
@@ -104,13 +101,41 @@ def test_verify_qk_rotated(B, L):
     out = torch.full(inp["q"].shape, float("nan"), dtype=torch.bfloat16, device=dev)
     eagle3_verify_attn(q_r.to(dev), tk, inp["tree_v"].to(dev), inp["k_cache"].to(dev), inp["v_cache"].to(dev),
                        torch.as_tensor(par, device=dev), torch.as_tensor(inp["prefix_len"], device=dev), out,
-                       max_prefix_len=max(lens), qk_rotated=True)
+                       max_prefix_len=max(lens), num_splits=num_splits, qk_rotated=True)
     torch.cuda.synchronize()
-    assert torch.equal(tk.cpu(), k_r)
-    rows = sorted({0, B // 2, B - 1})
+    assert torch.equal(tk.cpu(), k_r)                                        # tree_k is not rewritten
+    return out.float().cpu().numpy()
+
+
+def _check_out(inp, o, rows):
     ref_o, _, _ = oatt.verify_attention(inp["q_f32"], inp["tree_k_f32"], inp["tree_v_f32"], inp["k_cache_f32"],
                                         inp["v_cache_f32"], inp["parents"], inp["prefix_len"], batch_rows=rows)
-    o = out.float().cpu().numpy()
     for b in rows:
         ok, err = close(o[b], ref_o[b], ATOL, RTOL)
         assert ok, f"out b={b} max err {err}"
+
+
+@pytest.mark.parametrize("B,L", [(3, 200), (64, 2048)])
+def test_verify_qk_rotated(B, L):
+    """qk_rotated: q and tree_k arrive rotated at prefix_len + depth (as the RoPE projection leaves
+    them); the output equals the oracle's on the un-rotated inputs and tree_k is left as given."""
+    lens = [L] * B if B > 8 else [L, 0, L // 3]
+    inp = synth.verify_attn_batch(35, B, 60, 32, 8, 128, lens, S_max=max(lens) + 64)
+    _check_out(inp, _run_rotated(inp, lens), sorted({0, B // 2, B - 1}))
+
+
+@pytest.mark.parametrize("splits", [2, 3])
+def test_verify_qk_rotated_splits_ragged(splits):
+    lens = [0, 1, 64, 65, 200]
+    inp = synth.verify_attn_batch(36, len(lens), 60, 32, 8, 128, lens, S_max=300)
+    _check_out(inp, _run_rotated(inp, lens, num_splits=splits), range(len(lens)))
+
+
+def test_verify_qk_rotated_other_ratio():
+    """qk_rotated loads Q in boxes of (128 / rep) slots: rep = 8 works, rep = 3 is refused."""
+    lens = [130, 77]
+    inp = synth.verify_attn_batch(37, 2, 30, 16, 2, 128, lens, S_max=200)    # rep 8, 240 rows
+    _check_out(inp, _run_rotated(inp, lens), range(2))
+    inp = synth.verify_attn_batch(37, 2, 20, 12, 4, 128, lens, S_max=200)    # rep 3
+    with pytest.raises(Exception):
+        _run_rotated(inp, lens)
