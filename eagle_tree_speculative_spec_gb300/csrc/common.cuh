@@ -171,4 +171,28 @@ constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
 
 E3_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// ------------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be dispatched while the
+// previous kernel of its stream retires its last blocks; it runs pdl_wait() before its first
+// global memory access, which returns once that kernel has completed and its writes are visible
+// (for an ordinary launch it returns at once).
+// ------------------------------------------------------------------------------------------------
+E3_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace e3

@@ -128,6 +128,7 @@ struct NormParams {
 };
 
 __global__ void __launch_bounds__(NT_NORM) rmsnorm_kernel(const NormParams p) {
+    pdl_wait();
     __shared__ float red[NT_NORM / 32];
     const int r = blockIdx.x;
     int src = p.gather ? p.gather[r] : r;
@@ -1079,6 +1080,7 @@ extern "C" eagle3_status_t eagle3_rmsnorm(const eagle3_rmsnorm_args_t *a, eagle3
     p.out = (__nv_bfloat16 *)a->out;
     p.tap = (__nv_bfloat16 *)a->tap_out;
     p.dev_status = a->dev_status;
-    rmsnorm_kernel<<<a->rows, NT_NORM, 0, (cudaStream_t)stream>>>(p);
+    if (launch_pdl(rmsnorm_kernel, dim3(a->rows), dim3(NT_NORM), 0, (cudaStream_t)stream, p) != cudaSuccess)
+        return EAGLE3_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EAGLE3_OK : EAGLE3_ERR_CUDA;
 }

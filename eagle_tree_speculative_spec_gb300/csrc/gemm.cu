@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_base_slot;
+    pdl_wait();   // the previous kernel's outputs (this launch's inputs, or buffers it overwrites)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -626,6 +627,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // Split-K reduction in split order, then the epilogue.  One thread per output element pair.
 __global__ void gemm_reduce_kernel(const GemmParams p) {
+    pdl_wait();
     const int n_out = p.N;
     const size_t total = (size_t)p.M * n_out;
     for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
@@ -883,15 +885,20 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
         if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, false>, ma, mb, mb2, mo, p) != cudaSuccess)
             return EAGLE3_ERR_CUDA;
     } else if (p.rope_cols) {
-        gemm_tc_kernel<256, true><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
+        if (launch_pdl(gemm_tc_kernel<256, true>, dim3(pl.grid), dim3(NTHREADS), C::SMEM, (cudaStream_t)stream, ma,
+                       mb, mb2, mo, p) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
     } else {
-        gemm_tc_kernel<256, false><<<pl.grid, NTHREADS, C::SMEM, (cudaStream_t)stream>>>(ma, mb, mb2, mo, p);
+        if (launch_pdl(gemm_tc_kernel<256, false>, dim3(pl.grid), dim3(NTHREADS), C::SMEM, (cudaStream_t)stream, ma,
+                       mb, mb2, mo, p) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (pl.splits > 1) {
         const size_t total = (size_t)a->m * a->n;
         const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sm_count() * 8);
-        gemm_reduce_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
+        if (launch_pdl(gemm_reduce_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, p) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
     return EAGLE3_OK;

@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ SmemStatic ss;
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     volatile int *abort = &ss.abort_flag;
+    pdl_wait();   // the previous kernel's outputs (q / tree_k / caches) before any global access
     const int half = blockIdx.x % p.halves, split = blockIdx.x / p.halves, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo;
@@ -653,6 +654,7 @@ __global__ void __launch_bounds__(NT, 1)
 // rows per warp, at the slot's position (prefix length + depth from the parent array, or the given
 // position), with the same angle arguments and arithmetic the attention kernel uses for Q.
 __global__ void tree_rotate_kernel(const Params p) {
+    pdl_wait();
     const int nq = p.q_hi - p.q_lo;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t w = t >> 3;                    // row
@@ -690,6 +692,7 @@ __global__ void tree_rotate_kernel(const Params p) {
 
 // Merge split partials in split order: one warp per (b, query slot, head) row.
 __global__ void verify_combine_kernel(const Params p) {
+    pdl_wait();
     const int nq = p.q_hi - p.q_lo;
     const int rows = p.B * nq * p.Hq;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -911,13 +914,17 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     } else {
         // the query slots' keys rotated in tree_k first; the attention streams them like the prefix
         const int64_t warps = (int64_t)pt.nb * nq * a.Hkv;
-        tree_rotate_kernel<<<(unsigned)((warps + 31) / 32), 256, 0, stream>>>(p);   // 32 rows per block
-        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+        if (launch_pdl(tree_rotate_kernel, dim3((unsigned)((warps + 31) / 32)), dim3(256), 0, stream, p) !=
+            cudaSuccess)   // 32 rows per block
+            return EAGLE3_ERR_CUDA;
     }
-    verify_attn_kernel<<<dim3(splits * p.halves, a.Hkv, pt.nb), NT, SMEM_DYN, stream>>>(mk, mv, mtk, mtv, mq, p);
+    if (launch_pdl(verify_attn_kernel, dim3(splits * p.halves, a.Hkv, pt.nb), dim3(NT), SMEM_DYN, stream, mk, mv, mtk,
+                   mtv, mq, p) != cudaSuccess)
+        return EAGLE3_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
-        verify_combine_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+        if (launch_pdl(verify_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream, p) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
     return EAGLE3_OK;
