@@ -897,7 +897,19 @@ def run_kernel(args):
                                  eng.draft_len, eng.tokens, eng.parents, eng.depth, eng.anc, eng.score,
                                  n_heads=c["Hq"], ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
                                  max_draft_len=c["L0"], workspace=ws)
-        ms = _time_loop(fn, args.steps, args.warmup)
+        ms_eager = _time_loop(fn, args.steps, args.warmup)
+        # the call as the step runs it: captured once into a CUDA graph and replayed (eager issue of
+        # its ~70 launches from the host can take longer than the GPU work at small batches)
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            fn()
+        ms = _time_loop(graph.replay, args.steps, args.warmup)
+        out.update(ms_eager=round(ms_eager, 4))
         d, F, V, qw = c["d"], c["F"], c["V"], eng.qkv_w
         layer = lambda m: 2 * m * (2 * d * qw + c["Hq"] * 128 * d + 2 * d * F + F * d)
         rows_c = B * c["W"]
