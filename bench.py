@@ -731,7 +731,8 @@ def run_reference(args):
     value = cfg["B"] * cfg["N"] * args.steps / total
     cb = cpu_baseline(cfg)
     cb["value"] = round(value, 6)
-    line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+    # n_gpus: the launch's GPU count (the oracle itself runs on the host cores, rank 0 only)
+    line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "EAGLE-3 draft-and-verify step, Llama-3.1-8B-shaped target + EAGLE-3 head, "
