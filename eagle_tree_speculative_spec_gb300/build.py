@@ -58,10 +58,24 @@ def _compile(src, verbose, ptxas_verbose):
 
 
 def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile every kernel and link libeagle3.so; returns the library path."""
+    """Compile every kernel and link libeagle3.so; returns the library path.  Processes that build
+    at the same time (one per rank) take turns on a lock file: the later ones find the library
+    up to date."""
     if not force and not _stale(LIB, _deps()):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    import fcntl
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not _stale(LIB, _deps()):
+                return LIB
+            return _build_locked(verbose, ptxas_verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose, ptxas_verbose):
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, ptxas_verbose), srcs))
