@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(NT_NORM) draft_prologue_kernel(const PrologueP
 // ------------------------------------------------------------------------------------------------
 // Row top-k (k <= 16) by (logit desc, token asc) and the fixed-point log-normaliser at T = 1.
 // ------------------------------------------------------------------------------------------------
-constexpr int NT_TOPK = 256;
+constexpr int NT_TOPK = 256;      // threads per CTA, cluster kernel and one-wave row counts
+constexpr int NT_TOPK_NARROW = 128; // threads per CTA when the rows overflow one wave of NT_TOPK CTAs
 
 E3_DEV uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
@@ -249,17 +250,17 @@ E3_DEV float max4_nan(float4 v) {
     return r;
 }
 
-struct TopkSmem {
-    uint64_t buf[NT_TOPK / 32][TK_CAP];
-    uint64_t wres[NT_TOPK / 32][KMAX];
+template <int NT> struct TopkSmem {
+    uint64_t buf[NT / 32][TK_CAP];
+    uint64_t wres[NT / 32][KMAX];
     uint64_t fin[KMAX];
-    uint64_t sred[NT_TOPK / 32];
+    uint64_t sred[NT / 32];
     uint64_t s_cta;                 // this CTA's share of the normaliser (cluster version)
 };
 
 // Top-k candidates of the slice [lo, hi) of row z into sm.fin (sorted, KMAX entries, the first k
 // meaningful; 0 = none).
-E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
+template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int lo, int hi, int k) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
     if (lane < KMAX) sm.wres[warp][lane] = 0ull;
@@ -289,11 +290,11 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
     const bool vec = ((((uintptr_t)zs) & 15) == 0);
     const int n4 = vec ? n / 4 : 0;
     constexpr int U = 4;   // float4 loads in flight per thread
-    const int n4u = n4 / (U * NT_TOPK) * (U * NT_TOPK);   // float4 groups every lane has
-    for (int j0 = threadIdx.x; j0 < n4u; j0 += U * NT_TOPK) {
+    const int n4u = n4 / (U * NT) * (U * NT);   // float4 groups every lane has
+    for (int j0 = threadIdx.x; j0 < n4u; j0 += U * NT) {
         float4 v[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(zs) + j0 + u * NT_TOPK);
+        for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(zs) + j0 + u * NT);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             // some element is not below the threshold <=> their maximum is not (a NaN propagates, and
@@ -301,7 +302,7 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
             const bool any = !(max4_nan(v[u]) < tau_f);
             if (!__any_sync(0xffffffffu, any)) continue;
             if (cnt + 4 * 32 > TK_CAP) flush();
-            const uint32_t j = (uint32_t)lo + 4u * (uint32_t)(j0 + u * NT_TOPK);
+            const uint32_t j = (uint32_t)lo + 4u * (uint32_t)(j0 + u * NT);
             offer(v[u].x, j, true);
             offer(v[u].y, j + 1, true);
             offer(v[u].z, j + 2, true);
@@ -309,7 +310,7 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
         }
     }
     // the rest, one element per lane per round, with warp-uniform trip counts
-    for (int base = 4 * n4u; base < n; base += NT_TOPK) {
+    for (int base = 4 * n4u; base < n; base += NT) {
         const int i = base + threadIdx.x;
         const bool valid = i < n;
         const float v = valid ? __ldg(zs + i) : 0.0f;
@@ -321,7 +322,7 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
     if (warp == 0) {
         uint64_t best[KMAX], res[KMAX];
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT_TOPK / 32 ? sm.wres[lane][q] : 0ull;
+        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT / 32 ? sm.wres[lane][q] : 0ull;
         warp_merge(best, res, k);
         if (lane == 0)
 #pragma unroll
@@ -332,7 +333,7 @@ E3_DEV void topk_slice(TopkSmem &sm, const float *z, int lo, int hi, int k) {
 
 // Fixed-point normaliser terms of the slice [lo, hi) of row z with m = the row maximum: the CTA's
 // sum (valid in thread 0)
-E3_DEV uint64_t normaliser_slice(TopkSmem &sm, const float *z, int lo, int hi, float m) {
+template <int NT> E3_DEV uint64_t normaliser_slice(TopkSmem<NT> &sm, const float *z, int lo, int hi, float m) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float *zs = z + lo;
     const int n = hi - lo;
@@ -340,20 +341,20 @@ E3_DEV uint64_t normaliser_slice(TopkSmem &sm, const float *z, int lo, int hi, f
     const int n4 = vec ? n / 4 : 0;
     uint64_t s = 0;
 #pragma unroll 4
-    for (int j = threadIdx.x; j < n4; j += NT_TOPK) {
+    for (int j = threadIdx.x; j < n4; j += NT) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(zs) + j);
         // each weight is up to 2^31: widen before adding
         const uint2 w01 = dsm_weight_pair(v.x, v.y, m, 1.0f), w23 = dsm_weight_pair(v.z, v.w, m, 1.0f);
         s += ((uint64_t)w01.x + w01.y) + ((uint64_t)w23.x + w23.y);
     }
-    for (int i = 4 * n4 + threadIdx.x; i < n; i += NT_TOPK) s += dsm_weight(dsm_scaled(__ldg(zs + i), m, 1.0f));
+    for (int i = 4 * n4 + threadIdx.x; i < n; i += NT) s += dsm_weight(dsm_scaled(__ldg(zs + i), m, 1.0f));
 #pragma unroll
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) sm.sred[warp] = s;
     __syncthreads();
     uint64_t S = 0;
     if (threadIdx.x == 0)
-        for (int w = 0; w < NT_TOPK / 32; ++w) S += sm.sred[w];
+        for (int w = 0; w < NT / 32; ++w) S += sm.sred[w];
     return S;
 }
 
@@ -367,10 +368,11 @@ E3_DEV void topk_write(const uint64_t *fin, uint64_t S, float m, int row, int k,
     }
 }
 
-// One CTA per row (many rows).
-__global__ void __launch_bounds__(NT_TOPK) topk_kernel(const float *logits, int64_t ld, int V, int k,
-                                                       int32_t *out_tok, float *out_lq) {
-    __shared__ TopkSmem sm;
+// One CTA of NT threads per row (many rows).
+template <int NT>
+__global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t ld, int V, int k, int32_t *out_tok,
+                                                  float *out_lq) {
+    __shared__ TopkSmem<NT> sm;
     const int row = blockIdx.x;
     const float *z = logits + (size_t)row * ld;
     topk_slice(sm, z, 0, V, k);
@@ -389,7 +391,7 @@ __global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
     topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, int32_t *out_tok, float *out_lq) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ TopkSmem sm;
+    __shared__ TopkSmem<NT_TOPK> sm;
     __shared__ uint64_t fin_all[KMAX];
     const int rank = (int)cluster.block_rank(), row = blockIdx.x / TOPK_CL;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -967,18 +969,25 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         eagle3_linear_args_t l = lin(rows, m.V, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
                                      a->dev_status);
         E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
-        // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs
-        static int sms = 0;
+        // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs;
+        // more rows than one wave of NT_TOPK-thread CTAs holds: narrower CTAs, so that all rows are
+        // in flight at once (the scan is bound by the loads each SM keeps in flight)
+        static int sms = 0, wave = 0;
         if (!sms) {
-            int dev = 0;
+            int dev = 0, per_sm = 0;
             cudaGetDevice(&dev);
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<NT_TOPK>, NT_TOPK, 0);
+            wave = sms * (per_sm > 0 ? per_sm : 1);
         }
+        int32_t *otok = (int32_t *)P(pl.o_ttok);
+        float *olq = (float *)P(pl.o_tlq);
         if ((int64_t)rows * TOPK_CL <= 2LL * sms)
-            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok),
-                                                                    (float *)P(pl.o_tlq));
+            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, otok, olq);
+        else if (rows <= wave)
+            topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, otok, olq);
         else
-            topk_kernel<<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, (int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq));
+            topk_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, 0, st>>>(logits, m.V, m.V, K, otok, olq);
         E3_LAUNCHED();
         return EAGLE3_OK;
     };
