@@ -175,9 +175,14 @@ E3_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_sha
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be dispatched while the
 // previous kernel of its stream retires its last blocks; it runs pdl_wait() before its first
 // global memory access, which returns once that kernel has completed and its writes are visible
-// (for an ordinary launch it returns at once).
+// (for an ordinary launch it returns at once).  pdl_trigger() lets the next kernel be dispatched
+// before this one ends: its blocks take SMs as this kernel's blocks retire and run their prologue
+// there (barrier setup, TMEM allocation) up to their own pdl_wait().  The next kernel is dispatched
+// only once every block of this one has triggered or exited, so its blocks never hold resources
+// that a block of this kernel still waits for; its pdl_wait() still waits for this whole kernel.
 // ------------------------------------------------------------------------------------------------
 E3_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+E3_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

@@ -129,6 +129,7 @@ struct NormParams {
 
 __global__ void __launch_bounds__(NT_NORM) rmsnorm_kernel(const NormParams p) {
     pdl_wait();
+    pdl_trigger();
     __shared__ float red[NT_NORM / 32];
     const int r = blockIdx.x;
     int src = p.gather ? p.gather[r] : r;

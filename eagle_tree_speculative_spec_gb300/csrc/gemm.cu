@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::fence_after();
     const uint32_t tmem = *tmem_base_slot;
     pdl_wait();   // the previous kernel's outputs (this launch's inputs, or buffers it overwrites)
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -628,6 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // Split-K reduction in split order, then the epilogue.  One thread per output element pair.
 __global__ void gemm_reduce_kernel(const GemmParams p) {
     pdl_wait();
+    pdl_trigger();
     const int n_out = p.N;
     const size_t total = (size_t)p.M * n_out;
     for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {

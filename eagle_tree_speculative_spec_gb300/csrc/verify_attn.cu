@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     volatile int *abort = &ss.abort_flag;
     pdl_wait();   // the previous kernel's outputs (q / tree_k / caches) before any global access
+    pdl_trigger();
     const int half = blockIdx.x % p.halves, split = blockIdx.x / p.halves, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rep = p.rep, nk = p.q_hi, nq = p.q_hi - p.q_lo;
@@ -655,6 +656,7 @@ __global__ void __launch_bounds__(NT, 1)
 // position), with the same angle arguments and arithmetic the attention kernel uses for Q.
 __global__ void tree_rotate_kernel(const Params p) {
     pdl_wait();
+    pdl_trigger();
     const int nq = p.q_hi - p.q_lo;
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t w = t >> 3;                    // row
@@ -693,6 +695,7 @@ __global__ void tree_rotate_kernel(const Params p) {
 // Merge split partials in split order: one warp per (b, query slot, head) row.
 __global__ void verify_combine_kernel(const Params p) {
     pdl_wait();
+    pdl_trigger();
     const int nq = p.q_hi - p.q_lo;
     const int rows = p.B * nq * p.Hq;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
