@@ -626,7 +626,7 @@ def run_gpu(args):
 
 # DRAM bytes (read + write) of one SwiGLU gate+up launch at the bench shape, from the ncu capture
 # summarised in profiles/gemm_gateup_m3840.md (set it to None when the kernel changes)
-GATEUP_TRAFFIC_BYTES = 267316224 + 96963584
+GATEUP_TRAFFIC_BYTES = 267724288 + 97391360
 
 
 def _draft_launches(cfg):
