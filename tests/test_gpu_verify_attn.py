@@ -74,14 +74,51 @@ def test_verify_other_gqa_ratio():
     _check(inp, _run(inp, 130), range(2))
 
 
-@pytest.mark.parametrize("B,L", [(1, 512), (8, 4096), (64, 4096), (1, 16384)])
+def _full_size_batch(seed, B, N, Hq, Hkv, D, L, S_max, rows):
+    """A batch whose sampled rows come from the shared generator (the oracle's inputs) and whose
+    other rows are seeded N(0, 1) draws made on the device, each with its own random tree: every
+    sequence is distinct, and only the sampled ones are generated on the host."""
+    dev = require_gpu()
+    q = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
+    tk = torch.empty((B, N, Hkv, D), dtype=torch.bfloat16, device=dev)
+    tv = torch.empty_like(tk)
+    kc = torch.zeros((B, Hkv, S_max, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    parents = np.empty((B, N), np.int32)
+    host = {k: [] for k in ("q", "tree_k", "tree_v", "k_cache", "v_cache", "parents")}
+    g = torch.Generator(device=dev)
+    for b in range(B):
+        if b in rows:
+            vals = synth.verify_attn_row(seed, b, N, Hq, Hkv, D, L, S_max)
+            for name, dst, x in zip(("q", "tree_k", "tree_v", "k_cache", "v_cache"), (q, tk, tv, kc, vc), vals[:5]):
+                t, f = synth.to_bf16(x)
+                dst[b].copy_(t)
+                host[name].append(f)
+            parents[b] = vals[5]
+            host["parents"].append(vals[5])
+        else:
+            parents[b] = synth.random_tree(synth.rng(seed, b), N)
+            g.manual_seed(seed * 1000003 + b)
+            for dst in (q[b], tk[b], tv[b], kc[b, :, :L], vc[b, :, :L]):
+                dst.copy_(torch.randn(dst.shape, generator=g, device=dev))
+    sub = {k + "_f32": np.stack(v) for k, v in host.items() if k != "parents"}
+    sub["parents"] = np.stack(host["parents"])
+    sub["prefix_len"] = np.full(len(rows), L, np.int32)
+    dev_inp = dict(q=q, tree_k=tk, tree_v=tv, k_cache=kc, v_cache=vc, parents=parents,
+                   prefix_len=np.full(B, L, np.int32))
+    return dev_inp, sub
+
+
+@pytest.mark.parametrize("B", [1, 8, 64])
+@pytest.mark.parametrize("L", [512, 4096, 16384])
 def test_verify_full_size(B, L):
-    """Llama-3.1-8B shapes (32/8 heads, head_dim 128, N = 60) at the sizes of the verify workload;
-    the oracle checks sampled sequences."""
-    inp = synth.verify_attn_batch(3, B, 60, 32, 8, 128, [L] * B, S_max=L + 64)
-    got = _run(inp, L)
+    """Llama-3.1-8B shapes (32/8 heads, head_dim 128, N = 60) over the verify workload's grid of
+    batch sizes and prefix lengths (up to 64 x 16384: 8.6 GB of KV cache); the oracle checks sampled
+    sequences."""
     rows = sorted({0, B // 2, B - 1})
-    _check(inp, got, rows)
+    inp, sub = _full_size_batch(3, B, 60, 32, 8, 128, L, L + 64, rows)
+    o, lse, krot = _run(inp, L)
+    _check(sub, (o[rows], lse[rows], krot[rows]), range(len(rows)))
 
 
 def _run_rotated(inp, lens, num_splits=0):
