@@ -886,18 +886,26 @@ def run_kernel(args):
         B = c["B"]
         tc1 = torch.ones(B, dtype=torch.int32, device=dev)
         dl0 = eng.draft_len.clone()
+        # a reduced draft vocabulary: its own [Vd, d] head and the sorted target ids it covers
+        Vd = args.draft_vocab if args.draft_vocab > 0 else c["V"]
+        dw, d2t = eng.draft_w, None
+        if Vd != c["V"]:
+            cpu_g = torch.Generator().manual_seed(7)
+            dw = dict(eng.draft_w)
+            dw["lm_head"] = (torch.randn(Vd, c["d"], generator=cpu_g) * 0.02).to(torch.bfloat16).to(dev)
+            d2t = torch.randperm(c["V"], generator=cpu_g)[:Vd].sort().values.to(torch.int32).to(dev)
         a = e3._lib.draft_tree_args(eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache, eng.draft_len,
                                     eng.tokens, eng.parents, eng.depth, eng.anc, eng.score, n_heads=c["Hq"],
                                     ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                                    max_draft_len=c["L0"])
+                                    max_draft_len=c["L0"], d2t=d2t)
         ws = torch.empty(e3._lib.eagle3_draft_tree_workspace_size(a), dtype=torch.uint8, device=dev)
 
         def fn():
             eng.draft_len.copy_(dl0)
-            e3.eagle3_draft_tree(eng.draft_w, eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache,
+            e3.eagle3_draft_tree(dw, eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache,
                                  eng.draft_len, eng.tokens, eng.parents, eng.depth, eng.anc, eng.score,
                                  n_heads=c["Hq"], ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                                 max_draft_len=c["L0"], workspace=ws)
+                                 max_draft_len=c["L0"], d2t=d2t, workspace=ws)
         ms_eager = _time_loop(fn, args.steps, args.warmup)
         # the call as the step runs it: captured once into a CUDA graph and replayed (eager issue of
         # its ~70 launches from the host can take longer than the GPU work at small batches)
@@ -911,12 +919,12 @@ def run_kernel(args):
             fn()
         ms = _time_loop(graph.replay, args.steps, args.warmup)
         out.update(ms_eager=round(ms_eager, 4))
-        d, F, V, qw = c["d"], c["F"], c["V"], eng.qkv_w
+        d, F, V, qw = c["d"], c["F"], Vd, eng.qkv_w
         layer = lambda m: 2 * m * (2 * d * qw + c["Hq"] * 128 * d + 2 * d * F + F * d)
         rows_c = B * c["W"]
         flops = 2 * rows_c * 3 * d * d + layer(rows_c) + 2 * B * d * V + 5 * (layer(10 * B) + 2 * 10 * B * d * V)
         wbytes = 2 * (3 * d * d + 2 * d * qw + c["Hq"] * 128 * d + 3 * d * F + d * V)
-        out.update(batch=B, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
+        out.update(batch=B, draft_vocab=Vd, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
                    frac_tensor=round(flops / ms / 1e9 / tf_sust, 4),
                    weight_gbs_6_passes=round(6 * wbytes / ms / 1e6, 1))
     elif args.kernel == "gemm":
@@ -1015,6 +1023,8 @@ def main():
     ap.add_argument("--n", type=int, default=CFG["F"], help="--kernel gemm: output features")
     ap.add_argument("--k", type=int, default=CFG["d"], help="--kernel gemm: input features")
     ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32", "residual"])
+    ap.add_argument("--draft-vocab", type=int, default=0,
+                    help="--kernel draft: a reduced draft vocabulary of this many target ids (0 = all)")
     ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm", "tiny"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)

@@ -92,7 +92,7 @@ class DraftTreeArgs(ctypes.Structure):
                 ("tc_max", _i32), ("s_max", _i32), ("max_draft_len", _i32), ("rope_theta", _f32), ("rms_eps", _f32),
                 ("aux", _p), ("next_tokens", _p), ("tc", _p), ("draft_k_cache", _p), ("draft_v_cache", _p),
                 ("draft_len", _p), ("tokens", _p), ("parents", _p), ("depth_out", _p), ("anc_mask", _p),
-                ("score", _p), ("dbg_logits", _p), ("dev_status", _p)]
+                ("score", _p), ("dbg_logits", _p), ("dev_status", _p), ("draft_vocab", _i32), ("d2t", _p)]
 
 
 F32_EPI_NONE, F32_EPI_RESIDUAL, F32_EPI_SWIGLU = 0, 1, 2
@@ -357,7 +357,7 @@ def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, split
 
 def draft_tree_args(aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out, anc_mask, score, *,
                     n_heads, ffn, vocab, depth, top_k, max_draft_len, rope_theta=500000.0, rms_eps=1e-5,
-                    dbg_logits=None, dev_status=None):
+                    dbg_logits=None, dev_status=None, d2t=None):
     B, tc_max, d3 = aux.shape
     Hkv, S, D = k_cache.shape[1:]
     N = tokens.shape[1]
@@ -372,7 +372,8 @@ def draft_tree_args(aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, p
                          depth_out=_ptr(depth_out, i32, "depth_out"), anc_mask=_ptr(anc_mask, torch.int64, "anc_mask"),
                          score=_ptr(score, torch.float32, "score"),
                          dbg_logits=_ptr(dbg_logits, torch.float32, "dbg_logits"),
-                         dev_status=_ptr(dev_status, i32, "dev_status"))
+                         dev_status=_ptr(dev_status, i32, "dev_status"),
+                         draft_vocab=0 if d2t is None else int(d2t.numel()), d2t=_ptr(d2t, i32, "d2t"))
 
 
 def draft_weights(w):
@@ -386,13 +387,15 @@ def eagle3_draft_tree_workspace_size(args):
 
 def eagle3_draft_tree(weights, aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out,
                       anc_mask, score, *, n_heads, ffn, vocab, depth, top_k, max_draft_len, rope_theta=500000.0,
-                      rms_eps=1e-5, dbg_logits=None, dev_status=None, workspace=None, stream=None):
+                      rms_eps=1e-5, dbg_logits=None, dev_status=None, d2t=None, workspace=None, stream=None):
     """Draft head + dynamic tree.  weights: dict of bf16 tensors (see DRAFT_WEIGHT_NAMES);
     aux [B, tc_max, 3d] bf16; next_tokens [B, tc_max] / tc [B] / draft_len [B] int32; caches
-    [B, Hkv, S, D] bf16; outputs [B, N] (anc_mask int64 bit patterns of the uint64 masks)."""
+    [B, Hkv, S, D] bf16; outputs [B, N] (anc_mask int64 bit patterns of the uint64 masks).
+    d2t: optional [Vd] int32 CUDA tensor, the target ids of a reduced draft vocabulary (lm_head is
+    then [Vd, d] and dbg_logits rows have Vd entries)."""
     a = draft_tree_args(aux, next_tokens, tc, k_cache, v_cache, draft_len, tokens, parents, depth_out, anc_mask, score,
                         n_heads=n_heads, ffn=ffn, vocab=vocab, depth=depth, top_k=top_k, max_draft_len=max_draft_len,
-                        rope_theta=rope_theta, rms_eps=rms_eps, dbg_logits=dbg_logits, dev_status=dev_status)
+                        rope_theta=rope_theta, rms_eps=rms_eps, dbg_logits=dbg_logits, dev_status=dev_status, d2t=d2t)
     wts = draft_weights(weights)
     L = lib()
     need = L.eagle3_draft_tree_workspace_size(ctypes.byref(a))

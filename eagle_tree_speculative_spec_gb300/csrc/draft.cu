@@ -359,20 +359,34 @@ template <int NT> E3_DEV uint64_t normaliser_slice(TopkSmem<NT> &sm, const float
     return S;
 }
 
-E3_DEV void topk_write(const uint64_t *fin, uint64_t S, float m, int row, int k, int32_t *out_tok, float *out_lq) {
+// Output of a row's top-k: token ids (through the draft-to-target map when there is one) and logq.
+struct TopkOut {
+    int32_t *tok;
+    float *lq;
+    const int32_t *d2t;   // [V] target id of each draft id (V: the row length), or NULL
+    int v_target;         // bound of the mapped ids
+    int32_t *dev_status;
+};
+
+E3_DEV void topk_write(const uint64_t *fin, uint64_t S, float m, int row, int V, int k, const TopkOut &o) {
     if (threadIdx.x < k) {
         const float ln_s = dsm_log31(S);
         const uint64_t e = fin[threadIdx.x];
         const float zx = key_to_float((uint32_t)(e >> 32));
-        out_tok[(size_t)row * k + threadIdx.x] = (int32_t)unpack_idx(e);
-        out_lq[(size_t)row * k + threadIdx.x] = __fsub_rn(dsm_scaled(zx, m, 1.0f), ln_s);
+        const uint32_t idx = unpack_idx(e);
+        int32_t tok = (int32_t)idx;
+        if (o.d2t) {
+            tok = idx < (uint32_t)V ? __ldg(o.d2t + idx) : -1;
+            if (tok < 0 || tok >= o.v_target) flag(o.dev_status, EAGLE3_DEV_BAD_TOKEN);
+        }
+        o.tok[(size_t)row * k + threadIdx.x] = tok;
+        o.lq[(size_t)row * k + threadIdx.x] = __fsub_rn(dsm_scaled(zx, m, 1.0f), ln_s);
     }
 }
 
 // One CTA of NT threads per row (many rows).
 template <int NT>
-__global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t ld, int V, int k, int32_t *out_tok,
-                                                  float *out_lq) {
+__global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t ld, int V, int k, const TopkOut o) {
     __shared__ TopkSmem<NT> sm;
     const int row = blockIdx.x;
     const float *z = logits + (size_t)row * ld;
@@ -382,14 +396,14 @@ __global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t l
     const uint64_t s = normaliser_slice(sm, z, 0, V, m);
     if (threadIdx.x == 0) S = s;
     __syncthreads();
-    topk_write(sm.fin, S, m, row, k, out_tok, out_lq);
+    topk_write(sm.fin, S, m, row, V, k, o);
 }
 
 // A cluster of TOPK_CL CTAs per row (few rows): CTA r scans slice r, the slices' top-k lists and
 // normaliser sums are combined through distributed shared memory in rank order.
 constexpr int TOPK_CL = 8;
 __global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
-    topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, int32_t *out_tok, float *out_lq) {
+    topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, const TopkOut o) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ TopkSmem<NT_TOPK> sm;
@@ -424,7 +438,7 @@ __global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
             S = t;
         }
         __syncthreads();
-        topk_write(fin_all, S, m, row, k, out_tok, out_lq);
+        topk_write(fin_all, S, m, row, V, k, o);
     }
     cluster.sync();   // no CTA leaves while its shared memory may still be read
 }
@@ -650,7 +664,7 @@ struct Layout {
 };
 
 struct Dims {
-    int B, d, Hq, Hkv, F, V, K, depth, N, tc_max, S, max_len;
+    int B, d, Hq, Hkv, F, V, Vd, K, depth, N, tc_max, S, max_len;
     int qkv_w, Rc, Rd, R, P, maxc, lm_rows;
 };
 
@@ -662,6 +676,7 @@ Dims dims_of(const eagle3_draft_tree_args_t *a) {
     m.Hkv = a->n_kv_heads;
     m.F = a->ffn;
     m.V = a->vocab;
+    m.Vd = a->draft_vocab > 0 ? a->draft_vocab : a->vocab;
     m.K = a->top_k;
     m.depth = a->depth;
     m.N = a->n_nodes;
@@ -689,7 +704,9 @@ eagle3_status_t draft_validate(const eagle3_draft_tree_args_t *a) {
     if ((a->depth - 1) * a->top_k > MAX_SLOTS) return EAGLE3_ERR_UNSUPPORTED;
     if (a->top_k * (a->n_heads / a->n_kv_heads) > 256 || a->tc_max * (a->n_heads / a->n_kv_heads) > 256)
         return EAGLE3_ERR_UNSUPPORTED;
-    if (a->top_k > a->vocab) return EAGLE3_ERR_UNSUPPORTED;
+    if (a->draft_vocab < 0 || a->draft_vocab > a->vocab) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->draft_vocab > 0 && a->draft_vocab != a->vocab && !a->d2t) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->top_k > (a->draft_vocab > 0 ? a->draft_vocab : a->vocab)) return EAGLE3_ERR_UNSUPPORTED;
     if ((int64_t)a->max_draft_len + a->tc_max > a->s_max) return EAGLE3_ERR_CAPACITY;
     if (a->batch == 0) return EAGLE3_OK;
     if (!a->aux || !a->next_tokens || !a->tc || !a->draft_k_cache || !a->draft_v_cache || !a->draft_len ||
@@ -816,7 +833,7 @@ Plan make_plan(const Dims &m, const eagle3_draft_tree_args_t *a) {
     pl.o_act = L.add((size_t)m.R * m.F * bf);
     pl.o_abuf = L.add((size_t)(m.Rc + std::max(1, m.P) * m.B) * m.d * bf);
     pl.o_nrm = L.add((size_t)m.lm_rows * m.d * bf);
-    pl.o_logits = L.add(a->dbg_logits ? 16 : (size_t)m.lm_rows * m.V * 4);
+    pl.o_logits = L.add(a->dbg_logits ? 16 : (size_t)m.lm_rows * m.Vd * 4);
     pl.o_ttok = L.add((size_t)m.lm_rows * m.K * 4);
     pl.o_tlq = L.add((size_t)m.lm_rows * m.K * 4);
     pl.o_cs = L.add((size_t)m.B * m.maxc * 4);
@@ -836,8 +853,8 @@ Plan make_plan(const Dims &m, const eagle3_draft_tree_args_t *a) {
     size_t g = 0;
     const int shapes[][4] = {{m.Rc, m.d, 3 * m.d, EAGLE3_EPI_BF16},       {m.R, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
                              {m.R, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.R, m.F, m.d, EAGLE3_EPI_SWIGLU},
-                             {m.R, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL},   {m.B, m.V, m.d, EAGLE3_EPI_F32},
-                             {m.Rd, m.V, m.d, EAGLE3_EPI_F32},            {m.Rd, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
+                             {m.R, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL},   {m.B, m.Vd, m.d, EAGLE3_EPI_F32},
+                             {m.Rd, m.Vd, m.d, EAGLE3_EPI_F32},            {m.Rd, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
                              {m.Rd, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.Rd, m.F, m.d, EAGLE3_EPI_SWIGLU},
                              {m.Rd, m.d, m.F, EAGLE3_EPI_BF16_RESIDUAL},  {m.Rc, m.qkv_w, 2 * m.d, EAGLE3_EPI_BF16},
                              {m.Rc, m.d, m.Hq * HD, EAGLE3_EPI_BF16_RESIDUAL}, {m.Rc, m.F, m.d, EAGLE3_EPI_SWIGLU},
@@ -967,7 +984,7 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         n3.out = (__nv_bfloat16 *)P(pl.o_nrm);
         rmsnorm_kernel<<<rows, NT_NORM, 0, st>>>(n3);
         E3_LAUNCHED();
-        eagle3_linear_args_t l = lin(rows, m.V, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
+        eagle3_linear_args_t l = lin(rows, m.Vd, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
                                      a->dev_status);
         E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
         // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs;
@@ -981,14 +998,13 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<NT_TOPK>, NT_TOPK, 0);
             wave = sms * (per_sm > 0 ? per_sm : 1);
         }
-        int32_t *otok = (int32_t *)P(pl.o_ttok);
-        float *olq = (float *)P(pl.o_tlq);
+        const TopkOut o = {(int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq), a->d2t, m.V, a->dev_status};
         if ((int64_t)rows * TOPK_CL <= 2LL * sms)
-            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, otok, olq);
+            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, o);
         else if (rows <= wave)
-            topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.V, m.V, K, otok, olq);
+            topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, o);
         else
-            topk_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, 0, st>>>(logits, m.V, m.V, K, otok, olq);
+            topk_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, 0, st>>>(logits, m.Vd, m.Vd, K, o);
         E3_LAUNCHED();
         return EAGLE3_OK;
     };
@@ -1059,7 +1075,7 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         E3_TRY(tree_attn_launch(depth_attn(m, a, ws, pl, t), aws, pl.aws, st));
         __nv_bfloat16 *a_rows = abuf + (size_t)(m.Rc + (t - 2) * rows) * d;
         E3_TRY(layer_tail(rows, P(pl.o_xres), a_rows));
-        float *logits = logits_base + (a->dbg_logits ? (size_t)(t - 1) * rows * m.V : 0);
+        float *logits = logits_base + (a->dbg_logits ? (size_t)(t - 1) * rows * m.Vd : 0);
         E3_TRY(lm_head(rows, a_rows, nullptr, logits));
         select_step_kernel<<<B, 256, 0, st>>>(T, t);
         E3_LAUNCHED();

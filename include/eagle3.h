@@ -265,6 +265,15 @@ eagle3_status_t eagle3_verify_attn_noalloc(const eagle3_verify_attn_args_t *args
  * desc, creation asc) order, with creation = frontier rank * top_k + child rank.
  * Weights are bf16 [out, in]; q/k/v rows are stacked in w_qkv ((Hq + 2 Hkv) * D rows).  head_dim
  * 128; top_k <= 16; (depth - 1) * top_k <= 64; n_nodes - 1 <= top_k + (depth - 1) * top_k^2.
+ *
+ * Reduced draft vocabulary ("EAGLE-3: Engineering Implementation of LLM Inference Acceleration",
+ * sections VIII.5-VIII.6: the draft's own LM head projects onto a subset of Vd target tokens, and
+ * a draft-to-target map gives each draft id its target id): with draft_vocab = Vd > 0 and d2t set,
+ * lm_head is [Vd, d], top-k and logq run over the Vd draft logits (ties to the lower draft id) and
+ * every candidate token is d2t[draft id], a target id; d2t holds the subset's target ids in
+ * increasing order.  A mapped id outside [0, vocab) sets EAGLE3_DEV_BAD_TOKEN.  For SAMPLED
+ * acceptance, scatter the draft logits into the target vocabulary with -inf elsewhere (those
+ * tokens then have q = 0).
  * ---------------------------------------------------------------------------------------------- */
 typedef struct {
     const uint16_t *w_fc;        /* [d, 3d]                                                          */
@@ -278,7 +287,7 @@ typedef struct {
     const uint16_t *w_up;        /* [F, d]                                                           */
     const uint16_t *w_down;      /* [d, F]                                                           */
     const uint16_t *final_norm;  /* [d]                                                              */
-    const uint16_t *lm_head;     /* [V, d]                                                           */
+    const uint16_t *lm_head;     /* [V, d], or [Vd, d] with a reduced draft vocabulary               */
 } eagle3_draft_weights_t;
 
 typedef struct {
@@ -306,10 +315,12 @@ typedef struct {
     int32_t *depth_out;          /* [B, n_nodes] out                                                 */
     uint64_t *anc_mask;          /* [B, n_nodes] out: bit j set <=> node j is the node or an ancestor */
     float *score;                /* [B, n_nodes] out: cumulative logq (root 0)                       */
-    float *dbg_logits;           /* optional [depth, top_k * B, V] fp32: every draft row's logits;
+    float *dbg_logits;           /* optional [depth, top_k * B, Vd] fp32: every draft row's logits;
                                     depth 1 uses rows 0..B-1 (row b), depth t rows r * B + b for
                                     frontier rank r; may be NULL                                    */
     int32_t *dev_status;         /* optional                                                         */
+    int32_t draft_vocab;         /* Vd: rows of lm_head, 1..V; 0 = V (no reduced vocabulary)          */
+    const int32_t *d2t;          /* [Vd] target id of each draft id, or NULL (identity; Vd must be V) */
 } eagle3_draft_tree_args_t;
 
 size_t eagle3_draft_tree_workspace_size(const eagle3_draft_tree_args_t *args);

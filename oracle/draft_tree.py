@@ -29,6 +29,13 @@ row at position L-1; a frontier node at depth t-1 runs the row
 (x = a of its parent's row, e = its token) at position L-1+(t-1), attending
 to the draft cache, to its tree ancestors' rows and to itself.
 
+Reduced draft vocabulary ("EAGLE-3: Engineering Implementation of LLM
+Inference Acceleration", sections VIII.5-VIII.6): the draft's LM head covers a
+sorted subset of target tokens and ``d2t[i]`` is the target id of draft id i.
+Top-k and logq then run over the draft logits (ties to the lower draft id) and
+a candidate's token is the mapped target id; this equals expanding over the
+target vocabulary with -inf outside the subset (pinned in the tests).
+
 parity unpinned beyond invariants: the EAGLE-2 source is not on the pages.
 The invariants tested are the node count, depth bound, ancestor closure,
 frontier = top-k at each depth, final set = top N-1 over all candidates by
@@ -48,12 +55,13 @@ def topk_tokens(row, k):
     return [int(i) for i in idx[:k]]
 
 
-def select_tree(expand, depth, top_k, n_nodes, cands=None):
+def select_tree(expand, depth, top_k, n_nodes, cands=None, d2t=None):
     """Run the dynamic tree selection.
 
     expand(t, frontier) returns fp32 logits [len(frontier), V]; for t = 1 the
     frontier is [None] (the root row), otherwise a list of candidate ids at
-    depth t-1 in frontier-rank order.  ``cands`` (a list the caller may read
+    depth t-1 in frontier-rank order; with ``d2t`` the logits are over the
+    draft vocabulary and tokens are mapped to target ids.  ``cands`` (a list the caller may read
     from inside expand) receives the candidate table: dicts with token, score,
     depth, creation, parent (candidate id, -1 for the root).  Returns tokens,
     parents, depth, score per emitted node (node 0 = root, token -1 here), the
@@ -67,7 +75,8 @@ def select_tree(expand, depth, top_k, n_nodes, cands=None):
             lq = dsm.logq(logits[r])
             for c, tok in enumerate(topk_tokens(logits[r], top_k)):
                 score = lq[tok] if f is None else np.float32(cands[f]["score"] + lq[tok])
-                cands.append({"token": tok, "score": np.float32(score), "depth": t,
+                tgt = tok if d2t is None else int(d2t[tok])
+                cands.append({"token": tgt, "score": np.float32(score), "depth": t,
                               "creation": r * top_k + c, "parent": -1 if f is None else f})
         frontiers.append(front)
         if t < depth:
@@ -94,7 +103,7 @@ def select_tree(expand, depth, top_k, n_nodes, cands=None):
 
 
 def draft_tree_for_sequence(draft, d_cache, a_root, root_token, L, depth, top_k, n_nodes,
-                            logits_log=None, select_logits=None):
+                            logits_log=None, select_logits=None, d2t=None):
     """Build the tree for one sequence with the oracle draft model.
 
     d_cache holds draft K/V for positions 0..L-1; a_root is the last catch-up
@@ -134,6 +143,6 @@ def draft_tree_for_sequence(draft, d_cache, a_root, root_token, L, depth, top_k,
             logits_log.append(out)
         return out if select_logits is None else np.asarray(select_logits(t, front), dtype=np.float32)
 
-    res = select_tree(expand, depth, top_k, n_nodes, cands)
+    res = select_tree(expand, depth, top_k, n_nodes, cands, d2t)
     res["tokens"][0] = root_token
     return res

@@ -116,3 +116,29 @@ def test_linear_rope_host_validation(kw, want):
     L = built_lib()
     a = _linear(**kw)
     assert L.eagle3_linear(ctypes.byref(a), None, 0, None) == want
+
+
+def _draft(**kw):
+    base = dict(batch=2, hidden=256, n_heads=4, n_kv_heads=2, head_dim=128, ffn=512, vocab=1000, depth=4, top_k=4,
+                n_nodes=12, tc_max=2, s_max=64, max_draft_len=32, rope_theta=500000.0, rms_eps=1e-5, aux=16,
+                next_tokens=16, tc=16, draft_k_cache=16, draft_v_cache=16, draft_len=16, tokens=16, parents=16,
+                depth_out=16, anc_mask=16, score=16, dbg_logits=None, dev_status=None, draft_vocab=0, d2t=None)
+    base.update(kw)
+    return B.DraftTreeArgs(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(batch=0), 0),
+    (dict(batch=0, draft_vocab=300, d2t=16), 0),
+    (dict(draft_vocab=-1), 1),
+    (dict(draft_vocab=1001, d2t=16), 1),      # larger than the target vocabulary
+    (dict(draft_vocab=300), 1),               # a reduced vocabulary needs its map
+    (dict(draft_vocab=3, d2t=16), 2),         # top_k above the draft vocabulary
+    (dict(head_dim=64), 2),
+    (dict(max_draft_len=63), 3),              # max_draft_len + tc_max > s_max
+    (dict(tokens=None), 1),
+])
+def test_draft_tree_host_validation(kw, want):
+    L = built_lib()
+    a = _draft(**kw)
+    assert L.eagle3_draft_tree(None, ctypes.byref(a), None, 0, None) == want

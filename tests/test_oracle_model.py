@@ -204,3 +204,33 @@ def test_dynamic_tree_invariants(depth, top_k, n_nodes):
 def test_top1_tree_is_a_chain():
     res = draft_tree.select_tree(_random_expand(5, 100), 4, 1, 5)
     assert res["parents"].tolist() == [-1, 0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("depth,top_k,n_nodes", [(6, 10, 60), (4, 3, 16)])
+def test_reduced_vocab_equals_target_vocab_with_masked_tokens(depth, top_k, n_nodes):
+    """A reduced draft vocabulary (sorted target ids d2t, "EAGLE-3: Engineering Implementation of
+    LLM Inference Acceleration", sections VIII.5-VIII.6) is the same tree as the target-vocabulary
+    draft whose logits are -inf outside the subset: the scattered draft distribution."""
+    V, Vd = 300, 80
+    d2t = np.sort(np.random.default_rng(9).choice(V, Vd, replace=False))
+    reduced = draft_tree.select_tree(_random_expand(21, Vd), depth, top_k, n_nodes, d2t=d2t)
+    draft_rows = _random_expand(21, Vd)
+
+    def expand_full(t, front):
+        z = np.full((len(front), V), -np.inf, np.float32)
+        z[:, d2t] = draft_rows(t, front)
+        return z
+
+    full = draft_tree.select_tree(expand_full, depth, top_k, n_nodes)
+    for key in ("tokens", "parents", "depth"):
+        assert (reduced[key] == full[key]).all(), key
+    assert np.array_equal(reduced["score"].view(np.uint32), full["score"].view(np.uint32))
+    assert set(reduced["tokens"][1:].tolist()) <= set(d2t.tolist())
+
+
+def test_identity_map_is_the_plain_tree():
+    V = 200
+    plain = draft_tree.select_tree(_random_expand(22, V), 4, 4, 12)
+    mapped = draft_tree.select_tree(_random_expand(22, V), 4, 4, 12, d2t=np.arange(V))
+    for key in ("tokens", "parents", "depth", "score"):
+        assert np.array_equal(plain[key], mapped[key]), key
