@@ -142,3 +142,13 @@ def test_draft_tree_host_validation(kw, want):
     L = built_lib()
     a = _draft(**kw)
     assert L.eagle3_draft_tree(None, ctypes.byref(a), None, 0, None) == want
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no fallback implementation."""
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libeagle3.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        B.lib()
+    with pytest.raises(RuntimeError):
+        B.eagle3_draft_tree_workspace_size(_draft())
