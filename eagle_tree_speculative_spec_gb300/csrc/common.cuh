@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/eagle3.h"
 
 #define E3_DEV __device__ __forceinline__
@@ -183,6 +185,39 @@ E3_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_sha
 // ------------------------------------------------------------------------------------------------
 E3_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 E3_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Host-side value computed once per device (for the device current at the call) and kept:
+// kernel attributes and device attribute queries.  Safe for concurrent callers.
+template <typename T>
+struct PerDevice {
+    static constexpr int MAX_DEVICES = 128;
+    std::mutex mu;
+    bool done[MAX_DEVICES] = {};
+    T val[MAX_DEVICES] = {};
+    template <typename F>
+    T get(F f) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return f();
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            val[dev] = f();
+            done[dev] = true;
+        }
+        return val[dev];
+    }
+};
+
+// SMs of the current device, 0 when it cannot be queried (no device)
+inline int device_sm_count() {
+    static PerDevice<int> cache;
+    return cache.get([] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess)
+            n = 0;
+        return n > 0 ? n : 0;
+    });
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

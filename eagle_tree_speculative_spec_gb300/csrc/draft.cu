@@ -990,14 +990,15 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs;
         // more rows than one wave of NT_TOPK-thread CTAs holds: narrower CTAs, so that all rows are
         // in flight at once (the scan is bound by the loads each SM keeps in flight)
-        static int sms = 0, wave = 0;
-        if (!sms) {
-            int dev = 0, per_sm = 0;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<NT_TOPK>, NT_TOPK, 0);
-            wave = sms * (per_sm > 0 ? per_sm : 1);
-        }
+        const int sms = device_sm_count();
+        static PerDevice<int> topk_per_sm;
+        const int per_sm = topk_per_sm.get([] {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_kernel<NT_TOPK>, NT_TOPK, 0) != cudaSuccess)
+                n = 0;
+            return n > 0 ? n : 1;
+        });
+        const int wave = sms * per_sm;
         const TopkOut o = {(int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq), a->d2t, m.V, a->dev_status};
         if ((int64_t)rows * TOPK_CL <= 2LL * sms)
             topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, o);

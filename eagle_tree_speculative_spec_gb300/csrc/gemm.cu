@@ -662,15 +662,15 @@ __global__ void gemm_reduce_kernel(const GemmParams p) {
 
 // ---- host side ----------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         cudaDriverEntryPointQueryResult q;
         void *ptr = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }
+            return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    }();
     return fn;
 }
 
@@ -702,14 +702,8 @@ bool make_out_map(CUtensorMap *m, void *base, int rows, int cols, int64_t ld_ele
 }
 
 int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
+    const int n = device_sm_count();
+    return n > 0 ? n : 148;   // no device (workspace sizing on a host without one): a typical count
 }
 
 struct Plan {
@@ -861,15 +855,16 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     if (p.rope_cols && !p.tma_out) return EAGLE3_ERR_UNSUPPORTED;
 
     using C = Cfg<256>;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(gemm_tc_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-                cudaSuccess)
-            return EAGLE3_ERR_CUDA;
-        attr = true;
-    }
+    static PerDevice<cudaError_t> attr;
+    if (attr.get([] {
+            cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<256, false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemm_tc_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+            return e;
+        }) != cudaSuccess)
+        return EAGLE3_ERR_CUDA;
     if (pl.streamk) {
         // flags start at zero; blocks wait on one another, so all of them must be resident
         if (cudaMemsetAsync(p.sk_flag, 0, (size_t)pl.grid * sizeof(int), (cudaStream_t)stream) != cudaSuccess)

@@ -725,15 +725,15 @@ __global__ void verify_combine_kernel(const Params p) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         cudaDriverEntryPointQueryResult q;
         void *ptr = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }
+            return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    }();
     return fn;
 }
 
@@ -796,14 +796,8 @@ int plan_splits(int ctas, int max_prefix, int requested, int sm_count) {
 }
 
 int sm_count_cached() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
-    }
-    return n;
+    const int n = device_sm_count();
+    return n > 0 ? n : 1;
 }
 
 // Query rows of a (sequence, KV head): one 128-row M tile per CTA; more rows are cut into two
@@ -955,13 +949,12 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
     const void *row_bases[] = {a.q, a.k, a.v, a.out};
     for (const void *r : row_bases)
         if ((uintptr_t)r & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_DYN) !=
-            cudaSuccess)
-            return EAGLE3_ERR_CUDA;
-        attr_done = true;
-    }
+    static PerDevice<cudaError_t> attr;
+    if (attr.get([] {
+            return cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)SMEM_DYN);
+        }) != cudaSuccess)
+        return EAGLE3_ERR_CUDA;
     Part parts[2];
     const int n = plan_parts(a, parts);
     for (int i = 0; i < n; ++i) {
