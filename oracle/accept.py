@@ -38,7 +38,7 @@ in rational arithmetic on a tiny vocabulary, a chi-square test over many
 Philox seeds, the closed form (1 - a**(k+1)) / (1 - a) of the expected
 tokens per step for a chain, and the section III.5 worked example
 (tests/test_oracle_accept.py).  The greedy walk is pinned by greedy
-speculative decoding matching vanilla greedy decoding (tests/test_oracle_llama.py).
+speculative decoding matching vanilla greedy decoding (tests/test_oracle_model.py).
 """
 import numpy as np
 

@@ -23,8 +23,9 @@ Pinned by: a chain tree reduces to ordinary causal attention over
 prefix + chain (textbook attention written with a dense causal mask), each
 node's output equals attention over prefix + its own root-to-node path
 computed as a separate sequence (the invariant the tree-drafts page checks to
-1.5e-05), and RoPE preserving norms and relative-position invariance
-(tests/test_oracle_attention.py).
+1.5e-05), RoPE preserving norms and relative-position invariance, and RoPE
+equal to the complex rotation of the half-split pairs with inv_j = theta**(-2j/D)
+(tests/test_oracle_model.py).
 """
 import math
 

@@ -15,7 +15,7 @@ the new prefix length is L + n + 1.  Optional aux rows (the target hidden
 states the next draft catch-up consumes) are gathered in path order.
 
 Pinned by: the compacted cache equals the cache that appending the path's
-tokens one position at a time would build (tests/test_oracle_compact.py).
+tokens one position at a time would build (tests/test_oracle_basics.py).
 """
 import numpy as np
 

@@ -29,7 +29,7 @@ multiply-add).
 
 Pinned by: EXP against math.exp (relative error bound), LOG31 against
 math.log, and p against the fp64 softmax (|p - softmax| <= V * 2**-31 + eps);
-see tests/test_oracle_dsm.py.
+see tests/test_oracle_basics.py.
 """
 import math
 

@@ -26,7 +26,8 @@ explicit key list in position order), so a row's values do not depend on which
 other rows share the call.  That makes greedy speculative decoding produce
 exactly the vanilla greedy tokens, the losslessness check that "EAGLE-3:
 Engineering Implementation of LLM Inference Acceleration" section XI.6 and the
-tree-drafts page run.  Pinned by that equality (tests/test_oracle_llama.py).
+tree-drafts page run.  Pinned by that equality, and RMSNorm and SiLU by
+torch.nn.functional.rms_norm and silu (tests/test_oracle_model.py).
 """
 import math
 

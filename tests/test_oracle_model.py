@@ -26,6 +26,32 @@ def test_rope_preserves_norm_and_is_relative():
     assert np.allclose(att.rope_apply(q, [0]), q)
 
 
+def test_rope_is_the_complex_rotation_of_half_split_pairs():
+    """Rotate-half RoPE is the complex rotation z_j * exp(i * pos * inv_j) of z_j = x_j + i x_{j+D/2},
+    with inv_j = theta^(-2j/D): the pairing and the frequencies, which the invariants above do not
+    fix (an interleaved pairing or another frequency law keeps norms and relative positions)."""
+    assert att.rope_inv(4, 10000.0).tolist() == [1.0, np.float32(0.01)]
+    r = np.random.default_rng(3)
+    D, T = 128, 5
+    x = r.standard_normal((T, 2, D))
+    pos = np.array([0, 1, 17, 2048, 131071])
+    got = att.rope_apply(x, pos)
+    ang = pos[:, None].astype(np.float32) * att.rope_inv(D)[None, :]          # fp32 angles
+    z = (x[..., : D // 2] + 1j * x[..., D // 2:]) * np.exp(1j * ang.astype(np.float64))[:, None, :]
+    ref = np.concatenate([z.real, z.imag], -1)
+    assert np.abs(got - ref).max() < 1e-12
+
+
+def test_rmsnorm_and_silu_match_torch():
+    torch = pytest.importorskip("torch")
+    r = np.random.default_rng(4)
+    x, w = r.standard_normal((7, 96)), r.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (96,), torch.from_numpy(w), 1e-5).numpy()
+    assert np.abs(llama.rmsnorm(x, w, 1e-5) - ref).max() < 1e-12
+    y = 6.0 * r.standard_normal(1000)
+    assert np.abs(llama.silu(y) - torch.nn.functional.silu(torch.from_numpy(y)).numpy()).max() < 1e-12
+
+
 def _inputs(seed, N, L, Hq=4, Hkv=2, D=16, parents=None):
     r = np.random.default_rng(seed)
     q = r.standard_normal((1, N, Hq, D))
