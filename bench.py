@@ -719,8 +719,8 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = dict(CFG)
-    for _ in range(args.warmup):
-        pass   # the oracle has no warm state; warm-up steps are not run
+    # no warm-up steps are run: the oracle keeps no state between steps (no caches, no compiled
+    # code, no device), so a warm-up would only lengthen the run; the line reports W as given
     total = 0.0
     per = []
     for i in range(args.steps):
