@@ -11,8 +11,10 @@ and 0 <= parents[i] < i (topological order), N <= 64, so the visibility row
 of node i fits a 64-bit word: bit j set <=> node j is i or an ancestor of i.
 
 Pinned by: the 6x6 mask the page prints for parents [-1, 0, 0, 1, 1, 2]
-(tests/golden/tree_mask_6.txt) and by agreement between the brute-force
-ancestor walk and the bitmask recurrence on random trees.
+(tests/golden/tree_mask_6.txt), by agreement between the brute-force
+ancestor walk and the bitmask recurrence on random trees, and, for
+``static_tree``, by the node counts the page's exercise 1 answers (14 and 30
+draft nodes for branching [2, 2, 1, 1] and [3, 3, 2]).
 """
 import numpy as np
 
@@ -29,6 +31,21 @@ def validate(parents):
     for i in range(1, len(p)):
         if not 0 <= p[i] < i:
             raise ValueError(f"parent of node {i} must be in [0, {i})")
+
+
+def static_tree(branching):
+    """Parent array of a static tree: every node at depth t - 1 has branching[t - 1] children
+    ("Advanced speculative decoding: tree drafts and EAGLE", section "Exercises", exercise 1).
+    Nodes are numbered depth by depth; node 0 is the root."""
+    parents, level = [-1], [0]
+    for b in branching:
+        nxt = []
+        for par in level:
+            for _ in range(int(b)):
+                nxt.append(len(parents))
+                parents.append(par)
+        level = nxt
+    return np.asarray(parents, dtype=np.int32)
 
 
 def depths(parents):

@@ -173,3 +173,18 @@ def test_compaction_equals_sequential_append():
         assert (slot[b, alen[b] + 1:] == -1).all()
         assert (aux_out[b, : alen[b] + 1] == aux[b, paths[b, : alen[b] + 1]]).all()
         assert (v2[:, b, :, L[b]: L[b] + alen[b] + 1] == np.moveaxis(tv[:, b, paths[b, : alen[b] + 1]], 1, 2)).all()
+
+
+@pytest.mark.parametrize("branching,n_draft", [([2, 2, 1, 1], 14), ([3, 3, 2], 30)])
+def test_static_tree_node_counts(branching, n_draft):
+    """"Advanced speculative decoding: tree drafts and EAGLE", "Exercises", exercise 1 and its
+    answer: 2 + 4 + 4 + 4 = 14 and 3 + 9 + 18 = 30 draft nodes besides the root."""
+    parents = tree.static_tree(branching)
+    tree.validate(parents)
+    assert len(parents) - 1 == n_draft
+    d = tree.depths(parents)
+    width = 1
+    for t, b in enumerate(branching, start=1):
+        width *= b
+        assert int((d == t).sum()) == width
+        assert all(int((parents[d == t] == p).sum()) == b for p in np.flatnonzero(d == t - 1))
