@@ -188,3 +188,31 @@ def test_static_tree_node_counts(branching, n_draft):
         width *= b
         assert int((d == t).sum()) == width
         assert all(int((parents[d == t] == p).sum()) == b for p in np.flatnonzero(d == t - 1))
+
+
+def test_spec_decode_metadata_worked_example(golden_dir):
+    from oracle import ragged
+    fields = {}
+    for line in open(os.path.join(golden_dir, "spec_decode_metadata_5req.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, v = line.split(":")
+        fields[k.strip()] = [int(x) for x in v.split()]
+    got = ragged.spec_decode_metadata(fields["cu_num_scheduled_tokens"], fields["num_draft_tokens"])
+    for k in ("cu_num_draft_tokens", "logits_indices", "target_logits_indices", "bonus_logits_indices"):
+        assert got[k].tolist() == fields[k], k
+
+
+def test_spec_decode_metadata_invariants():
+    from oracle import ragged
+    r = np.random.default_rng(5)
+    d = r.integers(0, 8, 40)
+    sched = d + 1 + r.integers(0, 50, 40)
+    got = ragged.spec_decode_metadata(np.cumsum(sched), d)
+    n_rows = int((d + 1).sum())
+    assert len(got["logits_indices"]) == n_rows
+    rows = np.sort(np.concatenate([got["target_logits_indices"], got["bonus_logits_indices"]]))
+    assert rows.tolist() == list(range(n_rows))          # every logits row is a target or a bonus row
+    assert (np.diff(got["logits_indices"]) > 0).all()
+    with pytest.raises(ValueError):
+        ragged.spec_decode_metadata([2, 3], [2, 0])       # 2 scheduled tokens cannot carry 2 drafts + 1
