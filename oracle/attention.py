@@ -123,3 +123,37 @@ def causal_attention(q, k, v, scale):
     s = s - s.max(-1, keepdims=True)
     e = np.exp(s)
     return (e / e.sum(-1, keepdims=True)) @ v
+
+
+def ttt_attention(q, ks, vs, scale):
+    """Training-time-test attention of one simulated step (NEXT-3's kernel; no device side yet).
+
+    Source: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", sections VII.5
+    (Figure 6's mask: the query at position i attends to the native keys up to i and, of every
+    simulated step, to the key at position i alone) and VIII (``forward_ttt``).
+    q [T, Hq, D]; ks / vs: lists of [T, Hkv, D], entry 0 the native step's keys (causal), entry
+    t >= 1 simulated step t's keys, of which the query at position i sees only position i.
+    Written as the definition: attention over all steps' keys concatenated, with that mask built
+    explicitly.  Returns [T, Hq, D] fp64.
+
+    Pinned by: with no simulated step it is textbook causal attention, and it equals the
+    per-position dot-product form the page uses (the page measures 1.19e-7 in fp32)."""
+    q = np.asarray(q, dtype=np.float64)
+    T, Hq, D = q.shape
+    Hkv = ks[0].shape[1]
+    S = len(ks)
+    mask = np.zeros((T, S * T), dtype=bool)
+    mask[:, :T] = np.tril(np.ones((T, T), dtype=bool))
+    for t in range(1, S):
+        mask[np.arange(T), t * T + np.arange(T)] = True
+    K = np.concatenate([np.asarray(k, dtype=np.float64) for k in ks], 0)      # [S*T, Hkv, D]
+    V = np.concatenate([np.asarray(v, dtype=np.float64) for v in vs], 0)
+    out = np.empty((T, Hq, D))
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        s = (q[:, h] @ K[:, g].T) * scale
+        s = np.where(mask, s, -np.inf)
+        s = s - s.max(-1, keepdims=True)
+        e = np.exp(s)
+        out[:, h] = (e / e.sum(-1, keepdims=True)) @ V[:, g]
+    return out

@@ -260,3 +260,36 @@ def test_identity_map_is_the_plain_tree():
     mapped = draft_tree.select_tree(_random_expand(22, V), 4, 4, 12, d2t=np.arange(V))
     for key in ("tokens", "parents", "depth", "score"):
         assert np.array_equal(plain[key], mapped[key]), key
+
+
+def test_ttt_attention_without_simulated_steps_is_causal():
+    r = np.random.default_rng(6)
+    T, Hq, Hkv, D = 9, 4, 2, 16
+    q, k, v = r.standard_normal((T, Hq, D)), r.standard_normal((T, Hkv, D)), r.standard_normal((T, Hkv, D))
+    got = att.ttt_attention(q, [k], [v], 0.25)
+    for h in range(Hq):
+        ref = att.causal_attention(q[:, h], k[:, h // 2], v[:, h // 2], 0.25)
+        assert np.abs(got[:, h] - ref).max() < 1e-12
+
+
+def test_ttt_attention_equals_the_diagonal_dot_product_form():
+    """The page's check of its forward_ttt ("EAGLE-3: Engineering Implementation of LLM Inference
+    Acceleration", section VIII): causal scores against the native keys plus one dot product per
+    simulated step at the query's own position, softmax over both."""
+    r = np.random.default_rng(7)
+    T, Hq, Hkv, D, S = 11, 4, 2, 16, 4
+    q = r.standard_normal((T, Hq, D))
+    ks = [r.standard_normal((T, Hkv, D)) for _ in range(S)]
+    vs = [r.standard_normal((T, Hkv, D)) for _ in range(S)]
+    scale = 1 / math.sqrt(D)
+    got = att.ttt_attention(q, ks, vs, scale)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        for i in range(T):
+            s0 = [float(q[i, h] @ ks[0][j, g]) * scale for j in range(i + 1)]
+            sd = [float(q[i, h] @ ks[t][i, g]) * scale for t in range(1, S)]
+            w = np.exp(np.array(s0 + sd) - max(s0 + sd))
+            w /= w.sum()
+            ref = sum(w[j] * vs[0][j, g] for j in range(i + 1))
+            ref = ref + sum(w[i + t] * vs[t][i, g] for t in range(1, S))
+            assert np.abs(got[i, h] - ref).max() < 1e-12
