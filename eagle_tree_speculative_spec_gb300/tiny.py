@@ -196,19 +196,20 @@ def speculative_greedy(target, draft, prompt, max_new, k_draft=4):
     P = len(prompt)
     logits, aux, tk, tv = target.forward(prompt, list(range(P)), chain_visible(P), 0)
     target.cache.commit(tk, tv, list(range(P)), P)
-    ids = list(prompt)
-    pending = _argmax(logits[P - 1])
-    new_g = draft.fuse(aux)
-    d_len, accepted = 0, []
+    committed = list(prompt)
+    root = _argmax(logits[P - 1])
+    fresh_g = draft.fuse(aux)
+    drafted, per_cycle = 0, []
     N = k_draft + 1
     parents = _t([-1] + list(range(k_draft)), dev, torch.int32).view(1, N)
-    while len(ids) - P < max_new:
-        n = len(ids)
-        # catch-up: positions d_len..n-1 get (g_i, e_{t_{i+1}}), appended to the draft cache
-        nxt = ids[d_len + 1:] + [pending]
-        a, dk, dv = draft.layer(nxt, new_g, list(range(d_len, n)), chain_visible(len(nxt)), d_len)
-        draft.cache.commit(dk, dv, list(range(len(nxt))), len(nxt))
-        d_len = n
+    while len(committed) - P < max_new:
+        n = len(committed)
+        # catch-up: each committed position the draft cache lacks (drafted .. n-1) runs once, with
+        # its fused target feature and the embedding of the token after it (the root for the last)
+        cu_tokens = committed[drafted + 1:] + [root]
+        a, dk, dv = draft.layer(cu_tokens, fresh_g, list(range(drafted, n)), chain_visible(len(cu_tokens)), drafted)
+        draft.cache.commit(dk, dv, list(range(len(cu_tokens))), len(cu_tokens))
+        drafted = n
         # chain draft: depth 1 from the last catch-up row; each later depth one row at position
         # n + depth - 2 over the draft cache and the chain rows before it (kept in the cache slots
         # after n, which the next catch-up overwrites)
@@ -219,9 +220,9 @@ def speculative_greedy(target, draft, prompt, max_new, k_draft=4):
             draft.cache.commit(rk, rv, [0], 1)
             chain.append(_argmax(draft.logits(row_a)[0]))
             a_prev = row_a
-        draft.cache.length.copy_(torch.tensor([d_len], dtype=torch.int32))   # drop the chain rows
-        # verify the chain [pending] + chain at positions n + depth
-        tokens = [pending] + chain
+        draft.cache.length.copy_(torch.tensor([drafted], dtype=torch.int32))   # drop the chain rows
+        # verify [root] + chain at positions n + depth
+        tokens = [root] + chain
         logits, aux, tk, tv = target.forward(tokens, list(range(n, n + N)), chain_visible(N), n)
         tok_d = _t(tokens, dev, torch.int32).view(1, N)
         alen = torch.empty(1, dtype=torch.int32, device=dev)
@@ -232,8 +233,8 @@ def speculative_greedy(target, draft, prompt, max_new, k_draft=4):
         n_acc = int(alen.item())
         path_h = [int(v) for v in path[0, :n_acc + 1].tolist()]
         aux_rows = target.cache.commit(tk, tv, path_h, N, aux=aux)
-        ids += [tokens[c] for c in path_h]
-        pending = int(nroot.item())
-        new_g = draft.fuse(aux_rows)
-        accepted.append(n_acc)
-    return ids[P:P + max_new], accepted
+        committed += [tokens[c] for c in path_h]
+        root = int(nroot.item())
+        fresh_g = draft.fuse(aux_rows)
+        per_cycle.append(n_acc)
+    return committed[P:P + max_new], per_cycle

@@ -20,9 +20,9 @@
  *
  * Tree conventions (all entry points): a draft tree of N <= 64 nodes is a
  * parent array `parents[N]` with parents[0] = -1 (node 0 is the root, the
- * token the target produced last step) and 0 <= parents[i] < i.  Node i sees
- * the cached prefix, its ancestors and itself; its position is
- * prefix_len + depth(i).
+ * token the target produced last step) and 0 <= parents[i] < i.  Node i
+ * attends to every cached prefix position, to the nodes on its path from the
+ * root and to itself, and sits at position prefix_len + depth(i).
  */
 #ifndef EAGLE3_H
 #define EAGLE3_H
@@ -62,9 +62,9 @@ int eagle3_version(void);
  * eagle3_accept - lossless acceptance of a verified draft tree.
  *
  * Defines: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration", sections III.5
- * and X.3-X.6 (accept a drafted token x with probability min(1, p(x)/q(x)); on rejection resample
- * from norm(max(0, p - q)); if every draft is accepted draw a bonus token from the last target
- * distribution), "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation"
+ * and X.3-X.6 (a drafted token x survives when a uniform draw falls below p(x)/q(x), capped at 1;
+ * after a rejection the replacement comes from max(0, p - q) renormalised; when every draft
+ * survives, one extra token comes from the last target distribution), "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation"
  * (greedy walk: follow the child whose token equals the target argmax) and exercise 2 (multiple
  * candidates per node: try the children in turn, replacing p by the residual after each
  * rejection), and "Speculative Decoding (EAGLE3) in the vLLM Neuron Framework", section
@@ -125,8 +125,8 @@ eagle3_status_t eagle3_accept(const eagle3_accept_args_t *args, void *workspace,
  * eagle3_compact_kv - copy the accepted path's K/V into contiguous cache slots.
  *
  * Defines: "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation" (the
- * path's K/V were computed during verification at the right positions; append them to the cache
- * without recomputation, drop the rejected nodes) and "EAGLE-3: Engineering Implementation of LLM
+ * verify pass already produced the path nodes' K/V at their final positions, so they are copied
+ * into the cache instead of recomputed, and the other nodes are discarded) and "EAGLE-3: Engineering Implementation of LLM
  * Inference Acceleration", section XI.4 (the target cache keeps exactly the committed positions).
  *
  * For each sequence b with L = prefix_len[b] and n = accept_len[b]: for j = 0..n, every layer and

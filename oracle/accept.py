@@ -2,10 +2,11 @@
 
 Sources:
 * "EAGLE-3: Engineering Implementation of LLM Inference Acceleration",
-  section III.5 and sections X.3-X.6: accept draft token x with probability
-  min(1, p(x) / q(x)) front to back; on the first rejection resample from
-  norm(max(0, p - q)) and drop the rest; if everything is accepted, draw one
-  bonus token from the last target distribution.  At temperature 0 the rule
+  section III.5 and sections X.3-X.6: drafts are tested in order, each kept
+  when a uniform draw falls below p(x) / q(x) (capped at 1); the first
+  rejection ends the walk with a replacement drawn from max(0, p - q)
+  renormalised; when all drafts are kept, one more token is drawn from the
+  last target distribution.  At temperature 0 the rule
   reduces to "accept iff the draft equals the target argmax" (section I).
 * "Advanced speculative decoding: tree drafts and EAGLE", section
   "Implementation" (greedy tree walk: from the root, follow the child whose

@@ -48,14 +48,16 @@ def rope_angles(pos, D, theta=ROPE_THETA):
 
 
 def rope_apply(x, pos, theta=ROPE_THETA):
-    """Rotate-half RoPE.  x: [T, H, D] (any float dtype), pos: [T] -> fp64."""
+    """Rotate-half RoPE.  x: [T, H, D] (any float dtype), pos: [T] -> fp64.
+
+    Element j of the first half and element j of the second half form a pair that is rotated
+    by the angle pos * inv_j."""
     x = np.asarray(x, dtype=np.float64)
-    D = x.shape[-1]
-    ang = rope_angles(pos, D, theta).astype(np.float64)          # [T, D/2]
-    cos = np.concatenate([np.cos(ang), np.cos(ang)], -1)[:, None, :]
-    sin = np.concatenate([np.sin(ang), np.sin(ang)], -1)[:, None, :]
-    x1, x2 = x[..., : D // 2], x[..., D // 2:]
-    return x * cos + np.concatenate([-x2, x1], -1) * sin
+    half = x.shape[-1] // 2
+    ang = rope_angles(pos, 2 * half, theta).astype(np.float64)[:, None, :]    # [T, 1, D/2]
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
 
 
 def attend(q, keys, values, scale):

@@ -1,10 +1,10 @@
 """Compaction of the accepted path's K/V into contiguous cache slots.
 
 Source: "Advanced speculative decoding: tree drafts and EAGLE", section
-"Implementation" (``cache.update(layer, k[:, :, path], v[:, :, path])``: the
-K/V of the nodes on the accepted path were computed during verification at the
-right positions, so they are appended to the cache with no recomputation; the
-rejected nodes are dropped) and "EAGLE-3: Engineering Implementation of LLM
+"Implementation" (the cache update after acceptance: the verify pass already
+produced the K/V of the accepted path's nodes at their final positions, so
+those rows are copied into the cache rather than recomputed, and every other
+node is discarded) and "EAGLE-3: Engineering Implementation of LLM
 Inference Acceleration", section XI.4 (the target cache keeps exactly the
 committed positions).
 

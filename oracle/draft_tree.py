@@ -3,7 +3,7 @@
 Sources: "EAGLE-3: Engineering Implementation of LLM Inference Acceleration",
 sections IV.3 and XI.6 (EAGLE-2's dynamic tree: acceptance is estimated from
 draft confidence, the tree is expanded and pruned at the end of drafting; the
-official engine's budget is total_token = 60, depth = 7, top_k = 10),
+official engine defaults to 60 nodes, depth 7 and top-k 10),
 "EAGLE-3: Training-Time Test for Speculative Decoding", section "Dynamic Draft
 Trees Spend Verification Where It Can Pay Off", and "Advanced speculative
 decoding: tree drafts and EAGLE" (``build_draft_tree``: each node's children

@@ -197,37 +197,39 @@ def vanilla_greedy(target, prompt, max_new):
 def speculative_greedy(target, draft, prompt, max_new, build_tree):
     """EAGLE-3 greedy speculative decoding for one sequence.
 
-    ``build_tree(draft_step, a_last, pending, L)`` returns (tokens, parents) of the
-    draft tree with the pending token as node 0; ``draft_step(rows)`` runs draft
+    ``build_tree(draft_step, a_last, root, L)`` returns (tokens, parents) of the
+    draft tree with the root token (the target's last output) as node 0; ``draft_step(rows)`` runs draft
     rows for tree nodes (see :func:`oracle.draft_tree.draft_tree_for_sequence`).
     Returns (generated tokens, accepted drafts per cycle)."""
     P = len(prompt)
     t_cache, d_cache = target.new_cache(), KV(1)
     logits, aux, nk, nv = target.forward(prompt, np.arange(P), t_cache, chain_visible(P))
     target.commit(t_cache, nk, nv, list(range(P)))
-    ids = list(prompt)
-    pending = argmax(logits[-1].astype(np.float32))
-    new_g = draft.fuse(aux)
-    d_len, accepted = 0, []
-    while len(ids) - P < max_new:
-        n = len(ids)
-        # 1) catch-up: positions d_len..n-1 get (g_i, e_{t_{i+1}})
-        nxt = ids[d_len + 1:] + [pending]
-        a, dk, dv = draft.layer(nxt, new_g, np.arange(d_len, n), d_cache, chain_visible(len(nxt)))
+    committed = list(prompt)
+    root = argmax(logits[-1].astype(np.float32))
+    fresh_g = draft.fuse(aux)
+    drafted, per_cycle = 0, []
+    while len(committed) - P < max_new:
+        n = len(committed)
+        # 1) catch-up: each committed position the draft cache lacks (drafted .. n-1) runs once,
+        #    with its fused target feature and the embedding of the token after it (root last)
+        cu_tokens = committed[drafted + 1:] + [root]
+        a, dk, dv = draft.layer(cu_tokens, fresh_g, np.arange(drafted, n), d_cache, chain_visible(len(cu_tokens)))
         d_cache.append(0, dk, dv)
-        d_len = n
-        # 2) draft tree rooted at the pending token
-        tokens, parents = build_tree(draft, d_cache, a[-1], pending, n)
+        drafted = n
+        # 2) the draft tree under the root token
+        tokens, parents = build_tree(draft, d_cache, a[-1], root, n)
         # 3) verify: one target pass over the tree at positions n + depth
         pos = n + depths(parents)
         logits, aux, nk, nv = target.forward(tokens, pos, t_cache, tree_visible(parents))
         res = accept_greedy(tokens, parents, logits.astype(np.float32))
         path = res["path"]
-        # 4) commit: the path's target K/V; g for the kept positions; draft cache stays at d_len
+        # 4) commit the accepted path's target K/V and keep its features for the next catch-up;
+        #    the draft cache already ends at the last committed position
         target.commit(t_cache, nk, nv, path)
-        ids += [int(tokens[c]) for c in path]
-        pending = res["next_root"]
-        new_g = draft.fuse(aux[path])
-        accepted.append(res["accept_len"])
-    out = (ids + [pending])[P:P + max_new]
-    return out, accepted
+        committed += [int(tokens[c]) for c in path]
+        root = res["next_root"]
+        fresh_g = draft.fuse(aux[path])
+        per_cycle.append(res["accept_len"])
+    out = (committed + [root])[P:P + max_new]
+    return out, per_cycle

@@ -1,9 +1,9 @@
 """Draft-tree bookkeeping: depth, RoPE positions, ancestor mask and bitmask.
 
 Source: "Advanced speculative decoding: tree drafts and EAGLE", section "Why
-trees" and its ``tree_mask`` / ``depths`` helpers: node i sees the committed
-prefix, its ancestors and itself; its position is prefix length + depth, so
-siblings share a position.  The root (node 0, parent -1) is the token the
+trees" and its mask and depth helpers: node i attends to every committed
+prefix position, to the nodes on its path from the root and to itself, and sits
+at position prefix length + depth, so siblings share a position.  The root (node 0, parent -1) is the token the
 target gave in the previous step.
 
 Representation used on both sides: ``parents`` int32 [N] with parents[0] = -1
@@ -49,10 +49,8 @@ def static_tree(branching):
 
 
 def depths(parents):
-    d = []
-    for i, p in enumerate(parents):
-        d.append(0 if p == -1 else d[int(p)] + 1)
-    return np.asarray(d, dtype=np.int64)
+    """Depth of every node: the number of its proper ancestors."""
+    return mask_matrix(parents).sum(axis=1).astype(np.int64) - 1
 
 
 def positions(parents, prefix_len):
@@ -61,14 +59,18 @@ def positions(parents, prefix_len):
 
 
 def mask_matrix(parents):
-    """Boolean [N, N] visibility matrix by walking up from each node."""
-    n = len(parents)
-    m = np.zeros((n, n), dtype=bool)
-    for i in range(n):
-        j = i
-        while j != -1:
-            m[i, j] = True
-            j = int(parents[j])
+    """Boolean [N, N] visibility matrix, brute force: all nodes step to their parents together,
+    and each step marks the ancestor reached."""
+    p = np.asarray([int(v) for v in parents], dtype=np.int64)
+    n = len(p)
+    m = np.eye(n, dtype=bool)
+    cur = np.arange(n)
+    for _ in range(n):
+        cur = np.where(cur >= 0, p[np.maximum(cur, 0)], -1)
+        live = np.flatnonzero(cur >= 0)
+        if live.size == 0:
+            break
+        m[live, cur[live]] = True
     return m
 
 
