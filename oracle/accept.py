@@ -19,7 +19,7 @@ Sources:
   bonus] padded with -1; with a deterministic (greedy) draft q = 1 at the
   drafted token, so the residual is p with that token zeroed.
 
-Readings taken (each one is listed in the design doc):
+Readings taken (the pages state the multi-candidate rule only in prose):
 * Children of a node are tried in ascending node index.
 * argmax uses a total order on fp32 bit patterns (``order_key``) and the
   lowest token id on ties.

@@ -11,7 +11,7 @@ are the draft's top-k tokens; node 0 is the root).
 
 The pages give the selection rule only in prose, so this is the plainest
 reading of "expand to depth D with top-k per node, rerank by cumulative
-log-probability down to N nodes" (listed in the design doc):
+log-probability down to N nodes":
 * depth 1: the root row's top-k tokens; score = logq (the DSM log-normaliser
   at T = 1, :mod:`oracle.dsm`); ties in top-k go to the lower token id.
 * depth t = 2..D: the frontier is the k best depth-(t-1) candidates by
@@ -38,8 +38,10 @@ target vocabulary with -inf outside the subset (pinned in the tests).
 
 parity unpinned beyond invariants: the EAGLE-2 source is not on the pages.
 The invariants tested are the node count, depth bound, ancestor closure,
-frontier = top-k at each depth, final set = top N-1 over all candidates by
-brute-force sort, and that top_k = 1 gives the chain drafting of section XI.2.
+frontier = top-k at each depth, every candidate's score recomputed as the fp32
+running sum of the log-softmax of its ancestors' expansion rows at their
+tokens, final set = top N-1 over all candidates by brute-force sort, and that
+top_k = 1 gives the chain drafting of section XI.2.
 """
 import numpy as np
 

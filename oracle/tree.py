@@ -12,7 +12,9 @@ of node i fits a 64-bit word: bit j set <=> node j is i or an ancestor of i.
 
 Pinned by: the 6x6 mask the page prints for parents [-1, 0, 0, 1, 1, 2]
 (tests/golden/tree_mask_6.txt), by agreement between the brute-force
-ancestor walk and the bitmask recurrence on random trees, and, for
+ancestor walk and the bitmask recurrence on random trees, by depth from the
+parent recurrence equal to the walk's ancestor count (two separate code
+paths), and, for
 ``static_tree``, by the node counts the page's exercise 1 answers (14 and 30
 draft nodes for branching [2, 2, 1, 1] and [3, 3, 2]).
 """
@@ -49,8 +51,13 @@ def static_tree(branching):
 
 
 def depths(parents):
-    """Depth of every node: the number of its proper ancestors."""
-    return mask_matrix(parents).sum(axis=1).astype(np.int64) - 1
+    """Depth of every node by the parent recurrence: the root is at depth 0 and every other node
+    is one deeper than its parent (parents precede their children)."""
+    validate(parents)
+    d = np.zeros(len(parents), dtype=np.int64)
+    for i in range(1, len(parents)):
+        d[i] = d[int(parents[i])] + 1
+    return d
 
 
 def positions(parents, prefix_len):
@@ -59,18 +66,16 @@ def positions(parents, prefix_len):
 
 
 def mask_matrix(parents):
-    """Boolean [N, N] visibility matrix, brute force: all nodes step to their parents together,
-    and each step marks the ancestor reached."""
-    p = np.asarray([int(v) for v in parents], dtype=np.int64)
-    n = len(p)
-    m = np.eye(n, dtype=bool)
-    cur = np.arange(n)
-    for _ in range(n):
-        cur = np.where(cur >= 0, p[np.maximum(cur, 0)], -1)
-        live = np.flatnonzero(cur >= 0)
-        if live.size == 0:
-            break
-        m[live, cur[live]] = True
+    """Boolean [N, N] visibility matrix by brute force: row i marks every node met while walking
+    from node i up to the root, node i included."""
+    validate(parents)
+    n = len(parents)
+    m = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        j = i
+        while j != -1:
+            m[i, j] = True
+            j = int(parents[j])
     return m
 
 

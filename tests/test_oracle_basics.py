@@ -91,6 +91,59 @@ def test_weights_match_softmax():
             assert np.abs(lq[big] - np.log(sm[big])).max() < 1e-5
 
 
+def _logq_excess(fn, z, T):
+    """Largest |fn(z) - log softmax(z / T)| over the row, divided by its error bound.
+
+    The bound follows the arithmetic: t_i = fp32(fp32(z_i - m) * fp32(1/T)) is within 3 ulp-units
+    (2**-24 relative each) of x_i = (z_i - m) / T; EXP is within 4 * 2**-24 relative; the weights
+    are truncated to 2**-31 each against a sum of at least 1 (the maximum weighs 1), so S loses at
+    most V * 2**-31 relative; LOG31 is within 4e-7 of ln(S * 2**-31) (max(1, |.|) relative); the
+    final fp32 subtraction rounds by half an ulp of the result."""
+    x = (z.astype(np.float64) - float(z.max())) / T
+    lse = math.log(np.exp(x).sum())
+    ref = x - lse
+    got = fn(z, dsm.inv_temperature(T)).astype(np.float64)
+    bound = (2.0**-22 * (np.abs(x) + np.abs(x).max() + 1.0) + len(z) * 2.0**-31
+             + 4e-7 * max(1.0, lse) + 2.0**-23 * np.abs(ref))
+    return float((np.abs(got - ref) / bound).max())
+
+
+def _logq_sign_slip(z, inv_t):
+    t = dsm.scaled(z, inv_t)
+    return (t + dsm.log31(dsm.weights(z, inv_t)[1])).astype(np.float32)
+
+
+def _logq_raw_logit(z, inv_t):
+    t = (np.asarray(z, np.float32) * np.float32(inv_t)).astype(np.float32)
+    return (t - dsm.log31(dsm.weights(z, inv_t)[1])).astype(np.float32)
+
+
+def _logq_no_temperature(z, inv_t):
+    return dsm.logq(z, np.float32(1.0))
+
+
+def _logq_fix_bits_off_by_one(z, inv_t):
+    t = dsm.scaled(z, inv_t)
+    return (t - (dsm.log31(dsm.weights(z, inv_t)[1]) - np.float32(math.log(2.0)))).astype(np.float32)
+
+
+@pytest.mark.parametrize("V", [8, 1000, 128256])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_logq_is_log_softmax(V, T):
+    """logq = the log of the tempered softmax ("EAGLE-3: Engineering Implementation of LLM
+    Inference Acceleration", section X, probs = softmax(z / T)), over whole N(0, 3^2) rows, within
+    the bound of its fixed-point arithmetic; planted mistakes (sign of the normaliser, the row
+    maximum not subtracted, the temperature dropped, the fixed point off by one bit) all fail."""
+    r = np.random.default_rng(V + int(10 * T))
+    z = (3 * r.standard_normal(V)).astype(np.float32) + np.float32(5.0)   # the maximum is not 0
+    assert _logq_excess(dsm.logq, z, T) <= 1.0
+    planted = [_logq_sign_slip, _logq_raw_logit, _logq_fix_bits_off_by_one]
+    if T != 1.0:
+        planted.append(_logq_no_temperature)
+    for bad in planted:
+        assert _logq_excess(bad, z, T) > 1.0, bad.__name__
+
+
 def test_logq_of_certain_token_is_zero():
     z = np.full(16, -1000.0, np.float32)
     z[3] = 0.0

@@ -174,15 +174,62 @@ def test_tree_verify_logits_equal_path_logits():
     assert _tree_vs_paths(target, prompt, parents, tokens, everything) > 1e-6
 
 
+def _torch_stream(w, cfg, tokens, theta=att.ROPE_THETA, eps=1e-5):
+    """The tiny Llama's residual stream written with torch ops in fp64, independently of the
+    oracle: torch rms_norm, scaled_dot_product_attention with a causal mask, SiLU, and RoPE as the
+    complex rotation of half-split pairs at the fp32 angles fp32(pos) * fp32(theta^(-2j/D)).
+    Returns [x entering layer 0, x entering layer 1, ..., x after the last layer] and the logits."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    d, H, KVH, D, nl = cfg["d"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["n_layers"]
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    T = len(tokens)
+    inv = torch.tensor((float(theta) ** (-2.0 * np.arange(D // 2) / D)).astype(np.float32))
+    ang = (torch.arange(T, dtype=torch.float32)[:, None] * inv[None, :]).double()       # [T, D/2]
+    rot = torch.polar(torch.ones_like(ang), ang)
+
+    def rope(x):                                   # [T, heads, D]
+        z = torch.complex(x[..., : D // 2], x[..., D // 2:]) * rot[:, None, :]
+        return torch.cat([z.real, z.imag], -1)
+
+    x = t(w["embed"])[torch.tensor(tokens)]
+    streams = [x]
+    for l in range(nl):
+        p = f"layers.{l}."
+        h = F.rms_norm(x, (d,), t(w[p + "attn_norm"]), eps)
+        q = rope((h @ t(w[p + "wq"]).T).view(T, H, D))
+        k = rope((h @ t(w[p + "wk"]).T).view(T, KVH, D)).repeat_interleave(H // KVH, 1)
+        v = (h @ t(w[p + "wv"]).T).view(T, KVH, D).repeat_interleave(H // KVH, 1)
+        o = F.scaled_dot_product_attention(q.transpose(0, 1), k.transpose(0, 1), v.transpose(0, 1),
+                                           is_causal=True).transpose(0, 1).reshape(T, H * D)
+        x = x + o @ t(w[p + "wo"]).T
+        h = F.rms_norm(x, (d,), t(w[p + "mlp_norm"]), eps)
+        x = x + (F.silu(h @ t(w[p + "w_gate"]).T) * (h @ t(w[p + "w_up"]).T)) @ t(w[p + "w_down"]).T
+        streams.append(x)
+    logits = F.rms_norm(x, (d,), t(w["final_norm"]), eps) @ t(w["lm_head"]).T
+    return [s.numpy() for s in streams], logits.numpy()
+
+
 def test_aux_taps_enter_layers():
+    """Aux tap of layer i = the residual stream entering decoder layer i, i.e. after layers
+    0..i-1 and before any norm ("EAGLE-3: Engineering Implementation of LLM Inference
+    Acceleration", sections IX.1-IX.3; "Speculative Decoding (EAGLE3) in the vLLM Neuron
+    Framework", "Auxiliary Hidden State Extraction": captured before the layer runs).  Checked
+    against the stream of an independent torch fp64 model; a tap of layer i's output (the planted
+    off-by-one) differs from it, and the oracle's logits match the torch model's."""
     target, _ = _tiny()
-    prompt = synth.tiny_prompt(0)[:5]
+    cfg = synth.TINY
+    d = cfg["d"]
+    prompt = synth.tiny_prompt(0)[:9]
     cache = target.new_cache()
-    _, aux, _, _ = target.forward(prompt, np.arange(5), cache, llama.chain_visible(5))
-    assert aux.shape == (5, 3 * 64)
-    # layer-1 tap is the output of layer 0: embedding + attention + MLP residuals
-    emb = target.w["embed"][prompt].astype(np.float64)
-    assert not np.allclose(aux[:, :64], emb)
+    logits, aux, _, _ = target.forward(prompt, np.arange(9), cache, llama.chain_visible(9))
+    streams, ref_logits = _torch_stream(target.w, cfg, prompt)
+    assert aux.shape == (9, 3 * d)
+    assert np.abs(logits - ref_logits).max() < 1e-10
+    for k, layer in enumerate(synth.TINY_AUX_LAYERS):
+        tap = aux[:, k * d:(k + 1) * d]
+        assert np.abs(tap - streams[layer]).max() < 1e-12
+        assert np.abs(tap - streams[layer + 1]).max() > 1e-4       # not the layer's output
 
 
 # ----------------------------------------------------------------------------- dynamic tree
@@ -221,6 +268,24 @@ def test_dynamic_tree_invariants(depth, top_k, n_nodes):
         prev = [i for i, c in enumerate(cands) if c["depth"] == t - 1]
         prev.sort(key=lambda i: (-float(cands[i]["score"]), cands[i]["creation"]))
         assert res["frontiers"][t - 1] == prev[:top_k]
+    # scores are cumulative log-probabilities: a candidate made from frontier rank r of depth t
+    # scores its parent's score plus the log-softmax of that expansion row at its token, summed in
+    # fp32 from the root down (the log-softmax itself is pinned in test_oracle_basics)
+    from oracle import dsm
+    for c in cands:
+        path, j = [], c
+        while True:
+            path.append(j)
+            if j["parent"] == -1:
+                break
+            j = cands[j["parent"]]
+        acc = None
+        for node in reversed(path):
+            row = logs[node["depth"] - 1][node["creation"] // top_k]
+            lq = dsm.logq(row)[node["token"]]
+            acc = lq if acc is None else np.float32(acc + lq)
+        assert np.float32(acc).view(np.uint32) == np.float32(c["score"]).view(np.uint32)
+        assert c["token"] in draft_tree.topk_tokens(logs[c["depth"] - 1][c["creation"] // top_k], top_k)
     # each expansion contributes the row's top-k tokens (ties to the lower id)
     first = [c for c in cands if c["depth"] == 1]
     row = logs[0][0]
