@@ -99,22 +99,25 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------------------- GPU arm
 class Engine:
-    """Device state of the speculative-decoding loop and one step over the C ABI."""
+    """The bench workload around the package's SpeculativeStep: random-init Llama-3.1-8B-shaped
+    target and EAGLE-3 head (N(0, 0.02), norms 1), N(0, 1) prefilled caches, and per-launch timing
+    of the dominant kernels with CUDA events on the launching stream."""
 
     def __init__(self, cfg, steps_total, dev, timing=True, fused_rope=True):
+        from eagle_tree_speculative_spec_gb300.step import SpeculativeStep
         import eagle_tree_speculative_spec_gb300 as e3
         self.e3, self.cfg, self.dev, self.timing = e3, cfg, dev, timing
         # the target's QKV projection rotates q and the tree keys (EPI_BF16_ROPE) and the verify
         # attention takes them as they are; False: the attention rotates them itself
         self.fused_rope = fused_rope
         c = cfg
-        B, N, d, V, D = c["B"], c["N"], c["d"], c["V"], c["D"]
+        B, d, V, D = c["B"], c["d"], c["V"], c["D"]
         Hq, Hkv, F, Lyr = c["Hq"], c["Hkv"], c["F"], c["layers"]
-        self.qkv_w = (Hq + 2 * Hkv) * D
-        self.S = c["L0"] + c["W"] * (steps_total + 2) + 64
+        qkv_w = (Hq + 2 * Hkv) * D
+        S = c["L0"] + c["W"] * (steps_total + 2) + 64
         # host-side length bound of every launch, fixed for the run so one captured graph serves every step
         # (the kernels read the exact per-sequence lengths from device memory)
-        self.max_prefix = c["L0"] + c["W"] * (steps_total + 1)
+        max_prefix = c["L0"] + c["W"] * (steps_total + 1)
         g = torch.Generator(device=dev)
         g.manual_seed(1234)
         bf = torch.bfloat16
@@ -123,66 +126,32 @@ class Engine:
             return (torch.randn(*shape, generator=g, device=dev, dtype=torch.float32) * std).to(bf)
 
         ones = lambda n: torch.ones(n, device=dev, dtype=bf)
-        # target (random init N(0, 0.02), norms 1)
-        self.embed = w(V, d)
-        self.wqkv = [w(self.qkv_w, d) for _ in range(Lyr)]
-        self.wo = [w(d, Hq * D) for _ in range(Lyr)]
-        self.wg = [w(F, d) for _ in range(Lyr)]
-        self.wu = [w(F, d) for _ in range(Lyr)]
-        self.wd = [w(d, F) for _ in range(Lyr)]
-        self.norm1 = [ones(d) for _ in range(Lyr)]
-        self.norm2 = [ones(d) for _ in range(Lyr)]
-        self.final_norm = ones(d)
-        self.lm_head = w(V, d)
+        embed = w(V, d)
+        target = {"embed": embed, "wqkv": [w(qkv_w, d) for _ in range(Lyr)], "wo": [w(d, Hq * D) for _ in range(Lyr)],
+                  "wg": [w(F, d) for _ in range(Lyr)], "wu": [w(F, d) for _ in range(Lyr)],
+                  "wd": [w(d, F) for _ in range(Lyr)], "norm1": [ones(d) for _ in range(Lyr)],
+                  "norm2": [ones(d) for _ in range(Lyr)], "final_norm": ones(d), "lm_head": w(V, d)}
         # draft head (shares the target embedding; own LM head)
-        self.draft_w = {"w_fc": w(d, 3 * d), "embed": self.embed, "input_norm": ones(d), "hidden_norm": ones(d),
-                        "w_qkv": w(self.qkv_w, 2 * d), "w_o": w(d, Hq * D), "post_norm": ones(d),
-                        "w_gate": w(F, d), "w_up": w(F, d), "w_down": w(d, F), "final_norm": ones(d),
-                        "lm_head": w(V, d)}
+        draft = {"w_fc": w(d, 3 * d), "embed": embed, "input_norm": ones(d), "hidden_norm": ones(d),
+                 "w_qkv": w(qkv_w, 2 * d), "w_o": w(d, Hq * D), "post_norm": ones(d),
+                 "w_gate": w(F, d), "w_up": w(F, d), "w_down": w(d, F), "final_norm": ones(d), "lm_head": w(V, d)}
+        scfg = dict(c, mode=e3.TOPK)
+        self.step_obj = st = SpeculativeStep(scfg, target, draft, S, max_prefix, dev, fused_rope=fused_rope)
+        self.S, self.max_prefix = S, max_prefix
         # caches: prefixes of L0 positions of N(0, 1) keys / values (as if prefilled)
-        S = self.S
-        self.k_cache = torch.zeros(Lyr, B, Hkv, S, D, device=dev, dtype=bf)
-        self.v_cache = torch.zeros_like(self.k_cache)
-        self.k_cache[..., : c["L0"], :].normal_(generator=g)
-        self.v_cache[..., : c["L0"], :].normal_(generator=g)
-        self.dk_cache = torch.zeros(B, Hkv, S, D, device=dev, dtype=bf)
-        self.dv_cache = torch.zeros_like(self.dk_cache)
-        self.dk_cache[..., : c["L0"] - 1, :].normal_(generator=g)
-        self.dv_cache[..., : c["L0"] - 1, :].normal_(generator=g)
-        i32 = torch.int32
-        self.prefix_len = torch.full((B,), c["L0"], dtype=i32, device=dev)
-        self.draft_len = torch.full((B,), c["L0"] - 1, dtype=i32, device=dev)
+        st.k_cache[..., : c["L0"], :].normal_(generator=g)
+        st.v_cache[..., : c["L0"], :].normal_(generator=g)
+        st.dk_cache[..., : c["L0"] - 1, :].normal_(generator=g)
+        st.dv_cache[..., : c["L0"] - 1, :].normal_(generator=g)
+        st.prefix_len.fill_(c["L0"])
+        st.draft_len.fill_(c["L0"] - 1)
         # catch-up input of the first step: the last prompt position's aux states and the root token
-        W = c["W"]
-        self.aux_in = torch.zeros(B, W, 3 * d, device=dev, dtype=bf)
-        self.aux_in[:, 0].normal_(generator=g)
-        self.next_tok = torch.randint(0, V, (B, W), generator=g, device=dev, dtype=i32)
-        self.tc = torch.ones(B, dtype=i32, device=dev)
-        # per-step buffers
-        self.tokens = torch.empty(B, N, dtype=i32, device=dev)
-        self.parents = torch.empty(B, N, dtype=i32, device=dev)
-        self.depth = torch.empty(B, N, dtype=i32, device=dev)
-        self.anc = torch.empty(B, N, dtype=torch.int64, device=dev)
-        self.score = torch.empty(B, N, dtype=torch.float32, device=dev)
-        R = B * N
-        self.x = torch.empty(R, d, device=dev, dtype=bf)
-        self.h = torch.empty(R, d, device=dev, dtype=bf)
-        self.qkv = torch.empty(Lyr, R, self.qkv_w, device=dev, dtype=bf)
-        self.attn = torch.empty(R, Hq * D, device=dev, dtype=bf)
-        self.act = torch.empty(R, F, device=dev, dtype=bf)
-        self.aux_tree = torch.empty(R, 3 * d, device=dev, dtype=bf)
-        self.logits = torch.empty(R, V, device=dev, dtype=torch.float32)
-        self.accept_len = torch.empty(B, dtype=i32, device=dev)
-        self.path = torch.empty(B, W, dtype=i32, device=dev)
-        self.next_root = torch.empty(B, dtype=i32, device=dev)
-        self.slot_map = torch.empty(B, W, dtype=i32, device=dev)
-        self.dev_status = torch.zeros(1, dtype=i32, device=dev)
-        self.step_counter = torch.zeros(1, dtype=torch.int64, device=dev)   # Philox step, advanced on device
-        # workspaces (sized once for the largest shapes)
-        self.ws_lin = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        self.ws_attn = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        self.ws_acc = torch.empty(16, dtype=torch.uint8, device=dev)
-        self.ws_draft = None
+        st.aux_in[:, 0].normal_(generator=g)
+        st.next_tok.copy_(torch.randint(0, V, st.next_tok.shape, generator=g, device=dev, dtype=torch.int32))
+        st.tc.fill_(1)
+        # the per-sequence state and outputs are the step's buffers
+        for name in ("prefix_len", "draft_len", "aux_in", "next_tok", "tc", "accept_len", "dev_status", "tokens"):
+            setattr(self, name, getattr(st, name))
         self.steps_done = 0
         self.kernel_ms = {"gemm": 0.0, "gemm_gateup": 0.0, "verify_attn": 0.0}
         self.kernel_calls = {"gemm": 0, "gemm_gateup": 0, "verify_attn": 0}
@@ -221,130 +190,22 @@ class Engine:
         self.kernel_ms = {k: 0.0 for k in self.kernel_ms}
         self.kernel_calls = {k: 0 for k in self.kernel_calls}
 
-    # -- the step as a list of prepared C calls: every argument struct is built once, only the fields
-    #    that change between steps (host bounds, the Philox step counter) are patched before a call
-    def _prepare(self):
-        import ctypes
-        e3, c = self.e3, self.cfg
-        L = e3._lib.lib()
-        B, N, d, D, Hq, Hkv = c["B"], c["N"], c["d"], c["D"], c["Hq"], c["Hkv"]
-        R = B * N
-        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        ops = []
-        keep = []                                       # keep structs alive
-
-        def ws(t):
-            return (ctypes.c_void_p(t.data_ptr()), ctypes.c_size_t(t.numel())) if t is not None else (None, 0)
-
-        # draft
-        da = e3._lib.draft_tree_args(self.aux_in, self.next_tok, self.tc, self.dk_cache, self.dv_cache,
-                                     self.draft_len, self.tokens, self.parents, self.depth, self.anc, self.score,
-                                     n_heads=Hq, ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
-                                     max_draft_len=self.max_prefix - 1, dev_status=self.dev_status)
-        self.ws_draft = torch.empty(L.eagle3_draft_tree_workspace_size(ctypes.byref(da)), dtype=torch.uint8,
-                                    device=self.dev)
-        dw = e3._lib.draft_weights(self.draft_w)
-        keep += [da, dw]
-        wp, wb = ws(self.ws_draft)
-        ops.append((None, lambda a=da, w=dw: L.eagle3_draft_tree(ctypes.byref(w), ctypes.byref(a), wp, wb, st)))
-
-        def norm(x, w, out, gather=None, tap=None):
-            a = e3._lib.RmsnormArgs(rows=out.shape[0], dim=w.shape[0], n_src=x.shape[0], eps=1e-5, ld_in=x.stride(0),
-                                    ld_out=out.stride(0), ld_tap=0 if tap is None else tap.stride(0),
-                                    input=x.data_ptr(), w=w.data_ptr(),
-                                    gather=None if gather is None else gather.data_ptr(), out=out.data_ptr(),
-                                    tap_out=None if tap is None else tap.data_ptr(),
-                                    dev_status=self.dev_status.data_ptr())
-            keep.append(a)
-            ops.append((None, lambda a=a: L.eagle3_rmsnorm(ctypes.byref(a), st)))
-
-        lp, lb = ws(self.ws_lin)
-
-        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm", rope_cols=0):
-            a = e3._lib.LinearArgs(m=x.shape[0], n=w.shape[0], k=x.shape[1], epilogue=epi, splits=0, ld_x=0, ld_w=0,
-                                   ld_out=0, ld_res=0, x=x.data_ptr(), w=w.data_ptr(),
-                                   w2=None if w2 is None else w2.data_ptr(), out=out.data_ptr(),
-                                   residual=None if res is None else res.data_ptr(),
-                                   dev_status=self.dev_status.data_ptr(), rope_cols=rope_cols,
-                                   rope_rows_per_seq=N, rope_theta=500000.0,
-                                   rope_base=self.prefix_len.data_ptr() if rope_cols else None,
-                                   rope_depth=self.depth.data_ptr() if rope_cols else None)
-            keep.append(a)
-            ops.append((kind, lambda a=a: L.eagle3_linear(ctypes.byref(a), lp, lb, st)))
-
-        taps = {t: i for i, t in enumerate(c["taps"])}
-        norm(self.embed, self.norm1[0], self.h, gather=self.tokens.view(-1), tap=self.x)
-        ap, ab = ws(self.ws_attn)
-        for l in range(c["layers"]):
-            if l > 0:
-                tap = self.aux_tree[:, taps[l] * d:(taps[l] + 1) * d] if l in taps else None
-                norm(self.x, self.norm1[l], self.h, tap=tap)
-            qkv = self.qkv[l]
-            if self.fused_rope:
-                # q and the tree keys leave the projection rotated at prefix_len + depth
-                lin(self.h, self.wqkv[l], qkv, epi=e3.EPI_BF16_ROPE, rope_cols=(Hq + Hkv) * D)
-            else:
-                lin(self.h, self.wqkv[l], qkv)
-            q = qkv.view(B, N, self.qkv_w)[:, :, : Hq * D].unflatten(2, (Hq, D))
-            kt = qkv.view(B, N, self.qkv_w)[:, :, Hq * D:(Hq + Hkv) * D].unflatten(2, (Hkv, D))
-            vt = qkv.view(B, N, self.qkv_w)[:, :, (Hq + Hkv) * D:].unflatten(2, (Hkv, D))
-            va = e3._lib.verify_attn_args(q, kt, vt, self.k_cache[l], self.v_cache[l], self.parents, self.prefix_len,
-                                          self.attn.view(B, N, Hq, D), max_prefix_len=self.max_prefix,
-                                          dev_status=self.dev_status, qk_rotated=self.fused_rope)
-            keep.append(va)
-            ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st)))
-            lin(self.attn, self.wo[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
-            norm(self.x, self.norm2[l], self.h)
-            lin(self.h, self.wg[l], self.act, epi=e3.EPI_SWIGLU, w2=self.wu[l], kind="gemm_gateup")
-            lin(self.act, self.wd[l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
-        norm(self.x, self.final_norm, self.h)
-        lin(self.h, self.lm_head, self.logits, epi=e3.EPI_F32)
-        aa = e3._lib.AcceptArgs(mode=e3.TOPK, batch=B, n_nodes=N, vocab=c["V"], max_path=c["W"],
-                                temperature=c["temperature"], seed=c["seed"], step=0,
-                                target_logits=self.logits.data_ptr(), draft_logits=None,
-                                tokens=self.tokens.data_ptr(), parents=self.parents.data_ptr(),
-                                accept_len=self.accept_len.data_ptr(), path=self.path.data_ptr(),
-                                emitted=self.next_tok.data_ptr(), next_root=self.next_root.data_ptr(),
-                                dev_status=self.dev_status.data_ptr(), step_counter=self.step_counter.data_ptr())
-        keep.append(aa)
-        cp, cb = ws(self.ws_acc)
-        ops.append((None, lambda a=aa: L.eagle3_accept(ctypes.byref(a), cp, cb, st)))
-        kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=Hq * D)
-        vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(Hq + Hkv) * D)
-        ca = e3._lib.CompactArgs(n_layers=c["layers"], batch=B, n_nodes=N, n_kv_heads=Hkv, head_dim=D, elem_bytes=2,
-                                 s_max=self.S, max_path=c["W"], cache_layer_stride=B * Hkv * self.S * D,
-                                 tree_layer_stride=R * self.qkv_w, tree_node_stride=self.qkv_w,
-                                 k_cache=self.k_cache.data_ptr(), v_cache=self.v_cache.data_ptr(),
-                                 tree_k=kflat.data_ptr(), tree_v=vflat.data_ptr(), path=self.path.data_ptr(),
-                                 accept_len=self.accept_len.data_ptr(), prefix_len=self.prefix_len.data_ptr(),
-                                 slot_map=self.slot_map.data_ptr(), committed=self.tc.data_ptr(), aux_dim=3 * d,
-                                 aux_tree=self.aux_tree.data_ptr(), aux_out=self.aux_in.data_ptr(),
-                                 dev_status=self.dev_status.data_ptr())
-        keep.append(ca)
-        ops.append((None, lambda a=ca: L.eagle3_compact_kv(ctypes.byref(a), st)))
-        self._ops, self._keep = ops, keep
-
     def _issue(self, evs, external=False):
-        for kind, call in self._ops:
-            if kind is not None and evs is not None:
-                self._timed(kind, call, evs, external)
-            else:
-                status = call()
-                if status:
-                    raise RuntimeError(f"libeagle3 call failed with status {status}")
+        timed = None if evs is None else (lambda kind, call: self._timed(kind, call, evs, external))
+        self.step_obj.run(timed=timed)
 
     def step(self):
         """One eager step: every C call issued from the host."""
-        if not hasattr(self, "_ops"):
-            self._prepare()
+        if not self.step_obj.verify_ops:
+            self.step_obj.prepare()
         self._issue(self._ev if self.timing else None)
         self.steps_done += 1
 
     def capture(self, n):
         """Capture n CUDA graphs of one step each (same kernels; each graph owns its timing events, so
         every replay of a timed loop over the n graphs can be read back afterwards)."""
-        if not hasattr(self, "_ops"):
-            self._prepare()
+        if not self.step_obj.verify_ops:
+            self.step_obj.prepare()
         self.graphs = []
         pool = None
         for _ in range(n):
@@ -366,19 +227,9 @@ class Engine:
         """Kernel nodes of the first captured graph, by function name (driver graph API)."""
         return graph_kernel_names(self.graphs[0][0])
 
-    def flops_per_step(self):
-        """Algorithmic GEMM flops of one step (target verify + draft head)."""
-        c = self.cfg
-        d, F, V, Hq, D, qw = c["d"], c["F"], c["V"], c["Hq"], c["D"], self.qkv_w
-        R = c["B"] * c["N"]
-        per_layer = 2 * R * (d * qw + Hq * D * d + 2 * d * F + F * d)
-        target = c["layers"] * per_layer + 2 * R * d * V
-        rows_d = c["B"] * c["top_k"]
-        draft_layer = lambda m: 2 * m * (2 * d * qw + Hq * D * d + 2 * d * F + F * d)
-        tc_rows = c["B"] * c["W"]          # catch-up rows are padded to W per sequence
-        draft = (2 * tc_rows * 3 * d * d + draft_layer(tc_rows) + 2 * c["B"] * d * V
-                 + (c["depth"] - 1) * (draft_layer(rows_d) + 2 * rows_d * d * V))
-        return target, draft
+    def flops_per_step(self, catchup_rows=None):
+        """Algorithmic GEMM flops of one step (target verify, draft head over the real catch-up rows)."""
+        return self.step_obj.flops(catchup_rows)
 
     def attn_bytes_per_launch(self, L):
         """Algorithmic HBM bytes of one verify-attention launch (one layer, whole batch)."""
@@ -534,12 +385,14 @@ def run_gpu(args):
     ms = max_over_ranks(ms, dev)
     status = int(eng.dev_status.item())
 
-    # ---- e2e through host buffers: per step H2D of the step's inputs, D2H of its result
+    # ---- e2e through host buffers: every step's inputs come from pinned host memory and its outputs go
+    # back to it, and the outputs of step i are the inputs of step i + 1 (the decoding loop's own data
+    # flow, carried through the host): catch-up aux rows, the emitted tokens (last one = next root), the
+    # committed counts; the accepted lengths are read back as the step's result
     c = cfg
     host_aux = eng.aux_in.cpu().pin_memory()
     host_tok = eng.next_tok.cpu().pin_memory()
     host_tc = eng.tc.cpu().pin_memory()
-    out_tok = torch.empty_like(eng.next_tok, device="cpu").pin_memory()
     out_len = torch.empty_like(eng.accept_len, device="cpu").pin_memory()
     eng.timing = False
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -553,13 +406,15 @@ def run_gpu(args):
             eng.replay(i)
         else:
             eng.step()
-        out_tok.copy_(eng.next_tok, non_blocking=True)
+        host_aux.copy_(eng.aux_in, non_blocking=True)
+        host_tok.copy_(eng.next_tok, non_blocking=True)
+        host_tc.copy_(eng.tc, non_blocking=True)
         out_len.copy_(eng.accept_len, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     h2d = host_aux.numel() * 2 + host_tok.numel() * 4 + host_tc.numel() * 4
-    d2h = out_tok.numel() * 4 + out_len.numel() * 4
+    d2h = h2d + out_len.numel() * 4
 
     units = cfg["B"] * cfg["N"] * args.steps * world
     value = job_rate(cfg["B"] * cfg["N"] * args.steps, world, ms)
@@ -594,6 +449,9 @@ def run_gpu(args):
                      "peak": tf_sust, "unit": "TFLOP/s",
                      "frac": round(gu_tflops / tf_sust, 4) if gu_tflops else None,
                      "traffic": GATEUP_TRAFFIC_BYTES,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of this "
+                                       "kernel at this shape (a separate capture, not this run)",
+                     "frac_of_burst": round(gu_tflops / tf_burst, 4) if gu_tflops else None,
                      "kernel": f"gemm_tc_kernel, SwiGLU gate+up projection M={R} N=2x{cfg['F']} K={cfg['d']} "
                                f"({gu_flops / 1e12:.3f} TFLOP per launch, {cfg['layers']} launches per step)",
                      "ms_per_launch": round(gu_ms, 4),
@@ -624,8 +482,8 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-# DRAM bytes (read + write) of one SwiGLU gate+up launch at the bench shape, from the ncu capture
-# summarised in profiles/gemm_gateup_m3840.md (set it to None when the kernel changes)
+# DRAM bytes (read + write) of one SwiGLU gate+up launch at the bench shape, from an ncu capture of the
+# current GEMM kernel (to be set to None when the kernel changes)
 GATEUP_TRAFFIC_BYTES = 267724288 + 97391360
 
 
@@ -707,7 +565,10 @@ def cpu_baseline(cfg):
     step, parts = oracle_sample_seconds(cfg)
     threads = host_threads()
     value = cfg["N"] / step          # verified tree tokens per second for one sequence on the host
-    return {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+    return {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "extrapolated": True,
+            "scale_factors": {"layers": cfg["layers"], "lm_head_rows": cfg["N"] / 6, "lm_head_vocab": 8,
+                              "draft_rows_per_verify_row": (1 + (cfg["depth"] - 1) * cfg["top_k"]) / cfg["N"],
+                              "batch": cfg["B"]},
             "sample": ("one sequence: one layer of verify attention (60 nodes, 2048 prefix), one target "
                        "layer's projections and 6 LM-head rows (1/8 of the vocabulary) in fp64, TOPK acceptance at V=128256; "
                        "extrapolated to 32 layers + LM head + draft head; seconds per part: "
@@ -738,7 +599,7 @@ def run_reference(args):
             "config": {"workload": "EAGLE-3 draft-and-verify step, Llama-3.1-8B-shaped target + EAGLE-3 head, "
                                    "B=64, N=60 (depth 6, top-k 10), prefix 2048, T=1, compaction on",
                        "global_batch": cfg["B"], "seq_len": cfg["L0"], "parallelism": "host cores"},
-            "impl": "reference", "cpu_baseline": cb,
+            "impl": "reference", "cpu_baseline": cb, "extrapolated": True,
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -883,27 +744,28 @@ def run_kernel(args):
         c = dict(CFG)
         c["B"] = args.batch
         eng = Engine(c, 4, dev, timing=False)
+        so = eng.step_obj
         B = c["B"]
         tc1 = torch.ones(B, dtype=torch.int32, device=dev)
         dl0 = eng.draft_len.clone()
         # a reduced draft vocabulary: its own [Vd, d] head and the sorted target ids it covers
         Vd = args.draft_vocab if args.draft_vocab > 0 else c["V"]
-        dw, d2t = eng.draft_w, None
+        dw, d2t = so.draft_w, None
         if Vd != c["V"]:
             cpu_g = torch.Generator().manual_seed(7)
-            dw = dict(eng.draft_w)
+            dw = dict(so.draft_w)
             dw["lm_head"] = (torch.randn(Vd, c["d"], generator=cpu_g) * 0.02).to(torch.bfloat16).to(dev)
             d2t = torch.randperm(c["V"], generator=cpu_g)[:Vd].sort().values.to(torch.int32).to(dev)
-        a = e3._lib.draft_tree_args(eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache, eng.draft_len,
-                                    eng.tokens, eng.parents, eng.depth, eng.anc, eng.score, n_heads=c["Hq"],
+        a = e3._lib.draft_tree_args(eng.aux_in, eng.next_tok, tc1, so.dk_cache, so.dv_cache, eng.draft_len,
+                                    so.tokens, so.parents, so.depth, so.anc, so.score, n_heads=c["Hq"],
                                     ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
                                     max_draft_len=c["L0"], d2t=d2t)
         ws = torch.empty(e3._lib.eagle3_draft_tree_workspace_size(a), dtype=torch.uint8, device=dev)
 
         def fn():
             eng.draft_len.copy_(dl0)
-            e3.eagle3_draft_tree(dw, eng.aux_in, eng.next_tok, tc1, eng.dk_cache, eng.dv_cache,
-                                 eng.draft_len, eng.tokens, eng.parents, eng.depth, eng.anc, eng.score,
+            e3.eagle3_draft_tree(dw, eng.aux_in, eng.next_tok, tc1, so.dk_cache, so.dv_cache,
+                                 eng.draft_len, so.tokens, so.parents, so.depth, so.anc, so.score,
                                  n_heads=c["Hq"], ffn=c["F"], vocab=c["V"], depth=c["depth"], top_k=c["top_k"],
                                  max_draft_len=c["L0"], d2t=d2t, workspace=ws)
         ms_eager = _time_loop(fn, args.steps, args.warmup)
@@ -919,9 +781,9 @@ def run_kernel(args):
             fn()
         ms = _time_loop(graph.replay, args.steps, args.warmup)
         out.update(ms_eager=round(ms_eager, 4))
-        d, F, V, qw = c["d"], c["F"], Vd, eng.qkv_w
+        d, F, V, qw = c["d"], c["F"], Vd, so.qkv_w
         layer = lambda m: 2 * m * (2 * d * qw + c["Hq"] * 128 * d + 2 * d * F + F * d)
-        rows_c = B * c["W"]
+        rows_c = B           # one real catch-up row per sequence (tc = 1); the launch pads to tc_max rows
         flops = 2 * rows_c * 3 * d * d + layer(rows_c) + 2 * B * d * V + 5 * (layer(10 * B) + 2 * 10 * B * d * V)
         wbytes = 2 * (3 * d * d + 2 * d * qw + c["Hq"] * 128 * d + 3 * d * F + d * V)
         out.update(batch=B, draft_vocab=Vd, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),

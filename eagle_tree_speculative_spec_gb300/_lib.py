@@ -130,6 +130,8 @@ def _declare(L):
     L.eagle3_verify_attn_workspace_size.argtypes = [P(VerifyAttnArgs)]
     L.eagle3_verify_attn.restype = ctypes.c_int
     L.eagle3_verify_attn.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_test_verify_attn_timeout.restype = ctypes.c_int
+    L.eagle3_test_verify_attn_timeout.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _i32, _i64, _p]
     L.eagle3_verify_attn_noalloc.restype = ctypes.c_int
     L.eagle3_verify_attn_noalloc.argtypes = [P(VerifyAttnArgs), _p]
     L.eagle3_linear_workspace_size.restype = ctypes.c_size_t
@@ -323,6 +325,25 @@ def eagle3_verify_attn(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len,
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.eagle3_verify_attn(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_verify_attn")
+
+
+def eagle3_test_verify_attn_timeout(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *,
+                                    max_prefix_len, stall_tile, wait_limit_cycles, num_splits=0, dev_status=None,
+                                    workspace=None, stream=None, qk_rotated=False):
+    """Test hook (include/eagle3_testing.h): eagle3_verify_attn with prefix tile `stall_tile` never
+    loaded and every bounded wait limited to wait_limit_cycles, so the timeout path runs."""
+    a = verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out,
+                         max_prefix_len=max_prefix_len, num_splits=num_splits, dev_status=dev_status,
+                         qk_rotated=qk_rotated)
+    L = lib()
+    need = L.eagle3_verify_attn_workspace_size(ctypes.byref(a))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.eagle3_test_verify_attn_timeout(ctypes.byref(a), ws_ptr, ws_bytes, int(stall_tile),
+                                             int(wait_limit_cycles), _stream(stream)),
+           "eagle3_test_verify_attn_timeout")
 
 
 def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, splits=0, dev_status=None,

@@ -31,6 +31,11 @@ struct AttnLaunch {
     float *lse;
     int32_t *dev_status;
     int qk_rotated = 0;              // q and the tree keys arrive rotated (no RoPE, no tree_k write)
+    // bounded waits give up after this many clocks; a test of the timeout path shortens it
+    long long wait_limit = WAIT_LIMIT_CYCLES;
+    // test of the timeout path only: the K producer never loads this prefix tile (local index
+    // within the CTA's split), so the wait for it runs out; -1 = off
+    int stall_tile = -1;
 };
 
 size_t tree_attn_workspace(const AttnLaunch &a);

@@ -30,14 +30,14 @@ E3_DEV bool mbar_try(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: false if the phase did not complete within WAIT_LIMIT_CYCLES (or abort is set).
-E3_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// Bounded wait: false if the phase did not complete within `limit` clocks (or abort is set).
+E3_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, long long limit = WAIT_LIMIT_CYCLES) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             return false;
         }

@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include "attn.cuh"
+#include "eagle3_testing.h"
 #include "tc.cuh"
 
 namespace e3 {
@@ -69,6 +70,8 @@ struct Params {
     int tree_slot_inner;            // tree maps: slots are the middle dimension (else the outer)
     int s_mid;                      // with two halves, the first half's query slots are [q_lo, q_lo + s_mid)
     int qk_rotated;                 // q and the tree keys arrive rotated: Q is loaded by TMA as is
+    int stall_tile;                 // timeout-path test only: this prefix tile is never loaded (-1 off)
+    long long wait_limit;           // clocks after which a bounded wait gives up
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
     // element (b, slot i, head h) lives at base + b * sb + i * si + h * D
@@ -121,9 +124,9 @@ E3_DEV float fmax3(float a, float b, float c) {
 }
 
 // warp-uniform bounded wait (lane 0 polls, the outcome is broadcast)
-E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, long long limit) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort, limit) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -229,6 +232,7 @@ __global__ void __launch_bounds__(NT, 1)
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             npre = min(ST_K, n_prefix);   // fresh stages: nothing to wait for
             for (int j = 0; j < npre; ++j) {
+                if (j == p.stall_tile) continue;   // timeout-path test: this tile never arrives
                 uint8_t *dst = sm + OFF_K + j * KV_TILE;
                 tc::mbar_expect_tx(&ss.k_full[j], KV_TILE);
                 tc::tma_load_2d(dst, &tm_k, 0, row0 + j * BK, &ss.k_full[j]);
@@ -271,18 +275,20 @@ __global__ void __launch_bounds__(NT, 1)
             tc::prefetch_tmap(map);
             if (last) tc::prefetch_tmap(tmap);
             // V stage 1 holds the RoPE angle table until Q is staged (not used when Q arrives rotated)
-            bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort);
+            bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort, p.wait_limit);
             const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             const int j0 = is_k ? npre : 0;                  // thread 0 issued K tiles [0, npre) in phase A
             uint32_t issued = is_k ? (1u << npre) - 1u : 0u, last_par = 0;
+            if (is_k && p.stall_tile >= 0 && p.stall_tile < npre) issued &= ~(1u << p.stall_tile);
             for (int j = j0; j < n_tiles && go; ++j) {
                 const int s = j % stages;
                 const uint32_t ph = (uint32_t)(j / stages) & 1u;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort)) {
+                if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort, p.wait_limit)) {
                     flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
                     break;
                 }
                 uint8_t *dst = ring + s * KV_TILE;
+                if (is_k && j == p.stall_tile && j < n_prefix) continue;   // timeout-path test: never loaded
                 if (j < n_prefix) {
                     tc::mbar_expect_tx(&full[s], KV_TILE);
                     const int y = row0 + j * BK;
@@ -300,14 +306,14 @@ __global__ void __launch_bounds__(NT, 1)
             if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             if (is_k && p.qk_rotated) {   // the Q load too (bounded)
                 const long long t0 = clock64();
-                while (!tc::mbar_try(&ss.q_ready, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+                while (!tc::mbar_try(&ss.q_ready, 0) && clock64() - t0 < p.wait_limit) {
                 }
             }
             // no TMA write may be in flight when the CTA exits (bounded)
             for (int s = 0; s < stages; ++s) {
                 if (!((issued >> s) & 1u)) continue;
                 const long long t0 = clock64();
-                while (!tc::mbar_try(&full[s], (last_par >> s) & 1u) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+                while (!tc::mbar_try(&full[s], (last_par >> s) & 1u) && clock64() - t0 < p.wait_limit) {
                 }
             }
         }
@@ -316,16 +322,16 @@ __global__ void __launch_bounds__(NT, 1)
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t IDESC_P = tc::idesc_bf16(MT, BK);
             constexpr uint32_t IDESC_T = tc::idesc_bf16(MT, BKT);
-            bool ok = tc::mbar_wait(&ss.q_ready, 0, abort);   // Q and the tree tile are staged
+            bool ok = tc::mbar_wait(&ss.q_ready, 0, abort, p.wait_limit);   // Q and the tree tile are staged
             const uint32_t qaddr = smem_u32(sm + OFF_Q);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const bool tree = j == n_prefix;
-                if (!tc::mbar_wait(&ss.k_full[j % ST_K], (uint32_t)(j / ST_K) & 1u, abort)) {
+                if (!tc::mbar_wait(&ss.k_full[j % ST_K], (uint32_t)(j / ST_K) & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
                 // buffer j % 3 last held P(j - 3): P V(j - 3) must have read it (another thread issues it)
-                if (j >= NS && !tc::mbar_wait(&ss.pv_done[j % NS], (uint32_t)((j - NS) / NS) & 1u, abort)) {
+                if (j >= NS && !tc::mbar_wait(&ss.pv_done[j % NS], (uint32_t)((j - NS) / NS) & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             tc::mma_commit(&ss.s_done);
             const long long t0 = clock64();
-            while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < p.wait_limit) {
             }
         }
     } else if (warp == 11) {
@@ -356,11 +362,11 @@ __global__ void __launch_bounds__(NT, 1)
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const bool tree = j == n_prefix;
-                if (!tc::mbar_wait(&ss.v_full[j % ST_V], (uint32_t)(j / ST_V) & 1u, abort)) {
+                if (!tc::mbar_wait(&ss.v_full[j % ST_V], (uint32_t)(j / ST_V) & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
-                if (!tc::mbar_wait(&ss.p_full[j % NS], (uint32_t)(j / NS) & 1u, abort)) {
+                if (!tc::mbar_wait(&ss.p_full[j % NS], (uint32_t)(j / NS) & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             tc::mma_commit(&ss.pv_mma_done);
             const long long t0 = clock64();
-            while (!tc::mbar_try(&ss.pv_mma_done, 0) && clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            while (!tc::mbar_try(&ss.pv_mma_done, 0) && clock64() - t0 < p.wait_limit) {
             }
         }
     } else {
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(NT, 1)
         // eight): after a timeout a warp skips its waits and finishes the loop on garbage
         for (int j = 0; j < n_tiles; ++j) {
             const int u = j % NS;
-            if (ok && !warp_wait(&ss.s_full[u], (uint32_t)(j / NS) & 1u, abort)) ok = false;
+            if (ok && !warp_wait(&ss.s_full[u], (uint32_t)(j / NS) & 1u, abort, p.wait_limit)) ok = false;
             tc::fence_after();
             const bool tree = j == n_prefix;             // the last split's final tile
             const int hw = (tree ? BKT : BK) / 2;        // columns of this warp: 64 (prefix) or 32 (tree)
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(NT, 1)
             const bool any_need = __any_sync(0xffffffffu, need);
             if (any_need && j > 0) {
                 // O is about to be rescaled: the previous P V must be finished first
-                if (ok && !warp_wait(&ss.pv_done[(j - 1) % NS], (uint32_t)((j - 1) / NS) & 1u, abort)) ok = false;
+                if (ok && !warp_wait(&ss.pv_done[(j - 1) % NS], (uint32_t)((j - 1) / NS) & 1u, abort, p.wait_limit)) ok = false;
                 tc::fence_after();
             }
             if (any_need) {
@@ -591,7 +597,7 @@ __global__ void __launch_bounds__(NT, 1)
         float o[64];
         bool have = false;
         if (ok && n_tiles > 0 &&
-            warp_wait(&ss.pv_done[(n_tiles - 1) % NS], (uint32_t)((n_tiles - 1) / NS) & 1u, abort)) {
+            warp_wait(&ss.pv_done[(n_tiles - 1) % NS], (uint32_t)((n_tiles - 1) / NS) & 1u, abort, p.wait_limit)) {
             tc::fence_after();
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -904,6 +910,8 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
         !make_tree_map(&mtv, p.v, pt.nb, nk_all, (int64_t)a.Hkv * D, a.v_sb, a.v_si))
         return EAGLE3_ERR_CUDA;
     p.qk_rotated = a.qk_rotated ? 1 : 0;
+    p.stall_tile = a.stall_tile;
+    p.wait_limit = a.wait_limit;
     CUtensorMap mq = mk;   // unused unless Q arrives rotated
     if (p.qk_rotated) {
         if ((a.q_si <= a.q_sb ? 1 : 0) != p.tree_slot_inner) return EAGLE3_ERR_UNSUPPORTED;
@@ -1042,6 +1050,19 @@ extern "C" eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *a
     return tree_attn_launch(verify_launch(a), workspace, ws_bytes, (cudaStream_t)stream);
 }
 
+extern "C" eagle3_status_t eagle3_test_verify_attn_timeout(const eagle3_verify_attn_args_t *a, void *workspace,
+                                                           size_t ws_bytes, int32_t stall_tile,
+                                                           int64_t wait_limit_cycles, eagle3_stream_t stream) {
+    if (stall_tile < 0 || wait_limit_cycles < 1000 || wait_limit_cycles > WAIT_LIMIT_CYCLES)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    const eagle3_status_t st = verify_validate(a);
+    if (st != EAGLE3_OK || a->batch == 0) return st;
+    AttnLaunch l = verify_launch(a);
+    l.stall_tile = stall_tile;
+    l.wait_limit = wait_limit_cycles;
+    return tree_attn_launch(l, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------------------------------------------------
 // eagle3_verify_attn_noalloc: the same attention for callers that cannot allocate device memory
 // (for example a runtime that hands all device memory to its own pool before the first step, or
@@ -1055,18 +1076,41 @@ namespace {
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)32 << 20;   // 32 MiB, held by every device that loads the library
 __device__ __align__(256) uint8_t g_verify_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
-// Host code cannot use the array's name as a device address: look the address up once per device
-// (with that device current) and keep it.
+// Host code cannot use the array's name as a device address: look the address up with the device
+// current and keep it per device, tagged with the CUDA context it belongs to.  A context that was
+// destroyed and recreated (cudaDeviceReset, or the primary context released and retained again)
+// loads the module anew, so the address is looked up again when the current context changes.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CUcontext current_context() {
+    static const CtxGetCurrentFn fn = [] {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return (CtxGetCurrentFn)ptr;
+        return (CtxGetCurrentFn) nullptr;
+    }();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
 void *noalloc_scratch_address() {
     static std::mutex mu;
     static void *addr[128] = {nullptr};
+    static CUcontext owner[128] = {nullptr};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
+    if (!ctx || !addr[dev] || owner[dev] != ctx) {
+        void *p = nullptr;   // the lookup also makes the device's primary context current
         if (cudaGetSymbolAddress(&p, g_verify_noalloc_scratch) != cudaSuccess) return nullptr;
+        ctx = current_context();
+        if (!ctx) return nullptr;
         addr[dev] = p;
+        owner[dev] = ctx;
     }
     return addr[dev];
 }

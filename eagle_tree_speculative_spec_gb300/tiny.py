@@ -189,9 +189,15 @@ def vanilla_greedy(target, prompt, max_new):
     return out
 
 
-def speculative_greedy(target, draft, prompt, max_new, k_draft=4):
+def speculative_greedy(target, draft, prompt, max_new, k_draft=4, propose=None):
     """EAGLE-3 greedy speculative decoding with a chain draft of k_draft tokens.  Returns the
-    generated tokens and the accepted drafts per cycle."""
+    generated tokens and the accepted drafts per cycle.
+
+    propose(n, root, k), when given, returns the k chain tokens to verify in place of the draft's
+    own argmax choices (n = committed positions, root = the token at position n).  The draft head
+    still runs its catch-up and its chain rows on those tokens, so a proposer that agrees with the
+    target exercises accepted drafts, multi-row commits and catch-ups of several rows, which a
+    random-init draft never reaches."""
     dev = target.dev
     P = len(prompt)
     logits, aux, tk, tv = target.forward(prompt, list(range(P)), chain_visible(P), 0)
@@ -214,11 +220,12 @@ def speculative_greedy(target, draft, prompt, max_new, k_draft=4):
         # n + depth - 2 over the draft cache and the chain rows before it (kept in the cache slots
         # after n, which the next catch-up overwrites)
         a_prev = a[-1:].clone()
-        chain = [_argmax(draft.logits(a_prev)[0])]
+        forced = None if propose is None else [int(t) for t in propose(n, root, k_draft)]
+        chain = [_argmax(draft.logits(a_prev)[0]) if forced is None else forced[0]]
         for t in range(2, k_draft + 1):
             row_a, rk, rv = draft.layer([chain[-1]], a_prev, [n + t - 2], [[0]], n + t - 2)
             draft.cache.commit(rk, rv, [0], 1)
-            chain.append(_argmax(draft.logits(row_a)[0]))
+            chain.append(_argmax(draft.logits(row_a)[0]) if forced is None else forced[t - 1])
             a_prev = row_a
         draft.cache.length.copy_(torch.tensor([drafted], dtype=torch.int32))   # drop the chain rows
         # verify [root] + chain at positions n + depth

@@ -231,7 +231,10 @@ eagle3_status_t eagle3_verify_attn(const eagle3_verify_attn_args_t *args, void *
  * 32 MiB scratch array that the library places in device memory (every GPU that loads the library
  * holds it until the process exits).  The call allocates nothing: no cudaMalloc / cudaFree.
  *  - The first call on each device looks up the scratch address (cudaGetSymbolAddress) with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture.  The address is kept per
+ *    device together with the CUDA context it was looked up in; after cudaDeviceReset (or any
+ *    other destruction of that context) the next call looks it up again, so that call too should
+ *    come before any stream capture.
  *  - A split plan that needs more than 32 MiB (batch * n_nodes * n_heads * splits * 520 bytes)
  *    returns EAGLE3_ERR_WORKSPACE before launching; pass a smaller num_splits to fit.
  *  - All calls share the one scratch array: calls that can overlap on the GPU (different streams,

@@ -37,3 +37,22 @@ def close(got, want, atol, rtol):
     want = np.asarray(want, dtype=np.float64)
     err = np.abs(got - want)
     return bool((err <= atol + rtol * np.abs(want)).all()), float(err.max()) if err.size else 0.0
+
+
+def agreeing_proposer(ref, prompt_len, k, vocab, corrupt_every=3):
+    """A stand-in draft that proposes the vanilla greedy continuation ``ref`` (so drafts are
+    accepted), with one position corrupted in every ``corrupt_every``-th cycle (cycles 1, 4, 7, ...
+    corrupt positions 0, 1, 2, ... in turn), so accept lengths cover k and values below it."""
+    cycle = [0]
+
+    def propose(n, root, kk):
+        i = n - prompt_len                   # root is generated token i
+        assert root == ref[i]
+        nxt = [ref[i + 1 + j] if i + 1 + j < len(ref) else 0 for j in range(kk)]
+        c = cycle[0]
+        cycle[0] += 1
+        if c % corrupt_every == 1:
+            pos = (c // corrupt_every) % kk
+            nxt[pos] = (nxt[pos] + 1) % vocab
+        return nxt
+    return propose

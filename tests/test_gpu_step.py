@@ -1,0 +1,291 @@
+"""GPU parity of the composed draft-and-verify step (eagle_tree_speculative_spec_gb300.step) at a
+small bf16 shape: 4 target layers, d = 256, 4 / 2 heads of 128, FFN 512, vocab 1000, aux taps at
+layers {1, 2, 3}, B = 3 sequences with ragged prefixes, 12-node trees (depth 4, top-k 4).
+
+Checked against the oracle ("Advanced speculative decoding: tree drafts and EAGLE", section
+"Implementation": each tree node's logits are those of its path run as a sequence, and only the
+accepted path's K/V is appended; "EAGLE-3: Engineering Implementation of LLM Inference
+Acceleration", sections IX and XI: the aux states entering the tapped layers feed the draft's next
+catch-up):
+* the target's tree logits, the aux taps and every layer's tree K/V (rotated at prefix + depth)
+  against oracle.llama.Llama.forward over the GPU's tree, within the bf16 tolerance;
+* acceptance (greedy and TOPK) bit-exact against oracle.accept on the GPU's own logits;
+* the caches, slot map, prefix lengths and the next step's catch-up inputs after compaction
+  bit-exact against oracle.compact on the GPU's tree K/V.
+Planted acceptance: the tree's tokens along one root-to-leaf chain are replaced, one level at a
+time, by the target's own greedy predictions, so that at least two drafts are accepted and the
+compaction copies several rows; the next step's draft catch-up then runs with T_c > 1 rows, and
+its appended draft K/V are checked against the oracle draft layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import accept as oacc
+from oracle import compact as ocomp
+from oracle import llama as ollama
+from oracle import tree as otree
+from tests._util import close, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+CFG = dict(layers=4, d=256, Hq=4, Hkv=2, D=128, F=512, V=1000, taps=(1, 2, 3), B=3, N=12, depth=4, top_k=4, W=5,
+           temperature=1.0, seed=5, rope_theta=500000.0, eps=1e-5)
+PREFIX = [5, 1, 17]
+ATOL, RTOL = 2e-2, 1e-2
+
+
+def _weights(seed=3):
+    c = CFG
+    tw = synth.llama_weights(seed, c["d"], c["layers"], c["Hq"], c["Hkv"], c["D"], c["F"], c["V"])
+    dw = synth.eagle3_weights(seed, c["d"], c["Hq"], c["Hkv"], c["D"], c["F"], c["V"], embed=tw["embed"])
+    # bf16 rounding: the GPU gets the bf16 tensors, the oracle the same values in fp64
+    t_gpu, t_f = {}, {}
+    for k, v in tw.items():
+        t_gpu[k], t_f[k] = synth.to_bf16(v)
+    d_gpu, d_f = {}, {}
+    for k, v in dw.items():
+        d_gpu[k], d_f[k] = synth.to_bf16(v)
+    return t_gpu, t_f, d_gpu, d_f
+
+
+def _build(dev, mode):
+    from eagle_tree_speculative_spec_gb300 import step as estep
+    c = CFG
+    t_gpu, t_f, d_gpu, d_f = _weights()
+    L = lambda l, n: t_gpu[f"layers.{l}.{n}"].to(dev)
+    target = {"embed": t_gpu["embed"].to(dev), "lm_head": t_gpu["lm_head"].to(dev),
+              "final_norm": t_gpu["final_norm"].to(dev),
+              "wqkv": [torch.cat([L(l, "wq"), L(l, "wk"), L(l, "wv")], 0).contiguous() for l in range(c["layers"])],
+              "wo": [L(l, "wo") for l in range(c["layers"])], "wg": [L(l, "w_gate") for l in range(c["layers"])],
+              "wu": [L(l, "w_up") for l in range(c["layers"])], "wd": [L(l, "w_down") for l in range(c["layers"])],
+              "norm1": [L(l, "attn_norm") for l in range(c["layers"])],
+              "norm2": [L(l, "mlp_norm") for l in range(c["layers"])]}
+    names = {"w_fc": "fc", "embed": "embed", "input_norm": "input_norm", "hidden_norm": "hidden_norm",
+             "w_o": "wo", "post_norm": "post_norm", "w_gate": "w_gate", "w_up": "w_up", "w_down": "w_down",
+             "final_norm": "final_norm", "lm_head": "lm_head"}
+    draft = {g: d_gpu[o].to(dev) for g, o in names.items()}
+    draft["w_qkv"] = torch.cat([d_gpu["wq"], d_gpu["wk"], d_gpu["wv"]], 0).to(dev).contiguous()
+    S = 64
+    st = estep.SpeculativeStep(dict(c, mode=mode), target, draft, S, S - c["N"] - 8, dev)
+    # prefilled caches: N(0, 1) rotated keys / values at positions < prefix; draft cache one shorter
+    r = synth.rng(17, 1)
+    kc = np.zeros((c["layers"], c["B"], c["Hkv"], S, c["D"]), np.float32)
+    vc = np.zeros_like(kc)
+    dk = np.zeros((c["B"], c["Hkv"], S, c["D"]), np.float32)
+    dv = np.zeros_like(dk)
+    for b, Lb in enumerate(PREFIX):
+        kc[:, b, :, :Lb] = r.standard_normal((c["layers"], c["Hkv"], Lb, c["D"]), dtype=np.float32)
+        vc[:, b, :, :Lb] = r.standard_normal((c["layers"], c["Hkv"], Lb, c["D"]), dtype=np.float32)
+        dk[b, :, : Lb - 1] = r.standard_normal((c["Hkv"], Lb - 1, c["D"]), dtype=np.float32)
+        dv[b, :, : Lb - 1] = r.standard_normal((c["Hkv"], Lb - 1, c["D"]), dtype=np.float32)
+    for name, arr in (("k_cache", kc), ("v_cache", vc), ("dk_cache", dk), ("dv_cache", dv)):
+        getattr(st, name).copy_(synth.to_bf16(arr)[0].to(dev))
+    st.prefix_len.copy_(torch.tensor(PREFIX, dtype=torch.int32))
+    st.draft_len.copy_(torch.tensor(PREFIX, dtype=torch.int32) - 1)
+    aux0 = np.zeros((c["B"], c["W"], 3 * c["d"]), np.float32)
+    aux0[:, 0] = r.standard_normal((c["B"], 3 * c["d"]), dtype=np.float32)
+    st.aux_in.copy_(synth.to_bf16(aux0)[0].to(dev))
+    st.next_tok.copy_(torch.as_tensor(r.integers(0, c["V"], (c["B"], c["W"])), dtype=torch.int32))
+    st.tc.fill_(1)
+    st.prepare(ws_linear_bytes=64 << 20, ws_attn_bytes=16 << 20)
+    return st, t_f, d_f
+
+
+STATE = ("k_cache", "v_cache", "dk_cache", "dv_cache", "prefix_len", "draft_len", "aux_in", "next_tok", "tc",
+         "step_counter")
+
+
+def _snapshot(st):
+    return {n: getattr(st, n).clone() for n in STATE}
+
+
+def _restore(st, snap):
+    for n in STATE:
+        getattr(st, n).copy_(snap[n])
+
+
+def _host(st):
+    """Everything the checks read, copied to the host after a step."""
+    c = CFG
+    out = {n: getattr(st, n).cpu() for n in ("tokens", "parents", "depth", "accept_len", "path", "next_root",
+                                              "slot_map", "prefix_len", "tc", "next_tok", "dev_status", "draft_len")}
+    out = {k: v.numpy() for k, v in out.items()}
+    out["logits"] = st.logits.view(c["B"], c["N"], c["V"]).cpu().numpy()
+    out["aux_tree"] = st.aux_tree.view(c["B"], c["N"], -1).float().cpu().numpy()
+    out["aux_in"] = st.aux_in.float().cpu().numpy()
+    out["tree_k"] = np.stack([st.tree_k(l).float().cpu().numpy() for l in range(c["layers"])])
+    out["tree_v"] = np.stack([st.tree_v(l).float().cpu().numpy() for l in range(c["layers"])])
+    for n in ("k_cache", "v_cache", "dk_cache", "dv_cache"):
+        out[n] = getattr(st, n).float().cpu().numpy()
+    return out
+
+
+def _oracle_target(t_f):
+    c = CFG
+    w = {k: v.astype(np.float64) for k, v in t_f.items()}
+    return ollama.Llama(w, c["layers"], c["Hq"], c["Hkv"], c["D"], eps=c["eps"], theta=c["rope_theta"],
+                        aux_layers=c["taps"])
+
+
+def _kv(cache_k, cache_v, b, Lb):
+    """The oracle's per-layer K/V lists of one sequence's cached prefix."""
+    kv = ollama.KV(cache_k.shape[0])
+    for l in range(cache_k.shape[0]):
+        kv.append(l, [cache_k[l, b, :, p].astype(np.float64) for p in range(Lb)],
+                  [cache_v[l, b, :, p].astype(np.float64) for p in range(Lb)])
+    return kv
+
+
+def _check_verify(target, before, g):
+    """Target forward over the GPU's tree (float), acceptance (exact), compaction (exact)."""
+    c = CFG
+    for b in range(c["B"]):
+        Lb = int(before["prefix_len"][b])
+        par = g["parents"][b].tolist()
+        otree.validate(par)
+        assert (g["depth"][b] == otree.depths(par)).all()
+        assert g["tokens"][b, 0] == before["next_tok"][b, before["tc"][b] - 1]       # the root
+        logits, aux, nk, nv = target.forward(g["tokens"][b].tolist(), Lb + otree.depths(par),
+                                             _kv(before["k_cache"], before["v_cache"], b, Lb),
+                                             ollama.tree_visible(par))
+        ok, err = close(g["logits"][b], logits, ATOL, RTOL)
+        assert ok, ("logits", b, err)
+        ok, err = close(g["aux_tree"][b], aux, ATOL, RTOL)
+        assert ok, ("aux taps", b, err)
+        for l in range(c["layers"]):
+            ok, err = close(g["tree_k"][l, b], nk[l], ATOL, RTOL)
+            assert ok, ("tree k", l, b, err)
+            ok, err = close(g["tree_v"][l, b], nv[l], ATOL, RTOL)
+            assert ok, ("tree v", l, b, err)
+
+
+def _check_accept_and_compact(mode, before, g, step):
+    c = CFG
+    B, W = c["B"], c["W"]
+    for b in range(B):
+        res = oacc.accept(mode, g["tokens"][b], g["parents"][b], g["logits"][b], temperature=c["temperature"],
+                          seed=c["seed"], step=step, b=b)
+        path, emitted = oacc.pad(res, W)
+        assert g["accept_len"][b] == res["accept_len"], b
+        assert (g["path"][b] == path).all(), b
+        assert (g["next_tok"][b] == emitted).all(), b
+        assert g["next_root"][b] == res["next_root"], b
+    kref, vref, slot_map, new_len, aux_out = ocomp.compact_kv(
+        before["k_cache"], before["v_cache"], g["tree_k"], g["tree_v"], g["path"], g["accept_len"],
+        before["prefix_len"], W, aux_tree=g["aux_tree"])
+    assert np.array_equal(g["k_cache"], kref) and np.array_equal(g["v_cache"], vref)
+    assert (g["slot_map"] == slot_map).all()
+    assert (g["prefix_len"] == new_len).all()
+    assert (g["tc"] == g["accept_len"] + 1).all()
+    n_rows = g["accept_len"] + 1
+    for b in range(B):
+        assert np.array_equal(g["aux_in"][b, : n_rows[b]], aux_out[b, : n_rows[b]])
+
+
+def _plant_chain(st, snap, greedy_pred):
+    """Rewrite the tokens along the path to the deepest node of each tree so that the target's greedy
+    walk follows it: level by level, the chain node's token := the argmax of its parent's logits,
+    re-verifying after each level (a node's logits depend on its ancestors' tokens only)."""
+    c = CFG
+    parents = st.parents.cpu().numpy()
+    chains = []
+    for b in range(c["B"]):
+        dep = otree.depths(parents[b].tolist())
+        chains.append(otree.path_to(parents[b], int(np.argmax(dep))))      # root .. the deepest node
+    deepest = max(len(ch) for ch in chains)
+    for lvl in range(1, deepest):
+        logits = st.logits.view(c["B"], c["N"], c["V"]).cpu().numpy()
+        tok = st.tokens.cpu().numpy()
+        for b, chain in enumerate(chains):
+            if lvl < len(chain):
+                pred = greedy_pred(logits[b, chain[lvl - 1]])
+                tok[b, chain[lvl]] = pred
+                # a lower-index sibling with the same token would be taken first: give it another one
+                for sib in otree.children(parents[b], chain[lvl - 1]):
+                    if sib < chain[lvl] and tok[b, sib] == pred:
+                        tok[b, sib] = (pred + 1) % c["V"]
+        st.tokens.copy_(torch.as_tensor(tok))
+        _restore(st, snap)
+        st.run(draft=False)
+        torch.cuda.synchronize()
+    return chains
+
+
+@pytest.mark.parametrize("mode_name", ["greedy", "topk"])
+def test_step_matches_oracle(mode_name):
+    from eagle_tree_speculative_spec_gb300 import GREEDY, TOPK
+    dev = require_gpu()
+    mode = {"greedy": GREEDY, "topk": TOPK}[mode_name]
+    st, t_f, _ = _build(dev, mode)
+    target = _oracle_target(t_f)
+    snap0 = _snapshot(st)
+    before = {n: (getattr(st, n).float() if getattr(st, n).dtype == torch.bfloat16 else getattr(st, n)).cpu().numpy()
+              for n in STATE}
+    st.run()
+    torch.cuda.synchronize()
+    g = _host(st)
+    assert g["dev_status"][0] == 0
+    # the draft caught up one row per sequence and built a valid tree
+    assert (g["draft_len"] == np.asarray(PREFIX)).all()
+    _check_verify(target, before, g)
+    _check_accept_and_compact(mode, before, g, step=0)
+
+
+def test_step_with_planted_acceptance_and_catchup():
+    from eagle_tree_speculative_spec_gb300 import GREEDY
+    dev = require_gpu()
+    c = CFG
+    st, t_f, d_f = _build(dev, GREEDY)
+    target = _oracle_target(t_f)
+    st.issue(st.draft_ops)                      # the draft: catch-up row appended, tree built
+    torch.cuda.synchronize()
+    snap = _snapshot(st)                        # every planted re-run of the verify starts here
+    st.run(draft=False)
+    torch.cuda.synchronize()
+    chains = _plant_chain(st, snap, oacc.argmax)
+    before = {n: (snap[n].float() if snap[n].dtype == torch.bfloat16 else snap[n]).cpu().numpy() for n in STATE}
+    _restore(st, snap)
+    st.run(draft=False)
+    torch.cuda.synchronize()
+    g = _host(st)
+    assert g["dev_status"][0] == 0
+    for b, chain in enumerate(chains):
+        assert g["accept_len"][b] >= len(chain) - 1 >= 2, (b, g["accept_len"][b], chain)
+    _check_verify(target, before, g)
+    _check_accept_and_compact(GREEDY, before, g, step=0)
+
+    # next step: the draft catches up the committed rows (T_c = accepted + 1 > 1) from the aux rows
+    # and tokens the compaction gathered; its appended K/V against the oracle draft layer
+    dk_before = st.dk_cache.float().cpu().numpy()
+    dv_before = st.dv_cache.float().cpu().numpy()
+    dl_before = st.draft_len.cpu().numpy().copy()
+    tc = st.tc.cpu().numpy().copy()
+    aux_rows = st.aux_in.float().cpu().numpy()
+    cu_tok = st.next_tok.cpu().numpy().copy()
+    st.run()
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) == 0
+    dl_after = st.draft_len.cpu().numpy()
+    assert (dl_after == dl_before + tc).all()
+    dk_after = st.dk_cache.float().cpu().numpy()
+    dv_after = st.dv_cache.float().cpu().numpy()
+    w = {k: v.astype(np.float64) for k, v in d_f.items()}
+    draft = ollama.Eagle3Draft(w, c["Hq"], c["Hkv"], c["D"], eps=c["eps"], theta=c["rope_theta"])
+    for b in range(c["B"]):
+        n, L0 = int(tc[b]), int(dl_before[b])
+        assert n >= 3
+        kv = ollama.KV(1)
+        kv.append(0, [dk_before[b, :, p].astype(np.float64) for p in range(L0)],
+                  [dv_before[b, :, p].astype(np.float64) for p in range(L0)])
+        g_rows = draft.fuse(aux_rows[b, :n])
+        _, k, v = draft.layer(cu_tok[b, :n].tolist(), g_rows, np.arange(L0, L0 + n), kv, ollama.chain_visible(n))
+        ok, err = close(dk_after[b, :, L0:L0 + n].transpose(1, 0, 2), k, ATOL, RTOL)
+        assert ok, ("draft k", b, err)
+        ok, err = close(dv_after[b, :, L0:L0 + n].transpose(1, 0, 2), v, ATOL, RTOL)
+        assert ok, ("draft v", b, err)
+        # rows before the catch-up are untouched
+        assert np.array_equal(dk_after[b, :, :L0], dk_before[b, :, :L0])
+    # the new tree's root is the previous step's correction / bonus token
+    assert (st.tokens[:, 0].cpu().numpy() == cu_tok[np.arange(c["B"]), tc - 1]).all()

@@ -8,7 +8,7 @@ import torch
 
 import synth
 from oracle import llama
-from tests._util import require_gpu
+from tests._util import agreeing_proposer, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -57,3 +57,23 @@ def test_tiny_speculative_equals_vanilla_and_oracle(prompt_seed):
     ot = llama.Llama(tw, cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
                      aux_layers=synth.TINY_AUX_LAYERS)
     assert vanilla == llama.vanilla_greedy(ot, prompt, 64)
+
+
+def test_tiny_speculative_with_accepted_drafts():
+    """The same losslessness check with drafts that are accepted: a proposer that follows vanilla
+    greedy (with a planted mismatch every third cycle) drives full acceptance of all 4 drafts and
+    partial acceptance, so the GPU path runs multi-row commits, catch-ups of several rows and the
+    draft-cache rollback after an accepted chain; the output still equals vanilla greedy."""
+    from eagle_tree_speculative_spec_gb300 import tiny
+    dev = require_gpu()
+    cfg, tw, dw = _weights()
+    prompt = synth.tiny_prompt(0)
+    vanilla = tiny.vanilla_greedy(_target(cfg, tw, dev), prompt, 64)
+    ot = llama.Llama(tw, cfg["n_layers"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"],
+                     aux_layers=synth.TINY_AUX_LAYERS)
+    assert vanilla == llama.vanilla_greedy(ot, prompt, 64)
+    propose = agreeing_proposer(vanilla, len(prompt), 4, cfg["vocab"])
+    draft = tiny.TinyDraft(dw, cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], 160, dev)
+    spec, accepted = tiny.speculative_greedy(_target(cfg, tw, dev), draft, prompt, 64, k_draft=4, propose=propose)
+    assert spec == vanilla
+    assert 4 in accepted and any(1 <= a <= 3 for a in accepted), accepted

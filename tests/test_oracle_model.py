@@ -8,6 +8,7 @@ import synth
 from oracle import attention as att
 from oracle import draft_tree, llama, tree
 from oracle.accept import order_key
+from tests._util import agreeing_proposer
 
 
 # ----------------------------------------------------------------------------- RoPE / attention
@@ -144,6 +145,39 @@ def test_greedy_speculative_equals_vanilla_tree():
     ref = llama.vanilla_greedy(target, prompt, 24)
     out, _ = llama.speculative_greedy(target, draft, prompt, 24, _builder(3, 3, 10))
     assert out == ref
+
+
+def _proposal_builder(propose, k, siblings=False):
+    """build_tree for the oracle loop from a proposer: the proposal as a chain under the root and,
+    with siblings, one extra child per level carrying another token (a tree whose accepted path is
+    one of several branches)."""
+    def build(draft, d_cache, a_last, root, L):
+        chain = propose(L, root, k)
+        tokens, parents = [root] + chain, [-1] + list(range(k))
+        if siblings:
+            for j in range(1, k + 1):
+                tokens.append((chain[j - 1] + 17) % draft.w["lm_head"].shape[0])
+                parents.append(j - 1)
+        return tokens, parents
+    return build
+
+
+@pytest.mark.parametrize("siblings", [False, True])
+def test_greedy_speculative_equals_vanilla_with_accepted_drafts(siblings):
+    """Losslessness with drafts that are accepted: a proposer that follows vanilla greedy (with
+    planted mismatches) drives accept lengths of 4 and of 1-3, multi-row commits and catch-ups of
+    several rows ("EAGLE-3: Engineering Implementation of LLM Inference Acceleration", section XI.6:
+    the kept positions are caught up by the draft, the rest of the draft is rolled back); the
+    output still equals vanilla greedy token for token."""
+    target, draft = _tiny()
+    prompt = synth.tiny_prompt(0)
+    ref = llama.vanilla_greedy(target, prompt, 64)
+    V = synth.TINY["vocab"]
+    propose = agreeing_proposer(ref, len(prompt), 4, V)
+    out, accepted = llama.speculative_greedy(target, draft, prompt, 64, _proposal_builder(propose, 4, siblings))
+    assert out == ref
+    assert 4 in accepted and any(1 <= a <= 3 for a in accepted), accepted
+    assert sum(accepted) + len(accepted) >= 64 - 1
 
 
 def _tree_vs_paths(target, prompt, parents, tokens, visible):
