@@ -260,8 +260,10 @@ template <int NT> struct TopkSmem {
 };
 
 // Top-k candidates of the slice [lo, hi) of row z into sm.fin (sorted, KMAX entries, the first k
-// meaningful; 0 = none).
-template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int lo, int hi, int k) {
+// meaningful; 0 = none) and, in the same pass over the slice, its fixed-point normaliser terms with
+// m = the row maximum (known beforehand: the LM head's epilogue published it): the CTA's sum is
+// returned (valid in thread 0).
+template <int NT> E3_DEV uint64_t topk_slice(TopkSmem<NT> &sm, const float *z, int lo, int hi, int k, float m) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
     if (lane < KMAX) sm.wres[warp][lane] = 0ull;
@@ -269,6 +271,7 @@ template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int l
     uint64_t tau = 0ull;             // packed key of the warp's k-th best so far (0: fewer than k)
     float tau_f = key_to_float(0u);  // a NaN: every value passes `!(v < tau_f)`
     int cnt = 0;                     // warp-uniform fill of buf[warp]
+    uint64_t s = 0;                  // normaliser terms of this thread's elements
     auto flush = [&]() {
         tau = warp_flush(sm.wres[warp], sm.buf[warp], cnt, k, lane);
         tau_f = key_to_float((uint32_t)(tau >> 32));
@@ -282,9 +285,9 @@ template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int l
             key = pack_argmax(v, idx);
             pass = key > tau;
         }
-        const uint32_t m = __ballot_sync(0xffffffffu, pass);
-        if (pass) sm.buf[warp][cnt + __popc(m & lt_mask)] = key;
-        cnt += __popc(m);
+        const uint32_t msk = __ballot_sync(0xffffffffu, pass);
+        if (pass) sm.buf[warp][cnt + __popc(msk & lt_mask)] = key;
+        cnt += __popc(msk);
     };
     const float *zs = z + lo;
     const int n = hi - lo;
@@ -298,6 +301,9 @@ template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int l
         for (int u = 0; u < U; ++u) v[u] = __ldg(reinterpret_cast<const float4 *>(zs) + j0 + u * NT);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            // each weight is up to 2^31: widen before adding
+            const uint2 w01 = dsm_weight_pair(v[u].x, v[u].y, m, 1.0f), w23 = dsm_weight_pair(v[u].z, v[u].w, m, 1.0f);
+            s += ((uint64_t)w01.x + w01.y) + ((uint64_t)w23.x + w23.y);
             // some element is not below the threshold <=> their maximum is not (a NaN propagates, and
             // passes, as it does element by element)
             const bool any = !(max4_nan(v[u]) < tau_f);
@@ -315,10 +321,14 @@ template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int l
         const int i = base + threadIdx.x;
         const bool valid = i < n;
         const float v = valid ? __ldg(zs + i) : 0.0f;
+        if (valid) s += dsm_weight(dsm_scaled(v, m, 1.0f));
         if (cnt + 32 > TK_CAP) flush();
         offer(v, (uint32_t)(lo + i), valid);
     }
     if (cnt > 0) flush();
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) sm.sred[warp] = s;
     __syncthreads();
     if (warp == 0) {
         uint64_t best[KMAX], res[KMAX];
@@ -329,33 +339,10 @@ template <int NT> E3_DEV void topk_slice(TopkSmem<NT> &sm, const float *z, int l
 #pragma unroll
             for (int q = 0; q < KMAX; ++q) sm.fin[q] = res[q];
     }
-    __syncthreads();
-}
-
-// Fixed-point normaliser terms of the slice [lo, hi) of row z with m = the row maximum: the CTA's
-// sum (valid in thread 0)
-template <int NT> E3_DEV uint64_t normaliser_slice(TopkSmem<NT> &sm, const float *z, int lo, int hi, float m) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float *zs = z + lo;
-    const int n = hi - lo;
-    const bool vec = ((((uintptr_t)zs) & 15) == 0);
-    const int n4 = vec ? n / 4 : 0;
-    uint64_t s = 0;
-#pragma unroll 4
-    for (int j = threadIdx.x; j < n4; j += NT) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(zs) + j);
-        // each weight is up to 2^31: widen before adding
-        const uint2 w01 = dsm_weight_pair(v.x, v.y, m, 1.0f), w23 = dsm_weight_pair(v.z, v.w, m, 1.0f);
-        s += ((uint64_t)w01.x + w01.y) + ((uint64_t)w23.x + w23.y);
-    }
-    for (int i = 4 * n4 + threadIdx.x; i < n; i += NT) s += dsm_weight(dsm_scaled(__ldg(zs + i), m, 1.0f));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sm.sred[warp] = s;
-    __syncthreads();
     uint64_t S = 0;
     if (threadIdx.x == 0)
         for (int w = 0; w < NT / 32; ++w) S += sm.sred[w];
+    __syncthreads();
     return S;
 }
 
@@ -384,16 +371,16 @@ E3_DEV void topk_write(const uint64_t *fin, uint64_t S, float m, int row, int V,
     }
 }
 
-// One CTA of NT threads per row (many rows).
+// One CTA of NT threads per row (many rows).  row_max[row] holds the order key of the row's maximum.
 template <int NT>
-__global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t ld, int V, int k, const TopkOut o) {
+__global__ void __launch_bounds__(NT)
+    topk_kernel(const float *logits, int64_t ld, int V, int k, const uint32_t *row_max, const TopkOut o) {
     __shared__ TopkSmem<NT> sm;
+    __shared__ uint64_t S;
     const int row = blockIdx.x;
     const float *z = logits + (size_t)row * ld;
-    topk_slice(sm, z, 0, V, k);
-    const float m = key_to_float((uint32_t)(sm.fin[0] >> 32));
-    __shared__ uint64_t S;
-    const uint64_t s = normaliser_slice(sm, z, 0, V, m);
+    const float m = key_to_float(__ldg(row_max + row));
+    const uint64_t s = topk_slice(sm, z, 0, V, k, m);
     if (threadIdx.x == 0) S = s;
     __syncthreads();
     topk_write(sm.fin, S, m, row, V, k, o);
@@ -403,7 +390,7 @@ __global__ void __launch_bounds__(NT) topk_kernel(const float *logits, int64_t l
 // normaliser sums are combined through distributed shared memory in rank order.
 constexpr int TOPK_CL = 8;
 __global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
-    topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, const TopkOut o) {
+    topk_cluster_kernel(const float *logits, int64_t ld, int V, int k, const uint32_t *row_max, const TopkOut o) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ TopkSmem<NT_TOPK> sm;
@@ -411,26 +398,23 @@ __global__ void __cluster_dims__(TOPK_CL, 1, 1) __launch_bounds__(NT_TOPK)
     const int rank = (int)cluster.block_rank(), row = blockIdx.x / TOPK_CL;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float *z = logits + (size_t)row * ld;
+    const float m = key_to_float(__ldg(row_max + row));
     const int slice = ((V + TOPK_CL - 1) / TOPK_CL + 3) / 4 * 4;   // a multiple of 4 elements
     const int lo = min(V, rank * slice), hi = min(V, lo + slice);
-    topk_slice(sm, z, lo, hi, k);
-    cluster.sync();
-    if (warp == 0) {
-        uint64_t best[KMAX], res[KMAX];
-        const uint64_t *src = cluster.map_shared_rank(sm.fin, lane < TOPK_CL ? lane : 0);
-#pragma unroll
-        for (int q = 0; q < KMAX; ++q) best[q] = lane < TOPK_CL ? src[q] : 0ull;
-        warp_merge(best, res, k);
-        if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < KMAX; ++q) fin_all[q] = res[q];
-    }
-    __syncthreads();
-    const float m = key_to_float((uint32_t)(fin_all[0] >> 32));
-    const uint64_t s = normaliser_slice(sm, z, lo, hi, m);
+    const uint64_t s = topk_slice(sm, z, lo, hi, k, m);
     if (threadIdx.x == 0) sm.s_cta = s;
     cluster.sync();
     if (rank == 0) {
+        if (warp == 0) {
+            uint64_t best[KMAX], res[KMAX];
+            const uint64_t *src = cluster.map_shared_rank(sm.fin, lane < TOPK_CL ? lane : 0);
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) best[q] = lane < TOPK_CL ? src[q] : 0ull;
+            warp_merge(best, res, k);
+            if (lane == 0)
+#pragma unroll
+                for (int q = 0; q < KMAX; ++q) fin_all[q] = res[q];
+        }
         __shared__ uint64_t S;
         if (threadIdx.x == 0) {
             uint64_t t = 0;
@@ -736,6 +720,7 @@ eagle3_linear_args_t lin(int m, int n, int k, int epi, const void *x, const void
 struct Plan {
     Layout lay;
     size_t o_g, o_a2k, o_xres, o_qkvc, o_pool, o_attn, o_x1, o_h, o_act, o_abuf, o_nrm, o_logits, o_ttok, o_tlq;
+    size_t o_rmax;   // [depth][lm_rows] row-maximum keys of each LM-head call (zeroed at the call's start)
     size_t o_cs, o_ct, o_cp, o_cd, o_ncand, o_front, o_rtok, o_rx, o_panc, o_ppos, o_canc, o_cpos, o_root, o_gws,
         o_aws;
     size_t gws, aws;
@@ -836,6 +821,7 @@ Plan make_plan(const Dims &m, const eagle3_draft_tree_args_t *a) {
     pl.o_logits = L.add(a->dbg_logits ? 16 : (size_t)m.lm_rows * m.Vd * 4);
     pl.o_ttok = L.add((size_t)m.lm_rows * m.K * 4);
     pl.o_tlq = L.add((size_t)m.lm_rows * m.K * 4);
+    pl.o_rmax = L.add((size_t)m.depth * m.lm_rows * 4);
     pl.o_cs = L.add((size_t)m.B * m.maxc * 4);
     pl.o_ct = L.add((size_t)m.B * m.maxc * 4);
     pl.o_cp = L.add((size_t)m.B * m.maxc * 4);
@@ -924,6 +910,8 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
     np.ld_tap = 0;
     np.dev_status = a->dev_status;
 
+    // row-maximum words of every LM-head call start at zero (below every order key but a negative NaN's)
+    if (cudaMemsetAsync(P(pl.o_rmax), 0, (size_t)m.depth * m.lm_rows * 4, st) != cudaSuccess) return EAGLE3_ERR_CUDA;
     // ---------------------------------------------------------------- catch-up rows
     catchup_meta_kernel<<<B, 64, 0, st>>>(B, m.tc_max, a->draft_len, a->tc, (uint64_t *)P(pl.o_canc),
                                           (int32_t *)P(pl.o_cpos), (int32_t *)P(pl.o_root), a->dev_status);
@@ -973,7 +961,8 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
                                       nullptr, a->dev_status);
         return eagle3_linear(&l3, gws, pl.gws, stream_);
     };
-    auto lm_head = [&](int rows, const __nv_bfloat16 *a_rows, const int32_t *gather, float *logits) -> eagle3_status_t {
+    auto lm_head = [&](int rows, const __nv_bfloat16 *a_rows, const int32_t *gather, float *logits,
+                       int depth_t) -> eagle3_status_t {
         NormParams n3 = np;
         n3.rows = rows;
         n3.n_src = gather ? m.Rc : rows;
@@ -986,6 +975,9 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         E3_LAUNCHED();
         eagle3_linear_args_t l = lin(rows, m.Vd, d, EAGLE3_EPI_F32, P(pl.o_nrm), W->lm_head, logits, nullptr, nullptr,
                                      a->dev_status);
+        // the epilogue publishes each row's maximum, so the top-k reads the logits once
+        uint32_t *rmax = (uint32_t *)P(pl.o_rmax) + (size_t)(depth_t - 1) * m.lm_rows;
+        l.row_max = rmax;
         E3_TRY(eagle3_linear(&l, gws, pl.gws, stream_));
         // few rows: a cluster per row, so that the scan of the vocabulary is spread over the SMs;
         // more rows than one wave of NT_TOPK-thread CTAs holds: narrower CTAs, so that all rows are
@@ -1001,11 +993,11 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         const int wave = sms * per_sm;
         const TopkOut o = {(int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq), a->d2t, m.V, a->dev_status};
         if ((int64_t)rows * TOPK_CL <= 2LL * sms)
-            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, o);
+            topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
         else if (rows <= wave)
-            topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, o);
+            topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
         else
-            topk_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, 0, st>>>(logits, m.Vd, m.Vd, K, o);
+            topk_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
         E3_LAUNCHED();
         return EAGLE3_OK;
     };
@@ -1021,7 +1013,7 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
                                             (__nv_bfloat16 *)a->draft_v_cache, a->draft_len, a->tc, m.max_len,
                                             a->dev_status);
         E3_LAUNCHED();
-        E3_TRY(lm_head(B, abuf, (const int32_t *)P(pl.o_root), logits_base));
+        E3_TRY(lm_head(B, abuf, (const int32_t *)P(pl.o_root), logits_base, 1));
     }
 
     Tree T;
@@ -1077,7 +1069,7 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         __nv_bfloat16 *a_rows = abuf + (size_t)(m.Rc + (t - 2) * rows) * d;
         E3_TRY(layer_tail(rows, P(pl.o_xres), a_rows));
         float *logits = logits_base + (a->dbg_logits ? (size_t)(t - 1) * rows * m.Vd : 0);
-        E3_TRY(lm_head(rows, a_rows, nullptr, logits));
+        E3_TRY(lm_head(rows, a_rows, nullptr, logits, t));
         select_step_kernel<<<B, 256, 0, st>>>(T, t);
         E3_LAUNCHED();
     }

@@ -62,7 +62,16 @@ struct GemmParams {
     int rope_cols, rope_rows;
     const int32_t *rope_base, *rope_depth;
     float rope_inv[64];              // theta^(-2j/128), computed in double, rounded to float
+    uint32_t *row_max;               // F32: [M] atomic max of each row's output order keys, or null
 };
+
+// Order key of each of 32 outputs at columns col0.. (those < N), folded into a running maximum.
+E3_DEV uint32_t chunk_max_key(uint32_t run, const float (&v)[32], int col0, int N) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (col0 + i < N) run = max(run, order_key(v[i]));
+    return run;
+}
 
 // One piece of work of a CTA: k-blocks [kb0, kb1) of output tile (mb, nb).
 enum { IT_FULL = 0, IT_SPLITK = 1, IT_CONTRIB = 2, IT_OWNER = 3 };
@@ -495,6 +504,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float rope_pos = 0.0f;
                 if (rope_epi && row < p.M) rope_pos = (float)(p.rope_base[row / p.rope_rows] + p.rope_depth[row]);
                 uint4 u_hi[8];                // the second half of a rotated head, for the next chunk
+                uint32_t rmax = 0u;           // F32 with row_max: this row's largest output key in the tile
                 for (int sc = 0; sc < chunks; ++sc) {
                     if (res && sc + 1 < chunks) load_residual(p, row, nb * BN + (sc + 1) * 64, r_next);
                     uint4 u[8];
@@ -530,6 +540,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         float v[32];
                         tc::tmem_ld32(t_row + sc * 32, v);
                         add_contrib(v, sc * 32);
+                        if (p.row_max) rmax = chunk_max_key(rmax, v, nb * BN + sc * 32, p.N);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             u[j] = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
@@ -586,13 +597,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         for (int j = 0; j < 8; ++j) r_cur[j] = r_next[j];
                     }
                 }
+                if (p.row_max && row < p.M && rmax) atomicMax(p.row_max + row, rmax);
             } else if (!swiglu) {
+                uint32_t rmax = 0u;
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tc::tmem_ld32(t_row + c * 32, v);
                     add_contrib(v, c * 32);
+                    if (p.row_max) rmax = chunk_max_key(rmax, v, nb * BN + c * 32, p.N);
                     store_chunk(p, row, nb * BN + c * 32, v);
                 }
+                if (p.row_max && row < p.M && rmax) atomicMax(p.row_max + row, rmax);
             } else {
                 for (int c = 0; c < BN / 64; ++c) {
                     float g[32], u[32];
@@ -626,37 +641,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-// Split-K reduction in split order, then the epilogue.  One thread per output element pair.
+// Row maxima of a warp's 32 consecutive outputs (which may span several rows): one atomic max per
+// distinct row, from the lowest lane holding it.  All lanes of the warp call this together.
+E3_DEV void warp_row_max(uint32_t *row_max, int row, uint32_t key, bool valid) {
+    uint32_t pending = __ballot_sync(0xffffffffu, valid);
+    const int lane = threadIdx.x & 31;
+    while (pending) {
+        const int lead = __ffs(pending) - 1;
+        const int r = __shfl_sync(0xffffffffu, row, lead);
+        const bool mine = valid && row == r;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, mine ? key : 0u);
+        if (lane == lead && m) atomicMax(row_max + r, m);
+        pending &= ~__ballot_sync(0xffffffffu, mine);
+    }
+}
+
+// Split-K reduction in split order, then the epilogue.  One thread per output element.
 __global__ void gemm_reduce_kernel(const GemmParams p) {
     pdl_wait();
     pdl_trigger();
     const int n_out = p.N;
     const size_t total = (size_t)p.M * n_out;
-    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
-        const int row = (int)(idx / n_out), col = (int)(idx % n_out);
-        float acc, acc2 = 0.0f;
-        if (p.epi == EAGLE3_EPI_SWIGLU) {
-            // accumulator tile nb holds [gate cols | up cols], BN/2 output columns each
-            const int half = p.n_acc / p.tiles_n / 2;
-            const int nb = col / half, j = col % half;
-            const size_t cg = (size_t)nb * 2 * half + j, cu = cg + half;
-            acc = 0.0f;
-            for (int s = 0; s < p.splits; ++s) {
-                const float *w = p.ws + ((size_t)s * p.M + row) * p.n_acc;
-                acc += w[cg];
-                acc2 += w[cu];
+    const size_t stride = (size_t)gridDim.x * blockDim.x;   // a multiple of 32: the loop is warp-uniform
+    const int lane = threadIdx.x & 31;
+    for (size_t base = (size_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total; base += stride) {
+        const size_t idx = base + lane;
+        const bool valid = idx < total;
+        const int row = valid ? (int)(idx / n_out) : 0, col = valid ? (int)(idx % n_out) : 0;
+        uint32_t key = 0u;
+        if (valid) {
+            float acc, acc2 = 0.0f;
+            if (p.epi == EAGLE3_EPI_SWIGLU) {
+                // accumulator tile nb holds [gate cols | up cols], BN/2 output columns each
+                const int half = p.n_acc / p.tiles_n / 2;
+                const int nb = col / half, j = col % half;
+                const size_t cg = (size_t)nb * 2 * half + j, cu = cg + half;
+                acc = 0.0f;
+                for (int s = 0; s < p.splits; ++s) {
+                    const float *w = p.ws + ((size_t)s * p.M + row) * p.n_acc;
+                    acc += w[cg];
+                    acc2 += w[cu];
+                }
+                acc = silu(acc) * acc2;
+            } else {
+                acc = 0.0f;
+                for (int s = 0; s < p.splits; ++s) acc += p.ws[((size_t)s * p.M + row) * p.n_acc + col];
             }
-            acc = silu(acc) * acc2;
-        } else {
-            acc = 0.0f;
-            for (int s = 0; s < p.splits; ++s) acc += p.ws[((size_t)s * p.M + row) * p.n_acc + col];
+            if (p.epi == EAGLE3_EPI_F32) {
+                ((float *)p.out)[(size_t)row * p.ld_out + col] = acc;
+                key = order_key(acc);
+            } else {
+                if (p.epi == EAGLE3_EPI_BF16_RESIDUAL) acc += __bfloat162float(p.residual[(size_t)row * p.ld_res + col]);
+                ((__nv_bfloat16 *)p.out)[(size_t)row * p.ld_out + col] = __float2bfloat16_rn(acc);
+            }
         }
-        if (p.epi == EAGLE3_EPI_F32) {
-            ((float *)p.out)[(size_t)row * p.ld_out + col] = acc;
-        } else {
-            if (p.epi == EAGLE3_EPI_BF16_RESIDUAL) acc += __bfloat162float(p.residual[(size_t)row * p.ld_res + col]);
-            ((__nv_bfloat16 *)p.out)[(size_t)row * p.ld_out + col] = __float2bfloat16_rn(acc);
-        }
+        if (p.row_max) warp_row_max(p.row_max, row, key, valid);   // every lane of the warp, one call site
     }
 }
 
@@ -785,6 +824,7 @@ eagle3_status_t validate(const eagle3_linear_args_t *a) {
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->epilogue == EAGLE3_EPI_SWIGLU && !a->w2) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->epilogue == EAGLE3_EPI_BF16_RESIDUAL && !a->residual) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->row_max && (a->epilogue != EAGLE3_EPI_F32 || ((uintptr_t)a->row_max & 3))) return EAGLE3_ERR_INVALID_ARGUMENT;
     const int64_t ld_x = a->ld_x ? a->ld_x : a->k, ld_w = a->ld_w ? a->ld_w : a->k;
     if (ld_x < a->k || ld_w < a->k || (ld_x % 8) || (ld_w % 8)) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)a->x | (uintptr_t)a->w | (uintptr_t)a->w2) & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
@@ -847,6 +887,7 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.rope_rows = a->rope_rows_per_seq > 0 ? a->rope_rows_per_seq : 1;
     p.rope_base = a->rope_base;
     p.rope_depth = a->rope_depth;
+    p.row_max = a->epilogue == EAGLE3_EPI_F32 ? a->row_max : nullptr;
     for (int j = 0; j < 64; ++j)
         p.rope_inv[j] = p.rope_cols ? (float)std::pow((double)a->rope_theta, -2.0 * j / 128.0) : 0.0f;
     CUtensorMap mo;

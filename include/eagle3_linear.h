@@ -65,6 +65,12 @@ typedef struct {
     float rope_theta;           /* > 0                                                            */
     const int32_t *rope_base;   /* [ceil(m / rope_rows_per_seq)] base position per sequence        */
     const int32_t *rope_depth;  /* [m] offset per row                                             */
+    /* F32 only (NULL otherwise): [m] row-maximum words.  Each is raised (atomic max) to the order
+       key of the largest output of its row, so a reader of the row (e.g. a top-k with a
+       normaliser that subtracts the row maximum) needs no pass of its own to find it.  The order key
+       of x maps its fp32 bit pattern b to b ^ 0x80000000 for x >= 0 (sign bit clear) and to ~b
+       otherwise, so unsigned order is float order.  The caller sets the words to 0 beforehand.   */
+    uint32_t *row_max;
 } eagle3_linear_args_t;
 
 size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *args);

@@ -172,3 +172,28 @@ def test_linear_rope_epilogue_padded_pitch():
     want[:, :256] = oatt.rope_apply(want[:, :256].reshape(m, 2, 128), pos, 10000.0).reshape(m, 256)
     ok, err = close(got[:, :n], want, 2e-2, 1e-2)
     assert ok, f"max err {err}"
+
+
+@pytest.mark.parametrize("m,n,k,splits", [
+    (10, 128256, 4096, 0),    # one M tile, many N tiles: stream-K (owners finish the cut tiles)
+    (10, 32000, 4096, 0),     # one M tile, few N tiles: split-K (the reduce kernel writes the outputs)
+    (640, 128256, 512, 0),    # many tiles: data-parallel, TMA-stored
+    (130, 1001, 256, 0),      # unaligned row pitch: direct stores
+    (33, 300, 512, 3)])       # forced split-K, rows spanning a warp's outputs
+def test_linear_f32_row_max(m, n, k, splits):
+    """The fp32 epilogue's row maxima: each row's word ends at the order key of the row's largest
+    output (bit-exact against the maximum of the outputs the same call wrote), however the plan
+    finishes the tiles."""
+    from eagle_tree_speculative_spec_gb300 import EPI_F32, eagle3_linear
+    dev = require_gpu()
+    x, w, _ = _inputs(m, n, k, 11)
+    out = torch.full((m, n), float("nan"), dtype=torch.float32, device=dev)
+    rmax = torch.zeros(m, dtype=torch.int32, device=dev)
+    eagle3_linear(x.to(dev), w.to(dev), out, epilogue=EPI_F32, splits=splits, row_max=rmax)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    bits = got.view(np.uint32).astype(np.uint64)
+    keys = np.where(bits >> 31, ~bits & 0xFFFFFFFF, bits | 0x80000000)
+    assert np.array_equal(rmax.cpu().numpy().view(np.uint32).astype(np.uint64), keys.max(1))
+    ok, err = close(got, _ref(x, w), 1e-3, 1e-3)
+    assert ok, err
