@@ -56,7 +56,8 @@ class CompactArgs(ctypes.Structure):
                 ("cache_layer_stride", _i64), ("tree_layer_stride", _i64), ("tree_node_stride", _i64),
                 ("k_cache", _p), ("v_cache", _p), ("tree_k", _p), ("tree_v", _p),
                 ("path", _p), ("accept_len", _p), ("prefix_len", _p), ("slot_map", _p), ("committed", _p),
-                ("aux_dim", _i32), ("aux_tree", _p), ("aux_out", _p), ("dev_status", _p)]
+                ("aux_dim", _i32), ("aux_tree", _p), ("aux_out", _p), ("dev_status", _p),
+                ("block_table", _p), ("max_blocks", _i32), ("block_size", _i32), ("n_slots", _i32)]
 
 
 class VerifyAttnArgs(ctypes.Structure):
@@ -65,7 +66,8 @@ class VerifyAttnArgs(ctypes.Structure):
                 ("q_node_stride", _i64), ("kv_node_stride", _i64), ("rope_theta", _f32), ("sm_scale", _f32),
                 ("q", _p), ("tree_k", _p), ("tree_v", _p), ("k_cache", _p), ("v_cache", _p),
                 ("parents", _p), ("prefix_len", _p), ("out", _p), ("lse", _p), ("dev_status", _p),
-                ("qk_rotated", _i32)]
+                ("qk_rotated", _i32), ("block_table", _p), ("max_blocks", _i32), ("block_size", _i32),
+                ("n_slots", _i32)]
 
 
 class LinearArgs(ctypes.Structure):
@@ -73,10 +75,30 @@ class LinearArgs(ctypes.Structure):
                 ("ld_x", _i64), ("ld_w", _i64), ("ld_out", _i64), ("ld_res", _i64),
                 ("x", _p), ("w", _p), ("w2", _p), ("out", _p), ("residual", _p), ("dev_status", _p),
                 ("rope_cols", _i32), ("rope_rows_per_seq", _i32), ("rope_theta", ctypes.c_float),
-                ("rope_base", _p), ("rope_depth", _p)]
+                ("rope_base", _p), ("rope_depth", _p), ("row_max", _p)]
 
 
 EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU, EPI_BF16_ROPE = 0, 1, 2, 3, 4
+DEV_BAD_COUNTS = 0x20
+
+
+class SpecDecodeMetadataArgs(ctypes.Structure):
+    _fields_ = [("n_requests", _i32), ("max_rows", _i32), ("cu_num_scheduled_tokens", _p), ("num_draft_tokens", _p),
+                ("cu_num_draft_tokens", _p), ("logits_indices", _p), ("target_logits_indices", _p),
+                ("bonus_logits_indices", _p), ("num_rows", _p), ("dev_status", _p)]
+
+
+class TttAttnArgs(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("seq_len", _i32), ("n_heads", _i32), ("n_kv_heads", _i32), ("head_dim", _i32),
+                ("n_steps", _i32), ("sm_scale", _f32), ("q", _p), ("k", _p), ("v", _p), ("out", _p),
+                ("dev_status", _p)]
+
+
+class ChainVerifyArgs(ctypes.Structure):
+    _fields_ = [("n_requests", _i32), ("vocab", _i32), ("max_drafts", _i32), ("temperature", _f32),
+                ("seed", _u64), ("step", _u64), ("logits", _p), ("draft_tokens", _p), ("cu_num_draft_tokens", _p),
+                ("is_greedy", _p), ("output_tokens", _p), ("num_accepted", _p), ("dev_status", _p),
+                ("step_counter", _p)]
 
 DRAFT_WEIGHT_NAMES = ("w_fc", "embed", "input_norm", "hidden_norm", "w_qkv", "w_o", "post_norm", "w_gate",
                       "w_up", "w_down", "final_norm", "lm_head")
@@ -130,6 +152,14 @@ def _declare(L):
     L.eagle3_verify_attn_workspace_size.argtypes = [P(VerifyAttnArgs)]
     L.eagle3_verify_attn.restype = ctypes.c_int
     L.eagle3_verify_attn.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_ttt_attn_workspace_size.restype = ctypes.c_size_t
+    L.eagle3_ttt_attn_workspace_size.argtypes = [P(TttAttnArgs)]
+    L.eagle3_ttt_attn.restype = ctypes.c_int
+    L.eagle3_ttt_attn.argtypes = [P(TttAttnArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_spec_decode_metadata.restype = ctypes.c_int
+    L.eagle3_spec_decode_metadata.argtypes = [P(SpecDecodeMetadataArgs), _p]
+    L.eagle3_chain_verify.restype = ctypes.c_int
+    L.eagle3_chain_verify.argtypes = [P(ChainVerifyArgs), _p]
     L.eagle3_test_verify_attn_timeout.restype = ctypes.c_int
     L.eagle3_test_verify_attn_timeout.argtypes = [P(VerifyAttnArgs), _p, ctypes.c_size_t, _i32, _i64, _p]
     L.eagle3_verify_attn_noalloc.restype = ctypes.c_int
@@ -228,12 +258,19 @@ def eagle3_accept(mode, target_logits, tokens, parents, accept_len, path, emitte
 
 def eagle3_compact_kv(k_cache, v_cache, tree_k, tree_v, path, accept_len, prefix_len, slot_map, *,
                       aux_tree=None, aux_out=None, committed=None, tree_node_stride=0, tree_layer_stride=0,
-                      dev_status=None, stream=None):
-    """k_cache / v_cache [layers, B, Hkv, S_max, D] (bf16 or fp32); tree_k / tree_v: [layers, B, N, Hkv, D]
-    tensors, or flat views into fused QKV buffers described by tree_node_stride / tree_layer_stride
-    (elements; then pass tree_k / tree_v as 1-D tensors starting at the first key / value element);
-    path / slot_map [B, W]; accept_len, prefix_len [B] int32; aux_tree [B, N, A], aux_out [B, W, A]."""
-    layers, B, Hkv, S, D = k_cache.shape
+                      dev_status=None, stream=None, block_table=None, block_size=0):
+    """k_cache / v_cache [layers, B, Hkv, S_max, D] (bf16 or fp32), or with block_table [B, max_blocks]
+    paged pools [layers, n_slots, Hkv, D]; tree_k / tree_v: [layers, B, N, Hkv, D] tensors, or flat
+    views into fused QKV buffers described by tree_node_stride / tree_layer_stride (elements; then
+    pass tree_k / tree_v as 1-D tensors starting at the first key / value element); path / slot_map
+    [B, W]; accept_len, prefix_len [B] int32; aux_tree [B, N, A], aux_out [B, W, A]."""
+    paged = block_table is not None
+    if paged:
+        layers, n_slots, Hkv, D = k_cache.shape
+        B, S = path.shape[0], 0
+    else:
+        layers, B, Hkv, S, D = k_cache.shape
+        n_slots = 0
     if tree_k.dim() == 5:
         N = tree_k.shape[2]
         if tuple(tree_k.shape) != (layers, B, N, Hkv, D) or tree_v.shape != tree_k.shape:
@@ -251,7 +288,8 @@ def eagle3_compact_kv(k_cache, v_cache, tree_k, tree_v, path, accept_len, prefix
     A = 0 if aux_tree is None else aux_tree.shape[-1]
     a = CompactArgs(n_layers=layers, batch=B, n_nodes=N, n_kv_heads=Hkv, head_dim=D,
                     elem_bytes=k_cache.element_size(), s_max=S, max_path=path.shape[1],
-                    cache_layer_stride=B * Hkv * S * D, tree_layer_stride=tls, tree_node_stride=tns,
+                    cache_layer_stride=(n_slots if paged else B * S) * Hkv * D, tree_layer_stride=tls,
+                    tree_node_stride=tns,
                     k_cache=_ptr(k_cache, None, "k_cache"), v_cache=_ptr(v_cache, None, "v_cache"),
                     tree_k=tree_k.data_ptr(), tree_v=tree_v.data_ptr(),
                     path=_ptr(path, torch.int32, "path"), accept_len=_ptr(accept_len, torch.int32, "accept_len"),
@@ -259,7 +297,10 @@ def eagle3_compact_kv(k_cache, v_cache, tree_k, tree_v, path, accept_len, prefix
                     slot_map=_ptr(slot_map, torch.int32, "slot_map"),
                     committed=_ptr(committed, torch.int32, "committed"), aux_dim=A,
                     aux_tree=_ptr(aux_tree, None, "aux_tree"), aux_out=_ptr(aux_out, None, "aux_out"),
-                    dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+                    dev_status=_ptr(dev_status, torch.int32, "dev_status"),
+                    block_table=_ptr(block_table, torch.int32, "block_table"),
+                    max_blocks=block_table.shape[1] if paged else 0, block_size=int(block_size) if paged else 0,
+                    n_slots=n_slots)
     for t in (tree_k, tree_v):
         if not t.is_cuda:
             raise ValueError("tree_k / tree_v must be CUDA tensors")
@@ -274,15 +315,25 @@ def _view_ptr(t, dtype, name):
 
 
 def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
-                     lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None, qk_rotated=False):
+                     lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None, qk_rotated=False,
+                     block_table=None, block_size=0):
     """q [B, N, Hq, D] and tree_k / tree_v [B, N, Hkv, D] may be node-strided views (e.g. slices of a
     fused [B, N, (Hq + 2 Hkv) * D] projection output); everything else is dense.  qk_rotated: q and
-    tree_k already carry RoPE at prefix_len + depth (EPI_BF16_ROPE projection)."""
+    tree_k already carry RoPE at prefix_len + depth (EPI_BF16_ROPE projection).  Paged cache:
+    block_table [B, max_blocks] int32 and k_cache / v_cache pools [n_slots, Hkv, D]."""
     B, N, Hq, D = q.shape
     Hkv = tree_k.shape[2]
-    S = k_cache.shape[2]
+    if block_table is not None:
+        n_slots = k_cache.shape[0]
+        S = 0
+        cache_shape = (n_slots, Hkv, D)
+        if block_table.dim() != 2 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [B, max_blocks]")
+    else:
+        S = k_cache.shape[2]
+        cache_shape = (B, Hkv, S, D)
     for name, t, shape in (("tree_k", tree_k, (B, N, Hkv, D)), ("tree_v", tree_v, (B, N, Hkv, D)),
-                           ("k_cache", k_cache, (B, Hkv, S, D)), ("v_cache", v_cache, (B, Hkv, S, D)),
+                           ("k_cache", k_cache, cache_shape), ("v_cache", v_cache, cache_shape),
                            ("out", out, (B, N, Hq, D)), ("parents", parents, (B, N))):
         if tuple(t.shape) != shape:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
@@ -303,7 +354,11 @@ def verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, o
                           parents=_ptr(parents, torch.int32, "parents"),
                           prefix_len=_ptr(prefix_len, torch.int32, "prefix_len"),
                           out=_ptr(out, bf, "out"), lse=_ptr(lse, torch.float32, "lse"),
-                          dev_status=_ptr(dev_status, torch.int32, "dev_status"), qk_rotated=1 if qk_rotated else 0)
+                          dev_status=_ptr(dev_status, torch.int32, "dev_status"), qk_rotated=1 if qk_rotated else 0,
+                          block_table=_ptr(block_table, torch.int32, "block_table"),
+                          max_blocks=0 if block_table is None else block_table.shape[1],
+                          block_size=int(block_size) if block_table is not None else 0,
+                          n_slots=0 if block_table is None else k_cache.shape[0])
 
 
 def eagle3_verify_attn_workspace_size(args):
@@ -312,12 +367,13 @@ def eagle3_verify_attn_workspace_size(args):
 
 def eagle3_verify_attn(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out, *, max_prefix_len,
                        lse=None, rope_theta=500000.0, sm_scale=0.0, num_splits=0, dev_status=None,
-                       workspace=None, stream=None, qk_rotated=False):
+                       workspace=None, stream=None, qk_rotated=False, block_table=None, block_size=0):
     """Tree-masked verify attention for one layer (bf16, head_dim 128); rotates tree_k in place
-    unless qk_rotated (q and tree_k already rotated)."""
+    unless qk_rotated (q and tree_k already rotated).  With block_table the caches are paged pools."""
     a = verify_attn_args(q, tree_k, tree_v, k_cache, v_cache, parents, prefix_len, out,
                          max_prefix_len=max_prefix_len, lse=lse, rope_theta=rope_theta, sm_scale=sm_scale,
-                         num_splits=num_splits, dev_status=dev_status, qk_rotated=qk_rotated)
+                         num_splits=num_splits, dev_status=dev_status, qk_rotated=qk_rotated,
+                         block_table=block_table, block_size=block_size)
     L = lib()
     need = L.eagle3_verify_attn_workspace_size(ctypes.byref(a))
     if workspace is None:
@@ -346,13 +402,71 @@ def eagle3_test_verify_attn_timeout(q, tree_k, tree_v, k_cache, v_cache, parents
            "eagle3_test_verify_attn_timeout")
 
 
+def eagle3_spec_decode_metadata(cu_num_scheduled_tokens, num_draft_tokens, cu_num_draft_tokens, logits_indices,
+                                target_logits_indices, bonus_logits_indices, num_rows, *, dev_status=None, stream=None):
+    """Index bookkeeping of a ragged verify batch (int32 CUDA tensors; logits_indices and
+    target_logits_indices have the capacity max_rows)."""
+    R = cu_num_scheduled_tokens.numel()
+    i32 = torch.int32
+    a = SpecDecodeMetadataArgs(n_requests=R, max_rows=logits_indices.numel(),
+                               cu_num_scheduled_tokens=_ptr(cu_num_scheduled_tokens, i32, "cu_num_scheduled_tokens"),
+                               num_draft_tokens=_ptr(num_draft_tokens, i32, "num_draft_tokens"),
+                               cu_num_draft_tokens=_ptr(cu_num_draft_tokens, i32, "cu_num_draft_tokens"),
+                               logits_indices=_ptr(logits_indices, i32, "logits_indices"),
+                               target_logits_indices=_ptr(target_logits_indices, i32, "target_logits_indices"),
+                               bonus_logits_indices=_ptr(bonus_logits_indices, i32, "bonus_logits_indices"),
+                               num_rows=_ptr(num_rows, i32, "num_rows"), dev_status=_ptr(dev_status, i32, "dev_status"))
+    if target_logits_indices.numel() != logits_indices.numel():
+        raise ValueError("logits_indices and target_logits_indices share the capacity max_rows")
+    _check(lib().eagle3_spec_decode_metadata(ctypes.byref(a), _stream(stream)), "eagle3_spec_decode_metadata")
+
+
+def eagle3_ttt_attn(q, k, v, out, *, sm_scale=0.0, dev_status=None, workspace=None, stream=None):
+    """Training-time-test attention: q [Bt, T, Hq, D], k / v [S, Bt, T, Hkv, D] (step 0 native, then
+    the simulated steps), out [Bt, T, Hq, D]; bf16, rotated."""
+    Bt, T, Hq, D = q.shape
+    S, _, _, Hkv, _ = k.shape
+    bf = torch.bfloat16
+    if tuple(k.shape) != (S, Bt, T, Hkv, D) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("shapes: q / out [Bt, T, Hq, D], k / v [S, Bt, T, Hkv, D]")
+    a = TttAttnArgs(batch=Bt, seq_len=T, n_heads=Hq, n_kv_heads=Hkv, head_dim=D, n_steps=S, sm_scale=float(sm_scale),
+                    q=_ptr(q, bf, "q"), k=_ptr(k, bf, "k"), v=_ptr(v, bf, "v"), out=_ptr(out, bf, "out"),
+                    dev_status=_ptr(dev_status, torch.int32, "dev_status"))
+    L = lib()
+    need = L.eagle3_ttt_attn_workspace_size(ctypes.byref(a))
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.eagle3_ttt_attn(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_ttt_attn")
+
+
+def eagle3_chain_verify(logits, draft_tokens, cu_num_draft_tokens, output_tokens, *, is_greedy=None, num_accepted=None,
+                        temperature=1.0, seed=0, step=0, dev_status=None, step_counter=None, stream=None):
+    """Chain rejection sampling of a ragged batch: logits [rows, V] fp32, draft_tokens [sum d] and
+    cu_num_draft_tokens [R] int32, output_tokens [R, K + 1] int32."""
+    R, W = output_tokens.shape
+    i32 = torch.int32
+    a = ChainVerifyArgs(n_requests=R, vocab=logits.shape[1], max_drafts=W - 1, temperature=float(temperature),
+                        seed=int(seed), step=int(step), logits=_ptr(logits, torch.float32, "logits"),
+                        draft_tokens=_ptr(draft_tokens, i32, "draft_tokens") if draft_tokens.numel() else None,
+                        cu_num_draft_tokens=_ptr(cu_num_draft_tokens, i32, "cu_num_draft_tokens"),
+                        is_greedy=_ptr(is_greedy, i32, "is_greedy"), output_tokens=_ptr(output_tokens, i32, "output_tokens"),
+                        num_accepted=_ptr(num_accepted, i32, "num_accepted"), dev_status=_ptr(dev_status, i32, "dev_status"),
+                        step_counter=_ptr(step_counter, torch.int64, "step_counter"))
+    if cu_num_draft_tokens.numel() != R:
+        raise ValueError("one cu_num_draft_tokens entry per output row")
+    _check(lib().eagle3_chain_verify(ctypes.byref(a), _stream(stream)), "eagle3_chain_verify")
+
+
 def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, splits=0, dev_status=None,
                   workspace=None, stream=None, rope_cols=0, rope_rows_per_seq=1, rope_theta=500000.0,
-                  rope_base=None, rope_depth=None):
+                  rope_base=None, rope_depth=None, row_max=None):
     """out = epilogue(x W^T) on the tensor cores.  x [m, k] bf16, w (and w2) [n, k] bf16,
     out [m, n] bf16 (fp32 for EPI_F32), residual [m, n] bf16 for EPI_BF16_RESIDUAL.
     EPI_BF16_ROPE rotates columns [0, rope_cols) per 128-wide head at row position
-    rope_base[row // rope_rows_per_seq] + rope_depth[row] (int32 device tensors)."""
+    rope_base[row // rope_rows_per_seq] + rope_depth[row] (int32 device tensors).  row_max (EPI_F32,
+    int32 [m] holding the uint32 words, zeroed by the caller): each row's maximum output order key."""
     m, k = x.shape
     n = w.shape[0]
     if w.shape[1] != k or (w2 is not None and tuple(w2.shape) != (n, k)):
@@ -366,7 +480,8 @@ def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, split
                    residual=_ptr(residual, bf, "residual"), dev_status=_ptr(dev_status, torch.int32, "dev_status"),
                    rope_cols=int(rope_cols), rope_rows_per_seq=int(rope_rows_per_seq), rope_theta=float(rope_theta),
                    rope_base=_ptr(rope_base, torch.int32, "rope_base"),
-                   rope_depth=_ptr(rope_depth, torch.int32, "rope_depth"))
+                   rope_depth=_ptr(rope_depth, torch.int32, "rope_depth"),
+                   row_max=_ptr(row_max, torch.int32, "row_max"))
     L = lib()
     need = L.eagle3_linear_workspace_size(ctypes.byref(a))
     if workspace is None:

@@ -36,6 +36,11 @@ struct AttnLaunch {
     // test of the timeout path only: the K producer never loads this prefix tile (local index
     // within the CTA's split), so the wait for it runs out; -1 = off
     int stall_tile = -1;
+    // paged cache: k_cache / v_cache are a pool [n_slots, Hkv, 128]; position p of sequence b is
+    // slot block_table[b * bt_stride + p / block_size] * block_size + p % block_size (64 | block_size);
+    // pool_slots = slots in the pool
+    const int32_t *block_table = nullptr;
+    int bt_stride = 0, block_size = 0, pool_slots = 0;
 };
 
 size_t tree_attn_workspace(const AttnLaunch &a);

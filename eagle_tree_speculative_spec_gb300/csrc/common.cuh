@@ -142,6 +142,30 @@ E3_DEV float dsm_log31(uint64_t S) {
     return __fadd_rn(__fmul_rn((float)(e - FIX_BITS), LN2_F), lnm);
 }
 
+// EXP_NOISE(w): an Exp(1) draw from a 32-bit word.  u = (2 (w >> 9) + 1) * 2^-24 (odd numerator
+// S < 2^24, exact in fp32); S = 2^e * m folded into [sqrt(1/2), sqrt(2)) as in dsm_log31, and
+// E = (24 - e) ln 2 - ln m = -ln u with the same atanh series and RN steps (no cancellation near
+// u = 1, and E > 0 for every w).
+E3_DEV float dsm_exp_noise(uint32_t w) {
+    const uint32_t S = 2u * (w >> 9) + 1u;
+    int e = 31 - __clz(S);                                                 // bit length - 1
+    float m = __fmul_rn((float)S, __int_as_float((127 - e) << 23));        // exact: S < 2^24
+    if (m > SQRT2_F) {
+        m = __fmul_rn(m, 0.5f);
+        e += 1;
+    }
+    const float s = __fdiv_rn(__fsub_rn(m, 1.0f), __fadd_rn(m, 1.0f));
+    const float s2 = __fmul_rn(s, s);
+    float q = 0x1.745d18p-4f;                   // 1/11
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.c71c72p-4f);      // 1/9
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.24924ap-3f);      // 1/7
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.99999ap-3f);      // 1/5
+    q = __fadd_rn(__fmul_rn(q, s2), 0x1.555556p-2f);      // 1/3
+    q = __fadd_rn(__fmul_rn(q, s2), 1.0f);
+    const float lnm = __fmul_rn(__fmul_rn(2.0f, s), q);
+    return __fsub_rn(__fmul_rn((float)(24 - e), LN2_F), lnm);
+}
+
 // ------------------------------------------------------------------------------------------------
 // Total order on fp32 bit patterns: a > b as floats <=> key(a) > key(b) (and +0 > -0, NaN on top).
 // Packed with the index so that the maximum of the packed value is the maximum key with the

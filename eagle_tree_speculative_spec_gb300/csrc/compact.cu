@@ -25,7 +25,28 @@ struct Params {
     int32_t *prefix_len, *slot_map, *committed, *dev_status;
     const uint8_t *aux_tree;
     uint8_t *aux_out;
+    // paged cache: position p of sequence b is slot block_table[b * bt_stride + p / block_size] *
+    // block_size + p % block_size of a pool [n_slots, Hkv, D] per layer; null = contiguous
+    const int32_t *block_table;
+    int bt_stride, block_size, n_pages;
 };
+
+// The slot of position pos of sequence b in a paged cache, or -1 when its page id is outside the pool.
+E3_DEV long long paged_slot(const Params &p, int b, int pos) {
+    const int page = p.block_table[(size_t)b * p.bt_stride + pos / p.block_size];
+    if (page < 0 || page >= p.n_pages) return -1;
+    return (long long)page * p.block_size + pos % p.block_size;
+}
+
+// Whether sequence b's accepted path fits its cache (and, paged, lands on valid pages).
+E3_DEV bool path_fits(const Params &p, int b, int L, int n) {
+    if (n < 0 || n >= p.W || L < 0) return false;
+    if (!p.block_table) return L + n + 1 <= p.S;
+    if ((long long)L + n + 1 > (long long)p.bt_stride * p.block_size) return false;
+    for (int j = 0; j <= n; ++j)
+        if (paged_slot(p, b, L + j) < 0) return false;
+    return true;
+}
 
 E3_DEV void copy_bytes(uint8_t *dst, const uint8_t *src, size_t n) {
     // both pointers and n are multiples of 16 when the host allowed the vector path
@@ -62,7 +83,7 @@ __global__ void __launch_bounds__(NT) compact_copy_kernel(const Params p) {
     const int L = p.prefix_len[b];
     if (j > n) return;
     const int src = p.path[(size_t)b * p.W + j];
-    if (n < 0 || n >= p.W || src < 0 || src >= p.N || L < 0 || L + n + 1 > p.S) {
+    if (src < 0 || src >= p.N || !path_fits(p, b, L, n)) {
         if (threadIdx.x == 0 && j == 0 && layer == 0 && kv == 0 && !aux) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
         return;
     }
@@ -75,6 +96,10 @@ __global__ void __launch_bounds__(NT) compact_copy_kernel(const Params p) {
     const uint8_t *tsrc = (kv ? p.tree_v : p.tree_k) + ((size_t)layer * p.tree_ls +
                           ((size_t)b * p.N + src) * (size_t)p.tree_ns) * p.E;
     uint8_t *cdst = (kv ? p.v_cache : p.k_cache) + (size_t)layer * p.cache_ls * p.E;
+    if (p.block_table) {   // the slot holds all heads of the position contiguously, like the tree row
+        copy_bytes(cdst + (size_t)paged_slot(p, b, L + j) * p.Hkv * drow, tsrc, (size_t)p.Hkv * drow);
+        return;
+    }
     for (int h = 0; h < p.Hkv; ++h) {
         uint8_t *d = cdst + (((size_t)b * p.Hkv + h) * p.S + (size_t)(L + j)) * drow;
         copy_bytes(d, tsrc + (size_t)h * drow, drow);
@@ -86,12 +111,16 @@ __global__ void compact_finish_kernel(const Params p) {
     if (b >= p.B) return;
     const int n = p.accept_len[b];
     const int L = p.prefix_len[b];
-    bool ok = n >= 0 && n < p.W && L >= 0 && L + n + 1 <= p.S;
+    bool ok = path_fits(p, b, L, n);
     for (int j = 0; ok && j <= n; ++j) {
         const int src = p.path[(size_t)b * p.W + j];
         ok = src >= 0 && src < p.N;
     }
-    for (int j = 0; j < p.W; ++j) p.slot_map[(size_t)b * p.W + j] = (ok && j <= n) ? L + j : -1;
+    for (int j = 0; j < p.W; ++j) {
+        int slot = -1;
+        if (ok && j <= n) slot = p.block_table ? (int)paged_slot(p, b, L + j) : L + j;
+        p.slot_map[(size_t)b * p.W + j] = slot;
+    }
     if (ok) p.prefix_len[b] = L + n + 1;
     if (p.committed) p.committed[b] = ok ? n + 1 : 0;
 }
@@ -104,7 +133,9 @@ using namespace e3;
 extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eagle3_stream_t stream) {
     if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->n_layers < 1 || a->batch < 0 || a->n_nodes < 1 || a->n_kv_heads < 1 || a->head_dim < 1 ||
-        a->s_max < 1 || a->max_path < 1 || a->aux_dim < 0)
+        (!a->block_table && a->s_max < 1) || a->max_path < 1 || a->aux_dim < 0)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->block_table && (a->block_size < 1 || a->max_blocks < 1 || a->n_slots < a->block_size))
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->elem_bytes != 2 && a->elem_bytes != 4) return EAGLE3_ERR_UNSUPPORTED;
     if (a->n_nodes > 64) return EAGLE3_ERR_UNSUPPORTED;
@@ -113,7 +144,8 @@ extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eag
         !a->prefix_len || !a->slot_map)
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->aux_dim > 0 && (!a->aux_tree || !a->aux_out)) return EAGLE3_ERR_INVALID_ARGUMENT;
-    const int64_t dense_cache = (int64_t)a->batch * a->n_kv_heads * a->s_max * a->head_dim;
+    const int64_t dense_cache = a->block_table ? (int64_t)a->n_slots * a->n_kv_heads * a->head_dim
+                                               : (int64_t)a->batch * a->n_kv_heads * a->s_max * a->head_dim;
     if (a->tree_node_stride < 0 || (a->tree_node_stride && a->tree_node_stride < (int64_t)a->n_kv_heads * a->head_dim))
         return EAGLE3_ERR_INVALID_ARGUMENT;
     const int64_t tree_ns = a->tree_node_stride ? a->tree_node_stride : (int64_t)a->n_kv_heads * a->head_dim;
@@ -146,6 +178,10 @@ extern "C" eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *a, eag
     p.dev_status = a->dev_status;
     p.aux_tree = (const uint8_t *)a->aux_tree;
     p.aux_out = (uint8_t *)a->aux_out;
+    p.block_table = a->block_table;
+    p.bt_stride = a->max_blocks;
+    p.block_size = a->block_size;
+    p.n_pages = a->block_table ? a->n_slots / a->block_size : 0;
 
     const long long items = (long long)a->n_layers * 2 * a->batch * a->max_path +
                             (a->aux_dim > 0 ? (long long)a->batch * a->max_path : 0);

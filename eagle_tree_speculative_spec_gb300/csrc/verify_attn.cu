@@ -71,6 +71,8 @@ struct Params {
     int s_mid;                      // with two halves, the first half's query slots are [q_lo, q_lo + s_mid)
     int qk_rotated;                 // q and the tree keys arrive rotated: Q is loaded by TMA as is
     int stall_tile;                 // timeout-path test only: this prefix tile is never loaded (-1 off)
+    const int32_t *block_table;     // paged cache (slot pool [n_slots, Hkv, 128]) or null (contiguous)
+    int bt_stride, block_size, n_pages;
     long long wait_limit;           // clocks after which a bounded wait gives up
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
@@ -192,6 +194,31 @@ __global__ void __launch_bounds__(NT, 1)
     const int k_hi = last ? L : min(L, (t_lo + p.tiles_per_split) * BK);
     const int n_prefix = (k_hi - k_lo + BK - 1) / BK;
     const int n_tiles = n_prefix + (last ? 1 : 0);
+    // one 128-key prefix tile of K or V into a stage (two 64-column blocks of 16 KB).  Contiguous
+    // cache: two 128-row boxes of the [B * Hkv * S, 128] view.  Paged cache: four 64-slot boxes of
+    // the [n_slots, Hkv, 128] pool (a 64-aligned run of positions stays inside one page); runs past
+    // the prefix, or on a page id outside the pool, start at slot -64 and read as zeros.
+    const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
+    auto load_prefix_tile = [&](uint8_t *dst, const CUtensorMap *map, int j, uint64_t *bar) {
+        if (!p.block_table) {
+            const int y = row0 + j * BK;
+            tc::tma_load_2d(dst, map, 0, y, bar);
+            tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, bar);
+            return;
+        }
+        const int32_t *bt = p.block_table + (size_t)b * p.bt_stride;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int pos = k_lo + j * BK + 64 * h;
+            int slot = -64;
+            if (pos < L) {
+                const int page = __ldg(bt + pos / p.block_size);
+                if (page >= 0 && page < p.n_pages) slot = page * p.block_size + pos % p.block_size;
+            }
+            tc::tma_load_3d(dst + h * 8192, map, 0, g, slot, bar);
+            tc::tma_load_3d(dst + KV_TILE / 2 + h * 8192, map, 64, g, slot, bar);
+        }
+    };
 
     // ---- phase A: barriers, TMEM, raw tree description into shared memory.  Thread 0, which is also
     // the K producer, issues the first K tiles (and Q when it arrives rotated) as soon as their
@@ -229,14 +256,12 @@ __global__ void __launch_bounds__(NT, 1)
                     tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, b, s_lo, &ss.q_ready);
                 }
             }
-            const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             npre = min(ST_K, n_prefix);   // fresh stages: nothing to wait for
             for (int j = 0; j < npre; ++j) {
                 if (j == p.stall_tile) continue;   // timeout-path test: this tile never arrives
                 uint8_t *dst = sm + OFF_K + j * KV_TILE;
                 tc::mbar_expect_tx(&ss.k_full[j], KV_TILE);
-                tc::tma_load_2d(dst, &tm_k, 0, row0 + j * BK, &ss.k_full[j]);
-                tc::tma_load_2d(dst + KV_TILE / 2, &tm_k, 64, row0 + j * BK, &ss.k_full[j]);
+                load_prefix_tile(dst, &tm_k, j, &ss.k_full[j]);
             }
         }
     }
@@ -276,7 +301,6 @@ __global__ void __launch_bounds__(NT, 1)
             if (last) tc::prefetch_tmap(tmap);
             // V stage 1 holds the RoPE angle table until Q is staged (not used when Q arrives rotated)
             bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort, p.wait_limit);
-            const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
             const int j0 = is_k ? npre : 0;                  // thread 0 issued K tiles [0, npre) in phase A
             uint32_t issued = is_k ? (1u << npre) - 1u : 0u, last_par = 0;
             if (is_k && p.stall_tile >= 0 && p.stall_tile < npre) issued &= ~(1u << p.stall_tile);
@@ -291,9 +315,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (is_k && j == p.stall_tile && j < n_prefix) continue;   // timeout-path test: never loaded
                 if (j < n_prefix) {
                     tc::mbar_expect_tx(&full[s], KV_TILE);
-                    const int y = row0 + j * BK;
-                    tc::tma_load_2d(dst, map, 0, y, &full[s]);
-                    tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
+                    load_prefix_tile(dst, map, j, &full[s]);
                 } else {
                     tc::mbar_expect_tx(&full[s], 2 * BKT * 128);
                     const int y = p.tree_slot_inner ? 0 : b, z = p.tree_slot_inner ? b : 0;
@@ -780,6 +802,20 @@ bool make_q_map(CUtensorMap *m, const void *base, int nb, int n_slots, int Hq, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// paged pool [n_slots, Hkv, 128] as a 3-D tensor (columns, head, slot); boxes of 64 columns x 1
+// head x 64 slots land like 64 rows of a cache tile
+bool make_pool_map(CUtensorMap *m, const void *base, int64_t n_slots, int Hkv) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)n_slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_cache_map(CUtensorMap *m, const void *base, int64_t rows) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -900,11 +936,20 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     const int nk_all = a.q_hi;                       // tree slots visible as keys
     p.tree_slot_inner = a.k_si <= a.k_sb ? 1 : 0;
     if ((a.v_si <= a.v_sb ? 1 : 0) != p.tree_slot_inner) return EAGLE3_ERR_UNSUPPORTED;
-    const size_t cache_off = b0 * a.Hkv * a.S * D;
-    const int64_t cache_rows = (int64_t)pt.nb * a.Hkv * a.S;
-    if (!make_cache_map(&mk, a.k_cache + cache_off, cache_rows) ||
-        !make_cache_map(&mv, a.v_cache + cache_off, cache_rows))
-        return EAGLE3_ERR_CUDA;
+    p.block_table = a.block_table ? a.block_table + b0 * a.bt_stride : nullptr;
+    p.bt_stride = a.bt_stride;
+    p.block_size = a.block_size;
+    p.n_pages = a.block_table ? a.pool_slots / a.block_size : 0;
+    if (a.block_table) {
+        if (!make_pool_map(&mk, a.k_cache, a.pool_slots, a.Hkv) || !make_pool_map(&mv, a.v_cache, a.pool_slots, a.Hkv))
+            return EAGLE3_ERR_CUDA;
+    } else {
+        const size_t cache_off = b0 * a.Hkv * a.S * D;
+        const int64_t cache_rows = (int64_t)pt.nb * a.Hkv * a.S;
+        if (!make_cache_map(&mk, a.k_cache + cache_off, cache_rows) ||
+            !make_cache_map(&mv, a.v_cache + cache_off, cache_rows))
+            return EAGLE3_ERR_CUDA;
+    }
     CUtensorMap mtk, mtv;
     if (!make_tree_map(&mtk, p.k, pt.nb, nk_all, (int64_t)a.Hkv * D, a.k_sb, a.k_si) ||
         !make_tree_map(&mtv, p.v, pt.nb, nk_all, (int64_t)a.Hkv * D, a.v_sb, a.v_si))
@@ -979,13 +1024,19 @@ using namespace e3;
 static eagle3_status_t verify_validate(const eagle3_verify_attn_args_t *a) {
     if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->batch < 0 || a->n_nodes < 1 || a->n_heads < 1 || a->n_kv_heads < 1 || a->head_dim < 1 ||
-        a->s_max < 1 || a->max_prefix_len < 0 || a->num_splits < 0 || a->q_node_stride < 0 || a->kv_node_stride < 0)
+        (!a->block_table && a->s_max < 1) || a->max_prefix_len < 0 || a->num_splits < 0 || a->q_node_stride < 0 || a->kv_node_stride < 0)
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->n_heads % a->n_kv_heads) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->head_dim != D || a->n_nodes > 64) return EAGLE3_ERR_UNSUPPORTED;
     int s_mid = 0;
     if (!plan_halves(a->n_nodes, a->n_heads / a->n_kv_heads, &s_mid)) return EAGLE3_ERR_UNSUPPORTED;
-    if ((int64_t)a->max_prefix_len + a->n_nodes > a->s_max) return EAGLE3_ERR_CAPACITY;
+    if (a->block_table) {
+        if (a->block_size < 64 || a->block_size % 64 || a->max_blocks < 1 || a->n_slots < a->block_size)
+            return EAGLE3_ERR_INVALID_ARGUMENT;
+        if ((int64_t)a->max_blocks * a->block_size < a->max_prefix_len) return EAGLE3_ERR_CAPACITY;
+    } else if ((int64_t)a->max_prefix_len + a->n_nodes > a->s_max) {
+        return EAGLE3_ERR_CAPACITY;
+    }
     if (!(a->rope_theta > 0.0f) || a->sm_scale < 0.0f) return EAGLE3_ERR_INVALID_ARGUMENT;
     if ((a->q_node_stride && (a->q_node_stride < (int64_t)a->n_heads * D || a->q_node_stride % 8)) ||
         (a->kv_node_stride && (a->kv_node_stride < (int64_t)a->n_kv_heads * D || a->kv_node_stride % 8)))
@@ -1035,6 +1086,10 @@ static AttnLaunch verify_launch(const eagle3_verify_attn_args_t *a) {
     l.lse = a->lse;
     l.dev_status = a->dev_status;
     l.qk_rotated = a->qk_rotated ? 1 : 0;
+    l.block_table = a->block_table;
+    l.bt_stride = a->max_blocks;
+    l.block_size = a->block_size;
+    l.pool_slots = a->n_slots;
     return l;
 }
 

@@ -161,6 +161,15 @@ typedef struct {
     const void *aux_tree;        /* [B, N, A] (elem_bytes each) or NULL                               */
     void *aux_out;               /* [B, W, A] or NULL                                                 */
     int32_t *dev_status;         /* optional                                                          */
+    /* Paged cache (as in eagle3_verify_attn): when block_table is set, each layer of k_cache /
+       v_cache is a pool [n_slots, Hkv, D] (layers cache_layer_stride elements apart), position p of
+       sequence b is slot block_table[b * max_blocks + p / block_size] * block_size + p % block_size,
+       slot_map receives those slots, and a sequence fits when L + n + 1 <= max_blocks * block_size
+       with every page id it writes inside [0, n_slots / block_size); s_max is then not used.     */
+    const int32_t *block_table;  /* [B, max_blocks] page ids, or NULL (contiguous cache)               */
+    int32_t max_blocks;          /* columns of block_table                                             */
+    int32_t block_size;          /* positions per page, >= 1                                           */
+    int32_t n_slots;             /* slots in each layer's pool                                         */
 } eagle3_compact_args_t;
 
 eagle3_status_t eagle3_compact_kv(const eagle3_compact_args_t *args, eagle3_stream_t stream);
@@ -217,6 +226,18 @@ typedef struct {
                                    from eagle3_linear's EAGLE3_EPI_BF16_ROPE); neither is rotated
                                    again and tree_k is not written.  Needs (Hq / Hkv) to divide 128
                                    and a q node pitch of whole 16 bytes (else EAGLE3_ERR_UNSUPPORTED) */
+    /* Paged cache ("Speculative Decoding (EAGLE3) in the vLLM Neuron Framework", "EagleProposer:
+       Draft Model Management": slot = block_table[pos / block_size] * block_size + pos % block_size).
+       When block_table is set, k_cache / v_cache are a pool of n_slots slots of [Hkv, D] each
+       ([n_slots, Hkv, D] bf16, n_slots = pages * block_size) and position p of sequence b is slot
+       block_table[b * max_blocks + p / block_size] * block_size + p % block_size; s_max is then not
+       used.  block_size must be a multiple of 64 and max_blocks * block_size >= max_prefix_len.
+       Only the entries of positions < prefix_len[b] are read; page ids outside [0, n_slots /
+       block_size) read as zeros.                                                              */
+    const int32_t *block_table;  /* [B, max_blocks] page ids, or NULL (contiguous cache)               */
+    int32_t max_blocks;          /* columns of block_table                                             */
+    int32_t block_size;          /* positions per page                                                 */
+    int32_t n_slots;             /* slots in the pool                                                  */
 } eagle3_verify_attn_args_t;
 
 size_t eagle3_verify_attn_workspace_size(const eagle3_verify_attn_args_t *args);

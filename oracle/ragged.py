@@ -11,6 +11,14 @@ at (cu_num_draft_tokens[r] - d_r) + r; its first d_r rows are its draft-verifica
 its last row is its bonus row.
 
 Pinned by the worked example the page prints (tests/golden/spec_decode_metadata_5req.txt).
+
+Paged cache addressing, from "Speculative Decoding (EAGLE3) in the vLLM Neuron Framework",
+section "EagleProposer: Draft Model Management": position pos of a sequence lives in slot
+block_table[pos // block_size] * block_size + pos % block_size of the cache pool.  Pinned by its
+invariants (tests/test_oracle_basics.py): every position of a sequence lands in one of its own
+pages, consecutive positions of a page are consecutive slots, distinct positions of all
+sequences with disjoint pages never share a slot, and a pool written position by position and
+read back through the table is the contiguous cache.
 """
 import numpy as np
 
@@ -34,3 +42,15 @@ def spec_decode_metadata(cu_num_scheduled_tokens, num_draft_tokens):
     return {"cu_num_draft_tokens": np.cumsum(d), "logits_indices": np.asarray(logits, np.int64),
             "target_logits_indices": np.asarray(target, np.int64),
             "bonus_logits_indices": np.asarray(bonus, np.int64)}
+
+
+def slot_mapping(block_table_row, block_size, positions):
+    """Pool slots of the given positions of one sequence (int64 array)."""
+    bt = np.asarray(block_table_row, dtype=np.int64)
+    pos = np.asarray(positions, dtype=np.int64)
+    return bt[pos // block_size] * block_size + pos % block_size
+
+
+def paged_view(pool, block_table_row, block_size, length):
+    """The sequence's cache [length, ...] read from a pool [n_slots, ...] through its block table."""
+    return np.asarray(pool)[slot_mapping(block_table_row, block_size, np.arange(length))]

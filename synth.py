@@ -232,3 +232,38 @@ TINY_AUX_LAYERS = (1, 2, 3)
 
 def tiny_prompt(seed=0, length=32, vocab=256):
     return [int(t) for t in rng(seed, 99).integers(0, vocab, length)]
+
+
+# ----------------------------------------------------------------------------- ragged chains
+def chain_batch(seed, R, K, V, greedy_every=3):
+    """A ragged verify batch of R requests: draft counts in 0..K, target logits N(0, 3^2) for each
+    request's d + 1 rows (its verification rows, then its bonus row), draft tokens that are the
+    argmax of the row's logits plus N(0, 1) noise (a draft that often, not always, agrees), and
+    every greedy_every-th request greedy.  Returns numpy arrays: num_draft [R], logits [rows, V]
+    fp32, drafts [sum d] int32, greedy [R] int32."""
+    r = rng(seed, 31)
+    d = r.integers(0, K + 1, R).astype(np.int32)
+    rows = int(d.sum()) + R
+    logits = (3.0 * r.standard_normal((rows, V), dtype=np.float32)).astype(np.float32)
+    drafts, row = [], 0
+    for i in range(R):
+        for j in range(int(d[i])):
+            noisy = logits[row + j] + r.standard_normal(V, dtype=np.float32)
+            drafts.append(int(np.argmax(noisy)))
+        row += int(d[i]) + 1
+    greedy = (np.arange(R) % greedy_every == 0).astype(np.int32)
+    return d, logits, np.asarray(drafts, np.int32), greedy
+
+
+# ----------------------------------------------------------------------------- training-time test
+def ttt_batch(seed, Bt, T, Hq, Hkv, D, S):
+    """q [Bt, T, Hq, D] and k / v [S, Bt, T, Hkv, D] (step 0 native, then S - 1 simulated steps),
+    N(0, 1) rounded to bf16: (torch bf16 tensors, fp32 numpy copies)."""
+    r = rng(seed, 41)
+    q = r.standard_normal((Bt, T, Hq, D), dtype=np.float32)
+    k = r.standard_normal((S, Bt, T, Hkv, D), dtype=np.float32)
+    v = r.standard_normal((S, Bt, T, Hkv, D), dtype=np.float32)
+    out = {}
+    for name, arr in (("q", q), ("k", k), ("v", v)):
+        out[name], out[name + "_f32"] = to_bf16(arr)
+    return out

@@ -12,6 +12,9 @@ C_SOURCE = r"""
 #include "eagle3.h"
 #include "eagle3_linear.h"
 #include "eagle3_f32.h"
+#include "eagle3_chain.h"
+#include "eagle3_testing.h"
+#include "eagle3_ttt.h"
 
 #include <stdio.h>
 #include <string.h>
@@ -42,6 +45,32 @@ int main(void) {
     d.s_max = 64;
     d.draft_vocab = 300;                                                     /* reduced, without d2t */
     if (eagle3_draft_tree(NULL, &d, NULL, 0, NULL) != EAGLE3_ERR_INVALID_ARGUMENT) return 3;
+    {
+        eagle3_chain_verify_args_t c;
+        eagle3_spec_decode_metadata_args_t m;
+        memset(&c, 0, sizeof c);
+        c.vocab = 10;
+        c.temperature = 1.0f;
+        if (eagle3_chain_verify(&c, NULL) != EAGLE3_OK) return 6;                 /* no requests */
+        c.n_requests = 3;
+        c.max_drafts = 256;                                                      /* above 255 */
+        if (eagle3_chain_verify(&c, NULL) != EAGLE3_ERR_INVALID_ARGUMENT) return 7;
+        memset(&m, 0, sizeof m);
+        m.n_requests = -1;
+        if (eagle3_spec_decode_metadata(&m, NULL) != EAGLE3_ERR_INVALID_ARGUMENT) return 8;
+        if (eagle3_test_verify_attn_timeout(NULL, NULL, 0, -1, 1000, NULL) != EAGLE3_ERR_INVALID_ARGUMENT) return 9;
+    }
+    {
+        eagle3_ttt_attn_args_t t;
+        memset(&t, 0, sizeof t);
+        t.seq_len = 96;                                                          /* not a multiple of 64 */
+        t.n_heads = 32;
+        t.n_kv_heads = 8;
+        t.head_dim = 128;
+        t.n_steps = 2;
+        t.batch = 1;
+        if (eagle3_ttt_attn(&t, NULL, 0, NULL) != EAGLE3_ERR_UNSUPPORTED) return 10;
+    }
     if (strlen(eagle3_status_string(EAGLE3_ERR_CAPACITY)) == 0) return 4;
     if (eagle3_version() < 100) return 5;
     printf("ok %d\n", eagle3_version());

@@ -269,3 +269,33 @@ def test_spec_decode_metadata_invariants():
     assert (np.diff(got["logits_indices"]) > 0).all()
     with pytest.raises(ValueError):
         ragged.spec_decode_metadata([2, 3], [2, 0])       # 2 scheduled tokens cannot carry 2 drafts + 1
+
+
+# ----------------------------------------------------------------------------- paged cache addressing
+def test_slot_mapping_invariants():
+    from oracle import ragged
+    r = np.random.default_rng(12)
+    bs, n_pages, B, blocks = 64, 97, 5, 7
+    pages = r.permutation(n_pages)[: B * blocks].reshape(B, blocks)      # disjoint pages per sequence
+    seen = set()
+    for b in range(B):
+        L = int(r.integers(1, blocks * bs + 1))
+        slots = ragged.slot_mapping(pages[b], bs, np.arange(L))
+        # every position lands in one of the sequence's own pages, at its offset within the page
+        assert np.isin(slots // bs, pages[b]).all()
+        assert (slots % bs == np.arange(L) % bs).all()
+        # consecutive positions of a page are consecutive slots; a new page starts at a page boundary
+        for p in range(1, L):
+            if p % bs:
+                assert slots[p] == slots[p - 1] + 1
+            else:
+                assert slots[p] % bs == 0
+        # distinct positions never share a slot, within or across sequences
+        assert len(set(slots.tolist()) & seen) == 0 and len(set(slots.tolist())) == L
+        seen |= set(slots.tolist())
+        # a pool written position by position reads back as the contiguous cache
+        cache = r.standard_normal((L, 3))
+        pool = np.zeros((n_pages * bs, 3))
+        for p in range(L):
+            pool[ragged.slot_mapping(pages[b], bs, [p])[0]] = cache[p]
+        assert np.array_equal(ragged.paged_view(pool, pages[b], bs, L), cache)
