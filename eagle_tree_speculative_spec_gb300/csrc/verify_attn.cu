@@ -679,6 +679,502 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Persistent variant for queries and tree keys that arrive rotated (qk_rotated) with a parent
+// array: one CTA per SM walks the work items (sequence, KV head, split, half) c, c + grid, ...
+// Barriers, TMEM and the TMA descriptors are set up once, and the rings never drain between
+// items: the K / V producers run ahead into the next item while the softmax warps finish the
+// epilogue of the current one, and the S issuer starts the next item's S tiles as soon as its Q
+// has landed.  Every ring position and barrier phase is counted over the whole CTA life (tile
+// counters kt / vt / st, item counter qn), so phases stay consistent across items.  Extra
+// barriers: q_full (the item's Q landed), q_empty (the last S MMA of the item has read Q: the
+// next Q may overwrite it) and o_free (the epilogue has read O: the next item's first P V may
+// overwrite it).  Work items, tiles and warp roles are otherwise those of verify_attn_kernel.
+// ------------------------------------------------------------------------------------------------
+struct PersSmem {
+    uint64_t k_full[ST_K], k_empty[ST_K], v_full[ST_V], v_empty[ST_V];
+    uint64_t s_full[NS], p_full[NS], pv_done[NS];
+    uint64_t s_done, pv_mma_done;
+    uint64_t q_full, q_empty, o_free;
+    uint64_t anc[64];
+    int32_t par[64];
+    float mx_x[2][2][MT];
+    float l_x[2][MT];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct ItemGeo {
+    int b, g, split, half, L, k_lo, k_hi, n_prefix, n_tiles, s_lo, s_hi, nrows;
+    bool last, clamped;
+};
+
+E3_DEV ItemGeo item_geo(const Params &p, int it) {
+    ItemGeo w;
+    w.half = it % p.halves;
+    int r = it / p.halves;
+    w.split = r % p.splits;
+    r /= p.splits;
+    w.g = r % p.Hkv;
+    w.b = r / p.Hkv;
+    w.last = w.split == p.splits - 1;
+    int L = __ldg(p.prefix_len + w.b);
+    w.clamped = L < 0 || L > p.max_prefix;
+    w.L = L = max(0, min(L, p.max_prefix));
+    const int t_lo = w.split * p.tiles_per_split;
+    w.k_lo = min(L, t_lo * BK);
+    w.k_hi = w.last ? L : min(L, (t_lo + p.tiles_per_split) * BK);
+    w.n_prefix = (w.k_hi - w.k_lo + BK - 1) / BK;
+    w.n_tiles = w.n_prefix + (w.last ? 1 : 0);
+    w.s_lo = p.q_lo + (w.half ? p.s_mid : 0);
+    w.s_hi = p.halves == 1 ? p.q_hi : (w.half ? p.q_hi : p.q_lo + p.s_mid);
+    w.nrows = (w.s_hi - w.s_lo) * p.rep;
+    return w;
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    verify_attn_pers_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_tk, const __grid_constant__ CUtensorMap tm_tv,
+                            const __grid_constant__ CUtensorMap tm_q, const Params p, const int items) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PersSmem ss;
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    volatile int *abort = &ss.abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rep = p.rep, nk = p.q_hi;
+    if (tid == 0) {
+        for (int s = 0; s < ST_K; ++s) {
+            tc::mbar_init(&ss.k_full[s], 1);
+            tc::mbar_init(&ss.k_empty[s], 1);
+        }
+        for (int s = 0; s < ST_V; ++s) {
+            tc::mbar_init(&ss.v_full[s], 1);
+            tc::mbar_init(&ss.v_empty[s], 1);
+        }
+        for (int u = 0; u < NS; ++u) {
+            tc::mbar_init(&ss.s_full[u], 1);
+            tc::mbar_init(&ss.p_full[u], 8);
+            tc::mbar_init(&ss.pv_done[u], 1);
+        }
+        tc::mbar_init(&ss.s_done, 1);
+        tc::mbar_init(&ss.pv_mma_done, 1);
+        tc::mbar_init(&ss.q_full, 1);
+        tc::mbar_init(&ss.q_empty, 1);
+        tc::mbar_init(&ss.o_free, 8);
+        ss.abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&ss.tmem_base, 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = ss.tmem_base;
+    pdl_wait();   // the previous kernel's outputs (q / tree keys / caches) before any global access
+    pdl_trigger();
+
+    auto k_tile = [&](uint32_t t) -> uint8_t * { return sm + OFF_K + (t % ST_K) * KV_TILE; };
+    auto v_tile = [&](uint32_t t) -> uint8_t * { return sm + OFF_V + (t % ST_V) * KV_TILE; };
+
+    if (warp == 0 || warp == 10) {
+        // ------------------------------------------------------------------ TMA producers
+        if (lane == 0) {
+            const bool is_k = warp == 0;
+            const int stages = is_k ? ST_K : ST_V;
+            const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+            const CUtensorMap *tmap = is_k ? &tm_tk : &tm_tv;
+            uint64_t *full = is_k ? ss.k_full : ss.v_full;
+            uint64_t *empty = is_k ? ss.k_empty : ss.v_empty;
+            uint8_t *ring = sm + (is_k ? OFF_K : OFF_V);
+            tc::prefetch_tmap(map);
+            tc::prefetch_tmap(tmap);
+            if (is_k) tc::prefetch_tmap(&tm_q);
+            uint32_t t = 0, qn = 0;
+            bool go = true;
+            for (int it = blockIdx.x; it < items && go; it += gridDim.x) {
+                const ItemGeo w = item_geo(p, it);
+                if (w.n_tiles == 0) continue;
+                if (is_k) {
+                    // Q of this item: the previous item's S MMAs must have read the buffer
+                    if (qn > 0 && !tc::mbar_wait(&ss.q_empty, (qn - 1) & 1u, abort, p.wait_limit)) {
+                        go = false;
+                        break;
+                    }
+                    tc::mbar_expect_tx(&ss.q_full, Q_TILE);
+                    const int hs = w.g * rep;
+                    if (p.tree_slot_inner) {
+                        tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, w.s_lo, w.b, &ss.q_full);
+                        tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, w.s_lo, w.b, &ss.q_full);
+                    } else {
+                        tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, w.b, w.s_lo, &ss.q_full);
+                        tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, w.b, w.s_lo, &ss.q_full);
+                    }
+                    ++qn;
+                }
+                const int row0 = ((w.b * p.Hkv + w.g) * p.S) + w.k_lo;
+                for (int j = 0; j < w.n_tiles; ++j, ++t) {
+                    const int s = (int)(t % stages);
+                    const uint32_t ph = (t / stages) & 1u;
+                    if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort, p.wait_limit)) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t *dst = ring + s * KV_TILE;
+                    if (is_k && j == p.stall_tile && j < w.n_prefix) continue;   // timeout-path test: never loaded
+                    if (j < w.n_prefix) {
+                        tc::mbar_expect_tx(&full[s], KV_TILE);
+                        if (!p.block_table) {
+                            const int y = row0 + j * BK;
+                            tc::tma_load_2d(dst, map, 0, y, &full[s]);
+                            tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
+                        } else {
+                            const int32_t *bt = p.block_table + (size_t)w.b * p.bt_stride;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int pos = w.k_lo + j * BK + 64 * h;
+                                int slot = -64;
+                                if (pos < w.L) {
+                                    const int page = __ldg(bt + pos / p.block_size);
+                                    if (page >= 0 && page < p.n_pages) slot = page * p.block_size + pos % p.block_size;
+                                }
+                                tc::tma_load_3d(dst + h * 8192, map, 0, w.g, slot, &full[s]);
+                                tc::tma_load_3d(dst + KV_TILE / 2 + h * 8192, map, 64, w.g, slot, &full[s]);
+                            }
+                        }
+                    } else {
+                        tc::mbar_expect_tx(&full[s], 2 * BKT * 128);
+                        const int y = p.tree_slot_inner ? 0 : w.b, z = p.tree_slot_inner ? w.b : 0;
+                        tc::tma_load_3d(dst, tmap, w.g * D, y, z, &full[s]);
+                        tc::tma_load_3d(dst + KV_TILE / 2, tmap, w.g * D + 64, y, z, &full[s]);
+                    }
+                }
+            }
+            if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            // no TMA write may be in flight when the CTA exits: the last load of every stage, and Q
+            for (uint32_t u = t > (uint32_t)stages ? t - stages : 0; u < t; ++u) {
+                const long long t0 = clock64();
+                while (!tc::mbar_try(&full[u % stages], (u / stages) & 1u) && clock64() - t0 < p.wait_limit) {
+                }
+            }
+            if (is_k && qn > 0) {
+                const long long t0 = clock64();
+                while (!tc::mbar_try(&ss.q_full, (qn - 1) & 1u) && clock64() - t0 < p.wait_limit) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ S = Q K^T issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_P = tc::idesc_bf16(MT, BK);
+            constexpr uint32_t IDESC_T = tc::idesc_bf16(MT, BKT);
+            const uint32_t qaddr = smem_u32(sm + OFF_Q);
+            uint32_t kt = 0, st = 0, qn = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const ItemGeo w = item_geo(p, it);
+                if (w.n_tiles == 0) continue;
+                if (!tc::mbar_wait(&ss.q_full, qn & 1u, abort, p.wait_limit)) {
+                    ok = false;
+                    break;
+                }
+                for (int j = 0; j < w.n_tiles; ++j, ++kt, ++st) {
+                    const bool tree = j == w.n_prefix;
+                    if (!tc::mbar_wait(&ss.k_full[kt % ST_K], (kt / ST_K) & 1u, abort, p.wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    // buffer st % NS last held P(st - NS): its P V must have read it
+                    if (st >= NS && !tc::mbar_wait(&ss.pv_done[st % NS], ((st - NS) / NS) & 1u, abort, p.wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t kaddr = smem_u32(k_tile(kt));
+                    const uint32_t kblk = KV_TILE / 2;
+                    const uint32_t d_s = tmem + TM_S + (uint32_t)((st % NS) * BK);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+                        tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
+                                        tc::desc_sw128(kaddr + blk * kblk + kk * 32), tree ? IDESC_T : IDESC_P,
+                                        k > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&ss.s_full[st % NS]);
+                    tc::mma_commit(&ss.k_empty[kt % ST_K]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&ss.q_empty);   // the item's S MMAs are done with Q
+                ++qn;
+            }
+            if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            tc::mma_commit(&ss.s_done);
+            const long long t0 = clock64();
+            while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < p.wait_limit) {
+            }
+        }
+    } else if (warp == 11) {
+        // ------------------------------------------------------------------ O += P V issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
+            uint32_t vt = 0, st = 0, qn = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+                const ItemGeo w = item_geo(p, it);
+                if (w.n_tiles == 0) continue;
+                for (int j = 0; j < w.n_tiles; ++j, ++vt, ++st) {
+                    const bool tree = j == w.n_prefix;
+                    if (!tc::mbar_wait(&ss.v_full[vt % ST_V], (vt / ST_V) & 1u, abort, p.wait_limit) ||
+                        !tc::mbar_wait(&ss.p_full[st % NS], (st / NS) & 1u, abort, p.wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    // the item's first P V overwrites O: the previous item's epilogue must have read it
+                    if (j == 0 && qn > 0 && !tc::mbar_wait(&ss.o_free, (qn - 1) & 1u, abort, p.wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t vaddr = smem_u32(v_tile(vt));
+                    const uint32_t vblk = KV_TILE / 2;
+                    const uint32_t t_p = tmem + TM_S + (uint32_t)((st % NS) * BK);   // P over S
+                    const int ksteps = (tree ? BKT : BK) / 16;
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        tc::mma_bf16_ts(tmem, t_p + (uint32_t)(kk * 8),
+                                        tc::desc_mn_sw128(vaddr + kk * 2048, vblk, 1024), IDESC_PV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(&ss.pv_done[st % NS]);
+                    tc::mma_commit(&ss.v_empty[vt % ST_V]);
+                }
+                ++qn;
+            }
+            if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            tc::mma_commit(&ss.pv_mma_done);
+            const long long t0 = clock64();
+            while (!tc::mbar_try(&ss.pv_mma_done, 0) && clock64() - t0 < p.wait_limit) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax warps
+        const int w8 = warp - 2;
+        const int quarter = warp & 3;
+        const int hc = w8 >> 2;
+        const int rl = quarter * 32 + lane;              // row within the M tile
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t st = 0, qn = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            const ItemGeo w = item_geo(p, it);
+            const bool first_of_seq = w.split == 0 && w.g == 0 && w.half == 0;
+            if (w.clamped && first_of_seq && tid == 64) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
+            const int nq = p.q_hi - p.q_lo;
+            if (w.n_tiles == 0) {
+                // an empty split: its partial (m = -inf, l = 0, O = 0) for the merge
+                if (p.splits > 1 && rl < w.nrows) {
+                    const int qi = w.s_lo - p.q_lo + rl / rep, h = w.g * rep + rl % rep;
+                    const size_t prow_i = ((size_t)w.b * nq + qi) * p.Hq + h;
+                    const size_t rows_all = (size_t)p.B * nq * p.Hq;
+                    float *po = p.part_o + ((size_t)w.split * rows_all + prow_i) * D + (size_t)hc * 64;
+                    for (int cc = 0; cc < 64; cc += 4) *reinterpret_cast<float4 *>(po + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (hc == 0) {
+                        float *pm = p.part_ml + ((size_t)w.split * rows_all + prow_i) * 2;
+                        pm[0] = -INFINITY;
+                        pm[1] = 0.0f;
+                    }
+                }
+                continue;
+            }
+            // ancestor-or-self bits of the item's sequence: slot i walks its own parent chain
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the previous item's walk is read
+            {
+                const int i = tid - 64;
+                if (i < nk) ss.par[i] = __ldg(p.parents + (size_t)w.b * p.n_slots + i);
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            {
+                const int i = tid - 64;
+                if (i < nk) {
+                    auto invalid = [&](int j) {
+                        const int pj = ss.par[j];
+                        return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
+                    };
+                    uint64_t bits = 1ull << i;
+                    int j = i;
+                    const bool bad = invalid(i);
+                    while (j > 0 && !invalid(j)) {
+                        j = ss.par[j];
+                        bits |= 1ull << j;
+                    }
+                    ss.anc[i] = bits;
+                    if (bad && first_of_seq) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+                }
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            // only these item values stay live through the tile loop (the epilogue recomputes the rest;
+            // the tree tile reads its row's ancestor bits from shared memory)
+            const int n_tiles = w.n_tiles, n_prefix = w.n_prefix, k_lo = w.k_lo, k_hi = w.k_hi;
+            const int anc_slot = rl < w.nrows ? w.s_lo + rl / rep : -1;
+            float m_run = -INFINITY, l_run = 0.0f;
+            for (int j = 0; j < n_tiles; ++j, ++st) {
+                const int u = (int)(st % NS);
+                if (ok && !warp_wait(&ss.s_full[u], (st / NS) & 1u, abort, p.wait_limit)) ok = false;
+                tc::fence_after();
+                const bool tree = j == n_prefix;
+                const int hw = (tree ? BKT : BK) / 2;
+                const int col0 = hc * hw;
+                float sc[64];
+                {
+                    float a[32];
+                    tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0), a);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[i] = a[i];
+                    if (hw == 64) {
+                        tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0 + 32), a);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sc[32 + i] = a[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sc[32 + i] = -INFINITY;
+                    }
+                }
+                const int key0 = k_lo + j * BK + col0;
+                const bool full = !tree && key0 + hw <= k_hi;
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (full) {
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], sc[i], sc[i + 1]);
+                } else {
+                    const uint64_t bits = (tree && anc_slot >= 0) ? ss.anc[anc_slot] : 0ull;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int key = col0 + i;
+                        const bool valid =
+                            i < hw && (tree ? (key < nk && ((bits >> key) & 1ull)) : (key0 + i < k_hi));
+                        sc[i] = valid ? sc[i] : -INFINITY;
+                        mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
+                    }
+                }
+                // exchange buffers alternate with the CTA-wide tile count, so that consecutive tiles
+                // (also across items) never share one
+                float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+                ss.mx_x[st & 1][hc][rl] = mx;
+                asm volatile("bar.sync 2, 256;" ::: "memory");
+                mx = fmaxf(mx, ss.mx_x[st & 1][hc ^ 1][rl]);
+                const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
+                const bool any_need = __any_sync(0xffffffffu, need);
+                if (any_need && j > 0) {
+                    if (ok && !warp_wait(&ss.pv_done[(st - 1) % NS], ((st - 1) / NS) & 1u, abort, p.wait_limit))
+                        ok = false;
+                    tc::fence_after();
+                }
+                if (any_need) {
+                    const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                    const float corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
+                    if (j > 0) {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            float o[32];
+                            const uint32_t ta = t_lane + (uint32_t)(hc * 64 + cc * 32);
+                            tc::tmem_ld32(ta, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= corr;
+                            tc::tmem_st32(ta, o);
+                        }
+                    }
+                    l_run *= corr;
+                    m_run = m_new;
+                }
+                const float nmu = m_run == -INFINITY ? 0.0f : -m_run;
+                uint32_t pk[32];
+                float2 sq[4] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+                const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nmu2 = make_float2(nmu, nmu);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float2 x = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sc2, nmu2);
+                    const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    sq[e & 3] = __fadd2_rn(sq[e & 3], pe);
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(pe.x, pe.y);
+                    pk[e] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                const float2 s01 = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
+                l_run += s01.x + s01.y;
+                if (hw == 64)
+                    tc::tmem_st32u(t_lane + TM_S + (uint32_t)(u * BK + hc * 32), pk);
+                else
+                    tc::tmem_st16u(t_lane + TM_S + (uint32_t)(u * BK + hc * 16), pk);
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ss.p_full[u]);
+            }
+            // ---- epilogue of the item: this warp's 64 columns of O / l, 32 at a time (fewer live
+            // registers), then O is free for the next item
+            const ItemGeo we = item_geo(p, it);
+            ss.l_x[hc][rl] = l_run;
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            const float l_all = ss.l_x[0][rl] + ss.l_x[1][rl];
+            const bool have =
+                ok && warp_wait(&ss.pv_done[(st - 1) % NS], ((st - 1) / NS) & 1u, abort, p.wait_limit);
+            if (!have) ok = false;
+            tc::fence_after();
+            const float m_fin = have ? m_run : -INFINITY, l_fin = have ? l_all : 0.0f;
+            const bool row_ok = rl < we.nrows;
+            const int qi = we.s_lo - p.q_lo + rl / rep, h = we.g * rep + rl % rep;
+            const size_t prow_i = ((size_t)we.b * nq + qi) * p.Hq + h;
+            const size_t rows_all = (size_t)p.B * nq * p.Hq;
+            const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                float t[32];
+                tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
+                if (!row_ok) continue;
+                if (p.splits == 1) {
+                    __nv_bfloat16 *dst = p.out + (size_t)we.b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D +
+                                         (size_t)hc * 64 + cc * 32;
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float a0 = have ? t[c8 + 2 * e] * inv_l : 0.0f;
+                            const float a1 = have ? t[c8 + 2 * e + 1] * inv_l : 0.0f;
+                            __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
+                            wv[e] = *reinterpret_cast<uint32_t *>(&hv);
+                        }
+                        *reinterpret_cast<uint4 *>(dst + c8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                } else {
+                    float *po = p.part_o + ((size_t)we.split * rows_all + prow_i) * D + (size_t)hc * 64 + cc * 32;
+#pragma unroll
+                    for (int c4 = 0; c4 < 32; c4 += 4)
+                        *reinterpret_cast<float4 *>(po + c4) =
+                            have ? make_float4(t[c4], t[c4 + 1], t[c4 + 2], t[c4 + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ss.o_free);
+            ++qn;
+            if (row_ok && hc == 0) {
+                if (p.splits == 1) {
+                    if (p.lse) p.lse[prow_i] = (m_fin + log2f(l_fin)) * 0.6931471805599453f;
+                } else {
+                    float *pm = p.part_ml + ((size_t)we.split * rows_all + prow_i) * 2;
+                    pm[0] = m_fin;
+                    pm[1] = l_fin;
+                }
+            }
+        }
+        if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 // Rotated tree keys back into tree_k: eight threads per (sequence, query slot, KV head) row, four
 // rows per warp, at the slot's position (prefix length + depth from the parent array, or the given
 // position), with the same angle arguments and arithmetic the attention kernel uses for Q.
@@ -968,9 +1464,17 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
             cudaSuccess)   // 32 rows per block
             return EAGLE3_ERR_CUDA;
     }
-    if (launch_pdl(verify_attn_kernel, dim3(splits * p.halves, a.Hkv, pt.nb), dim3(NT), SMEM_DYN, stream, mk, mv, mtk,
-                   mtv, mq, p) != cudaSuccess)
+    if (p.qk_rotated && p.parents && !a.one_cta_per_item) {
+        // rotated q with a parent array: one persistent CTA per SM walks the work items
+        const int items = splits * p.halves * a.Hkv * pt.nb;
+        const int grid = std::min(items, sm_count_cached());
+        if (launch_pdl(verify_attn_pers_kernel, dim3(grid), dim3(NT), SMEM_DYN, stream, mk, mv, mtk, mtv, mq, p,
+                       items) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
+    } else if (launch_pdl(verify_attn_kernel, dim3(splits * p.halves, a.Hkv, pt.nb), dim3(NT), SMEM_DYN, stream, mk,
+                          mv, mtk, mtv, mq, p) != cudaSuccess) {
         return EAGLE3_ERR_CUDA;
+    }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (splits > 1) {
         if (launch_pdl(verify_combine_kernel, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, stream, p) != cudaSuccess)
@@ -1004,8 +1508,12 @@ eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws
         if ((uintptr_t)r & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
     static PerDevice<cudaError_t> attr;
     if (attr.get([] {
-            return cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)SMEM_DYN);
+            cudaError_t e = cudaFuncSetAttribute(verify_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)SMEM_DYN);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(verify_attn_pers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_DYN);
+            return e;
         }) != cudaSuccess)
         return EAGLE3_ERR_CUDA;
     Part parts[2];
