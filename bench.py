@@ -606,14 +606,24 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------------------- kernels
 def _time_loop(fn, steps, warmup, flush=None):
-    """Average device time per call with CUDA events; optional L2 flush between calls."""
+    """Average device time per call with CUDA events on the launching stream.  Without a flush the
+    calls run back to back between one pair of events (for inputs larger than L2), so the host's
+    time to issue a call overlaps the previous call; with a flush, every call gets its own events
+    after an L2 flush."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
     total = 0.0
     for _ in range(steps):
-        if flush is not None:
-            flush()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -621,6 +631,19 @@ def _time_loop(fn, steps, warmup, flush=None):
         torch.cuda.synchronize()
         total += a.elapsed_time(b)
     return total / steps
+
+
+def _raw_call(c_fn, args, ws):
+    """A prepared C call on the current stream (argument struct built once): no Python marshalling
+    inside the timed region."""
+    import ctypes
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    wp = ctypes.c_void_p(ws.data_ptr()) if ws is not None else None
+    wb = ctypes.c_size_t(ws.numel() if ws is not None else 0)
+    status = c_fn(ctypes.byref(args), wp, wb, st)
+    if status:
+        raise RuntimeError(f"libeagle3 call failed with status {status}")
+    return lambda: c_fn(ctypes.byref(args), wp, wb, st)
 
 
 def run_generate(args):
@@ -711,8 +734,8 @@ def run_kernel(args):
         # default: q and tree_k taken as already rotated (the fused RoPE projection's output, as in the
         # step); --rope-in-attention: the call rotates them (and writes the rotated tree keys back)
         qkr = not args.rope_in_attention
-        fn = lambda: e3.eagle3_verify_attn(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L, workspace=ws,
-                                           qk_rotated=qkr)
+        a = e3._lib.verify_attn_args(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=L, qk_rotated=qkr)
+        fn = _raw_call(e3._lib.lib().eagle3_verify_attn, a, ws)
         ms = _time_loop(fn, args.steps, args.warmup, flush if B * L * 4096 < 512e6 else None)
         nbytes = B * (4096 * L + 245760 + 983040 + (0 if qkr else 122880))
         out.update(batch=B, prefix=L, qk_rotated=qkr, ms=round(ms, 4), gbs=round(nbytes / ms / 1e6, 1),
@@ -732,9 +755,14 @@ def run_kernel(args):
         emitted = torch.empty(B, W, dtype=torch.int32, device=dev)
         nroot = torch.empty(B, dtype=torch.int32, device=dev)
         ws = torch.empty(2 * B * V * 4 + 16, dtype=torch.uint8, device=dev)
-        fn = lambda: e3.eagle3_accept(mode, zt_d, tok_d, par_d, alen, path, emitted, nroot, draft_logits=zd_d,
-                                      temperature=1.0, seed=1, workspace=ws)
-        ms = _time_loop(fn, args.steps, args.warmup, flush)
+        a = e3._lib.AcceptArgs(mode=int(mode), batch=B, n_nodes=N, vocab=V, max_path=W, temperature=1.0, seed=1,
+                               step=0, target_logits=zt_d.data_ptr(),
+                               draft_logits=zd_d.data_ptr() if zd_d is not None else None,
+                               tokens=tok_d.data_ptr(), parents=par_d.data_ptr(), accept_len=alen.data_ptr(),
+                               path=path.data_ptr(), emitted=emitted.data_ptr(), next_root=nroot.data_ptr(),
+                               dev_status=None, step_counter=None)
+        fn = _raw_call(e3._lib.lib().eagle3_accept, a, ws)
+        ms = _time_loop(fn, args.steps, args.warmup, flush)   # the visited rows fit in L2: flush between calls
         visited = int((alen.to(torch.int64) + 1).sum().item())
         rows = visited * (2 if mode == e3.SAMPLED else 1)
         nbytes = rows * V * 4
@@ -803,8 +831,14 @@ def run_kernel(args):
         res = torch.randn(M, N, generator=g, device=dev).to(bf) if epi == e3.EPI_BF16_RESIDUAL else None
         o = torch.empty(M, N, device=dev, dtype=torch.float32 if epi == e3.EPI_F32 else bf)
         ws = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        fn = lambda: e3.eagle3_linear(x, w, o, epilogue=epi, w2=w2, residual=res, workspace=ws)
-        ms = _time_loop(fn, args.steps, args.warmup)
+        a = e3._lib.LinearArgs(m=M, n=N, k=K, epilogue=epi, splits=0, ld_x=0, ld_w=0, ld_out=0, ld_res=0,
+                               x=x.data_ptr(), w=w.data_ptr(), w2=None if w2 is None else w2.data_ptr(),
+                               out=o.data_ptr(), residual=None if res is None else res.data_ptr(), dev_status=None,
+                               rope_cols=0, rope_rows_per_seq=1, rope_theta=500000.0, rope_base=None,
+                               rope_depth=None, row_max=None)
+        fn = _raw_call(e3._lib.lib().eagle3_linear, a, ws)
+        big = (x.numel() + w.numel() * (2 if w2 is not None else 1)) * 2 > 256e6   # inputs well beyond L2
+        ms = _time_loop(fn, args.steps, args.warmup, None if big else flush)
         flops = 2.0 * M * N * K * (2 if w2 is not None else 1)
         out.update(m=M, n=N, k=K, epilogue=args.epilogue, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
                    frac_sustained=round(flops / ms / 1e9 / tf_sust, 4), frac_burst=round(flops / ms / 1e9 / tf_burst, 4))

@@ -63,6 +63,11 @@ struct GemmParams {
     const int32_t *rope_base, *rope_depth;
     float rope_inv[64];              // theta^(-2j/128), computed in double, rounded to float
     uint32_t *row_max;               // F32: [M] atomic max of each row's output order keys, or null
+    // split tail: whole waves of tiles run data-parallel (tiles [0, tail_dp)); each tile of the
+    // partial last wave is split into tail_splits k-ranges whose fp32 partials go to tail_ws
+    // ([unit][BM][n_acc per tile] in unit order) and a second kernel adds them in split order
+    int tail_dp, tail_splits;
+    float *tail_ws;
 };
 
 // Order key of each of 32 outputs at columns col0.. (those < N), folded into a running maximum.
@@ -74,7 +79,7 @@ E3_DEV uint32_t chunk_max_key(uint32_t run, const float (&v)[32], int col0, int 
 }
 
 // One piece of work of a CTA: k-blocks [kb0, kb1) of output tile (mb, nb).
-enum { IT_FULL = 0, IT_SPLITK = 1, IT_CONTRIB = 2, IT_OWNER = 3 };
+enum { IT_FULL = 0, IT_SPLITK = 1, IT_CONTRIB = 2, IT_OWNER = 3, IT_TAIL = 4 };
 struct Item {
     int mb, nb, sp, kb0, kb1, kind, u;
 };
@@ -118,13 +123,26 @@ struct WorkIter {
             return true;
         }
         if (unit >= p.units) return false;
+        if (p.tail_splits > 1 && unit >= p.tail_dp) {
+            // a k-range of a tile of the partial last wave; w.u = its partial slot
+            const int v = unit - p.tail_dp, t = p.tail_dp + v / p.tail_splits;
+            w.u = v;
+            w.mb = t % p.tiles_m;
+            w.nb = t / p.tiles_m;
+            w.sp = v % p.tail_splits;
+            w.kb0 = w.sp * p.kb_per_split;
+            w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
+            w.kind = IT_TAIL;
+            unit += gridDim.x;
+            return true;
+        }
         w.u = unit;
         w.mb = unit % p.tiles_m;
         const int r = unit / p.tiles_m;
         w.nb = r % p.tiles_n;
         w.sp = r / p.tiles_n;
-        w.kb0 = w.sp * p.kb_per_split;
-        w.kb1 = min(p.kb_total, w.kb0 + p.kb_per_split);
+        w.kb0 = p.tail_splits > 1 ? 0 : w.sp * p.kb_per_split;
+        w.kb1 = p.tail_splits > 1 ? p.kb_total : min(p.kb_total, w.kb0 + p.kb_per_split);
         w.kind = p.splits > 1 ? IT_SPLITK : IT_FULL;
         unit += gridDim.x;
         return true;
@@ -396,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Item w;
         while (wi.next(p, w)) {
             const int mb = w.mb, nb = w.nb, sp = w.sp;
-            if (p.epi == EAGLE3_EPI_BF16_RESIDUAL && w.kind != IT_CONTRIB && p.splits == 1) {
+            if (p.epi == EAGLE3_EPI_BF16_RESIDUAL && w.kind != IT_CONTRIB && w.kind != IT_TAIL && p.splits == 1) {
                 // pull this tile's residual row into L2 while the main loop runs (one bulk prefetch
                 // of the row's whole-16-byte part; the epilogue reads it from there)
                 const int prow = mb * BM + quarter * 32 + lane, col0 = nb * BN;
@@ -477,6 +495,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) atomicAdd(&p.sk_flag[blockIdx.x], 1);
+            } else if (w.kind == IT_TAIL) {
+                // fp32 partials of a split tail tile: the tile's accumulator layout, unit after unit
+                float *wsr = p.tail_ws + ((size_t)w.u * BM + rl) * BN;
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tc::tmem_ld32(t_row + c * 32, v);   // warp-collective: every lane loads
+                    if (row < p.M) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            __stcg(reinterpret_cast<float4 *>(wsr + c * 32 + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                    }
+                }
             } else if (p.splits > 1) {
                 // fp32 partials in accumulator layout.  tcgen05.ld is warp-collective: every lane
                 // loads, only lanes that own a row < M store.
@@ -699,6 +729,68 @@ __global__ void gemm_reduce_kernel(const GemmParams p) {
     }
 }
 
+// The split tail's tiles: each output of such a tile is the sum of its tail_splits partials in split
+// order, then the epilogue.  Block (tile, row group): 4 rows x 64 threads, a thread 4 columns of the
+// accumulator tile.
+__global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const GemmParams p) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int BNT = 256;   // accumulator columns per tile (the plan's tile width)
+    const int t = p.tail_dp + blockIdx.x;
+    const int mb = t % p.tiles_m, nb = t / p.tiles_m;
+    const int rl = blockIdx.y * 4 + (threadIdx.x >> 6), c4 = (threadIdx.x & 63) * 4;
+    const int row = mb * BM + rl;
+    const bool swiglu = p.epi == EAGLE3_EPI_SWIGLU;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const size_t slot0 = (size_t)blockIdx.x * p.tail_splits;
+    if (row < p.M)
+        for (int sp = 0; sp < p.tail_splits; ++sp) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.tail_ws + ((slot0 + sp) * BM + rl) * BNT + c4));
+            acc[0] += v.x;
+            acc[1] += v.y;
+            acc[2] += v.z;
+            acc[3] += v.w;
+        }
+    // SwiGLU tiles hold [gate columns | up columns]: the first half's threads pair with the second's
+    float up[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t key = 0u;
+    bool any = false;
+    if (row < p.M && (!swiglu || c4 < BNT / 2)) {
+        if (swiglu) {
+            // the up columns of this thread's gate columns live 128 columns further in the same row
+            float u4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int sp = 0; sp < p.tail_splits; ++sp) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4 *>(p.tail_ws + ((slot0 + sp) * BM + rl) * BNT + BNT / 2 + c4));
+                u4[0] += v.x;
+                u4[1] += v.y;
+                u4[2] += v.z;
+                u4[3] += v.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) up[e] = u4[e];
+        }
+        const int col0 = swiglu ? nb * (BNT / 2) + c4 : nb * BNT + c4;
+        for (int e = 0; e < 4; ++e) {
+            const int col = col0 + e;
+            if (col >= p.N) continue;
+            float o = acc[e];
+            if (swiglu) o = silu(o) * up[e];
+            if (p.epi == EAGLE3_EPI_F32) {
+                ((float *)p.out)[(size_t)row * p.ld_out + col] = o;
+                const uint32_t k = order_key(o);
+                key = any ? max(key, k) : k;
+                any = true;
+            } else {
+                if (p.epi == EAGLE3_EPI_BF16_RESIDUAL) o += __bfloat162float(p.residual[(size_t)row * p.ld_res + col]);
+                ((__nv_bfloat16 *)p.out)[(size_t)row * p.ld_out + col] = __float2bfloat16_rn(o);
+            }
+        }
+    }
+    // a warp's 32 threads cover 128 columns of one row: one atomic max per warp
+    if (p.row_max) warp_row_max(p.row_max, row, key, any);
+}
+
 // ---- host side ----------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -747,6 +839,7 @@ int sm_count() {
 
 struct Plan {
     int bn, tiles_m, tiles_n, splits, kb_total, kb_per_split, units, n_acc, grid, streamk, dp_tiles;
+    int tail_dp = 0, tail_splits = 1;   // split tail (see GemmParams)
     size_t ws_bytes;
 };
 
@@ -795,6 +888,35 @@ Plan plan(const eagle3_linear_args_t *a) {
         pl.grid = sms;
         pl.ws_bytes = (size_t)sms * BM * pl.bn * sizeof(float) + (size_t)sms * sizeof(int);
         return pl;
+    }
+    // split tail: whole waves data-parallel, and the partial last wave's tiles split along k into as
+    // many ranges (2..8, at least 4 k-blocks each) as fill the SMs best, when that fills them at least
+    // 10 points better; no CTA waits on another, so the launch stays an ordinary (dependent) one
+    if (!rope && a->splits <= 0 && auto_splits == 1) {
+        const int dp = (tiles / sms) * sms, tail = tiles - dp;
+        if (dp > 0 && tail > 0) {
+            int best = 1;
+            double fill = (double)tail / sms;
+            for (int sp = 2; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
+                const int per = (pl.kb_total + sp - 1) / sp;
+                if (tail * sp > sms || (sp - 1) * per >= pl.kb_total) continue;   // no empty last range
+                const double f = (double)tail * sp / sms;
+                if (f > fill + 0.1) {
+                    best = sp;
+                    fill = f;
+                }
+            }
+            if (best > 1) {
+                pl.tail_dp = dp;
+                pl.tail_splits = best;
+                pl.splits = 1;
+                pl.kb_per_split = (pl.kb_total + best - 1) / best;
+                pl.units = dp + tail * best;
+                pl.grid = sms;
+                pl.ws_bytes = (size_t)tail * best * BM * pl.bn * sizeof(float);
+                return pl;
+            }
+        }
     }
     int splits = rope ? 1 : (a->splits > 0 ? a->splits : auto_splits);
     splits = std::max(1, std::min(splits, pl.kb_total));
@@ -888,6 +1010,9 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.rope_base = a->rope_base;
     p.rope_depth = a->rope_depth;
     p.row_max = a->epilogue == EAGLE3_EPI_F32 ? a->row_max : nullptr;
+    p.tail_dp = pl.tail_dp;
+    p.tail_splits = pl.tail_splits;
+    p.tail_ws = pl.tail_splits > 1 ? (float *)workspace : nullptr;
     for (int j = 0; j < 64; ++j)
         p.rope_inv[j] = p.rope_cols ? (float)std::pow((double)a->rope_theta, -2.0 * j / 128.0) : 0.0f;
     CUtensorMap mo;
@@ -932,6 +1057,13 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
             return EAGLE3_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    if (pl.tail_splits > 1) {
+        const int tail_tiles = pl.tiles_m * pl.tiles_n - pl.tail_dp;
+        if (launch_pdl(gemm_tail_reduce_kernel, dim3(tail_tiles, BM / 4), dim3(256), 0, (cudaStream_t)stream, p) !=
+            cudaSuccess)
+            return EAGLE3_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
     if (pl.splits > 1) {
         const size_t total = (size_t)a->m * a->n;
         const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sm_count() * 8);

@@ -197,3 +197,35 @@ def test_linear_f32_row_max(m, n, k, splits):
     assert np.array_equal(rmax.cpu().numpy().view(np.uint32).astype(np.uint64), keys.max(1))
     ok, err = close(got, _ref(x, w), 1e-3, 1e-3)
     assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,epi_name", [
+    (1280, 4096, 2048, "residual"),   # 160 tiles: 152 whole, 8 tail tiles split 8 ways
+    (1280, 2048, 2048, "swiglu"),     # 10 x 16 SwiGLU tiles (gate / up halves paired in the reduce)
+    (1290, 4100, 1024, "bf16"),       # ragged edges: 187 tiles, 35 tail tiles split 4 ways
+    (1280, 4096, 2048, "f32")])       # fp32 logits with the row maxima published by the reduce
+def test_linear_split_tail(m, n, k, epi_name):
+    """Whole waves of tiles run data-parallel and the partial last wave's tiles are split along k,
+    their partials added in split order by a second kernel: the same products as the fp64 matmul."""
+    import eagle_tree_speculative_spec_gb300 as e3
+    epi = {"residual": e3.EPI_BF16_RESIDUAL, "swiglu": e3.EPI_SWIGLU, "bf16": e3.EPI_BF16, "f32": e3.EPI_F32}[epi_name]
+    dev = require_gpu()
+    x, w, w2 = _inputs(m, n, k, 13, swiglu=epi == e3.EPI_SWIGLU)
+    res = torch.randn(m, n).to(torch.bfloat16) if epi == e3.EPI_BF16_RESIDUAL else None
+    out = torch.full((m, n), float("nan"), dtype=torch.float32 if epi == e3.EPI_F32 else torch.bfloat16, device=dev)
+    rmax = torch.zeros(m, dtype=torch.int32, device=dev) if epi == e3.EPI_F32 else None
+    e3.eagle3_linear(x.to(dev), w.to(dev), out, epilogue=epi, w2=None if w2 is None else w2.to(dev),
+                     residual=None if res is None else res.to(dev), row_max=rmax)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    if epi == e3.EPI_SWIGLU:
+        want = _silu(_ref(x, w)) * _ref(x, w2)
+    else:
+        want = _ref(x, w) + (res.double().numpy() if res is not None else 0.0)
+    tol = (1e-3, 1e-3) if epi == e3.EPI_F32 else (2e-2, 1e-2)
+    ok, err = close(got, want, *tol)
+    assert ok, err
+    if rmax is not None:
+        bits = got.view(np.uint32).astype(np.uint64)
+        keys = np.where(bits >> 31, ~bits & 0xFFFFFFFF, bits | 0x80000000)
+        assert np.array_equal(rmax.cpu().numpy().view(np.uint32).astype(np.uint64), keys.max(1))
