@@ -50,6 +50,11 @@ class AcceptArgs(ctypes.Structure):
                 ("step_counter", _p)]
 
 
+class AcceptLazyArgs(ctypes.Structure):
+    _fields_ = [("accept", AcceptArgs), ("hidden", _i32), ("hidden_states", _p), ("lm_head", _p),
+                ("dbg_level_logits", _p)]
+
+
 class CompactArgs(ctypes.Structure):
     _fields_ = [("n_layers", _i32), ("batch", _i32), ("n_nodes", _i32), ("n_kv_heads", _i32),
                 ("head_dim", _i32), ("elem_bytes", _i32), ("s_max", _i32), ("max_path", _i32),
@@ -146,6 +151,10 @@ def _declare(L):
     L.eagle3_accept_workspace_size.argtypes = [P(AcceptArgs)]
     L.eagle3_accept.restype = ctypes.c_int
     L.eagle3_accept.argtypes = [P(AcceptArgs), _p, ctypes.c_size_t, _p]
+    L.eagle3_accept_lazy_workspace_size.restype = ctypes.c_size_t
+    L.eagle3_accept_lazy_workspace_size.argtypes = [P(AcceptLazyArgs)]
+    L.eagle3_accept_lazy.restype = ctypes.c_int
+    L.eagle3_accept_lazy.argtypes = [P(AcceptLazyArgs), _p, ctypes.c_size_t, _p]
     L.eagle3_compact_kv.restype = ctypes.c_int
     L.eagle3_compact_kv.argtypes = [P(CompactArgs), _p]
     L.eagle3_verify_attn_workspace_size.restype = ctypes.c_size_t
@@ -254,6 +263,43 @@ def eagle3_accept(mode, target_logits, tokens, parents, accept_len, path, emitte
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(L.eagle3_accept(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_accept")
+
+
+def accept_lazy_args(mode, hidden_states, lm_head, tokens, parents, accept_len, path, emitted, next_root, *,
+                     temperature=1.0, seed=0, step=0, dev_status=None, step_counter=None, dbg_level_logits=None):
+    """AcceptLazyArgs: hidden_states [B, N, d] bf16 (final-normed), lm_head [V, d] bf16."""
+    B, N, d = hidden_states.shape
+    V = lm_head.shape[0]
+    bf = torch.bfloat16
+    if lm_head.shape[1] != d or tuple(tokens.shape) != (B, N) or tuple(parents.shape) != (B, N):
+        raise ValueError("shapes: hidden_states [B, N, d], lm_head [V, d], tokens / parents [B, N]")
+    acc = AcceptArgs(mode=int(mode), batch=B, n_nodes=N, vocab=V, max_path=path.shape[1],
+                     temperature=float(temperature), seed=int(seed), step=int(step), target_logits=None,
+                     draft_logits=None, tokens=_ptr(tokens, torch.int32, "tokens"),
+                     parents=_ptr(parents, torch.int32, "parents"), accept_len=_ptr(accept_len, torch.int32, "accept_len"),
+                     path=_ptr(path, torch.int32, "path"), emitted=_ptr(emitted, torch.int32, "emitted"),
+                     next_root=_ptr(next_root, torch.int32, "next_root"),
+                     dev_status=_ptr(dev_status, torch.int32, "dev_status"),
+                     step_counter=_ptr(step_counter, torch.int64, "step_counter"))
+    return AcceptLazyArgs(accept=acc, hidden=d, hidden_states=_ptr(hidden_states, bf, "hidden_states"),
+                          lm_head=_ptr(lm_head, bf, "lm_head"),
+                          dbg_level_logits=_ptr(dbg_level_logits, torch.float32, "dbg_level_logits"))
+
+
+def eagle3_accept_lazy(mode, hidden_states, lm_head, tokens, parents, accept_len, path, emitted, next_root, *,
+                       temperature=1.0, seed=0, step=0, dev_status=None, step_counter=None, dbg_level_logits=None,
+                       workspace=None, stream=None):
+    """Acceptance with a lazy target LM head (GREEDY or TOPK): logits only for the visited nodes."""
+    a = accept_lazy_args(mode, hidden_states, lm_head, tokens, parents, accept_len, path, emitted, next_root,
+                         temperature=temperature, seed=seed, step=step, dev_status=dev_status,
+                         step_counter=step_counter, dbg_level_logits=dbg_level_logits)
+    L = lib()
+    need = L.eagle3_accept_lazy_workspace_size(ctypes.byref(a))
+    if workspace is None:
+        workspace = _workspace(need, hidden_states.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(L.eagle3_accept_lazy(ctypes.byref(a), ws_ptr, ws_bytes, _stream(stream)), "eagle3_accept_lazy")
 
 
 def eagle3_compact_kv(k_cache, v_cache, tree_k, tree_v, path, accept_len, prefix_len, slot_map, *,

@@ -18,6 +18,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "eagle3_linear.h"
 
 namespace cg = cooperative_groups;
 
@@ -38,6 +39,12 @@ struct Params {
     int32_t *accept_len, *path, *emitted, *next_root, *dev_status;
     uint32_t *ws_p, *ws_q;   // [B, V] each, SAMPLED only
     const uint64_t *step_counter;   // when set, the step is read from device memory
+    // one level of the walk (the lazy LM head): the target logits of each sequence's current node
+    // are row b of zt ([B, V]); the walk state lives in st_* and path rows; a sequence that moves to
+    // a child saves its state and counts itself in *moved; one that stops writes its outputs
+    int level_mode;
+    int32_t *st_node, *st_plen, *st_done, *moved;
+    const int32_t *level_active;     // sequences still walking before this level (0: nothing to do)
 };
 
 struct Smem {
@@ -189,6 +196,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
     const int N = p.N, V = p.V;
     const uint64_t step = p.step_counter ? *p.step_counter : p.step;
     int phase = 0;
+    if (p.level_mode && (*p.level_active == 0 || p.st_done[b])) return;   // uniform across the cluster
 
     // ---- tree into shared memory, validated identically by every CTA
     if (threadIdx.x == 0) s.flag = 0;
@@ -212,6 +220,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
             if (threadIdx.x == 0) {
                 p.accept_len[b] = 0;
                 p.next_root[b] = -1;
+                if (p.level_mode) p.st_done[b] = 1;
             }
         }
         return;   // uniform across the cluster: no cluster barrier has been used yet
@@ -221,11 +230,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
     const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
     int node = 0, plen = 1;
     if (threadIdx.x == 0) s.path[0] = 0;
+    if (p.level_mode) {   // resume the walk where the previous level left it
+        node = p.st_node[b];
+        plen = p.st_plen[b];
+        for (int j = threadIdx.x; j < plen; j += NT) s.path[j] = p.path[(size_t)b * p.W + j];
+        __syncthreads();
+    }
     uint64_t parts[CL];
     uint64_t red[2];
+    // a move to a child: the full walk continues with it; one level saves the state and stops here
+    auto advance = [&](int next) -> bool {
+        if (!p.level_mode) return false;
+        cluster.sync();   // no CTA leaves while another may still read its slots
+        if (rank == 0 && threadIdx.x == 0) {
+            p.st_node[b] = next;
+            p.st_plen[b] = plen + 1;
+            p.path[(size_t)b * p.W + plen] = next;
+            atomicAdd(p.moved, 1);
+        }
+        return true;
+    };
 
     for (;;) {
-        const size_t row_off = ((size_t)b * N + node) * (size_t)V;
+        const size_t row_off = p.level_mode ? (size_t)b * V : ((size_t)b * N + node) * (size_t)V;
         const float *zt = p.zt + row_off;
 
         if (p.mode == EAGLE3_ACCEPT_GREEDY) {
@@ -243,6 +270,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
                     break;
                 }
             if (next >= 0 && plen < p.W) {
+                if (advance(next)) return;
                 node = next;
                 if (threadIdx.x == 0) s.path[plen] = next;
                 ++plen;
@@ -253,6 +281,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
             if (rank == 0) {
                 __syncthreads();
                 write_outputs(p, b, s.path, plen, pred);
+                if (p.level_mode && threadIdx.x == 0) p.st_done[b] = 1;
             }
             return;
         }
@@ -346,6 +375,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
         }
 
         if (next >= 0 && plen < p.W) {
+            if (advance(next)) return;
             node = next;
             if (threadIdx.x == 0) s.path[plen] = next;
             ++plen;
@@ -391,11 +421,80 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT) accept_kernel(c
                                     [&](int i, float) -> uint64_t { return wsp[i]; });
         }
         write_outputs(p, b, s.path, plen, tok);
+        if (p.level_mode && threadIdx.x == 0) p.st_done[b] = 1;
         return;
     }
 }
 
 __global__ void step_increment_kernel(uint64_t *counter) { *counter += 1; }
+
+// ---- lazy LM head: the level loop's small kernels ------------------------------------------
+// every walk starts at the root: state, path rows, the moved counter
+__global__ void lazy_init_kernel(int B, int W, int32_t *st_node, int32_t *st_plen, int32_t *st_done, int32_t *path,
+                                 int32_t *moved) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b == 0) *moved = B;   // level 0: every sequence walks
+    if (b >= B) return;
+    st_node[b] = 0;
+    st_plen[b] = 1;
+    st_done[b] = 0;
+    path[(size_t)b * W] = 0;
+}
+
+// before a level: the sequences still walking (those that moved in the previous level) become the
+// level's active count, and the move counter restarts
+__global__ void lazy_level_kernel(int32_t *moved, int32_t *active) {
+    *active = *moved;
+    *moved = 0;
+}
+
+// the final-normed hidden state of every walking sequence's current node, as the GEMM's rows
+__global__ void lazy_gather_kernel(int N, int d, const __nv_bfloat16 *hs, const int32_t *st_node,
+                                   const int32_t *st_done, const int32_t *active, __nv_bfloat16 *x) {
+    const int b = blockIdx.x;
+    if (*active == 0 || st_done[b]) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(hs + ((size_t)b * N + st_node[b]) * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(x + (size_t)b * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+struct LazyLayout {
+    size_t x, z, node, plen, done, moved, active, gemm, total;
+};
+
+LazyLayout lazy_layout(const eagle3_accept_lazy_args_t *a, size_t gemm_ws) {
+    LazyLayout l;
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = at;
+        at += (bytes + 255) / 256 * 256;
+        return o;
+    };
+    const size_t B = (size_t)a->accept.batch;
+    l.x = take(B * a->hidden * 2);
+    l.z = take(B * a->accept.vocab * 4);
+    l.node = take(B * 4);
+    l.plen = take(B * 4);
+    l.done = take(B * 4);
+    l.moved = take(4);
+    l.active = take(4);
+    l.gemm = take(gemm_ws);
+    l.total = at + 256;
+    return l;
+}
+
+eagle3_linear_args_t lazy_linear(const eagle3_accept_lazy_args_t *a, const void *x, void *z) {
+    eagle3_linear_args_t l = {};
+    l.m = a->accept.batch;
+    l.n = a->accept.vocab;
+    l.k = a->hidden;
+    l.epilogue = EAGLE3_EPI_F32;
+    l.x = (const uint16_t *)x;
+    l.w = a->lm_head;
+    l.out = z;
+    l.dev_status = a->accept.dev_status;
+    return l;
+}
 
 }  // namespace
 }  // namespace e3
@@ -449,11 +548,111 @@ extern "C" eagle3_status_t eagle3_accept(const eagle3_accept_args_t *a, void *wo
     p.ws_p = sampled ? (uint32_t *)workspace : nullptr;
     p.ws_q = sampled ? (uint32_t *)workspace + (size_t)a->batch * a->vocab : nullptr;
     p.step_counter = a->step_counter;
+    p.level_mode = 0;
+    p.st_node = p.st_plen = p.st_done = p.moved = nullptr;
+    p.level_active = nullptr;
     accept_kernel<<<dim3(a->batch * CL), dim3(NT), 0, (cudaStream_t)stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     if (a->step_counter) {
         // stream-ordered after every CTA of the acceptance kernel has read the counter
         step_increment_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(a->step_counter);
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
+    return EAGLE3_OK;
+}
+
+namespace e3 {
+eagle3_status_t linear_launch(const eagle3_linear_args_t *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
+                              const int32_t *skip_if_zero);
+}
+
+static eagle3_status_t lazy_validate(const eagle3_accept_lazy_args_t *a) {
+    if (!a) return EAGLE3_ERR_INVALID_ARGUMENT;
+    const eagle3_accept_args_t *c = &a->accept;
+    if (c->mode == EAGLE3_ACCEPT_SAMPLED) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->mode != EAGLE3_ACCEPT_GREEDY && c->mode != EAGLE3_ACCEPT_TOPK) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (c->batch < 0 || c->n_nodes < 1 || c->vocab < 1 || c->max_path < 1 || a->hidden < 8 || a->hidden % 8)
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (c->n_nodes > MAXN || c->vocab > (1 << 22)) return EAGLE3_ERR_UNSUPPORTED;
+    if (c->mode == EAGLE3_ACCEPT_TOPK && (!(c->temperature > 0.0f) || !(c->temperature < 3.0e38f)))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (c->batch == 0) return EAGLE3_OK;
+    if (!c->tokens || !c->parents || !c->accept_len || !c->path || !c->emitted || !c->next_root ||
+        !a->hidden_states || !a->lm_head || (((uintptr_t)a->hidden_states | (uintptr_t)a->lm_head) & 15))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    return EAGLE3_OK;
+}
+
+extern "C" size_t eagle3_accept_lazy_workspace_size(const eagle3_accept_lazy_args_t *a) {
+    if (lazy_validate(a) != EAGLE3_OK || a->accept.batch == 0) return 0;
+    const uint16_t *dummy = reinterpret_cast<const uint16_t *>((uintptr_t)256);   // sizing only
+    eagle3_accept_lazy_args_t t = *a;
+    t.lm_head = dummy;
+    eagle3_linear_args_t l = lazy_linear(&t, dummy, (void *)dummy);
+    return lazy_layout(a, eagle3_linear_workspace_size(&l)).total;
+}
+
+extern "C" eagle3_status_t eagle3_accept_lazy(const eagle3_accept_lazy_args_t *a, void *workspace, size_t ws_bytes,
+                                              eagle3_stream_t stream_) {
+    const eagle3_status_t st = lazy_validate(a);
+    if (st != EAGLE3_OK || a->accept.batch == 0) return st;
+    const eagle3_accept_args_t *c = &a->accept;
+    const size_t need = eagle3_accept_lazy_workspace_size(a);
+    if (!workspace || ws_bytes < need) return EAGLE3_ERR_WORKSPACE;
+    uint8_t *ws = (uint8_t *)(((uintptr_t)workspace + 255) & ~(uintptr_t)255);
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const int B = c->batch, W = c->max_path;
+    const eagle3_linear_args_t probe = lazy_linear(a, ws, ws);
+    const LazyLayout L = lazy_layout(a, eagle3_linear_workspace_size(&probe));
+    auto P = [&](size_t o) { return (void *)(ws + o); };
+    int32_t *st_node = (int32_t *)P(L.node), *st_plen = (int32_t *)P(L.plen), *st_done = (int32_t *)P(L.done);
+    int32_t *moved = (int32_t *)P(L.moved), *active = (int32_t *)P(L.active);
+    lazy_init_kernel<<<(B + 127) / 128, 128, 0, stream>>>(B, W, st_node, st_plen, st_done, c->path, moved);
+    if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+
+    Params p;
+    p.mode = c->mode;
+    p.B = B;
+    p.N = c->n_nodes;
+    p.V = c->vocab;
+    p.W = W;
+    p.inv_t = c->mode == EAGLE3_ACCEPT_GREEDY ? 1.0f : 1.0f / c->temperature;
+    p.seed = c->seed;
+    p.step = c->step;
+    p.zt = (const float *)P(L.z);
+    p.zd = nullptr;
+    p.tokens = c->tokens;
+    p.parents = c->parents;
+    p.accept_len = c->accept_len;
+    p.path = c->path;
+    p.emitted = c->emitted;
+    p.next_root = c->next_root;
+    p.dev_status = c->dev_status;
+    p.ws_p = p.ws_q = nullptr;
+    p.step_counter = c->step_counter;
+    p.level_mode = 1;
+    p.st_node = st_node;
+    p.st_plen = st_plen;
+    p.st_done = st_done;
+    p.moved = moved;
+    p.level_active = active;
+    const eagle3_linear_args_t lin = lazy_linear(a, P(L.x), P(L.z));
+    for (int level = 0; level < W; ++level) {
+        lazy_level_kernel<<<1, 1, 0, stream>>>(moved, active);
+        lazy_gather_kernel<<<B, 128, 0, stream>>>(c->n_nodes, a->hidden, (const __nv_bfloat16 *)a->hidden_states,
+                                                 st_node, st_done, active, (__nv_bfloat16 *)P(L.x));
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+        const eagle3_status_t s2 = linear_launch(&lin, P(L.gemm), L.total - L.gemm, stream, active);
+        if (s2 != EAGLE3_OK) return s2;
+        if (a->dbg_level_logits &&
+            cudaMemcpyAsync(a->dbg_level_logits + (size_t)level * B * c->vocab, P(L.z), (size_t)B * c->vocab * 4,
+                            cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return EAGLE3_ERR_CUDA;
+        accept_kernel<<<dim3(B * CL), dim3(NT), 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
+    }
+    if (c->step_counter) {
+        step_increment_kernel<<<1, 1, 0, stream>>>(c->step_counter);
         if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
     }
     return EAGLE3_OK;

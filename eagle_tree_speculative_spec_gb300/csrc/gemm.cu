@@ -68,7 +68,12 @@ struct GemmParams {
     // ([unit][BM][n_acc per tile] in unit order) and a second kernel adds them in split order
     int tail_dp, tail_splits;
     float *tail_ws;
+    // when set and the word it points to is 0 (read after the previous kernel completed), the
+    // launch does nothing: a caller whose row count is known only on the device skips idle launches
+    const int32_t *skip_if_zero;
 };
+
+E3_DEV bool skipped(const GemmParams &p) { return p.skip_if_zero && *(volatile const int32_t *)p.skip_if_zero == 0; }
 
 // Order key of each of 32 outputs at columns col0.. (those < N), folded into a running maximum.
 E3_DEV uint32_t chunk_max_key(uint32_t run, const float (&v)[32], int col0, int N) {
@@ -303,6 +308,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_base_slot;
     pdl_wait();   // the previous kernel's outputs (this launch's inputs, or buffers it overwrites)
     pdl_trigger();
+    if (skipped(p)) {   // uniform: every thread reads the same word
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            __syncwarp();
+            tc::fence_after();
+            tc::tmem_dealloc(tmem, C::TMEM_COLS);
+        }
+        return;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -690,6 +705,7 @@ E3_DEV void warp_row_max(uint32_t *row_max, int row, uint32_t key, bool valid) {
 __global__ void gemm_reduce_kernel(const GemmParams p) {
     pdl_wait();
     pdl_trigger();
+    if (skipped(p)) return;
     const int n_out = p.N;
     const size_t total = (size_t)p.M * n_out;
     const size_t stride = (size_t)gridDim.x * blockDim.x;   // a multiple of 32: the loop is warp-uniform
@@ -735,6 +751,7 @@ __global__ void gemm_reduce_kernel(const GemmParams p) {
 __global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const GemmParams p) {
     pdl_wait();
     pdl_trigger();
+    if (skipped(p)) return;
     constexpr int BNT = 256;   // accumulator columns per tile (the plan's tile width)
     const int t = p.tail_dp + blockIdx.x;
     const int mb = t % p.tiles_m, nb = t / p.tiles_m;
@@ -963,8 +980,18 @@ extern "C" size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *a) {
     return plan(a).ws_bytes;
 }
 
+namespace e3 {
+eagle3_status_t linear_launch(const eagle3_linear_args_t *a, void *workspace, size_t ws_bytes, cudaStream_t stream,
+                              const int32_t *skip_if_zero);
+}
+
 extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *workspace, size_t ws_bytes,
                                          eagle3_stream_t stream) {
+    return e3::linear_launch(a, workspace, ws_bytes, (cudaStream_t)stream, nullptr);
+}
+
+eagle3_status_t e3::linear_launch(const eagle3_linear_args_t *a, void *workspace, size_t ws_bytes,
+                                  cudaStream_t stream, const int32_t *skip_if_zero) {
     const eagle3_status_t st = validate(a);
     if (st != EAGLE3_OK || a->m == 0) return st;
     const Plan pl = plan(a);
@@ -1013,6 +1040,7 @@ extern "C" eagle3_status_t eagle3_linear(const eagle3_linear_args_t *a, void *wo
     p.tail_dp = pl.tail_dp;
     p.tail_splits = pl.tail_splits;
     p.tail_ws = pl.tail_splits > 1 ? (float *)workspace : nullptr;
+    p.skip_if_zero = skip_if_zero;
     for (int j = 0; j < 64; ++j)
         p.rope_inv[j] = p.rope_cols ? (float)std::pow((double)a->rope_theta, -2.0 * j / 128.0) : 0.0f;
     CUtensorMap mo;

@@ -962,6 +962,28 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         uint32_t st = 0, qn = 0;
         bool ok = true;
+        const int per_b = p.halves * p.splits * p.Hkv;   // work items per sequence
+        int walked = -1;                                  // the item whose ancestor bits ss.anc holds
+        // ancestor-or-self bits of sequence b from parent values already in ss.par: slot i walks its
+        // own parent chain (the softmax warps only; the caller synchronises before and after)
+        auto walk = [&](bool flag_bad) {
+            const int i = tid - 64;
+            if (i < nk) {
+                auto invalid = [&](int j) {
+                    const int pj = ss.par[j];
+                    return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
+                };
+                uint64_t bits = 1ull << i;
+                int j = i;
+                const bool bad = invalid(i);
+                while (j > 0 && !invalid(j)) {
+                    j = ss.par[j];
+                    bits |= 1ull << j;
+                }
+                ss.anc[i] = bits;
+                if (bad && flag_bad) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+            }
+        };
         for (int it = blockIdx.x; it < items; it += gridDim.x) {
             const ItemGeo w = item_geo(p, it);
             const bool first_of_seq = w.split == 0 && w.g == 0 && w.half == 0;
@@ -983,32 +1005,24 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 continue;
             }
-            // ancestor-or-self bits of the item's sequence: slot i walks its own parent chain
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // the previous item's walk is read
-            {
-                const int i = tid - 64;
-                if (i < nk) ss.par[i] = __ldg(p.parents + (size_t)w.b * p.n_slots + i);
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            {
-                const int i = tid - 64;
-                if (i < nk) {
-                    auto invalid = [&](int j) {
-                        const int pj = ss.par[j];
-                        return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
-                    };
-                    uint64_t bits = 1ull << i;
-                    int j = i;
-                    const bool bad = invalid(i);
-                    while (j > 0 && !invalid(j)) {
-                        j = ss.par[j];
-                        bits |= 1ull << j;
-                    }
-                    ss.anc[i] = bits;
-                    if (bad && first_of_seq) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+            // ancestor-or-self bits of the item's sequence (usually walked already, after the previous
+            // item's last tile, from parents loaded during that item)
+            if (walked != it) {
+                asm volatile("bar.sync 1, 256;" ::: "memory");   // the previous bits are no longer read
+                {
+                    const int i = tid - 64;
+                    if (i < nk) ss.par[i] = __ldg(p.parents + (size_t)w.b * p.n_slots + i);
                 }
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                walk(first_of_seq);
+                walked = it;
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
+            // the next item's parent values, loaded now so that their latency hides behind the tiles
+            const int it_next = it + gridDim.x;
+            int par_next = 0;
+            if (it_next < items && tid - 64 < nk)
+                par_next = __ldg(p.parents + (size_t)(it_next / per_b) * p.n_slots + (tid - 64));
             // only these item values stay live through the tile loop (the epilogue recomputes the rest;
             // the tree tile reads its row's ancestor bits from shared memory)
             const int n_tiles = w.n_tiles, n_prefix = w.n_prefix, k_lo = w.k_lo, k_hi = w.k_hi;
@@ -1105,8 +1119,17 @@ __global__ void __launch_bounds__(NT, 1)
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&ss.p_full[u]);
             }
-            // ---- epilogue of the item: this warp's 64 columns of O / l, 32 at a time (fewer live
-            // registers), then O is free for the next item
+            // the next item's ancestor bits (this item's tree tile, its last, has read the current ones)
+            if (it_next < items) {
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (tid - 64 < nk) ss.par[tid - 64] = par_next;
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                const ItemGeo wn = item_geo(p, it_next);
+                walk(wn.split == 0 && wn.g == 0 && wn.half == 0);
+                walked = it_next;
+            }
+            // ---- epilogue of the item: this warp's 64 columns of O / l, then O is free for the next
+            // item; bf16 outputs are packed before O is released and stored after
             const ItemGeo we = item_geo(p, it);
             ss.l_x[hc][rl] = l_run;
             asm volatile("bar.sync 2, 256;" ::: "memory");
@@ -1121,37 +1144,46 @@ __global__ void __launch_bounds__(NT, 1)
             const size_t prow_i = ((size_t)we.b * nq + qi) * p.Hq + h;
             const size_t rows_all = (size_t)p.B * nq * p.Hq;
             const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                float t[32];
-                tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
-                if (!row_ok) continue;
-                if (p.splits == 1) {
-                    __nv_bfloat16 *dst = p.out + (size_t)we.b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D +
-                                         (size_t)hc * 64 + cc * 32;
+            if (p.splits == 1) {
+                uint32_t pk[32];                  // this warp's 64 columns of the row, packed bf16 pairs
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                        uint32_t wv[4];
+                for (int cc = 0; cc < 2; ++cc) {
+                    float t[32];
+                    tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float a0 = have ? t[c8 + 2 * e] * inv_l : 0.0f;
-                            const float a1 = have ? t[c8 + 2 * e + 1] * inv_l : 0.0f;
-                            __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
-                            wv[e] = *reinterpret_cast<uint32_t *>(&hv);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + c8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 hv = __floats2bfloat162_rn(have ? t[2 * e] * inv_l : 0.0f,
+                                                                  have ? t[2 * e + 1] * inv_l : 0.0f);
+                        pk[cc * 16 + e] = *reinterpret_cast<uint32_t *>(&hv);
                     }
-                } else {
+                }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ss.o_free);
+                if (row_ok) {
+                    __nv_bfloat16 *dst =
+                        p.out + (size_t)we.b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D + (size_t)hc * 64;
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8)
+                        *reinterpret_cast<uint4 *>(dst + 8 * c8) =
+                            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                }
+            } else {
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    float t[32];
+                    tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
+                    if (!row_ok) continue;
                     float *po = p.part_o + ((size_t)we.split * rows_all + prow_i) * D + (size_t)hc * 64 + cc * 32;
 #pragma unroll
                     for (int c4 = 0; c4 < 32; c4 += 4)
                         *reinterpret_cast<float4 *>(po + c4) =
                             have ? make_float4(t[c4], t[c4 + 1], t[c4 + 2], t[c4 + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&ss.o_free);
             }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&ss.o_free);
             ++qn;
             if (row_ok && hc == 0) {
                 if (p.splits == 1) {

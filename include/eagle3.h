@@ -122,6 +122,33 @@ eagle3_status_t eagle3_accept(const eagle3_accept_args_t *args, void *workspace,
                               eagle3_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * eagle3_accept_lazy - eagle3_accept with a lazy target LM head: target logits only for the nodes
+ * the walk visits.
+ *
+ * Defines: "Speculative Decoding (EAGLE3) in the vLLM Neuron Framework", section "Rejection
+ * Sampling" (the target's distribution is needed only where a decision is taken) with the walk of
+ * eagle3_accept.  The walk visits one node per level; level by level the library gathers the
+ * final-normed hidden state of every sequence's current node, computes its logits
+ * (x W_lm^T, fp32, on the tensor cores, M = batch) and advances the walk by one node, until every
+ * sequence has stopped (at most max_path levels; a level in which no sequence is still walking
+ * launches kernels that return at once).  Results are those of eagle3_accept on the logits of the
+ * visited nodes as computed here.  Modes GREEDY and TOPK (SAMPLED needs the draft logits of the
+ * visited nodes too: EAGLE3_ERR_UNSUPPORTED).  accept.target_logits is not read.
+ * ---------------------------------------------------------------------------------------------- */
+typedef struct {
+    eagle3_accept_args_t accept; /* as for eagle3_accept (target_logits unused)                      */
+    int32_t hidden;              /* d, a multiple of 8                                               */
+    const uint16_t *hidden_states; /* [B, N, d] bf16: every tree node's final-normed hidden state    */
+    const uint16_t *lm_head;     /* [V, d] bf16                                                      */
+    float *dbg_level_logits;     /* optional [max_path, B, V] fp32: each level's logits row per
+                                    sequence (rows of sequences that had stopped are not defined)    */
+} eagle3_accept_lazy_args_t;
+
+size_t eagle3_accept_lazy_workspace_size(const eagle3_accept_lazy_args_t *args);
+eagle3_status_t eagle3_accept_lazy(const eagle3_accept_lazy_args_t *args, void *workspace,
+                                   size_t workspace_bytes, eagle3_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
  * eagle3_compact_kv - copy the accepted path's K/V into contiguous cache slots.
  *
  * Defines: "Advanced speculative decoding: tree drafts and EAGLE", section "Implementation" (the
