@@ -324,7 +324,7 @@ def run_gpu(args):
     # all work on one side stream: graph capture needs a stream other than the legacy default one
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    eng = Engine(cfg, args.steps * 2 + max(args.warmup, args.steps) + 3, dev, fused_rope=not args.rope_in_attention)
+    eng = Engine(cfg, args.steps * 3 + 2 * max(args.warmup, args.steps) + 8, dev, fused_rope=not args.rope_in_attention)
     use_graph = not args.eager
     if use_graph and not external_events_ok():
         eng.timing = False                      # timing events cannot live inside a graph: time kernels eagerly
@@ -419,6 +419,31 @@ def run_gpu(args):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+
+    # ---- the same step with the lazy target LM head (eagle3_accept_lazy: the head's logits only for
+    # the nodes the acceptance walk visits), continuing from the state the loops above left
+    eng.step_obj.prepare(lazy_head=True)
+    if use_graph:
+        eng.capture(args.steps)
+        for i in range(max(args.warmup, args.steps)):
+            eng.replay(i)
+    else:
+        for _ in range(args.warmup):
+            eng.step()
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lazy_acc = torch.zeros((), dtype=torch.int64, device=dev)
+    l0.record()
+    for i in range(args.steps):
+        if use_graph:
+            eng.replay(i)
+        else:
+            eng.step()
+        lazy_acc += (eng.accept_len.to(torch.int64) + 1).sum()
+    l1.record()
+    torch.cuda.synchronize()
+    lazy_ms = max_over_ranks(l0.elapsed_time(l1), dev)
+    status |= int(eng.dev_status.item())
     h2d = host_aux.numel() * 2 + host_tok.numel() * 4 + host_tc.numel() * 4
     d2h = h2d + out_len.numel() * 4
 
@@ -474,6 +499,12 @@ def run_gpu(args):
                                                      / hbm, 4),
                                        "how": "layer 0's prepared call issued 20 times back to back after the "
                                               "timed steps (no event nodes around it)"}},
+        "lazy_head": {"value": round(job_rate(cfg["B"] * cfg["N"] * args.steps, world, lazy_ms), 2), "unit": UNIT,
+                      "ms_per_step": round(lazy_ms / args.steps, 4),
+                      "tau": round(float(lazy_acc.item()) / (cfg["B"] * args.steps) - 1.0, 4),
+                      "how": "the same step with eagle3_accept_lazy in place of the full LM head and "
+                             "eagle3_accept (identical acceptance; head logits only for the visited nodes), "
+                             f"{args.steps} steps timed after the e2e loop"},
         "accepted_tokens_per_s": round(float(accepted.item()) * world / (ms / 1e3), 2),
         "tau": round(tau, 4),
         "e2e": {"value": round(units / (e2e_ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,

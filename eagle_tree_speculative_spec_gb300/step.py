@@ -19,6 +19,8 @@ A step, every part of it a libeagle3 call on the caller's stream:
       eagle3_linear     O projection + residual, post-norm, SwiGLU gate/up, down + residual
   eagle3_rmsnorm + eagle3_linear   final norm, LM head (fp32 logits)
   eagle3_accept         greedy walk or lossless rejection sampling over the tree
+                        (lazy_head: eagle3_accept_lazy instead of the LM head and eagle3_accept; the
+                        head's logits are computed level by level, only for the nodes the walk visits)
   eagle3_compact_kv     the accepted path's K/V of every layer into the caches (read in place
                         from the fused QKV outputs), the path's aux rows and tokens into the next
                         step's catch-up inputs, prefix_len += accepted + 1
@@ -90,7 +92,8 @@ class SpeculativeStep:
         self.attn = torch.empty(R, Hq * D, device=dev, dtype=bf)
         self.act = torch.empty(R, F, device=dev, dtype=bf)
         self.aux_tree = torch.empty(R, 3 * d, device=dev, dtype=bf)
-        self.logits = torch.empty(R, V, device=dev, dtype=torch.float32)
+        self.logits = None                 # [R, V] fp32, allocated by a full-head prepare()
+        self.lazy_head = False
         self.accept_len = torch.empty(B, dtype=i32, device=dev)
         self.path = torch.empty(B, W, dtype=i32, device=dev)
         self.next_root = torch.empty(B, dtype=i32, device=dev)
@@ -117,10 +120,15 @@ class SpeculativeStep:
         return self.qkv[layer].view(c["B"], c["N"], self.qkv_w)[:, :, lo:].unflatten(2, (c["Hkv"], c["D"]))
 
     # ------------------------------------------------------------------------------ preparation
-    def prepare(self, ws_linear_bytes=512 << 20, ws_attn_bytes=256 << 20):
+    def prepare(self, ws_linear_bytes=512 << 20, ws_attn_bytes=256 << 20, lazy_head=False):
         """Build every argument struct of the step once.  Ops are (kind, call) pairs; kind names
-        the calls a profiler may want to time ("gemm", "gemm_gateup", "verify_attn") or is None."""
+        the calls a profiler may want to time ("gemm", "gemm_gateup", "verify_attn") or is None.
+        lazy_head: the acceptance computes the target LM head's logits itself, one level of the walk
+        at a time and only for the nodes it visits (same decisions as the full head; the logits
+        buffer is then not written)."""
         e3, c = _lib, self.cfg
+        self.lazy_head = bool(lazy_head)
+        self._keep = []
         L = e3.lib()
         B, N, d, D, Hq, Hkv = c["B"], c["N"], c["d"], c["D"], c["Hq"], c["Hkv"]
         R = B * N
@@ -201,20 +209,31 @@ class SpeculativeStep:
             lin(self.h, T["wg"][l], self.act, epi=e3.EPI_SWIGLU, w2=T["wu"][l], kind="gemm_gateup")
             lin(self.act, T["wd"][l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
         norm(self.x, T["final_norm"], self.h)
-        lin(self.h, T["lm_head"], self.logits, epi=e3.EPI_F32)
         # ---- acceptance over the tree (the emitted row is the next step's catch-up tokens)
-        aa = e3.AcceptArgs(mode=int(c["mode"]), batch=B, n_nodes=N, vocab=c["V"], max_path=c["W"],
-                           temperature=float(c.get("temperature", 1.0)), seed=int(c.get("seed", 0)), step=0,
-                           target_logits=self.logits.data_ptr(), draft_logits=None,
-                           tokens=self.tokens.data_ptr(), parents=self.parents.data_ptr(),
-                           accept_len=self.accept_len.data_ptr(), path=self.path.data_ptr(),
-                           emitted=self.next_tok.data_ptr(), next_root=self.next_root.data_ptr(),
-                           dev_status=dev_st, step_counter=self.step_counter.data_ptr())
+        if self.lazy_head:
+            aa = e3.accept_lazy_args(c["mode"], self.h.view(B, N, d), T["lm_head"], self.tokens, self.parents,
+                                     self.accept_len, self.path, self.next_tok, self.next_root,
+                                     temperature=float(c.get("temperature", 1.0)), seed=int(c.get("seed", 0)),
+                                     dev_status=self.dev_status, step_counter=self.step_counter)
+            need = L.eagle3_accept_lazy_workspace_size(ctypes.byref(aa))
+            accept_fn = L.eagle3_accept_lazy
+        else:
+            if self.logits is None:
+                self.logits = torch.empty(R, c["V"], device=self.dev, dtype=torch.float32)
+            lin(self.h, T["lm_head"], self.logits, epi=e3.EPI_F32)
+            aa = e3.AcceptArgs(mode=int(c["mode"]), batch=B, n_nodes=N, vocab=c["V"], max_path=c["W"],
+                               temperature=float(c.get("temperature", 1.0)), seed=int(c.get("seed", 0)), step=0,
+                               target_logits=self.logits.data_ptr(), draft_logits=None,
+                               tokens=self.tokens.data_ptr(), parents=self.parents.data_ptr(),
+                               accept_len=self.accept_len.data_ptr(), path=self.path.data_ptr(),
+                               emitted=self.next_tok.data_ptr(), next_root=self.next_root.data_ptr(),
+                               dev_status=dev_st, step_counter=self.step_counter.data_ptr())
+            need = L.eagle3_accept_workspace_size(ctypes.byref(aa))
+            accept_fn = L.eagle3_accept
         keep.append(aa)
-        need = L.eagle3_accept_workspace_size(ctypes.byref(aa))
         self.ws_acc = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
         cp, cb = ws(self.ws_acc)
-        ops.append((None, lambda a=aa: L.eagle3_accept(ctypes.byref(a), cp, cb, st)))
+        ops.append((None, lambda a=aa, f=accept_fn: f(ctypes.byref(a), cp, cb, st)))
         # ---- compaction: tree K/V read in place from the fused QKV outputs (node pitch qkv_w)
         kflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=Hq * D)
         vflat = torch.as_strided(self.qkv, (1,), (1,), storage_offset=(Hq + Hkv) * D)
@@ -252,16 +271,17 @@ class SpeculativeStep:
             self.prepare()
         self.issue(self.ops if draft else self.verify_ops, timed)
 
-    def flops(self, catchup_rows=None):
+    def flops(self, catchup_rows=None, head_rows=None):
         """Algorithmic GEMM flops of one step: (target verify, draft head).  The draft counts the
         real catch-up rows (sum of tc over the batch; default one per sequence, the committed count
-        of a step that accepted nothing), not the rows the launch pads to tc_max."""
+        of a step that accepted nothing), not the rows the launch pads to tc_max.  head_rows: rows of
+        the target LM head (default every tree node; with the lazy head, the visited nodes)."""
         c = self.cfg
         d, F, V, Hq, D, qw = c["d"], c["F"], c["V"], c["Hq"], c["D"], self.qkv_w
         Vd = V if self.d2t is None else int(self.d2t.numel())
         R = c["B"] * c["N"]
         per_layer = 2 * R * (d * qw + Hq * D * d + 2 * d * F + F * d)
-        target = c["layers"] * per_layer + 2 * R * d * V
+        target = c["layers"] * per_layer + 2 * (R if head_rows is None else head_rows) * d * V
         rows_d = c["B"] * c["top_k"]
         draft_layer = lambda m: 2 * m * (2 * d * qw + Hq * D * d + 2 * d * F + F * d)
         tc_rows = c["B"] if catchup_rows is None else catchup_rows

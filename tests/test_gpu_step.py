@@ -289,3 +289,37 @@ def test_step_with_planted_acceptance_and_catchup():
         assert np.array_equal(dk_after[b, :, :L0], dk_before[b, :, :L0])
     # the new tree's root is the previous step's correction / bonus token
     assert (st.tokens[:, 0].cpu().numpy() == cu_tok[np.arange(c["B"]), tc - 1]).all()
+
+
+@pytest.mark.parametrize("mode_name", ["greedy", "topk"])
+def test_step_lazy_head_equals_full_head(mode_name):
+    """The step with the lazy target LM head (eagle3_accept_lazy) from the same state as the full-head
+    step, on planted trees whose walks go several levels deep: acceptance, the emitted tokens, the
+    compacted caches and the next step's inputs are identical."""
+    from eagle_tree_speculative_spec_gb300 import GREEDY, TOPK
+    dev = require_gpu()
+    mode = {"greedy": GREEDY, "topk": TOPK}[mode_name]
+    st, _, _ = _build(dev, mode)
+    st.issue(st.draft_ops)
+    torch.cuda.synchronize()
+    snap = _snapshot(st)
+    st.run(draft=False)
+    torch.cuda.synchronize()
+    _plant_chain(st, snap, oacc.argmax)
+    _restore(st, snap)
+    st.run(draft=False)
+    torch.cuda.synchronize()
+    full = _host(st)
+    assert full["dev_status"][0] == 0
+    if mode == GREEDY:
+        assert (full["accept_len"] >= 2).all()
+    st.prepare(ws_linear_bytes=64 << 20, ws_attn_bytes=16 << 20, lazy_head=True)
+    _restore(st, snap)
+    st.run(draft=False)
+    torch.cuda.synchronize()
+    lazy = _host(st)
+    for k in full:
+        if k == "logits":                       # not written by the lazy head
+            continue
+        assert np.array_equal(full[k], lazy[k]), k
+    assert int(st.step_counter.item()) == 1
