@@ -682,24 +682,45 @@ __global__ void __launch_bounds__(NT, 1)
 // ------------------------------------------------------------------------------------------------
 // Persistent variant for queries and tree keys that arrive rotated (qk_rotated) with a parent
 // array: one CTA per SM walks the work items (sequence, KV head, split, half) c, c + grid, ...
-// Barriers, TMEM and the TMA descriptors are set up once, and the rings never drain between
-// items: the K / V producers run ahead into the next item while the softmax warps finish the
-// epilogue of the current one, and the S issuer starts the next item's S tiles as soon as its Q
-// has landed.  Every ring position and barrier phase is counted over the whole CTA life (tile
-// counters kt / vt / st, item counter qn), so phases stay consistent across items.  Extra
-// barriers: q_full (the item's Q landed), q_empty (the last S MMA of the item has read Q: the
-// next Q may overwrite it) and o_free (the epilogue has read O: the next item's first P V may
-// overwrite it).  Work items, tiles and warp roles are otherwise those of verify_attn_kernel.
+// Barriers, TMEM and the TMA descriptors are set up once, and nothing drains between items.
+// Warp roles (16 warps):
+//   warp 0        TMA: each item's Q, then its K tiles into the 3-stage ring
+//   warp 1        S = Q K^T into one of three TMEM buffers (S(t) waits for its K tile and for
+//                 P V(t - 3), which read the buffer last)
+//   warp 2        TMA: V tiles into the 2-stage ring
+//   warp 3        O += P V.  The S and P V MMAs come from two threads: one thread issues a
+//                 tcgen05.mma with N = 128 about every 110 cycles, two threads together keep the
+//                 tensor pipe at its 64-cycle rate
+//   warps 4..11   softmax, two warps per TMEM lane quarter (each half of a row's 128 scores), as
+//                 in verify_attn_kernel; at the end of an item they hand the row statistics (m, l)
+//                 to the epilogue warps and go straight on to the next item's tiles
+//   warps 12..15  epilogue, one warp per lane quarter: the normalised output rows (or the split
+//                 partials) read from O as soon as the item's last P V has landed, then the
+//                 ancestor bits of the next item's tree tile (from its parent array)
+// TMEM: O at columns [0, 128), three S / P buffers at [128, 512).  An item's first P V waits until
+// the epilogue has read the previous item's O; the S tiles queued ahead of it keep the pipe busy.
+// Every ring position and barrier phase is counted over the whole CTA life (global tile counter,
+// item counter n over the CTA's non-empty items), so phases stay consistent across items.
 // ------------------------------------------------------------------------------------------------
+constexpr int NS_P = 3;                       // S / P buffers of the persistent kernel
+constexpr int NWARP_P = 16;
+constexpr int NT_P = NWARP_P * 32;
+constexpr uint32_t TM_S_P = 128;              // O at columns [0, 128)
+static_assert(TM_S_P + NS_P * BK <= 512, "TMEM budget");
+
 struct PersSmem {
     uint64_t k_full[ST_K], k_empty[ST_K], v_full[ST_V], v_empty[ST_V];
-    uint64_t s_full[NS], p_full[NS], pv_done[NS];
+    uint64_t s_full[NS_P], p_full[NS_P], pv_done[NS_P];
+    uint64_t q_full, q_empty;
+    uint64_t o_full, o_free;                  // the item's O complete / read by the epilogue
+    uint64_t anc_full[2], anc_empty[2];       // per ancestor-bit buffer (parity of the tree-tile item)
+    uint64_t l_full[2], l_empty[2];           // per row-statistics buffer (item parity)
     uint64_t s_done, pv_mma_done;
-    uint64_t q_full, q_empty, o_free;
-    uint64_t anc[64];
+    uint64_t anc[2][64];                      // [tree-item parity][slot]
     int32_t par[64];
-    float mx_x[2][2][MT];
-    float l_x[2][MT];
+    float mx_x[2][2][MT];                     // [tile parity][column half][row]
+    float l_x[2][2][MT];                      // [item parity][column half][row]
+    float m_x[2][MT];                         // [item parity][row]
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -732,7 +753,7 @@ E3_DEV ItemGeo item_geo(const Params &p, int it) {
     return w;
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT_P, 1)
     verify_attn_pers_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ CUtensorMap tm_tk, const __grid_constant__ CUtensorMap tm_tv,
                             const __grid_constant__ CUtensorMap tm_q, const Params p, const int items) {
@@ -751,16 +772,23 @@ __global__ void __launch_bounds__(NT, 1)
             tc::mbar_init(&ss.v_full[s], 1);
             tc::mbar_init(&ss.v_empty[s], 1);
         }
-        for (int u = 0; u < NS; ++u) {
+        for (int u = 0; u < NS_P; ++u) {
             tc::mbar_init(&ss.s_full[u], 1);
             tc::mbar_init(&ss.p_full[u], 8);
             tc::mbar_init(&ss.pv_done[u], 1);
         }
-        tc::mbar_init(&ss.s_done, 1);
-        tc::mbar_init(&ss.pv_mma_done, 1);
+        tc::mbar_init(&ss.o_full, 1);
+        tc::mbar_init(&ss.o_free, 4);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&ss.anc_full[b], 4);
+            tc::mbar_init(&ss.anc_empty[b], 8);
+            tc::mbar_init(&ss.l_full[b], 256);       // every softmax thread, after its own writes
+            tc::mbar_init(&ss.l_empty[b], 128);      // every epilogue thread, after its own reads
+        }
         tc::mbar_init(&ss.q_full, 1);
         tc::mbar_init(&ss.q_empty, 1);
-        tc::mbar_init(&ss.o_free, 8);
+        tc::mbar_init(&ss.s_done, 1);
+        tc::mbar_init(&ss.pv_mma_done, 1);
         ss.abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -772,10 +800,7 @@ __global__ void __launch_bounds__(NT, 1)
     pdl_wait();   // the previous kernel's outputs (q / tree keys / caches) before any global access
     pdl_trigger();
 
-    auto k_tile = [&](uint32_t t) -> uint8_t * { return sm + OFF_K + (t % ST_K) * KV_TILE; };
-    auto v_tile = [&](uint32_t t) -> uint8_t * { return sm + OFF_V + (t % ST_V) * KV_TILE; };
-
-    if (warp == 0 || warp == 10) {
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------------ TMA producers
         if (lane == 0) {
             const bool is_k = warp == 0;
@@ -867,43 +892,43 @@ __global__ void __launch_bounds__(NT, 1)
             constexpr uint32_t IDESC_P = tc::idesc_bf16(MT, BK);
             constexpr uint32_t IDESC_T = tc::idesc_bf16(MT, BKT);
             const uint32_t qaddr = smem_u32(sm + OFF_Q);
-            uint32_t kt = 0, st = 0, qn = 0;
+            uint32_t kt = 0, n = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 const ItemGeo w = item_geo(p, it);
                 if (w.n_tiles == 0) continue;
-                if (!tc::mbar_wait(&ss.q_full, qn & 1u, abort, p.wait_limit)) {
+                if (!tc::mbar_wait(&ss.q_full, n & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
-                for (int j = 0; j < w.n_tiles; ++j, ++kt, ++st) {
+                for (int j = 0; j < w.n_tiles; ++j, ++kt) {
                     const bool tree = j == w.n_prefix;
                     if (!tc::mbar_wait(&ss.k_full[kt % ST_K], (kt / ST_K) & 1u, abort, p.wait_limit)) {
                         ok = false;
                         break;
                     }
-                    // buffer st % NS last held P(st - NS): its P V must have read it
-                    if (st >= NS && !tc::mbar_wait(&ss.pv_done[st % NS], ((st - NS) / NS) & 1u, abort, p.wait_limit)) {
+                    // buffer kt % NS_P last held P(kt - 3): its P V must have read it
+                    if (kt >= NS_P &&
+                        !tc::mbar_wait(&ss.pv_done[kt % NS_P], ((kt - NS_P) / NS_P) & 1u, abort, p.wait_limit)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t kaddr = smem_u32(k_tile(kt));
-                    const uint32_t kblk = KV_TILE / 2;
-                    const uint32_t d_s = tmem + TM_S + (uint32_t)((st % NS) * BK);
+                    const uint32_t kaddr = smem_u32(sm + OFF_K + (kt % ST_K) * KV_TILE);
+                    const uint32_t d_s = tmem + TM_S_P + (kt % NS_P) * (uint32_t)BK;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t blk = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-                        tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kk * 32),
-                                        tc::desc_sw128(kaddr + blk * kblk + kk * 32), tree ? IDESC_T : IDESC_P,
+                        const uint32_t blk = (uint32_t)(k >> 2), kq = (uint32_t)(k & 3);
+                        tc::mma_bf16_ss(d_s, tc::desc_sw128(qaddr + blk * (Q_TILE / 2) + kq * 32),
+                                        tc::desc_sw128(kaddr + blk * (KV_TILE / 2) + kq * 32), tree ? IDESC_T : IDESC_P,
                                         k > 0 ? 1u : 0u);
                     }
-                    tc::mma_commit(&ss.s_full[st % NS]);
+                    tc::mma_commit(&ss.s_full[kt % NS_P]);
                     tc::mma_commit(&ss.k_empty[kt % ST_K]);
                 }
                 if (!ok) break;
                 tc::mma_commit(&ss.q_empty);   // the item's S MMAs are done with Q
-                ++qn;
+                ++n;
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             tc::mma_commit(&ss.s_done);
@@ -911,41 +936,40 @@ __global__ void __launch_bounds__(NT, 1)
             while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < p.wait_limit) {
             }
         }
-    } else if (warp == 11) {
+    } else if (warp == 3) {
         // ------------------------------------------------------------------ O += P V issuer
         if (lane == 0) {
             constexpr uint32_t IDESC_PV = tc::idesc_bf16_bmn(MT, D);
-            uint32_t vt = 0, st = 0, qn = 0;
+            uint32_t vt = 0, n = 0;
             bool ok = true;
             for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
                 const ItemGeo w = item_geo(p, it);
                 if (w.n_tiles == 0) continue;
-                for (int j = 0; j < w.n_tiles; ++j, ++vt, ++st) {
+                for (int j = 0; j < w.n_tiles; ++j, ++vt) {
                     const bool tree = j == w.n_prefix;
                     if (!tc::mbar_wait(&ss.v_full[vt % ST_V], (vt / ST_V) & 1u, abort, p.wait_limit) ||
-                        !tc::mbar_wait(&ss.p_full[st % NS], (st / NS) & 1u, abort, p.wait_limit)) {
+                        !tc::mbar_wait(&ss.p_full[vt % NS_P], (vt / NS_P) & 1u, abort, p.wait_limit)) {
                         ok = false;
                         break;
                     }
-                    // the item's first P V overwrites O: the previous item's epilogue must have read it
-                    if (j == 0 && qn > 0 && !tc::mbar_wait(&ss.o_free, (qn - 1) & 1u, abort, p.wait_limit)) {
+                    // the item's first P V overwrites O: the epilogue must have read the previous item's
+                    if (j == 0 && n >= 1 && !tc::mbar_wait(&ss.o_free, (n - 1) & 1u, abort, p.wait_limit)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t vaddr = smem_u32(v_tile(vt));
-                    const uint32_t vblk = KV_TILE / 2;
-                    const uint32_t t_p = tmem + TM_S + (uint32_t)((st % NS) * BK);   // P over S
+                    const uint32_t vaddr = smem_u32(sm + OFF_V + (vt % ST_V) * KV_TILE);
+                    const uint32_t t_p = tmem + TM_S_P + (vt % NS_P) * (uint32_t)BK;   // P over S
                     const int ksteps = (tree ? BKT : BK) / 16;
-                    for (int kk = 0; kk < ksteps; ++kk) {
+                    for (int kk = 0; kk < ksteps; ++kk)
                         tc::mma_bf16_ts(tmem, t_p + (uint32_t)(kk * 8),
-                                        tc::desc_mn_sw128(vaddr + kk * 2048, vblk, 1024), IDESC_PV,
+                                        tc::desc_mn_sw128(vaddr + kk * 2048, KV_TILE / 2, 1024), IDESC_PV,
                                         (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::mma_commit(&ss.pv_done[st % NS]);
+                    tc::mma_commit(&ss.pv_done[vt % NS_P]);
                     tc::mma_commit(&ss.v_empty[vt % ST_V]);
+                    if (j == w.n_tiles - 1) tc::mma_commit(&ss.o_full);
                 }
-                ++qn;
+                ++n;
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
             tc::mma_commit(&ss.pv_mma_done);
@@ -953,96 +977,38 @@ __global__ void __launch_bounds__(NT, 1)
             while (!tc::mbar_try(&ss.pv_mma_done, 0) && clock64() - t0 < p.wait_limit) {
             }
         }
-    } else {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ softmax warps
-        const int w8 = warp - 2;
+        const int w8 = warp - 4;
         const int quarter = warp & 3;
         const int hc = w8 >> 2;
         const int rl = quarter * 32 + lane;              // row within the M tile
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-        uint32_t st = 0, qn = 0;
+        uint32_t st = 0, n = 0, na = 0;                  // na: items with a tree tile so far
         bool ok = true;
-        const int per_b = p.halves * p.splits * p.Hkv;   // work items per sequence
-        int walked = -1;                                  // the item whose ancestor bits ss.anc holds
-        // ancestor-or-self bits of sequence b from parent values already in ss.par: slot i walks its
-        // own parent chain (the softmax warps only; the caller synchronises before and after)
-        auto walk = [&](bool flag_bad) {
-            const int i = tid - 64;
-            if (i < nk) {
-                auto invalid = [&](int j) {
-                    const int pj = ss.par[j];
-                    return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
-                };
-                uint64_t bits = 1ull << i;
-                int j = i;
-                const bool bad = invalid(i);
-                while (j > 0 && !invalid(j)) {
-                    j = ss.par[j];
-                    bits |= 1ull << j;
-                }
-                ss.anc[i] = bits;
-                if (bad && flag_bad) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
-            }
-        };
         for (int it = blockIdx.x; it < items; it += gridDim.x) {
             const ItemGeo w = item_geo(p, it);
-            const bool first_of_seq = w.split == 0 && w.g == 0 && w.half == 0;
-            if (w.clamped && first_of_seq && tid == 64) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
-            const int nq = p.q_hi - p.q_lo;
-            if (w.n_tiles == 0) {
-                // an empty split: its partial (m = -inf, l = 0, O = 0) for the merge
-                if (p.splits > 1 && rl < w.nrows) {
-                    const int qi = w.s_lo - p.q_lo + rl / rep, h = w.g * rep + rl % rep;
-                    const size_t prow_i = ((size_t)w.b * nq + qi) * p.Hq + h;
-                    const size_t rows_all = (size_t)p.B * nq * p.Hq;
-                    float *po = p.part_o + ((size_t)w.split * rows_all + prow_i) * D + (size_t)hc * 64;
-                    for (int cc = 0; cc < 64; cc += 4) *reinterpret_cast<float4 *>(po + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (hc == 0) {
-                        float *pm = p.part_ml + ((size_t)w.split * rows_all + prow_i) * 2;
-                        pm[0] = -INFINITY;
-                        pm[1] = 0.0f;
-                    }
-                }
-                continue;
-            }
-            // ancestor-or-self bits of the item's sequence (usually walked already, after the previous
-            // item's last tile, from parents loaded during that item)
-            if (walked != it) {
-                asm volatile("bar.sync 1, 256;" ::: "memory");   // the previous bits are no longer read
-                {
-                    const int i = tid - 64;
-                    if (i < nk) ss.par[i] = __ldg(p.parents + (size_t)w.b * p.n_slots + i);
-                }
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                walk(first_of_seq);
-                walked = it;
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            // the next item's parent values, loaded now so that their latency hides behind the tiles
-            const int it_next = it + gridDim.x;
-            int par_next = 0;
-            if (it_next < items && tid - 64 < nk)
-                par_next = __ldg(p.parents + (size_t)(it_next / per_b) * p.n_slots + (tid - 64));
-            // only these item values stay live through the tile loop (the epilogue recomputes the rest;
-            // the tree tile reads its row's ancestor bits from shared memory)
+            if (w.n_tiles == 0) continue;
             const int n_tiles = w.n_tiles, n_prefix = w.n_prefix, k_lo = w.k_lo, k_hi = w.k_hi;
             const int anc_slot = rl < w.nrows ? w.s_lo + rl / rep : -1;
+            const uint32_t o_acc = t_lane;
             float m_run = -INFINITY, l_run = 0.0f;
             for (int j = 0; j < n_tiles; ++j, ++st) {
-                const int u = (int)(st % NS);
-                if (ok && !warp_wait(&ss.s_full[u], (st / NS) & 1u, abort, p.wait_limit)) ok = false;
+                const int u = (int)(st % NS_P);
+                if (ok && !warp_wait(&ss.s_full[u], (st / NS_P) & 1u, abort, p.wait_limit)) ok = false;
                 tc::fence_after();
                 const bool tree = j == n_prefix;
                 const int hw = (tree ? BKT : BK) / 2;
                 const int col0 = hc * hw;
+                const uint32_t t_s = t_lane + TM_S_P + (uint32_t)(u * BK);
                 float sc[64];
                 {
                     float a[32];
-                    tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0), a);
+                    tc::tmem_ld32(t_s + (uint32_t)col0, a);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) sc[i] = a[i];
                     if (hw == 64) {
-                        tc::tmem_ld32(t_lane + TM_S + (uint32_t)(u * BK + col0 + 32), a);
+                        tc::tmem_ld32(t_s + (uint32_t)(col0 + 32), a);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) sc[32 + i] = a[i];
                     } else {
@@ -1057,7 +1023,11 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], sc[i], sc[i + 1]);
                 } else {
-                    const uint64_t bits = (tree && anc_slot >= 0) ? ss.anc[anc_slot] : 0ull;
+                    uint64_t bits = 0ull;
+                    if (tree) {   // the epilogue warps have walked this item's tree
+                        if (ok && !warp_wait(&ss.anc_full[na & 1u], (na >> 1) & 1u, abort, p.wait_limit)) ok = false;
+                        if (anc_slot >= 0) bits = ss.anc[na & 1u][anc_slot];
+                    }
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
                         const int key = col0 + i;
@@ -1075,25 +1045,10 @@ __global__ void __launch_bounds__(NT, 1)
                 mx = fmaxf(mx, ss.mx_x[st & 1][hc ^ 1][rl]);
                 const bool need = (m_run == -INFINITY) ? (mx > -INFINITY) : (mx > m_run + RESCALE_LOG2);
                 const bool any_need = __any_sync(0xffffffffu, need);
-                if (any_need && j > 0) {
-                    if (ok && !warp_wait(&ss.pv_done[(st - 1) % NS], ((st - 1) / NS) & 1u, abort, p.wait_limit))
-                        ok = false;
-                    tc::fence_after();
-                }
+                float corr = 1.0f;
                 if (any_need) {
                     const float m_new = need ? fmaxf(m_run, mx) : m_run;
-                    const float corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
-                    if (j > 0) {
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            float o[32];
-                            const uint32_t ta = t_lane + (uint32_t)(hc * 64 + cc * 32);
-                            tc::tmem_ld32(ta, o);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= corr;
-                            tc::tmem_st32(ta, o);
-                        }
-                    }
+                    corr = need ? (m_run == -INFINITY ? 0.0f : fast_exp2(m_run - m_new)) : 1.0f;
                     l_run *= corr;
                     m_run = m_new;
                 }
@@ -1112,89 +1067,162 @@ __global__ void __launch_bounds__(NT, 1)
                 const float2 s01 = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
                 l_run += s01.x + s01.y;
                 if (hw == 64)
-                    tc::tmem_st32u(t_lane + TM_S + (uint32_t)(u * BK + hc * 32), pk);
+                    tc::tmem_st32u(t_s + (uint32_t)(hc * 32), pk);
                 else
-                    tc::tmem_st16u(t_lane + TM_S + (uint32_t)(u * BK + hc * 16), pk);
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.p_full[u]);
-            }
-            // the next item's ancestor bits (this item's tree tile, its last, has read the current ones)
-            if (it_next < items) {
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                if (tid - 64 < nk) ss.par[tid - 64] = par_next;
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                const ItemGeo wn = item_geo(p, it_next);
-                walk(wn.split == 0 && wn.g == 0 && wn.half == 0);
-                walked = it_next;
-            }
-            // ---- epilogue of the item: this warp's 64 columns of O / l, then O is free for the next
-            // item; bf16 outputs are packed before O is released and stored after
-            const ItemGeo we = item_geo(p, it);
-            ss.l_x[hc][rl] = l_run;
-            asm volatile("bar.sync 2, 256;" ::: "memory");
-            const float l_all = ss.l_x[0][rl] + ss.l_x[1][rl];
-            const bool have =
-                ok && warp_wait(&ss.pv_done[(st - 1) % NS], ((st - 1) / NS) & 1u, abort, p.wait_limit);
-            if (!have) ok = false;
-            tc::fence_after();
-            const float m_fin = have ? m_run : -INFINITY, l_fin = have ? l_all : 0.0f;
-            const bool row_ok = rl < we.nrows;
-            const int qi = we.s_lo - p.q_lo + rl / rep, h = we.g * rep + rl % rep;
-            const size_t prow_i = ((size_t)we.b * nq + qi) * p.Hq + h;
-            const size_t rows_all = (size_t)p.B * nq * p.Hq;
-            const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
-            if (p.splits == 1) {
-                uint32_t pk[32];                  // this warp's 64 columns of the row, packed bf16 pairs
+                    tc::tmem_st16u(t_s + (uint32_t)(hc * 16), pk);
+                // O rescaled (the scores are dead by now) once P V of the previous tile has landed in
+                // it, and before this tile's P V, which waits for the P arrival below
+                if (any_need && j > 0) {
+                    if (ok && !warp_wait(&ss.pv_done[(st - 1) % NS_P], ((st - 1) / NS_P) & 1u, abort, p.wait_limit))
+                        ok = false;
+                    tc::fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float t[32];
-                    tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float o[32];
+                        const uint32_t ta = o_acc + (uint32_t)(hc * 64 + cc * 32);
+                        tc::tmem_ld32(ta, o);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        __nv_bfloat162 hv = __floats2bfloat162_rn(have ? t[2 * e] * inv_l : 0.0f,
-                                                                  have ? t[2 * e + 1] * inv_l : 0.0f);
-                        pk[cc * 16 + e] = *reinterpret_cast<uint32_t *>(&hv);
+                        for (int i = 0; i < 32; ++i) o[i] *= corr;
+                        tc::tmem_st32(ta, o);
                     }
                 }
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.o_free);
-                if (row_ok) {
-                    __nv_bfloat16 *dst =
-                        p.out + (size_t)we.b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D + (size_t)hc * 64;
+                if (lane == 0) tc::mbar_arrive(&ss.p_full[u]);
+            }
+            // the item's ancestor bits are no longer read; its row statistics go to the epilogue
+            if (w.last) {
+                if (lane == 0) tc::mbar_arrive(&ss.anc_empty[na & 1u]);
+                ++na;
+            }
+            if (n >= 2 && ok && !warp_wait(&ss.l_empty[n & 1u], ((n - 2) >> 1) & 1u, abort, p.wait_limit)) ok = false;
+            ss.l_x[n & 1u][hc][rl] = l_run;
+            if (hc == 0) ss.m_x[n & 1u][rl] = m_run;
+            tc::mbar_arrive(&ss.l_full[n & 1u]);
+            ++n;
+        }
+        if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------------ epilogue warps
+        const int quarter = warp & 3;
+        const int rl = quarter * 32 + lane;
+        const int te = tid - 12 * 32;                    // 0..127
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int nq = p.q_hi - p.q_lo;
+        const size_t rows_all = (size_t)p.B * nq * p.Hq;
+        bool ok = true;
+        uint32_t n = 0, na = 0;
+        // ancestor-or-self bits of a tree-tile item's tree into ss.anc[m & 1] (m counts those items): slot i
+        // walks its own parent chain
+        auto prepare_anc = [&](const ItemGeo &w, uint32_t m, int par_val) {
+            if (m >= 2 && ok && !warp_wait(&ss.anc_empty[m & 1u], ((m - 2) >> 1) & 1u, abort, p.wait_limit)) ok = false;
+            if (te < nk) ss.par[te] = par_val;
+            asm volatile("bar.sync 3, 128;" ::: "memory");
+            if (te < nk) {
+                auto invalid = [&](int j) {
+                    const int pj = ss.par[j];
+                    return j == 0 ? pj != -1 : (pj < 0 || pj >= j);
+                };
+                uint64_t bits = 1ull << te;
+                int j = te;
+                const bool bad = invalid(te);
+                while (j > 0 && !invalid(j)) {
+                    j = ss.par[j];
+                    bits |= 1ull << j;
+                }
+                ss.anc[m & 1u][te] = bits;
+                if (bad && w.g == 0 && w.half == 0) flag(p.dev_status, EAGLE3_DEV_BAD_TREE);
+            }
+            asm volatile("bar.sync 3, 128;" ::: "memory");   // every walk done before ss.par changes
+            if (lane == 0) tc::mbar_arrive(&ss.anc_full[m & 1u]);
+        };
+        auto epilogue = [&](const ItemGeo &w, uint32_t m) {
+            bool have = ok && warp_wait(&ss.l_full[m & 1u], (m >> 1) & 1u, abort, p.wait_limit);
+            const float l_all = ss.l_x[m & 1u][0][rl] + ss.l_x[m & 1u][1][rl];
+            const float m_row = ss.m_x[m & 1u][rl];
+            tc::mbar_arrive(&ss.l_empty[m & 1u]);
+            have = have && warp_wait(&ss.o_full, m & 1u, abort, p.wait_limit);
+            if (!have) ok = false;
+            tc::fence_after();
+            const float m_fin = have ? m_row : -INFINITY, l_fin = have ? l_all : 0.0f;
+            const bool row_ok = rl < w.nrows;
+            const int qi = w.s_lo - p.q_lo + rl / rep, h = w.g * rep + rl % rep;
+            const size_t prow_i = ((size_t)w.b * nq + qi) * p.Hq + h;
+            const float inv_l = l_fin > 0.0f ? 1.0f / l_fin : 0.0f;
+            const uint32_t o_acc = t_lane;
+            if (p.splits == 1) {
+                __nv_bfloat16 *dst = p.out + (size_t)w.b * p.o_sb + (size_t)qi * p.o_si + (size_t)h * D;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    float t[32];
+                    tc::tmem_ld32(o_acc + (uint32_t)(cc * 32), t);   // warp-collective
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8)
-                        *reinterpret_cast<uint4 *>(dst + 8 * c8) =
-                            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 hv = __floats2bfloat162_rn(have ? t[2 * e] * inv_l : 0.0f,
+                                                                  have ? t[2 * e + 1] * inv_l : 0.0f);
+                        pk[e] = *reinterpret_cast<uint32_t *>(&hv);
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            *reinterpret_cast<uint4 *>(dst + cc * 32 + 8 * c8) =
+                                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+                    }
                 }
             } else {
+                float *po = p.part_o + ((size_t)w.split * rows_all + prow_i) * D;
 #pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < 4; ++cc) {
                     float t[32];
-                    tc::tmem_ld32(t_lane + (uint32_t)(hc * 64 + cc * 32), t);   // warp-collective
+                    tc::tmem_ld32(o_acc + (uint32_t)(cc * 32), t);   // warp-collective
                     if (!row_ok) continue;
-                    float *po = p.part_o + ((size_t)we.split * rows_all + prow_i) * D + (size_t)hc * 64 + cc * 32;
 #pragma unroll
                     for (int c4 = 0; c4 < 32; c4 += 4)
-                        *reinterpret_cast<float4 *>(po + c4) =
+                        *reinterpret_cast<float4 *>(po + cc * 32 + c4) =
                             have ? make_float4(t[c4], t[c4 + 1], t[c4 + 2], t[c4 + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&ss.o_free);
             }
-            ++qn;
-            if (row_ok && hc == 0) {
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ss.o_free);
+            if (row_ok) {
                 if (p.splits == 1) {
                     if (p.lse) p.lse[prow_i] = (m_fin + log2f(l_fin)) * 0.6931471805599453f;
                 } else {
-                    float *pm = p.part_ml + ((size_t)we.split * rows_all + prow_i) * 2;
+                    float *pm = p.part_ml + ((size_t)w.split * rows_all + prow_i) * 2;
                     pm[0] = m_fin;
                     pm[1] = l_fin;
                 }
             }
+        };
+        ItemGeo prev;
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            const ItemGeo w = item_geo(p, it);
+            const bool first_of_seq = w.split == 0 && w.g == 0 && w.half == 0;
+            if (w.clamped && first_of_seq && te == 0) flag(p.dev_status, EAGLE3_DEV_CAPACITY);
+            if (w.n_tiles == 0) {
+                // an empty split: its partial (m = -inf, l = 0, O = 0) for the merge
+                if (p.splits > 1 && rl < w.nrows) {
+                    const int qi = w.s_lo - p.q_lo + rl / rep, h = w.g * rep + rl % rep;
+                    const size_t prow_i = ((size_t)w.b * nq + qi) * p.Hq + h;
+                    float *po = p.part_o + ((size_t)w.split * rows_all + prow_i) * D;
+                    for (int cc = 0; cc < D; cc += 4) *reinterpret_cast<float4 *>(po + cc) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float *pm = p.part_ml + ((size_t)w.split * rows_all + prow_i) * 2;
+                    pm[0] = -INFINITY;
+                    pm[1] = 0.0f;
+                }
+                continue;
+            }
+            // the parent values load while the previous item's epilogue waits for its last P V; only
+            // an item with the tree tile (the last split) needs the ancestor bits
+            const int par_val = (w.last && te < nk) ? __ldg(p.parents + (size_t)w.b * p.n_slots + te) : 0;
+            if (n >= 1) epilogue(prev, n - 1);
+            if (w.last) prepare_anc(w, na++, par_val);
+            prev = w;
+            ++n;
         }
+        if (n >= 1) epilogue(prev, n - 1);
         if (!ok && lane == 0) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
     }
 
@@ -1500,7 +1528,7 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
         // rotated q with a parent array: one persistent CTA per SM walks the work items
         const int items = splits * p.halves * a.Hkv * pt.nb;
         const int grid = std::min(items, sm_count_cached());
-        if (launch_pdl(verify_attn_pers_kernel, dim3(grid), dim3(NT), SMEM_DYN, stream, mk, mv, mtk, mtv, mq, p,
+        if (launch_pdl(verify_attn_pers_kernel, dim3(grid), dim3(NT_P), SMEM_DYN, stream, mk, mv, mtk, mtv, mq, p,
                        items) != cudaSuccess)
             return EAGLE3_ERR_CUDA;
     } else if (launch_pdl(verify_attn_kernel, dim3(splits * p.halves, a.Hkv, pt.nb), dim3(NT), SMEM_DYN, stream, mk,
