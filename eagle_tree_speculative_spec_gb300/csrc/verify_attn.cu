@@ -125,6 +125,17 @@ E3_DEV float fmax3(float a, float b, float c) {
     return r;
 }
 
+// Visibility of a row's half tile as a bit mask: bit i set when column col0 + i (i < hw) is a key the
+// row sees: on the tree tile an ancestor-or-self slot below nk (anc_bits: the row's slot bits), on a
+// prefix tile a key below k_hi (key0: the key of column col0).  Built once per tile, so the per-score
+// test is a fixed-position bit test.
+E3_DEV uint64_t visible_mask(bool tree, uint64_t anc_bits, int col0, int nk, int key0, int k_hi, int hw) {
+    const int n = min(hw, tree ? nk - col0 : k_hi - key0);   // columns in range
+    uint64_t m = n >= 64 ? ~0ull : (n <= 0 ? 0ull : ((1ull << n) - 1ull));
+    if (tree) m &= anc_bits >> col0;                         // col0 < 64 on the tree tile
+    return m;
+}
+
 // warp-uniform bounded wait (lane 0 polls, the outcome is broadcast)
 E3_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, long long limit) {
     int ok = 0;
@@ -547,11 +558,11 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int i = 0; i < 64; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], sc[i], sc[i + 1]);
             } else {
+                const uint64_t vm = visible_mask(tree, bits, col0, nk, key0, k_hi, hw);
+                const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
-                    const int key = col0 + i;            // tree: node index
-                    const bool valid =
-                        i < hw && (tree ? (key < nk && ((bits >> key) & 1ull)) : (key0 + i < k_hi));
+                    const bool valid = (((i < 32) ? vlo : vhi) >> (i & 31)) & 1u;
                     sc[i] = valid ? sc[i] : -INFINITY;
                     mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
                 }
@@ -684,9 +695,11 @@ __global__ void __launch_bounds__(NT, 1)
 // array: one CTA per SM walks the work items (sequence, KV head, split, half) c, c + grid, ...
 // Barriers, TMEM and the TMA descriptors are set up once, and nothing drains between items.
 // Warp roles (16 warps):
-//   warp 0        TMA: each item's Q, then its K tiles into the 3-stage ring
+//   warp 0        TMA: K tiles into the 3-stage ring, running ahead across items
 //   warp 1        S = Q K^T into one of three TMEM buffers (S(t) waits for its K tile and for
-//                 P V(t - 3), which read the buffer last)
+//                 P V(t - 3), which read the buffer last).  This thread also loads each item's Q:
+//                 the next item's Q may only land once the item's last S has read the buffer, and
+//                 S waits for it anyway, so the K producer never stalls on it
 //   warp 2        TMA: V tiles into the 2-stage ring
 //   warp 3        O += P V.  The S and P V MMAs come from two threads: one thread issues a
 //                 tcgen05.mma with N = 128 about every 110 cycles, two threads together keep the
@@ -812,29 +825,11 @@ __global__ void __launch_bounds__(NT_P, 1)
             uint8_t *ring = sm + (is_k ? OFF_K : OFF_V);
             tc::prefetch_tmap(map);
             tc::prefetch_tmap(tmap);
-            if (is_k) tc::prefetch_tmap(&tm_q);
-            uint32_t t = 0, qn = 0;
+            uint32_t t = 0;
             bool go = true;
             for (int it = blockIdx.x; it < items && go; it += gridDim.x) {
                 const ItemGeo w = item_geo(p, it);
                 if (w.n_tiles == 0) continue;
-                if (is_k) {
-                    // Q of this item: the previous item's S MMAs must have read the buffer
-                    if (qn > 0 && !tc::mbar_wait(&ss.q_empty, (qn - 1) & 1u, abort, p.wait_limit)) {
-                        go = false;
-                        break;
-                    }
-                    tc::mbar_expect_tx(&ss.q_full, Q_TILE);
-                    const int hs = w.g * rep;
-                    if (p.tree_slot_inner) {
-                        tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, w.s_lo, w.b, &ss.q_full);
-                        tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, w.s_lo, w.b, &ss.q_full);
-                    } else {
-                        tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, w.b, w.s_lo, &ss.q_full);
-                        tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, w.b, w.s_lo, &ss.q_full);
-                    }
-                    ++qn;
-                }
                 const int row0 = ((w.b * p.Hkv + w.g) * p.S) + w.k_lo;
                 for (int j = 0; j < w.n_tiles; ++j, ++t) {
                     const int s = (int)(t % stages);
@@ -874,15 +869,10 @@ __global__ void __launch_bounds__(NT_P, 1)
                 }
             }
             if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
-            // no TMA write may be in flight when the CTA exits: the last load of every stage, and Q
+            // no TMA write may be in flight when the CTA exits: the last load of every stage
             for (uint32_t u = t > (uint32_t)stages ? t - stages : 0; u < t; ++u) {
                 const long long t0 = clock64();
                 while (!tc::mbar_try(&full[u % stages], (u / stages) & 1u) && clock64() - t0 < p.wait_limit) {
-                }
-            }
-            if (is_k && qn > 0) {
-                const long long t0 = clock64();
-                while (!tc::mbar_try(&ss.q_full, (qn - 1) & 1u) && clock64() - t0 < p.wait_limit) {
                 }
             }
         }
@@ -892,15 +882,37 @@ __global__ void __launch_bounds__(NT_P, 1)
             constexpr uint32_t IDESC_P = tc::idesc_bf16(MT, BK);
             constexpr uint32_t IDESC_T = tc::idesc_bf16(MT, BKT);
             const uint32_t qaddr = smem_u32(sm + OFF_Q);
-            uint32_t kt = 0, n = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+            tc::prefetch_tmap(&tm_q);
+            // the CTA's next item with tiles after `it`, or items
+            auto next_item = [&](int it) {
+                for (it += gridDim.x; it < items; it += gridDim.x)
+                    if (item_geo(p, it).n_tiles > 0) return it;
+                return items;
+            };
+            // the item's Q: two 64-column boxes (column, first head of the KV group, then slot and
+            // sequence in the order of the tensor map's dimensions)
+            auto load_q = [&](int it) {
                 const ItemGeo w = item_geo(p, it);
-                if (w.n_tiles == 0) continue;
+                const int c1 = w.g * rep, c2 = p.tree_slot_inner ? w.s_lo : w.b, c3 = p.tree_slot_inner ? w.b : w.s_lo;
+                tc::mbar_expect_tx(&ss.q_full, Q_TILE);
+                tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, c1, c2, c3, &ss.q_full);
+                tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, c1, c2, c3, &ss.q_full);
+            };
+            uint32_t kt = 0, n = 0;
+            bool ok = true, q_pending = false;
+            int it = next_item(blockIdx.x - (int)gridDim.x);
+            if (it < items) {
+                load_q(it);
+                q_pending = true;
+            }
+            for (; it < items && ok;) {
+                const ItemGeo w = item_geo(p, it);
+                const int it_next = next_item(it);
                 if (!tc::mbar_wait(&ss.q_full, n & 1u, abort, p.wait_limit)) {
                     ok = false;
                     break;
                 }
+                q_pending = false;
                 for (int j = 0; j < w.n_tiles; ++j, ++kt) {
                     const bool tree = j == w.n_prefix;
                     if (!tc::mbar_wait(&ss.k_full[kt % ST_K], (kt / ST_K) & 1u, abort, p.wait_limit)) {
@@ -928,9 +940,24 @@ __global__ void __launch_bounds__(NT_P, 1)
                 }
                 if (!ok) break;
                 tc::mma_commit(&ss.q_empty);   // the item's S MMAs are done with Q
+                if (it_next < items) {
+                    // the next item's Q once this item's S MMAs have read the buffer
+                    if (!tc::mbar_wait(&ss.q_empty, n & 1u, abort, p.wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    load_q(it_next);
+                    q_pending = true;
+                }
                 ++n;
+                it = it_next;
             }
             if (!ok) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
+            if (q_pending) {   // no TMA write may be in flight when the CTA exits
+                const long long t0 = clock64();
+                while (!tc::mbar_try(&ss.q_full, n & 1u) && clock64() - t0 < p.wait_limit) {
+                }
+            }
             tc::mma_commit(&ss.s_done);
             const long long t0 = clock64();
             while (!tc::mbar_try(&ss.s_done, 0) && clock64() - t0 < p.wait_limit) {
@@ -1028,11 +1055,11 @@ __global__ void __launch_bounds__(NT_P, 1)
                         if (ok && !warp_wait(&ss.anc_full[na & 1u], (na >> 1) & 1u, abort, p.wait_limit)) ok = false;
                         if (anc_slot >= 0) bits = ss.anc[na & 1u][anc_slot];
                     }
+                    const uint64_t vm = visible_mask(tree, bits, col0, nk, key0, k_hi, hw);
+                    const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
-                        const int key = col0 + i;
-                        const bool valid =
-                            i < hw && (tree ? (key < nk && ((bits >> key) & 1ull)) : (key0 + i < k_hi));
+                        const bool valid = (((i < 32) ? vlo : vhi) >> (i & 31)) & 1u;
                         sc[i] = valid ? sc[i] : -INFINITY;
                         mq[i & 3] = fmaxf(mq[i & 3], sc[i]);
                     }
