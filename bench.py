@@ -526,7 +526,7 @@ def run_gpu(args):
 
 # DRAM bytes (read + write) of one SwiGLU gate+up launch at the bench shape, from an ncu capture of the
 # current GEMM kernel (to be set to None when the kernel changes)
-GATEUP_TRAFFIC_BYTES = 267724288 + 97391360
+GATEUP_TRAFFIC_BYTES = 267338240 + 100351232
 
 
 def _draft_launches(cfg):
