@@ -24,6 +24,7 @@
 
 #include "../../include/eagle3_linear.h"
 #include "attn.cuh"
+#include "tc.cuh"
 
 namespace e3 {
 namespace {
@@ -259,6 +260,30 @@ template <int NT> struct TopkSmem {
     uint64_t s_cta;                 // this CTA's share of the normaliser (cluster version)
 };
 
+// The CTA's warps' lists merged into sm.fin and the per-thread normaliser terms summed (the sum is
+// returned, valid in thread 0)
+template <int NT> E3_DEV uint64_t topk_finish(TopkSmem<NT> &sm, uint64_t s, int k) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) sm.sred[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t best[KMAX], res[KMAX];
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT / 32 ? sm.wres[lane][q] : 0ull;
+        warp_merge(best, res, k);
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) sm.fin[q] = res[q];
+    }
+    uint64_t S = 0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < NT / 32; ++w) S += sm.sred[w];
+    __syncthreads();
+    return S;
+}
+
 // Top-k candidates of the slice [lo, hi) of row z into sm.fin (sorted, KMAX entries, the first k
 // meaningful; 0 = none) and, in the same pass over the slice, its fixed-point normaliser terms with
 // m = the row maximum (known beforehand: the LM head's epilogue published it): the CTA's sum is
@@ -326,24 +351,7 @@ template <int NT> E3_DEV uint64_t topk_slice(TopkSmem<NT> &sm, const float *z, i
         offer(v, (uint32_t)(lo + i), valid);
     }
     if (cnt > 0) flush();
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sm.sred[warp] = s;
-    __syncthreads();
-    if (warp == 0) {
-        uint64_t best[KMAX], res[KMAX];
-#pragma unroll
-        for (int q = 0; q < KMAX; ++q) best[q] = lane < NT / 32 ? sm.wres[lane][q] : 0ull;
-        warp_merge(best, res, k);
-        if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < KMAX; ++q) sm.fin[q] = res[q];
-    }
-    uint64_t S = 0;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < NT / 32; ++w) S += sm.sred[w];
-    __syncthreads();
-    return S;
+    return topk_finish(sm, s, k);
 }
 
 // Output of a row's top-k: token ids (through the draft-to-target map when there is one) and logq.
@@ -382,6 +390,131 @@ __global__ void __launch_bounds__(NT)
     const float m = key_to_float(__ldg(row_max + row));
     const uint64_t s = topk_slice(sm, z, 0, V, k, m);
     if (threadIdx.x == 0) S = s;
+    __syncthreads();
+    topk_write(sm.fin, S, m, row, V, k, o);
+}
+
+// One CTA of NT threads per row, the row streamed through a shared-memory ring: thread 0 issues
+// bulk copies of TKR_CHUNK-float chunks (TKR_STAGES in flight), every warp scans each chunk from
+// shared memory as it lands.  The bytes in flight per CTA no longer depend on registers (the
+// register-fed loop keeps four 16-byte loads per thread in flight), so a wave of rows streams
+// at a higher rate.  Same selection and normaliser arithmetic as topk_slice, so the result is
+// bit-identical.  Needs a row length and a row pitch that are multiples of 4 floats, 16-byte
+// aligned logits.  All waits are bounded (EAGLE3_DEV_TIMEOUT, the CTA drains its copies).
+constexpr int TKR_CHUNK = 2048;    // floats per stage (8 KB)
+constexpr int TKR_STAGES = 4;
+constexpr uint32_t TKR_RING_BYTES = TKR_STAGES * TKR_CHUNK * 4;
+
+template <int NT>
+__global__ void __launch_bounds__(NT)
+    topk_ring_kernel(const float *logits, int64_t ld, int V, int k, const uint32_t *row_max, const TopkOut o) {
+    extern __shared__ __align__(128) float ring[];   // [TKR_STAGES][TKR_CHUNK]
+    __shared__ TopkSmem<NT> sm;
+    __shared__ uint64_t full[TKR_STAGES], empty[TKR_STAGES];
+    __shared__ uint64_t S;
+    __shared__ int abort_flag;
+    pdl_wait();
+    pdl_trigger();
+    volatile int *abort = &abort_flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    const int row = blockIdx.x;
+    const float *z = logits + (size_t)row * ld;
+    const float m = key_to_float(__ldg(row_max + row));
+    const int nch = (V + TKR_CHUNK - 1) / TKR_CHUNK;
+    auto chunk_len = [&](int c) { return min(TKR_CHUNK, V - c * TKR_CHUNK); };
+    auto issue = [&](int c) {   // thread 0
+        const int s = c % TKR_STAGES;
+        const uint32_t bytes = (uint32_t)chunk_len(c) * 4u;
+        tc::mbar_expect_tx(&full[s], bytes);
+        tc::bulk_load(ring + (size_t)s * TKR_CHUNK, z + (size_t)c * TKR_CHUNK, bytes, &full[s]);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TKR_STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], NT / 32);
+        }
+        abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (lane < KMAX) sm.wres[warp][lane] = 0ull;
+    __syncthreads();
+    int issued = 0;   // thread 0: chunks whose copy has been issued
+    if (threadIdx.x == 0)
+        for (; issued < min(nch, TKR_STAGES); ++issued) issue(issued);
+
+    uint64_t tau = 0ull;
+    float tau_f = key_to_float(0u);
+    int cnt = 0;
+    uint64_t s = 0;
+    bool ok = true;
+    auto flush = [&]() {
+        tau = warp_flush(sm.wres[warp], sm.buf[warp], cnt, k, lane);
+        tau_f = key_to_float((uint32_t)(tau >> 32));
+        cnt = 0;
+    };
+    auto offer = [&](float v, uint32_t idx, bool valid) {
+        bool pass = valid && !(v < tau_f);
+        uint64_t key = 0ull;
+        if (pass) {
+            key = pack_argmax(v, idx);
+            pass = key > tau;
+        }
+        const uint32_t msk = __ballot_sync(0xffffffffu, pass);
+        if (pass) sm.buf[warp][cnt + __popc(msk & lt_mask)] = key;
+        cnt += __popc(msk);
+    };
+    for (int c = 0; c < nch; ++c) {
+        const int st = c % TKR_STAGES;
+        const uint32_t ph = (uint32_t)(c / TKR_STAGES) & 1u;
+        int got = 0;
+        if (lane == 0) got = (ok && tc::mbar_wait(&full[st], ph, abort)) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) ok = false;
+        const int n = chunk_len(c), n4 = n / 4;
+        const float4 *src = reinterpret_cast<const float4 *>(ring + (size_t)st * TKR_CHUNK);
+        if (ok) {
+            // every lane of a warp runs the same number of rounds (the offers are warp-collective)
+            for (int j0 = warp * 32; j0 < n4; j0 += NT) {
+                const int j = j0 + lane;
+                const bool valid = j < n4;
+                const float4 v = valid ? src[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (valid) {
+                    const uint2 w01 = dsm_weight_pair(v.x, v.y, m, 1.0f), w23 = dsm_weight_pair(v.z, v.w, m, 1.0f);
+                    s += ((uint64_t)w01.x + w01.y) + ((uint64_t)w23.x + w23.y);
+                }
+                const bool any = valid && !(max4_nan(v) < tau_f);
+                if (!__any_sync(0xffffffffu, any)) continue;
+                if (cnt + 4 * 32 > TK_CAP) flush();
+                const uint32_t e = (uint32_t)(c * TKR_CHUNK) + 4u * (uint32_t)j;
+                offer(v.x, e, valid);
+                offer(v.y, e + 1, valid);
+                offer(v.z, e + 2, valid);
+                offer(v.w, e + 3, valid);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[st]);
+        // thread 0 refills the stage once every warp has scanned it
+        if (threadIdx.x == 0 && issued < nch && issued == c + TKR_STAGES) {
+            if (ok && tc::mbar_wait(&empty[st], ph, abort))
+                issue(issued++);
+            else
+                ok = false;
+        }
+    }
+    if (cnt > 0) flush();
+    if (!ok && lane == 0) flag(o.dev_status, EAGLE3_DEV_TIMEOUT);
+    if (threadIdx.x == 0) {   // no copy may still be in flight when the CTA exits
+        for (int c = max(0, issued - TKR_STAGES); c < issued; ++c) {
+            const long long t0 = clock64();
+            while (!tc::mbar_try(&full[c % TKR_STAGES], (uint32_t)(c / TKR_STAGES) & 1u) &&
+                   clock64() - t0 < WAIT_LIMIT_CYCLES) {
+            }
+        }
+    }
+    const uint64_t tot = topk_finish(sm, s, k);
+    if (threadIdx.x == 0) S = tot;
     __syncthreads();
     topk_write(sm.fin, S, m, row, V, k, o);
 }
@@ -992,8 +1125,13 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         });
         const int wave = sms * per_sm;
         const TopkOut o = {(int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq), a->d2t, m.V, a->dev_status};
+        // the shared-memory ring needs 16-byte rows: rows of a multiple of 4 floats, aligned logits
+        const bool ring_ok = m.Vd % 4 == 0 && ((uintptr_t)logits & 15) == 0;
         if ((int64_t)rows * TOPK_CL <= 2LL * sms)
             topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
+        else if (ring_ok)
+            topk_ring_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, TKR_RING_BYTES, st>>>(logits, m.Vd, m.Vd, K, rmax,
+                                                                                          o);
         else if (rows <= wave)
             topk_kernel<NT_TOPK><<<rows, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
         else

@@ -61,6 +61,15 @@ E3_DEV void tma_load_4d(void *smem_dst, const CUtensorMap *map, int x, int y, in
         : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory, completing on `bar`
+// (transaction bytes); both addresses 16-byte aligned
+E3_DEV void bulk_load(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // TMA store of a 2-D box from shared memory (bulk-group completion), and the waits on it
 E3_DEV void tma_store_2d(const CUtensorMap *map, int x, int y, const void *smem_src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
