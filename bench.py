@@ -103,7 +103,7 @@ class Engine:
     target and EAGLE-3 head (N(0, 0.02), norms 1), N(0, 1) prefilled caches, and per-launch timing
     of the dominant kernels with CUDA events on the launching stream."""
 
-    def __init__(self, cfg, steps_total, dev, timing=True, fused_rope=True):
+    def __init__(self, cfg, steps_total, dev, timing=True, fused_rope=True, fold_norms=True):
         from eagle_tree_speculative_spec_gb300.step import SpeculativeStep
         import eagle_tree_speculative_spec_gb300 as e3
         self.e3, self.cfg, self.dev, self.timing = e3, cfg, dev, timing
@@ -136,7 +136,8 @@ class Engine:
                  "w_qkv": w(qkv_w, 2 * d), "w_o": w(d, Hq * D), "post_norm": ones(d),
                  "w_gate": w(F, d), "w_up": w(F, d), "w_down": w(d, F), "final_norm": ones(d), "lm_head": w(V, d)}
         scfg = dict(c, mode=e3.TOPK)
-        self.step_obj = st = SpeculativeStep(scfg, target, draft, S, max_prefix, dev, fused_rope=fused_rope)
+        self.step_obj = st = SpeculativeStep(scfg, target, draft, S, max_prefix, dev, fused_rope=fused_rope,
+                                             fold_norms=fold_norms)
         self.S, self.max_prefix = S, max_prefix
         # caches: prefixes of L0 positions of N(0, 1) keys / values (as if prefilled)
         st.k_cache[..., : c["L0"], :].normal_(generator=g)
@@ -324,7 +325,8 @@ def run_gpu(args):
     # all work on one side stream: graph capture needs a stream other than the legacy default one
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    eng = Engine(cfg, args.steps * 3 + 2 * max(args.warmup, args.steps) + 8, dev, fused_rope=not args.rope_in_attention)
+    eng = Engine(cfg, args.steps * 3 + 2 * max(args.warmup, args.steps) + 8, dev, fused_rope=not args.rope_in_attention,
+                 fold_norms=not args.norm_kernels)
     use_graph = not args.eager
     if use_graph and not external_events_ok():
         eng.timing = False                      # timing events cannot live inside a graph: time kernels eagerly
@@ -967,6 +969,9 @@ def main():
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)
     ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
+    ap.add_argument("--norm-kernels", action="store_true",
+                    help="run every RMSNorm of the target as its own kernel instead of folding it into the "
+                         "neighbouring projections")
     ap.add_argument("--rope-in-attention", action="store_true",
                     help="plain QKV projection, RoPE applied inside the verify attention (the unfused path)")
     args = ap.parse_args()

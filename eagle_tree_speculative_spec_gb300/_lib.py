@@ -80,7 +80,8 @@ class LinearArgs(ctypes.Structure):
                 ("ld_x", _i64), ("ld_w", _i64), ("ld_out", _i64), ("ld_res", _i64),
                 ("x", _p), ("w", _p), ("w2", _p), ("out", _p), ("residual", _p), ("dev_status", _p),
                 ("rope_cols", _i32), ("rope_rows_per_seq", _i32), ("rope_theta", ctypes.c_float),
-                ("rope_base", _p), ("rope_depth", _p), ("row_max", _p)]
+                ("rope_base", _p), ("rope_depth", _p), ("row_max", _p),
+                ("row_ssq", _p), ("row_ssq_in", _p), ("ssq_blocks", _i32), ("ssq_dim", _i32), ("ssq_eps", _f32)]
 
 
 EPI_BF16, EPI_F32, EPI_BF16_RESIDUAL, EPI_SWIGLU, EPI_BF16_ROPE = 0, 1, 2, 3, 4
@@ -507,12 +508,16 @@ def eagle3_chain_verify(logits, draft_tokens, cu_num_draft_tokens, output_tokens
 
 def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, splits=0, dev_status=None,
                   workspace=None, stream=None, rope_cols=0, rope_rows_per_seq=1, rope_theta=500000.0,
-                  rope_base=None, rope_depth=None, row_max=None):
+                  rope_base=None, rope_depth=None, row_max=None, row_ssq=None, row_ssq_in=None, ssq_dim=0,
+                  ssq_eps=1e-5):
     """out = epilogue(x W^T) on the tensor cores.  x [m, k] bf16, w (and w2) [n, k] bf16,
     out [m, n] bf16 (fp32 for EPI_F32), residual [m, n] bf16 for EPI_BF16_RESIDUAL.
     EPI_BF16_ROPE rotates columns [0, rope_cols) per 128-wide head at row position
     rope_base[row // rope_rows_per_seq] + rope_depth[row] (int32 device tensors).  row_max (EPI_F32,
-    int32 [m] holding the uint32 words, zeroed by the caller): each row's maximum output order key."""
+    int32 [m] holding the uint32 words, zeroed by the caller): each row's maximum output order key.
+    row_ssq (fp32 [ceil(n / 256), m], bf16 epilogues): per row and 256-column block, the sum of
+    squares of the bf16 outputs.  row_ssq_in (fp32 [blocks, m]): scale each output row by
+    rsqrt(sum / ssq_dim + ssq_eps) before the epilogue (an RMSNorm folded into this projection)."""
     m, k = x.shape
     n = w.shape[0]
     if w.shape[1] != k or (w2 is not None and tuple(w2.shape) != (n, k)):
@@ -527,7 +532,10 @@ def eagle3_linear(x, w, out, *, epilogue=EPI_BF16, w2=None, residual=None, split
                    rope_cols=int(rope_cols), rope_rows_per_seq=int(rope_rows_per_seq), rope_theta=float(rope_theta),
                    rope_base=_ptr(rope_base, torch.int32, "rope_base"),
                    rope_depth=_ptr(rope_depth, torch.int32, "rope_depth"),
-                   row_max=_ptr(row_max, torch.int32, "row_max"))
+                   row_max=_ptr(row_max, torch.int32, "row_max"), row_ssq=_ptr(row_ssq, torch.float32, "row_ssq"),
+                   row_ssq_in=_ptr(row_ssq_in, torch.float32, "row_ssq_in"),
+                   ssq_blocks=0 if row_ssq_in is None else int(row_ssq_in.shape[0]), ssq_dim=int(ssq_dim),
+                   ssq_eps=float(ssq_eps))
     L = lib()
     need = L.eagle3_linear_workspace_size(ctypes.byref(a))
     if workspace is None:

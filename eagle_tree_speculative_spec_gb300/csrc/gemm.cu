@@ -71,7 +71,34 @@ struct GemmParams {
     // when set and the word it points to is 0 (read after the previous kernel completed), the
     // launch does nothing: a caller whose row count is known only on the device skips idle launches
     const int32_t *skip_if_zero;
+    // folded RMSNorm: row_ssq [tiles_n][M] out (bf16 epilogues, the squares of the stored outputs per
+    // row and tile); ssq_in [ssq_blocks][M]: each accumulator row scaled by
+    // rsqrt(sum / ssq_dim + ssq_eps) before the epilogue
+    float *row_ssq;
+    const float *ssq_in;
+    int ssq_blocks;
+    float ssq_inv_dim, ssq_eps;
 };
+
+// the folded RMSNorm's scale of a row (1 without row_ssq_in): the blocks' sums added in block order
+E3_DEV float row_norm_scale(const GemmParams &p, int row) {
+    if (!p.ssq_in || row >= p.M) return 1.0f;
+    float s = 0.0f;
+    for (int b = 0; b < p.ssq_blocks; ++b) s += __ldg(p.ssq_in + (size_t)b * p.M + row);
+    return rsqrtf(s * p.ssq_inv_dim + p.ssq_eps);
+}
+
+// sum of squares of eight bf16 pairs (as stored), added in order
+E3_DEV float ssq_bf16x8(const uint4 &u, float acc) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+        acc = fmaf(f.x, f.x, acc);
+        acc = fmaf(f.y, f.y, acc);
+    }
+    return acc;
+}
 
 E3_DEV bool skipped(const GemmParams &p) { return p.skip_if_zero && *(volatile const int32_t *)p.skip_if_zero == 0; }
 
@@ -223,8 +250,8 @@ E3_DEV void add_residual(float *v, const uint4 (&r)[NV]) {
 }
 
 // Epilogue of one 32-column chunk of one row, from fp32 accumulators.
-E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)[32]) {
-    if (row >= p.M) return;
+E3_DEV float store_chunk(const GemmParams &p, int row, int col0, const float (&v)[32]) {
+    if (row >= p.M) return 0.0f;
     if (p.epi == EAGLE3_EPI_F32) {
         float *o = (float *)p.out + (size_t)row * p.ld_out + col0;
         if (col0 + 32 <= p.N && ((((uintptr_t)o) & 15) == 0)) {
@@ -234,7 +261,7 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
             for (int i = 0; i < 32; ++i)
                 if (col0 + i < p.N) o[i] = v[i];
         }
-        return;
+        return 0.0f;
     }
     __nv_bfloat16 *o = (__nv_bfloat16 *)p.out + (size_t)row * p.ld_out + col0;
     float w[32];
@@ -245,6 +272,7 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
         load_residual(p, row, col0, r);
         add_residual(w, r);
     }
+    float ssq = 0.0f;
     if (col0 + 32 <= p.N && ((((uintptr_t)o) & 15) == 0)) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
@@ -256,11 +284,18 @@ E3_DEV void store_chunk(const GemmParams &p, int row, int col0, const float (&v)
             pk.z = *reinterpret_cast<uint32_t *>(&h2);
             pk.w = *reinterpret_cast<uint32_t *>(&h3);
             *reinterpret_cast<uint4 *>(o + i) = pk;
+            ssq = ssq_bf16x8(pk, ssq);
         }
     } else {
         for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) o[i] = __float2bfloat16_rn(w[i]);
+            if (col0 + i < p.N) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(w[i]);
+                o[i] = b;
+                const float f = __bfloat162float(b);
+                ssq = fmaf(f, f, ssq);
+            }
     }
+    return ssq;
 }
 
 // ROPE: the instantiation with the rotary epilogue (kept apart so that the others do not carry its
@@ -452,6 +487,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int rl = quarter * 32 + lane;       // row within the tile
             const int row = mb * BM + rl;
             const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            // folded RMSNorm: this row's scale, applied to the accumulators after the stream-K
+            // contributions and before the epilogue; the stored outputs' sum of squares goes out
+            const float nscale = row_norm_scale(p, row);
+            auto nscale32 = [&](float (&v)[32]) {
+                if (p.ssq_in) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= nscale;
+                }
+            };
+            float ssq_acc = 0.0f;
             // stream-K owner: the CTAs after this one whose shares start inside this tile hold the
             // rest of its k-blocks; wait (bounded, warp-uniform) until all their warps wrote
             int c_lo = 0, c_hi = 0;
@@ -564,6 +609,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             float a[32], c[32];
                             tc::tmem_ld32(t_row + sc * 64 + h * 32, a);
                             tc::tmem_ld32(t_row + (sc + 1) * 64 + h * 32, c);
+                            nscale32(a);
+                            nscale32(c);
 #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
                                 float lo[2], hi[2];
@@ -585,6 +632,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         float v[32];
                         tc::tmem_ld32(t_row + sc * 32, v);
                         add_contrib(v, sc * 32);
+                        nscale32(v);
                         if (p.row_max) rmax = chunk_max_key(rmax, v, nb * BN + sc * 32, p.N);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -598,6 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             if (!swiglu) {
                                 tc::tmem_ld32(t_row + sc * 64 + h * 32, t);
                                 add_contrib(t, sc * 64 + h * 32);
+                                nscale32(t);
                             } else {
                                 float g[32];
                                 const int c = sc * 2 + h;
@@ -605,6 +654,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 tc::tmem_ld32(t_row + BN / 2 + c * 32, t);
                                 add_contrib(g, c * 32);
                                 add_contrib(t, BN / 2 + c * 32);
+                                nscale32(g);
+                                nscale32(t);
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) t[i] = silu(g[i]) * t[i];
                             }
@@ -620,6 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
                             u[j] = make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
                                               *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                            if (p.row_ssq) ssq_acc = ssq_bf16x8(u[j], ssq_acc);
                         }
                     }
                     // the buffer was last stored from two chunks ago: that store must have read it
@@ -643,16 +695,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
                 if (p.row_max && row < p.M && rmax) atomicMax(p.row_max + row, rmax);
+                if (p.row_ssq && row < p.M) p.row_ssq[(size_t)nb * p.M + row] = ssq_acc;
             } else if (!swiglu) {
                 uint32_t rmax = 0u;
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tc::tmem_ld32(t_row + c * 32, v);
                     add_contrib(v, c * 32);
+                    nscale32(v);
                     if (p.row_max) rmax = chunk_max_key(rmax, v, nb * BN + c * 32, p.N);
-                    store_chunk(p, row, nb * BN + c * 32, v);
+                    ssq_acc += store_chunk(p, row, nb * BN + c * 32, v);
                 }
                 if (p.row_max && row < p.M && rmax) atomicMax(p.row_max + row, rmax);
+                if (p.row_ssq && row < p.M) p.row_ssq[(size_t)nb * p.M + row] = ssq_acc;
             } else {
                 for (int c = 0; c < BN / 64; ++c) {
                     float g[32], u[32];
@@ -660,6 +715,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tc::tmem_ld32(t_row + BN / 2 + c * 32, u);
                     add_contrib(g, c * 32);
                     add_contrib(u, BN / 2 + c * 32);
+                    nscale32(g);
+                    nscale32(u);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) g[i] = silu(g[i]) * u[i];
                     store_chunk(p, row, nb * (BN / 2) + c * 32, g);
@@ -772,6 +829,7 @@ __global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const GemmParams 
     float up[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t key = 0u;
     bool any = false;
+    float ssq = 0.0f;   // row_ssq: squares of this thread's stored outputs
     if (row < p.M && (!swiglu || c4 < BNT / 2)) {
         if (swiglu) {
             // the up columns of this thread's gate columns live 128 columns further in the same row
@@ -787,12 +845,13 @@ __global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const GemmParams 
 #pragma unroll
             for (int e = 0; e < 4; ++e) up[e] = u4[e];
         }
+        const float ns = row_norm_scale(p, row);   // the folded RMSNorm (1 without it)
         const int col0 = swiglu ? nb * (BNT / 2) + c4 : nb * BNT + c4;
         for (int e = 0; e < 4; ++e) {
             const int col = col0 + e;
             if (col >= p.N) continue;
-            float o = acc[e];
-            if (swiglu) o = silu(o) * up[e];
+            float o = p.ssq_in ? acc[e] * ns : acc[e];
+            if (swiglu) o = silu(o) * (p.ssq_in ? up[e] * ns : up[e]);
             if (p.epi == EAGLE3_EPI_F32) {
                 ((float *)p.out)[(size_t)row * p.ld_out + col] = o;
                 const uint32_t k = order_key(o);
@@ -800,12 +859,26 @@ __global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const GemmParams 
                 any = true;
             } else {
                 if (p.epi == EAGLE3_EPI_BF16_RESIDUAL) o += __bfloat162float(p.residual[(size_t)row * p.ld_res + col]);
-                ((__nv_bfloat16 *)p.out)[(size_t)row * p.ld_out + col] = __float2bfloat16_rn(o);
+                const __nv_bfloat16 b = __float2bfloat16_rn(o);
+                ((__nv_bfloat16 *)p.out)[(size_t)row * p.ld_out + col] = b;
+                const float f = __bfloat162float(b);
+                ssq = fmaf(f, f, ssq);
             }
         }
     }
     // a warp's 32 threads cover 128 columns of one row: one atomic max per warp
     if (p.row_max) warp_row_max(p.row_max, row, key, any);
+    if (p.row_ssq) {
+        // the row's sum of squares: each warp's 128 columns by shuffles, then the row's two warps in
+        // column order
+        __shared__ float part[8];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+        if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ssq;
+        __syncthreads();
+        if ((threadIdx.x & 63) == 0 && row < p.M)
+            p.row_ssq[(size_t)nb * p.M + row] = part[(threadIdx.x >> 5)] + part[(threadIdx.x >> 5) + 1];
+    }
 }
 
 // ---- host side ----------------------------------------------------------------------------------
@@ -885,7 +958,8 @@ Plan plan(const eagle3_linear_args_t *a) {
     // count only when it fills it by 2% more; the partials are reduced in split order.
     int auto_splits = 1;
     const bool rope = a->epilogue == EAGLE3_EPI_BF16_ROPE;   // rotated in the epilogue: one k pass per tile
-    if (!rope && a->splits <= 0 && pl.tiles_m == 1 && tiles <= 2 * sms) {
+    const bool folded = a->row_ssq || a->row_ssq_in;   // per-row epilogue inputs / outputs: no k-split reduce
+    if (!rope && !folded && a->splits <= 0 && pl.tiles_m == 1 && tiles <= 2 * sms) {
         double best = 0.0;
         for (int sp = 1; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
             const int units = tiles * sp, w = (units + sms - 1) / sms;
@@ -964,6 +1038,12 @@ eagle3_status_t validate(const eagle3_linear_args_t *a) {
     if (a->epilogue == EAGLE3_EPI_SWIGLU && !a->w2) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->epilogue == EAGLE3_EPI_BF16_RESIDUAL && !a->residual) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->row_max && (a->epilogue != EAGLE3_EPI_F32 || ((uintptr_t)a->row_max & 3))) return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->row_ssq && ((a->epilogue != EAGLE3_EPI_BF16 && a->epilogue != EAGLE3_EPI_BF16_RESIDUAL) ||
+                       ((uintptr_t)a->row_ssq & 3)))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if (a->row_ssq_in && (a->ssq_blocks < 1 || a->ssq_dim < 1 || !(a->ssq_eps >= 0.0f) || ((uintptr_t)a->row_ssq_in & 3)))
+        return EAGLE3_ERR_INVALID_ARGUMENT;
+    if ((a->row_ssq || a->row_ssq_in) && a->splits > 1) return EAGLE3_ERR_UNSUPPORTED;
     const int64_t ld_x = a->ld_x ? a->ld_x : a->k, ld_w = a->ld_w ? a->ld_w : a->k;
     if (ld_x < a->k || ld_w < a->k || (ld_x % 8) || (ld_w % 8)) return EAGLE3_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)a->x | (uintptr_t)a->w | (uintptr_t)a->w2) & 15) return EAGLE3_ERR_INVALID_ARGUMENT;
@@ -1041,6 +1121,11 @@ eagle3_status_t e3::linear_launch(const eagle3_linear_args_t *a, void *workspace
     p.tail_splits = pl.tail_splits;
     p.tail_ws = pl.tail_splits > 1 ? (float *)workspace : nullptr;
     p.skip_if_zero = skip_if_zero;
+    p.row_ssq = a->row_ssq;
+    p.ssq_in = a->row_ssq_in;
+    p.ssq_blocks = a->row_ssq_in ? a->ssq_blocks : 0;
+    p.ssq_inv_dim = a->row_ssq_in ? 1.0f / (float)a->ssq_dim : 0.0f;
+    p.ssq_eps = a->ssq_eps;
     for (int j = 0; j < 64; ++j)
         p.rope_inv[j] = p.rope_cols ? (float)std::pow((double)a->rope_theta, -2.0 * j / 128.0) : 0.0f;
     CUtensorMap mo;

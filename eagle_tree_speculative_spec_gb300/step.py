@@ -17,6 +17,11 @@ A step, every part of it a libeagle3 call on the caller's stream:
       eagle3_linear     fused QKV projection; q and k leave it rotated at prefix_len + depth
       eagle3_verify_attn tree-masked attention over the layer's cache and the tree
       eagle3_linear     O projection + residual, post-norm, SwiGLU gate/up, down + residual
+                        (fold_norms: the RMSNorms before QKV, gate/up and the LM head are folded
+                        into those projections: the O and down projections emit each row's sum of
+                        squares, the next projection reads the raw residual stream with the norm
+                        weight folded into its weights and scales its output rows; only layer 0
+                        (which gathers the embeddings) and the tapped layers keep a norm kernel)
   eagle3_rmsnorm + eagle3_linear   final norm, LM head (fp32 logits)
   eagle3_accept         greedy walk or lossless rejection sampling over the tree
                         (lazy_head: eagle3_accept_lazy instead of the LM head and eagle3_accept; the
@@ -54,7 +59,7 @@ class SpeculativeStep:
     The caller fills the caches and the per-sequence state (prefix_len, draft_len, aux_in,
     next_tok, tc) before the first step; the buffers are attributes of this object."""
 
-    def __init__(self, cfg, target, draft, s_max, max_prefix, dev, fused_rope=True, d2t=None):
+    def __init__(self, cfg, target, draft, s_max, max_prefix, dev, fused_rope=True, d2t=None, fold_norms=False):
         c = self.cfg = dict(cfg)
         if len(c["taps"]) != 3 or min(c["taps"]) < 1 or max(c["taps"]) >= c["layers"]:
             raise ValueError("three aux taps in [1, layers) are needed")
@@ -62,6 +67,7 @@ class SpeculativeStep:
             raise ValueError("the path width must hold depth + 1 nodes")
         self.target, self.draft_w, self.dev = target, draft, dev
         self.fused_rope = fused_rope
+        self.fold_norms = bool(fold_norms)
         self.S, self.max_prefix = int(s_max), int(max_prefix)
         self.d2t = d2t
         B, N, d, V, D = c["B"], c["N"], c["d"], c["V"], c["D"]
@@ -99,6 +105,12 @@ class SpeculativeStep:
         self.next_root = torch.empty(B, dtype=i32, device=dev)
         self.slot_map = torch.empty(B, W, dtype=i32, device=dev)
         self.dev_status = torch.zeros(1, dtype=i32, device=dev)
+        # folded RMSNorm: per row and 256-column block, the sum of squares of the residual stream as
+        # stored (after the O projection, and after the down projection)
+        self.ssq_blocks = (d + 255) // 256
+        self.ssq_mid = torch.zeros(self.ssq_blocks, R, dtype=torch.float32, device=dev)
+        self.ssq_next = torch.zeros(self.ssq_blocks, R, dtype=torch.float32, device=dev)
+        self._folded = None
         self.step_counter = torch.zeros(1, dtype=torch.int64, device=dev)   # Philox step, advanced on device
         self.draft_ops, self.verify_ops = [], []
         self._keep = []
@@ -168,14 +180,18 @@ class SpeculativeStep:
         self.ws_lin = torch.empty(ws_linear_bytes, dtype=torch.uint8, device=self.dev)
         lp, lb = ws(self.ws_lin)
 
-        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm", rope_cols=0):
+        def lin(x, w, out, epi=0, w2=None, res=None, kind="gemm", rope_cols=0, ssq_out=None, ssq_in=None):
             a = e3.LinearArgs(m=x.shape[0], n=w.shape[0], k=x.shape[1], epilogue=epi, splits=0, ld_x=0, ld_w=0,
                               ld_out=0, ld_res=0, x=x.data_ptr(), w=w.data_ptr(),
                               w2=None if w2 is None else w2.data_ptr(), out=out.data_ptr(),
                               residual=None if res is None else res.data_ptr(), dev_status=dev_st,
                               rope_cols=rope_cols, rope_rows_per_seq=N, rope_theta=theta,
                               rope_base=self.prefix_len.data_ptr() if rope_cols else None,
-                              rope_depth=self.depth.data_ptr() if rope_cols else None)
+                              rope_depth=self.depth.data_ptr() if rope_cols else None,
+                              row_ssq=None if ssq_out is None else ssq_out.data_ptr(),
+                              row_ssq_in=None if ssq_in is None else ssq_in.data_ptr(),
+                              ssq_blocks=0 if ssq_in is None else self.ssq_blocks,
+                              ssq_dim=0 if ssq_in is None else d, ssq_eps=eps)
             if L.eagle3_linear_workspace_size(ctypes.byref(a)) > ws_linear_bytes:
                 raise ValueError("linear workspace too small for the step's shapes")
             keep.append(a)
@@ -183,19 +199,28 @@ class SpeculativeStep:
 
         T = self.target
         taps = {t: i for i, t in enumerate(c["taps"])}
+        fold = self.fold_norms
+        if fold and self._folded is None:
+            self._folded = self._fold_weights()
+        Fw = self._folded
         # layer 0's norm reads the tree tokens' embedding rows and keeps them as the residual stream
         norm(T["embed"], T["norm1"][0], self.h, gather=self.tokens.view(-1), tap=self.x)
         self.ws_attn = torch.empty(ws_attn_bytes, dtype=torch.uint8, device=self.dev)
         ap, ab = ws(self.ws_attn)
         for l in range(c["layers"]):
-            if l > 0:
+            # the attention norm: a kernel on layer 0 (embedding gather) and on tapped layers (the tap
+            # copies the stream entering the layer); otherwise folded into the QKV projection
+            fold1 = fold and l > 0 and l not in taps
+            if l > 0 and not fold1:
                 tap = self.aux_tree[:, taps[l] * d:(taps[l] + 1) * d] if l in taps else None
                 norm(self.x, T["norm1"][l], self.h, tap=tap)
             qkv = self.qkv[l]
+            a_in, w_qkv = (self.x, Fw["wqkv"][l]) if fold1 else (self.h, T["wqkv"][l])
+            s_in = self.ssq_next if fold1 else None
             if self.fused_rope:
-                lin(self.h, T["wqkv"][l], qkv, epi=e3.EPI_BF16_ROPE, rope_cols=(Hq + Hkv) * D)
+                lin(a_in, w_qkv, qkv, epi=e3.EPI_BF16_ROPE, rope_cols=(Hq + Hkv) * D, ssq_in=s_in)
             else:
-                lin(self.h, T["wqkv"][l], qkv)
+                lin(a_in, w_qkv, qkv, ssq_in=s_in)
             va = e3.verify_attn_args(self.tree_q(l), self.tree_k(l), self.tree_v(l), self.k_cache[l],
                                      self.v_cache[l], self.parents, self.prefix_len, self.attn.view(B, N, Hq, D),
                                      max_prefix_len=self.max_prefix, rope_theta=theta, dev_status=self.dev_status,
@@ -204,11 +229,19 @@ class SpeculativeStep:
                 raise ValueError("attention workspace too small for the step's shapes")
             keep.append(va)
             ops.append(("verify_attn", lambda a=va: L.eagle3_verify_attn(ctypes.byref(a), ap, ab, st)))
-            lin(self.attn, T["wo"][l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
-            norm(self.x, T["norm2"][l], self.h)
-            lin(self.h, T["wg"][l], self.act, epi=e3.EPI_SWIGLU, w2=T["wu"][l], kind="gemm_gateup")
-            lin(self.act, T["wd"][l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x)
-        norm(self.x, T["final_norm"], self.h)
+            lin(self.attn, T["wo"][l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x,
+                ssq_out=self.ssq_mid if fold else None)
+            if fold:   # the post-attention norm folded into the gate / up projection
+                lin(self.x, Fw["wg"][l], self.act, epi=e3.EPI_SWIGLU, w2=Fw["wu"][l], kind="gemm_gateup",
+                    ssq_in=self.ssq_mid)
+            else:
+                norm(self.x, T["norm2"][l], self.h)
+                lin(self.h, T["wg"][l], self.act, epi=e3.EPI_SWIGLU, w2=T["wu"][l], kind="gemm_gateup")
+            lin(self.act, T["wd"][l], self.x, epi=e3.EPI_BF16_RESIDUAL, res=self.x,
+                ssq_out=self.ssq_next if fold else None)
+        fold_f = fold and not self.lazy_head   # the lazy head gathers normalised rows
+        if not fold_f:
+            norm(self.x, T["final_norm"], self.h)
         # ---- acceptance over the tree (the emitted row is the next step's catch-up tokens)
         if self.lazy_head:
             aa = e3.accept_lazy_args(c["mode"], self.h.view(B, N, d), T["lm_head"], self.tokens, self.parents,
@@ -220,7 +253,10 @@ class SpeculativeStep:
         else:
             if self.logits is None:
                 self.logits = torch.empty(R, c["V"], device=self.dev, dtype=torch.float32)
-            lin(self.h, T["lm_head"], self.logits, epi=e3.EPI_F32)
+            if fold_f:
+                lin(self.x, Fw["lm_head"], self.logits, epi=e3.EPI_F32, ssq_in=self.ssq_next)
+            else:
+                lin(self.h, T["lm_head"], self.logits, epi=e3.EPI_F32)
             aa = e3.AcceptArgs(mode=int(c["mode"]), batch=B, n_nodes=N, vocab=c["V"], max_path=c["W"],
                                temperature=float(c.get("temperature", 1.0)), seed=int(c.get("seed", 0)), step=0,
                                target_logits=self.logits.data_ptr(), draft_logits=None,
@@ -250,6 +286,20 @@ class SpeculativeStep:
         self.verify_ops = ops
         self.ops = self.draft_ops + self.verify_ops
         return self
+
+    def _fold_weights(self):
+        """Weights with the RMSNorm weight folded in, W' = W diag(g), made once (bf16 of the fp32
+        product); a norm weight of all ones leaves W itself."""
+        T, c = self.target, self.cfg
+
+        def fold(w, g):
+            if bool(torch.all(g == 1)):
+                return w
+            return (w.float() * g.float()[None, :]).to(torch.bfloat16).contiguous()
+        return {"wqkv": [fold(T["wqkv"][l], T["norm1"][l]) for l in range(c["layers"])],
+                "wg": [fold(T["wg"][l], T["norm2"][l]) for l in range(c["layers"])],
+                "wu": [fold(T["wu"][l], T["norm2"][l]) for l in range(c["layers"])],
+                "lm_head": fold(T["lm_head"], T["final_norm"])}
 
     # ------------------------------------------------------------------------------ issue
     @staticmethod

@@ -71,6 +71,26 @@ typedef struct {
        of x maps its fp32 bit pattern b to b ^ 0x80000000 for x >= 0 (sign bit clear) and to ~b
        otherwise, so unsigned order is float order.  The caller sets the words to 0 beforehand.   */
     uint32_t *row_max;
+    /* RMSNorm folded into the neighbouring projections ("EAGLE-3: Engineering Implementation of
+       LLM Inference Acceleration", appendix C: RMSNorm(x) = x * rsqrt(mean(x^2) + eps) * g before
+       every projection that reads the residual stream).  Since
+           RMSNorm(x) W^T = diag(rsqrt(mean(x^2) + eps)) (x W'^T),  W' = W diag(g),
+       a projection may read the un-normalised stream x with the norm weight folded into its
+       weights and scale each output row afterwards, given the row's sum of squares, which the
+       projection that produced x can emit on the way out.
+       row_ssq (BF16 / BF16_RESIDUAL only; NULL otherwise): [ceil(n / 256)][m] fp32 out: for each
+         row and each block of 256 output columns, the sum of squares of the bf16 outputs as stored
+         (in a fixed order; blocks are whole-row sums when added in block order).
+       row_ssq_in (optional): [ssq_blocks][m] fp32, such sums of the rows of x: each output row's
+         accumulator is multiplied by rsqrt((sum over blocks in order) / ssq_dim + ssq_eps) before
+         the epilogue (before the residual add, the rotation, the SwiGLU or the fp32 store).
+       Either option rules out the k-split plans with a separate reduction (a k-split caller
+       request returns EAGLE3_ERR_UNSUPPORTED).                                                  */
+    float *row_ssq;
+    const float *row_ssq_in;
+    int32_t ssq_blocks;         /* >= 1 with row_ssq_in                                            */
+    int32_t ssq_dim;            /* >= 1 with row_ssq_in: the length of the rows of x               */
+    float ssq_eps;              /* >= 0                                                            */
 } eagle3_linear_args_t;
 
 size_t eagle3_linear_workspace_size(const eagle3_linear_args_t *args);

@@ -229,3 +229,89 @@ def test_linear_split_tail(m, n, k, epi_name):
         bits = got.view(np.uint32).astype(np.uint64)
         keys = np.where(bits >> 31, ~bits & 0xFFFFFFFF, bits | 0x80000000)
         assert np.array_equal(rmax.cpu().numpy().view(np.uint32).astype(np.uint64), keys.max(1))
+
+
+@pytest.mark.parametrize("m,n,k,epi_name", [
+    (130, 1000, 256, "residual"),      # data-parallel, a partial 256-column block, direct-store tails
+    (1280, 4096, 2048, "residual"),    # split tail: the reduce kernel writes outputs and row sums
+    (768, 4096, 12288, "bf16"),        # stream-K: owners finish the cut tiles
+    (300, 1000, 512, "bf16")])         # unaligned pitch of the output: direct stores
+def test_linear_row_ssq(m, n, k, epi_name):
+    """row_ssq: for each row and block of 256 output columns, the sum of squares of the bf16 outputs
+    the same call stored (any plan) — the per-row statistic a folded RMSNorm of the next projection
+    needs."""
+    import eagle_tree_speculative_spec_gb300 as e3
+    epi = {"residual": e3.EPI_BF16_RESIDUAL, "bf16": e3.EPI_BF16}[epi_name]
+    dev = require_gpu()
+    x, w, _ = _inputs(m, n, k, 17)
+    res = torch.randn(m, n).to(torch.bfloat16) if epi == e3.EPI_BF16_RESIDUAL else None
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=dev)
+    blocks = (n + 255) // 256
+    ssq = torch.full((blocks, m), float("nan"), dtype=torch.float32, device=dev)
+    e3.eagle3_linear(x.to(dev), w.to(dev), out, epilogue=epi, residual=None if res is None else res.to(dev),
+                     row_ssq=ssq)
+    torch.cuda.synchronize()
+    o = out.double().cpu().numpy()
+    want = np.stack([(o[:, 256 * b:256 * (b + 1)] ** 2).sum(1) for b in range(blocks)])
+    got = ssq.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-6), np.abs(got - want).max()
+    ok, err = close(o, _ref(x, w) + (res.double().numpy() if res is not None else 0.0), 2e-2, 1e-2)
+    assert ok, err
+
+
+@pytest.mark.parametrize("m,n,k,epi_name", [
+    (130, 1000, 256, "bf16"), (1280, 2048, 2048, "swiglu"), (768, 4096, 12288, "residual"),
+    (640, 16384, 512, "f32"), (120, 768, 256, "rope"), (1290, 4100, 1024, "bf16")])
+def test_linear_folded_rmsnorm(m, n, k, epi_name):
+    """row_ssq_in: every output row is scaled by rsqrt(sum of the row's block sums / dim + eps)
+    before the epilogue, i.e. RMSNorm(x) W^T = diag(rsqrt(mean(x^2) + eps)) x W^T with x's sums of
+    squares given per block (data-parallel, split-tail, stream-K and TMA-stored fp32 plans)."""
+    from oracle import attention as oatt
+    import eagle_tree_speculative_spec_gb300 as e3
+    epi = {"bf16": e3.EPI_BF16, "swiglu": e3.EPI_SWIGLU, "residual": e3.EPI_BF16_RESIDUAL, "f32": e3.EPI_F32,
+           "rope": e3.EPI_BF16_ROPE}[epi_name]
+    dev = require_gpu()
+    x, w, w2 = _inputs(m, n, k, 19, swiglu=epi == e3.EPI_SWIGLU)
+    xd = x.double().numpy()
+    blocks, eps = 3, 1e-5
+    # the row sums of squares of x, cut into three uneven blocks (their order is the addition order)
+    cuts = [0, k // 3, (2 * k) // 3, k]
+    sums = np.stack([(xd[:, cuts[b]:cuts[b + 1]] ** 2).sum(1) for b in range(blocks)]).astype(np.float32)
+    scale = 1.0 / np.sqrt(sums.astype(np.float64).sum(0) / k + eps)
+    res = torch.randn(m, n).to(torch.bfloat16) if epi == e3.EPI_BF16_RESIDUAL else None
+    out = torch.full((m, n), float("nan"), dtype=torch.float32 if epi == e3.EPI_F32 else torch.bfloat16, device=dev)
+    kw = {}
+    if epi == e3.EPI_BF16_ROPE:
+        g = np.random.default_rng(21)
+        base = g.integers(0, 5000, (m + 59) // 60).astype(np.int32)
+        depth = g.integers(0, 7, m).astype(np.int32)
+        kw = dict(rope_cols=512, rope_rows_per_seq=60, rope_theta=500000.0,
+                  rope_base=torch.as_tensor(base, device=dev), rope_depth=torch.as_tensor(depth, device=dev))
+    e3.eagle3_linear(x.to(dev), w.to(dev), out, epilogue=epi, w2=None if w2 is None else w2.to(dev),
+                     residual=None if res is None else res.to(dev), row_ssq_in=torch.as_tensor(sums, device=dev),
+                     ssq_dim=k, ssq_eps=eps, **kw)
+    torch.cuda.synchronize()
+    acc = _ref(x, w) * scale[:, None]
+    if epi == e3.EPI_SWIGLU:
+        want = _silu(acc) * (_ref(x, w2) * scale[:, None])
+    elif epi == e3.EPI_BF16_ROPE:
+        want = acc.copy()
+        pos = base[np.arange(m) // 60] + depth
+        want[:, :512] = oatt.rope_apply(acc[:, :512].reshape(m, 4, 128), pos, 500000.0).reshape(m, 512)
+    else:
+        want = acc + (res.double().numpy() if res is not None else 0.0)
+    tol = (1e-3, 1e-3) if epi == e3.EPI_F32 else (2e-2, 1e-2)
+    ok, err = close(out.float().cpu().numpy(), want, *tol)
+    assert ok, err
+
+
+def test_linear_folded_rmsnorm_rejects_k_split():
+    """A caller-requested k split with a per-row epilogue input or output is refused on the host."""
+    import eagle_tree_speculative_spec_gb300 as e3
+    dev = require_gpu()
+    x, w, _ = _inputs(64, 512, 256, 1)
+    out = torch.empty(64, 512, dtype=torch.bfloat16, device=dev)
+    ssq = torch.zeros(2, 64, dtype=torch.float32, device=dev)
+    with pytest.raises(e3.Eagle3Error):
+        e3.eagle3_linear(x.to(dev), w.to(dev), out, splits=2, row_ssq=ssq)

@@ -1,6 +1,7 @@
 """GPU parity of the composed draft-and-verify step (eagle_tree_speculative_spec_gb300.step) at a
-small bf16 shape: 4 target layers, d = 256, 4 / 2 heads of 128, FFN 512, vocab 1000, aux taps at
-layers {1, 2, 3}, B = 3 sequences with ragged prefixes, 12-node trees (depth 4, top-k 4).
+small bf16 shape: 5 target layers, d = 256, 4 / 2 heads of 128, FFN 512, vocab 1000, aux taps at
+layers {1, 2, 4} (layer 3 untapped), norm weights 1 + N(0, 0.1^2), B = 3 sequences with ragged
+prefixes, 12-node trees (depth 4, top-k 4).
 
 Checked against the oracle ("Advanced speculative decoding: tree drafts and EAGLE", section
 "Implementation": each tree node's logits are those of its path run as a sequence, and only the
@@ -30,7 +31,7 @@ from tests._util import close, require_gpu
 
 pytestmark = pytest.mark.gpu
 
-CFG = dict(layers=4, d=256, Hq=4, Hkv=2, D=128, F=512, V=1000, taps=(1, 2, 3), B=3, N=12, depth=4, top_k=4, W=5,
+CFG = dict(layers=5, d=256, Hq=4, Hkv=2, D=128, F=512, V=1000, taps=(1, 2, 4), B=3, N=12, depth=4, top_k=4, W=5,
            temperature=1.0, seed=5, rope_theta=500000.0, eps=1e-5)
 PREFIX = [5, 1, 17]
 ATOL, RTOL = 2e-2, 1e-2
@@ -39,6 +40,10 @@ ATOL, RTOL = 2e-2, 1e-2
 def _weights(seed=3):
     c = CFG
     tw = synth.llama_weights(seed, c["d"], c["layers"], c["Hq"], c["Hkv"], c["D"], c["F"], c["V"])
+    # norm weights away from 1, so that a norm folded into the next projection's weights is exercised
+    r = np.random.default_rng(seed + 100)
+    for name in [n for n in tw if n.endswith("_norm")]:
+        tw[name] = (1.0 + 0.1 * r.standard_normal(tw[name].shape)).astype(np.float32)
     dw = synth.eagle3_weights(seed, c["d"], c["Hq"], c["Hkv"], c["D"], c["F"], c["V"], embed=tw["embed"])
     # bf16 rounding: the GPU gets the bf16 tensors, the oracle the same values in fp64
     t_gpu, t_f = {}, {}
@@ -50,7 +55,7 @@ def _weights(seed=3):
     return t_gpu, t_f, d_gpu, d_f
 
 
-def _build(dev, mode):
+def _build(dev, mode, fold_norms=False):
     from eagle_tree_speculative_spec_gb300 import step as estep
     c = CFG
     t_gpu, t_f, d_gpu, d_f = _weights()
@@ -68,7 +73,7 @@ def _build(dev, mode):
     draft = {g: d_gpu[o].to(dev) for g, o in names.items()}
     draft["w_qkv"] = torch.cat([d_gpu["wq"], d_gpu["wk"], d_gpu["wv"]], 0).to(dev).contiguous()
     S = 64
-    st = estep.SpeculativeStep(dict(c, mode=mode), target, draft, S, S - c["N"] - 8, dev)
+    st = estep.SpeculativeStep(dict(c, mode=mode), target, draft, S, S - c["N"] - 8, dev, fold_norms=fold_norms)
     # prefilled caches: N(0, 1) rotated keys / values at positions < prefix; draft cache one shorter
     r = synth.rng(17, 1)
     kc = np.zeros((c["layers"], c["B"], c["Hkv"], S, c["D"]), np.float32)
@@ -213,12 +218,16 @@ def _plant_chain(st, snap, greedy_pred):
     return chains
 
 
+@pytest.mark.parametrize("fold", [False, True], ids=["norm_kernels", "folded_norms"])
 @pytest.mark.parametrize("mode_name", ["greedy", "topk"])
-def test_step_matches_oracle(mode_name):
+def test_step_matches_oracle(mode_name, fold):
+    """One step against the oracle; `folded_norms`: the RMSNorms before QKV (layers without a tap),
+    gate / up and the LM head folded into those projections (row sums of squares from the O and down
+    projections)."""
     from eagle_tree_speculative_spec_gb300 import GREEDY, TOPK
     dev = require_gpu()
     mode = {"greedy": GREEDY, "topk": TOPK}[mode_name]
-    st, t_f, _ = _build(dev, mode)
+    st, t_f, _ = _build(dev, mode, fold_norms=fold)
     target = _oracle_target(t_f)
     snap0 = _snapshot(st)
     before = {n: (getattr(st, n).float() if getattr(st, n).dtype == torch.bfloat16 else getattr(st, n)).cpu().numpy()
