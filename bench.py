@@ -505,7 +505,9 @@ def run_gpu(args):
                       "ms_per_step": round(lazy_ms / args.steps, 4),
                       "tau": round(float(lazy_acc.item()) / (cfg["B"] * args.steps) - 1.0, 4),
                       "how": "the same step with eagle3_accept_lazy in place of the full LM head and "
-                             "eagle3_accept (identical acceptance; head logits only for the visited nodes), "
+                             "eagle3_accept (head logits only for the visited nodes; the lazy head reads rows "
+                             "normalised by the norm kernel where the full head folds the norm, so decisions "
+                             "agree up to that rounding), "
                              f"{args.steps} steps timed after the e2e loop"},
         "accepted_tokens_per_s": round(float(accepted.item()) * world / (ms / 1e3), 2),
         "tau": round(tau, 4),
