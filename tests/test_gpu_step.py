@@ -55,7 +55,7 @@ def _weights(seed=3):
     return t_gpu, t_f, d_gpu, d_f
 
 
-def _build(dev, mode, fold_norms=False):
+def _build(dev, mode, fold_norms=False, fused_rope=True):
     from eagle_tree_speculative_spec_gb300 import step as estep
     c = CFG
     t_gpu, t_f, d_gpu, d_f = _weights()
@@ -73,7 +73,8 @@ def _build(dev, mode, fold_norms=False):
     draft = {g: d_gpu[o].to(dev) for g, o in names.items()}
     draft["w_qkv"] = torch.cat([d_gpu["wq"], d_gpu["wk"], d_gpu["wv"]], 0).to(dev).contiguous()
     S = 64
-    st = estep.SpeculativeStep(dict(c, mode=mode), target, draft, S, S - c["N"] - 8, dev, fold_norms=fold_norms)
+    st = estep.SpeculativeStep(dict(c, mode=mode), target, draft, S, S - c["N"] - 8, dev, fold_norms=fold_norms,
+                               fused_rope=fused_rope)
     # prefilled caches: N(0, 1) rotated keys / values at positions < prefix; draft cache one shorter
     r = synth.rng(17, 1)
     kc = np.zeros((c["layers"], c["B"], c["Hkv"], S, c["D"]), np.float32)
@@ -218,16 +219,18 @@ def _plant_chain(st, snap, greedy_pred):
     return chains
 
 
-@pytest.mark.parametrize("fold", [False, True], ids=["norm_kernels", "folded_norms"])
+@pytest.mark.parametrize("fold,rope", [(False, True), (True, True), (True, False)],
+                         ids=["norm_kernels", "folded_norms", "folded_norms_rope_in_attention"])
 @pytest.mark.parametrize("mode_name", ["greedy", "topk"])
-def test_step_matches_oracle(mode_name, fold):
+def test_step_matches_oracle(mode_name, fold, rope):
     """One step against the oracle; `folded_norms`: the RMSNorms before QKV (layers without a tap),
     gate / up and the LM head folded into those projections (row sums of squares from the O and down
-    projections)."""
+    projections); `rope_in_attention`: the QKV projection leaves q and the tree keys unrotated and
+    the attention rotates them."""
     from eagle_tree_speculative_spec_gb300 import GREEDY, TOPK
     dev = require_gpu()
     mode = {"greedy": GREEDY, "topk": TOPK}[mode_name]
-    st, t_f, _ = _build(dev, mode, fold_norms=fold)
+    st, t_f, _ = _build(dev, mode, fold_norms=fold, fused_rope=rope)
     target = _oracle_target(t_f)
     snap0 = _snapshot(st)
     before = {n: (getattr(st, n).float() if getattr(st, n).dtype == torch.bfloat16 else getattr(st, n)).cpu().numpy()
