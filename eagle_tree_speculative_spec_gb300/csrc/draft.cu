@@ -1127,7 +1127,7 @@ extern "C" eagle3_status_t eagle3_draft_tree(const eagle3_draft_weights_t *W, co
         const TopkOut o = {(int32_t *)P(pl.o_ttok), (float *)P(pl.o_tlq), a->d2t, m.V, a->dev_status};
         // the shared-memory ring needs 16-byte rows: rows of a multiple of 4 floats, aligned logits
         const bool ring_ok = m.Vd % 4 == 0 && ((uintptr_t)logits & 15) == 0;
-        if ((int64_t)rows * TOPK_CL <= 2LL * sms)
+        if ((int64_t)rows * TOPK_CL <= 4LL * sms)   // up to ~4 cluster CTAs per SM (the B = 64 root rows)
             topk_cluster_kernel<<<rows * TOPK_CL, NT_TOPK, 0, st>>>(logits, m.Vd, m.Vd, K, rmax, o);
         else if (ring_ok)
             topk_ring_kernel<NT_TOPK_NARROW><<<rows, NT_TOPK_NARROW, TKR_RING_BYTES, st>>>(logits, m.Vd, m.Vd, K, rmax,
