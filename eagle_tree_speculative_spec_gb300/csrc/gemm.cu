@@ -970,8 +970,31 @@ Plan plan(const eagle3_linear_args_t *a) {
             }
         }
     }
+    // split tail: whole waves data-parallel, and the partial last wave's tiles split along k into as
+    // many ranges (2..8, at least 4 k-blocks each) as fill the SMs best, when that fills them at least
+    // 10 points better; no CTA waits on another, so the launch stays an ordinary (dependent) one
+    int tail_best = 1;
+    double tail_fill = 0.0;
+    const int tail_dp = (tiles / sms) * sms, tail_tiles = tiles - tail_dp;
+    if (!rope && a->splits <= 0 && auto_splits == 1 && tail_dp > 0 && tail_tiles > 0) {
+        tail_fill = (double)tail_tiles / sms;
+        for (int sp = 2; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
+            const int per = (pl.kb_total + sp - 1) / sp;
+            if (tail_tiles * sp > sms || (sp - 1) * per >= pl.kb_total) continue;   // no empty last range
+            const double f = (double)tail_tiles * sp / sms;
+            if (f > tail_fill + 0.1) {
+                tail_best = sp;
+                tail_fill = f;
+            }
+        }
+    }
+    // stream-K, unless several M tiles run whole waves data-parallel and the split tail fills the
+    // last wave at least 75%: then the split tail is faster (an ordinary launch that starts under the
+    // previous kernel's last wave, no flags); e.g. 3840 x 4096 x 14336 with the residual epilogue,
+    // 0.323 ms stream-K against 0.299 ms with a 6-way split tail
     pl.streamk = !rope && a->splits <= 0 && auto_splits == 1 && (pl.kb_total >= 192 || pl.tiles_m == 1) &&
-                 (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms;
+                 (double)tiles / ((double)waves * sms) < 0.97 && T >= 8LL * sms &&
+                 !(pl.tiles_m > 1 && tail_best > 1 && tail_fill >= 0.75);
     if (pl.streamk) {
         pl.splits = 1;
         pl.kb_per_split = pl.kb_total;
@@ -980,34 +1003,15 @@ Plan plan(const eagle3_linear_args_t *a) {
         pl.ws_bytes = (size_t)sms * BM * pl.bn * sizeof(float) + (size_t)sms * sizeof(int);
         return pl;
     }
-    // split tail: whole waves data-parallel, and the partial last wave's tiles split along k into as
-    // many ranges (2..8, at least 4 k-blocks each) as fill the SMs best, when that fills them at least
-    // 10 points better; no CTA waits on another, so the launch stays an ordinary (dependent) one
-    if (!rope && a->splits <= 0 && auto_splits == 1) {
-        const int dp = (tiles / sms) * sms, tail = tiles - dp;
-        if (dp > 0 && tail > 0) {
-            int best = 1;
-            double fill = (double)tail / sms;
-            for (int sp = 2; sp <= 8 && pl.kb_total / sp >= 4; ++sp) {
-                const int per = (pl.kb_total + sp - 1) / sp;
-                if (tail * sp > sms || (sp - 1) * per >= pl.kb_total) continue;   // no empty last range
-                const double f = (double)tail * sp / sms;
-                if (f > fill + 0.1) {
-                    best = sp;
-                    fill = f;
-                }
-            }
-            if (best > 1) {
-                pl.tail_dp = dp;
-                pl.tail_splits = best;
-                pl.splits = 1;
-                pl.kb_per_split = (pl.kb_total + best - 1) / best;
-                pl.units = dp + tail * best;
-                pl.grid = sms;
-                pl.ws_bytes = (size_t)tail * best * BM * pl.bn * sizeof(float);
-                return pl;
-            }
-        }
+    if (tail_best > 1) {
+        pl.tail_dp = tail_dp;
+        pl.tail_splits = tail_best;
+        pl.splits = 1;
+        pl.kb_per_split = (pl.kb_total + tail_best - 1) / tail_best;
+        pl.units = tail_dp + tail_tiles * tail_best;
+        pl.grid = sms;
+        pl.ws_bytes = (size_t)tail_tiles * tail_best * BM * pl.bn * sizeof(float);
+        return pl;
     }
     int splits = rope ? 1 : (a->splits > 0 ? a->splits : auto_splits);
     splits = std::max(1, std::min(splits, pl.kb_total));
