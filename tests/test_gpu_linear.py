@@ -103,11 +103,13 @@ def test_linear_in_place_residual():
 @pytest.mark.parametrize("m,n,k,epi", [
     (768, 4096, 12288, "bf16"), (300, 1000, 12296, "bf16"), (130, 4096, 14336, "residual"),
     (200, 4096, 12288, "f32"), (640, 2048, 12288, "swiglu"), (1, 4096, 14336, "bf16"),
-    (3840, 4096, 14336, "bf16")])
+    (3584, 2816, 12288, "bf16"),      # 308 tiles: 152 data-parallel, the rest shared out (4 tail tiles)
+    (64, 128256, 4096, "f32")])       # one M tile, 501 tiles: 304 data-parallel in front
 def test_linear_stream_k(m, n, k, epi):
-    """Long-K shapes whose output tiles leave the last wave partly empty run the stream-K schedule:
-    tiles cut between CTAs are finished by the CTA holding their first k-block, which adds the
-    others' fp32 slots in CTA order (M = 3840 also has data-parallel waves in front)."""
+    """Long-K shapes whose output tiles leave the last wave partly empty (and which a split of the
+    last wave's tiles cannot fill), and single-M-tile launches, run the stream-K schedule: tiles cut
+    between CTAs are finished by the CTA holding their first k-block, which adds the others' fp32
+    slots in CTA order; the last two shapes have data-parallel waves in front."""
     import eagle_tree_speculative_spec_gb300 as e3
     code = {"bf16": e3.EPI_BF16, "residual": e3.EPI_BF16_RESIDUAL, "f32": e3.EPI_F32, "swiglu": e3.EPI_SWIGLU}[epi]
     got, want = _run(m, n, k, code, seed=5)
@@ -203,7 +205,8 @@ def test_linear_f32_row_max(m, n, k, splits):
     (1280, 4096, 2048, "residual"),   # 160 tiles: 152 whole, 8 tail tiles split 8 ways
     (1280, 2048, 2048, "swiglu"),     # 10 x 16 SwiGLU tiles (gate / up halves paired in the reduce)
     (1290, 4100, 1024, "bf16"),       # ragged edges: 187 tiles, 35 tail tiles split 4 ways
-    (1280, 4096, 2048, "f32")])       # fp32 logits with the row maxima published by the reduce
+    (1280, 4096, 2048, "f32"),        # fp32 logits with the row maxima published by the reduce
+    (3840, 4096, 14336, "residual")])  # the target's down projection: 24 tail tiles split 6 ways
 def test_linear_split_tail(m, n, k, epi_name):
     """Whole waves of tiles run data-parallel and the partial last wave's tiles are split along k,
     their partials added in split order by a second kernel: the same products as the fp64 matmul."""
