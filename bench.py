@@ -403,10 +403,8 @@ def run_gpu(args):
     host_tc = eng.tc.cpu().pin_memory()
     out_len = torch.empty_like(eng.accept_len, device="cpu").pin_memory()
     eng.timing = False
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for i in range(args.steps):
+
+    def e2e_step(i):
         eng.aux_in.copy_(host_aux, non_blocking=True)
         eng.next_tok.copy_(host_tok, non_blocking=True)
         eng.tc.copy_(host_tc, non_blocking=True)
@@ -418,6 +416,16 @@ def run_gpu(args):
         host_tok.copy_(eng.next_tok, non_blocking=True)
         host_tc.copy_(eng.tc, non_blocking=True)
         out_len.copy_(eng.accept_len, non_blocking=True)
+
+    # untimed warm-up steps right before the timed ones, as for the device-timed loop: after the pause
+    # above, the first steps run at a higher clock than the power cap then settles to
+    for i in range(args.warmup):
+        e2e_step(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(args.steps):
+        e2e_step(i)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)

@@ -149,3 +149,58 @@ def test_accept_device_step_counter(mode):
         got = {k: v.cpu().numpy() for k, v in out.items()}
         _compare(got, mode, zt, zd, tokens, parents, W, range(B), seed=3, step=s0 + r)
     assert int(counter.item()) == s0 + 3
+
+
+def _chi2_pvalue(hist, p):
+    """Chi-square p-value of a histogram against probabilities p (cells with p = 0 must be empty)."""
+    from scipy import stats
+    assert hist[p == 0].sum() == 0
+    keep = p > 0
+    exp = p[keep] * hist.sum()
+    return stats.chisquare(hist[keep], exp).pvalue
+
+
+@pytest.mark.parametrize("mode", [oacc.TOPK, oacc.SAMPLED])
+def test_accept_emits_the_target_distribution(mode):
+    """Losslessness through the C ABI ("Speculative Decoding (EAGLE3) in the vLLM Neuron Framework",
+    "Rejection Sampling"): 16384 sequences share one small tree and its logits and differ only in
+    their Philox streams (the sequence index), so one call draws 16384 independent acceptances.  The
+    first emitted token follows the target's p at the root (chi-square p-value > 1e-3, total
+    variation < 0.02); for TOPK the token emitted after an accepted child follows that child's p.
+    SAMPLED children are drawn from the draft's distribution by the oracle's draw."""
+    from oracle import dsm
+    r = np.random.default_rng(21)
+    V, B, W, seed = 8, 16384, 4, 4242
+    parents1 = [-1, 0, 0, 0, 1, 1, 2] if mode == oacc.TOPK else [-1, 0, 0, 0]
+    N = len(parents1)
+    zt1 = (1.5 * r.standard_normal((N, V))).astype(np.float32)
+    if mode == oacc.TOPK:
+        # deterministic top-k children: the root's three likeliest tokens, then each child's likeliest
+        top = lambda z, k: [int(x) for x in np.argsort(-z, kind="stable")[:k]]
+        tokens1 = [0] + top(zt1[0], 3) + top(zt1[1], 2) + top(zt1[2], 1)
+    zd1 = (zt1 + r.standard_normal((N, V))).astype(np.float32)
+    zt = np.ascontiguousarray(np.broadcast_to(zt1, (B, N, V)))
+    zd = np.ascontiguousarray(np.broadcast_to(zd1, (B, N, V))) if mode == oacc.SAMPLED else None
+    parents = np.tile(np.asarray(parents1, np.int32), (B, 1))
+    if mode == oacc.TOPK:
+        tokens = np.tile(np.asarray(tokens1, np.int32), (B, 1))
+    else:
+        tokens = np.zeros((B, N), np.int32)
+        for b in range(B):
+            kids = oacc.draw_children(zd1[0], 1.0, N - 1, seed=seed, step=0, b=b, node=0)
+            assert len(kids) == N - 1
+            tokens[b, 1:] = kids
+    got = _run(mode, zt, zd, tokens, parents, W, seed=seed, step=0)
+    _compare(got, mode, zt, zd, tokens, parents, W, [0, 1, B - 1], seed=seed)
+    inv_t = dsm.inv_temperature(1.0)
+    first = np.bincount(got["emitted"][:, 0], minlength=V).astype(np.float64)
+    p0 = np.asarray(dsm.probabilities(zt1[0], inv_t), np.float64)
+    assert _chi2_pvalue(first, p0) > 1e-3
+    assert 0.5 * np.abs(first / B - p0).sum() < 0.02
+    if mode == oacc.TOPK:
+        for c in (1, 2):   # children of the root that have children of their own
+            sel = (got["accept_len"] >= 1) & (got["path"][:, 1] == c)
+            assert sel.sum() > 500
+            h = np.bincount(got["emitted"][sel, 1], minlength=V).astype(np.float64)
+            pc = np.asarray(dsm.probabilities(zt1[c], inv_t), np.float64)
+            assert _chi2_pvalue(h, pc) > 1e-3
