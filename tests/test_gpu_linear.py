@@ -206,7 +206,8 @@ def test_linear_f32_row_max(m, n, k, splits):
     (1280, 2048, 2048, "swiglu"),     # 10 x 16 SwiGLU tiles (gate / up halves paired in the reduce)
     (1290, 4100, 1024, "bf16"),       # ragged edges: 187 tiles, 35 tail tiles split 4 ways
     (1280, 4096, 2048, "f32"),        # fp32 logits with the row maxima published by the reduce
-    (3840, 4096, 14336, "residual")])  # the target's down projection: 24 tail tiles split 6 ways
+    (3840, 4096, 14336, "residual"),  # the target's down projection: 24 tail tiles split 6 ways
+    (1290, 4100, 12288, "residual")])  # ragged, long k: 35 tail tiles split 4 ways (stream-K's shape before)
 def test_linear_split_tail(m, n, k, epi_name):
     """Whole waves of tiles run data-parallel and the partial last wave's tiles are split along k,
     their partials added in split order by a second kernel: the same products as the fp64 matmul."""
@@ -238,6 +239,7 @@ def test_linear_split_tail(m, n, k, epi_name):
     (130, 1000, 256, "residual"),      # data-parallel, a partial 256-column block, direct-store tails
     (1280, 4096, 2048, "residual"),    # split tail: the reduce kernel writes outputs and row sums
     (768, 4096, 12288, "bf16"),        # stream-K: owners finish the cut tiles
+    (1290, 4100, 12288, "residual"),   # ragged split tail at long k (35 tail tiles, 4 ranges)
     (300, 1000, 512, "bf16")])         # unaligned pitch of the output: direct stores
 def test_linear_row_ssq(m, n, k, epi_name):
     """row_ssq: for each row and block of 256 output columns, the sum of squares of the bf16 outputs
