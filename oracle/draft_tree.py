@@ -40,8 +40,11 @@ parity unpinned beyond invariants: the EAGLE-2 source is not on the pages.
 The invariants tested are the node count, depth bound, ancestor closure,
 frontier = top-k at each depth, every candidate's score recomputed as the fp32
 running sum of the log-softmax of its ancestors' expansion rows at their
-tokens, final set = top N-1 over all candidates by brute-force sort, and that
-top_k = 1 gives the chain drafting of section XI.2.
+tokens, final set = top N-1 over all candidates by brute-force sort, that
+top_k = 1 gives the chain drafting of section XI.2, and that at depth 2 with a
+budget keeping every candidate (N = 1 + k + k^2) the tree is the fixed-branching
+expansion [k, k] of "Advanced speculative decoding: tree drafts and EAGLE"
+(``build_draft_tree``) for a path-dependent draft.
 """
 import numpy as np
 

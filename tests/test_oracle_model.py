@@ -326,6 +326,54 @@ def test_dynamic_tree_invariants(depth, top_k, n_nodes):
     assert [c["token"] for c in first] == list(np.lexsort((np.arange(300), -order_key(row)))[:top_k])
 
 
+@pytest.mark.parametrize("top_k,V", [(3, 50), (7, 300)])   # 1 + k + k^2 <= 64 nodes
+def test_full_budget_depth2_is_the_static_expansion(top_k, V):
+    """With depth 2 and a node budget that keeps every candidate (N = 1 + k + k^2), the dynamic tree
+    is the fixed-branching expansion of "Advanced speculative decoding: tree drafts and EAGLE"
+    ("Implementation", build_draft_tree with branching [k, k]): the root's k likeliest draft tokens,
+    and under each of them that node's own k likeliest.  The draft here is path-dependent (each
+    node's logits are drawn from a seed made of the tokens on its path), so a wrong parent link or
+    a child taken from another node's row changes the set of paths."""
+    def logits_for(path):
+        seed = 7
+        for tok in path:
+            seed = (seed * 1000003 + tok + 1) % (2 ** 31)
+        return (2.0 * np.random.default_rng(seed).standard_normal(V)).astype(np.float32)
+
+    def best(row, k):
+        return sorted(range(V), key=lambda i: (-float(row[i]), i))[:k]
+
+    cands = []
+
+    def path_of(cid):
+        toks = []
+        while cid != -1:
+            toks.append(cands[cid]["token"])
+            cid = cands[cid]["parent"]
+        return tuple(reversed(toks))
+
+    def expand(t, front):
+        return np.stack([logits_for(() if f is None else path_of(f)) for f in front])
+
+    res = draft_tree.select_tree(expand, 2, top_k, 1 + top_k + top_k * top_k, cands=cands)
+    tokens, parents = res["tokens"], res["parents"]
+    got = set()
+    for i in range(1, len(tokens)):
+        path, j = [], i
+        while j != 0:
+            path.append(int(tokens[j]))
+            j = int(parents[j])
+        got.add(tuple(reversed(path)))
+    # the static expansion, level by level
+    want = set()
+    for a in best(logits_for(()), top_k):
+        want.add((a,))
+        for b in best(logits_for((a,)), top_k):
+            want.add((a, b))
+    assert len(got) == top_k + top_k * top_k
+    assert got == want
+
+
 def test_top1_tree_is_a_chain():
     res = draft_tree.select_tree(_random_expand(5, 100), 4, 1, 5)
     assert res["parents"].tolist() == [-1, 0, 1, 2, 3]
