@@ -170,3 +170,18 @@ def test_draft_tree_full_shapes_replay(B, Vd):
     assert (g["parents"][:, 0] == -1).all() and (g["depth"] <= depth).all()
     for b in range(B):
         assert all(0 <= g["parents"][b, i] < i for i in range(1, N))
+
+
+@pytest.mark.parametrize("B", [24, 200])
+def test_draft_tree_rows_not_multiple_of_four_floats(B):
+    """Logit rows of 1001 floats (not a multiple of 16 bytes, so no shared-memory ring) with more rows
+    than the cluster top-k takes: B = 24 (96 frontier rows) runs the register-fed top-k with 256-thread
+    CTAs; B = 200 (200 root rows, then 800 frontier rows, more than one wave of those) also runs its
+    128-thread variant.  The tree must equal the oracle's selection on the GPU's logits."""
+    d, Hq, Hkv, F, V, depth, K, N = 256, 4, 2, 512, 1001, 3, 4, 10
+    L = 20
+    s = _setup(6, B, d, Hq, Hkv, F, V, [1] * B, [L] * B, L + 32)
+    g = _run_gpu(s, Hq, F, V, depth, K, N, L)
+    for b in sorted({0, 1, B // 2, B - 1}):
+        _check_replay(g, s, b, B, depth, K, N)
+    assert (g["draft_len"] == L + 1).all()
