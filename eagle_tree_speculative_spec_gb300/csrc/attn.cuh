@@ -41,9 +41,6 @@ struct AttnLaunch {
     // pool_slots = slots in the pool
     const int32_t *block_table = nullptr;
     int bt_stride = 0, block_size = 0, pool_slots = 0;
-    // rotated q with a parent array normally runs on the persistent kernel (one CTA per SM walking
-    // the work items); 1 = one CTA per work item instead (the non-persistent kernel)
-    int one_cta_per_item = 0;
 };
 
 size_t tree_attn_workspace(const AttnLaunch &a);

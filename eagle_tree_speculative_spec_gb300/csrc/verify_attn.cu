@@ -23,11 +23,12 @@
 //                 than 8 (the result is the same, the intermediate weights stay below 2^8)
 // A kernel before this one rotates the query slots' keys in tree_k at their positions (prefix
 // length + depth); the last split then also streams the tree tile (64 rows of tree_k / tree_v, by
-// TMA like the prefix) and masks it with the ancestor bitmask.  When q and the tree keys arrive
-// already rotated (qk_rotated: the QKV projection applied RoPE), that kernel does not run and Q
-// comes in by one 4-D TMA load instead of the softmax warps' staging.  Thread 0 issues Q and the
-// first K tiles as soon as it has initialised their barriers.  With more than one split the
-// partial (O, m, l) go to the workspace and another kernel merges them in split order.
+// TMA like the prefix) and masks it with the ancestor bitmask.  Thread 0 issues the first K tiles
+// as soon as it has initialised their barriers.  With more than one split the partial (O, m, l) go
+// to the workspace and another kernel merges them in split order.  Queries and tree keys that
+// arrive already rotated (qk_rotated: the QKV projection applied RoPE, always with a parent array)
+// run on the persistent kernel further below, which loads Q by 4-D TMA boxes and needs neither the
+// key rotation nor the staging.
 // All waits are bounded; a timeout sets EAGLE3_DEV_TIMEOUT and the CTA drains and exits.
 #include <cudaTypedefs.h>
 
@@ -179,7 +180,7 @@ E3_DEV void rope_chunks(uint4 &lo, uint4 &hi, const float cs[8], const float sn[
 __global__ void __launch_bounds__(NT, 1)
     verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_tk, const __grid_constant__ CUtensorMap tm_tv,
-                       const __grid_constant__ CUtensorMap tm_q, const Params p) {
+                       const Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ SmemStatic ss;
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -251,22 +252,10 @@ __global__ void __launch_bounds__(NT, 1)
         }
         tc::mbar_init(&ss.s_done, 1);
         tc::mbar_init(&ss.pv_mma_done, 1);
-        tc::mbar_init(&ss.q_ready, p.qk_rotated ? 1 : 8);   // the Q load, or the eight staging warps
+        tc::mbar_init(&ss.q_ready, 8);   // the eight staging warps
         ss.abort_flag = 0;
         tc::fence_barrier_init();
         if (n_tiles > 0) {
-            if (p.qk_rotated) {
-                // Q as is: two 64-column blocks of (slot, head) rows, rows = slot * rep + head
-                tc::mbar_expect_tx(&ss.q_ready, Q_TILE);
-                const int hs = g * rep;
-                if (p.tree_slot_inner) {
-                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, s_lo, b, &ss.q_ready);
-                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, s_lo, b, &ss.q_ready);
-                } else {
-                    tc::tma_load_4d(sm + OFF_Q, &tm_q, 0, hs, b, s_lo, &ss.q_ready);
-                    tc::tma_load_4d(sm + OFF_Q + Q_TILE / 2, &tm_q, 64, hs, b, s_lo, &ss.q_ready);
-                }
-            }
             npre = min(ST_K, n_prefix);   // fresh stages: nothing to wait for
             for (int j = 0; j < npre; ++j) {
                 if (j == p.stall_tile) continue;   // timeout-path test: this tile never arrives
@@ -310,8 +299,8 @@ __global__ void __launch_bounds__(NT, 1)
             uint8_t *ring = sm + (is_k ? OFF_K : OFF_V);
             tc::prefetch_tmap(map);
             if (last) tc::prefetch_tmap(tmap);
-            // V stage 1 holds the RoPE angle table until Q is staged (not used when Q arrives rotated)
-            bool go = is_k || p.qk_rotated || tc::mbar_wait(&ss.q_ready, 0, abort, p.wait_limit);
+            // V stage 1 holds the RoPE angle table until Q is staged
+            bool go = is_k || tc::mbar_wait(&ss.q_ready, 0, abort, p.wait_limit);
             const int j0 = is_k ? npre : 0;                  // thread 0 issued K tiles [0, npre) in phase A
             uint32_t issued = is_k ? (1u << npre) - 1u : 0u, last_par = 0;
             if (is_k && p.stall_tile >= 0 && p.stall_tile < npre) issued &= ~(1u << p.stall_tile);
@@ -337,11 +326,6 @@ __global__ void __launch_bounds__(NT, 1)
                 last_par = (last_par & ~(1u << s)) | (ph << s);
             }
             if (!go) flag(p.dev_status, EAGLE3_DEV_TIMEOUT);
-            if (is_k && p.qk_rotated) {   // the Q load too (bounded)
-                const long long t0 = clock64();
-                while (!tc::mbar_try(&ss.q_ready, 0) && clock64() - t0 < p.wait_limit) {
-                }
-            }
             // no TMA write may be in flight when the CTA exits (bounded)
             for (int s = 0; s < stages; ++s) {
                 if (!((issued >> s) & 1u)) continue;
@@ -446,7 +430,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight softmax warps only
-        if (!p.qk_rotated) {
+        {
             const int c = lane & 7, sub = lane >> 3;
             // RoPE angles of every position in [pos_lo, pos_lo + span), once per CTA, in V stage 1
             // (its first load waits for Q to be staged); others are computed directly
@@ -1551,15 +1535,15 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
             cudaSuccess)   // 32 rows per block
             return EAGLE3_ERR_CUDA;
     }
-    if (p.qk_rotated && p.parents && !a.one_cta_per_item) {
-        // rotated q with a parent array: one persistent CTA per SM walks the work items
+    if (p.qk_rotated) {
+        // rotated q (always with a parent array): one persistent CTA per SM walks the work items
         const int items = splits * p.halves * a.Hkv * pt.nb;
         const int grid = std::min(items, sm_count_cached());
         if (launch_pdl(verify_attn_pers_kernel, dim3(grid), dim3(NT_P), SMEM_DYN, stream, mk, mv, mtk, mtv, mq, p,
                        items) != cudaSuccess)
             return EAGLE3_ERR_CUDA;
     } else if (launch_pdl(verify_attn_kernel, dim3(splits * p.halves, a.Hkv, pt.nb), dim3(NT), SMEM_DYN, stream, mk,
-                          mv, mtk, mtv, mq, p) != cudaSuccess) {
+                          mv, mtk, mtv, p) != cudaSuccess) {
         return EAGLE3_ERR_CUDA;
     }
     if (cudaGetLastError() != cudaSuccess) return EAGLE3_ERR_CUDA;
@@ -1584,6 +1568,8 @@ size_t tree_attn_workspace(const AttnLaunch &a) {
 
 eagle3_status_t tree_attn_launch(const AttnLaunch &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     if (a.B == 0 || a.q_hi <= a.q_lo) return EAGLE3_OK;
+    // rotated q runs on the persistent kernel, which walks a parent array (ancestor masks: in-call RoPE)
+    if (a.qk_rotated && !a.parents) return EAGLE3_ERR_UNSUPPORTED;
     const size_t need = tree_attn_workspace(a);
     if (need && (!workspace || ws_bytes < need || ((uintptr_t)workspace & 15))) return EAGLE3_ERR_WORKSPACE;
     // rows of q / tree k / tree v / out are moved 16 bytes at a time
