@@ -60,7 +60,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -93,8 +93,9 @@ class ClockSampler:
         sm = sorted(float(r[1]) for r in rows if num(r[1]))
         mx = max([float(r[2]) for r in rows if num(r[2])] or [0.0])
         reasons = sorted({self.NAMES[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        pw = sorted(float(r[3]) for r in rows if num(r[3]))
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "power_w": pw[len(pw) // 2] if pw else None}
 
 
 # ----------------------------------------------------------------------------------------- GPU arm
