@@ -897,6 +897,98 @@ def run_kernel(args):
         flops = 2.0 * M * N * K * (2 if w2 is not None else 1)
         out.update(m=M, n=N, k=K, epilogue=args.epilogue, ms=round(ms, 4), tflops=round(flops / ms / 1e9, 1),
                    frac_sustained=round(flops / ms / 1e9 / tf_sust, 4), frac_burst=round(flops / ms / 1e9 / tf_burst, 4))
+    elif args.kernel == "next":
+        # the NEXT rows, each on its prepared C call: the verify attention through block tables (paged
+        # KV) beside the contiguous cache, the training-time-test attention, the chain rejection
+        # sampler of a ragged batch and the batch's index bookkeeping
+        import ctypes
+
+        import numpy as np
+
+        import synth
+        L_ = e3._lib
+        lib = L_.lib()
+        stp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        bf, i32 = torch.bfloat16, torch.int32
+        cpu_g = torch.Generator().manual_seed(11)
+        B, N, Hq, Hkv, D = 64, 60, 32, 8, 128
+        paged = {}
+        for Lp in (2048, 4096):
+            q = torch.randn(B, N, Hq, D, generator=g, device=dev).to(bf)
+            tk = torch.randn(B, N, Hkv, D, generator=g, device=dev).to(bf)
+            tv = torch.randn(B, N, Hkv, D, generator=g, device=dev).to(bf)
+            parents = torch.as_tensor(synth.random_tree(synth.rng(3), N)).to(i32).repeat(B, 1).to(dev)
+            plen = torch.full((B,), Lp, dtype=i32, device=dev)
+            o = torch.empty(B, N, Hq, D, device=dev, dtype=bf)
+            nbytes = B * (4096 * Lp + 245760 + 983040)     # as the contiguous call (the pool is read once too)
+            row = {}
+            for bs in (0, 64, 256):                         # 0: the contiguous cache
+                if bs == 0:
+                    kc = torch.randn(B, Hkv, Lp + 64, D, generator=g, device=dev).to(bf)
+                    vc = torch.randn(B, Hkv, Lp + 64, D, generator=g, device=dev).to(bf)
+                    a = L_.verify_attn_args(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=Lp, qk_rotated=True)
+                else:
+                    max_blocks = (Lp + bs - 1) // bs + 1
+                    n_pages = B * max_blocks
+                    bt = torch.randperm(n_pages, generator=cpu_g).view(B, max_blocks).to(i32).to(dev)
+                    kc = torch.randn(n_pages * bs, Hkv, D, generator=g, device=dev).to(bf)
+                    vc = torch.randn(n_pages * bs, Hkv, D, generator=g, device=dev).to(bf)
+                    a = L_.verify_attn_args(q, tk, tv, kc, vc, parents, plen, o, max_prefix_len=Lp, qk_rotated=True,
+                                            block_table=bt, block_size=bs)
+                ws = torch.empty(max(16, L_.eagle3_verify_attn_workspace_size(a)), dtype=torch.uint8, device=dev)
+                ms = _time_loop(_raw_call(lib.eagle3_verify_attn, a, ws), args.steps, args.warmup)
+                row["contiguous" if bs == 0 else f"block_size_{bs}"] = {
+                    "ms": round(ms, 4), "frac_hbm": round(nbytes / ms / 1e6 / hbm, 4)}
+                del kc, vc
+            paged[f"prefix_{Lp}"] = row
+        out["paged_verify_attn"] = dict(paged, batch=B, nodes=N, bytes_per_call="B * (4096 L + 1.23 MB)")
+        # training-time-test attention: 8 sequences of 2048 positions, the native step and 2 simulated
+        Bt, T, S_ = 8, 2048, 3
+        q = torch.randn(Bt, T, Hq, D, generator=g, device=dev).to(bf)
+        k = torch.randn(S_, Bt, T, Hkv, D, generator=g, device=dev).to(bf)
+        v = torch.randn(S_, Bt, T, Hkv, D, generator=g, device=dev).to(bf)
+        o = torch.empty_like(q)
+        a = L_.TttAttnArgs(batch=Bt, seq_len=T, n_heads=Hq, n_kv_heads=Hkv, head_dim=D, n_steps=S_, sm_scale=0.0,
+                           q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), out=o.data_ptr(), dev_status=None)
+        ws = torch.empty(max(16, lib.eagle3_ttt_attn_workspace_size(ctypes.byref(a))), dtype=torch.uint8, device=dev)
+        ms = _time_loop(_raw_call(lib.eagle3_ttt_attn, a, ws), args.steps, args.warmup)
+        flops = 4.0 * D * Bt * Hq * (T * (T + 1) / 2 + T * (S_ - 1))   # causal QK and PV, plus the diagonal keys
+        out["ttt_attn"] = {"batch": Bt, "seq_len": T, "steps": S_, "heads": [Hq, Hkv], "ms": round(ms, 4),
+                           "tflops": round(flops / ms / 1e9, 1), "frac_burst": round(flops / ms / 1e9 / tf_burst, 4)}
+        del q, k, v, o
+        # chain rejection sampler: 64 requests of 0..5 drafts over V = 128256 (logits N(0, 3^2)), and the
+        # ragged batch's index bookkeeping
+        R, K, V = 64, 5, 128256
+        d, logits, drafts, greedy = synth.chain_batch(7, R, K, V)
+        z = torch.as_tensor(logits, device=dev)
+        dr = torch.as_tensor(drafts, dtype=i32, device=dev)
+        cu = torch.as_tensor(np.cumsum(d).astype(np.int32), device=dev)
+        gr = torch.as_tensor(greedy, dtype=i32, device=dev)
+        oc = torch.empty(R, K + 1, dtype=i32, device=dev)
+        nacc = torch.empty(R, dtype=i32, device=dev)
+        a = L_.ChainVerifyArgs(n_requests=R, vocab=V, max_drafts=K, temperature=1.0, seed=2, step=0,
+                               logits=z.data_ptr(), draft_tokens=dr.data_ptr(), cu_num_draft_tokens=cu.data_ptr(),
+                               is_greedy=gr.data_ptr(), output_tokens=oc.data_ptr(), num_accepted=nacc.data_ptr(),
+                               dev_status=None, step_counter=None)
+        ms = _time_loop(lambda: lib.eagle3_chain_verify(ctypes.byref(a), stp), args.steps, args.warmup, flush)
+        torch.cuda.synchronize()
+        visited = int((nacc.to(torch.int64) + 1).sum())     # rows each request's walk reads
+        out["chain_verify"] = {"requests": R, "max_drafts": K, "vocab": V, "rows": int(z.shape[0]),
+                               "rows_visited": visited, "us": round(ms * 1e3, 1),
+                               "gbs_two_passes_per_visited_row": round(2 * visited * V * 4 / ms / 1e6, 1)}
+        nd = torch.as_tensor(d, device=dev)
+        cu_sched = torch.as_tensor(np.cumsum(d + 1).astype(np.int32), device=dev)
+        max_rows = int(d.sum()) + R
+        li = torch.empty(max_rows, dtype=i32, device=dev)
+        tli = torch.empty(max_rows, dtype=i32, device=dev)
+        bli = torch.empty(R, dtype=i32, device=dev)
+        nrows = torch.empty(1, dtype=i32, device=dev)
+        a = L_.SpecDecodeMetadataArgs(n_requests=R, max_rows=max_rows, cu_num_scheduled_tokens=cu_sched.data_ptr(),
+                                      num_draft_tokens=nd.data_ptr(), cu_num_draft_tokens=cu.data_ptr(),
+                                      logits_indices=li.data_ptr(), target_logits_indices=tli.data_ptr(),
+                                      bonus_logits_indices=bli.data_ptr(), num_rows=nrows.data_ptr(), dev_status=None)
+        ms = _time_loop(lambda: lib.eagle3_spec_decode_metadata(ctypes.byref(a), stp), args.steps, args.warmup)
+        out["spec_decode_metadata"] = {"requests": R, "us": round(ms * 1e3, 2)}
     elif args.kernel == "tiny":
         # the tiny lossless configuration (fp32, 4-layer d = 64 target and its EAGLE-3 head, 32-token
         # prompt): greedy speculative decoding with a K = 4 chain and vanilla greedy decoding, 64 new
@@ -976,7 +1068,7 @@ def main():
     ap.add_argument("--epilogue", default="swiglu", choices=["swiglu", "bf16", "f32", "residual"])
     ap.add_argument("--draft-vocab", type=int, default=0,
                     help="--kernel draft: a reduced draft vocabulary of this many target ids (0 = all)")
-    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm", "tiny"],
+    ap.add_argument("--kernel", choices=["verify_attn", "accept", "draft", "gemm", "tiny", "next"],
                     help="time one kernel of the path instead of the whole step")
     ap.add_argument("--prefix", type=int, default=4096)
     ap.add_argument("--mode", default="topk", choices=["greedy", "topk", "sampled"])
