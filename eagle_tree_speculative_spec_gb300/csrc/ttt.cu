@@ -24,6 +24,7 @@ int ttt_chunk(int rep) { return rep > 4 ? 256 / rep : 64; }
 
 struct Geometry {
     int rep, C, chunks, max_blocks;
+    int page;   // positions per page of the identity block table: 128 when T allows (whole-tile boxes), else 64
     size_t o_bt, o_par, o_pre, o_lse, o_attn, total;
 };
 
@@ -32,7 +33,8 @@ Geometry geometry(const eagle3_ttt_attn_args_t *a) {
     g.rep = a->n_heads / a->n_kv_heads;
     g.C = ttt_chunk(g.rep);
     g.chunks = a->batch * (a->seq_len / g.C);
-    g.max_blocks = a->seq_len / 64;
+    g.page = a->seq_len % 128 == 0 ? 128 : 64;
+    g.max_blocks = a->seq_len / g.page;
     size_t at = 0;
     auto take = [&](size_t bytes) {
         const size_t o = at;
@@ -174,7 +176,7 @@ AttnLaunch causal_launch(const eagle3_ttt_attn_args_t *a, const Geometry &g, uin
     l.qk_rotated = 1;
     l.block_table = ws ? (const int32_t *)(ws + g.o_bt) : (const int32_t *)nullptr;
     l.bt_stride = g.max_blocks;
-    l.block_size = 64;
+    l.block_size = g.page;
     l.pool_slots = a->batch * T;
     return l;
 }

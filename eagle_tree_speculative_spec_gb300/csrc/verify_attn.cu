@@ -74,6 +74,7 @@ struct Params {
     int stall_tile;                 // timeout-path test only: this prefix tile is never loaded (-1 off)
     const int32_t *block_table;     // paged cache (slot pool [n_slots, Hkv, 128]) or null (contiguous)
     int bt_stride, block_size, n_pages;
+    int pool_box;                   // slots per box of the pool's tensor map: 128 (block_size % 128 == 0) or 64
     long long wait_limit;           // clocks after which a bounded wait gives up
     float scale_log2;               // sm_scale * log2(e)
     float inv_freq[D / 2];
@@ -207,9 +208,11 @@ __global__ void __launch_bounds__(NT, 1)
     const int n_prefix = (k_hi - k_lo + BK - 1) / BK;
     const int n_tiles = n_prefix + (last ? 1 : 0);
     // one 128-key prefix tile of K or V into a stage (two 64-column blocks of 16 KB).  Contiguous
-    // cache: two 128-row boxes of the [B * Hkv * S, 128] view.  Paged cache: four 64-slot boxes of
-    // the [n_slots, Hkv, 128] pool (a 64-aligned run of positions stays inside one page); runs past
-    // the prefix, or on a page id outside the pool, start at slot -64 and read as zeros.
+    // cache: two 128-row boxes of the [B * Hkv * S, 128] view.  Paged cache: two 128-slot boxes of
+    // the [n_slots, Hkv, 128] pool when pages hold a multiple of 128 positions (a tile, which starts
+    // at a multiple of 128, stays inside one page), else four 64-slot boxes (a 64-aligned run stays
+    // inside one page); runs past the prefix, or on a page id outside the pool, start at a negative
+    // slot and read as zeros.
     const int row0 = ((b * p.Hkv + g) * p.S) + k_lo;
     auto load_prefix_tile = [&](uint8_t *dst, const CUtensorMap *map, int j, uint64_t *bar) {
         if (!p.block_table) {
@@ -219,6 +222,17 @@ __global__ void __launch_bounds__(NT, 1)
             return;
         }
         const int32_t *bt = p.block_table + (size_t)b * p.bt_stride;
+        if (p.pool_box == BK) {
+            const int pos = k_lo + j * BK;
+            int slot = -BK;
+            if (pos < L) {
+                const int page = __ldg(bt + pos / p.block_size);
+                if (page >= 0 && page < p.n_pages) slot = page * p.block_size + pos % p.block_size;
+            }
+            tc::tma_load_3d(dst, map, 0, g, slot, bar);
+            tc::tma_load_3d(dst + KV_TILE / 2, map, 64, g, slot, bar);
+            return;
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int pos = k_lo + j * BK + 64 * h;
@@ -830,6 +844,16 @@ __global__ void __launch_bounds__(NT_P, 1)
                             const int y = row0 + j * BK;
                             tc::tma_load_2d(dst, map, 0, y, &full[s]);
                             tc::tma_load_2d(dst + KV_TILE / 2, map, 64, y, &full[s]);
+                        } else if (p.pool_box == BK) {   // one page holds the whole tile
+                            const int32_t *bt = p.block_table + (size_t)w.b * p.bt_stride;
+                            const int pos = w.k_lo + j * BK;
+                            int slot = -BK;
+                            if (pos < w.L) {
+                                const int page = __ldg(bt + pos / p.block_size);
+                                if (page >= 0 && page < p.n_pages) slot = page * p.block_size + pos % p.block_size;
+                            }
+                            tc::tma_load_3d(dst, map, 0, w.g, slot, &full[s]);
+                            tc::tma_load_3d(dst + KV_TILE / 2, map, 64, w.g, slot, &full[s]);
                         } else {
                             const int32_t *bt = p.block_table + (size_t)w.b * p.bt_stride;
 #pragma unroll
@@ -1370,13 +1394,13 @@ bool make_q_map(CUtensorMap *m, const void *base, int nb, int n_slots, int Hq, i
 }
 
 // paged pool [n_slots, Hkv, 128] as a 3-D tensor (columns, head, slot); boxes of 64 columns x 1
-// head x 64 slots land like 64 rows of a cache tile
-bool make_pool_map(CUtensorMap *m, const void *base, int64_t n_slots, int Hkv) {
+// head x box_slots (64 or 128) slots land like that many rows of a cache tile
+bool make_pool_map(CUtensorMap *m, const void *base, int64_t n_slots, int Hkv, int box_slots) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)n_slots};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_slots};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1507,8 +1531,10 @@ eagle3_status_t launch_part(const AttnLaunch &a, const Part &pt, void *workspace
     p.bt_stride = a.bt_stride;
     p.block_size = a.block_size;
     p.n_pages = a.block_table ? a.pool_slots / a.block_size : 0;
+    p.pool_box = a.block_table && a.block_size % BK == 0 ? BK : 64;
     if (a.block_table) {
-        if (!make_pool_map(&mk, a.k_cache, a.pool_slots, a.Hkv) || !make_pool_map(&mv, a.v_cache, a.pool_slots, a.Hkv))
+        if (!make_pool_map(&mk, a.k_cache, a.pool_slots, a.Hkv, p.pool_box) ||
+            !make_pool_map(&mv, a.v_cache, a.pool_slots, a.Hkv, p.pool_box))
             return EAGLE3_ERR_CUDA;
     } else {
         const size_t cache_off = b0 * a.Hkv * a.S * D;
