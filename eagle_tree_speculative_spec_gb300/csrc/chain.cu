@@ -9,13 +9,18 @@
 // target distribution).
 //
 // Design: the bookkeeping is one CTA running a chunked block-wide scan over the requests.  The
-// sampler runs one CTA of 512 threads per request: each visited row is read by the whole CTA with
-// 16-byte loads (a row maximum pass, then one pass for the fixed-point normaliser or one for the
-// Gumbel-max draw, which makes one Philox block per four tokens).  Only the rows of the drafts up
-// to the first rejection are read.  Every decision is broadcast through shared memory, so all
-// threads of a CTA follow one control path.
+// sampler runs one thread-block cluster of CLC CTAs per request: CTA r of the cluster reads its
+// slice of every visited row with 16-byte loads (a row maximum pass, then one pass for the
+// fixed-point normaliser or one for the Gumbel-max draw, which makes one Philox block per four
+// tokens, keyed by the four tokens' index in the row).  The slices' maxima, sums and argmax keys
+// are combined through distributed shared memory in rank order, so every CTA holds the same values
+// and takes the same decisions.  Only the rows of the drafts up to the first rejection are read.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "eagle3_chain.h"
+
+namespace cg = cooperative_groups;
 
 namespace e3 {
 namespace {
@@ -93,7 +98,8 @@ __global__ void __launch_bounds__(NT_META) spec_meta_kernel(const eagle3_spec_de
 // ---------------------------------------------------------------------------------------------
 // Sampler
 // ---------------------------------------------------------------------------------------------
-constexpr int NT = 512;
+constexpr int CLC = 8;     // CTAs per cluster (one cluster per request)
+constexpr int NT = 256;    // threads per CTA
 constexpr int NW = NT / 32;
 constexpr uint32_t ACCEPT_C0 = 0x7fffffffu;
 
@@ -110,6 +116,7 @@ struct CParams {
 struct CSmem {
     uint64_t part[NW];
     uint64_t bcast;
+    uint64_t cl[2];   // this CTA's partial of the cluster-wide reduction (double-buffered by parity)
 };
 
 // block-wide reductions of one value per thread; the result is returned to every thread
@@ -148,12 +155,31 @@ E3_DEV uint64_t block_sum_u64(CSmem &s, uint64_t v) {
     return r;
 }
 
-// f(x, z_x) over a row, four consecutive tokens per step (one 16-byte load when the row allows)
+// The cluster-wide maximum / sum of one value per CTA (every thread passes its CTA's value; every
+// thread gets the result): each CTA publishes its value, one cluster barrier, every thread reads the
+// CLC values in rank order.  Partials alternate between two slots, so one barrier per reduction
+// suffices: a slot is rewritten two reductions later, after every CTA has passed the barrier in
+// between, i.e. after every CTA has read it.
+template <bool MAX>
+E3_DEV uint64_t cluster_reduce_u64(CSmem &s, cg::cluster_group &cluster, uint32_t &par, uint64_t v) {
+    if (threadIdx.x == 0) s.cl[par] = v;
+    cluster.sync();
+    uint64_t acc = 0;
+#pragma unroll
+    for (int r = 0; r < CLC; ++r) {
+        const uint64_t x = *cluster.map_shared_rank(&s.cl[par], r);
+        acc = MAX ? (x > acc ? x : acc) : acc + x;
+    }
+    par ^= 1u;
+    return acc;
+}
+
+// f(j, x0, z[x0 .. x0+3]) over this CTA's slice of a row: the float4 groups j in [j_lo, j_hi) of
+// tokens 4j .. 4j+3 (one 16-byte load when the row allows)
 template <typename F>
-E3_DEV void for_row4(const float *z, int V, F f) {
+E3_DEV void for_row4(const float *z, int V, int j_lo, int j_hi, F f) {
     const bool vec = (((uintptr_t)z) & 15) == 0;
-    const int n4 = (V + 3) / 4;
-    for (int j = threadIdx.x; j < n4; j += NT) {
+    for (int j = j_lo + (int)threadIdx.x; j < j_hi; j += NT) {
         float v[4];
         const int x0 = 4 * j;
         if (vec && x0 + 4 <= V) {
@@ -170,12 +196,15 @@ E3_DEV void for_row4(const float *z, int V, F f) {
     }
 }
 
-__global__ void __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
+__global__ void __cluster_dims__(CLC, 1, 1) __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
     __shared__ CSmem s;
     __shared__ int bad;
     pdl_wait();
     pdl_trigger();
-    const int r = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const bool writer = rank == 0;          // the CTA that writes the request's outputs
+    const int r = blockIdx.x / CLC;
     const int end = p.cu[r], start = r > 0 ? p.cu[r - 1] : 0, d = end - start;
     int32_t *out = p.out + (size_t)r * (p.K + 1);
     const uint64_t step = p.step_counter ? *p.step_counter : p.step;
@@ -187,14 +216,20 @@ __global__ void __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
             if (t < 0 || t >= p.V) atomicOr(&bad, EAGLE3_DEV_BAD_TOKEN);
         }
     __syncthreads();
-    if (bad) {
-        for (int i = threadIdx.x; i <= p.K; i += NT) out[i] = -1;
-        if (threadIdx.x == 0) {
-            if (p.n_acc) p.n_acc[r] = -1;
-            flag(p.dev_status, bad);
+    if (bad) {   // every CTA of the cluster sees the same counts and tokens: all leave here
+        if (writer) {
+            for (int i = threadIdx.x; i <= p.K; i += NT) out[i] = -1;
+            if (threadIdx.x == 0) {
+                if (p.n_acc) p.n_acc[r] = -1;
+                flag(p.dev_status, bad);
+            }
         }
         return;
     }
+    // this CTA's slice of every row: float4 groups [j_lo, j_hi)
+    const int n4 = (p.V + 3) / 4, per = (n4 + CLC - 1) / CLC;
+    const int j_lo = min(n4, rank * per), j_hi = min(n4, j_lo + per);
+    uint32_t par = 0;
     const int row0 = start + r;            // (cu_num_draft_tokens[r] - d) + r
     const bool greedy = p.greedy && p.greedy[r];
     const uint32_t k0 = (uint32_t)p.seed, k1 = (uint32_t)(p.seed >> 32);
@@ -204,7 +239,7 @@ __global__ void __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
         const int dt = i < d ? p.drafts[start + i] : -1;
         if (greedy) {
             uint64_t best = 0;
-            for_row4(z, p.V, [&](int, int x0, const float(&v)[4]) {
+            for_row4(z, p.V, j_lo, j_hi, [&](int, int x0, const float(&v)[4]) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (x0 + e < p.V) {
@@ -212,42 +247,43 @@ __global__ void __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
                         best = k > best ? k : best;
                     }
             });
-            const int pred = (int)unpack_idx(block_max_u64(s, best));
+            const int pred = (int)unpack_idx(cluster_reduce_u64<true>(s, cluster, par, block_max_u64(s, best)));
             if (i < d && dt == pred) {
-                if (threadIdx.x == 0) out[i] = dt;
+                if (writer && threadIdx.x == 0) out[i] = dt;
                 continue;
             }
-            if (threadIdx.x == 0) out[i] = pred;
+            if (writer && threadIdx.x == 0) out[i] = pred;
             n = i;
             break;
         }
         // row maximum (total order of fp32 bit patterns)
         uint32_t mk = 0;
-        for_row4(z, p.V, [&](int, int x0, const float(&v)[4]) {
+        for_row4(z, p.V, j_lo, j_hi, [&](int, int x0, const float(&v)[4]) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (x0 + e < p.V) mk = max(mk, order_key(v[e]));
         });
-        const float m = key_to_float((uint32_t)block_max_u64(s, mk));
+        const float m = key_to_float((uint32_t)cluster_reduce_u64<true>(s, cluster, par, block_max_u64(s, mk)));
         if (i < d) {
             uint64_t sum = 0;
-            for_row4(z, p.V, [&](int, int x0, const float(&v)[4]) {
+            for_row4(z, p.V, j_lo, j_hi, [&](int, int x0, const float(&v)[4]) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (x0 + e < p.V) sum += dsm_weight(dsm_scaled(v[e], m, p.inv_t));
             });
-            const uint64_t S = block_sum_u64(s, sum);
+            // integer sums: exact whatever the order of the slices
+            const uint64_t S = cluster_reduce_u64<false>(s, cluster, par, block_sum_u64(s, sum));
             const uint64_t Wd = dsm_weight(dsm_scaled(__ldg(z + dt), m, p.inv_t));
             const uint32_t u32 = philox4x32_10(ACCEPT_C0, 256u * (uint32_t)r + (uint32_t)i, (uint32_t)step,
                                                (uint32_t)(step >> 32), k0, k1).x0;
             if ((unsigned __int128)u32 * S < ((unsigned __int128)Wd << 32)) {
-                if (threadIdx.x == 0) out[i] = dt;
+                if (writer && threadIdx.x == 0) out[i] = dt;
                 continue;
             }
         }
         // rejected (or every draft kept): the Gumbel-max draw over the row, the draft's entry removed
         uint64_t best = 0;
-        for_row4(z, p.V, [&](int j, int x0, const float(&v)[4]) {
+        for_row4(z, p.V, j_lo, j_hi, [&](int j, int x0, const float(&v)[4]) {
             const U4 w = philox4x32_10((uint32_t)j, 256u * (uint32_t)r + (uint32_t)i, (uint32_t)step,
                                        (uint32_t)(step >> 32), k0, k1);
             const uint32_t words[4] = {w.x0, w.x1, w.x2, w.x3};
@@ -261,13 +297,16 @@ __global__ void __launch_bounds__(NT) chain_verify_kernel(const CParams p) {
                 best = k > best ? k : best;
             }
         });
-        const int tok = (int)unpack_idx(block_max_u64(s, best));
-        if (threadIdx.x == 0) out[i] = tok;
+        const int tok = (int)unpack_idx(cluster_reduce_u64<true>(s, cluster, par, block_max_u64(s, best)));
+        if (writer && threadIdx.x == 0) out[i] = tok;
         n = i;
         break;
     }
-    for (int i = n + 1 + threadIdx.x; i <= p.K; i += NT) out[i] = -1;
-    if (threadIdx.x == 0 && p.n_acc) p.n_acc[r] = n;
+    if (writer) {
+        for (int i = n + 1 + threadIdx.x; i <= p.K; i += NT) out[i] = -1;
+        if (threadIdx.x == 0 && p.n_acc) p.n_acc[r] = n;
+    }
+    cluster.sync();   // last use of remote shared memory: every CTA passes before any leaves
 }
 
 __global__ void chain_step_increment_kernel(uint64_t *counter) { *counter += 1; }
@@ -289,7 +328,8 @@ extern "C" eagle3_status_t eagle3_spec_decode_metadata(const eagle3_spec_decode_
 }
 
 extern "C" eagle3_status_t eagle3_chain_verify(const eagle3_chain_verify_args_t *a, eagle3_stream_t stream) {
-    if (!a || a->n_requests < 0 || a->vocab < 1 || a->vocab > (1 << 22) || a->max_drafts < 0 || a->max_drafts > 255)
+    if (!a || a->n_requests < 0 || a->n_requests > (1 << 24) || a->vocab < 1 || a->vocab > (1 << 22) ||
+        a->max_drafts < 0 || a->max_drafts > 255)
         return EAGLE3_ERR_INVALID_ARGUMENT;
     if (a->n_requests == 0) return EAGLE3_OK;
     if (!a->logits || !a->cu_num_draft_tokens || !a->output_tokens || (a->max_drafts > 0 && !a->draft_tokens))
@@ -310,7 +350,7 @@ extern "C" eagle3_status_t eagle3_chain_verify(const eagle3_chain_verify_args_t 
     p.n_acc = a->num_accepted;
     p.dev_status = a->dev_status;
     p.step_counter = a->step_counter;
-    if (launch_pdl(chain_verify_kernel, dim3(a->n_requests), dim3(NT), 0, (cudaStream_t)stream, p) != cudaSuccess)
+    if (launch_pdl(chain_verify_kernel, dim3(a->n_requests * CLC), dim3(NT), 0, (cudaStream_t)stream, p) != cudaSuccess)
         return EAGLE3_ERR_CUDA;
     if (a->step_counter) {
         chain_step_increment_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(a->step_counter);

@@ -84,7 +84,7 @@ eagle3_status_t eagle3_spec_decode_metadata(const eagle3_spec_decode_metadata_ar
  * flagged (EAGLE3_DEV_BAD_COUNTS / EAGLE3_DEV_BAD_TOKEN).  d_r <= 255.
  * ---------------------------------------------------------------------------------------------- */
 typedef struct {
-    int32_t n_requests;                   /* R >= 0                                                  */
+    int32_t n_requests;                   /* R in [0, 2^24]: one 8-CTA cluster per request           */
     int32_t vocab;                        /* V in [1, 2^22]                                          */
     int32_t max_drafts;                   /* K: output rows hold K + 1 tokens; 0 <= K <= 255          */
     float temperature;                    /* T > 0 for random requests                              */
