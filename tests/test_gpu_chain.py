@@ -105,7 +105,8 @@ def _chain_ref(logits, d, drafts, greedy, K, T, seed, step, r):
     return out + [-1] * (K + 1 - len(out)), n
 
 
-@pytest.mark.parametrize("R,K,V,T", [(64, 5, 128256, 1.0), (9, 3, 1001, 0.7)])
+@pytest.mark.parametrize("R,K,V,T", [(64, 5, 128256, 1.0), (9, 3, 1001, 0.7),
+                                     (6, 2, 5, 1.0)])   # V = 5: most CTAs of a cluster get an empty slice
 def test_chain_verify_matches_oracle(R, K, V, T):
     d, logits, drafts, greedy = synth.chain_batch(R + V, R, K, V)
     seed = 2
